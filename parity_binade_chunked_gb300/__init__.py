@@ -1,0 +1,163 @@
+"""Exact sequential fp64 sums on one GB300 (sm_103a).
+
+A thin ctypes binding over the C-ABI library ``libseqsum.so`` (declared in
+``include/seqsum.h``).  The binding only marshals arguments: every step of the
+sum runs in the library's CUDA kernels.  There is no CPU fallback -- if the
+library cannot be loaded, every call raises.
+
+PyTorch is used for device memory and streams only: the tensors passed in
+must be CUDA tensors, and the work is enqueued on the current torch stream
+unless a stream is given.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+__all__ = ["seqsum_f64", "seqsum_f64_batched", "seqsum_f64_batched_sized", "get_stats",
+           "debug_set_plan", "release_workspace", "version", "lib", "SeqsumError"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SeqsumError(RuntimeError):
+    pass
+
+
+class _Stats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "tiles", "chunks_run", "chunks_list", "chunks_fallback", "lanes_dirty", "walk_segments",
+        "runs_rejected", "terms_added", "items", "pool_overflow", "tiles_complex",
+        "lookback_steps")] + [("device_status", ctypes.c_int32), ("device_error_bits", ctypes.c_int32)]
+
+
+def lib():
+    """Load libseqsum.so (building it first if needed).  Raises if it cannot."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                path = _build.build()
+            L = ctypes.CDLL(path)
+            vp, i64, i32, d = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_double
+            L.seqsum_f64.argtypes = [vp, i64, d, vp, vp]
+            L.seqsum_f64.restype = ctypes.c_int
+            L.seqsum_f64_batched.argtypes = [vp, vp, i32, vp, vp, vp]
+            L.seqsum_f64_batched.restype = ctypes.c_int
+            L.seqsum_f64_batched_sized.argtypes = [vp, i64, vp, i32, vp, vp, vp]
+            L.seqsum_f64_batched_sized.restype = ctypes.c_int
+            L.seqsum_get_stats.argtypes = [ctypes.POINTER(_Stats)]
+            L.seqsum_get_stats.restype = ctypes.c_int
+            L.seqsum_strerror.argtypes = [ctypes.c_int]
+            L.seqsum_strerror.restype = ctypes.c_char_p
+            L.seqsum_last_cuda_error.argtypes = []
+            L.seqsum_last_cuda_error.restype = ctypes.c_int
+            L.seqsum_release_workspace.argtypes = []
+            L.seqsum_release_workspace.restype = None
+            L.seqsum_debug_set_plan.argtypes = [ctypes.c_int]
+            L.seqsum_debug_set_plan.restype = ctypes.c_int
+            L.seqsum_version.argtypes = []
+            L.seqsum_version.restype = ctypes.c_char_p
+            _lib = L
+        return _lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        L = lib()
+        raise SeqsumError(f"seqsum: {L.seqsum_strerror(rc).decode()} (code {rc}, "
+                          f"cuda error {L.seqsum_last_cuda_error()})")
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev_f64(t, name):
+    import torch
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.float64 and t.is_contiguous()):
+        raise TypeError(f"{name} must be a contiguous CUDA float64 tensor")
+    return t
+
+
+def seqsum_f64(x, s0: float = 0.0, out=None, stream=None):
+    """out[0] = s0 + x[0] + ... + x[n-1], added in index order, exactly as the
+    CPU loop rounds each add.  Returns `out` (a 1-element CUDA float64 tensor);
+    the value is ready once `stream` reaches it."""
+    import torch
+    x = _dev_f64(x, "x").reshape(-1)
+    if out is None:
+        out = torch.empty(1, dtype=torch.float64, device=x.device)
+    _dev_f64(out, "out")
+    with torch.cuda.device(x.device):
+        _check(lib().seqsum_f64(ctypes.c_void_p(x.data_ptr()), x.numel(), float(s0),
+                                ctypes.c_void_p(out.data_ptr()), _stream_handle(stream)))
+    return out
+
+
+def seqsum_f64_batched(x, offsets, s0s, outs=None, stream=None):
+    """outs[k] = s0s[k] + x[offsets[k]] + ... + x[offsets[k+1]-1] for every k.
+    Reads offsets[0] and offsets[-1] back once to size the workspace."""
+    import torch
+    x = _dev_f64(x, "x").reshape(-1)
+    if not (offsets.is_cuda and offsets.dtype == torch.int64 and offsets.is_contiguous()):
+        raise TypeError("offsets must be a contiguous CUDA int64 tensor")
+    nsums = offsets.numel() - 1
+    _dev_f64(s0s, "s0s")
+    if outs is None:
+        outs = torch.empty(max(nsums, 0), dtype=torch.float64, device=x.device)
+    _dev_f64(outs, "outs")
+    with torch.cuda.device(x.device):
+        _check(lib().seqsum_f64_batched(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(offsets.data_ptr()),
+                                        nsums, ctypes.c_void_p(s0s.data_ptr()),
+                                        ctypes.c_void_p(outs.data_ptr()), _stream_handle(stream)))
+    return outs
+
+
+def seqsum_f64_batched_sized(x, offsets, s0s, outs=None, stream=None, x_len=None):
+    """As seqsum_f64_batched, without any host wait: x_len (default x.numel())
+    bounds every offset."""
+    import torch
+    x = _dev_f64(x, "x").reshape(-1)
+    if not (offsets.is_cuda and offsets.dtype == torch.int64 and offsets.is_contiguous()):
+        raise TypeError("offsets must be a contiguous CUDA int64 tensor")
+    nsums = offsets.numel() - 1
+    _dev_f64(s0s, "s0s")
+    if outs is None:
+        outs = torch.empty(max(nsums, 0), dtype=torch.float64, device=x.device)
+    _dev_f64(outs, "outs")
+    n = x.numel() if x_len is None else int(x_len)
+    with torch.cuda.device(x.device):
+        _check(lib().seqsum_f64_batched_sized(ctypes.c_void_p(x.data_ptr()), n,
+                                              ctypes.c_void_p(offsets.data_ptr()), nsums,
+                                              ctypes.c_void_p(s0s.data_ptr()),
+                                              ctypes.c_void_p(outs.data_ptr()), _stream_handle(stream)))
+    return outs
+
+
+def get_stats() -> dict:
+    """Device counters of the calls since the last get_stats() (waits)."""
+    st = _Stats()
+    _check(lib().seqsum_get_stats(ctypes.byref(st)))
+    return {name: getattr(st, name) for name, _ in _Stats._fields_}
+
+
+def debug_set_plan(mode: int) -> int:
+    """Force the plan of later calls (tests only); returns the old mode."""
+    return lib().seqsum_debug_set_plan(int(mode))
+
+
+def release_workspace():
+    lib().seqsum_release_workspace()
+
+
+def version() -> str:
+    return lib().seqsum_version().decode()

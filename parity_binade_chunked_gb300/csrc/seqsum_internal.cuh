@@ -1,0 +1,95 @@
+// Internal layout shared by the kernel and API translation units.
+#pragma once
+#include <cuda.h>
+#include <stdint.h>
+
+namespace sq {
+
+// ---- geometry (a lane owns one 128-byte row of 16 consecutive terms)
+constexpr int kLaneTerms = 16;
+constexpr int kWarps = 8;                       // warps per CTA = chunks per tile
+constexpr int kThreads = kWarps * 32;
+constexpr int kChunkTerms = 32 * kLaneTerms;    // 512 terms: one warp's chunk
+constexpr int kTileTerms = kWarps * kChunkTerms;// 4096 terms = 32 KB: one TMA box
+constexpr int kStages = 2;
+constexpr int kStageBytes = kTileTerms * 8;
+constexpr int kDynSmem = kStages * kStageBytes + 1024;   // + alignment slack
+constexpr int kWalkBatch = kStageBytes / 32;    // tile records per walk batch (1024, one stage)
+
+// ---- record kinds
+enum : uint32_t { K_RUN = 0, K_FALLBACK = 1, K_LIST = 2, K_COMPLEX = 3 };
+
+// A chunk, tile or item record: 32 bytes.
+//   K_RUN      : a run computed for binade e (F_ZERO runs apply in any binade)
+//   K_FALLBACK : the covered terms are added one by one by the walk
+//   K_LIST     : (chunk) items pool[inc .. inc + lo), in order
+//   K_COMPLEX  : (tile) the walk descends into the tile's chunk records
+struct __align__(16) Rec {
+  int64_t inc, lo, hi;
+  uint32_t meta;      // bits 0-7: d (int8), 8-15: flags, 16-19: kind
+  int16_t e;          // binade
+  uint16_t count;     // terms covered (items)
+};
+
+__host__ __device__ inline uint32_t rec_meta(int32_t d, uint32_t flags, uint32_t kind) {
+  return ((uint32_t)(uint8_t)(int8_t)d) | ((flags & 0xFFu) << 8) | (kind << 16);
+}
+__host__ __device__ inline int32_t rec_d(uint32_t meta) { return (int32_t)(int8_t)(meta & 0xFFu); }
+__host__ __device__ inline uint32_t rec_flags(uint32_t meta) { return (meta >> 8) & 0xFFu; }
+__host__ __device__ inline uint32_t rec_kind(uint32_t meta) { return (meta >> 16) & 0xFu; }
+
+// ---- counters in the workspace
+enum : int {
+  C_TICKET = 0,      // next tile ticket
+  C_EXIT = 1,        // CTAs that finished
+  C_POOL = 2,        // items allocated
+  C_ERR = 3,         // error bits (ERR_*)
+  C_NTILES = 4,      // tiles of a batched call (written by the set-up kernel)
+  C_COUNT = 8
+};
+enum : uint32_t {
+  ERR_TMA_TIMEOUT = 1u,       // a TMA copy did not complete within the wait limit
+  ERR_PLAN_TIMEOUT = 2u,      // a look-back wait gave up (the plan only; results stay exact)
+  ERR_BAD_OFFSETS = 4u,       // offsets not non-decreasing
+  ERR_CAPACITY = 8u,          // a batched call needed more tiles than its workspace holds
+};
+
+// ---- statistics (accumulated on the device, read and cleared by the host)
+enum : int {
+  S_TILES = 0, S_CHUNK_RUN, S_CHUNK_LIST, S_CHUNK_FALLBACK, S_LANE_DIRTY,
+  S_WALK_SEGMENTS, S_RUN_REJECTED, S_TERMS_ADDED, S_ITEMS, S_POOL_OVERFLOW,
+  S_TILE_COMPLEX, S_LOOKBACK_STEPS, S_COUNT = 16
+};
+
+// ---- kernel parameters
+struct Params {
+  const double *x;
+  const int64_t *offsets;      // batched: nsums + 1 entries (device); null for a single sum
+  const double *s0s;           // batched: device; null for a single sum
+  double *outs;                // device
+  double s0;                   // single sum start value
+  int64_t n;                   // single sum length (batched: unused)
+  int64_t ntiles;              // single: known on the host; batched: -1 (read C_NTILES)
+  int64_t tma_rows;            // rows of 16 terms the tensor map covers (0: no TMA)
+  int32_t nsums;
+  uint32_t epoch;
+  int32_t plan_mode;           // 0 normal; >0 forced plans for tests
+  int32_t pad;
+  // workspace
+  uint64_t *status;            // 2 words per tile: tagged approximate prefix
+  Rec *tile_rec;
+  Rec *chunk_rec;
+  Rec *pool;
+  int64_t pool_cap;
+  uint32_t *ctr;               // C_COUNT counters
+  uint32_t *done;              // per sum: tiles finished
+  int64_t *tile_begin;         // batched: nsums + 1 entries
+  int64_t cap_tiles;           // tiles the workspace holds
+  unsigned long long *stats;   // S_COUNT counters
+};
+
+cudaError_t launch_seqsum(const Params &p, const CUtensorMap *tmap, int grid, cudaStream_t st);
+cudaError_t launch_setup(const Params &p, cudaStream_t st);
+int kernel_max_blocks_per_sm();
+
+}  // namespace sq
