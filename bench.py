@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary configs")
     ap.add_argument("--quick", action="store_true", help="few steps, no CPU baseline (profiling runs)")
+    ap.add_argument("--height-mult", type=int, default=1,
+                    help="plane this many times taller (profiling captures larger than L2)")
     return ap.parse_args()
 
 
@@ -206,7 +208,7 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
-    wl = W.config(args.config)
+    wl = W.config(args.config, height_mult=args.height_mult)
     x = wl.x
     n = len(x)
     s0 = float(wl.s0[0])
@@ -267,7 +269,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.config} 3840x2160 single sum ({n} terms)", "n_terms": n,
+        "config": {"workload": f"{args.config} {wl.shape[0][0]}x{wl.shape[0][1]} single sum ({n} terms)", "n_terms": n,
                    "recipe": wl.recipe, "l2": "flushed before every step (256 MB write)",
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "parity_0ulp": parity and e2e_ok,

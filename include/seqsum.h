@@ -103,6 +103,8 @@ typedef struct {
   int64_t pool_overflow;     /* split chunks that found no room and fell back */
   int64_t tiles_complex;     /* tiles the walk descended into */
   int64_t lookback_steps;    /* look-back windows read by the plan */
+  int64_t t_stream_ns;       /* latest call: kernel start to the start of its (last) walk */
+  int64_t t_walk_ns;         /* latest call: duration of its (last) walk */
   int32_t device_status;     /* 0, or a negative SEQSUM_E* code */
   int32_t device_error_bits; /* raw device error bits */
 } seqsum_stats;

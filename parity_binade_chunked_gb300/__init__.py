@@ -32,7 +32,7 @@ class _Stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
         "tiles", "chunks_run", "chunks_list", "chunks_fallback", "lanes_dirty", "walk_segments",
         "runs_rejected", "terms_added", "items", "pool_overflow", "tiles_complex",
-        "lookback_steps")] + [("device_status", ctypes.c_int32), ("device_error_bits", ctypes.c_int32)]
+        "lookback_steps", "t_stream_ns", "t_walk_ns")] + [("device_status", ctypes.c_int32), ("device_error_bits", ctypes.c_int32)]
 
 
 def lib():

@@ -154,6 +154,35 @@ SQ_HD void run_push(Run &a, int64_t re, int32_t t, uint32_t tf) {
             ((a.flags | tf) & (F_POISON | F_HASINF_P | F_HASINF_N | F_HASNAN));
 }
 
+// The same increment for a term whose sign is handled by the caller, in the
+// common case: binade e with e >= -969 and |x| < 2^e (s >= 1).  hi/lo are the
+// term's two 32-bit halves; c = 64 - (e + 1023).  r = x / 2^(e-52) rounded
+// half-up is returned in r (the even-start increment when `tie` is false);
+// `tie` says the shifted-out bits were exactly one half.
+//
+// M * 2^(64-s) is formed with two 32x32->64 multiplies by 2^((64-s) mod 32):
+// its upper 64 bits are M >> s and its lower 64 bits the shifted-out bits,
+// left aligned.  Subnormal terms and zeros are treated as if they had the
+// hidden bit; for e >= -969 that makes s >= 54 for them, where the result is
+// r = 0 without a tie either way.
+SQ_HD void term_inc_fast(uint32_t hi, uint32_t lo, int c, uint64_t &r, bool &tie) {
+  const uint32_t E = (hi >> 20) & 0x7FFu;
+  const uint32_t mh = (hi & 0xFFFFFu) | 0x100000u;
+  int j = (int)E + c;                          // j = 64 - s, in [0, 63] (s > 64 clamps to 0)
+  j = j < 0 ? 0 : j;
+  const uint32_t w = 1u << (j & 31);
+  const bool J = j >= 32;
+  const uint64_t A = (uint64_t)lo * w, B = (uint64_t)mh * w;
+  const uint32_t A0 = (uint32_t)A, A1 = (uint32_t)(A >> 32), B0 = (uint32_t)B, B1 = (uint32_t)(B >> 32);
+  const uint32_t P = B0 | A1;
+  const uint32_t Rh = J ? A0 : P;              // shifted-out bits, top word
+  const bool Rl = !J && (A0 != 0);             // any shifted-out bit in the lower word
+  tie = (Rh == 0x80000000u) && !Rl;
+  const bool up = (Rh > 0x80000000u) || ((Rh == 0x80000000u) && Rl);
+  const uint64_t f = J ? (((uint64_t)B1 << 32) | P) : (uint64_t)B1;
+  r = f + (up ? 1u : 0u);
+}
+
 SQ_HD int64_t sq_min(int64_t a, int64_t b) { return a < b ? a : b; }
 SQ_HD int64_t sq_max(int64_t a, int64_t b) { return a > b ? a : b; }
 

@@ -22,10 +22,11 @@ using sq::Rec;
 struct Workspace {
   int device = 0;
   cudaStream_t stream = nullptr;
-  int64_t cap_tiles = 0, cap_sums = 0, pool_cap = 0;
-  uint64_t *status = nullptr;
-  Rec *tile_rec = nullptr, *chunk_rec = nullptr, *pool = nullptr;
-  uint32_t *ctr = nullptr, *done = nullptr;
+  int64_t cap_tiles = 0, cap_sums = 0;
+  uint64_t *status = nullptr;        // look-back words, 2 per tile
+  Rec *hdr = nullptr;                // one header per tile
+  Rec *items = nullptr;              // kTileSlots items per tile
+  uint32_t *ctr = nullptr;
   int64_t *tile_begin = nullptr;
   unsigned long long *stats = nullptr;
   uint32_t epoch = 0;
@@ -52,14 +53,12 @@ int cuda_fail(cudaError_t e) {
 
 void ws_free(Workspace *w) {
   cudaFree(w->status);
-  cudaFree(w->tile_rec);
-  cudaFree(w->chunk_rec);
-  cudaFree(w->pool);
+  cudaFree(w->hdr);
+  cudaFree(w->items);
   cudaFree(w->tile_begin);
-  cudaFree(w->done);
-  w->status = nullptr; w->tile_rec = w->chunk_rec = w->pool = nullptr;
-  w->tile_begin = nullptr; w->done = nullptr;
-  w->cap_tiles = w->cap_sums = w->pool_cap = 0;
+  w->status = nullptr; w->hdr = w->items = nullptr;
+  w->tile_begin = nullptr;
+  w->cap_tiles = w->cap_sums = 0;
 }
 
 // Workspace for (current device, stream) holding at least `tiles` tiles and
@@ -86,23 +85,18 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
     const int64_t ct = tiles > w->cap_tiles ? tiles + tiles / 4 + 16 : w->cap_tiles;
     const int64_t cs = sums > w->cap_sums ? sums + 16 : w->cap_sums;
     ws_free(w);
-    const int64_t chunks = ct * sq::kWarps;
-    const int64_t pool = chunks * 4 + 4096;
     if (cudaMalloc(&w->status, ct * 2 * sizeof(uint64_t)) != cudaSuccess ||
-        cudaMalloc(&w->tile_rec, ct * sizeof(Rec)) != cudaSuccess ||
-        cudaMalloc(&w->chunk_rec, chunks * sizeof(Rec)) != cudaSuccess ||
-        cudaMalloc(&w->pool, pool * sizeof(Rec)) != cudaSuccess ||
-        cudaMalloc(&w->tile_begin, (cs + 1) * sizeof(int64_t)) != cudaSuccess ||
-        cudaMalloc(&w->done, cs * sizeof(uint32_t)) != cudaSuccess) {
+        cudaMalloc(&w->hdr, ct * sizeof(Rec)) != cudaSuccess ||
+        cudaMalloc(&w->items, ct * sq::kTileSlots * sizeof(Rec)) != cudaSuccess ||
+        cudaMalloc(&w->tile_begin, (cs + 1) * sizeof(int64_t)) != cudaSuccess) {
       ws_free(w);
       g_last_cuda = (int)cudaGetLastError();
       return SEQSUM_ENOMEM;
     }
     cudaMemset(w->status, 0, ct * 2 * sizeof(uint64_t));
-    cudaMemset(w->done, 0, cs * sizeof(uint32_t));
+    cudaMemset(w->hdr, 0, ct * sizeof(Rec));
     w->cap_tiles = ct;
     w->cap_sums = cs;
-    w->pool_cap = pool;
     w->epoch = 0;
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e);
   }
@@ -135,6 +129,7 @@ void next_epoch(Workspace *w, cudaStream_t stream) {
   w->epoch++;
   if (w->epoch > 127) {
     cudaMemsetAsync(w->status, 0, w->cap_tiles * 2 * sizeof(uint64_t), stream);
+    cudaMemsetAsync(w->hdr, 0, w->cap_tiles * sizeof(Rec), stream);
     w->epoch = 1;
   }
 }
@@ -160,12 +155,9 @@ int64_t tensor_map(Workspace *w, const double *x, int64_t n_total) {
 
 void fill_ws(Params &p, Workspace *w) {
   p.status = w->status;
-  p.tile_rec = w->tile_rec;
-  p.chunk_rec = w->chunk_rec;
-  p.pool = w->pool;
-  p.pool_cap = w->pool_cap;
+  p.hdr = w->hdr;
+  p.items = w->items;
   p.ctr = w->ctr;
-  p.done = w->done;
   p.tile_begin = w->tile_begin;
   p.cap_tiles = w->cap_tiles;
   p.stats = w->stats;
@@ -211,9 +203,11 @@ int batched_impl(const double *x, int64_t x_len, const int64_t *offsets, int32_t
   p.plan_mode = g_plan_mode;
   fill_ws(p, w);
   p.tma_rows = tensor_map(w, x, x_len);
+  p.nwalkers = nsums < sq::kMaxWalkers ? nsums : sq::kMaxWalkers;
   cudaError_t e = sq::launch_setup(p, stream);
   if (e != cudaSuccess) return cuda_fail(e);
-  const int grid = g_num_sms[w->device] * g_blocks_per_sm;
+  int grid = g_num_sms[w->device] * g_blocks_per_sm;
+  if (grid < p.nwalkers + 1) grid = p.nwalkers + 1;
   static CUtensorMap dummy;
   e = sq::launch_seqsum(p, p.tma_rows ? &w->tmap : &dummy, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -247,9 +241,10 @@ int seqsum_f64(const double *x, int64_t n, double s0, double *out, cudaStream_t 
   p.plan_mode = g_plan_mode;
   fill_ws(p, w);
   p.tma_rows = n > 0 ? tensor_map(w, x, n) : 0;
+  p.nwalkers = 1;
   const int dev = w->device;
   int64_t grid = (int64_t)g_num_sms[dev] * g_blocks_per_sm;
-  if (tiles < grid) grid = tiles > 0 ? tiles : 1;
+  if (tiles + 1 < grid) grid = tiles + 1;             // one walker + streaming CTAs
   static CUtensorMap dummy;
   cudaError_t e = sq::launch_seqsum(p, p.tma_rows ? &w->tmap : &dummy, (int)grid, stream);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -298,6 +293,8 @@ int seqsum_get_stats(seqsum_stats *st) {
   st->pool_overflow = (int64_t)s[sq::S_POOL_OVERFLOW];
   st->tiles_complex = (int64_t)s[sq::S_TILE_COMPLEX];
   st->lookback_steps = (int64_t)s[sq::S_LOOKBACK_STEPS];
+  st->t_stream_ns = (int64_t)(s[sq::S_T_WALK0] - s[sq::S_T_START]);
+  st->t_walk_ns = (int64_t)(s[sq::S_T_WALK1] - s[sq::S_T_WALK0]);
   st->device_error_bits = (int32_t)err;
   if (err & sq::ERR_CAPACITY) st->device_status = SEQSUM_ECAPACITY;
   else if (err & sq::ERR_BAD_OFFSETS) st->device_status = SEQSUM_EOFFSETS;

@@ -11,38 +11,47 @@ constexpr int kWarps = 8;                       // warps per CTA = chunks per ti
 constexpr int kThreads = kWarps * 32;
 constexpr int kChunkTerms = 32 * kLaneTerms;    // 512 terms: one warp's chunk
 constexpr int kTileTerms = kWarps * kChunkTerms;// 4096 terms = 32 KB: one TMA box
-constexpr int kStages = 2;
+constexpr int kStages = 3;                      // copy of tile i+2 | plan of i+1 | runs of i
 constexpr int kStageBytes = kTileTerms * 8;
 constexpr int kDynSmem = kStages * kStageBytes + 1024;   // + alignment slack
-constexpr int kWalkBatch = kStageBytes / 32;    // tile records per walk batch (1024, one stage)
+constexpr int kChunkSlots = 16;                 // item slots per chunk in a tile's item area
+constexpr int kTileSlots = kWarps * kChunkSlots;
+constexpr int kWalkTiles = 1024;                // tile headers per walk batch (32 KB)
+constexpr int kWalkElems = 1536;                // flat elements per walk batch (48 KB)
+constexpr int kMaxWalkers = 8;
 
 // ---- record kinds
-enum : uint32_t { K_RUN = 0, K_FALLBACK = 1, K_LIST = 2, K_COMPLEX = 3 };
+enum : uint32_t { K_RUN = 0, K_FALLBACK = 1, K_TERMS = 2, K_COMPLEX = 3 };
 
-// A chunk, tile or item record: 32 bytes.
+// A tile header or an item: 32 bytes.
 //   K_RUN      : a run computed for binade e (F_ZERO runs apply in any binade)
-//   K_FALLBACK : the covered terms are added one by one by the walk
-//   K_LIST     : (chunk) items pool[inc .. inc + lo), in order
-//   K_COMPLEX  : (tile) the walk descends into the tile's chunk records
+//   K_FALLBACK : the covered terms are added one by one from the plane
+//   K_TERMS    : up to three terms carried inline (inc, lo, hi hold their
+//                bits), added one by one
+//   K_COMPLEX  : (tile header) the items live in the tile's item area; inc
+//                holds eight 8-bit item counts, one per chunk
+// Tile headers carry the call's tag in the top byte of lo and of hi, so a
+// reader can check both 16-byte halves.
 struct __align__(16) Rec {
   int64_t inc, lo, hi;
-  uint32_t meta;      // bits 0-7: d (int8), 8-15: flags, 16-19: kind
+  uint32_t meta;      // bits 0-7: d (int8), 8-15: flags, 16-19: kind, 20-31: first term in the tile
   int16_t e;          // binade
-  uint16_t count;     // terms covered (items)
+  uint16_t count;     // terms covered
 };
 
-__host__ __device__ inline uint32_t rec_meta(int32_t d, uint32_t flags, uint32_t kind) {
-  return ((uint32_t)(uint8_t)(int8_t)d) | ((flags & 0xFFu) << 8) | (kind << 16);
+__host__ __device__ inline uint32_t rec_meta(int32_t d, uint32_t flags, uint32_t kind, uint32_t tstart = 0) {
+  return ((uint32_t)(uint8_t)(int8_t)d) | ((flags & 0xFFu) << 8) | ((kind & 0xFu) << 16) | ((tstart & 0xFFFu) << 20);
 }
 __host__ __device__ inline int32_t rec_d(uint32_t meta) { return (int32_t)(int8_t)(meta & 0xFFu); }
 __host__ __device__ inline uint32_t rec_flags(uint32_t meta) { return (meta >> 8) & 0xFFu; }
 __host__ __device__ inline uint32_t rec_kind(uint32_t meta) { return (meta >> 16) & 0xFu; }
+__host__ __device__ inline uint32_t rec_tstart(uint32_t meta) { return meta >> 20; }
 
 // ---- counters in the workspace
 enum : int {
   C_TICKET = 0,      // next tile ticket
   C_EXIT = 1,        // CTAs that finished
-  C_POOL = 2,        // items allocated
+  C_SUMTICKET = 2,   // next sum for a walker
   C_ERR = 3,         // error bits (ERR_*)
   C_NTILES = 4,      // tiles of a batched call (written by the set-up kernel)
   C_COUNT = 8
@@ -50,15 +59,22 @@ enum : int {
 enum : uint32_t {
   ERR_TMA_TIMEOUT = 1u,       // a TMA copy did not complete within the wait limit
   ERR_PLAN_TIMEOUT = 2u,      // a look-back wait gave up (the plan only; results stay exact)
-  ERR_BAD_OFFSETS = 4u,       // offsets not non-decreasing
+  ERR_BAD_OFFSETS = 4u,       // offsets out of order or out of range
   ERR_CAPACITY = 8u,          // a batched call needed more tiles than its workspace holds
+  ERR_WALK_TIMEOUT = 16u,     // the walk waited too long for a tile record
 };
 
 // ---- statistics (accumulated on the device, read and cleared by the host)
 enum : int {
   S_TILES = 0, S_CHUNK_RUN, S_CHUNK_LIST, S_CHUNK_FALLBACK, S_LANE_DIRTY,
   S_WALK_SEGMENTS, S_RUN_REJECTED, S_TERMS_ADDED, S_ITEMS, S_POOL_OVERFLOW,
-  S_TILE_COMPLEX, S_LOOKBACK_STEPS, S_COUNT = 16
+  S_TILE_COMPLEX, S_LOOKBACK_STEPS,
+  S_WALK_BATCHES = 12,
+  // timestamps (globaltimer ns) of the latest call, plain stores:
+  S_T_START = 13,      // block 0 started
+  S_T_WALK0 = 14,      // the last tile header the walk needed became ready
+  S_T_WALK1 = 15,      // the walk ended
+  S_COUNT = 16
 };
 
 // ---- kernel parameters
@@ -77,13 +93,12 @@ struct Params {
   int32_t pad;
   // workspace
   uint64_t *status;            // 2 words per tile: tagged approximate prefix
-  Rec *tile_rec;
-  Rec *chunk_rec;
-  Rec *pool;
-  int64_t pool_cap;
+  Rec *hdr;                    // one header per tile
+  Rec *items;                  // kTileSlots items per tile
   uint32_t *ctr;               // C_COUNT counters
-  uint32_t *done;              // per sum: tiles finished
   int64_t *tile_begin;         // batched: nsums + 1 entries
+  int32_t nwalkers;            // CTAs 0 .. nwalkers-1 walk; the others stream
+  int32_t pad2;
   int64_t cap_tiles;           // tiles the workspace holds
   unsigned long long *stats;   // S_COUNT counters
 };

@@ -1,31 +1,38 @@
 // The device path of the exact sequential fp64 sum (sm_103a).
 //
-// One persistent kernel does all of it:
-//   1. streams the term plane once: a tile of 4096 terms (32 KB) per TMA box,
-//      two stages per CTA, swizzled (128B) so that each lane reads its own
-//      128-byte row of 16 consecutive terms without bank conflicts;
-//   2. forms approximate chunk sums in fp32 from the terms' bits and a
-//      parallel approximate prefix over tiles (decoupled look-back) that
-//      names each chunk's starting binade (Research-1424, section 3: "a first
-//      pass can add each row on its own and a prefix over the rows gives S at
-//      each row start ... which names the binade except next to a power of
-//      two"; Research-1433, finding 5; open question "compute the plan's
-//      prefix with a scan across the lanes");
-//   3. turns every term into its even/odd increment pair by integer shifts
-//      (binade_math.cuh) and composes them in order: a lane's 16 terms, then
-//      the warp's 32 lanes in a fixed shuffle tree, then the tile's 8 chunks
-//      (Research-1433, finding 6: "composes each lane's ... terms in order and
-//      then the lanes in an ordered tree");
-//   4. the CTA that finishes a sum's last tile walks the sum in order with the
-//      exact running value: runs of tiles that share a binade are composed in
-//      parallel first, so the serial part steps over whole segments
-//      (Research-1433, open question: "compose runs of chunks that share a
-//      binade so that the walk steps over 64 or 1024 chunks at a time"); a run
-//      the exact check rejects is descended into, and a chunk or lane the
-//      plan could not place is added term by term in fp64 (finding 4).
+// One persistent kernel.  CTAs 0 .. nwalkers-1 walk; every other CTA streams
+// tiles of 4096 terms (32 KB, one TMA box) taken in ticket order, in a
+// three-stage pipeline: the copy of tile i+2 is in flight while the plan of
+// tile i+1 and the runs of tile i are formed.
 //
-// This translation unit is built with --fmad=false; the term-by-term adds use
-// __dadd_rn, one IEEE binary64 add each, in index order.
+//  * Plan (Research-1424, section 3: "a first pass can add each row on its own
+//    and a prefix over the rows gives S at each row start ... which names the
+//    binade except next to a power of two"; Research-1433, finding 5 and the
+//    open question "compute the plan's prefix with a scan across the lanes"):
+//    every term's fp32 image is built from its bits with integer operations,
+//    a tile's approximate sum is published as soon as the tile has landed,
+//    and a decoupled look-back over the published sums, 256 tiles per read,
+//    gives each tile its approximate starting value in double-float.  No
+//    fp64 instruction is used for the plan.
+//  * Runs (finding 2 "Inside a binade the loop is an integer sum", finding 3
+//    "Ties need the parity of the running integer"): a chunk of 512 terms
+//    whose whole range lies inside one binade is turned into its increment
+//    by integer shifts (binade_math.cuh) and composed: each lane's 16 terms
+//    in order, then the warp's 32 lanes in a fixed shuffle tree (finding 6).
+//  * A chunk the plan cannot place in one binade is split: lanes that fit a
+//    binade become runs, and inside the other lanes each term is placed on
+//    its own; only the terms whose approximate prefix lies next to a power of
+//    two are carried, as values, to be added one by one (finding 4).
+//  * The walk (finding 4; open question "compose runs of chunks that share a
+//    binade so that the walk steps over 64 or 1024 chunks at a time") runs
+//    at the same time as the stream: it reads tile headers as they appear,
+//    composes every maximal run of same-binade records in parallel, and on
+//    one warp applies the composites to the exact running value, adds the
+//    carried terms with __dadd_rn, and falls back to term-by-term adds where
+//    the exact check rejects a run.
+//
+// This translation unit is built with --fmad=false; every fp64 add of the
+// walk is one __dadd_rn, in index order.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -36,15 +43,20 @@
 namespace sq {
 
 // ---------------------------------------------------------------- constants
-// Relative error allowance of the approximate prefix against the running sum
-// of |x| (fp32 terms truncated to 24 bits, fp32 sums of 16 and of 32 values,
-// fp64 across chunks and tiles: about 2^-19.5 at worst).  The plan only
-// chooses where to look; a wrong guess costs a fallback, never a wrong bit.
-constexpr double kEps = 0x1p-18;
-constexpr double kTiny = 0x1p-1000;
+// Relative error allowance of the plan against the running sum of |x|: fp32
+// term images keep 20 fraction bits (truncated), fp32 sums of 16 and 32
+// values, double-float across chunks and tiles.  The plan only chooses where
+// to look; a wrong guess costs a fallback, never a wrong bit.
+constexpr float kEps = 0x1p-18f;
+constexpr float kRelF32 = 0x1p-21f;            // rounding of one fp32 prefix value
+constexpr float kTinyF = 0x1p-120f;
 constexpr int kZeroE = -2000;                  // binade key of a run of zeros
-constexpr int kComplexKey = -100000;           // a tile that is a segment of its own
 constexpr uint64_t kWaitNs = 2000000000ull;    // bounded device waits: 2 s
+constexpr uint32_t kMagLo = 896u << 20;        // exponent 896 = 2^-127
+constexpr int kWalkOffEl = 32768;              // walker layout in the dynamic shared memory
+constexpr int kWalkOffPos = 65536;
+constexpr int kWalkOffHead = 69632;
+constexpr int kWalkOffEnds = 70656;
 
 // ---------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -86,45 +98,65 @@ __device__ __forceinline__ void tma_load_box(void *dst, const CUtensorMap *map, 
       "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
 }
-__device__ __forceinline__ uint64_t ld_vol_u64(const uint64_t *p) {
-  uint64_t v;
-  asm volatile("ld.volatile.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
+__device__ __forceinline__ void ld_vol_v2(const void *p, uint64_t &a, uint64_t &b) {
+  asm volatile("ld.volatile.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
-__device__ __forceinline__ void st_vol_u64(uint64_t *p, uint64_t v) {
-  asm volatile("st.volatile.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t lanemask_lt() {
-  uint32_t m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
+__device__ __forceinline__ void st_vol_v2(void *p, uint64_t a, uint64_t b) {
+  asm volatile("st.volatile.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
 }
 
-// ---------------------------------------------------------------- helpers
 __device__ __forceinline__ uint64_t dbits(double v) { return (uint64_t)__double_as_longlong(v); }
 __device__ __forceinline__ double bitsd(uint64_t b) { return __longlong_as_double((long long)b); }
 
-// A cheap fp32 image of a term built from its bits (integer ops only; the
-// fp64 pipe is not used): the top 23 fraction bits, exponent clamped to the
-// fp32 range.  Only the plan uses it.
-__device__ __forceinline__ float approx_f32(uint64_t b) {
-  const uint32_t hi = (uint32_t)(b >> 32), lo = (uint32_t)b;
-  int32_t v = (int32_t)(hi & 0x7FFFFFFFu) - (896 << 20);
-  v = max(v, 0);
-  v = min(v, (254 << 20) | 0xFFFFF);
-  const uint32_t fb = __funnelshift_l(lo, (uint32_t)v, 3) | (hi & 0x80000000u);
-  return __uint_as_float(fb);
+// ---------------------------------------------------------------- double-float
+// (hi + lo) pairs of fp32 for the plan's prefix; every op is one rounded fp32
+// add (no contraction in this translation unit).
+struct DF {
+  float hi, lo;
+};
+__device__ __forceinline__ DF two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return DF{s, err};
+}
+__device__ __forceinline__ DF df_add(DF x, DF y) {
+  const DF s = two_sum(x.hi, y.hi);
+  const float lo = __fadd_rn(s.lo, __fadd_rn(x.lo, y.lo));
+  const float hi = __fadd_rn(s.hi, lo);
+  return DF{hi, __fsub_rn(lo, __fsub_rn(hi, s.hi))};
+}
+__device__ __forceinline__ DF df_addf(DF x, float y) { return df_add(x, DF{y, 0.0f}); }
+__device__ __forceinline__ DF df_from_double(double v) {
+  const float h = (float)v;                       // once per sum
+  return DF{h, (float)(v - (double)h)};
+}
+__device__ __forceinline__ DF shfl_xor_df(DF v, int m) {
+  return DF{__shfl_xor_sync(0xffffffffu, v.hi, m), __shfl_xor_sync(0xffffffffu, v.lo, m)};
 }
 
-// Binade (unbiased exponent) shared by all of [lo, hi], or false.
-__device__ __forceinline__ bool one_binade(double lo, double hi, int &e) {
-  double a, b;
-  if (lo > 0.0) { a = lo; b = hi; }
-  else if (hi < 0.0) { a = -hi; b = -lo; }
+// ---------------------------------------------------------------- the plan's term image
+// fp32 image of a term from its high word: 20 fraction bits (truncated), the
+// exponent moved to the fp32 bias; magnitudes below 2^-127 give 0.  Terms of
+// 2^128 and above need the clamped form.
+__device__ __forceinline__ float approx_term(uint32_t hi) {
+  const uint32_t v = max(hi & 0x7FFFFFFFu, kMagLo);
+  return __uint_as_float(((v - kMagLo) * 8u) | (hi & 0x80000000u));
+}
+__device__ __forceinline__ float approx_term_clamped(uint32_t hi) {
+  const uint32_t v = min(max(hi & 0x7FFFFFFFu, kMagLo), (1150u << 20) | 0xFFFFFu);
+  return __uint_as_float(((v - kMagLo) * 8u) | (hi & 0x80000000u));
+}
+
+// Binade (unbiased exponent) shared by all of [lo, hi] (fp32), or false.
+__device__ __forceinline__ bool one_binade_f(float lo, float hi, int &e) {
+  float a, b;
+  if (lo > 0.0f) { a = lo; b = hi; }
+  else if (hi < 0.0f) { a = -hi; b = -lo; }
   else return false;
-  const int ea = (int)((dbits(a) >> 52) & 0x7FF), eb = (int)((dbits(b) >> 52) & 0x7FF);
-  if (ea != eb || ea == 0 || ea == 0x7FF) return false;
-  e = ea - 1023;
+  const int ea = (int)((__float_as_uint(a) >> 23) & 0xFF), eb = (int)((__float_as_uint(b) >> 23) & 0xFF);
+  if (ea != eb || ea == 0 || ea == 0xFF) return false;
+  e = ea - 127;
   return true;
 }
 
@@ -173,19 +205,11 @@ __device__ __forceinline__ Run shfl_run(const Run &r, int arg) {
   }
   return o;
 }
-__device__ __forceinline__ Rec shfl_rec(const Rec &r, int src) {
-  Rec o;
-  const int *s = reinterpret_cast<const int *>(&r);
-  int *d = reinterpret_cast<int *>(&o);
-#pragma unroll
-  for (int i = 0; i < 8; i++) d[i] = __shfl_sync(0xffffffffu, s[i], src);
-  return o;
-}
 
-__device__ __forceinline__ Rec make_rec(const Run &r, int e, uint32_t kind, uint32_t count) {
+__device__ __forceinline__ Rec make_rec(const Run &r, int e, uint32_t kind, uint32_t count, uint32_t tstart) {
   Rec q;
   q.inc = r.inc; q.lo = r.lo; q.hi = r.hi;
-  q.meta = rec_meta(r.d, r.flags, kind);
+  q.meta = rec_meta(r.d, r.flags, kind, tstart);
   q.e = (int16_t)e;
   q.count = (uint16_t)count;
   return q;
@@ -210,6 +234,34 @@ __device__ __forceinline__ void stcg_rec(Rec *p, const Rec &r) {
   int4 *q = reinterpret_cast<int4 *>(p);
   __stcg(q, s[0]);
   __stcg(q + 1, s[1]);
+}
+
+// Tile headers: the call's tag in the top byte of lo and of hi (so both
+// 16-byte halves carry it), values sign-extended from 56 bits.
+constexpr int64_t kBound56 = ((int64_t)1 << 55) - 1;
+__device__ __forceinline__ int64_t untag56(uint64_t v) { return (int64_t)(v << 8) >> 8; }
+__device__ __forceinline__ void publish_header(Rec *p, const Rec &r, uint32_t tag) {
+  const int64_t lo = max(min(r.lo, kBound56), -kBound56), hi = max(min(r.hi, kBound56), -kBound56);
+  const uint64_t a0 = (uint64_t)r.inc;
+  const uint64_t a1 = ((uint64_t)lo & 0x00FFFFFFFFFFFFFFull) | ((uint64_t)tag << 56);
+  const uint64_t b0 = ((uint64_t)hi & 0x00FFFFFFFFFFFFFFull) | ((uint64_t)tag << 56);
+  const uint64_t b1 = (uint64_t)r.meta | ((uint64_t)(uint16_t)r.e << 32) | ((uint64_t)r.count << 48);
+  st_vol_v2(p, a0, a1);
+  st_vol_v2(reinterpret_cast<char *>(p) + 16, b0, b1);
+}
+// False while the header does not carry `tag` in both halves.
+__device__ __forceinline__ bool read_header(const Rec *p, uint32_t tag, Rec &r) {
+  uint64_t a0, a1, b0, b1;
+  ld_vol_v2(p, a0, a1);
+  ld_vol_v2(reinterpret_cast<const char *>(p) + 16, b0, b1);
+  if ((uint32_t)(a1 >> 56) != tag || (uint32_t)(b0 >> 56) != tag) return false;
+  r.inc = (int64_t)a0;
+  r.lo = untag56(a1);
+  r.hi = untag56(b0);
+  r.meta = (uint32_t)b1;
+  r.e = (int16_t)(uint16_t)(b1 >> 32);
+  r.count = (uint16_t)(b1 >> 48);
+  return true;
 }
 
 // ---------------------------------------------------------------- tile geometry
@@ -239,91 +291,528 @@ __device__ __forceinline__ TileGeo tile_geo(const Params &p, int64_t t, int64_t 
     g.first_tile = __ldcg(&p.tile_begin[lo]);
     g.ntiles_sum = __ldcg(&p.tile_begin[lo + 1]) - g.first_tile;
     g.tile_in_sum = t - g.first_tile;
-    const int64_t s0 = p.offsets[lo];
-    g.start = s0 + g.tile_in_sum * kTileTerms;
+    g.start = p.offsets[lo] + g.tile_in_sum * kTileTerms;
     g.end = min(p.offsets[lo + 1], g.start + kTileTerms);
   }
   return g;
 }
 
+// ---------------------------------------------------------------- shared memory
+struct WarpAgg {
+  float sig, ab;
+  uint32_t orh, orz, mx, andh;
+};
+
+struct Smem {
+  uint64_t bar[kStages];
+  int64_t tk[kStages];
+  int tma[kStages];
+  WarpAgg wa[kStages][kWarps];
+  DF agg[kStages];
+  float agg_abs[kStages];
+  DF ex;
+  float ex_abs;
+  Rec chunk[kWarps];
+  int nitems[kWarps];               // >0: a split chunk's items in the tile's item area
+  unsigned long long st[S_COUNT];
+  // walker
+  uint64_t S;
+  int m, nel, restart, nseg;
+  int wflag[kWarps];
+  Run wagg[kWarps];
+  int wcnt[kWarps];
+  int sum_k;
+};
+
 // ---------------------------------------------------------------- look-back
-// Per tile two tagged 64-bit words: A = approximate prefix (fp64, low 8 bits
-// replaced by the tag), B = approximate |x| prefix (fp32) << 32 | tag.
-// tag = epoch << 1 | kind; kind 0 = this tile's aggregate, 1 = inclusive
-// prefix.  Each word is written and read whole, and a reader accepts a tile
-// only when both words carry the current tag, so no fence is needed.
-__device__ __forceinline__ void publish(uint64_t *st, double sig, float ab, uint32_t epoch, uint32_t kind) {
+// Per tile two tagged 64-bit words, written and read as one 16-byte access:
+//   A = sum.hi (fp32) << 32 | sum.lo (fp32) with its low 8 bits replaced by the tag
+//   B = |x| sum (fp32) << 32 | tag;   tag = epoch << 1 | kind,
+// kind 0 = the tile's own sum, 1 = the inclusive prefix.  A reader takes a
+// tile only when both words carry the current tag, so no fence is needed.
+__device__ __forceinline__ void publish_status(uint64_t *st, DF sig, float ab, uint32_t epoch, uint32_t kind) {
   const uint32_t tag = (epoch << 1) | kind;
-  const uint64_t A = (dbits(sig) & ~0xFFull) | tag;
+  const uint64_t A = ((uint64_t)__float_as_uint(sig.hi) << 32) | ((__float_as_uint(sig.lo) & ~0xFFu) | tag);
   const uint64_t B = ((uint64_t)__float_as_uint(ab) << 32) | tag;
-  st_vol_u64(st, A);
-  st_vol_u64(st + 1, B);
+  st_vol_v2(st, A, B);
 }
 
-// Run by one whole warp.  Returns the approximate exclusive prefix of tile t.
-__device__ void lookback(const Params &p, const TileGeo &g, int64_t t, double agg_sig, float agg_abs,
-                         double &ex_sig, float &ex_abs, unsigned long long *st) {
+struct Prefix {
+  DF ex;
+  float ex_abs;
+};
+
+// Run by one whole warp; returns the approximate exclusive prefix of tile t
+// (the first tile of sum `sum` starts from s0).  Each lane reads 8
+// consecutive statuses, so one round trip covers 256 tiles.
+__device__ __noinline__ Prefix lookback(const Params &p, int sum, int64_t first_tile, int64_t t, DF agg,
+                                        float agg_abs, unsigned long long *st) {
   const int lane = threadIdx.x & 31;
   const uint32_t ep = p.epoch;
-  if (g.tile_in_sum == 0) {
-    const double s0 = p.s0s ? p.s0s[g.sum] : p.s0;
-    ex_sig = s0;
-    ex_abs = fabsf((float)s0);
-    if (lane == 0) publish(p.status + 2 * t, s0 + agg_sig, ex_abs + agg_abs, ep, 1);
-    return;
+  if (t == first_tile) {                    // its inclusive prefix went out with its sum
+    const double s0 = p.s0s ? p.s0s[sum] : p.s0;
+    const DF ex = df_from_double(s0);
+    return Prefix{ex, fabsf(ex.hi)};
   }
-  if (lane == 0) publish(p.status + 2 * t, agg_sig, agg_abs, ep, 0);
-  double run_sig = 0.0;
+  DF run = DF{0.0f, 0.0f};
   float run_abs = 0.0f;
   int64_t j = t - 1;
   const uint64_t t0 = globaltimer();
   bool gave_up = false;
   while (true) {
     if (lane == 0) atomicAdd(&st[S_LOOKBACK_STEPS], 1ull);
-    const int64_t idx = j - lane;
-    double v = 0.0;
-    float a = 0.0f;
-    bool valid = true, incl = true;             // before the sum: a virtual prefix of 0
-    if (idx >= g.first_tile) {
-      const uint64_t A = ld_vol_u64(p.status + 2 * idx);
-      const uint64_t B = ld_vol_u64(p.status + 2 * idx + 1);
-      const uint32_t ta = (uint32_t)(A & 0xFF), tb = (uint32_t)(B & 0xFFFFFFFFu);
-      valid = ((ta >> 1) == ep) && (ta == tb);
-      incl = valid && (ta & 1u);
-      v = bitsd(A & ~0xFFull);
-      a = __uint_as_float((uint32_t)(B >> 32));
+    // this lane: tiles j - 8*lane - q, q = 0..7 (descending)
+    DF sum = DF{0.0f, 0.0f};
+    float sab = 0.0f;
+    bool incl = false;           // reached an inclusive status (or the sum's start)
+    bool ready = true;           // every status up to there is present
+    for (int q = 0; q < 8 && !incl; q++) {
+      const int64_t idx = j - 8 * lane - q;
+      if (idx < first_tile) { incl = true; break; }            // a virtual prefix of 0
+      uint64_t A, B;
+      ld_vol_v2(p.status + 2 * idx, A, B);
+      const uint32_t ta = (uint32_t)(A & 0xFF), tb = (uint32_t)B;
+      if (((ta >> 1) != ep) || (ta != tb)) { ready = false; break; }
+      sum = df_add(sum, DF{__uint_as_float((uint32_t)(A >> 32)), __uint_as_float((uint32_t)A & ~0xFFu)});
+      sab += __uint_as_float((uint32_t)(B >> 32));
+      if (ta & 1u) incl = true;
     }
-    const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
-    const uint32_t imask = __ballot_sync(0xffffffffu, incl);
+    const uint32_t rmask = __ballot_sync(0xffffffffu, ready);
+    const uint32_t imask = __ballot_sync(0xffffffffu, ready && incl);
     bool done = false, advance = false;
     int L = 31;
     if (imask) {
-      L = __ffs(imask) - 1;                           // nearest inclusive predecessor
+      L = __ffs(imask) - 1;                                     // lane holding the nearest inclusive
       const uint32_t need = (L == 31) ? 0xffffffffu : ((2u << L) - 1u);
-      done = (vmask & need) == need;
-    } else if (vmask == 0xffffffffu) {
+      done = (rmask & need) == need;
+    } else if (rmask == 0xffffffffu) {
       advance = true;
     }
     if (!done && !advance) {
-      if (globaltimer() - t0 > kWaitNs) { gave_up = true; done = true; L = 31; }
-      else { __nanosleep(32); continue; }
+      if (globaltimer() - t0 > kWaitNs) { gave_up = true; done = true; L = -1; }
+      else { __nanosleep(20); continue; }
     }
-    double cv = (lane <= L && valid) ? v : 0.0;
-    float ca = (lane <= L && valid) ? a : 0.0f;
+    DF c = (lane <= L) ? sum : DF{0.0f, 0.0f};
+    float ca = (lane <= L) ? sab : 0.0f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      cv += __shfl_xor_sync(0xffffffffu, cv, o);
+      c = df_add(c, shfl_xor_df(c, o));
       ca += __shfl_xor_sync(0xffffffffu, ca, o);
     }
-    run_sig += cv;
+    run = df_add(run, c);
     run_abs += ca;
     if (done) break;
-    j -= 32;
+    j -= 256;
   }
   if (gave_up && lane == 0) atomicOr(&p.ctr[C_ERR], ERR_PLAN_TIMEOUT);
-  ex_sig = run_sig;
-  ex_abs = run_abs;
-  if (lane == 0) publish(p.status + 2 * t, run_sig + agg_sig, run_abs + agg_abs, ep, 1);
+  if (lane == 0) publish_status(p.status + 2 * t, df_add(run, agg), run_abs + agg_abs, ep, 1);
+  return Prefix{run, run_abs};
+}
+
+// ---------------------------------------------------------------- lanes
+__device__ __forceinline__ void load_lane(const Params &p, const unsigned char *stage, bool use_tma,
+                                          int64_t row, int64_t lstart, int nv, int w, int lane, uint64_t *xs) {
+  if (use_tma && row < p.tma_rows) {
+    const unsigned char *rp = stage + (w * 32 + lane) * 128;
+    const int sw = lane & 7;
+#pragma unroll
+    for (int c = 0; c < 8; c++) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(rp + ((c ^ sw) << 4));
+      xs[2 * c] = ((uint64_t)v.y << 32) | v.x;
+      xs[2 * c + 1] = ((uint64_t)v.w << 32) | v.z;
+    }
+#pragma unroll
+    for (int i = 0; i < kLaneTerms; i++)
+      if (i >= nv) xs[i] = 0ull;
+  } else {
+    const unsigned long long *gp = reinterpret_cast<const unsigned long long *>(p.x) + lstart;
+#pragma unroll
+    for (int i = 0; i < kLaneTerms; i++) xs[i] = (i < nv) ? __ldg(gp + i) : 0ull;
+  }
+}
+
+// Exact run of a lane's terms under binade e (the general path).
+__device__ __forceinline__ Run lane_run_general(const uint64_t *xs, int nv, int e) {
+  Run r = run_empty();
+#pragma unroll
+  for (int i = 0; i < kLaneTerms; i++) {
+    if (i < nv) {
+      int64_t re;
+      int32_t d;
+      const bool poison = term_inc(xs[i], e, re, d);
+      run_push(r, re, d, term_flags(xs[i]) | (poison ? F_POISON : 0u));
+    }
+  }
+  return r;
+}
+
+// Items of one lane the plan could not place in a binade, term by term: runs
+// of terms whose approximate prefix stays inside one binade, and up to three
+// carried terms per item where it does not.  With out == nullptr only counts.
+__device__ __noinline__ int lane_items(const Params &p, const uint64_t *xs, int nv, float A, float dbase, uint64_t t, int w,
+                          int lane, Rec *out) {
+  float a = A;
+  int cur = 0, cur_e = 0, nterms = 0, cstart = 0, n = 0;
+  Run rr = run_empty();
+  int64_t vals[3] = {0, 0, 0};
+  uint32_t tf_or = 0;
+  const uint32_t tbase = (uint32_t)(w * kChunkTerms + lane * kLaneTerms);
+  for (int i = 0; i <= nv; i++) {
+    int kind = 0, ei = 0;
+    int64_t re = 0;
+    int32_t dd = 0;
+    if (i < nv) {
+      const float a1 = a + approx_term_clamped((uint32_t)(xs[i] >> 32));
+      const float d = dbase + kRelF32 * fmaxf(fabsf(a), fabsf(a1));
+      bool ok = one_binade_f(fminf(a, a1) - d, fmaxf(a, a1) + d, ei);
+      ok = plan_override(p.plan_mode, ok, ei, t, w, 100 + lane * 16 + i);
+      if (ok && term_inc(xs[i], ei, re, dd)) ok = false;
+      kind = ok ? 1 : 2;
+      a = a1;
+    }
+    // close the open item when this term does not extend it
+    const bool extend = (i < nv) && ((kind == 1 && cur == 1 && cur_e == ei) || (kind == 2 && cur == 2 && nterms < 3));
+    if (!extend && cur != 0) {
+      if (out) {
+        if (cur == 1) {
+          stcg_rec(out + n, make_rec(rr, cur_e, K_RUN, (uint32_t)(i - cstart), tbase + (uint32_t)cstart));
+        } else {
+          Run tr = run_empty();
+          tr.inc = vals[0]; tr.lo = vals[1]; tr.hi = vals[2]; tr.d = 0;
+          tr.flags = tf_or & (F_HASINF_P | F_HASINF_N | F_HASNAN);
+          stcg_rec(out + n, make_rec(tr, 0, K_TERMS, (uint32_t)nterms, tbase + (uint32_t)cstart));
+        }
+      }
+      n++;
+      cur = 0;
+    }
+    if (i == nv) break;
+    if (cur == 0) {
+      cur = kind;
+      cstart = i;
+      rr = run_empty();
+      nterms = 0;
+      tf_or = 0;
+      cur_e = ei;
+    }
+    if (kind == 1) {
+      run_push(rr, re, dd, term_flags(xs[i]));
+    } else {
+      vals[nterms++] = (int64_t)xs[i];
+      tf_or |= term_flags(xs[i]);
+    }
+  }
+  return n;
+}
+
+// A chunk the plan could not place in one binade.  Lanes that fit one become
+// runs (neighbouring runs of one binade merge); the other lanes are placed
+// term by term.  Writes the items for chunk w into the tile's item area and
+// returns their number, or 0 when they do not fit (the caller then records
+// the chunk as one fallback).
+__device__ __noinline__ int split_chunk(const Params &p, const unsigned char *stage, bool use_tma, int64_t row,
+                                       int64_t lstart, int nv, int w, int lane, DF sc, float ac, uint64_t t,
+                                       Rec *area, unsigned long long *st) {
+  uint64_t xs[kLaneTerms];
+  load_lane(p, stage, use_tma, row, lstart, nv, w, lane, xs);
+  float sig = 0.0f, ab = 0.0f;
+  uint32_t orz = 0;
+#pragma unroll
+  for (int i = 0; i < kLaneTerms; i++) {
+    const uint32_t hi = (uint32_t)(xs[i] >> 32);
+    const float f = approx_term_clamped(hi);
+    sig += f;
+    ab += fabsf(f);
+    orz |= (hi & 0x7FFFFFFFu) | (uint32_t)xs[i];
+  }
+  float isig = sig, iab = ab;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float a = __shfl_up_sync(0xffffffffu, isig, o);
+    const float b = __shfl_up_sync(0xffffffffu, iab, o);
+    if (lane >= o) { isig += a; iab += b; }
+  }
+  const DF A0 = df_addf(sc, isig - sig);
+  const float A = A0.hi + A0.lo;
+  const float P = 0.5f * (ab + sig), N = 0.5f * (ab - sig);
+  const float dbase = kEps * (ac + (iab - ab) + ab) + kTinyF;
+  const float dl = dbase + kRelF32 * (fabsf(A) + ab);
+  int e_l = 0;
+  bool clean = one_binade_f(A - N - dl, A + P + dl, e_l);
+  clean = plan_override(p.plan_mode, clean, e_l, t, w, lane + 1);
+  const bool zl = (orz == 0);
+  const bool dirty = !clean && !zl && nv > 0;
+  Run r = run_empty();
+  if (!dirty) r = lane_run_general(xs, nv, clean ? e_l : 0);
+  const int key = dirty ? -1 : (clean ? e_l : kZeroE);
+  const int ndirty = dirty ? lane_items(p, xs, nv, A, dbase, t, w, lane, nullptr) : 0;
+  if (dirty) atomicAdd(&st[S_LANE_DIRTY], 1ull);
+  // merge neighbouring runs of one key (lanes past the end join the previous)
+  const int pkey = __shfl_up_sync(0xffffffffu, key, 1);
+  const bool head = (lane == 0) || (nv > 0 && (dirty || pkey == -1 || key != pkey));
+  Run v = r;
+  int fl = head ? 1 : 0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const Run ov = shfl_run<SH_UP>(v, o);
+    const int of = __shfl_up_sync(0xffffffffu, fl, o);
+    if (lane >= o) { if (!fl) v = run_compose(ov, v); fl |= of; }
+  }
+  const uint32_t heads = __ballot_sync(0xffffffffu, head);
+  const bool end = (lane == 31) || ((heads >> (lane + 1)) & 1u);
+  const uint32_t le = heads & ((lane == 31) ? 0xffffffffu : ((2u << lane) - 1u));
+  const int hlane = 31 - __clz(le);
+  const int hkey = __shfl_sync(0xffffffffu, key, hlane);
+  // terms before each lane, for the item counts
+  int csum = nv;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int vv = __shfl_up_sync(0xffffffffu, csum, o);
+    if (lane >= o) csum += vv;
+  }
+  const int before_head = __shfl_sync(0xffffffffu, csum - nv, hlane);
+  const int myitems = dirty ? ndirty : ((end && hkey != -1) ? 1 : 0);
+  int ioff = myitems;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int vv = __shfl_up_sync(0xffffffffu, ioff, o);
+    if (lane >= o) ioff += vv;
+  }
+  const int total = __shfl_sync(0xffffffffu, ioff, 31);
+  ioff -= myitems;
+  if (total > kChunkSlots) return 0;
+  Rec *out = area + w * kChunkSlots;
+  if (!dirty && myitems)
+    stcg_rec(out + ioff, make_rec(v, hkey, K_RUN, (uint32_t)(csum - before_head),
+                                  (uint32_t)(w * kChunkTerms + hlane * kLaneTerms)));
+  if (dirty) lane_items(p, xs, nv, A, dbase, t, w, lane, out + ioff);
+  return total;
+}
+
+// ---------------------------------------------------------------- phase A: the plan's sums
+__device__ void phase_a(const Params &p, Smem &sm, const unsigned char *stage, int s, int64_t t, int64_t ntiles) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const TileGeo g = tile_geo(p, t, ntiles);
+  const int64_t lstart = g.start + (int64_t)w * kChunkTerms + (int64_t)lane * kLaneTerms;
+  const int nv = (int)max((int64_t)0, min((int64_t)kLaneTerms, g.end - lstart));
+  uint64_t xs[kLaneTerms];
+  load_lane(p, stage, sm.tma[s] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, xs);
+  float sig = 0.0f, ab = 0.0f;
+  uint32_t orh = 0, orz = 0, mx = 0, andh = 0xFFFFFFFFu;
+#pragma unroll
+  for (int i = 0; i < kLaneTerms; i++) {
+    const uint32_t hi = (uint32_t)(xs[i] >> 32);
+    const uint32_t mag = hi & 0x7FFFFFFFu;
+    orh |= hi;
+    orz |= mag | (uint32_t)xs[i];
+    mx = max(mx, mag);
+    andh &= (i < nv) ? hi : 0xFFFFFFFFu;
+    const float f = approx_term(hi);
+    sig += f;
+    ab += fabsf(f);
+  }
+  if (mx >= (1151u << 20)) {                 // a term of 2^128 or more: clamp the images
+    sig = 0.0f;
+    ab = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kLaneTerms; i++) {
+      const float f = approx_term_clamped((uint32_t)(xs[i] >> 32));
+      sig += f;
+      ab += fabsf(f);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sig += __shfl_xor_sync(0xffffffffu, sig, o);
+    ab += __shfl_xor_sync(0xffffffffu, ab, o);
+    orh |= __shfl_xor_sync(0xffffffffu, orh, o);
+    orz |= __shfl_xor_sync(0xffffffffu, orz, o);
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    andh &= __shfl_xor_sync(0xffffffffu, andh, o);
+  }
+  if (lane == 0) sm.wa[s][w] = WarpAgg{sig, ab, orh, orz, mx, andh};
+  __syncthreads();
+  if (w == 0) {
+    DF agg = DF{0.0f, 0.0f};
+    float agga = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kWarps; k++) { agg = df_addf(agg, sm.wa[s][k].sig); agga += sm.wa[s][k].ab; }
+    if (lane == 0) {
+      sm.agg[s] = agg;
+      sm.agg_abs[s] = agga;
+      if (g.tile_in_sum != 0) {
+        publish_status(p.status + 2 * t, agg, agga, p.epoch, 0);
+      } else {                                   // the first tile of a sum: s0 + its sum at once
+        const DF ex = df_from_double(p.s0s ? p.s0s[g.sum] : p.s0);
+        publish_status(p.status + 2 * t, df_add(ex, agg), fabsf(ex.hi) + agga, p.epoch, 1);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- phase B: runs of a tile
+__device__ void phase_b(const Params &p, Smem &sm, const unsigned char *stage, int s, int64_t t, int64_t ntiles) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  unsigned long long *st = sm.st;
+  const TileGeo g = tile_geo(p, t, ntiles);
+  if (w == 0) {
+    const Prefix pr = lookback(p, g.sum, g.first_tile, t, sm.agg[s], sm.agg_abs[s], st);
+    if (lane == 0) { sm.ex = pr.ex; sm.ex_abs = pr.ex_abs; }
+  }
+  __syncthreads();
+  // ---- plan of this warp's chunk
+  DF sc = sm.ex;
+  float ac = sm.ex_abs;
+  for (int k = 0; k < w; k++) { sc = df_addf(sc, sm.wa[s][k].sig); ac += sm.wa[s][k].ab; }
+  const WarpAgg me = sm.wa[s][w];
+  const int64_t cstart = g.start + (int64_t)w * kChunkTerms;
+  const int cnt_chunk = (int)max((int64_t)0, min((int64_t)kChunkTerms, g.end - cstart));
+  const int64_t lstart = cstart + (int64_t)lane * kLaneTerms;
+  const int nv = (int)max((int64_t)0, min((int64_t)kLaneTerms, g.end - lstart));
+  int e = 0;
+  bool clean;
+  {
+    const float P = 0.5f * (me.ab + me.sig), N = 0.5f * (me.ab - me.sig);
+    const float c = sc.hi + sc.lo;
+    const float delta = kEps * (ac + me.ab) + kRelF32 * (fabsf(c) + me.ab) + kTinyF;
+    clean = one_binade_f(c - N - delta, c + P + delta, e);
+    clean = plan_override(p.plan_mode, clean, e, (uint64_t)t, w, 0);
+  }
+  uint64_t xs[kLaneTerms];
+  load_lane(p, stage, sm.tma[s] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, xs);
+  Rec *area = p.items + t * kTileSlots;
+  Rec crec;
+  int nitems = 0;
+  const bool zero_chunk = (me.orz == 0);
+  if (clean || zero_chunk) {
+    if (zero_chunk) e = 0;
+    const int eb = e + 1023;
+    const bool fast = !zero_chunk && e >= -969 && e <= 1023 && (int)(me.mx >> 20) < eb;
+    Run r;
+    bool general_reduce = true;
+    if (fast) {
+      const int c = 64 - eb;
+      if ((me.orh >> 31) == 0) {
+        // non-negative terms: the run is a plain sum of increments
+        uint64_t a = 0;
+        bool anytie = false;
+#pragma unroll
+        for (int i = 0; i < kLaneTerms; i++) {
+          uint64_t ri;
+          bool tie;
+          term_inc_fast((uint32_t)(xs[i] >> 32), (uint32_t)xs[i], c, ri, tie);
+          a += ri;
+          anytie |= tie;
+        }
+        if (__ballot_sync(0xffffffffu, anytie) == 0) {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+          r.inc = (int64_t)a; r.lo = 0; r.hi = (int64_t)a; r.d = 0; r.flags = F_NONNEG;
+          general_reduce = false;
+        } else if (anytie) {
+          r = lane_run_general(xs, nv, e);
+        } else {
+          r.inc = (int64_t)a; r.lo = 0; r.hi = (int64_t)a; r.d = 0;
+          r.flags = F_NONNEG | (nv == 0 ? (F_NONPOS | F_ZERO | F_ALLNEGZ) : 0u);
+        }
+      } else {
+        // signed terms: positive and negative increments summed apart give
+        // bounds for every prefix
+        uint64_t P = 0, Nn = 0;
+        bool anytie = false;
+        uint32_t orl = 0, andl = 0xFFFFFFFFu;
+#pragma unroll
+        for (int i = 0; i < kLaneTerms; i++) {
+          const uint32_t hi = (uint32_t)(xs[i] >> 32);
+          uint64_t ri;
+          bool tie;
+          term_inc_fast(hi, (uint32_t)xs[i], c, ri, tie);
+          if (hi >> 31) Nn += ri; else P += ri;
+          anytie |= tie;
+          if (i < nv) { orl |= hi; andl &= hi; }
+        }
+        if (anytie) {
+          r = lane_run_general(xs, nv, e);
+        } else if (nv == 0) {
+          r = run_empty();
+        } else {
+          r.inc = (int64_t)(P - Nn); r.lo = -(int64_t)Nn; r.hi = (int64_t)P; r.d = 0;
+          r.flags = ((orl >> 31) ? 0u : F_NONNEG) | ((andl >> 31) ? F_NONPOS : 0u);
+        }
+      }
+    } else {
+      r = lane_run_general(xs, nv, e);
+    }
+    if (general_reduce) {
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const Run o = shfl_run<SH_DOWN>(r, off);
+        if ((lane & (2 * off - 1)) == 0) r = run_compose(r, o);
+      }
+    }
+    crec = make_rec(r, (r.flags & F_ZERO) ? kZeroE : e, K_RUN, (uint32_t)cnt_chunk, (uint32_t)(w * kChunkTerms));
+    if (lane == 0) atomicAdd(&st[S_CHUNK_RUN], 1ull);
+  } else {
+    nitems = split_chunk(p, stage, sm.tma[s] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, sc, ac,
+                         (uint64_t)t, area, st);
+    if (nitems == 0) {
+      Run fr = run_empty();
+      fr.flags = ((me.mx >= 0x7FF00000u) ? (F_HASINF_P | F_HASINF_N | F_HASNAN) : 0u);
+      crec = make_rec(fr, 0, K_FALLBACK, (uint32_t)cnt_chunk, (uint32_t)(w * kChunkTerms));
+      if (lane == 0) { stcg_rec(area + w * kChunkSlots, crec); atomicAdd(&st[S_POOL_OVERFLOW], 1ull); }
+      nitems = 1;
+    } else if (lane == 0) {
+      atomicAdd(&st[S_CHUNK_LIST], 1ull);
+      atomicAdd(&st[S_ITEMS], (unsigned long long)nitems);
+    }
+    crec.meta = rec_meta(0, 0, K_COMPLEX, 0);
+  }
+  if (lane == 0) {
+    sm.chunk[w] = crec;
+    sm.nitems[w] = nitems;
+  }
+  __threadfence();
+  __syncthreads();
+  // ---- the tile's header
+  if (tid == 0) {
+    bool all_run = true;
+    int et = kZeroE;
+    for (int k = 0; k < kWarps; k++) {
+      const Rec &c = sm.chunk[k];
+      if (rec_kind(c.meta) != K_RUN) { all_run = false; break; }
+      if (rec_flags(c.meta) & F_ZERO) continue;
+      if (et == kZeroE) et = c.e;
+      else if (c.e != et) { all_run = false; break; }
+    }
+    Rec hd;
+    if (all_run) {
+      Run acc = run_empty();
+      for (int k = 0; k < kWarps; k++) acc = run_compose(acc, rec_run(sm.chunk[k]));
+      hd = make_rec(acc, (acc.flags & F_ZERO) ? kZeroE : et, K_RUN, (uint32_t)(g.end - g.start), 0);
+    } else {
+      uint64_t packed = 0;
+      uint32_t orf = 0;
+      for (int k = 0; k < kWarps; k++) {
+        const Rec &c = sm.chunk[k];
+        int n = sm.nitems[k];
+        if (rec_kind(c.meta) == K_RUN) {
+          if (c.count > 0) { stcg_rec(area + k * kChunkSlots, c); n = 1; }
+          else n = 0;
+        }
+        orf |= rec_flags(c.meta);
+        packed |= (uint64_t)(uint32_t)n << (8 * k);
+      }
+      Run z = run_empty();
+      z.inc = (int64_t)packed;
+      z.flags = orf & (F_HASINF_P | F_HASINF_N | F_HASNAN);
+      hd = make_rec(z, 0, K_COMPLEX, (uint32_t)(g.end - g.start), 0);
+      hd.inc = (int64_t)packed;
+      atomicAdd(&st[S_TILE_COMPLEX], 1ull);
+    }
+    __threadfence();
+    publish_header(p.hdr + t, hd, (p.epoch << 1) | 1u);
+    atomicAdd(&st[S_TILES], 1ull);
+  }
 }
 
 // ---------------------------------------------------------------- the walk
@@ -348,546 +837,421 @@ __device__ uint64_t add_terms(const Params &p, uint64_t Sb, int64_t a, int64_t c
   for (int64_t base = 0; base < cnt; base += 32) {
     const double v = (base + lane < cnt) ? __ldg(p.x + a + base + lane) : 0.0;
     const int m = (int)min((int64_t)32, cnt - base);
-    for (int j = 0; j < m; j++) {
-      const double t = __shfl_sync(0xffffffffu, v, j);
-      S = __dadd_rn(S, t);
-    }
+    for (int j = 0; j < m; j++) S = __dadd_rn(S, __shfl_sync(0xffffffffu, v, j));
   }
   if (lane == 0) atomicAdd(&st[S_TERMS_ADDED], (unsigned long long)cnt);
   return dbits(S);
 }
 
-// Apply one record to S (warp-uniform).  A run the check rejects falls back
-// to term-by-term adds over the record's terms [a, a + cnt).
-__device__ uint64_t apply_or_add(const Params &p, uint64_t Sb, const Rec &q, int64_t a, int64_t cnt,
-                                 unsigned long long *st) {
-  const int lane = threadIdx.x & 31;
-  if (nonfinite(Sb)) return absorb(Sb, rec_flags(q.meta));
-  if (rec_kind(q.meta) == K_RUN) {
-    uint64_t T = Sb;
-    if (run_apply(T, rec_run(q), q.e) == APPLY_OK) return T;
-    if (lane == 0) atomicAdd(&st[S_RUN_REJECTED], 1ull);
-  }
-  return add_terms(p, Sb, a, cnt, st);
+__device__ __forceinline__ bool elem_alone(const Rec &q) { return rec_kind(q.meta) != K_RUN; }
+__device__ __forceinline__ int elem_key(const Rec &q) {
+  return (rec_flags(q.meta) & F_ZERO) ? kZeroE : (int)q.e;
 }
 
-// One chunk record (warp-uniform): a run, a list of items, or a fallback.
-__device__ uint64_t walk_chunk(const Params &p, uint64_t Sb, const Rec &c, int64_t a, int64_t cnt,
-                               unsigned long long *st) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t kind = rec_kind(c.meta);
-  if (kind != K_LIST) {
-    if (kind == K_FALLBACK && lane == 0) atomicAdd(&st[S_CHUNK_FALLBACK], 1ull);
-    return apply_or_add(p, Sb, c, a, cnt, st);
-  }
-  if (nonfinite(Sb)) return absorb(Sb, rec_flags(c.meta));
-  const int nit = (int)c.lo;
-  Rec mine;
-  if (lane < nit) mine = ldcg_rec(p.pool + c.inc + lane);
-  int64_t pos = a;
-  for (int i = 0; i < nit; i++) {
-    const Rec it = shfl_rec(mine, i);
-    const int64_t n_it = min((int64_t)it.count, a + cnt - pos);
-    Sb = apply_or_add(p, Sb, it, pos, n_it, st);
-    pos += it.count;
-  }
-  return Sb;
-}
-
-// A tile the segment composite could not cover: its chunks in order.
-__device__ uint64_t walk_tile(const Params &p, uint64_t Sb, int64_t t, const TileGeo &g, unsigned long long *st) {
-  const int lane = threadIdx.x & 31;
-  Rec mine;
-  if (lane < kWarps) mine = ldcg_rec(p.chunk_rec + t * kWarps + lane);
-  for (int c = 0; c < kWarps; c++) {
-    const int64_t a = g.start + (int64_t)c * kChunkTerms;
-    if (a >= g.end) break;
-    const int64_t cnt = min((int64_t)kChunkTerms, g.end - a);
-    Sb = walk_chunk(p, Sb, shfl_rec(mine, c), a, cnt, st);
-  }
-  return Sb;
-}
-
-__device__ __forceinline__ int seg_key(const Rec &q) {
-  // a complex tile is a segment of its own; runs of zeros apart from runs
-  if (rec_kind(q.meta) != K_RUN) return kComplexKey;
-  if (rec_flags(q.meta) & F_ZERO) return kZeroE;
-  return q.e;
-}
-
-// The in-order walk of the sum of tile g0 over its tiles, by the whole CTA;
-// the serial part runs on warp 0.  `srec` is a free stage buffer.
-__device__ void walk_sum(const Params &p, const TileGeo &g0, Rec *srec, unsigned long long *st) {
-  __shared__ int s_ends[kWalkBatch];
-  __shared__ unsigned char s_head[kWalkBatch];
-  __shared__ int s_wcnt[kWarps];
-  __shared__ int s_nends;
-  __shared__ uint64_t s_S;
-  __shared__ int s_restart;
-  __shared__ Run s_wagg[kWarps];
-  __shared__ int s_wflag[kWarps];
-  constexpr int B = kWalkBatch / kThreads;         // elements per thread
+// Walk sum k over its tiles [tb, te), as the headers appear.  Whole CTA; the
+// serial part runs on warp 0.  The dynamic shared memory of a walking CTA
+// (it never copies tiles) holds:
+//   [0, 32K)       tile headers of the batch, later the segment composites
+//   [32K, 64K)     the batch's flat list of elements (headers and items)
+//   [64K, 68K)     per element: tile offset in the batch << 12 | first term
+//   [68K, 69K)     per element: segment head flag
+//   [69K, 73K)     segment ends
+__device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *dyn, int k, int64_t tb, int64_t te,
+                         int64_t ntiles) {
+  Rec *hdrs = reinterpret_cast<Rec *>(dyn);
+  Rec *comp = hdrs;
+  Rec *el = reinterpret_cast<Rec *>(dyn + kWalkOffEl);
+  uint32_t *elpos = reinterpret_cast<uint32_t *>(dyn + kWalkOffPos);
+  unsigned char *head = dyn + kWalkOffHead;
+  int *ends = reinterpret_cast<int *>(dyn + kWalkOffEnds);
+  unsigned long long *st = sm.st;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t tb = g0.first_tile, te = g0.first_tile + g0.ntiles_sum;
-  const double s0 = p.s0s ? p.s0s[g0.sum] : p.s0;
-  if (tid == 0) s_S = dbits(s0);
-  int64_t base = tb;
+  const uint32_t tag = (p.epoch << 1) | 1u;
+  constexpr int B = kWalkElems / kThreads;          // elements per thread in the scan
+  constexpr int BT = kWalkTiles / kThreads;         // tiles per thread
+  const double s0 = p.s0s ? p.s0s[k] : p.s0;
+  if (tid == 0) sm.S = dbits(s0);
+  int64_t pos = tb;
   __syncthreads();
-  while (base < te) {
-    const int cnt = (int)min((int64_t)kWalkBatch, te - base);
-    for (int i = tid; i < cnt; i += kThreads) srec[i] = ldcg_rec(p.tile_rec + base + i);
-    __syncthreads();
-    for (int i = tid; i < cnt; i += kThreads) {
-      const int k = seg_key(srec[i]);
-      s_head[i] = (i == 0 || k == kComplexKey || seg_key(srec[i - 1]) != k) ? 1 : 0;
-    }
-    __syncthreads();
-    // --- per-thread segmented inclusive scan over B consecutive elements
-    Run agg = run_empty();
-    bool has_head = false;
-    int first_head = B;
-    for (int j = 0; j < B; j++) {
-      const int i = tid * B + j;
-      if (i >= cnt) break;
-      const Rec q = srec[i];
-      const bool head = s_head[i] != 0;
-      const Run r = rec_run(q);
-      if (head) { agg = r; if (!has_head) first_head = j; has_head = true; }
-      else agg = run_compose(agg, r);
-      srec[i] = make_rec(agg, q.e, rec_kind(q.meta), 0);
-    }
-    // --- block-level segmented scan of the thread aggregates
-    Run v = agg;
-    int f = has_head ? 1 : 0;
-    for (int off = 1; off < 32; off <<= 1) {
-      const Run o = shfl_run<SH_UP>(v, off);
-      const int of = __shfl_up_sync(0xffffffffu, f, off);
-      if (lane >= off) { if (!f) v = run_compose(o, v); f |= of; }
-    }
-    if (lane == 31) { s_wagg[warp] = v; s_wflag[warp] = f; }
-    __syncthreads();
-    Run ex = run_empty();                             // exclusive prefix of this thread
-    for (int w = 0; w < warp; w++) {
-      if (s_wflag[w]) ex = s_wagg[w];
-      else ex = run_compose(ex, s_wagg[w]);
-    }
-    {
-      const Run lv = shfl_run<SH_UP>(v, 1);
-      const int lf = __shfl_up_sync(0xffffffffu, f, 1);
-      if (lane >= 1) {
-        if (lf) ex = lv; else ex = run_compose(ex, lv);
+  while (pos < te) {
+    // ---- 1. the contiguous ready prefix [pos, pos + m)
+    const int want = (int)min((int64_t)kWalkTiles, te - pos);
+    const uint64_t t0 = globaltimer();
+    while (true) {
+      if (tid == 0) sm.m = want;
+      __syncthreads();
+      for (int i = tid; i < want; i += kThreads) {
+        Rec h;
+        if (read_header(p.hdr + pos + i, tag, h)) hdrs[i] = h;
+        else atomicMin(&sm.m, i);
       }
+      __syncthreads();
+      if (sm.m > 0) break;
+      if (globaltimer() - t0 > kWaitNs) {
+        if (tid == 0) { atomicOr(&p.ctr[C_ERR], ERR_WALK_TIMEOUT); p.outs[k] = __longlong_as_double(0x7FF8000000000000ll); }
+        __syncthreads();
+        return;
+      }
+      __nanosleep(200);
     }
-    for (int j = 0; j < first_head; j++) {            // elements before the first head
-      const int i = tid * B + j;
-      if (i >= cnt) break;
-      const Rec q = srec[i];
-      srec[i] = make_rec(run_compose(ex, rec_run(q)), q.e, rec_kind(q.meta), 0);
+    int m = sm.m;
+    __threadfence();
+    if (tid == 0) atomicAdd(&st[S_WALK_BATCHES], 1ull);
+    // ---- 2. elements per tile and their prefix; the batch is cut where the
+    //         flat list would overflow, then the prefix is taken again
+    int cnt[BT];
+    int mine = 0, wbase = 0, incl = 0;
+    for (int pass = 0; pass < 2; pass++) {
+      mine = 0;
+#pragma unroll
+      for (int q = 0; q < BT; q++) {
+        const int i = tid * BT + q;
+        int c = 0;
+        if (i < m) {
+          const Rec &h = hdrs[i];
+          if (rec_kind(h.meta) == K_COMPLEX) {
+            const uint64_t packed = (uint64_t)h.inc;
+            for (int cc = 0; cc < kWarps; cc++) c += (int)((packed >> (8 * cc)) & 0xFF);
+          } else {
+            c = 1;
+          }
+        }
+        cnt[q] = c;
+        mine += c;
+      }
+      incl = mine;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      __syncthreads();
+      if (lane == 31) sm.wcnt[warp] = incl;
+      __syncthreads();
+      wbase = 0;
+      for (int w = 0; w < warp; w++) wbase += sm.wcnt[w];
+      if (pass == 1) break;
+      int off = wbase + incl - mine;
+#pragma unroll
+      for (int q = 0; q < BT; q++) {
+        const int i = tid * BT + q;
+        if (i < m && off + cnt[q] > kWalkElems) atomicMin(&sm.m, i);
+        off += cnt[q];
+      }
+      __syncthreads();
+      m = sm.m;
+    }
+    // ---- 3. the flat element list
+    {
+      int off = wbase + incl - mine;
+#pragma unroll
+      for (int q = 0; q < BT; q++) {
+        const int i = tid * BT + q;
+        if (i >= m) break;
+        const Rec h = hdrs[i];
+        if (rec_kind(h.meta) != K_COMPLEX) {
+          el[off] = h;
+          elpos[off] = (uint32_t)i << 12;
+        } else {
+          const uint64_t packed = (uint64_t)h.inc;
+          const Rec *src = p.items + (pos + i) * kTileSlots;
+          int o2 = off;
+          for (int cc = 0; cc < kWarps; cc++) {
+            const int n = (int)((packed >> (8 * cc)) & 0xFF);
+            for (int u = 0; u < n; u++) {
+              const Rec it = ldcg_rec(src + cc * kChunkSlots + u);
+              el[o2] = it;
+              elpos[o2] = ((uint32_t)i << 12) | rec_tstart(it.meta);
+              o2++;
+            }
+          }
+        }
+        off += cnt[q];
+      }
+      if (tid == kThreads - 1) sm.nel = wbase + incl;
     }
     __syncthreads();
-    // --- segment ends, compacted in order
-    {
+    const int nel = min(sm.nel, kWalkElems);
+    // ---- 4. segmented scan and serial application (restarted after a rejected run)
+    int from = 0;
+    while (from < nel) {
+      for (int i = from + tid; i < nel; i += kThreads) {
+        const Rec q = el[i];
+        bool hd = (i == from) || elem_alone(q);
+        if (!hd) {
+          const Rec pq = el[i - 1];
+          hd = elem_alone(pq) || elem_key(pq) != elem_key(q);
+        }
+        head[i] = hd ? 1 : 0;
+      }
+      __syncthreads();
+      Run agg = run_empty();
+      bool has_head = false;
+      int first_head = B;
+      Run incls[B];
+#pragma unroll
+      for (int jj = 0; jj < B; jj++) {
+        const int i = tid * B + jj;
+        incls[jj] = run_empty();
+        if (i < from || i >= nel) continue;
+        const Run r = rec_run(el[i]);
+        if (head[i]) { agg = r; if (!has_head) first_head = jj; has_head = true; }
+        else agg = run_compose(agg, r);
+        incls[jj] = agg;
+      }
+      Run v = agg;
+      int f = has_head ? 1 : 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        const Run ov = shfl_run<SH_UP>(v, o);
+        const int of = __shfl_up_sync(0xffffffffu, f, o);
+        if (lane >= o) { if (!f) v = run_compose(ov, v); f |= of; }
+      }
+      if (lane == 31) { sm.wagg[warp] = v; sm.wflag[warp] = f; }
+      __syncthreads();
+      Run ex = run_empty();
+      for (int w = 0; w < warp; w++) {
+        if (sm.wflag[w]) ex = sm.wagg[w];
+        else ex = run_compose(ex, sm.wagg[w]);
+      }
+      {
+        const Run lv = shfl_run<SH_UP>(v, 1);
+        const int lf = __shfl_up_sync(0xffffffffu, f, 1);
+        if (lane >= 1) { if (lf) ex = lv; else ex = run_compose(ex, lv); }
+      }
+#pragma unroll
+      for (int jj = 0; jj < B; jj++)
+        if (jj < first_head) incls[jj] = run_compose(ex, incls[jj]);
+      // segment ends, compacted in order, with their composites
       int my = 0;
       int idx[B];
-      for (int j = 0; j < B; j++) {
-        const int i = tid * B + j;
-        if (i < cnt && (i == cnt - 1 || s_head[i + 1])) idx[my++] = i;
+#pragma unroll
+      for (int jj = 0; jj < B; jj++) {
+        const int i = tid * B + jj;
+        if (i >= from && i < nel && (i == nel - 1 || head[i + 1])) idx[my++] = jj;
       }
-      int incl = my;
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
+      int inc2 = my;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int vv = __shfl_up_sync(0xffffffffu, inc2, o);
+        if (lane >= o) inc2 += vv;
       }
-      if (lane == 31) s_wcnt[warp] = incl;
+      if (lane == 31) sm.wcnt[warp] = inc2;
       __syncthreads();
-      int wbase = 0;
-      for (int w = 0; w < warp; w++) wbase += s_wcnt[w];
-      const int pos = wbase + incl - my;
-      for (int j = 0; j < my; j++) s_ends[pos + j] = idx[j];
-      if (tid == kThreads - 1) s_nends = wbase + incl;
-    }
-    __syncthreads();
-    // --- the serial part: warp 0 applies segment after segment
-    if (warp == 0) {
-      uint64_t Sb = s_S;
-      int restart = -1;
-      int segstart = 0;
-      const int ne = s_nends;
-      for (int sidx = 0; sidx < ne; sidx++) {
-        const int e_i = s_ends[sidx];
-        const Rec comp = srec[e_i];
-        if (lane == 0) atomicAdd(&st[S_WALK_SEGMENTS], 1ull);
-        bool ok = false;
-        if (rec_kind(comp.meta) == K_RUN) {
-          if (nonfinite(Sb)) { Sb = absorb(Sb, rec_flags(comp.meta)); ok = true; }
-          else {
-            uint64_t T = Sb;
-            if (run_apply(T, rec_run(comp), comp.e) == APPLY_OK) { Sb = T; ok = true; }
-          }
-        }
-        if (!ok) {
-          if (lane == 0) atomicAdd(&st[rec_kind(comp.meta) == K_RUN ? S_RUN_REJECTED : S_TILE_COMPLEX], 1ull);
-          // the first prefix of the segment the check rejects (in parallel)
-          int kfail = e_i;
-          for (int c0 = segstart; c0 <= e_i; c0 += 32) {
-            const int i = c0 + lane;
-            bool bad = false;
-            if (i <= e_i) {
-              const Rec q = srec[i];
-              if (rec_kind(q.meta) != K_RUN || nonfinite(Sb)) bad = true;
-              else { uint64_t T = Sb; bad = run_apply(T, rec_run(q), q.e) != APPLY_OK; }
-            }
-            const uint32_t bm = __ballot_sync(0xffffffffu, bad);
-            if (bm) { kfail = c0 + __ffs(bm) - 1; break; }
-          }
-          if (kfail > segstart) {                      // the prefix before it passed
-            const Rec q = srec[kfail - 1];
-            uint64_t T = Sb;
-            if (run_apply(T, rec_run(q), q.e) == APPLY_OK) Sb = T;
-          }
-          const int64_t t = base + kfail;
-          Sb = walk_tile(p, Sb, t, tile_geo(p, t, te), st);
-          if (kfail < e_i) { restart = kfail + 1; break; }
-        }
-        segstart = e_i + 1;
+      int eb2 = 0;
+      for (int w = 0; w < warp; w++) eb2 += sm.wcnt[w];
+      const int epos = eb2 + inc2 - my;
+#pragma unroll
+      for (int jj = 0; jj < B; jj++) {
+        if (jj >= my) break;
+        const int i = tid * B + idx[jj];
+        const Rec q = el[i];
+        ends[epos + jj] = i;
+        comp[epos + jj] = make_rec(incls[idx[jj]], q.e, rec_kind(q.meta), q.count, rec_tstart(q.meta));
       }
-      if (lane == 0) { s_S = Sb; s_restart = restart; }
+      if (tid == kThreads - 1) sm.nseg = epos + my;
+      __syncthreads();
+      // ---- serial part on warp 0
+      if (warp == 0) {
+        uint64_t Sb = sm.S;
+        int restart = -1;
+        int segstart = from;
+        const int ns = sm.nseg;
+        for (int sidx = 0; sidx < ns; sidx++) {
+          const int ei = ends[sidx];
+          const Rec c = comp[sidx];
+          const uint32_t kind = rec_kind(c.meta);
+          if (lane == 0) atomicAdd(&st[S_WALK_SEGMENTS], 1ull);
+          if (nonfinite(Sb)) {
+            Sb = absorb(Sb, rec_flags(c.meta));
+            segstart = ei + 1;
+            continue;
+          }
+          if (kind == K_TERMS) {
+            const Rec q = el[ei];
+            double S = bitsd(Sb);
+            const int nt = (int)q.count;
+            if (nt > 0) S = __dadd_rn(S, bitsd((uint64_t)q.inc));
+            if (nt > 1) S = __dadd_rn(S, bitsd((uint64_t)q.lo));
+            if (nt > 2) S = __dadd_rn(S, bitsd((uint64_t)q.hi));
+            Sb = dbits(S);
+            if (lane == 0) atomicAdd(&st[S_TERMS_ADDED], (unsigned long long)nt);
+            segstart = ei + 1;
+            continue;
+          }
+          if (kind == K_FALLBACK) {
+            const uint32_t ep = elpos[ei];
+            const TileGeo g = tile_geo(p, pos + (ep >> 12), ntiles);
+            Sb = add_terms(p, Sb, g.start + (ep & 0xFFF), c.count, st);
+            if (lane == 0) atomicAdd(&st[S_CHUNK_FALLBACK], 1ull);
+            segstart = ei + 1;
+            continue;
+          }
+          {
+            uint64_t T = Sb;
+            if (run_apply(T, rec_run(c), c.e) == APPLY_OK) { Sb = T; segstart = ei + 1; continue; }
+          }
+          if (lane == 0) atomicAdd(&st[S_RUN_REJECTED], 1ull);
+          // the first element of the segment whose prefix composite the
+          // check rejects: the warp composes 32 prefixes at a time
+          int kfail = ei;
+          uint64_t Sok = Sb;
+          Run acc = run_empty();
+          for (int c0 = segstart; c0 <= ei; c0 += 32) {
+            const int i = c0 + lane;
+            Run r = (i <= ei) ? rec_run(el[i]) : run_empty();
+            for (int o = 1; o < 32; o <<= 1) {
+              const Run ov = shfl_run<SH_UP>(r, o);
+              if (lane >= o) r = run_compose(ov, r);
+            }
+            const Run pre = run_compose(acc, r);
+            bool bad = false;
+            if (i <= ei) { uint64_t T = Sb; bad = run_apply(T, pre, c.e) != APPLY_OK; }
+            const uint32_t bm = __ballot_sync(0xffffffffu, bad);
+            if (bm) {
+              kfail = c0 + __ffs(bm) - 1;
+              const int src = kfail - 1 - c0;
+              Run before = shfl_run<SH_IDX>(pre, src < 0 ? 0 : src);
+              if (src < 0) before = acc;
+              if (kfail > segstart) {
+                uint64_t T2 = Sb;
+                if (run_apply(T2, before, c.e) == APPLY_OK) Sok = T2;
+              }
+              break;
+            }
+            acc = shfl_run<SH_IDX>(pre, 31);
+          }
+          Sb = Sok;
+          {
+            const uint32_t ep = elpos[kfail];
+            const TileGeo g = tile_geo(p, pos + (ep >> 12), ntiles);
+            Sb = add_terms(p, Sb, g.start + (ep & 0xFFF), el[kfail].count, st);
+          }
+          if (kfail < ei) { restart = kfail + 1; break; }
+          segstart = ei + 1;
+        }
+        if (lane == 0) { sm.S = Sb; sm.restart = restart; }
+      }
+      __syncthreads();
+      const int rs = sm.restart;
+      __syncthreads();
+      if (rs < 0) break;
+      from = rs;
     }
-    __syncthreads();
-    base = (s_restart >= 0) ? base + s_restart : base + cnt;
+    pos += m;
+    if (pos >= te && tid == 0) p.stats[S_T_WALK0] = globaltimer();
     __syncthreads();
   }
   if (tid == 0) {
-    p.outs[g0.sum] = bitsd(s_S);
-    p.done[g0.sum] = 0;
+    p.outs[k] = bitsd(sm.S);
+    p.stats[S_T_WALK1] = globaltimer();
   }
   __syncthreads();
 }
 
 // ---------------------------------------------------------------- the kernel
 __global__ void __launch_bounds__(kThreads, 2)
-    seqsum_kernel(const Params p, const __grid_constant__ CUtensorMap tmap) {
+    seqsum_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmap) {
   extern __shared__ unsigned char dsm_raw[];
-  unsigned char *stage0 =
+  unsigned char *dyn =
       reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t s_bar[kStages];
-  __shared__ int64_t s_tk[kStages];
-  __shared__ int s_tma[kStages];
-  __shared__ float s_wsig[kWarps], s_wabs[kWarps];
-  __shared__ double s_ex_sig;
-  __shared__ float s_ex_abs;
-  __shared__ Rec s_chunk[kWarps];
-  __shared__ int64_t s_pend[2];          // tiles whose sums this CTA must walk
-  __shared__ int s_npend;
-  __shared__ unsigned long long s_st[S_COUNT];
-
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  __shared__ Smem sm;
+  const int tid = threadIdx.x;
   int64_t ntiles = (p.ntiles >= 0) ? p.ntiles : (int64_t)__ldcg(&p.ctr[C_NTILES]);
-  if (ntiles > p.cap_tiles) ntiles = 0;                  // set-up flagged ERR_CAPACITY
-  unsigned long long *st = s_st;
-  if (tid < S_COUNT) s_st[tid] = 0;
+  if (ntiles > p.cap_tiles) ntiles = 0;                  // the set-up flagged ERR_CAPACITY
+  if (tid < S_COUNT) sm.st[tid] = 0;
   if (tid == 0) {
-    for (int s = 0; s < kStages; s++) mbar_init(&s_bar[s], 1);
+    for (int s = 0; s < kStages; s++) mbar_init(&sm.bar[s], 1);
     fence_mbar_init();
-    s_npend = 0;
+    if (blockIdx.x == 0) p.stats[S_T_START] = globaltimer();
   }
-  if (p.offsets == nullptr && ntiles == 0 && blockIdx.x == 0 && tid == 0) p.outs[0] = p.s0;
   __syncthreads();
 
-  // thread 0: take the next ticket into stage s and start its copy
-  auto issue = [&](int s) {
-    const int64_t t = (int64_t)atomicAdd(&p.ctr[C_TICKET], 1u);
-    s_tk[s] = t;
-    s_tma[s] = 0;
-    if (t >= ntiles || p.tma_rows == 0) return;
-    const TileGeo g = tile_geo(p, t, ntiles);
-    if ((g.start & 15) != 0) return;
-    fence_proxy_async();
-    mbar_arrive_expect_tx(&s_bar[s], (uint32_t)kStageBytes);
-    tma_load_box(stage0 + s * kStageBytes, &tmap, &s_bar[s], 0, (int32_t)(g.start >> 4));
-    s_tma[s] = 1;
-  };
-  // the whole CTA: walk the sums this CTA finished (no ticket is held then)
-  auto flush_walks = [&]() {
-    const int np = s_npend;
-    for (int i = 0; i < np; i++) {
-      const TileGeo gw = tile_geo(p, s_pend[i], ntiles);
-      __threadfence();
-      walk_sum(p, gw, reinterpret_cast<Rec *>(stage0), st);
-    }
-    __syncthreads();
-    if (tid == 0) s_npend = 0;
-    __syncthreads();
-  };
-
-  if (tid == 0) issue(0);
-  __syncthreads();
-  uint32_t phase[kStages] = {0, 0};
-  int cur = 0;
-  while (true) {
-    const int64_t t = s_tk[cur];
-    if (t >= ntiles) { flush_walks(); break; }
-    const bool hold = s_npend > 0;          // walks pending: finish this tile, walk, then take more
-    __syncthreads();
-    if (tid == 0 && !hold) issue(cur ^ 1);
-    const TileGeo g = tile_geo(p, t, ntiles);
-    const int use_tma = s_tma[cur];
-
-    // ---- 1. the lane's 16 terms
-    uint64_t xs[kLaneTerms];
-    const int64_t lstart = g.start + (int64_t)w * kChunkTerms + (int64_t)lane * kLaneTerms;
-    const int nv = (int)max((int64_t)0, min((int64_t)kLaneTerms, g.end - lstart));
-    const int64_t row = (g.start >> 4) + w * 32 + lane;
-    if (use_tma) {
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(&s_bar[cur], phase[cur])) {
-        if (globaltimer() - t0 > kWaitNs) { atomicOr(&p.ctr[C_ERR], ERR_TMA_TIMEOUT); break; }
-      }
-      phase[cur] ^= 1u;
-    }
-    if (use_tma && row < p.tma_rows) {
-      const unsigned char *rp = stage0 + cur * kStageBytes + (w * 32 + lane) * 128;
-      const int sw = lane & 7;
-#pragma unroll
-      for (int c = 0; c < 8; c++) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(rp + ((c ^ sw) << 4));
-        xs[2 * c] = ((uint64_t)v.y << 32) | v.x;
-        xs[2 * c + 1] = ((uint64_t)v.w << 32) | v.z;
+  if ((int)blockIdx.x < p.nwalkers) {
+    // ---------------- walker CTA
+    if (p.offsets == nullptr) {
+      if (blockIdx.x == 0) {
+        if (ntiles == 0) { if (tid == 0) p.outs[0] = p.s0; }
+        else walk_sum(p, sm, dyn, 0, 0, ntiles, ntiles);
       }
     } else {
-      const unsigned long long *gp = reinterpret_cast<const unsigned long long *>(p.x) + lstart;
-#pragma unroll
-      for (int i = 0; i < kLaneTerms; i++) xs[i] = (i < nv) ? __ldg(gp + i) : 0ull;
+      while (true) {
+        if (tid == 0) sm.sum_k = (int)atomicAdd(&p.ctr[C_SUMTICKET], 1u);
+        __syncthreads();
+        const int k = sm.sum_k;
+        __syncthreads();
+        if (k >= p.nsums) break;
+        if (ntiles == 0) continue;                         // bad offsets or capacity: outputs already NaN
+        const int64_t tb = __ldcg(&p.tile_begin[k]), te = __ldcg(&p.tile_begin[k + 1]);
+        if (te > tb) walk_sum(p, sm, dyn, k, tb, te, ntiles);
+      }
     }
-#pragma unroll
-    for (int i = 0; i < kLaneTerms; i++)
-      if (i >= nv) xs[i] = 0ull;
-
-    // ---- 2. approximate sums for the plan
-    float sig = 0.0f, ab = 0.0f;
-    bool allzero = true;
-#pragma unroll
-    for (int i = 0; i < kLaneTerms; i++) {
-      const float f = approx_f32(xs[i]);
-      sig += f;
-      ab += fabsf(f);
-      allzero = allzero && ((xs[i] << 1) == 0);
-    }
-    float isig = sig, iab = ab;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float a = __shfl_up_sync(0xffffffffu, isig, o);
-      const float b = __shfl_up_sync(0xffffffffu, iab, o);
-      if (lane >= o) { isig += a; iab += b; }
-    }
-    const float xsig = isig - sig, xab = iab - ab;      // lane's exclusive prefix in the chunk
-    if (lane == 31) { s_wsig[w] = isig; s_wabs[w] = iab; }
-    __syncthreads();                                   // also: stage `cur` is free again
-
-    // ---- 3. the tile's approximate exclusive prefix (decoupled look-back)
-    if (w == 0) {
-      double agg = 0.0;
-      float agga = 0.0f;
-#pragma unroll
-      for (int k = 0; k < kWarps; k++) { agg += (double)s_wsig[k]; agga += s_wabs[k]; }
-      double exs;
-      float exa;
-      lookback(p, g, t, agg, agga, exs, exa, st);
-      if (lane == 0) { s_ex_sig = exs; s_ex_abs = exa; }
+  } else {
+    // ---------------- streaming CTA: copy of i+2 | plan of i+1 | runs of i
+    auto issue = [&](int s) {                            // thread 0
+      const int64_t t = (int64_t)atomicAdd(&p.ctr[C_TICKET], 1u);
+      sm.tk[s] = t;
+      sm.tma[s] = 0;
+      if (t >= ntiles || p.tma_rows == 0) return;
+      const TileGeo g = tile_geo(p, t, ntiles);
+      if ((g.start & 15) != 0) return;
+      fence_proxy_async();
+      mbar_arrive_expect_tx(&sm.bar[s], (uint32_t)kStageBytes);
+      tma_load_box(dyn + s * kStageBytes, &tmap, &sm.bar[s], 0, (int32_t)(g.start >> 4));
+      sm.tma[s] = 1;
+    };
+    uint32_t phases = 0;                                 // bit s: parity of stage s's barrier
+    auto wait_stage = [&](int s) {
+      if (sm.tma[s]) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(&sm.bar[s], (phases >> s) & 1u)) {
+          if (globaltimer() - t0 > kWaitNs) { atomicOr(&p.ctr[C_ERR], ERR_TMA_TIMEOUT); break; }
+        }
+        phases ^= 1u << s;
+      }
+    };
+    if (tid == 0) { issue(0); issue(1); }
+    __syncthreads();
+    if (sm.tk[0] < ntiles) {
+      wait_stage(0);
+      phase_a(p, sm, dyn, 0, sm.tk[0], ntiles);
     }
     __syncthreads();
-
-    // ---- 4. plan of this warp's chunk
-    double sc = s_ex_sig;
-    float ac = s_ex_abs;
-    for (int k = 0; k < w; k++) { sc += (double)s_wsig[k]; ac += s_wabs[k]; }
-    const float wsig = s_wsig[w], wabs = s_wabs[w];
-    const int64_t cstart = g.start + (int64_t)w * kChunkTerms;
-    const int cnt_chunk = (int)max((int64_t)0, min((int64_t)kChunkTerms, g.end - cstart));
-    int e_s = 0;
-    bool simple;
-    {
-      const double P = 0.5 * ((double)wabs + (double)wsig), N = 0.5 * ((double)wabs - (double)wsig);
-      const double delta = kEps * ((double)ac + (double)wabs) + kTiny;
-      simple = one_binade(sc - N - delta, sc + P + delta, e_s);
-      simple = plan_override(p.plan_mode, simple, e_s, (uint64_t)t, w, 0);
+    for (int i = 0;; i++) {
+      const int s = i % kStages, s1 = (i + 1) % kStages, s2 = (i + 2) % kStages;
+      const int64_t t = sm.tk[s];
+      if (t >= ntiles) break;
+      const int64_t t1 = sm.tk[s1];
+      __syncthreads();
+      if (tid == 0) {
+        if (t1 < ntiles) issue(s2);
+        else { sm.tk[s2] = ntiles; sm.tma[s2] = 0; }
+      }
+      if (t1 < ntiles) {
+        wait_stage(s1);
+        phase_a(p, sm, dyn + s1 * kStageBytes, s1, t1, ntiles);
+      }
+      __syncthreads();
+      phase_b(p, sm, dyn + s * kStageBytes, s, t, ntiles);
+      __syncthreads();
     }
-    int e_l = e_s;
-    bool clean_l = simple;
-    const bool zl = allzero;                            // lane of zeros (or no terms): exact anywhere
-    if (!simple) {
-      const double A = sc + (double)xsig;
-      const double P = 0.5 * ((double)ab + (double)sig), N = 0.5 * ((double)ab - (double)sig);
-      const double delta = kEps * ((double)ac + (double)xab + (double)ab) + kTiny;
-      clean_l = one_binade(A - N - delta, A + P + delta, e_l);
-      clean_l = plan_override(p.plan_mode, clean_l, e_l, (uint64_t)t, w, lane + 1);
-      const uint32_t bad = __ballot_sync(0xffffffffu, !clean_l && !zl);
-      const uint32_t placed = __ballot_sync(0xffffffffu, clean_l && !zl);
-      if (bad == 0) {
-        if (placed == 0) { simple = true; e_s = 0; }   // all zeros
-        else {
-          const int e_ref = __shfl_sync(0xffffffffu, e_l, __ffs(placed) - 1);
-          if (__ballot_sync(0xffffffffu, zl || e_l == e_ref) == 0xffffffffu) { simple = true; e_s = e_ref; }
-        }
-      }
-    }
-
-    // ---- 5. increments and composition
-    Rec crec;
-    if (simple) {
-      Run r = run_empty();
-#pragma unroll
-      for (int i = 0; i < kLaneTerms; i++) {
-        if (i < nv) {
-          int64_t re;
-          int32_t d;
-          const bool poison = term_inc(xs[i], e_s, re, d);
-          run_push(r, re, d, term_flags(xs[i]) | (poison ? F_POISON : 0u));
-        }
-      }
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const Run o = shfl_run<SH_DOWN>(r, off);
-        if ((lane & (2 * off - 1)) == 0) r = run_compose(r, o);
-      }
-      crec = make_rec(r, (r.flags & F_ZERO) ? kZeroE : e_s, K_RUN, (uint32_t)cnt_chunk);
-      if (lane == 0) atomicAdd(&st[S_CHUNK_RUN], 1ull);
-    } else {
-      // mixed chunk: lanes placed in a binade become runs under their own
-      // binade, unplaced lanes are added term by term; neighbouring lanes of
-      // one kind and binade merge into one item.
-      const bool fb = !clean_l && !zl;
-      Run r = run_empty();
-      uint32_t hasf = 0;
-#pragma unroll
-      for (int i = 0; i < kLaneTerms; i++) {
-        if (i < nv) {
-          const uint32_t tf = term_flags(xs[i]);
-          hasf |= tf;
-          if (!fb) {
-            int64_t re;
-            int32_t d;
-            const bool poison = term_inc(xs[i], clean_l ? e_l : 0, re, d);
-            run_push(r, re, d, tf | (poison ? F_POISON : 0u));
-          }
-        }
-      }
-      hasf &= (F_HASINF_P | F_HASINF_N | F_HASNAN);
-      const int kind = fb ? 1 : 0;
-      const int ekey = fb ? 0 : (clean_l ? e_l : kZeroE);
-      if (lane == 0) atomicAdd(&st[S_CHUNK_LIST], 1ull);
-      if (fb) atomicAdd(&st[S_LANE_DIRTY], 1ull);
-      const bool empty_lane = (nv == 0);               // past the end: joins the previous segment
-      const int pkind = __shfl_up_sync(0xffffffffu, kind, 1);
-      const int pkey = __shfl_up_sync(0xffffffffu, ekey, 1);
-      const bool head = (lane == 0) || (!empty_lane && (pkind != kind || pkey != ekey));
-      Run v = r;                                        // segmented inclusive scan
-      int f = head ? 1 : 0;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const Run o = shfl_run<SH_UP>(v, off);
-        const int of = __shfl_up_sync(0xffffffffu, f, off);
-        if (lane >= off) { if (!f) v = run_compose(o, v); f |= of; }
-      }
-      const uint32_t heads = __ballot_sync(0xffffffffu, head);
-      const bool end = (lane == 31) || ((heads >> (lane + 1)) & 1u);
-      const uint32_t ends = __ballot_sync(0xffffffffu, end);
-      const int nit = __popc(ends);
-      const uint32_t le = heads & ((lane == 31) ? 0xffffffffu : ((2u << lane) - 1u));
-      const int hlane = 31 - __clz(le);
-      const int skind = __shfl_sync(0xffffffffu, kind, hlane);
-      const int skey = __shfl_sync(0xffffffffu, ekey, hlane);
-      const int tstart = hlane * kLaneTerms;
-      const int tend = min((lane + 1) * kLaneTerms, cnt_chunk);
-      uint32_t orf = hasf;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) orf |= __shfl_xor_sync(0xffffffffu, orf, o);
-      uint32_t pbase = 0;
-      if (lane == 0) pbase = atomicAdd(&p.ctr[C_POOL], (uint32_t)nit);
-      pbase = __shfl_sync(0xffffffffu, pbase, 0);
-      Run lr = run_empty();
-      lr.flags = orf;
-      if ((int64_t)pbase + nit <= p.pool_cap) {
-        if (end) {
-          const int idx = __popc(ends & lanemask_lt());
-          Run iv = v;
-          if (skind == 1) { iv = run_empty(); iv.flags = orf; }
-          const Rec it = make_rec(iv, skind == 1 ? 0 : skey, skind == 1 ? K_FALLBACK : K_RUN,
-                                  (uint32_t)max(0, tend - tstart));
-          stcg_rec(p.pool + pbase + idx, it);
-        }
-        lr.inc = (int64_t)pbase;
-        lr.lo = nit;
-        lr.hi = 0;
-        crec = make_rec(lr, 0, K_LIST, (uint32_t)cnt_chunk);
-        if (lane == 0) atomicAdd(&st[S_ITEMS], (unsigned long long)nit);
-      } else {
-        crec = make_rec(lr, 0, K_FALLBACK, (uint32_t)cnt_chunk);
-        if (lane == 0) atomicAdd(&st[S_POOL_OVERFLOW], 1ull);
-      }
-    }
-    if (lane == 0) {
-      s_chunk[w] = crec;
-      stcg_rec(p.chunk_rec + t * kWarps + w, crec);
-    }
-    __threadfence();
-    __syncthreads();
-
-    // ---- 6. the tile's record, and the sum's completion count
-    if (tid == 0) {
-      bool all_run = true;
-      int et = kZeroE;
-      for (int k = 0; k < kWarps; k++) {
-        const Rec &c = s_chunk[k];
-        if (rec_kind(c.meta) != K_RUN) { all_run = false; break; }
-        if (rec_flags(c.meta) & F_ZERO) continue;
-        if (et == kZeroE) et = c.e;
-        else if (c.e != et) { all_run = false; break; }
-      }
-      Rec tr;
-      if (all_run) {
-        Run acc = run_empty();
-        for (int k = 0; k < kWarps; k++) acc = run_compose(acc, rec_run(s_chunk[k]));
-        tr = make_rec(acc, (acc.flags & F_ZERO) ? kZeroE : et, K_RUN, 0);
-      } else {
-        uint32_t orf = 0;
-        for (int k = 0; k < kWarps; k++) orf |= rec_flags(s_chunk[k].meta);
-        Run z = run_empty();
-        z.flags = orf & (F_HASINF_P | F_HASINF_N | F_HASNAN);
-        tr = make_rec(z, 0, K_COMPLEX, 0);
-      }
-      stcg_rec(p.tile_rec + t, tr);
-      atomicAdd(&st[S_TILES], 1ull);
-      __threadfence();
-      const uint32_t prev = atomicAdd(&p.done[g.sum], 1u);
-      if (prev + 1 == (uint32_t)g.ntiles_sum) s_pend[s_npend++] = t;
-    }
-    __syncthreads();
-    if (hold) {                              // no ticket held: walk now, then take the next
-      flush_walks();
-      if (tid == 0) issue(cur ^ 1);
-    }
-    __syncthreads();
-    cur ^= 1;
   }
 
   // ---- statistics and the last CTA's reset of the shared counters
   __syncthreads();
-  if (tid < S_COUNT && s_st[tid]) atomicAdd(&p.stats[tid], s_st[tid]);
+  if (tid < S_T_START && sm.st[tid]) atomicAdd(&p.stats[tid], sm.st[tid]);
   if (tid == 0) {
     __threadfence();
     if (atomicAdd(&p.ctr[C_EXIT], 1u) + 1 == gridDim.x) {
       p.ctr[C_TICKET] = 0;
+      p.ctr[C_SUMTICKET] = 0;
       p.ctr[C_EXIT] = 0;
-      p.ctr[C_POOL] = 0;
       __threadfence();
     }
   }
 }
 
-// Batched set-up: tiles per sum, their prefix (tile_begin), the start value of
-// empty sums, and the per-sum tile counters.  Offsets out of order or outside
-// [0, x_len] (x_len = p.n) stop the call: every output becomes NaN.
+// Batched set-up: tiles per sum and their prefix (tile_begin), the start value
+// of empty sums.  Offsets out of order or outside [0, x_len] (x_len = p.n),
+// or more tiles than the workspace holds, stop the call: every output
+// becomes NaN and an error bit is set.
 __global__ void setup_kernel(const Params p) {
   __shared__ int64_t s_carry;
   __shared__ int64_t s_w[32];
@@ -904,7 +1268,6 @@ __global__ void setup_kernel(const Params p) {
       if (len < 0 || a < 0 || b > p.n) { s_bad = 1; len = 0; }
       nt = (len + kTileTerms - 1) / kTileTerms;
       if (len == 0) p.outs[k] = p.s0s[k];
-      p.done[k] = 0;
     }
     int64_t incl = nt;
     for (int o = 1; o < 32; o <<= 1) {

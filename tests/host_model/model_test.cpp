@@ -97,6 +97,45 @@ static void test_one_term(long count) {
   if (acc < chk / 2) { fprintf(stderr, "too few accepted\n"); g_fail++; }
 }
 
+// --------------------------------------------------------- fast increment
+// term_inc_fast (the kernels' common path) against term_inc on random terms
+// and binades with e >= -969 and |x| < 2^e, including ties and zeros.
+static void test_fast_increment(long count) {
+  long n = 0;
+  for (long i = 0; i < count; i++) {
+    const int e = (int)(rnd() % 1990) - 969;
+    double x;
+    const uint64_t c = rnd() % 8;
+    if (c == 0) x = 0.0;
+    else if (c == 1) x = dbl(rnd() % (1ull << 52));                                  // subnormal
+    else if (c == 2) x = ldexp((double)(rnd() % 4096) + 0.5, e - 52 - (int)(rnd() % 12));
+    else if (c == 3) x = mk(e - 1, rnd(), false);                                      // just below 2^e
+    else x = mk(e - 1 - (int)(rnd() % 80), rnd(), false);
+    if (!(fabs(x) < ldexp(1.0, e))) continue;
+    const uint64_t b = bits(x);
+    int64_t re; int32_t d;
+    if (term_inc(b, e, re, d)) continue;
+    uint64_t r; bool tie;
+    term_inc_fast((uint32_t)(b >> 32), (uint32_t)b, 64 - (e + 1023), r, tie);
+    // term_inc gives re = f + up + (tie ? f & 1 : 0) and d = tie ? (f odd ? -1 : 1) : 0
+    bool ok;
+    if (tie) ok = (d != 0) && ((int64_t)r + (d < 0 ? 1 : 0) == re || (int64_t)r == re);
+    else ok = (d == 0) && ((int64_t)r == re);
+    if (tie) ok = ok && (d != 0);
+    if (!tie && d != 0) ok = false;
+    // exact relation at a tie: f = r (rounded down), re = f + (f & 1)
+    if (tie) ok = (re == (int64_t)(r + (r & 1))) && (d == ((r & 1) ? -1 : 1));
+    n++;
+    if (!ok) {
+      if (g_fail < 10)
+        fprintf(stderr, "fast increment mismatch: x=%a e=%d r=%llu tie=%d re=%lld d=%d\n", x, e,
+                (unsigned long long)r, (int)tie, (long long)re, d);
+      g_fail++;
+    }
+  }
+  printf("fast increment: %ld checked\n", n);
+}
+
 // ------------------------------------------------------------- short runs
 // Runs of 1..12 terms, built term by term and also as two composed halves,
 // applied to S under its own binade and under a neighbouring one.
@@ -257,6 +296,7 @@ static void test_pipeline() {
 int main(int argc, char **argv) {
   long count = argc > 1 ? atol(argv[1]) : 2000000;
   test_one_term(count);
+  test_fast_increment(count);
   test_short_runs(count / 2);
   test_pipeline();
   printf("mutation=%d failures=%ld\n", kMutate, g_fail);

@@ -219,10 +219,17 @@ def plane_c4_sum(width, height, seed):
     return np.where(pick, a, b)
 
 
-def config(name: str, scale_div: int = 1) -> Workload:
+def config(name: str, scale_div: int = 1, height_mult: int = 1) -> Workload:
     """The five workloads. ``scale_div`` > 1 shrinks width and height (for
-    quick tests); the recipe is otherwise unchanged."""
+    quick tests); ``height_mult`` > 1 makes a single-sum plane that many times
+    taller (larger than L2, for profiling); the recipe is otherwise unchanged."""
     d = scale_div
+    if height_mult > 1 and name != "c4":
+        base = config(name, scale_div)
+        w, h = base.shape[0]
+        planes = {"c1": plane_c1, "c2": plane_c2, "c3": plane_c3, "c5": plane_c5}
+        big = planes[name](w, h * height_mult)
+        return _single(name, big, w, h * height_mult, base.recipe + f", {height_mult}x taller")
     if name == "c1":
         w, h = 576 // d, 324 // d
         return _single("c1", plane_c1(w, h), w, h,
