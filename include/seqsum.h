@@ -107,6 +107,9 @@ typedef struct {
   int64_t t_walk_ns;         /* latest call: duration of its (last) walk */
   int32_t device_status;     /* 0, or a negative SEQSUM_E* code */
   int32_t device_error_bits; /* raw device error bits */
+  int32_t check_site;        /* self-checking builds: first failed check (0: none) */
+  int32_t check_pad;
+  int64_t check_value;       /* self-checking builds: the value that failed it */
 } seqsum_stats;
 
 /* Waits for the stream of the most recent call, copies its workspace's
@@ -128,6 +131,10 @@ void seqsum_release_workspace(void);
  * by term, 5 = random neighbouring binades).  Research-1433, finding 5: the
  * plan cannot make the result wrong, only slower.  Returns the old mode. */
 int seqsum_debug_set_plan(int mode);
+
+/* Test hook: copies up to 64 diagnostic words that self-checking builds of
+ * the library record (zeros otherwise) and clears them. */
+int seqsum_debug_read(unsigned long long *out, int n);
 
 /* Library version string. */
 const char *seqsum_version(void);

@@ -32,7 +32,9 @@ class _Stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
         "tiles", "chunks_run", "chunks_list", "chunks_fallback", "lanes_dirty", "walk_segments",
         "runs_rejected", "terms_added", "items", "pool_overflow", "tiles_complex",
-        "lookback_steps", "t_stream_ns", "t_walk_ns")] + [("device_status", ctypes.c_int32), ("device_error_bits", ctypes.c_int32)]
+        "lookback_steps", "t_stream_ns", "t_walk_ns")] + [
+        ("device_status", ctypes.c_int32), ("device_error_bits", ctypes.c_int32),
+        ("check_site", ctypes.c_int32), ("check_pad", ctypes.c_int32), ("check_value", ctypes.c_int64)]
 
 
 def lib():
@@ -40,9 +42,10 @@ def lib():
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.LIB
+            checks = os.environ.get("SEQSUM_CHECKS", "") == "1"
+            path = _build.CHECK_LIB if checks else _build.LIB
             if not os.path.exists(path):
-                path = _build.build()
+                path = _build.build(checks=checks)
             L = ctypes.CDLL(path)
             vp, i64, i32, d = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_double
             L.seqsum_f64.argtypes = [vp, i64, d, vp, vp]
@@ -61,6 +64,8 @@ def lib():
             L.seqsum_release_workspace.restype = None
             L.seqsum_debug_set_plan.argtypes = [ctypes.c_int]
             L.seqsum_debug_set_plan.restype = ctypes.c_int
+            L.seqsum_debug_read.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), ctypes.c_int]
+            L.seqsum_debug_read.restype = ctypes.c_int
             L.seqsum_version.argtypes = []
             L.seqsum_version.restype = ctypes.c_char_p
             _lib = L
@@ -153,6 +158,13 @@ def get_stats() -> dict:
 def debug_set_plan(mode: int) -> int:
     """Force the plan of later calls (tests only); returns the old mode."""
     return lib().seqsum_debug_set_plan(int(mode))
+
+
+def debug_read(n: int = 64) -> list:
+    """Diagnostic words recorded by a self-checking build (tests only)."""
+    buf = (ctypes.c_ulonglong * n)()
+    _check(lib().seqsum_debug_read(buf, n))
+    return list(buf)
 
 
 def release_workspace():

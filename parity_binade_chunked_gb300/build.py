@@ -16,6 +16,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libseqsum.so")
+# self-checking variant (-DSEQSUM_CHECKS): bounds checks on every computed index
+CHECK_BUILD = os.path.join(BUILD, "check")
+CHECK_LIB = os.path.join(CHECK_BUILD, "libseqsum.so")
 SOURCES = ["seqsum_kernel.cu", "seqsum_api.cu"]
 HEADERS = ["binade_math.cuh", "seqsum_internal.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -38,15 +41,18 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, extra_flags=(), verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, extra_flags=(), verbose: bool = False, checks: bool = False) -> str:
+    bdir, lib = (CHECK_BUILD, CHECK_LIB) if checks else (BUILD, LIB)
+    if checks:
+        extra_flags = tuple(extra_flags) + ("-DSEQSUM_CHECKS",)
+    os.makedirs(bdir, exist_ok=True)
     inc = os.path.join(os.path.dirname(HERE), "include")
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(inc, "seqsum.h"), __file__]
     objs = []
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(bdir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + hdrs):
             cmd = [nvcc(), *NVCC_FLAGS, *extra_flags, "-I", inc, "-c", s, "-o", o + ".tmp"]
@@ -66,17 +72,18 @@ def build(force: bool = False, extra_flags=(), verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=len(jobs) or 1) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     v = "-v" in sys.argv
     extra = ["-Xptxas", "-v"] if "--ptxas" in sys.argv else []
-    print(build(force="--force" in sys.argv or bool(extra), extra_flags=extra, verbose=v or bool(extra)))
+    print(build(force="--force" in sys.argv or bool(extra), extra_flags=extra, verbose=v or bool(extra),
+                checks="--checks" in sys.argv))

@@ -29,6 +29,7 @@ struct Workspace {
   uint32_t *ctr = nullptr;
   int64_t *tile_begin = nullptr;
   unsigned long long *stats = nullptr;
+  unsigned long long *dbg = nullptr;
   uint32_t epoch = 0;
   int64_t *h_pin = nullptr;          // pinned bounce for the batched size read-back
   // tensor map cache
@@ -76,6 +77,8 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
     if ((e = cudaMalloc(&w->stats, sq::S_COUNT * sizeof(unsigned long long))) != cudaSuccess)
       return cuda_fail(e);
     if ((e = cudaMallocHost(&w->h_pin, 2 * sizeof(int64_t))) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMalloc(&w->dbg, 64 * sizeof(unsigned long long))) != cudaSuccess) return cuda_fail(e);
+    cudaMemset(w->dbg, 0, 64 * sizeof(unsigned long long));
     cudaMemset(w->ctr, 0, sq::C_COUNT * sizeof(uint32_t));
     cudaMemset(w->stats, 0, sq::S_COUNT * sizeof(unsigned long long));
   }
@@ -161,6 +164,7 @@ void fill_ws(Params &p, Workspace *w) {
   p.tile_begin = w->tile_begin;
   p.cap_tiles = w->cap_tiles;
   p.stats = w->stats;
+  p.dbg = w->dbg;
 }
 
 int batched_impl(const double *x, int64_t x_len, const int64_t *offsets, int32_t nsums, const double *s0s,
@@ -279,6 +283,9 @@ int seqsum_get_stats(seqsum_stats *st) {
   if (e == cudaSuccess) e = cudaMemset(w->stats, 0, sizeof s);
   const uint32_t err = (e == cudaSuccess) ? c[sq::C_ERR] : 0u;
   if (e == cudaSuccess && err) e = cudaMemset(w->ctr + sq::C_ERR, 0, sizeof(uint32_t));
+  if (e == cudaSuccess && c[5]) e = cudaMemset(w->ctr + 5, 0, 3 * sizeof(uint32_t));
+  st->check_site = (int32_t)c[5];
+  st->check_value = (int64_t)(((uint64_t)c[7] << 32) | c[6]);
   cudaSetDevice(prev);
   if (e != cudaSuccess) return cuda_fail(e);
   st->tiles = (int64_t)s[sq::S_TILES];
@@ -298,7 +305,8 @@ int seqsum_get_stats(seqsum_stats *st) {
   st->device_error_bits = (int32_t)err;
   if (err & sq::ERR_CAPACITY) st->device_status = SEQSUM_ECAPACITY;
   else if (err & sq::ERR_BAD_OFFSETS) st->device_status = SEQSUM_EOFFSETS;
-  else if (err & sq::ERR_TMA_TIMEOUT) st->device_status = SEQSUM_ETIMEOUT;
+  else if (err & (sq::ERR_TMA_TIMEOUT | sq::ERR_WALK_TIMEOUT)) st->device_status = SEQSUM_ETIMEOUT;
+  else if (err & 32u) st->device_status = SEQSUM_EINVAL;
   else st->device_status = SEQSUM_OK;   // a plan timeout alone leaves results exact
   return SEQSUM_OK;
 }
@@ -336,6 +344,16 @@ void seqsum_release_workspace(void) {
   g_ws.clear();
   g_last = nullptr;
   cudaSetDevice(prev);
+}
+
+int seqsum_debug_read(unsigned long long *out, int n) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace *w = g_last;
+  if (!w || !out || n < 0 || n > 64) return SEQSUM_EINVAL;
+  cudaError_t e = cudaStreamSynchronize(w->stream);
+  if (e == cudaSuccess) e = cudaMemcpy(out, w->dbg, n * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(w->dbg, 0, 64 * sizeof(unsigned long long));
+  return e == cudaSuccess ? SEQSUM_OK : cuda_fail(e);
 }
 
 int seqsum_debug_set_plan(int mode) {

@@ -17,7 +17,7 @@ constexpr int kDynSmem = kStages * kStageBytes + 1024;   // + alignment slack
 constexpr int kChunkSlots = 16;                 // item slots per chunk in a tile's item area
 constexpr int kTileSlots = kWarps * kChunkSlots;
 constexpr int kWalkTiles = 1024;                // tile headers per walk batch (32 KB)
-constexpr int kWalkElems = 1536;                // flat elements per walk batch (48 KB)
+constexpr int kWalkElems = 1024;                // flat elements per walk batch (32 KB)
 constexpr int kMaxWalkers = 8;
 
 // ---- record kinds
@@ -99,6 +99,7 @@ struct Params {
   int64_t *tile_begin;         // batched: nsums + 1 entries
   int32_t nwalkers;            // CTAs 0 .. nwalkers-1 walk; the others stream
   int32_t pad2;
+  unsigned long long *dbg;     // self-checking builds: 64 diagnostic words
   int64_t cap_tiles;           // tiles the workspace holds
   unsigned long long *stats;   // S_COUNT counters
 };

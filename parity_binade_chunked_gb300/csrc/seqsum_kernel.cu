@@ -57,6 +57,13 @@ constexpr int kWalkOffEl = 32768;              // walker layout in the dynamic s
 constexpr int kWalkOffPos = 65536;
 constexpr int kWalkOffHead = 69632;
 constexpr int kWalkOffEnds = 70656;
+static_assert(kWalkTiles * (int)sizeof(Rec) <= kWalkOffEl, "walk headers overlap the element list");
+static_assert(kWalkElems * (int)sizeof(Rec) <= kWalkOffEl, "segment composites overlap the element list");
+static_assert(kWalkOffEl + kWalkElems * (int)sizeof(Rec) <= kWalkOffPos, "element list overlaps positions");
+static_assert(kWalkOffPos + kWalkElems * 4 <= kWalkOffHead, "positions overlap head flags");
+static_assert(kWalkOffHead + kWalkElems <= kWalkOffEnds, "head flags overlap segment ends");
+static_assert(kWalkOffEnds + kWalkElems * 4 <= kStages * kStageBytes, "walk buffers exceed the stages");
+static_assert(kWalkElems % kThreads == 0 && kWalkTiles % kThreads == 0, "walk batch split");
 
 // ---------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -107,6 +114,27 @@ __device__ __forceinline__ void st_vol_v2(void *p, uint64_t a, uint64_t b) {
 
 __device__ __forceinline__ uint64_t dbits(double v) { return (uint64_t)__double_as_longlong(v); }
 __device__ __forceinline__ double bitsd(uint64_t b) { return __longlong_as_double((long long)b); }
+
+// Self-checking build (-DSEQSUM_CHECKS): every computed global index and
+// every walker buffer index is checked before use; a failed check records
+// its site and value in the counters, sets ERR_CHECK and skips the access.
+#ifdef SEQSUM_CHECKS
+__device__ __forceinline__ bool sq_ok(const Params &p, bool cond, uint32_t site, int64_t val) {
+  if (!cond) {
+    if (atomicCAS(&p.ctr[5], 0u, site) == 0u) {
+      p.ctr[6] = (uint32_t)(uint64_t)val;
+      p.ctr[7] = (uint32_t)((uint64_t)val >> 32);
+    }
+    atomicOr(&p.ctr[C_ERR], 32u);
+  }
+  return cond;
+}
+#else
+#define sq_ok(p, cond, site, val) (true)
+#endif
+__device__ __forceinline__ bool item_ok(const Params &p, const Rec *q, uint32_t site) {
+  return sq_ok(p, q >= p.items && q < p.items + p.cap_tiles * kTileSlots, site, (int64_t)(q - p.items));
+}
 
 // ---------------------------------------------------------------- double-float
 // (hi + lo) pairs of fp32 for the plan's prefix; every op is one rounded fp32
@@ -369,8 +397,8 @@ __device__ __noinline__ Prefix lookback(const Params &p, int sum, int64_t first_
     for (int q = 0; q < 8 && !incl; q++) {
       const int64_t idx = j - 8 * lane - q;
       if (idx < first_tile) { incl = true; break; }            // a virtual prefix of 0
-      uint64_t A, B;
-      ld_vol_v2(p.status + 2 * idx, A, B);
+      uint64_t A = 0, B = 0;
+      if (sq_ok(p, idx >= 0 && idx < p.cap_tiles, 1, idx)) ld_vol_v2(p.status + 2 * idx, A, B);
       const uint32_t ta = (uint32_t)(A & 0xFF), tb = (uint32_t)B;
       if (((ta >> 1) != ep) || (ta != tb)) { ready = false; break; }
       sum = df_add(sum, DF{__uint_as_float((uint32_t)(A >> 32)), __uint_as_float((uint32_t)A & ~0xFFu)});
@@ -405,7 +433,8 @@ __device__ __noinline__ Prefix lookback(const Params &p, int sum, int64_t first_
     j -= 256;
   }
   if (gave_up && lane == 0) atomicOr(&p.ctr[C_ERR], ERR_PLAN_TIMEOUT);
-  if (lane == 0) publish_status(p.status + 2 * t, df_add(run, agg), run_abs + agg_abs, ep, 1);
+  if (lane == 0 && sq_ok(p, t >= 0 && t < p.cap_tiles, 2, t))
+    publish_status(p.status + 2 * t, df_add(run, agg), run_abs + agg_abs, ep, 1);
   return Prefix{run, run_abs};
 }
 
@@ -426,8 +455,9 @@ __device__ __forceinline__ void load_lane(const Params &p, const unsigned char *
       if (i >= nv) xs[i] = 0ull;
   } else {
     const unsigned long long *gp = reinterpret_cast<const unsigned long long *>(p.x) + lstart;
+    const bool ok = sq_ok(p, nv == 0 || (lstart >= 0 && lstart + nv <= p.n), 3, lstart);
 #pragma unroll
-    for (int i = 0; i < kLaneTerms; i++) xs[i] = (i < nv) ? __ldg(gp + i) : 0ull;
+    for (int i = 0; i < kLaneTerms; i++) xs[i] = (i < nv && ok) ? __ldg(gp + i) : 0ull;
   }
 }
 
@@ -473,7 +503,7 @@ __device__ __noinline__ int lane_items(const Params &p, const uint64_t *xs, int 
     // close the open item when this term does not extend it
     const bool extend = (i < nv) && ((kind == 1 && cur == 1 && cur_e == ei) || (kind == 2 && cur == 2 && nterms < 3));
     if (!extend && cur != 0) {
-      if (out) {
+      if (out && item_ok(p, out + n, 4)) {
         if (cur == 1) {
           stcg_rec(out + n, make_rec(rr, cur_e, K_RUN, (uint32_t)(i - cstart), tbase + (uint32_t)cstart));
         } else {
@@ -582,7 +612,7 @@ __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *st
   ioff -= myitems;
   if (total > kChunkSlots) return 0;
   Rec *out = area + w * kChunkSlots;
-  if (!dirty && myitems)
+  if (!dirty && myitems && item_ok(p, out + ioff, 5))
     stcg_rec(out + ioff, make_rec(v, hkey, K_RUN, (uint32_t)(csum - before_head),
                                   (uint32_t)(w * kChunkTerms + hlane * kLaneTerms)));
   if (dirty) lane_items(p, xs, nv, A, dbase, t, w, lane, out + ioff);
@@ -640,7 +670,8 @@ __device__ void phase_a(const Params &p, Smem &sm, const unsigned char *stage, i
     if (lane == 0) {
       sm.agg[s] = agg;
       sm.agg_abs[s] = agga;
-      if (g.tile_in_sum != 0) {
+      if (!sq_ok(p, t >= 0 && t < p.cap_tiles, 6, t)) {
+      } else if (g.tile_in_sum != 0) {
         publish_status(p.status + 2 * t, agg, agga, p.epoch, 0);
       } else {                                   // the first tile of a sum: s0 + its sum at once
         const DF ex = df_from_double(p.s0s ? p.s0s[g.sum] : p.s0);
@@ -680,6 +711,13 @@ __device__ void phase_b(const Params &p, Smem &sm, const unsigned char *stage, i
   }
   uint64_t xs[kLaneTerms];
   load_lane(p, stage, sm.tma[s] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, xs);
+#ifdef SEQSUM_CHECKS
+  if (t == 1100 && lane == 0) {
+    p.dbg[32 + w * 3] = (unsigned long long)__float_as_uint(sc.hi) | ((unsigned long long)__float_as_uint(sc.lo) << 32);
+    p.dbg[33 + w * 3] = (unsigned long long)(int64_t)e | ((unsigned long long)clean << 40);
+    p.dbg[34 + w * 3] = (unsigned long long)__float_as_uint(sm.ex.hi) | ((unsigned long long)__float_as_uint(me.sig) << 32);
+  }
+#endif
   Rec *area = p.items + t * kTileSlots;
   Rec crec;
   int nitems = 0;
@@ -759,7 +797,10 @@ __device__ void phase_b(const Params &p, Smem &sm, const unsigned char *stage, i
       Run fr = run_empty();
       fr.flags = ((me.mx >= 0x7FF00000u) ? (F_HASINF_P | F_HASINF_N | F_HASNAN) : 0u);
       crec = make_rec(fr, 0, K_FALLBACK, (uint32_t)cnt_chunk, (uint32_t)(w * kChunkTerms));
-      if (lane == 0) { stcg_rec(area + w * kChunkSlots, crec); atomicAdd(&st[S_POOL_OVERFLOW], 1ull); }
+      if (lane == 0) {
+        if (item_ok(p, area + w * kChunkSlots, 7)) stcg_rec(area + w * kChunkSlots, crec);
+        atomicAdd(&st[S_POOL_OVERFLOW], 1ull);
+      }
       nitems = 1;
     } else if (lane == 0) {
       atomicAdd(&st[S_CHUNK_LIST], 1ull);
@@ -796,7 +837,10 @@ __device__ void phase_b(const Params &p, Smem &sm, const unsigned char *stage, i
         const Rec &c = sm.chunk[k];
         int n = sm.nitems[k];
         if (rec_kind(c.meta) == K_RUN) {
-          if (c.count > 0) { stcg_rec(area + k * kChunkSlots, c); n = 1; }
+          if (c.count > 0) {
+            if (item_ok(p, area + k * kChunkSlots, 8)) stcg_rec(area + k * kChunkSlots, c);
+            n = 1;
+          }
           else n = 0;
         }
         orf |= rec_flags(c.meta);
@@ -810,7 +854,7 @@ __device__ void phase_b(const Params &p, Smem &sm, const unsigned char *stage, i
       atomicAdd(&st[S_TILE_COMPLEX], 1ull);
     }
     __threadfence();
-    publish_header(p.hdr + t, hd, (p.epoch << 1) | 1u);
+    if (sq_ok(p, t >= 0 && t < p.cap_tiles, 9, t)) publish_header(p.hdr + t, hd, (p.epoch << 1) | 1u);
     atomicAdd(&st[S_TILES], 1ull);
   }
 }
@@ -834,6 +878,7 @@ __device__ __forceinline__ uint64_t absorb(uint64_t Sb, uint32_t flags) {
 __device__ uint64_t add_terms(const Params &p, uint64_t Sb, int64_t a, int64_t cnt, unsigned long long *st) {
   const int lane = threadIdx.x & 31;
   double S = bitsd(Sb);
+  if (!sq_ok(p, a >= 0 && a + cnt <= p.n, 10, a)) cnt = 0;
   for (int64_t base = 0; base < cnt; base += 32) {
     const double v = (base + lane < cnt) ? __ldg(p.x + a + base + lane) : 0.0;
     const int m = (int)min((int64_t)32, cnt - base);
@@ -882,7 +927,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       __syncthreads();
       for (int i = tid; i < want; i += kThreads) {
         Rec h;
-        if (read_header(p.hdr + pos + i, tag, h)) hdrs[i] = h;
+        if (sq_ok(p, pos + i < p.cap_tiles, 11, pos + i) && read_header(p.hdr + pos + i, tag, h)) hdrs[i] = h;
         else atomicMin(&sm.m, i);
       }
       __syncthreads();
@@ -949,8 +994,10 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         if (i >= m) break;
         const Rec h = hdrs[i];
         if (rec_kind(h.meta) != K_COMPLEX) {
-          el[off] = h;
-          elpos[off] = (uint32_t)i << 12;
+          if (sq_ok(p, off >= 0 && off < kWalkElems, 12, off)) {
+            el[off] = h;
+            elpos[off] = (uint32_t)i << 12;
+          }
         } else {
           const uint64_t packed = (uint64_t)h.inc;
           const Rec *src = p.items + (pos + i) * kTileSlots;
@@ -958,9 +1005,12 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
           for (int cc = 0; cc < kWarps; cc++) {
             const int n = (int)((packed >> (8 * cc)) & 0xFF);
             for (int u = 0; u < n; u++) {
-              const Rec it = ldcg_rec(src + cc * kChunkSlots + u);
-              el[o2] = it;
-              elpos[o2] = ((uint32_t)i << 12) | rec_tstart(it.meta);
+              if (sq_ok(p, o2 >= 0 && o2 < kWalkElems && u < kChunkSlots, 13, ((int64_t)o2 << 32) | (u << 8) | cc) &&
+                  item_ok(p, src + cc * kChunkSlots + u, 14)) {
+                const Rec it = ldcg_rec(src + cc * kChunkSlots + u);
+                el[o2] = it;
+                elpos[o2] = ((uint32_t)i << 12) | rec_tstart(it.meta);
+              }
               o2++;
             }
           }
@@ -1043,6 +1093,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         if (jj >= my) break;
         const int i = tid * B + idx[jj];
         const Rec q = el[i];
+        if (!sq_ok(p, epos + jj < kWalkElems, 15, epos + jj)) break;
         ends[epos + jj] = i;
         comp[epos + jj] = make_rec(incls[idx[jj]], q.e, rec_kind(q.meta), q.count, rec_tstart(q.meta));
       }
@@ -1089,6 +1140,19 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
             if (run_apply(T, rec_run(c), c.e) == APPLY_OK) { Sb = T; segstart = ei + 1; continue; }
           }
           if (lane == 0) atomicAdd(&st[S_RUN_REJECTED], 1ull);
+#ifdef SEQSUM_CHECKS
+          if (lane == 0 && atomicCAS(&p.dbg[0], 0ull, 1ull) == 0ull) {
+            p.dbg[1] = (unsigned long long)pos; p.dbg[2] = (unsigned long long)ei;
+            p.dbg[3] = Sb; p.dbg[4] = (unsigned long long)(int64_t)c.e;
+            p.dbg[5] = (unsigned long long)c.inc; p.dbg[6] = (unsigned long long)c.lo;
+            p.dbg[7] = (unsigned long long)c.hi; p.dbg[8] = c.meta;
+            p.dbg[9] = elpos[ei]; p.dbg[10] = (unsigned long long)nel; p.dbg[11] = (unsigned long long)from;
+            p.dbg[12] = (unsigned long long)segstart; p.dbg[13] = (unsigned long long)sidx;
+            p.dbg[14] = (unsigned long long)ns; p.dbg[15] = el[segstart].count;
+            p.dbg[16] = (unsigned long long)(int64_t)el[segstart].e; p.dbg[17] = elpos[segstart];
+            p.dbg[18] = (unsigned long long)m;
+          }
+#endif
           // the first element of the segment whose prefix composite the
           // check rejects: the warp composes 32 prefixes at a time
           int kfail = ei;
