@@ -103,8 +103,16 @@ typedef struct {
   int64_t pool_overflow;     /* split chunks that found no room and fell back */
   int64_t tiles_complex;     /* tiles the walk descended into */
   int64_t lookback_steps;    /* look-back windows read by the plan */
-  int64_t t_stream_ns;       /* latest call: kernel start to the start of its (last) walk */
-  int64_t t_walk_ns;         /* latest call: duration of its (last) walk */
+  int64_t walk_batches;      /* batches of tile headers the walk took */
+  int64_t ns_tma_wait;       /* nanoseconds, summed over CTAs: waiting for tile copies */
+  int64_t ns_lookback;       /* ... in the plan's look-back */
+  int64_t ns_phase_a;        /* ... forming the plan's sums */
+  int64_t ns_phase_b;        /* ... forming runs (look-back included) */
+  int64_t ns_walk_wait;      /* ... the walk waiting for tile headers */
+  int64_t ns_walk_work;      /* ... the walk working */
+  int64_t t_stream_ns;       /* latest call: kernel start to the last tile header */
+  int64_t t_walk_tail_ns;    /* latest call: last tile header to the end of the walk */
+  int64_t t_total_ns;        /* latest call: kernel start to the end of the walk */
   int32_t device_status;     /* 0, or a negative SEQSUM_E* code */
   int32_t device_error_bits; /* raw device error bits */
   int32_t check_site;        /* self-checking builds: first failed check (0: none) */
@@ -132,8 +140,9 @@ void seqsum_release_workspace(void);
  * plan cannot make the result wrong, only slower.  Returns the old mode. */
 int seqsum_debug_set_plan(int mode);
 
-/* Test hook: copies up to 64 diagnostic words that self-checking builds of
- * the library record (zeros otherwise) and clears them. */
+/* Test hook: copies up to 16384 diagnostic words that self-checking builds
+ * of the library record (a trace of the walk; zeros otherwise) and clears
+ * them. */
 int seqsum_debug_read(unsigned long long *out, int n);
 
 /* Library version string. */

@@ -77,8 +77,8 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
     if ((e = cudaMalloc(&w->stats, sq::S_COUNT * sizeof(unsigned long long))) != cudaSuccess)
       return cuda_fail(e);
     if ((e = cudaMallocHost(&w->h_pin, 2 * sizeof(int64_t))) != cudaSuccess) return cuda_fail(e);
-    if ((e = cudaMalloc(&w->dbg, 64 * sizeof(unsigned long long))) != cudaSuccess) return cuda_fail(e);
-    cudaMemset(w->dbg, 0, 64 * sizeof(unsigned long long));
+    if ((e = cudaMalloc(&w->dbg, 16384 * sizeof(unsigned long long))) != cudaSuccess) return cuda_fail(e);
+    cudaMemset(w->dbg, 0, 16384 * sizeof(unsigned long long));
     cudaMemset(w->ctr, 0, sq::C_COUNT * sizeof(uint32_t));
     cudaMemset(w->stats, 0, sq::S_COUNT * sizeof(unsigned long long));
   }
@@ -300,8 +300,16 @@ int seqsum_get_stats(seqsum_stats *st) {
   st->pool_overflow = (int64_t)s[sq::S_POOL_OVERFLOW];
   st->tiles_complex = (int64_t)s[sq::S_TILE_COMPLEX];
   st->lookback_steps = (int64_t)s[sq::S_LOOKBACK_STEPS];
-  st->t_stream_ns = (int64_t)(s[sq::S_T_WALK0] - s[sq::S_T_START]);
-  st->t_walk_ns = (int64_t)(s[sq::S_T_WALK1] - s[sq::S_T_WALK0]);
+  st->walk_batches = (int64_t)s[sq::S_WALK_BATCHES];
+  st->ns_tma_wait = (int64_t)s[sq::S_NS_TMA_WAIT];
+  st->ns_lookback = (int64_t)s[sq::S_NS_LOOKBACK];
+  st->ns_phase_a = (int64_t)s[sq::S_NS_PHASE_A];
+  st->ns_phase_b = (int64_t)s[sq::S_NS_PHASE_B];
+  st->ns_walk_wait = (int64_t)s[sq::S_NS_WALK_WAIT];
+  st->ns_walk_work = (int64_t)s[sq::S_NS_WALK_WORK];
+  st->t_stream_ns = (int64_t)(s[sq::S_T_STREAM_END] - s[sq::S_T_START]);
+  st->t_walk_tail_ns = (int64_t)(s[sq::S_T_WALK1] - s[sq::S_T_STREAM_END]);
+  st->t_total_ns = (int64_t)(s[sq::S_T_WALK1] - s[sq::S_T_START]);
   st->device_error_bits = (int32_t)err;
   if (err & sq::ERR_CAPACITY) st->device_status = SEQSUM_ECAPACITY;
   else if (err & sq::ERR_BAD_OFFSETS) st->device_status = SEQSUM_EOFFSETS;
@@ -349,10 +357,10 @@ void seqsum_release_workspace(void) {
 int seqsum_debug_read(unsigned long long *out, int n) {
   std::lock_guard<std::mutex> lk(g_mu);
   Workspace *w = g_last;
-  if (!w || !out || n < 0 || n > 64) return SEQSUM_EINVAL;
+  if (!w || !out || n < 0 || n > 16384) return SEQSUM_EINVAL;
   cudaError_t e = cudaStreamSynchronize(w->stream);
   if (e == cudaSuccess) e = cudaMemcpy(out, w->dbg, n * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess) e = cudaMemset(w->dbg, 0, 64 * sizeof(unsigned long long));
+  if (e == cudaSuccess) e = cudaMemset(w->dbg, 0, 16384 * sizeof(unsigned long long));
   return e == cudaSuccess ? SEQSUM_OK : cuda_fail(e);
 }
 

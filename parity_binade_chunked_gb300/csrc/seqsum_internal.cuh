@@ -14,7 +14,7 @@ constexpr int kTileTerms = kWarps * kChunkTerms;// 4096 terms = 32 KB: one TMA b
 constexpr int kStages = 3;                      // copy of tile i+2 | plan of i+1 | runs of i
 constexpr int kStageBytes = kTileTerms * 8;
 constexpr int kDynSmem = kStages * kStageBytes + 1024;   // + alignment slack
-constexpr int kChunkSlots = 16;                 // item slots per chunk in a tile's item area
+constexpr int kChunkSlots = 32;                 // item slots per chunk in a tile's item area
 constexpr int kTileSlots = kWarps * kChunkSlots;
 constexpr int kWalkTiles = 1024;                // tile headers per walk batch (32 KB)
 constexpr int kWalkElems = 1024;                // flat elements per walk batch (32 KB)
@@ -68,13 +68,15 @@ enum : uint32_t {
 enum : int {
   S_TILES = 0, S_CHUNK_RUN, S_CHUNK_LIST, S_CHUNK_FALLBACK, S_LANE_DIRTY,
   S_WALK_SEGMENTS, S_RUN_REJECTED, S_TERMS_ADDED, S_ITEMS, S_POOL_OVERFLOW,
-  S_TILE_COMPLEX, S_LOOKBACK_STEPS,
-  S_WALK_BATCHES = 12,
-  // timestamps (globaltimer ns) of the latest call, plain stores:
-  S_T_START = 13,      // block 0 started
-  S_T_WALK0 = 14,      // the last tile header the walk needed became ready
-  S_T_WALK1 = 15,      // the walk ended
-  S_COUNT = 16
+  S_TILE_COMPLEX, S_LOOKBACK_STEPS, S_WALK_BATCHES,
+  // nanoseconds summed over CTAs (globaltimer)
+  S_NS_TMA_WAIT, S_NS_LOOKBACK, S_NS_PHASE_A, S_NS_PHASE_B, S_NS_WALK_WAIT, S_NS_WALK_WORK,
+  S_ACCUM_END,         // counters above are summed; below are timestamps of the latest call
+  S_T_START = 24,      // block 0 started
+  S_T_WALK0 = 25,      // the walk's last batch of headers was ready
+  S_T_WALK1 = 26,      // the walk ended
+  S_T_STREAM_END = 27, // the last tile header was published (max over CTAs)
+  S_COUNT = 32
 };
 
 // ---- kernel parameters

@@ -51,6 +51,7 @@ constexpr float kEps = 0x1p-18f;
 constexpr float kRelF32 = 0x1p-21f;            // rounding of one fp32 prefix value
 constexpr float kTinyF = 0x1p-120f;
 constexpr int kZeroE = -2000;                  // binade key of a run of zeros
+constexpr int kDirtyKey = -3000;               // merge key of a lane placed term by term
 constexpr uint64_t kWaitNs = 2000000000ull;    // bounded device waits: 2 s
 constexpr uint32_t kMagLo = 896u << 20;        // exponent 896 = 2^-127
 constexpr int kWalkOffEl = 32768;              // walker layout in the dynamic shared memory
@@ -389,20 +390,29 @@ __device__ __noinline__ Prefix lookback(const Params &p, int sum, int64_t first_
   bool gave_up = false;
   while (true) {
     if (lane == 0) atomicAdd(&st[S_LOOKBACK_STEPS], 1ull);
-    // this lane: tiles j - 8*lane - q, q = 0..7 (descending)
+    // this lane: tiles j - 8*lane - q, q = 0..7 (descending); the eight
+    // loads are issued together, then read in order
+    uint64_t A[8], B[8];
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+      const int64_t idx = j - 8 * lane - q;
+      A[q] = 0;
+      B[q] = 0;
+      if (idx >= first_tile && sq_ok(p, idx < p.cap_tiles, 1, idx)) ld_vol_v2(p.status + 2 * idx, A[q], B[q]);
+    }
     DF sum = DF{0.0f, 0.0f};
     float sab = 0.0f;
     bool incl = false;           // reached an inclusive status (or the sum's start)
     bool ready = true;           // every status up to there is present
-    for (int q = 0; q < 8 && !incl; q++) {
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+      if (incl || !ready) continue;
       const int64_t idx = j - 8 * lane - q;
-      if (idx < first_tile) { incl = true; break; }            // a virtual prefix of 0
-      uint64_t A = 0, B = 0;
-      if (sq_ok(p, idx >= 0 && idx < p.cap_tiles, 1, idx)) ld_vol_v2(p.status + 2 * idx, A, B);
-      const uint32_t ta = (uint32_t)(A & 0xFF), tb = (uint32_t)B;
-      if (((ta >> 1) != ep) || (ta != tb)) { ready = false; break; }
-      sum = df_add(sum, DF{__uint_as_float((uint32_t)(A >> 32)), __uint_as_float((uint32_t)A & ~0xFFu)});
-      sab += __uint_as_float((uint32_t)(B >> 32));
+      if (idx < first_tile) { incl = true; continue; }           // a virtual prefix of 0
+      const uint32_t ta = (uint32_t)(A[q] & 0xFF), tb = (uint32_t)B[q];
+      if (((ta >> 1) != ep) || (ta != tb)) { ready = false; continue; }
+      sum = df_add(sum, DF{__uint_as_float((uint32_t)(A[q] >> 32)), __uint_as_float((uint32_t)A[q] & ~0xFFu)});
+      sab += __uint_as_float((uint32_t)(B[q] >> 32));
       if (ta & 1u) incl = true;
     }
     const uint32_t rmask = __ballot_sync(0xffffffffu, ready);
@@ -574,12 +584,12 @@ __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *st
   const bool dirty = !clean && !zl && nv > 0;
   Run r = run_empty();
   if (!dirty) r = lane_run_general(xs, nv, clean ? e_l : 0);
-  const int key = dirty ? -1 : (clean ? e_l : kZeroE);
+  const int key = dirty ? kDirtyKey : (clean ? e_l : kZeroE);
   const int ndirty = dirty ? lane_items(p, xs, nv, A, dbase, t, w, lane, nullptr) : 0;
   if (dirty) atomicAdd(&st[S_LANE_DIRTY], 1ull);
   // merge neighbouring runs of one key (lanes past the end join the previous)
   const int pkey = __shfl_up_sync(0xffffffffu, key, 1);
-  const bool head = (lane == 0) || (nv > 0 && (dirty || pkey == -1 || key != pkey));
+  const bool head = (lane == 0) || (nv > 0 && (dirty || pkey == kDirtyKey || key != pkey));
   Run v = r;
   int fl = head ? 1 : 0;
 #pragma unroll
@@ -601,21 +611,52 @@ __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *st
     if (lane >= o) csum += vv;
   }
   const int before_head = __shfl_sync(0xffffffffu, csum - nv, hlane);
-  const int myitems = dirty ? ndirty : ((end && hkey != -1) ? 1 : 0);
-  int ioff = myitems;
+  // items per lane: a merged run at its end lane, or the dirty lane's own
+  // items; if they do not fit, each dirty lane becomes one fallback item
+  bool lane_fb = false;
+  int myitems = dirty ? ndirty : ((end && hkey != kDirtyKey) ? 1 : 0);
+  int ioff = 0, total = 0;
+  for (int attempt = 0; attempt < 2; attempt++) {
+    ioff = myitems;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int vv = __shfl_up_sync(0xffffffffu, ioff, o);
-    if (lane >= o) ioff += vv;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int vv = __shfl_up_sync(0xffffffffu, ioff, o);
+      if (lane >= o) ioff += vv;
+    }
+    total = __shfl_sync(0xffffffffu, ioff, 31);
+    ioff -= myitems;
+    if (total <= kChunkSlots) break;
+    lane_fb = true;
+    myitems = dirty ? 1 : ((end && hkey != kDirtyKey) ? 1 : 0);
   }
-  const int total = __shfl_sync(0xffffffffu, ioff, 31);
-  ioff -= myitems;
+#ifdef SEQSUM_CHECKS
+  if (t == 0 && w == 0) {
+    p.dbg[14000 + lane] = (unsigned long long)dirty | ((unsigned long long)clean << 1) | ((unsigned long long)zl << 2) |
+                          ((unsigned long long)head << 3) | ((unsigned long long)end << 4) |
+                          ((unsigned long long)lane_fb << 5) | ((unsigned long long)(hlane & 63) << 8) |
+                          ((unsigned long long)(myitems & 255) << 16) | ((unsigned long long)(ioff & 255) << 24) |
+                          ((unsigned long long)(total & 255) << 32) | ((unsigned long long)(ndirty & 255) << 40) |
+                          ((unsigned long long)(uint16_t)(int16_t)key << 48);
+    p.dbg[14040 + lane] = (unsigned long long)__float_as_uint(A) | ((unsigned long long)__float_as_uint(dl) << 32);
+    p.dbg[14080 + lane] = (unsigned long long)__float_as_uint(P) | ((unsigned long long)__float_as_uint(N) << 32);
+  }
+#endif
   if (total > kChunkSlots) return 0;
   Rec *out = area + w * kChunkSlots;
   if (!dirty && myitems && item_ok(p, out + ioff, 5))
     stcg_rec(out + ioff, make_rec(v, hkey, K_RUN, (uint32_t)(csum - before_head),
                                   (uint32_t)(w * kChunkTerms + hlane * kLaneTerms)));
-  if (dirty) lane_items(p, xs, nv, A, dbase, t, w, lane, out + ioff);
+  if (dirty && lane_fb) {
+    if (item_ok(p, out + ioff, 16)) {
+      Run fr = run_empty();
+      uint32_t tf = 0;
+      for (int i = 0; i < nv; i++) tf |= term_flags(xs[i]);
+      fr.flags = tf & (F_HASINF_P | F_HASINF_N | F_HASNAN);
+      stcg_rec(out + ioff, make_rec(fr, 0, K_FALLBACK, (uint32_t)nv, (uint32_t)(w * kChunkTerms + lane * kLaneTerms)));
+    }
+  } else if (dirty) {
+    lane_items(p, xs, nv, A, dbase, t, w, lane, out + ioff);
+  }
   return total;
 }
 
@@ -687,8 +728,9 @@ __device__ void phase_b(const Params &p, Smem &sm, const unsigned char *stage, i
   unsigned long long *st = sm.st;
   const TileGeo g = tile_geo(p, t, ntiles);
   if (w == 0) {
+    const uint64_t tl = globaltimer();
     const Prefix pr = lookback(p, g.sum, g.first_tile, t, sm.agg[s], sm.agg_abs[s], st);
-    if (lane == 0) { sm.ex = pr.ex; sm.ex_abs = pr.ex_abs; }
+    if (lane == 0) { sm.ex = pr.ex; sm.ex_abs = pr.ex_abs; atomicAdd(&st[S_NS_LOOKBACK], globaltimer() - tl); }
   }
   __syncthreads();
   // ---- plan of this warp's chunk
@@ -711,13 +753,6 @@ __device__ void phase_b(const Params &p, Smem &sm, const unsigned char *stage, i
   }
   uint64_t xs[kLaneTerms];
   load_lane(p, stage, sm.tma[s] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, xs);
-#ifdef SEQSUM_CHECKS
-  if (t == 1100 && lane == 0) {
-    p.dbg[32 + w * 3] = (unsigned long long)__float_as_uint(sc.hi) | ((unsigned long long)__float_as_uint(sc.lo) << 32);
-    p.dbg[33 + w * 3] = (unsigned long long)(int64_t)e | ((unsigned long long)clean << 40);
-    p.dbg[34 + w * 3] = (unsigned long long)__float_as_uint(sm.ex.hi) | ((unsigned long long)__float_as_uint(me.sig) << 32);
-  }
-#endif
   Rec *area = p.items + t * kTileSlots;
   Rec crec;
   int nitems = 0;
@@ -855,6 +890,7 @@ __device__ void phase_b(const Params &p, Smem &sm, const unsigned char *stage, i
     }
     __threadfence();
     if (sq_ok(p, t >= 0 && t < p.cap_tiles, 9, t)) publish_header(p.hdr + t, hd, (p.epoch << 1) | 1u);
+    atomicMax(&p.stats[S_T_STREAM_END], (unsigned long long)globaltimer());
     atomicAdd(&st[S_TILES], 1ull);
   }
 }
@@ -889,6 +925,24 @@ __device__ uint64_t add_terms(const Params &p, uint64_t Sb, int64_t a, int64_t c
 }
 
 __device__ __forceinline__ bool elem_alone(const Rec &q) { return rec_kind(q.meta) != K_RUN; }
+
+// Self-checking builds keep a trace of the walk: per serial step the term
+// range [a, b) it covered, what it was, and the running sum after it.
+constexpr int kDbgWords = 16384;
+#ifdef SEQSUM_CHECKS
+__device__ __forceinline__ void walk_trace(const Params &p, int64_t a, int64_t b, uint32_t what, uint64_t Sb) {
+  const unsigned long long r = atomicAdd(&p.dbg[0], 1ull);
+  if (1 + 4 * (r + 1) <= (unsigned long long)kDbgWords) {
+    p.dbg[1 + 4 * r] = (unsigned long long)a;
+    p.dbg[2 + 4 * r] = (unsigned long long)b;
+    p.dbg[3 + 4 * r] = what;
+    p.dbg[4 + 4 * r] = Sb;
+  }
+}
+#define WALK_TRACE(a, b, what, Sb) do { if (lane == 0) walk_trace(p, (a), (b), (what), (Sb)); } while (0)
+#else
+#define WALK_TRACE(a, b, what, Sb) do { } while (0)
+#endif
 __device__ __forceinline__ int elem_key(const Rec &q) {
   return (rec_flags(q.meta) & F_ZERO) ? kZeroE : (int)q.e;
 }
@@ -917,11 +971,13 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
   const double s0 = p.s0s ? p.s0s[k] : p.s0;
   if (tid == 0) sm.S = dbits(s0);
   int64_t pos = tb;
+  uint64_t t_work0 = 0;
   __syncthreads();
   while (pos < te) {
     // ---- 1. the contiguous ready prefix [pos, pos + m)
     const int want = (int)min((int64_t)kWalkTiles, te - pos);
     const uint64_t t0 = globaltimer();
+    if (tid == 0 && t_work0 != 0) atomicAdd(&st[S_NS_WALK_WORK], t0 - t_work0);
     while (true) {
       if (tid == 0) sm.m = want;
       __syncthreads();
@@ -941,7 +997,12 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
     }
     int m = sm.m;
     __threadfence();
-    if (tid == 0) atomicAdd(&st[S_WALK_BATCHES], 1ull);
+    if (tid == 0) {
+      atomicAdd(&st[S_WALK_BATCHES], 1ull);
+      t_work0 = globaltimer();
+      atomicAdd(&st[S_NS_WALK_WAIT], t_work0 - t0);
+      if (pos + m >= te) p.stats[S_T_WALK0] = t_work0;
+    }
     // ---- 2. elements per tile and their prefix; the batch is cut where the
     //         flat list would overflow, then the prefix is taken again
     int cnt[BT];
@@ -985,7 +1046,8 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       __syncthreads();
       m = sm.m;
     }
-    // ---- 3. the flat element list
+    // ---- 3. the flat element list: simple tiles by their thread; the items
+    //         of complex tiles by the whole block, one item per thread
     {
       int off = wbase + incl - mine;
 #pragma unroll
@@ -999,18 +1061,14 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
             elpos[off] = (uint32_t)i << 12;
           }
         } else {
+          // mark: elpos holds (tile << 12 | chunk << 8 | item) + a flag bit, filled below
           const uint64_t packed = (uint64_t)h.inc;
-          const Rec *src = p.items + (pos + i) * kTileSlots;
           int o2 = off;
           for (int cc = 0; cc < kWarps; cc++) {
             const int n = (int)((packed >> (8 * cc)) & 0xFF);
             for (int u = 0; u < n; u++) {
-              if (sq_ok(p, o2 >= 0 && o2 < kWalkElems && u < kChunkSlots, 13, ((int64_t)o2 << 32) | (u << 8) | cc) &&
-                  item_ok(p, src + cc * kChunkSlots + u, 14)) {
-                const Rec it = ldcg_rec(src + cc * kChunkSlots + u);
-                el[o2] = it;
-                elpos[o2] = ((uint32_t)i << 12) | rec_tstart(it.meta);
-              }
+              if (sq_ok(p, o2 >= 0 && o2 < kWalkElems && u < kChunkSlots, 13, ((int64_t)o2 << 32) | (u << 8) | cc))
+                elpos[o2] = 0x80000000u | ((uint32_t)i << 12) | ((uint32_t)cc << 8) | (uint32_t)u;
               o2++;
             }
           }
@@ -1020,6 +1078,31 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       if (tid == kThreads - 1) sm.nel = wbase + incl;
     }
     __syncthreads();
+    for (int j = tid; j < sm.nel && j < kWalkElems; j += kThreads) {
+      const uint32_t ep = elpos[j];
+      if (ep & 0x80000000u) {
+        const uint32_t i = (ep >> 12) & 0x7FFFFu, cc = (ep >> 8) & 0xFu, u = ep & 0xFFu;
+        const Rec *src = p.items + (pos + i) * kTileSlots + cc * kChunkSlots + u;
+        if (item_ok(p, src, 14)) {
+          const Rec it = ldcg_rec(src);
+          el[j] = it;
+          elpos[j] = (i << 12) | rec_tstart(it.meta);
+        }
+      }
+    }
+    __syncthreads();
+#ifdef SEQSUM_CHECKS
+    if (pos == tb) {
+      for (int j = tid; j < sm.nel && j < 4000; j += kThreads) {
+        const Rec q = el[j];
+        p.dbg[8192 + j] = (unsigned long long)rec_kind(q.meta) | ((unsigned long long)q.count << 8) |
+                          ((unsigned long long)rec_tstart(q.meta) << 24) | ((unsigned long long)elpos[j] << 36) |
+                          ((unsigned long long)(q.e & 0xFFF) << 52);
+      }
+      for (int i = tid; i < m && i < 64; i += kThreads) p.dbg[12800 + i] = (unsigned long long)hdrs[i].inc;
+      if (tid == 0) p.dbg[12799] = (unsigned long long)sm.nel;
+    }
+#endif
     const int nel = min(sm.nel, kWalkElems);
     // ---- 4. segmented scan and serial application (restarted after a rejected run)
     int from = 0;
@@ -1100,6 +1183,11 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       if (tid == kThreads - 1) sm.nseg = epos + my;
       __syncthreads();
       // ---- serial part on warp 0
+      auto abs_start = [&](int j) -> int64_t {
+        const uint32_t ep = elpos[j];
+        return tile_geo(p, pos + (ep >> 12), ntiles).start + (ep & 0xFFF);
+      };
+      (void)abs_start;
       if (warp == 0) {
         uint64_t Sb = sm.S;
         int restart = -1;
@@ -1112,6 +1200,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
           if (lane == 0) atomicAdd(&st[S_WALK_SEGMENTS], 1ull);
           if (nonfinite(Sb)) {
             Sb = absorb(Sb, rec_flags(c.meta));
+            WALK_TRACE(abs_start(segstart), abs_start(ei) + el[ei].count, 6u, Sb);
             segstart = ei + 1;
             continue;
           }
@@ -1124,6 +1213,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
             if (nt > 2) S = __dadd_rn(S, bitsd((uint64_t)q.hi));
             Sb = dbits(S);
             if (lane == 0) atomicAdd(&st[S_TERMS_ADDED], (unsigned long long)nt);
+            WALK_TRACE(abs_start(ei), abs_start(ei) + nt, 2u, Sb);
             segstart = ei + 1;
             continue;
           }
@@ -1132,32 +1222,27 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
             const TileGeo g = tile_geo(p, pos + (ep >> 12), ntiles);
             Sb = add_terms(p, Sb, g.start + (ep & 0xFFF), c.count, st);
             if (lane == 0) atomicAdd(&st[S_CHUNK_FALLBACK], 1ull);
+            WALK_TRACE(abs_start(ei), abs_start(ei) + c.count, 1u, Sb);
             segstart = ei + 1;
             continue;
           }
           {
             uint64_t T = Sb;
-            if (run_apply(T, rec_run(c), c.e) == APPLY_OK) { Sb = T; segstart = ei + 1; continue; }
+            if (run_apply(T, rec_run(c), c.e) == APPLY_OK) {
+              Sb = T;
+              WALK_TRACE(abs_start(segstart), abs_start(ei) + el[ei].count, 0u | ((uint32_t)(c.e & 0xFFFF) << 16), Sb);
+              segstart = ei + 1;
+              continue;
+            }
           }
           if (lane == 0) atomicAdd(&st[S_RUN_REJECTED], 1ull);
-#ifdef SEQSUM_CHECKS
-          if (lane == 0 && atomicCAS(&p.dbg[0], 0ull, 1ull) == 0ull) {
-            p.dbg[1] = (unsigned long long)pos; p.dbg[2] = (unsigned long long)ei;
-            p.dbg[3] = Sb; p.dbg[4] = (unsigned long long)(int64_t)c.e;
-            p.dbg[5] = (unsigned long long)c.inc; p.dbg[6] = (unsigned long long)c.lo;
-            p.dbg[7] = (unsigned long long)c.hi; p.dbg[8] = c.meta;
-            p.dbg[9] = elpos[ei]; p.dbg[10] = (unsigned long long)nel; p.dbg[11] = (unsigned long long)from;
-            p.dbg[12] = (unsigned long long)segstart; p.dbg[13] = (unsigned long long)sidx;
-            p.dbg[14] = (unsigned long long)ns; p.dbg[15] = el[segstart].count;
-            p.dbg[16] = (unsigned long long)(int64_t)el[segstart].e; p.dbg[17] = elpos[segstart];
-            p.dbg[18] = (unsigned long long)m;
-          }
-#endif
           // the first element of the segment whose prefix composite the
-          // check rejects: the warp composes 32 prefixes at a time
-          int kfail = ei;
-          uint64_t Sok = Sb;
-          Run acc = run_empty();
+          // check rejects: the warp composes 32 prefixes at a time.  The
+          // bounds of a composite depend on the shape of its tree, so this
+          // composition may accept what the scan's rejected: then the whole
+          // segment is applied as composed here.
+          int kfail = -1;
+          Run acc = run_empty(), before = run_empty();
           for (int c0 = segstart; c0 <= ei; c0 += 32) {
             const int i = c0 + lane;
             Run r = (i <= ei) ? rec_run(el[i]) : run_empty();
@@ -1172,21 +1257,35 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
             if (bm) {
               kfail = c0 + __ffs(bm) - 1;
               const int src = kfail - 1 - c0;
-              Run before = shfl_run<SH_IDX>(pre, src < 0 ? 0 : src);
+              before = shfl_run<SH_IDX>(pre, src < 0 ? 0 : src);
               if (src < 0) before = acc;
-              if (kfail > segstart) {
-                uint64_t T2 = Sb;
-                if (run_apply(T2, before, c.e) == APPLY_OK) Sok = T2;
-              }
               break;
             }
             acc = shfl_run<SH_IDX>(pre, 31);
           }
-          Sb = Sok;
+          if (kfail < 0) {
+            uint64_t T = Sb;
+            if (run_apply(T, acc, c.e) == APPLY_OK) {
+              Sb = T;
+              WALK_TRACE(abs_start(segstart), abs_start(ei) + el[ei].count, 3u, Sb);
+              segstart = ei + 1;
+              continue;
+            }
+            kfail = segstart;                            // not reached: the last prefix passed
+          } else if (kfail > segstart) {
+            uint64_t T = Sb;
+            if (run_apply(T, before, c.e) == APPLY_OK) {
+              Sb = T;
+              WALK_TRACE(abs_start(segstart), abs_start(kfail), 4u, Sb);
+            } else {
+              kfail = segstart;                          // not reached: that prefix passed
+            }
+          }
           {
             const uint32_t ep = elpos[kfail];
             const TileGeo g = tile_geo(p, pos + (ep >> 12), ntiles);
             Sb = add_terms(p, Sb, g.start + (ep & 0xFFF), el[kfail].count, st);
+            WALK_TRACE(abs_start(kfail), abs_start(kfail) + el[kfail].count, 5u, Sb);
           }
           if (kfail < ei) { restart = kfail + 1; break; }
           segstart = ei + 1;
@@ -1200,12 +1299,13 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       from = rs;
     }
     pos += m;
-    if (pos >= te && tid == 0) p.stats[S_T_WALK0] = globaltimer();
     __syncthreads();
   }
   if (tid == 0) {
     p.outs[k] = bitsd(sm.S);
-    p.stats[S_T_WALK1] = globaltimer();
+    const uint64_t tend = globaltimer();
+    p.stats[S_T_WALK1] = tend;
+    if (t_work0 != 0) atomicAdd(&st[S_NS_WALK_WORK], tend - t_work0);
   }
   __syncthreads();
 }
@@ -1269,6 +1369,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (globaltimer() - t0 > kWaitNs) { atomicOr(&p.ctr[C_ERR], ERR_TMA_TIMEOUT); break; }
         }
         phases ^= 1u << s;
+        if (tid == 0) atomicAdd(&sm.st[S_NS_TMA_WAIT], globaltimer() - t0);
       }
     };
     if (tid == 0) { issue(0); issue(1); }
@@ -1290,17 +1391,21 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       if (t1 < ntiles) {
         wait_stage(s1);
+        const uint64_t ta = globaltimer();
         phase_a(p, sm, dyn + s1 * kStageBytes, s1, t1, ntiles);
+        if (tid == 0) atomicAdd(&sm.st[S_NS_PHASE_A], globaltimer() - ta);
       }
       __syncthreads();
+      const uint64_t tb = globaltimer();
       phase_b(p, sm, dyn + s * kStageBytes, s, t, ntiles);
+      if (tid == 0) atomicAdd(&sm.st[S_NS_PHASE_B], globaltimer() - tb);
       __syncthreads();
     }
   }
 
   // ---- statistics and the last CTA's reset of the shared counters
   __syncthreads();
-  if (tid < S_T_START && sm.st[tid]) atomicAdd(&p.stats[tid], sm.st[tid]);
+  if (tid < S_ACCUM_END && sm.st[tid]) atomicAdd(&p.stats[tid], sm.st[tid]);
   if (tid == 0) {
     __threadfence();
     if (atomicAdd(&p.ctr[C_EXIT], 1u) + 1 == gridDim.x) {

@@ -264,3 +264,15 @@ def test_batched_bad_offsets_are_reported(sq):
     assert st["device_status"] == -6
     # the library stays usable
     check(sq, W.plane_c2(1000, 1, seed=1), 0.0, "after bad offsets")
+
+
+def test_negative_start_crossing_zero(sq):
+    """Sums that start negative and cross zero: the running value changes
+    sign and runs through many binades (random sub-ranges of a c3 plane)."""
+    x = W.plane_c3(200, 100, zero_rows=3)
+    rng = np.random.default_rng(11)
+    for _ in range(120):
+        n = int(rng.integers(1, 6000))
+        a = int(rng.integers(0, len(x) - n))
+        s0 = float(rng.choice([-3.0, -1.0, -0.25, -7.5, -10.0, 2.0]))
+        check(sq, x[a:a + n], s0, f"[{a}:{a + n}] s0={s0}")
