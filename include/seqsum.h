@@ -110,6 +110,8 @@ typedef struct {
   int64_t ns_phase_b;        /* ... forming runs (look-back included) */
   int64_t ns_walk_wait;      /* ... the walk waiting for tile headers */
   int64_t ns_walk_work;      /* ... the walk working */
+  int64_t torn_header_reads; /* tile-header reads that saw words of two publications (retried) */
+  int64_t torn_status_reads; /* look-back reads that saw words of two publications (retried) */
   int64_t t_stream_ns;       /* latest call: kernel start to the last tile header */
   int64_t t_walk_tail_ns;    /* latest call: last tile header to the end of the walk */
   int64_t t_total_ns;        /* latest call: kernel start to the end of the walk */

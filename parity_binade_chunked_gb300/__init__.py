@@ -33,7 +33,7 @@ class _Stats(ctypes.Structure):
         "tiles", "chunks_run", "chunks_list", "chunks_fallback", "lanes_dirty", "walk_segments",
         "runs_rejected", "terms_added", "items", "pool_overflow", "tiles_complex",
         "lookback_steps", "walk_batches", "ns_tma_wait", "ns_lookback", "ns_phase_a", "ns_phase_b",
-        "ns_walk_wait", "ns_walk_work", "t_stream_ns", "t_walk_tail_ns", "t_total_ns")] + [
+        "ns_walk_wait", "ns_walk_work", "torn_header_reads", "torn_status_reads", "t_stream_ns", "t_walk_tail_ns", "t_total_ns")] + [
         ("device_status", ctypes.c_int32), ("device_error_bits", ctypes.c_int32),
         ("check_site", ctypes.c_int32), ("check_pad", ctypes.c_int32), ("check_value", ctypes.c_int64)]
 

@@ -307,6 +307,8 @@ int seqsum_get_stats(seqsum_stats *st) {
   st->ns_phase_b = (int64_t)s[sq::S_NS_PHASE_B];
   st->ns_walk_wait = (int64_t)s[sq::S_NS_WALK_WAIT];
   st->ns_walk_work = (int64_t)s[sq::S_NS_WALK_WORK];
+  st->torn_header_reads = (int64_t)s[sq::S_TORN_HEADER];
+  st->torn_status_reads = (int64_t)s[sq::S_TORN_STATUS];
   st->t_stream_ns = (int64_t)(s[sq::S_T_STREAM_END] - s[sq::S_T_START]);
   st->t_walk_tail_ns = (int64_t)(s[sq::S_T_WALK1] - s[sq::S_T_STREAM_END]);
   st->t_total_ns = (int64_t)(s[sq::S_T_WALK1] - s[sq::S_T_START]);

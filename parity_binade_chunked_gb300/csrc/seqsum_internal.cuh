@@ -15,6 +15,8 @@ constexpr int kStages = 3;                      // copy of tile i+2 | plan of i+
 constexpr int kStageBytes = kTileTerms * 8;
 constexpr int kDynSmem = kStages * kStageBytes + 1024;   // + alignment slack
 constexpr int kChunkSlots = 32;                 // item slots per chunk in a tile's item area
+constexpr int kCountBits = 7;                   // bits per chunk in a complex header's packed counts
+static_assert(kChunkSlots < (1 << kCountBits), "packed item counts");
 constexpr int kTileSlots = kWarps * kChunkSlots;
 constexpr int kWalkTiles = 1024;                // tile headers per walk batch (32 KB)
 constexpr int kWalkElems = 1024;                // flat elements per walk batch (32 KB)
@@ -29,9 +31,10 @@ enum : uint32_t { K_RUN = 0, K_FALLBACK = 1, K_TERMS = 2, K_COMPLEX = 3 };
 //   K_TERMS    : up to three terms carried inline (inc, lo, hi hold their
 //                bits), added one by one
 //   K_COMPLEX  : (tile header) the items live in the tile's item area; inc
-//                holds eight 8-bit item counts, one per chunk
-// Tile headers carry the call's tag in the top byte of lo and of hi, so a
-// reader can check both 16-byte halves.
+//                holds eight 7-bit item counts, one per chunk
+// Tile headers carry the call's tag in every one of their four 64-bit words
+// (a 16-byte access need not be single-copy atomic), so a reader never mixes
+// words of two publications.
 struct __align__(16) Rec {
   int64_t inc, lo, hi;
   uint32_t meta;      // bits 0-7: d (int8), 8-15: flags, 16-19: kind, 20-31: first term in the tile
@@ -71,13 +74,16 @@ enum : int {
   S_TILE_COMPLEX, S_LOOKBACK_STEPS, S_WALK_BATCHES,
   // nanoseconds summed over CTAs (globaltimer)
   S_NS_TMA_WAIT, S_NS_LOOKBACK, S_NS_PHASE_A, S_NS_PHASE_B, S_NS_WALK_WAIT, S_NS_WALK_WORK,
+  S_TORN_HEADER,       // header reads that mixed words of two publications (retried)
+  S_TORN_STATUS,       // look-back reads that mixed words of two publications (retried)
   S_ACCUM_END,         // counters above are summed; below are timestamps of the latest call
-  S_T_START = 24,      // block 0 started
+  S_T_START = 24,      // block 0 started (timestamps follow the summed counters)
   S_T_WALK0 = 25,      // the walk's last batch of headers was ready
   S_T_WALK1 = 26,      // the walk ended
   S_T_STREAM_END = 27, // the last tile header was published (max over CTAs)
   S_COUNT = 32
 };
+static_assert(S_ACCUM_END <= S_T_START, "summed counters overlap the timestamps");
 
 // ---- kernel parameters
 struct Params {

@@ -54,6 +54,9 @@ constexpr int kZeroE = -2000;                  // binade key of a run of zeros
 constexpr int kDirtyKey = -3000;               // merge key of a lane placed term by term
 constexpr uint64_t kWaitNs = 2000000000ull;    // bounded device waits: 2 s
 constexpr uint32_t kMagLo = 896u << 20;        // exponent 896 = 2^-127
+constexpr uint64_t kCountMask = (1u << kCountBits) - 1;
+static_assert(((uint64_t)kChunkSlots << (kCountBits * (kWarps - 1))) < (1ull << 55),
+              "packed item counts must fit a tagged 56-bit word");
 constexpr int kWalkOffEl = 32768;              // walker layout in the dynamic shared memory
 constexpr int kWalkOffPos = 65536;
 constexpr int kWalkOffHead = 69632;
@@ -265,32 +268,42 @@ __device__ __forceinline__ void stcg_rec(Rec *p, const Rec &r) {
   __stcg(q + 1, s[1]);
 }
 
-// Tile headers: the call's tag in the top byte of lo and of hi (so both
-// 16-byte halves carry it), values sign-extended from 56 bits.
+// Tile headers: the call's tag in the top byte of each of the four 64-bit
+// words (inc, lo and hi sign-extended from 56 bits; in the last word the tag
+// takes the first-term bits of meta, which are 0 in a header).  A 16-byte
+// access need not be single-copy atomic, so a reader checks all four words
+// and never takes a header made of two publications.
 constexpr int64_t kBound56 = ((int64_t)1 << 55) - 1;
+constexpr uint64_t kLow56 = 0x00FFFFFFFFFFFFFFull;
 __device__ __forceinline__ int64_t untag56(uint64_t v) { return (int64_t)(v << 8) >> 8; }
+__device__ __forceinline__ uint64_t tag56(int64_t v, uint32_t tag) {
+  return ((uint64_t)max(min(v, kBound56), -kBound56) & kLow56) | ((uint64_t)tag << 56);
+}
 __device__ __forceinline__ void publish_header(Rec *p, const Rec &r, uint32_t tag) {
-  const int64_t lo = max(min(r.lo, kBound56), -kBound56), hi = max(min(r.hi, kBound56), -kBound56);
-  const uint64_t a0 = (uint64_t)r.inc;
-  const uint64_t a1 = ((uint64_t)lo & 0x00FFFFFFFFFFFFFFull) | ((uint64_t)tag << 56);
-  const uint64_t b0 = ((uint64_t)hi & 0x00FFFFFFFFFFFFFFull) | ((uint64_t)tag << 56);
-  const uint64_t b1 = (uint64_t)r.meta | ((uint64_t)(uint16_t)r.e << 32) | ((uint64_t)r.count << 48);
+  const uint64_t a0 = tag56(r.inc, tag);
+  const uint64_t a1 = tag56(r.lo, tag);
+  const uint64_t b0 = tag56(r.hi, tag);
+  const uint64_t b1 = (uint64_t)((r.meta & 0x00FFFFFFu) | (tag << 24)) | ((uint64_t)(uint16_t)r.e << 32) |
+                      ((uint64_t)r.count << 48);
   st_vol_v2(p, a0, a1);
   st_vol_v2(reinterpret_cast<char *>(p) + 16, b0, b1);
 }
-// False while the header does not carry `tag` in both halves.
-__device__ __forceinline__ bool read_header(const Rec *p, uint32_t tag, Rec &r) {
+// 1: the header carries `tag` in all four words; 0: not yet published;
+// -1: a mix of two publications (read again).
+__device__ __forceinline__ int read_header(const Rec *p, uint32_t tag, Rec &r) {
   uint64_t a0, a1, b0, b1;
   ld_vol_v2(p, a0, a1);
   ld_vol_v2(reinterpret_cast<const char *>(p) + 16, b0, b1);
-  if ((uint32_t)(a1 >> 56) != tag || (uint32_t)(b0 >> 56) != tag) return false;
-  r.inc = (int64_t)a0;
+  const int nt = ((uint32_t)(a0 >> 56) == tag) + ((uint32_t)(a1 >> 56) == tag) + ((uint32_t)(b0 >> 56) == tag) +
+                 ((uint32_t)((b1 >> 24) & 0xFFu) == tag);
+  if (nt != 4) return nt == 0 ? 0 : -1;
+  r.inc = untag56(a0);
   r.lo = untag56(a1);
   r.hi = untag56(b0);
-  r.meta = (uint32_t)b1;
+  r.meta = (uint32_t)b1 & 0x00FFFFFFu;
   r.e = (int16_t)(uint16_t)(b1 >> 32);
   r.count = (uint16_t)(b1 >> 48);
-  return true;
+  return 1;
 }
 
 // ---------------------------------------------------------------- tile geometry
@@ -410,7 +423,11 @@ __device__ __noinline__ Prefix lookback(const Params &p, int sum, int64_t first_
       const int64_t idx = j - 8 * lane - q;
       if (idx < first_tile) { incl = true; continue; }           // a virtual prefix of 0
       const uint32_t ta = (uint32_t)(A[q] & 0xFF), tb = (uint32_t)B[q];
-      if (((ta >> 1) != ep) || (ta != tb)) { ready = false; continue; }
+      if (((ta >> 1) != ep) || (ta != tb)) {
+        if (ta != tb && ((ta >> 1) == ep || (tb >> 1) == ep)) atomicAdd(&st[S_TORN_STATUS], 1ull);
+        ready = false;
+        continue;
+      }
       sum = df_add(sum, DF{__uint_as_float((uint32_t)(A[q] >> 32)), __uint_as_float((uint32_t)A[q] & ~0xFFu)});
       sab += __uint_as_float((uint32_t)(B[q] >> 32));
       if (ta & 1u) incl = true;
@@ -879,7 +896,7 @@ __device__ void phase_b(const Params &p, Smem &sm, const unsigned char *stage, i
           else n = 0;
         }
         orf |= rec_flags(c.meta);
-        packed |= (uint64_t)(uint32_t)n << (8 * k);
+        packed |= (uint64_t)(uint32_t)n << (kCountBits * k);
       }
       Run z = run_empty();
       z.inc = (int64_t)packed;
@@ -983,8 +1000,13 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       __syncthreads();
       for (int i = tid; i < want; i += kThreads) {
         Rec h;
-        if (sq_ok(p, pos + i < p.cap_tiles, 11, pos + i) && read_header(p.hdr + pos + i, tag, h)) hdrs[i] = h;
-        else atomicMin(&sm.m, i);
+        const int rh = sq_ok(p, pos + i < p.cap_tiles, 11, pos + i) ? read_header(p.hdr + pos + i, tag, h) : 0;
+        if (rh > 0) {
+          hdrs[i] = h;
+        } else {
+          atomicMin(&sm.m, i);
+          if (rh < 0) atomicAdd(&st[S_TORN_HEADER], 1ull);
+        }
       }
       __syncthreads();
       if (sm.m > 0) break;
@@ -1017,9 +1039,10 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
           const Rec &h = hdrs[i];
           if (rec_kind(h.meta) == K_COMPLEX) {
             const uint64_t packed = (uint64_t)h.inc;
-            for (int cc = 0; cc < kWarps; cc++) c += (int)((packed >> (8 * cc)) & 0xFF);
+            for (int cc = 0; cc < kWarps; cc++) c += (int)((packed >> (kCountBits * cc)) & kCountMask);
           } else {
             c = 1;
+            (void)sq_ok(p, h.count >= 1 && h.count <= kTileTerms, 18, h.count);
           }
         }
         cnt[q] = c;
@@ -1065,7 +1088,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
           const uint64_t packed = (uint64_t)h.inc;
           int o2 = off;
           for (int cc = 0; cc < kWarps; cc++) {
-            const int n = (int)((packed >> (8 * cc)) & 0xFF);
+            const int n = (int)((packed >> (kCountBits * cc)) & kCountMask);
             for (int u = 0; u < n; u++) {
               if (sq_ok(p, o2 >= 0 && o2 < kWalkElems && u < kChunkSlots, 13, ((int64_t)o2 << 32) | (u << 8) | cc))
                 elpos[o2] = 0x80000000u | ((uint32_t)i << 12) | ((uint32_t)cc << 8) | (uint32_t)u;
@@ -1084,7 +1107,12 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         const uint32_t i = (ep >> 12) & 0x7FFFFu, cc = (ep >> 8) & 0xFu, u = ep & 0xFFu;
         const Rec *src = p.items + (pos + i) * kTileSlots + cc * kChunkSlots + u;
         if (item_ok(p, src, 14)) {
-          const Rec it = ldcg_rec(src);
+          Rec it = ldcg_rec(src);
+          if (!sq_ok(p, rec_kind(it.meta) != K_COMPLEX && it.count >= 1 &&
+                            rec_tstart(it.meta) + it.count <= (uint32_t)kTileTerms,
+                     17, ((int64_t)it.meta << 16) | it.count)) {
+            it = make_rec(run_empty(), kZeroE, K_RUN, 0, 0);
+          }
           el[j] = it;
           elpos[j] = (i << 12) | rec_tstart(it.meta);
         }
