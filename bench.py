@@ -281,8 +281,11 @@ def main():
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
         "kernel_ms": {"median": statistics.median(times), "min": min(times), "max": max(times)},
-        "walk_stats_per_step": {k: v / (args.steps + args.warmup) for k, v in stats.items()
-                                if k not in ("device_status", "device_error_bits")},
+        # counters and ns_* (summed over CTAs) per call; t_* are the last call's own
+        "device_stats_per_call": {k: (v if k.startswith("t_") else v / (args.steps + args.warmup))
+                                  for k, v in stats.items()
+                                  if k not in ("device_status", "device_error_bits", "check_site", "check_pad",
+                                               "check_value")},
         "device_status": stats["device_status"],
         "wall_s": t_wall,
     }

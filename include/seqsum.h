@@ -102,16 +102,23 @@ typedef struct {
   int64_t items;             /* items written for split chunks */
   int64_t pool_overflow;     /* split chunks that found no room and fell back */
   int64_t tiles_complex;     /* tiles the walk descended into */
-  int64_t lookback_steps;    /* look-back windows read by the plan */
+  int64_t scan_windows;      /* windows of tile sums the plan's prefix scanner took */
   int64_t walk_batches;      /* batches of tile headers the walk took */
   int64_t ns_tma_wait;       /* nanoseconds, summed over CTAs: waiting for tile copies */
-  int64_t ns_lookback;       /* ... in the plan's look-back */
+  int64_t ns_prefix_wait;    /* ... run units waiting for the plan's prefix of their tile */
   int64_t ns_phase_a;        /* ... forming the plan's sums */
-  int64_t ns_phase_b;        /* ... forming runs (look-back included) */
+  int64_t ns_phase_b;        /* ... forming runs (the prefix wait included) */
   int64_t ns_walk_wait;      /* ... the walk waiting for tile headers */
   int64_t ns_walk_work;      /* ... the walk working */
   int64_t torn_header_reads; /* tile-header reads that saw words of two publications (retried) */
-  int64_t torn_status_reads; /* look-back reads that saw words of two publications (retried) */
+  int64_t torn_status_reads; /* prefix reads that saw words of two publications (retried) */
+  int64_t ns_scan;           /* the prefix scanner's time from its first to its last window */
+  int64_t ns_walk_count;     /* the walk's work by section: counting a batch's elements */
+  int64_t ns_walk_gather;    /* ... gathering headers and items into one list */
+  int64_t ns_walk_scan;      /* ... composing same-binade segments in parallel */
+  int64_t ns_walk_serial;    /* ... the in-order pass over the segments */
+  int64_t ns_walk_adds;      /* ... of which term-by-term fp64 adds */
+  int64_t plan_local;        /* run units that formed their chunk aggregates themselves */
   int64_t t_stream_ns;       /* latest call: kernel start to the last tile header */
   int64_t t_walk_tail_ns;    /* latest call: last tile header to the end of the walk */
   int64_t t_total_ns;        /* latest call: kernel start to the end of the walk */

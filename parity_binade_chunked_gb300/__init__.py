@@ -32,8 +32,9 @@ class _Stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
         "tiles", "chunks_run", "chunks_list", "chunks_fallback", "lanes_dirty", "walk_segments",
         "runs_rejected", "terms_added", "items", "pool_overflow", "tiles_complex",
-        "lookback_steps", "walk_batches", "ns_tma_wait", "ns_lookback", "ns_phase_a", "ns_phase_b",
-        "ns_walk_wait", "ns_walk_work", "torn_header_reads", "torn_status_reads", "t_stream_ns", "t_walk_tail_ns", "t_total_ns")] + [
+        "scan_windows", "walk_batches", "ns_tma_wait", "ns_prefix_wait", "ns_phase_a", "ns_phase_b",
+        "ns_walk_wait", "ns_walk_work", "torn_header_reads", "torn_status_reads", "ns_scan", "ns_walk_count", "ns_walk_gather",
+        "ns_walk_scan", "ns_walk_serial", "ns_walk_adds", "plan_local", "t_stream_ns", "t_walk_tail_ns", "t_total_ns")] + [
         ("device_status", ctypes.c_int32), ("device_error_bits", ctypes.c_int32),
         ("check_site", ctypes.c_int32), ("check_pad", ctypes.c_int32), ("check_value", ctypes.c_int64)]
 

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <map>
@@ -23,7 +24,8 @@ struct Workspace {
   int device = 0;
   cudaStream_t stream = nullptr;
   int64_t cap_tiles = 0, cap_sums = 0;
-  uint64_t *status = nullptr;        // look-back words, 2 per tile
+  uint64_t *status = nullptr;        // the plan's prefix words, 2 per tile
+  uint64_t *cagg = nullptr;          // the plan's chunk aggregates, 2 words per chunk
   Rec *hdr = nullptr;                // one header per tile
   Rec *items = nullptr;              // kTileSlots items per tile
   uint32_t *ctr = nullptr;
@@ -43,6 +45,7 @@ std::map<std::pair<int, cudaStream_t>, Workspace *> g_ws;
 Workspace *g_last = nullptr;
 int g_last_cuda = 0;
 int g_plan_mode = 0;
+int64_t g_wave = 0;                  // tiles plan units run ahead of run units (0: not yet read)
 int g_blocks_per_sm = 0;
 int g_num_sms[64] = {0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -54,10 +57,12 @@ int cuda_fail(cudaError_t e) {
 
 void ws_free(Workspace *w) {
   cudaFree(w->status);
+  cudaFree(w->cagg);
   cudaFree(w->hdr);
   cudaFree(w->items);
   cudaFree(w->tile_begin);
-  w->status = nullptr; w->hdr = w->items = nullptr;
+  w->status = w->cagg = nullptr;
+  w->hdr = w->items = nullptr;
   w->tile_begin = nullptr;
   w->cap_tiles = w->cap_sums = 0;
 }
@@ -89,6 +94,7 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
     const int64_t cs = sums > w->cap_sums ? sums + 16 : w->cap_sums;
     ws_free(w);
     if (cudaMalloc(&w->status, ct * 2 * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMalloc(&w->cagg, ct * sq::kWarps * 2 * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&w->hdr, ct * sizeof(Rec)) != cudaSuccess ||
         cudaMalloc(&w->items, ct * sq::kTileSlots * sizeof(Rec)) != cudaSuccess ||
         cudaMalloc(&w->tile_begin, (cs + 1) * sizeof(int64_t)) != cudaSuccess) {
@@ -97,6 +103,7 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
       return SEQSUM_ENOMEM;
     }
     cudaMemset(w->status, 0, ct * 2 * sizeof(uint64_t));
+    cudaMemset(w->cagg, 0, ct * sq::kWarps * 2 * sizeof(uint64_t));
     cudaMemset(w->hdr, 0, ct * sizeof(Rec));
     w->cap_tiles = ct;
     w->cap_sums = cs;
@@ -116,6 +123,14 @@ int ensure_device_info() {
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (g_blocks_per_sm == 0) g_blocks_per_sm = sq::kernel_max_blocks_per_sm();
+  if (g_wave == 0) {
+    // 1024 tiles (32 MB): more than the units a full grid holds in flight,
+    // so a run unit finds its prefix published, and little enough that the
+    // tile is still in L2 when its run unit reads it again.
+    g_wave = 1024;
+    const char *ev = getenv("SEQSUM_WAVE");
+    if (ev && atoll(ev) > 0) g_wave = atoll(ev);
+  }
   if (!g_encode) {
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -126,12 +141,14 @@ int ensure_device_info() {
   return SEQSUM_OK;
 }
 
-// Next epoch for the look-back tags (1..127); the status words are cleared
-// whenever the tag wraps, so a stale word can never carry a current tag.
+// Next epoch for the tags (1..127); every tagged word (the plan's prefix and
+// chunk aggregates, the tile headers) is cleared whenever the tag wraps, so a
+// stale word can never carry a current tag.
 void next_epoch(Workspace *w, cudaStream_t stream) {
   w->epoch++;
   if (w->epoch > 127) {
     cudaMemsetAsync(w->status, 0, w->cap_tiles * 2 * sizeof(uint64_t), stream);
+    cudaMemsetAsync(w->cagg, 0, w->cap_tiles * sq::kWarps * 2 * sizeof(uint64_t), stream);
     cudaMemsetAsync(w->hdr, 0, w->cap_tiles * sizeof(Rec), stream);
     w->epoch = 1;
   }
@@ -158,6 +175,7 @@ int64_t tensor_map(Workspace *w, const double *x, int64_t n_total) {
 
 void fill_ws(Params &p, Workspace *w) {
   p.status = w->status;
+  p.cagg = w->cagg;
   p.hdr = w->hdr;
   p.items = w->items;
   p.ctr = w->ctr;
@@ -208,10 +226,11 @@ int batched_impl(const double *x, int64_t x_len, const int64_t *offsets, int32_t
   fill_ws(p, w);
   p.tma_rows = tensor_map(w, x, x_len);
   p.nwalkers = nsums < sq::kMaxWalkers ? nsums : sq::kMaxWalkers;
+  p.wave = g_wave;
   cudaError_t e = sq::launch_setup(p, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   int grid = g_num_sms[w->device] * g_blocks_per_sm;
-  if (grid < p.nwalkers + 1) grid = p.nwalkers + 1;
+  if (grid < p.nwalkers + 2) grid = p.nwalkers + 2;     // walkers, the scanner, a streamer
   static CUtensorMap dummy;
   e = sq::launch_seqsum(p, p.tma_rows ? &w->tmap : &dummy, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -246,9 +265,10 @@ int seqsum_f64(const double *x, int64_t n, double s0, double *out, cudaStream_t 
   fill_ws(p, w);
   p.tma_rows = n > 0 ? tensor_map(w, x, n) : 0;
   p.nwalkers = 1;
+  p.wave = g_wave;
   const int dev = w->device;
   int64_t grid = (int64_t)g_num_sms[dev] * g_blocks_per_sm;
-  if (tiles + 1 < grid) grid = tiles + 1;             // one walker + streaming CTAs
+  if (2 * tiles + 2 < grid) grid = 2 * tiles + 2;     // the walker, the scanner, one streamer per unit
   static CUtensorMap dummy;
   cudaError_t e = sq::launch_seqsum(p, p.tma_rows ? &w->tmap : &dummy, (int)grid, stream);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -283,9 +303,9 @@ int seqsum_get_stats(seqsum_stats *st) {
   if (e == cudaSuccess) e = cudaMemset(w->stats, 0, sizeof s);
   const uint32_t err = (e == cudaSuccess) ? c[sq::C_ERR] : 0u;
   if (e == cudaSuccess && err) e = cudaMemset(w->ctr + sq::C_ERR, 0, sizeof(uint32_t));
-  if (e == cudaSuccess && c[5]) e = cudaMemset(w->ctr + 5, 0, 3 * sizeof(uint32_t));
-  st->check_site = (int32_t)c[5];
-  st->check_value = (int64_t)(((uint64_t)c[7] << 32) | c[6]);
+  if (e == cudaSuccess && c[sq::C_CHECK_SITE]) e = cudaMemset(w->ctr + sq::C_CHECK_SITE, 0, 3 * sizeof(uint32_t));
+  st->check_site = (int32_t)c[sq::C_CHECK_SITE];
+  st->check_value = (int64_t)(((uint64_t)c[sq::C_CHECK_HI] << 32) | c[sq::C_CHECK_LO]);
   cudaSetDevice(prev);
   if (e != cudaSuccess) return cuda_fail(e);
   st->tiles = (int64_t)s[sq::S_TILES];
@@ -299,16 +319,23 @@ int seqsum_get_stats(seqsum_stats *st) {
   st->items = (int64_t)s[sq::S_ITEMS];
   st->pool_overflow = (int64_t)s[sq::S_POOL_OVERFLOW];
   st->tiles_complex = (int64_t)s[sq::S_TILE_COMPLEX];
-  st->lookback_steps = (int64_t)s[sq::S_LOOKBACK_STEPS];
+  st->scan_windows = (int64_t)s[sq::S_SCAN_WINDOWS];
   st->walk_batches = (int64_t)s[sq::S_WALK_BATCHES];
   st->ns_tma_wait = (int64_t)s[sq::S_NS_TMA_WAIT];
-  st->ns_lookback = (int64_t)s[sq::S_NS_LOOKBACK];
+  st->ns_prefix_wait = (int64_t)s[sq::S_NS_PREFIX_WAIT];
   st->ns_phase_a = (int64_t)s[sq::S_NS_PHASE_A];
   st->ns_phase_b = (int64_t)s[sq::S_NS_PHASE_B];
   st->ns_walk_wait = (int64_t)s[sq::S_NS_WALK_WAIT];
   st->ns_walk_work = (int64_t)s[sq::S_NS_WALK_WORK];
   st->torn_header_reads = (int64_t)s[sq::S_TORN_HEADER];
   st->torn_status_reads = (int64_t)s[sq::S_TORN_STATUS];
+  st->ns_scan = (int64_t)s[sq::S_NS_SCAN];
+  st->ns_walk_count = (int64_t)s[sq::S_NS_WALK_COUNT];
+  st->ns_walk_gather = (int64_t)s[sq::S_NS_WALK_GATHER];
+  st->ns_walk_scan = (int64_t)s[sq::S_NS_WALK_SCAN];
+  st->ns_walk_serial = (int64_t)s[sq::S_NS_WALK_SERIAL];
+  st->ns_walk_adds = (int64_t)s[sq::S_NS_WALK_ADDS];
+  st->plan_local = (int64_t)s[sq::S_PLAN_LOCAL];
   st->t_stream_ns = (int64_t)(s[sq::S_T_STREAM_END] - s[sq::S_T_START]);
   st->t_walk_tail_ns = (int64_t)(s[sq::S_T_WALK1] - s[sq::S_T_STREAM_END]);
   st->t_total_ns = (int64_t)(s[sq::S_T_WALK1] - s[sq::S_T_START]);

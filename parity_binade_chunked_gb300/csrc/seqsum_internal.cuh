@@ -52,16 +52,20 @@ __host__ __device__ inline uint32_t rec_tstart(uint32_t meta) { return meta >> 2
 
 // ---- counters in the workspace
 enum : int {
-  C_TICKET = 0,      // next tile ticket
+  C_TICKET = 0,      // next unit ticket (plan and run units of the tiles)
   C_EXIT = 1,        // CTAs that finished
   C_SUMTICKET = 2,   // next sum for a walker
   C_ERR = 3,         // error bits (ERR_*)
   C_NTILES = 4,      // tiles of a batched call (written by the set-up kernel)
-  C_COUNT = 8
+  C_ROLE = 5,        // next CTA role: walkers, then the scanner, then streamers
+  C_CHECK_SITE = 8,  // self-checking builds: first failed check and its value
+  C_CHECK_LO = 9,
+  C_CHECK_HI = 10,
+  C_COUNT = 16
 };
 enum : uint32_t {
   ERR_TMA_TIMEOUT = 1u,       // a TMA copy did not complete within the wait limit
-  ERR_PLAN_TIMEOUT = 2u,      // a look-back wait gave up (the plan only; results stay exact)
+  ERR_PLAN_TIMEOUT = 2u,      // a wait for the plan's prefix gave up (the plan only; results stay exact)
   ERR_BAD_OFFSETS = 4u,       // offsets out of order or out of range
   ERR_CAPACITY = 8u,          // a batched call needed more tiles than its workspace holds
   ERR_WALK_TIMEOUT = 16u,     // the walk waited too long for a tile record
@@ -71,17 +75,23 @@ enum : uint32_t {
 enum : int {
   S_TILES = 0, S_CHUNK_RUN, S_CHUNK_LIST, S_CHUNK_FALLBACK, S_LANE_DIRTY,
   S_WALK_SEGMENTS, S_RUN_REJECTED, S_TERMS_ADDED, S_ITEMS, S_POOL_OVERFLOW,
-  S_TILE_COMPLEX, S_LOOKBACK_STEPS, S_WALK_BATCHES,
+  S_TILE_COMPLEX, S_SCAN_WINDOWS, S_WALK_BATCHES,
   // nanoseconds summed over CTAs (globaltimer)
-  S_NS_TMA_WAIT, S_NS_LOOKBACK, S_NS_PHASE_A, S_NS_PHASE_B, S_NS_WALK_WAIT, S_NS_WALK_WORK,
+  S_NS_TMA_WAIT, S_NS_PREFIX_WAIT, S_NS_PHASE_A, S_NS_PHASE_B, S_NS_WALK_WAIT, S_NS_WALK_WORK,
   S_TORN_HEADER,       // header reads that mixed words of two publications (retried)
-  S_TORN_STATUS,       // look-back reads that mixed words of two publications (retried)
+  S_TORN_STATUS,       // prefix reads that mixed words of two publications (retried)
+  S_NS_SCAN,           // the scanner's time from its first to its last window
+  S_PLAN_LOCAL,        // run units whose chunk aggregates were not published in time (formed locally)
+  // the walk's work by section (nanoseconds): counting a batch's elements,
+  // gathering them, the segmented scan, the in-order pass, and within that
+  // pass the term-by-term adds
+  S_NS_WALK_COUNT, S_NS_WALK_GATHER, S_NS_WALK_SCAN, S_NS_WALK_SERIAL, S_NS_WALK_ADDS,
   S_ACCUM_END,         // counters above are summed; below are timestamps of the latest call
-  S_T_START = 24,      // block 0 started (timestamps follow the summed counters)
-  S_T_WALK0 = 25,      // the walk's last batch of headers was ready
-  S_T_WALK1 = 26,      // the walk ended
-  S_T_STREAM_END = 27, // the last tile header was published (max over CTAs)
-  S_COUNT = 32
+  S_T_START = 40,      // block 0 started (timestamps follow the summed counters)
+  S_T_WALK0 = 41,      // the walk's last batch of headers was ready
+  S_T_WALK1 = 42,      // the walk ended
+  S_T_STREAM_END = 43, // the last tile header was published (max over CTAs)
+  S_COUNT = 48
 };
 static_assert(S_ACCUM_END <= S_T_START, "summed counters overlap the timestamps");
 
@@ -101,12 +111,14 @@ struct Params {
   int32_t pad;
   // workspace
   uint64_t *status;            // 2 words per tile: tagged approximate prefix
+  uint64_t *cagg;              // 2 words per chunk: tagged chunk aggregates of the plan
   Rec *hdr;                    // one header per tile
   Rec *items;                  // kTileSlots items per tile
   uint32_t *ctr;               // C_COUNT counters
   int64_t *tile_begin;         // batched: nsums + 1 entries
-  int32_t nwalkers;            // CTAs 0 .. nwalkers-1 walk; the others stream
+  int32_t nwalkers;            // CTA roles 0 .. nwalkers-1 walk, role nwalkers scans, the others stream
   int32_t pad2;
+  int64_t wave;                // plan units run this many tiles ahead of run units
   unsigned long long *dbg;     // self-checking builds: 64 diagnostic words
   int64_t cap_tiles;           // tiles the workspace holds
   unsigned long long *stats;   // S_COUNT counters

@@ -116,6 +116,14 @@ __device__ __forceinline__ void st_vol_v2(void *p, uint64_t a, uint64_t b) {
   asm volatile("st.volatile.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through L2 (the prefetch of a
+// run unit's plan words); completed by cp_async_wait_all of the same thread.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t dbits(double v) { return (uint64_t)__double_as_longlong(v); }
 __device__ __forceinline__ double bitsd(uint64_t b) { return __longlong_as_double((long long)b); }
 
@@ -125,9 +133,9 @@ __device__ __forceinline__ double bitsd(uint64_t b) { return __longlong_as_doubl
 #ifdef SEQSUM_CHECKS
 __device__ __forceinline__ bool sq_ok(const Params &p, bool cond, uint32_t site, int64_t val) {
   if (!cond) {
-    if (atomicCAS(&p.ctr[5], 0u, site) == 0u) {
-      p.ctr[6] = (uint32_t)(uint64_t)val;
-      p.ctr[7] = (uint32_t)((uint64_t)val >> 32);
+    if (atomicCAS(&p.ctr[C_CHECK_SITE], 0u, site) == 0u) {
+      p.ctr[C_CHECK_LO] = (uint32_t)(uint64_t)val;
+      p.ctr[C_CHECK_HI] = (uint32_t)((uint64_t)val >> 32);
     }
     atomicOr(&p.ctr[C_ERR], 32u);
   }
@@ -340,18 +348,42 @@ __device__ __forceinline__ TileGeo tile_geo(const Params &p, int64_t t, int64_t 
 }
 
 // ---------------------------------------------------------------- shared memory
+// A chunk's aggregates for the plan: the sum and |x| sum of the terms' fp32
+// images, the largest magnitude word, and whether any term has its sign bit
+// set or any term is non-zero.  Published by plan units as two tagged words
+//   w0 = sig bits << 32 | (ab bits with the low 8 bits replaced by the tag)
+//   w1 = mx << 32 | flags << 8 | tag,   tag = the call's epoch.
+enum : uint32_t { WA_NEG = 1u, WA_NZ = 2u };
 struct WarpAgg {
   float sig, ab;
-  uint32_t orh, orz, mx, andh;
+  uint32_t mx, flags;
 };
+__device__ __forceinline__ void publish_wagg(uint64_t *dst, const WarpAgg &a, uint32_t tag) {
+  const uint64_t w0 = ((uint64_t)__float_as_uint(a.sig) << 32) | ((__float_as_uint(a.ab) & ~0xFFu) | tag);
+  const uint64_t w1 = ((uint64_t)a.mx << 32) | ((a.flags & 0xFFu) << 8) | tag;
+  st_vol_v2(dst, w0, w1);
+}
+__device__ __forceinline__ bool decode_wagg(uint64_t w0, uint64_t w1, uint32_t tag, WarpAgg &a) {
+  if ((uint32_t)(w0 & 0xFF) != tag || (uint32_t)(w1 & 0xFF) != tag) return false;
+  a.sig = __uint_as_float((uint32_t)(w0 >> 32));
+  a.ab = __uint_as_float((uint32_t)w0 & ~0xFFu);
+  a.mx = (uint32_t)(w1 >> 32);
+  a.flags = ((uint32_t)w1 >> 8) & 0xFFu;
+  return true;
+}
 
 struct Smem {
   uint64_t bar[kStages];
   int64_t tk[kStages];
   int tma[kStages];
+  int plan[kStages];                // the stage holds a plan unit (else a run unit)
+  int role;
+  // a run unit's plan words, copied in ahead of its runs: the chunk
+  // aggregates and the prefix of the tile before, for tile raw_tile
+  uint64_t agg_raw[kStages][kWarps][2];
+  uint64_t pre_raw[kStages][2];
+  int64_t raw_tile[kStages];
   WarpAgg wa[kStages][kWarps];
-  DF agg[kStages];
-  float agg_abs[kStages];
   DF ex;
   float ex_abs;
   Rec chunk[kWarps];
@@ -364,105 +396,199 @@ struct Smem {
   Run wagg[kWarps];
   int wcnt[kWarps];
   int sum_k;
+  // scanner
+  DF scan_v[kWarps];
+  float scan_a[kWarps];
+  int scan_f[kWarps];
+  DF carry;
+  float carry_abs;
 };
 
-// ---------------------------------------------------------------- look-back
+// ---------------------------------------------------------------- the plan's prefix
 // Per tile two tagged 64-bit words, written and read as one 16-byte access:
 //   A = sum.hi (fp32) << 32 | sum.lo (fp32) with its low 8 bits replaced by the tag
 //   B = |x| sum (fp32) << 32 | tag;   tag = epoch << 1 | kind,
-// kind 0 = the tile's own sum, 1 = the inclusive prefix.  A reader takes a
-// tile only when both words carry the current tag, so no fence is needed.
+// kind 0 = the tile's own approximate sum, 1 = the inclusive prefix (s0 and
+// every tile of the sum up to this one).  A reader takes a word pair only when
+// both carry the same current tag.
 __device__ __forceinline__ void publish_status(uint64_t *st, DF sig, float ab, uint32_t epoch, uint32_t kind) {
   const uint32_t tag = (epoch << 1) | kind;
   const uint64_t A = ((uint64_t)__float_as_uint(sig.hi) << 32) | ((__float_as_uint(sig.lo) & ~0xFFu) | tag);
   const uint64_t B = ((uint64_t)__float_as_uint(ab) << 32) | tag;
   st_vol_v2(st, A, B);
 }
+__device__ __forceinline__ DF status_sum(uint64_t A) {
+  return DF{__uint_as_float((uint32_t)(A >> 32)), __uint_as_float((uint32_t)A & ~0xFFu)};
+}
+__device__ __forceinline__ float status_abs(uint64_t B) { return __uint_as_float((uint32_t)(B >> 32)); }
 
 struct Prefix {
   DF ex;
   float ex_abs;
 };
 
-// Run by one whole warp; returns the approximate exclusive prefix of tile t
-// (the first tile of sum `sum` starts from s0).  Each lane reads 8
-// consecutive statuses, so one round trip covers 256 tiles.
-__device__ __noinline__ Prefix lookback(const Params &p, int sum, int64_t first_tile, int64_t t, DF agg,
-                                        float agg_abs, unsigned long long *st) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t ep = p.epoch;
-  if (t == first_tile) {                    // its inclusive prefix went out with its sum
-    const double s0 = p.s0s ? p.s0s[sum] : p.s0;
-    const DF ex = df_from_double(s0);
+// Units of work.  Every tile has a plan unit (copy it, publish its approximate
+// sum) and a run unit (copy it again, form its runs from the prefix the
+// scanner published for the tile before it).  Tickets hand out the plan units
+// of the first `wave` tiles, then a run unit and a plan unit in turn, then the
+// remaining run units: the plan of tile t always precedes the run of tile
+// t + 1 by about `wave` tiles, so a run unit's prefix is normally published
+// long before it is read, and its tile is still in L2.  Returns true for a
+// plan unit.
+__device__ __forceinline__ bool unit_of(int64_t u, int64_t ntiles, int64_t wave, int64_t &tile) {
+  const int64_t w = min(wave, ntiles);
+  if (u < w) { tile = u; return true; }
+  const int64_t v = u - w, rest = ntiles - w;
+  if (v < 2 * rest) {
+    tile = (v & 1) ? w + (v >> 1) : (v >> 1);
+    return (v & 1) != 0;
+  }
+  tile = rest + (v - 2 * rest);
+  return false;
+}
+
+// The approximate exclusive prefix of tile t: s0 for the first tile of a sum,
+// else the inclusive prefix the scanner published for tile t - 1 (a bounded
+// wait; on a timeout the plan is only worse, the result stays exact).  One
+// thread.
+__device__ __forceinline__ Prefix read_prefix(const Params &p, int sum, int64_t first_tile, int64_t t,
+                                              unsigned long long *st) {
+  if (t == first_tile) {
+    const DF ex = df_from_double(p.s0s ? p.s0s[sum] : p.s0);
     return Prefix{ex, fabsf(ex.hi)};
   }
-  DF run = DF{0.0f, 0.0f};
-  float run_abs = 0.0f;
-  int64_t j = t - 1;
+  const uint32_t tag = (p.epoch << 1) | 1u;
   const uint64_t t0 = globaltimer();
-  bool gave_up = false;
+  if (!sq_ok(p, t >= 1 && t - 1 < p.cap_tiles, 1, t)) return Prefix{DF{0.0f, 0.0f}, 0.0f};
   while (true) {
-    if (lane == 0) atomicAdd(&st[S_LOOKBACK_STEPS], 1ull);
-    // this lane: tiles j - 8*lane - q, q = 0..7 (descending); the eight
-    // loads are issued together, then read in order
-    uint64_t A[8], B[8];
-#pragma unroll
-    for (int q = 0; q < 8; q++) {
-      const int64_t idx = j - 8 * lane - q;
+    uint64_t A, B;
+    ld_vol_v2(p.status + 2 * (t - 1), A, B);
+    const uint32_t ta = (uint32_t)(A & 0xFF), tb = (uint32_t)B;
+    if (ta == tag && tb == tag) return Prefix{status_sum(A), status_abs(B)};
+    if (ta != tb && ((ta >> 1) == p.epoch || (tb >> 1) == p.epoch)) atomicAdd(&st[S_TORN_STATUS], 1ull);
+    if (globaltimer() - t0 > kWaitNs) {
+      atomicOr(&p.ctr[C_ERR], ERR_PLAN_TIMEOUT);
+      return Prefix{DF{0.0f, 0.0f}, 0.0f};
+    }
+    __nanosleep(32);
+  }
+}
+
+// The scanner (a whole CTA): takes, from where it stands, the longest run of
+// tiles whose approximate sums are published (up to 1024 tiles), scans it --
+// a tile published as kind 1 starts a sum and already holds s0 plus its own
+// sum -- and publishes every other tile's inclusive prefix as kind 1
+// (Research-1424, section 3: a prefix over the row sums gives S at each row
+// start; Research-1433, open question: the plan's prefix as a scan).
+__device__ __noinline__ void scan_prefix(const Params &p, Smem &sm, int64_t ntiles) {
+  constexpr int PER = 4;
+  constexpr int WIN = kThreads * PER;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t ep = p.epoch;
+  unsigned long long *st = sm.st;
+  int64_t pos = 0;
+  DF carry = DF{0.0f, 0.0f};            // inclusive prefix of tile pos - 1
+  float carry_abs = 0.0f;
+  uint64_t tprog = globaltimer();
+  const uint64_t tbegin = tprog;
+  while (pos < ntiles) {
+    uint64_t A[PER], B[PER];
+#pragma unroll 1
+    for (int q = 0; q < PER; q++) {
+      const int64_t idx = pos + tid * PER + q;
       A[q] = 0;
       B[q] = 0;
-      if (idx >= first_tile && sq_ok(p, idx < p.cap_tiles, 1, idx)) ld_vol_v2(p.status + 2 * idx, A[q], B[q]);
+      if (idx < ntiles && sq_ok(p, idx < p.cap_tiles, 20, idx)) ld_vol_v2(p.status + 2 * idx, A[q], B[q]);
     }
-    DF sum = DF{0.0f, 0.0f};
-    float sab = 0.0f;
-    bool incl = false;           // reached an inclusive status (or the sum's start)
-    bool ready = true;           // every status up to there is present
-#pragma unroll
-    for (int q = 0; q < 8; q++) {
-      if (incl || !ready) continue;
-      const int64_t idx = j - 8 * lane - q;
-      if (idx < first_tile) { incl = true; continue; }           // a virtual prefix of 0
+    int myfirst = PER;
+#pragma unroll 1
+    for (int q = PER - 1; q >= 0; q--) {
+      const int64_t idx = pos + tid * PER + q;
       const uint32_t ta = (uint32_t)(A[q] & 0xFF), tb = (uint32_t)B[q];
-      if (((ta >> 1) != ep) || (ta != tb)) {
-        if (ta != tb && ((ta >> 1) == ep || (tb >> 1) == ep)) atomicAdd(&st[S_TORN_STATUS], 1ull);
-        ready = false;
-        continue;
+      if (!(idx < ntiles && (ta >> 1) == ep && ta == tb)) myfirst = q;
+    }
+    if (tid == 0) sm.m = WIN;
+    __syncthreads();
+    if (myfirst < PER) atomicMin(&sm.m, tid * PER + myfirst);
+    __syncthreads();
+    const int m = sm.m;                    // tiles [pos, pos + m) are published
+    __syncthreads();
+    if (m == 0) {
+      if (globaltimer() - tprog > kWaitNs) {
+        if (tid == 0) atomicOr(&p.ctr[C_ERR], ERR_PLAN_TIMEOUT);
+        break;
       }
-      sum = df_add(sum, DF{__uint_as_float((uint32_t)(A[q] >> 32)), __uint_as_float((uint32_t)A[q] & ~0xFFu)});
-      sab += __uint_as_float((uint32_t)(B[q] >> 32));
-      if (ta & 1u) incl = true;
+      __nanosleep(64);
+      continue;
     }
-    const uint32_t rmask = __ballot_sync(0xffffffffu, ready);
-    const uint32_t imask = __ballot_sync(0xffffffffu, ready && incl);
-    bool done = false, advance = false;
-    int L = 31;
-    if (imask) {
-      L = __ffs(imask) - 1;                                     // lane holding the nearest inclusive
-      const uint32_t need = (L == 31) ? 0xffffffffu : ((2u << L) - 1u);
-      done = (rmask & need) == need;
-    } else if (rmask == 0xffffffffu) {
-      advance = true;
+    tprog = globaltimer();
+    // this thread's elements, scanned in order; a kind-1 tile restarts the sum
+    DF v[PER];
+    float a[PER];
+    bool f[PER];
+    DF tv = DF{0.0f, 0.0f};
+    float tab = 0.0f;
+    bool tf = false;
+#pragma unroll 1
+    for (int q = 0; q < PER; q++) {
+      if (tid * PER + q < m) {
+        const DF val = status_sum(A[q]);
+        const float ab = status_abs(B[q]);
+        if (A[q] & 1u) { tv = val; tab = ab; tf = true; }
+        else { tv = df_add(tv, val); tab += ab; }
+      }
+      v[q] = tv;
+      a[q] = tab;
+      f[q] = tf;
     }
-    if (!done && !advance) {
-      if (globaltimer() - t0 > kWaitNs) { gave_up = true; done = true; L = -1; }
-      else { __nanosleep(20); continue; }
+    // across the warp, then across the warps (segmented: a head cuts the sum)
+    DF wv = tv;
+    float wab = tab;
+    int wf = tf ? 1 : 0;
+#pragma unroll 1
+    for (int o = 1; o < 32; o <<= 1) {
+      const DF ov = DF{__shfl_up_sync(0xffffffffu, wv.hi, o), __shfl_up_sync(0xffffffffu, wv.lo, o)};
+      const float oa = __shfl_up_sync(0xffffffffu, wab, o);
+      const int of = __shfl_up_sync(0xffffffffu, wf, o);
+      if (lane >= o) {
+        if (!wf) { wv = df_add(ov, wv); wab = oa + wab; }
+        wf |= of;
+      }
     }
-    DF c = (lane <= L) ? sum : DF{0.0f, 0.0f};
-    float ca = (lane <= L) ? sab : 0.0f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      c = df_add(c, shfl_xor_df(c, o));
-      ca += __shfl_xor_sync(0xffffffffu, ca, o);
+    if (lane == 31) { sm.scan_v[warp] = wv; sm.scan_a[warp] = wab; sm.scan_f[warp] = wf; }
+    __syncthreads();
+    DF ev = carry;
+    float eab = carry_abs;
+    for (int w2 = 0; w2 < warp; w2++) {
+      if (sm.scan_f[w2]) { ev = sm.scan_v[w2]; eab = sm.scan_a[w2]; }
+      else { ev = df_add(ev, sm.scan_v[w2]); eab += sm.scan_a[w2]; }
     }
-    run = df_add(run, c);
-    run_abs += ca;
-    if (done) break;
-    j -= 256;
+    {
+      const DF lv = DF{__shfl_up_sync(0xffffffffu, wv.hi, 1), __shfl_up_sync(0xffffffffu, wv.lo, 1)};
+      const float la = __shfl_up_sync(0xffffffffu, wab, 1);
+      const int lf = __shfl_up_sync(0xffffffffu, wf, 1);
+      if (lane >= 1) {
+        if (lf) { ev = lv; eab = la; }
+        else { ev = df_add(ev, lv); eab += la; }
+      }
+    }
+#pragma unroll 1
+    for (int q = 0; q < PER; q++) {
+      const int i = tid * PER + q;
+      if (i >= m) break;
+      const DF inc = f[q] ? v[q] : df_add(ev, v[q]);
+      const float inca = f[q] ? a[q] : eab + a[q];
+      if (!(A[q] & 1u)) publish_status(p.status + 2 * (pos + i), inc, inca, ep, 1);
+      if (i == m - 1) { sm.carry = inc; sm.carry_abs = inca; }
+    }
+    __syncthreads();
+    carry = sm.carry;
+    carry_abs = sm.carry_abs;
+    pos += m;
+    if (tid == 0) atomicAdd(&st[S_SCAN_WINDOWS], 1ull);
+    __syncthreads();
   }
-  if (gave_up && lane == 0) atomicOr(&p.ctr[C_ERR], ERR_PLAN_TIMEOUT);
-  if (lane == 0 && sq_ok(p, t >= 0 && t < p.cap_tiles, 2, t))
-    publish_status(p.status + 2 * t, df_add(run, agg), run_abs + agg_abs, ep, 1);
-  return Prefix{run, run_abs};
+  if (tid == 0) atomicAdd(&st[S_NS_SCAN], tprog - tbegin);
 }
 
 // ---------------------------------------------------------------- lanes
@@ -488,17 +614,31 @@ __device__ __forceinline__ void load_lane(const Params &p, const unsigned char *
   }
 }
 
-// Exact run of a lane's terms under binade e (the general path).
-__device__ __forceinline__ Run lane_run_general(const uint64_t *xs, int nv, int e) {
+// Exact run of a lane's terms under binade e (the general path: ties,
+// signed terms whose bounds need every prefix, binades outside the fast
+// path's range).  Kept out of line, with the lane's terms loaded again, so
+// that the hot path stays small.
+__device__ __noinline__ Run lane_run_general(const Params &p, const unsigned char *stage, bool use_tma,
+                                             int64_t row, int64_t lstart, int nv, int w, int lane, int e) {
+  const bool from_stage = use_tma && row < p.tma_rows;
+  const unsigned char *rp = stage + (w * 32 + lane) * 128;
+  const unsigned long long *gp = reinterpret_cast<const unsigned long long *>(p.x) + lstart;
+  if (!from_stage && !sq_ok(p, nv == 0 || (lstart >= 0 && lstart + nv <= p.n), 3, lstart)) nv = 0;
   Run r = run_empty();
-#pragma unroll
-  for (int i = 0; i < kLaneTerms; i++) {
-    if (i < nv) {
-      int64_t re;
-      int32_t d;
-      const bool poison = term_inc(xs[i], e, re, d);
-      run_push(r, re, d, term_flags(xs[i]) | (poison ? F_POISON : 0u));
+#pragma unroll 1
+  for (int i = 0; i < nv; i++) {
+    uint64_t x;
+    if (from_stage) {
+      // term i of the lane's 128-byte row: 16-byte chunk i/2, swizzled by the row
+      const uint2 v = *reinterpret_cast<const uint2 *>(rp + ((((i >> 1) ^ (lane & 7)) << 4) | ((i & 1) << 3)));
+      x = ((uint64_t)v.y << 32) | v.x;
+    } else {
+      x = __ldg(gp + i);
     }
+    int64_t re;
+    int32_t d;
+    const bool poison = term_inc(x, e, re, d);
+    run_push(r, re, d, term_flags(x) | (poison ? F_POISON : 0u));
   }
   return r;
 }
@@ -583,7 +723,7 @@ __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *st
     orz |= (hi & 0x7FFFFFFFu) | (uint32_t)xs[i];
   }
   float isig = sig, iab = ab;
-#pragma unroll
+#pragma unroll 1
   for (int o = 1; o < 32; o <<= 1) {
     const float a = __shfl_up_sync(0xffffffffu, isig, o);
     const float b = __shfl_up_sync(0xffffffffu, iab, o);
@@ -600,7 +740,7 @@ __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *st
   const bool zl = (orz == 0);
   const bool dirty = !clean && !zl && nv > 0;
   Run r = run_empty();
-  if (!dirty) r = lane_run_general(xs, nv, clean ? e_l : 0);
+  if (!dirty) r = lane_run_general(p, stage, use_tma, row, lstart, nv, w, lane, clean ? e_l : 0);
   const int key = dirty ? kDirtyKey : (clean ? e_l : kZeroE);
   const int ndirty = dirty ? lane_items(p, xs, nv, A, dbase, t, w, lane, nullptr) : 0;
   if (dirty) atomicAdd(&st[S_LANE_DIRTY], 1ull);
@@ -609,7 +749,7 @@ __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *st
   const bool head = (lane == 0) || (nv > 0 && (dirty || pkey == kDirtyKey || key != pkey));
   Run v = r;
   int fl = head ? 1 : 0;
-#pragma unroll
+#pragma unroll 1
   for (int o = 1; o < 32; o <<= 1) {
     const Run ov = shfl_run<SH_UP>(v, o);
     const int of = __shfl_up_sync(0xffffffffu, fl, o);
@@ -622,7 +762,7 @@ __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *st
   const int hkey = __shfl_sync(0xffffffffu, key, hlane);
   // terms before each lane, for the item counts
   int csum = nv;
-#pragma unroll
+#pragma unroll 1
   for (int o = 1; o < 32; o <<= 1) {
     const int vv = __shfl_up_sync(0xffffffffu, csum, o);
     if (lane >= o) csum += vv;
@@ -635,7 +775,7 @@ __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *st
   int ioff = 0, total = 0;
   for (int attempt = 0; attempt < 2; attempt++) {
     ioff = myitems;
-#pragma unroll
+#pragma unroll 1
     for (int o = 1; o < 32; o <<= 1) {
       const int vv = __shfl_up_sync(0xffffffffu, ioff, o);
       if (lane >= o) ioff += vv;
@@ -678,7 +818,11 @@ __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *st
 }
 
 // ---------------------------------------------------------------- phase A: the plan's sums
-__device__ void phase_a(const Params &p, Smem &sm, const unsigned char *stage, int s, int64_t t, int64_t ntiles) {
+// Chunk aggregates of a tile into sm.wa[s].  A plan unit (publish) also
+// publishes them, for the tile's run unit, and the tile's approximate sum --
+// or s0 plus it for the first tile of a sum -- for the scanner.
+__device__ __noinline__ void phase_a(const Params &p, Smem &sm, const unsigned char *stage, int s, int64_t t,
+                                     int64_t ntiles, bool publish) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const TileGeo g = tile_geo(p, t, ntiles);
   const int64_t lstart = g.start + (int64_t)w * kChunkTerms + (int64_t)lane * kLaneTerms;
@@ -686,7 +830,7 @@ __device__ void phase_a(const Params &p, Smem &sm, const unsigned char *stage, i
   uint64_t xs[kLaneTerms];
   load_lane(p, stage, sm.tma[s] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, xs);
   float sig = 0.0f, ab = 0.0f;
-  uint32_t orh = 0, orz = 0, mx = 0, andh = 0xFFFFFFFFu;
+  uint32_t orh = 0, orz = 0, mx = 0;
 #pragma unroll
   for (int i = 0; i < kLaneTerms; i++) {
     const uint32_t hi = (uint32_t)(xs[i] >> 32);
@@ -694,20 +838,9 @@ __device__ void phase_a(const Params &p, Smem &sm, const unsigned char *stage, i
     orh |= hi;
     orz |= mag | (uint32_t)xs[i];
     mx = max(mx, mag);
-    andh &= (i < nv) ? hi : 0xFFFFFFFFu;
-    const float f = approx_term(hi);
+    const float f = approx_term_clamped(hi);
     sig += f;
     ab += fabsf(f);
-  }
-  if (mx >= (1151u << 20)) {                 // a term of 2^128 or more: clamp the images
-    sig = 0.0f;
-    ab = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kLaneTerms; i++) {
-      const float f = approx_term_clamped((uint32_t)(xs[i] >> 32));
-      sig += f;
-      ab += fabsf(f);
-    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -716,20 +849,18 @@ __device__ void phase_a(const Params &p, Smem &sm, const unsigned char *stage, i
     orh |= __shfl_xor_sync(0xffffffffu, orh, o);
     orz |= __shfl_xor_sync(0xffffffffu, orz, o);
     mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    andh &= __shfl_xor_sync(0xffffffffu, andh, o);
   }
-  if (lane == 0) sm.wa[s][w] = WarpAgg{sig, ab, orh, orz, mx, andh};
+  if (lane == 0) sm.wa[s][w] = WarpAgg{sig, ab, mx, ((orh >> 31) ? WA_NEG : 0u) | (orz ? WA_NZ : 0u)};
   __syncthreads();
-  if (w == 0) {
+  if (publish && w == 0) {
+    const bool ok = sq_ok(p, t >= 0 && t < p.cap_tiles, 6, t);
+    if (ok && lane < kWarps) publish_wagg(p.cagg + 2 * (t * kWarps + lane), sm.wa[s][lane], p.epoch);
     DF agg = DF{0.0f, 0.0f};
     float agga = 0.0f;
 #pragma unroll
     for (int k = 0; k < kWarps; k++) { agg = df_addf(agg, sm.wa[s][k].sig); agga += sm.wa[s][k].ab; }
-    if (lane == 0) {
-      sm.agg[s] = agg;
-      sm.agg_abs[s] = agga;
-      if (!sq_ok(p, t >= 0 && t < p.cap_tiles, 6, t)) {
-      } else if (g.tile_in_sum != 0) {
+    if (lane == 0 && ok) {
+      if (g.tile_in_sum != 0) {
         publish_status(p.status + 2 * t, agg, agga, p.epoch, 0);
       } else {                                   // the first tile of a sum: s0 + its sum at once
         const DF ex = df_from_double(p.s0s ? p.s0s[g.sum] : p.s0);
@@ -739,17 +870,50 @@ __device__ void phase_a(const Params &p, Smem &sm, const unsigned char *stage, i
   }
 }
 
+// Warp 0 of a streaming CTA: start copying a run unit's plan words -- its
+// chunk aggregates (lanes 0-7) and the prefix of the tile before it (lane 8)
+// -- into the stage's slots; completed by cp_async_wait_all before the
+// barrier that precedes the unit's runs.
+__device__ __forceinline__ void prefetch_plan(const Params &p, Smem &sm, int s, int64_t t) {
+  const int lane = threadIdx.x & 31;
+  if (lane < kWarps) cp_async16(sm.agg_raw[s][lane], p.cagg + 2 * (t * kWarps + lane));
+  else if (lane == kWarps && t > 0) cp_async16(sm.pre_raw[s], p.status + 2 * (t - 1));
+  cp_async_commit();
+  if (lane == 0) sm.raw_tile[s] = t;
+}
+
 // ---------------------------------------------------------------- phase B: runs of a tile
-__device__ void phase_b(const Params &p, Smem &sm, const unsigned char *stage, int s, int64_t t, int64_t ntiles) {
+__device__ __noinline__ void phase_b(const Params &p, Smem &sm, const unsigned char *stage, int s, int64_t t, int64_t ntiles) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   unsigned long long *st = sm.st;
   const TileGeo g = tile_geo(p, t, ntiles);
-  if (w == 0) {
-    const uint64_t tl = globaltimer();
-    const Prefix pr = lookback(p, g.sum, g.first_tile, t, sm.agg[s], sm.agg_abs[s], st);
-    if (lane == 0) { sm.ex = pr.ex; sm.ex_abs = pr.ex_abs; atomicAdd(&st[S_NS_LOOKBACK], globaltimer() - tl); }
+  // the plan words copied in ahead (else wait for the prefix / form the
+  // chunk aggregates from the tile itself)
+  const bool have = sm.raw_tile[s] == t;
+  bool agg_ok = true;
+  if (tid < kWarps) {
+    WarpAgg a;
+    agg_ok = have && decode_wagg(sm.agg_raw[s][tid][0], sm.agg_raw[s][tid][1], p.epoch, a);
+    if (agg_ok) sm.wa[s][tid] = a;
   }
-  __syncthreads();
+  if (tid == 0) {
+    const uint32_t tag = (p.epoch << 1) | 1u;
+    const uint64_t A = sm.pre_raw[s][0], B = sm.pre_raw[s][1];
+    if (t != g.first_tile && have && (uint32_t)(A & 0xFF) == tag && (uint32_t)B == tag) {
+      sm.ex = status_sum(A);
+      sm.ex_abs = status_abs(B);
+    } else {
+      const uint64_t tl = globaltimer();
+      const Prefix pr = read_prefix(p, g.sum, g.first_tile, t, st);
+      sm.ex = pr.ex;
+      sm.ex_abs = pr.ex_abs;
+      atomicAdd(&st[S_NS_PREFIX_WAIT], globaltimer() - tl);
+    }
+  }
+  if (!__syncthreads_and(agg_ok)) {
+    if (tid == 0) atomicAdd(&st[S_PLAN_LOCAL], 1ull);
+    phase_a(p, sm, stage, s, t, ntiles, false);
+  }
   // ---- plan of this warp's chunk
   DF sc = sm.ex;
   float ac = sm.ex_abs;
@@ -773,16 +937,16 @@ __device__ void phase_b(const Params &p, Smem &sm, const unsigned char *stage, i
   Rec *area = p.items + t * kTileSlots;
   Rec crec;
   int nitems = 0;
-  const bool zero_chunk = (me.orz == 0);
+  const bool zero_chunk = (me.flags & WA_NZ) == 0;
   if (clean || zero_chunk) {
     if (zero_chunk) e = 0;
     const int eb = e + 1023;
     const bool fast = !zero_chunk && e >= -969 && e <= 1023 && (int)(me.mx >> 20) < eb;
     Run r;
-    bool general_reduce = true;
+    bool general = true, general_reduce = true;
     if (fast) {
       const int c = 64 - eb;
-      if ((me.orh >> 31) == 0) {
+      if ((me.flags & WA_NEG) == 0) {
         // non-negative terms: the run is a plain sum of increments
         uint64_t a = 0;
         bool anytie = false;
@@ -798,12 +962,11 @@ __device__ void phase_b(const Params &p, Smem &sm, const unsigned char *stage, i
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
           r.inc = (int64_t)a; r.lo = 0; r.hi = (int64_t)a; r.d = 0; r.flags = F_NONNEG;
-          general_reduce = false;
-        } else if (anytie) {
-          r = lane_run_general(xs, nv, e);
-        } else {
+          general = general_reduce = false;
+        } else if (!anytie) {
           r.inc = (int64_t)a; r.lo = 0; r.hi = (int64_t)a; r.d = 0;
           r.flags = F_NONNEG | (nv == 0 ? (F_NONPOS | F_ZERO | F_ALLNEGZ) : 0u);
+          general = false;
         }
       } else {
         // signed terms: positive and negative increments summed apart give
@@ -821,20 +984,20 @@ __device__ void phase_b(const Params &p, Smem &sm, const unsigned char *stage, i
           anytie |= tie;
           if (i < nv) { orl |= hi; andl &= hi; }
         }
-        if (anytie) {
-          r = lane_run_general(xs, nv, e);
-        } else if (nv == 0) {
-          r = run_empty();
-        } else {
-          r.inc = (int64_t)(P - Nn); r.lo = -(int64_t)Nn; r.hi = (int64_t)P; r.d = 0;
-          r.flags = ((orl >> 31) ? 0u : F_NONNEG) | ((andl >> 31) ? F_NONPOS : 0u);
+        if (!anytie) {
+          if (nv == 0) {
+            r = run_empty();
+          } else {
+            r.inc = (int64_t)(P - Nn); r.lo = -(int64_t)Nn; r.hi = (int64_t)P; r.d = 0;
+            r.flags = ((orl >> 31) ? 0u : F_NONNEG) | ((andl >> 31) ? F_NONPOS : 0u);
+          }
+          general = false;
         }
       }
-    } else {
-      r = lane_run_general(xs, nv, e);
     }
+    if (general) r = lane_run_general(p, stage, sm.tma[s] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, e);
     if (general_reduce) {
-#pragma unroll
+#pragma unroll 1
       for (int off = 1; off < 32; off <<= 1) {
         const Run o = shfl_run<SH_DOWN>(r, off);
         if ((lane & (2 * off - 1)) == 0) r = run_compose(r, o);
@@ -864,51 +1027,61 @@ __device__ void phase_b(const Params &p, Smem &sm, const unsigned char *stage, i
     sm.chunk[w] = crec;
     sm.nitems[w] = nitems;
   }
-  __threadfence();
+  // the items every warp wrote are ordered before the header by this barrier
+  // and the publishing thread's device-scope fence (a fence is cumulative)
   __syncthreads();
-  // ---- the tile's header
-  if (tid == 0) {
-    bool all_run = true;
-    int et = kZeroE;
-    for (int k = 0; k < kWarps; k++) {
-      const Rec &c = sm.chunk[k];
-      if (rec_kind(c.meta) != K_RUN) { all_run = false; break; }
-      if (rec_flags(c.meta) & F_ZERO) continue;
-      if (et == kZeroE) et = c.e;
-      else if (c.e != et) { all_run = false; break; }
-    }
+  // ---- the tile's header (warp 0): one run when every chunk is a run of one
+  // binade (runs of zeros fit any), else the chunks' items in the item area
+  if (w == 0) {
+    const unsigned full = 0xffffffffu;
+    Rec c = make_rec(run_empty(), kZeroE, K_RUN, 0, 0);
+    int n = 0;
+    if (lane < kWarps) { c = sm.chunk[lane]; n = sm.nitems[lane]; }
+    const uint32_t kind = rec_kind(c.meta), flags = rec_flags(c.meta);
+    const bool nz_run = lane < kWarps && kind == K_RUN && !(flags & F_ZERO);
+    const uint32_t nzm = __ballot_sync(full, nz_run);
+    const int et = nzm ? __shfl_sync(full, (int)c.e, __ffs(nzm) - 1) : kZeroE;
+    const bool mixed = lane < kWarps && (kind != K_RUN || (nz_run && c.e != et));
     Rec hd;
-    if (all_run) {
-      Run acc = run_empty();
-      for (int k = 0; k < kWarps; k++) acc = run_compose(acc, rec_run(sm.chunk[k]));
-      hd = make_rec(acc, (acc.flags & F_ZERO) ? kZeroE : et, K_RUN, (uint32_t)(g.end - g.start), 0);
-    } else {
-      uint64_t packed = 0;
-      uint32_t orf = 0;
-      for (int k = 0; k < kWarps; k++) {
-        const Rec &c = sm.chunk[k];
-        int n = sm.nitems[k];
-        if (rec_kind(c.meta) == K_RUN) {
-          if (c.count > 0) {
-            if (item_ok(p, area + k * kChunkSlots, 8)) stcg_rec(area + k * kChunkSlots, c);
-            n = 1;
-          }
-          else n = 0;
-        }
-        orf |= rec_flags(c.meta);
-        packed |= (uint64_t)(uint32_t)n << (kCountBits * k);
+    if (__ballot_sync(full, mixed) == 0) {
+      Run r = rec_run(c);
+#pragma unroll
+      for (int off = 1; off < kWarps; off <<= 1) {
+        const Run o = shfl_run<SH_DOWN>(r, off);
+        if ((lane & (2 * off - 1)) == 0) r = run_compose(r, o);
       }
+      // the header alone holds the tile: nothing to order before it
+      hd = make_rec(r, (r.flags & F_ZERO) ? kZeroE : et, K_RUN, (uint32_t)(g.end - g.start), 0);
+    } else {
+      if (lane < kWarps && kind == K_RUN) {
+        n = 0;
+        if (c.count > 0) {
+          if (item_ok(p, area + lane * kChunkSlots, 8)) stcg_rec(area + lane * kChunkSlots, c);
+          n = 1;
+        }
+      }
+      const uint64_t mine = (lane < kWarps) ? (uint64_t)(uint32_t)n << (kCountBits * lane) : 0ull;
+      const uint64_t packed = ((uint64_t)__reduce_or_sync(full, (uint32_t)(mine >> 32)) << 32) |
+                              __reduce_or_sync(full, (uint32_t)mine);
+      const uint32_t orf = __reduce_or_sync(full, lane < kWarps ? flags : 0u);
       Run z = run_empty();
       z.inc = (int64_t)packed;
       z.flags = orf & (F_HASINF_P | F_HASINF_N | F_HASNAN);
       hd = make_rec(z, 0, K_COMPLEX, (uint32_t)(g.end - g.start), 0);
       hd.inc = (int64_t)packed;
-      atomicAdd(&st[S_TILE_COMPLEX], 1ull);
+      __syncwarp();
+      // the items (written before the tile barrier, and by this warp) are
+      // ordered before the header by this device-scope fence
+      if (lane == 0) {
+        __threadfence();
+        atomicAdd(&st[S_TILE_COMPLEX], 1ull);
+      }
     }
-    __threadfence();
-    if (sq_ok(p, t >= 0 && t < p.cap_tiles, 9, t)) publish_header(p.hdr + t, hd, (p.epoch << 1) | 1u);
-    atomicMax(&p.stats[S_T_STREAM_END], (unsigned long long)globaltimer());
-    atomicAdd(&st[S_TILES], 1ull);
+    if (lane == 0) {
+      if (sq_ok(p, t >= 0 && t < p.cap_tiles, 9, t)) publish_header(p.hdr + t, hd, (p.epoch << 1) | 1u);
+      atomicMax(&p.stats[S_T_STREAM_END], (unsigned long long)globaltimer());
+      atomicAdd(&st[S_TILES], 1ull);
+    }
   }
 }
 
@@ -930,6 +1103,7 @@ __device__ __forceinline__ uint64_t absorb(uint64_t Sb, uint32_t flags) {
 // ends with the same S.  One __dadd_rn per term, in index order.
 __device__ uint64_t add_terms(const Params &p, uint64_t Sb, int64_t a, int64_t cnt, unsigned long long *st) {
   const int lane = threadIdx.x & 31;
+  const uint64_t t0 = globaltimer();
   double S = bitsd(Sb);
   if (!sq_ok(p, a >= 0 && a + cnt <= p.n, 10, a)) cnt = 0;
   for (int64_t base = 0; base < cnt; base += 32) {
@@ -937,7 +1111,10 @@ __device__ uint64_t add_terms(const Params &p, uint64_t Sb, int64_t a, int64_t c
     const int m = (int)min((int64_t)32, cnt - base);
     for (int j = 0; j < m; j++) S = __dadd_rn(S, __shfl_sync(0xffffffffu, v, j));
   }
-  if (lane == 0) atomicAdd(&st[S_TERMS_ADDED], (unsigned long long)cnt);
+  if (lane == 0) {
+    atomicAdd(&st[S_TERMS_ADDED], (unsigned long long)cnt);
+    atomicAdd(&st[S_NS_WALK_ADDS], globaltimer() - t0);
+  }
   return dbits(S);
 }
 
@@ -945,8 +1122,8 @@ __device__ __forceinline__ bool elem_alone(const Rec &q) { return rec_kind(q.met
 
 // Self-checking builds keep a trace of the walk: per serial step the term
 // range [a, b) it covered, what it was, and the running sum after it.
-constexpr int kDbgWords = 16384;
 #ifdef SEQSUM_CHECKS
+constexpr int kDbgWords = 16384;
 __device__ __forceinline__ void walk_trace(const Params &p, int64_t a, int64_t b, uint32_t what, uint64_t Sb) {
   const unsigned long long r = atomicAdd(&p.dbg[0], 1ull);
   if (1 + 4 * (r + 1) <= (unsigned long long)kDbgWords) {
@@ -1031,7 +1208,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
     int mine = 0, wbase = 0, incl = 0;
     for (int pass = 0; pass < 2; pass++) {
       mine = 0;
-#pragma unroll
+#pragma unroll 1
       for (int q = 0; q < BT; q++) {
         const int i = tid * BT + q;
         int c = 0;
@@ -1049,6 +1226,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         mine += c;
       }
       incl = mine;
+#pragma unroll 1
       for (int o = 1; o < 32; o <<= 1) {
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
@@ -1060,7 +1238,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       for (int w = 0; w < warp; w++) wbase += sm.wcnt[w];
       if (pass == 1) break;
       int off = wbase + incl - mine;
-#pragma unroll
+#pragma unroll 1
       for (int q = 0; q < BT; q++) {
         const int i = tid * BT + q;
         if (i < m && off + cnt[q] > kWalkElems) atomicMin(&sm.m, i);
@@ -1069,11 +1247,13 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       __syncthreads();
       m = sm.m;
     }
+    uint64_t tsec = 0;
+    if (tid == 0) { tsec = globaltimer(); atomicAdd(&st[S_NS_WALK_COUNT], tsec - t_work0); }
     // ---- 3. the flat element list: simple tiles by their thread; the items
     //         of complex tiles by the whole block, one item per thread
     {
       int off = wbase + incl - mine;
-#pragma unroll
+#pragma unroll 1
       for (int q = 0; q < BT; q++) {
         const int i = tid * BT + q;
         if (i >= m) break;
@@ -1132,6 +1312,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
     }
 #endif
     const int nel = min(sm.nel, kWalkElems);
+    if (tid == 0) { const uint64_t t2 = globaltimer(); atomicAdd(&st[S_NS_WALK_GATHER], t2 - tsec); tsec = t2; }
     // ---- 4. segmented scan and serial application (restarted after a rejected run)
     int from = 0;
     while (from < nel) {
@@ -1149,7 +1330,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       bool has_head = false;
       int first_head = B;
       Run incls[B];
-#pragma unroll
+#pragma unroll 1
       for (int jj = 0; jj < B; jj++) {
         const int i = tid * B + jj;
         incls[jj] = run_empty();
@@ -1161,6 +1342,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       }
       Run v = agg;
       int f = has_head ? 1 : 0;
+#pragma unroll 1
       for (int o = 1; o < 32; o <<= 1) {
         const Run ov = shfl_run<SH_UP>(v, o);
         const int of = __shfl_up_sync(0xffffffffu, f, o);
@@ -1169,6 +1351,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       if (lane == 31) { sm.wagg[warp] = v; sm.wflag[warp] = f; }
       __syncthreads();
       Run ex = run_empty();
+#pragma unroll 1
       for (int w = 0; w < warp; w++) {
         if (sm.wflag[w]) ex = sm.wagg[w];
         else ex = run_compose(ex, sm.wagg[w]);
@@ -1178,18 +1361,19 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         const int lf = __shfl_up_sync(0xffffffffu, f, 1);
         if (lane >= 1) { if (lf) ex = lv; else ex = run_compose(ex, lv); }
       }
-#pragma unroll
+#pragma unroll 1
       for (int jj = 0; jj < B; jj++)
         if (jj < first_head) incls[jj] = run_compose(ex, incls[jj]);
       // segment ends, compacted in order, with their composites
       int my = 0;
       int idx[B];
-#pragma unroll
+#pragma unroll 1
       for (int jj = 0; jj < B; jj++) {
         const int i = tid * B + jj;
         if (i >= from && i < nel && (i == nel - 1 || head[i + 1])) idx[my++] = jj;
       }
       int inc2 = my;
+#pragma unroll 1
       for (int o = 1; o < 32; o <<= 1) {
         const int vv = __shfl_up_sync(0xffffffffu, inc2, o);
         if (lane >= o) inc2 += vv;
@@ -1199,7 +1383,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       int eb2 = 0;
       for (int w = 0; w < warp; w++) eb2 += sm.wcnt[w];
       const int epos = eb2 + inc2 - my;
-#pragma unroll
+#pragma unroll 1
       for (int jj = 0; jj < B; jj++) {
         if (jj >= my) break;
         const int i = tid * B + idx[jj];
@@ -1210,12 +1394,14 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       }
       if (tid == kThreads - 1) sm.nseg = epos + my;
       __syncthreads();
+      if (tid == 0) { const uint64_t t2 = globaltimer(); atomicAdd(&st[S_NS_WALK_SCAN], t2 - tsec); tsec = t2; }
       // ---- serial part on warp 0
+#ifdef SEQSUM_CHECKS
       auto abs_start = [&](int j) -> int64_t {
         const uint32_t ep = elpos[j];
         return tile_geo(p, pos + (ep >> 12), ntiles).start + (ep & 0xFFF);
       };
-      (void)abs_start;
+#endif
       if (warp == 0) {
         uint64_t Sb = sm.S;
         int restart = -1;
@@ -1233,6 +1419,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
             continue;
           }
           if (kind == K_TERMS) {
+            const uint64_t ta0 = globaltimer();
             const Rec q = el[ei];
             double S = bitsd(Sb);
             const int nt = (int)q.count;
@@ -1240,7 +1427,10 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
             if (nt > 1) S = __dadd_rn(S, bitsd((uint64_t)q.lo));
             if (nt > 2) S = __dadd_rn(S, bitsd((uint64_t)q.hi));
             Sb = dbits(S);
-            if (lane == 0) atomicAdd(&st[S_TERMS_ADDED], (unsigned long long)nt);
+            if (lane == 0) {
+              atomicAdd(&st[S_TERMS_ADDED], (unsigned long long)nt);
+              atomicAdd(&st[S_NS_WALK_ADDS], globaltimer() - ta0);
+            }
             WALK_TRACE(abs_start(ei), abs_start(ei) + nt, 2u, Sb);
             segstart = ei + 1;
             continue;
@@ -1274,7 +1464,8 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
           for (int c0 = segstart; c0 <= ei; c0 += 32) {
             const int i = c0 + lane;
             Run r = (i <= ei) ? rec_run(el[i]) : run_empty();
-            for (int o = 1; o < 32; o <<= 1) {
+      #pragma unroll 1
+      for (int o = 1; o < 32; o <<= 1) {
               const Run ov = shfl_run<SH_UP>(r, o);
               if (lane >= o) r = run_compose(ov, r);
             }
@@ -1318,7 +1509,13 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
           if (kfail < ei) { restart = kfail + 1; break; }
           segstart = ei + 1;
         }
-        if (lane == 0) { sm.S = Sb; sm.restart = restart; }
+        if (lane == 0) {
+          sm.S = Sb;
+          sm.restart = restart;
+          const uint64_t t2 = globaltimer();
+          atomicAdd(&st[S_NS_WALK_SERIAL], t2 - tsec);
+          tsec = t2;
+        }
       }
       __syncthreads();
       const int rs = sm.restart;
@@ -1353,16 +1550,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int s = 0; s < kStages; s++) mbar_init(&sm.bar[s], 1);
     fence_mbar_init();
     if (blockIdx.x == 0) p.stats[S_T_START] = globaltimer();
+    // roles go to CTAs in the order they start, so every waiting role is
+    // held by a running CTA
+    sm.role = (int)atomicAdd(&p.ctr[C_ROLE], 1u);
   }
   __syncthreads();
+  const int role = sm.role;
 
-  if ((int)blockIdx.x < p.nwalkers) {
+  if (role < p.nwalkers) {
     // ---------------- walker CTA
     if (p.offsets == nullptr) {
-      if (blockIdx.x == 0) {
-        if (ntiles == 0) { if (tid == 0) p.outs[0] = p.s0; }
-        else walk_sum(p, sm, dyn, 0, 0, ntiles, ntiles);
-      }
+      if (ntiles == 0) { if (tid == 0) p.outs[0] = p.s0; }
+      else walk_sum(p, sm, dyn, 0, 0, ntiles, ntiles);
     } else {
       while (true) {
         if (tid == 0) sm.sum_k = (int)atomicAdd(&p.ctr[C_SUMTICKET], 1u);
@@ -1375,13 +1574,25 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (te > tb) walk_sum(p, sm, dyn, k, tb, te, ntiles);
       }
     }
+  } else if (role == p.nwalkers) {
+    // ---------------- the plan's prefix scanner
+    if (ntiles > 0) scan_prefix(p, sm, ntiles);
   } else {
-    // ---------------- streaming CTA: copy of i+2 | plan of i+1 | runs of i
+    // ---------------- streaming CTA: copy of unit i+2 | unit i+1: a plan
+    // unit's aggregates, or a run unit's plan words copied in | runs of unit i
+    const int warp = tid >> 5;
+    const int64_t nunits = 2 * ntiles;
+    uint32_t u_next = 0;                                 // thread 0: the next ticket, taken one issue ahead
     auto issue = [&](int s) {                            // thread 0
-      const int64_t t = (int64_t)atomicAdd(&p.ctr[C_TICKET], 1u);
-      sm.tk[s] = t;
+      const int64_t u = (int64_t)u_next;
+      u_next = atomicAdd(&p.ctr[C_TICKET], 1u);          // used at the next issue: its latency overlaps
       sm.tma[s] = 0;
-      if (t >= ntiles || p.tma_rows == 0) return;
+      sm.plan[s] = 0;
+      if (u >= nunits) { sm.tk[s] = ntiles; return; }    // no units left
+      int64_t t;
+      sm.plan[s] = unit_of(u, ntiles, p.wave, t) ? 1 : 0;
+      sm.tk[s] = t;
+      if (p.tma_rows == 0) return;
       const TileGeo g = tile_geo(p, t, ntiles);
       if ((g.start & 15) != 0) return;
       fence_proxy_async();
@@ -1400,11 +1611,21 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (tid == 0) atomicAdd(&sm.st[S_NS_TMA_WAIT], globaltimer() - t0);
       }
     };
-    if (tid == 0) { issue(0); issue(1); }
+    if (tid < kStages) sm.raw_tile[tid] = -1;
+    if (tid == 0) {
+      u_next = atomicAdd(&p.ctr[C_TICKET], 1u);
+      issue(0);
+      issue(1);
+    }
     __syncthreads();
     if (sm.tk[0] < ntiles) {
       wait_stage(0);
-      phase_a(p, sm, dyn, 0, sm.tk[0], ntiles);
+      if (sm.plan[0]) {
+        phase_a(p, sm, dyn, 0, sm.tk[0], ntiles, true);
+      } else if (warp == 0) {
+        prefetch_plan(p, sm, 0, sm.tk[0]);
+        cp_async_wait_all();
+      }
     }
     __syncthreads();
     for (int i = 0;; i++) {
@@ -1412,21 +1633,29 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int64_t t = sm.tk[s];
       if (t >= ntiles) break;
       const int64_t t1 = sm.tk[s1];
+      const bool run_s = sm.plan[s] == 0, plan_s1 = sm.plan[s1] != 0;
       __syncthreads();
       if (tid == 0) {
         if (t1 < ntiles) issue(s2);
-        else { sm.tk[s2] = ntiles; sm.tma[s2] = 0; }
+        else { sm.tk[s2] = ntiles; sm.tma[s2] = 0; sm.plan[s2] = 0; }
       }
       if (t1 < ntiles) {
         wait_stage(s1);
-        const uint64_t ta = globaltimer();
-        phase_a(p, sm, dyn + s1 * kStageBytes, s1, t1, ntiles);
-        if (tid == 0) atomicAdd(&sm.st[S_NS_PHASE_A], globaltimer() - ta);
+        if (plan_s1) {
+          const uint64_t ta = globaltimer();
+          phase_a(p, sm, dyn + s1 * kStageBytes, s1, t1, ntiles, true);
+          if (tid == 0) atomicAdd(&sm.st[S_NS_PHASE_A], globaltimer() - ta);
+        } else if (warp == 0) {
+          prefetch_plan(p, sm, s1, t1);
+        }
       }
       __syncthreads();
-      const uint64_t tb = globaltimer();
-      phase_b(p, sm, dyn + s * kStageBytes, s, t, ntiles);
-      if (tid == 0) atomicAdd(&sm.st[S_NS_PHASE_B], globaltimer() - tb);
+      if (run_s) {
+        const uint64_t tb = globaltimer();
+        phase_b(p, sm, dyn + s * kStageBytes, s, t, ntiles);
+        if (tid == 0) atomicAdd(&sm.st[S_NS_PHASE_B], globaltimer() - tb);
+      }
+      if (warp == 0) cp_async_wait_all();                // unit i+1's plan words have landed
       __syncthreads();
     }
   }
@@ -1439,6 +1668,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (atomicAdd(&p.ctr[C_EXIT], 1u) + 1 == gridDim.x) {
       p.ctr[C_TICKET] = 0;
       p.ctr[C_SUMTICKET] = 0;
+      p.ctr[C_ROLE] = 0;
       p.ctr[C_EXIT] = 0;
       __threadfence();
     }
