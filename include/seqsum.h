@@ -104,10 +104,10 @@ typedef struct {
   int64_t tiles_complex;     /* tiles the walk descended into */
   int64_t scan_windows;      /* windows of tile sums the plan's prefix scanner took */
   int64_t walk_batches;      /* batches of tile headers the walk took */
-  int64_t ns_tma_wait;       /* nanoseconds, summed over CTAs: waiting for tile copies */
+  int64_t ns_tma_wait;       /* nanoseconds, summed over CTAs: compute warps waiting for a unit */
   int64_t ns_prefix_wait;    /* ... run units waiting for the plan's prefix of their tile */
-  int64_t ns_phase_a;        /* ... forming the plan's sums */
-  int64_t ns_phase_b;        /* ... forming runs (the prefix wait included) */
+  int64_t ns_phase_a;        /* ... compute warps on plan units */
+  int64_t ns_phase_b;        /* ... compute warps on run units (the prefix wait included) */
   int64_t ns_walk_wait;      /* ... the walk waiting for tile headers */
   int64_t ns_walk_work;      /* ... the walk working */
   int64_t torn_header_reads; /* tile-header reads that saw words of two publications (retried) */
@@ -118,7 +118,9 @@ typedef struct {
   int64_t ns_walk_scan;      /* ... composing same-binade segments in parallel */
   int64_t ns_walk_serial;    /* ... the in-order pass over the segments */
   int64_t ns_walk_adds;      /* ... of which term-by-term fp64 adds */
-  int64_t plan_local;        /* run units that formed their chunk aggregates themselves */
+  int64_t plan_local;        /* tiles whose prefix range spans two binades (planned chunk by chunk) */
+  int64_t ns_ctrl_wait;      /* nanoseconds, summed: control warps waiting for their compute warps */
+  int64_t ns_scan_wait;      /* nanoseconds: the prefix scanner waiting for tiles' sums */
   int64_t t_stream_ns;       /* latest call: kernel start to the last tile header */
   int64_t t_walk_tail_ns;    /* latest call: last tile header to the end of the walk */
   int64_t t_total_ns;        /* latest call: kernel start to the end of the walk */
@@ -127,6 +129,10 @@ typedef struct {
   int32_t check_site;        /* self-checking builds: first failed check (0: none) */
   int32_t check_pad;
   int64_t check_value;       /* self-checking builds: the value that failed it */
+  int32_t timeout_site;      /* first bounded device wait that gave up (0: none) and its context */
+  int32_t timeout_pad;
+  int64_t timeout_a;
+  int64_t timeout_b;
 } seqsum_stats;
 
 /* Waits for the stream of the most recent call, copies its workspace's

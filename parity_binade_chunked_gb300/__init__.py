@@ -34,9 +34,11 @@ class _Stats(ctypes.Structure):
         "runs_rejected", "terms_added", "items", "pool_overflow", "tiles_complex",
         "scan_windows", "walk_batches", "ns_tma_wait", "ns_prefix_wait", "ns_phase_a", "ns_phase_b",
         "ns_walk_wait", "ns_walk_work", "torn_header_reads", "torn_status_reads", "ns_scan", "ns_walk_count", "ns_walk_gather",
-        "ns_walk_scan", "ns_walk_serial", "ns_walk_adds", "plan_local", "t_stream_ns", "t_walk_tail_ns", "t_total_ns")] + [
+        "ns_walk_scan", "ns_walk_serial", "ns_walk_adds", "plan_local", "ns_ctrl_wait", "ns_scan_wait", "t_stream_ns", "t_walk_tail_ns", "t_total_ns")] + [
         ("device_status", ctypes.c_int32), ("device_error_bits", ctypes.c_int32),
-        ("check_site", ctypes.c_int32), ("check_pad", ctypes.c_int32), ("check_value", ctypes.c_int64)]
+        ("check_site", ctypes.c_int32), ("check_pad", ctypes.c_int32), ("check_value", ctypes.c_int64),
+        ("timeout_site", ctypes.c_int32), ("timeout_pad", ctypes.c_int32), ("timeout_a", ctypes.c_int64),
+        ("timeout_b", ctypes.c_int64)]
 
 
 def lib():

@@ -25,7 +25,7 @@ struct Workspace {
   cudaStream_t stream = nullptr;
   int64_t cap_tiles = 0, cap_sums = 0;
   uint64_t *status = nullptr;        // the plan's prefix words, 2 per tile
-  uint64_t *cagg = nullptr;          // the plan's chunk aggregates, 2 words per chunk
+  uint64_t *tagg = nullptr;          // the plan's tile sums, 2 words per tile
   Rec *hdr = nullptr;                // one header per tile
   Rec *items = nullptr;              // kTileSlots items per tile
   uint32_t *ctr = nullptr;
@@ -57,11 +57,11 @@ int cuda_fail(cudaError_t e) {
 
 void ws_free(Workspace *w) {
   cudaFree(w->status);
-  cudaFree(w->cagg);
+  cudaFree(w->tagg);
   cudaFree(w->hdr);
   cudaFree(w->items);
   cudaFree(w->tile_begin);
-  w->status = w->cagg = nullptr;
+  w->status = w->tagg = nullptr;
   w->hdr = w->items = nullptr;
   w->tile_begin = nullptr;
   w->cap_tiles = w->cap_sums = 0;
@@ -94,7 +94,7 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
     const int64_t cs = sums > w->cap_sums ? sums + 16 : w->cap_sums;
     ws_free(w);
     if (cudaMalloc(&w->status, ct * 2 * sizeof(uint64_t)) != cudaSuccess ||
-        cudaMalloc(&w->cagg, ct * sq::kWarps * 2 * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMalloc(&w->tagg, ct * 2 * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&w->hdr, ct * sizeof(Rec)) != cudaSuccess ||
         cudaMalloc(&w->items, ct * sq::kTileSlots * sizeof(Rec)) != cudaSuccess ||
         cudaMalloc(&w->tile_begin, (cs + 1) * sizeof(int64_t)) != cudaSuccess) {
@@ -103,7 +103,7 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
       return SEQSUM_ENOMEM;
     }
     cudaMemset(w->status, 0, ct * 2 * sizeof(uint64_t));
-    cudaMemset(w->cagg, 0, ct * sq::kWarps * 2 * sizeof(uint64_t));
+    cudaMemset(w->tagg, 0, ct * 2 * sizeof(uint64_t));
     cudaMemset(w->hdr, 0, ct * sizeof(Rec));
     w->cap_tiles = ct;
     w->cap_sums = cs;
@@ -124,10 +124,10 @@ int ensure_device_info() {
   }
   if (g_blocks_per_sm == 0) g_blocks_per_sm = sq::kernel_max_blocks_per_sm();
   if (g_wave == 0) {
-    // 1024 tiles (32 MB): more than the units a full grid holds in flight,
-    // so a run unit finds its prefix published, and little enough that the
-    // tile is still in L2 when its run unit reads it again.
-    g_wave = 1024;
+    // 2048 tiles (64 MB): far more than the units a full grid holds in
+    // flight, so the scanner is well ahead of the run units, and little
+    // enough that a tile is still in L2 (129 MB) when its run unit reads it.
+    g_wave = 2048;
     const char *ev = getenv("SEQSUM_WAVE");
     if (ev && atoll(ev) > 0) g_wave = atoll(ev);
   }
@@ -141,14 +141,14 @@ int ensure_device_info() {
   return SEQSUM_OK;
 }
 
-// Next epoch for the tags (1..127); every tagged word (the plan's prefix and
-// chunk aggregates, the tile headers) is cleared whenever the tag wraps, so a
+// Next epoch for the tags (1..127); every tagged word (the plan's prefixes
+// and tile sums, the tile headers) is cleared whenever the tag wraps, so a
 // stale word can never carry a current tag.
 void next_epoch(Workspace *w, cudaStream_t stream) {
   w->epoch++;
   if (w->epoch > 127) {
     cudaMemsetAsync(w->status, 0, w->cap_tiles * 2 * sizeof(uint64_t), stream);
-    cudaMemsetAsync(w->cagg, 0, w->cap_tiles * sq::kWarps * 2 * sizeof(uint64_t), stream);
+    cudaMemsetAsync(w->tagg, 0, w->cap_tiles * 2 * sizeof(uint64_t), stream);
     cudaMemsetAsync(w->hdr, 0, w->cap_tiles * sizeof(Rec), stream);
     w->epoch = 1;
   }
@@ -175,7 +175,7 @@ int64_t tensor_map(Workspace *w, const double *x, int64_t n_total) {
 
 void fill_ws(Params &p, Workspace *w) {
   p.status = w->status;
-  p.cagg = w->cagg;
+  p.tagg = w->tagg;
   p.hdr = w->hdr;
   p.items = w->items;
   p.ctr = w->ctr;
@@ -304,6 +304,10 @@ int seqsum_get_stats(seqsum_stats *st) {
   const uint32_t err = (e == cudaSuccess) ? c[sq::C_ERR] : 0u;
   if (e == cudaSuccess && err) e = cudaMemset(w->ctr + sq::C_ERR, 0, sizeof(uint32_t));
   if (e == cudaSuccess && c[sq::C_CHECK_SITE]) e = cudaMemset(w->ctr + sq::C_CHECK_SITE, 0, 3 * sizeof(uint32_t));
+  if (e == cudaSuccess && c[sq::C_TO_SITE]) e = cudaMemset(w->ctr + sq::C_TO_SITE, 0, 3 * sizeof(uint32_t));
+  st->timeout_site = (int32_t)c[sq::C_TO_SITE];
+  st->timeout_a = (int64_t)c[sq::C_TO_A];
+  st->timeout_b = (int64_t)c[sq::C_TO_B];
   st->check_site = (int32_t)c[sq::C_CHECK_SITE];
   st->check_value = (int64_t)(((uint64_t)c[sq::C_CHECK_HI] << 32) | c[sq::C_CHECK_LO]);
   cudaSetDevice(prev);
@@ -336,6 +340,8 @@ int seqsum_get_stats(seqsum_stats *st) {
   st->ns_walk_serial = (int64_t)s[sq::S_NS_WALK_SERIAL];
   st->ns_walk_adds = (int64_t)s[sq::S_NS_WALK_ADDS];
   st->plan_local = (int64_t)s[sq::S_PLAN_LOCAL];
+  st->ns_ctrl_wait = (int64_t)s[sq::S_NS_CTRL_WAIT];
+  st->ns_scan_wait = (int64_t)s[sq::S_NS_SCAN_WAIT];
   st->t_stream_ns = (int64_t)(s[sq::S_T_STREAM_END] - s[sq::S_T_START]);
   st->t_walk_tail_ns = (int64_t)(s[sq::S_T_WALK1] - s[sq::S_T_STREAM_END]);
   st->t_total_ns = (int64_t)(s[sq::S_T_WALK1] - s[sq::S_T_START]);

@@ -8,7 +8,8 @@ namespace sq {
 // ---- geometry (a lane owns one 128-byte row of 16 consecutive terms)
 constexpr int kLaneTerms = 16;
 constexpr int kWarps = 8;                       // warps per CTA = chunks per tile
-constexpr int kThreads = kWarps * 32;
+constexpr int kThreads = kWarps * 32;           // compute threads of a CTA (the walker's and scanner's width)
+constexpr int kBlockThreads = kThreads + 32;    // + the control warp of a streaming CTA
 constexpr int kChunkTerms = 32 * kLaneTerms;    // 512 terms: one warp's chunk
 constexpr int kTileTerms = kWarps * kChunkTerms;// 4096 terms = 32 KB: one TMA box
 constexpr int kStages = 3;                      // copy of tile i+2 | plan of i+1 | runs of i
@@ -61,6 +62,9 @@ enum : int {
   C_CHECK_SITE = 8,  // self-checking builds: first failed check and its value
   C_CHECK_LO = 9,
   C_CHECK_HI = 10,
+  C_TO_SITE = 11,    // first bounded wait that gave up: its site and two words of context
+  C_TO_A = 12,
+  C_TO_B = 13,
   C_COUNT = 16
 };
 enum : uint32_t {
@@ -81,7 +85,9 @@ enum : int {
   S_TORN_HEADER,       // header reads that mixed words of two publications (retried)
   S_TORN_STATUS,       // prefix reads that mixed words of two publications (retried)
   S_NS_SCAN,           // the scanner's time from its first to its last window
-  S_PLAN_LOCAL,        // run units whose chunk aggregates were not published in time (formed locally)
+  S_PLAN_LOCAL,        // run units whose tile spans two binades (planned chunk by chunk)
+  S_NS_CTRL_WAIT,      // control warps waiting for their compute warps
+  S_NS_SCAN_WAIT,      // the scanner waiting for tiles' sums to be published
   // the walk's work by section (nanoseconds): counting a batch's elements,
   // gathering them, the segmented scan, the in-order pass, and within that
   // pass the term-by-term adds
@@ -111,7 +117,7 @@ struct Params {
   int32_t pad;
   // workspace
   uint64_t *status;            // 2 words per tile: tagged approximate prefix
-  uint64_t *cagg;              // 2 words per chunk: tagged chunk aggregates of the plan
+  uint64_t *tagg;              // 2 words per tile: its own approximate sum (tagged like status)
   Rec *hdr;                    // one header per tile
   Rec *items;                  // kTileSlots items per tile
   uint32_t *ctr;               // C_COUNT counters

@@ -35,6 +35,7 @@
 // walk is one __dadd_rn, in index order.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "binade_math.cuh"
@@ -114,6 +115,49 @@ __device__ __forceinline__ void ld_vol_v2(const void *p, uint64_t &a, uint64_t &
 }
 __device__ __forceinline__ void st_vol_v2(void *p, uint64_t a, uint64_t b) {
   asm volatile("st.volatile.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+
+// Named barrier kBarWide: the 256 threads of a walking or scanning CTA (its
+// control warp takes no part).  Streaming CTAs synchronise through mbarriers
+// only, every wait bounded.
+constexpr int kBarWide = 1;
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void wide_sync() { named_sync(kBarWide, kThreads); }
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// A bounded wait gave up: set its error bit and keep the first such site
+// with two words of context for the host.
+enum : uint32_t {
+  TO_FULL = 1, TO_DONE = 2, TO_SUMS = 3, TO_PREFIX = 4, TO_TILESUM = 5, TO_SCAN = 6, TO_WALK = 7
+};
+__device__ __noinline__ void note_timeout(const Params &p, uint32_t err, uint32_t site, uint32_t a, uint32_t b) {
+  atomicOr(&p.ctr[C_ERR], err);
+  if (atomicCAS(&p.ctr[C_TO_SITE], 0u, site) == 0u) {
+    p.ctr[C_TO_A] = a;
+    p.ctr[C_TO_B] = b;
+  }
+}
+// A bounded wait on an mbarrier phase; false on timeout.
+__device__ __forceinline__ bool mbar_wait(const Params &p, uint64_t *bar, uint32_t parity, uint32_t err,
+                                          uint32_t site, uint32_t a, uint32_t b) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitNs) {
+      note_timeout(p, err, site, a, b);
+      return false;
+    }
+  }
+  return true;
+}
+
+// the barrier's phase waits, besides its arrivals, for every earlier
+// cp.async of this thread
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // 16-byte asynchronous copy global -> shared through L2 (the prefetch of a
@@ -348,47 +392,32 @@ __device__ __forceinline__ TileGeo tile_geo(const Params &p, int64_t t, int64_t 
 }
 
 // ---------------------------------------------------------------- shared memory
-// A chunk's aggregates for the plan: the sum and |x| sum of the terms' fp32
-// images, the largest magnitude word, and whether any term has its sign bit
-// set or any term is non-zero.  Published by plan units as two tagged words
-//   w0 = sig bits << 32 | (ab bits with the low 8 bits replaced by the tag)
-//   w1 = mx << 32 | flags << 8 | tag,   tag = the call's epoch.
+// A chunk's aggregates: the sum and |x| sum of its terms' fp32 images (the
+// plan), the largest magnitude word and whether any term has its sign bit set
+// or any term is non-zero (the exact preconditions of the fast runs).
 enum : uint32_t { WA_NEG = 1u, WA_NZ = 2u };
 struct WarpAgg {
   float sig, ab;
   uint32_t mx, flags;
 };
-__device__ __forceinline__ void publish_wagg(uint64_t *dst, const WarpAgg &a, uint32_t tag) {
-  const uint64_t w0 = ((uint64_t)__float_as_uint(a.sig) << 32) | ((__float_as_uint(a.ab) & ~0xFFu) | tag);
-  const uint64_t w1 = ((uint64_t)a.mx << 32) | ((a.flags & 0xFFu) << 8) | tag;
-  st_vol_v2(dst, w0, w1);
-}
-__device__ __forceinline__ bool decode_wagg(uint64_t w0, uint64_t w1, uint32_t tag, WarpAgg &a) {
-  if ((uint32_t)(w0 & 0xFF) != tag || (uint32_t)(w1 & 0xFF) != tag) return false;
-  a.sig = __uint_as_float((uint32_t)(w0 >> 32));
-  a.ab = __uint_as_float((uint32_t)w0 & ~0xFFu);
-  a.mx = (uint32_t)(w1 >> 32);
-  a.flags = ((uint32_t)w1 >> 8) & 0xFFu;
-  return true;
-}
 
 struct Smem {
-  uint64_t bar[kStages];
-  int64_t tk[kStages];
-  int tma[kStages];
-  int plan[kStages];                // the stage holds a plan unit (else a run unit)
+  uint64_t full[kStages];           // streaming: the unit's copy and plan words landed
+  uint64_t done[kStages];           // streaming: the compute warps finished the unit
+  uint64_t sums[kStages];           // streaming: the compute warps' chunk sums (a tile planned chunk by chunk)
+  int64_t tk[kStages];              // the stage's tile
+  int tma[kStages];                 // its terms came by TMA (else from global memory)
+  int kind[kStages];                // U_PLAN, U_RUN or U_END
   int role;
-  // a run unit's plan words, copied in ahead of its runs: the chunk
-  // aggregates and the prefix of the tile before, for tile raw_tile
-  uint64_t agg_raw[kStages][kWarps][2];
-  uint64_t pre_raw[kStages][2];
-  int64_t raw_tile[kStages];
+  // a run unit's plan words, copied in ahead of its runs: the tile's own
+  // approximate sum and the prefix of the tile before (cp.async
+  // destinations: 16-byte aligned)
+  alignas(16) uint64_t tagg_raw[kStages][2];
+  alignas(16) uint64_t pre_raw[kStages][2];
   WarpAgg wa[kStages][kWarps];
-  DF ex;
-  float ex_abs;
-  Rec chunk[kWarps];
-  int nitems[kWarps];               // >0: a split chunk's items in the tile's item area
-  unsigned long long st[S_COUNT];
+  Rec chunk[kStages][kWarps];       // a run unit's chunk records
+  int nitems[kStages][kWarps];      // >0: a split chunk's items in the tile's item area
+  unsigned int st[S_COUNT];         // per-CTA statistics of one call (32-bit: native shared atomics)
   // walker
   uint64_t S;
   int m, nel, restart, nseg;
@@ -397,12 +426,18 @@ struct Smem {
   int wcnt[kWarps];
   int sum_k;
   // scanner
+  int scan_m[kWarps];
+  int scan_stop;
   DF scan_v[kWarps];
   float scan_a[kWarps];
   int scan_f[kWarps];
   DF carry;
   float carry_abs;
 };
+static_assert(offsetof(Smem, tagg_raw) % 16 == 0 && offsetof(Smem, pre_raw) % 16 == 0,
+              "cp.async destinations must be 16-byte aligned");
+static_assert(offsetof(Smem, full) % 8 == 0 && offsetof(Smem, done) % 8 == 0 && offsetof(Smem, sums) % 8 == 0,
+              "mbarriers are 8-byte aligned");
 
 // ---------------------------------------------------------------- the plan's prefix
 // Per tile two tagged 64-bit words, written and read as one 16-byte access:
@@ -452,7 +487,7 @@ __device__ __forceinline__ bool unit_of(int64_t u, int64_t ntiles, int64_t wave,
 // wait; on a timeout the plan is only worse, the result stays exact).  One
 // thread.
 __device__ __forceinline__ Prefix read_prefix(const Params &p, int sum, int64_t first_tile, int64_t t,
-                                              unsigned long long *st) {
+                                              unsigned int *st) {
   if (t == first_tile) {
     const DF ex = df_from_double(p.s0s ? p.s0s[sum] : p.s0);
     return Prefix{ex, fabsf(ex.hi)};
@@ -465,9 +500,9 @@ __device__ __forceinline__ Prefix read_prefix(const Params &p, int sum, int64_t 
     ld_vol_v2(p.status + 2 * (t - 1), A, B);
     const uint32_t ta = (uint32_t)(A & 0xFF), tb = (uint32_t)B;
     if (ta == tag && tb == tag) return Prefix{status_sum(A), status_abs(B)};
-    if (ta != tb && ((ta >> 1) == p.epoch || (tb >> 1) == p.epoch)) atomicAdd(&st[S_TORN_STATUS], 1ull);
+    if (ta != tb && ((ta >> 1) == p.epoch || (tb >> 1) == p.epoch)) atomicAdd(&st[S_TORN_STATUS], 1u);
     if (globaltimer() - t0 > kWaitNs) {
-      atomicOr(&p.ctr[C_ERR], ERR_PLAN_TIMEOUT);
+      note_timeout(p, ERR_PLAN_TIMEOUT, TO_PREFIX, (uint32_t)t, (uint32_t)(ta | (tb << 8) | (p.epoch << 16)));
       return Prefix{DF{0.0f, 0.0f}, 0.0f};
     }
     __nanosleep(32);
@@ -483,17 +518,19 @@ __device__ __forceinline__ Prefix read_prefix(const Params &p, int sum, int64_t 
 __device__ __noinline__ void scan_prefix(const Params &p, Smem &sm, int64_t ntiles) {
   constexpr int PER = 4;
   constexpr int WIN = kThreads * PER;
+  const unsigned full = 0xffffffffu;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t ep = p.epoch;
-  unsigned long long *st = sm.st;
+  unsigned int *st = sm.st;
   int64_t pos = 0;
   DF carry = DF{0.0f, 0.0f};            // inclusive prefix of tile pos - 1
   float carry_abs = 0.0f;
   uint64_t tprog = globaltimer();
   const uint64_t tbegin = tprog;
+  uint64_t twait = 0;
   while (pos < ntiles) {
     uint64_t A[PER], B[PER];
-#pragma unroll 1
+#pragma unroll
     for (int q = 0; q < PER; q++) {
       const int64_t idx = pos + tid * PER + q;
       A[q] = 0;
@@ -501,24 +538,30 @@ __device__ __noinline__ void scan_prefix(const Params &p, Smem &sm, int64_t ntil
       if (idx < ntiles && sq_ok(p, idx < p.cap_tiles, 20, idx)) ld_vol_v2(p.status + 2 * idx, A[q], B[q]);
     }
     int myfirst = PER;
-#pragma unroll 1
+#pragma unroll
     for (int q = PER - 1; q >= 0; q--) {
       const int64_t idx = pos + tid * PER + q;
       const uint32_t ta = (uint32_t)(A[q] & 0xFF), tb = (uint32_t)B[q];
       if (!(idx < ntiles && (ta >> 1) == ep && ta == tb)) myfirst = q;
     }
-    if (tid == 0) sm.m = WIN;
-    __syncthreads();
-    if (myfirst < PER) atomicMin(&sm.m, tid * PER + myfirst);
-    __syncthreads();
-    const int m = sm.m;                    // tiles [pos, pos + m) are published
-    __syncthreads();
+    // the published run [pos, pos + m): the first gap over the window
+    const uint32_t wmin = __reduce_min_sync(full, myfirst < PER ? (uint32_t)(tid * PER + myfirst) : (uint32_t)WIN);
+    if (lane == 0) sm.scan_m[warp] = (int)wmin;
+    wide_sync();
+    int m = WIN;
+#pragma unroll
+    for (int w2 = 0; w2 < kWarps; w2++) m = min(m, sm.scan_m[w2]);
     if (m == 0) {
-      if (globaltimer() - tprog > kWaitNs) {
-        if (tid == 0) atomicOr(&p.ctr[C_ERR], ERR_PLAN_TIMEOUT);
-        break;
+      // thread 0 alone decides whether to give up, so the CTA stays together
+      const uint64_t now = globaltimer();
+      if (tid == 0) {
+        sm.scan_stop = (now - tprog > kWaitNs) ? 1 : 0;
+        if (sm.scan_stop) note_timeout(p, ERR_PLAN_TIMEOUT, TO_SCAN, (uint32_t)pos, (uint32_t)ntiles);
       }
       __nanosleep(64);
+      twait += globaltimer() - now;
+      wide_sync();                       // sm.scan_stop is set; sm.scan_m may be written again
+      if (sm.scan_stop) break;
       continue;
     }
     tprog = globaltimer();
@@ -529,7 +572,7 @@ __device__ __noinline__ void scan_prefix(const Params &p, Smem &sm, int64_t ntil
     DF tv = DF{0.0f, 0.0f};
     float tab = 0.0f;
     bool tf = false;
-#pragma unroll 1
+#pragma unroll
     for (int q = 0; q < PER; q++) {
       if (tid * PER + q < m) {
         const DF val = status_sum(A[q]);
@@ -545,18 +588,18 @@ __device__ __noinline__ void scan_prefix(const Params &p, Smem &sm, int64_t ntil
     DF wv = tv;
     float wab = tab;
     int wf = tf ? 1 : 0;
-#pragma unroll 1
+#pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const DF ov = DF{__shfl_up_sync(0xffffffffu, wv.hi, o), __shfl_up_sync(0xffffffffu, wv.lo, o)};
-      const float oa = __shfl_up_sync(0xffffffffu, wab, o);
-      const int of = __shfl_up_sync(0xffffffffu, wf, o);
+      const DF ov = DF{__shfl_up_sync(full, wv.hi, o), __shfl_up_sync(full, wv.lo, o)};
+      const float oa = __shfl_up_sync(full, wab, o);
+      const int of = __shfl_up_sync(full, wf, o);
       if (lane >= o) {
         if (!wf) { wv = df_add(ov, wv); wab = oa + wab; }
         wf |= of;
       }
     }
     if (lane == 31) { sm.scan_v[warp] = wv; sm.scan_a[warp] = wab; sm.scan_f[warp] = wf; }
-    __syncthreads();
+    wide_sync();
     DF ev = carry;
     float eab = carry_abs;
     for (int w2 = 0; w2 < warp; w2++) {
@@ -564,31 +607,35 @@ __device__ __noinline__ void scan_prefix(const Params &p, Smem &sm, int64_t ntil
       else { ev = df_add(ev, sm.scan_v[w2]); eab += sm.scan_a[w2]; }
     }
     {
-      const DF lv = DF{__shfl_up_sync(0xffffffffu, wv.hi, 1), __shfl_up_sync(0xffffffffu, wv.lo, 1)};
-      const float la = __shfl_up_sync(0xffffffffu, wab, 1);
-      const int lf = __shfl_up_sync(0xffffffffu, wf, 1);
+      const DF lv = DF{__shfl_up_sync(full, wv.hi, 1), __shfl_up_sync(full, wv.lo, 1)};
+      const float la = __shfl_up_sync(full, wab, 1);
+      const int lf = __shfl_up_sync(full, wf, 1);
       if (lane >= 1) {
         if (lf) { ev = lv; eab = la; }
         else { ev = df_add(ev, lv); eab += la; }
       }
     }
-#pragma unroll 1
+#pragma unroll
     for (int q = 0; q < PER; q++) {
       const int i = tid * PER + q;
-      if (i >= m) break;
-      const DF inc = f[q] ? v[q] : df_add(ev, v[q]);
-      const float inca = f[q] ? a[q] : eab + a[q];
-      if (!(A[q] & 1u)) publish_status(p.status + 2 * (pos + i), inc, inca, ep, 1);
-      if (i == m - 1) { sm.carry = inc; sm.carry_abs = inca; }
+      if (i < m) {
+        const DF inc = f[q] ? v[q] : df_add(ev, v[q]);
+        const float inca = f[q] ? a[q] : eab + a[q];
+        if (!(A[q] & 1u)) publish_status(p.status + 2 * (pos + i), inc, inca, ep, 1);
+        if (i == m - 1) { sm.carry = inc; sm.carry_abs = inca; }
+      }
     }
-    __syncthreads();
+    wide_sync();
     carry = sm.carry;
     carry_abs = sm.carry_abs;
     pos += m;
-    if (tid == 0) atomicAdd(&st[S_SCAN_WINDOWS], 1ull);
-    __syncthreads();
+    if (tid == 0) atomicAdd(&st[S_SCAN_WINDOWS], 1u);
+    wide_sync();
   }
-  if (tid == 0) atomicAdd(&st[S_NS_SCAN], tprog - tbegin);
+  if (tid == 0) {
+    atomicAdd(&st[S_NS_SCAN], (unsigned)(tprog - tbegin));
+    atomicAdd(&st[S_NS_SCAN_WAIT], (unsigned)(twait));
+  }
 }
 
 // ---------------------------------------------------------------- lanes
@@ -709,7 +756,7 @@ __device__ __noinline__ int lane_items(const Params &p, const uint64_t *xs, int 
 // the chunk as one fallback).
 __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *stage, bool use_tma, int64_t row,
                                        int64_t lstart, int nv, int w, int lane, DF sc, float ac, uint64_t t,
-                                       Rec *area, unsigned long long *st) {
+                                       Rec *area, unsigned int *st) {
   uint64_t xs[kLaneTerms];
   load_lane(p, stage, use_tma, row, lstart, nv, w, lane, xs);
   float sig = 0.0f, ab = 0.0f;
@@ -743,7 +790,7 @@ __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *st
   if (!dirty) r = lane_run_general(p, stage, use_tma, row, lstart, nv, w, lane, clean ? e_l : 0);
   const int key = dirty ? kDirtyKey : (clean ? e_l : kZeroE);
   const int ndirty = dirty ? lane_items(p, xs, nv, A, dbase, t, w, lane, nullptr) : 0;
-  if (dirty) atomicAdd(&st[S_LANE_DIRTY], 1ull);
+  if (dirty) atomicAdd(&st[S_LANE_DIRTY], 1u);
   // merge neighbouring runs of one key (lanes past the end join the previous)
   const int pkey = __shfl_up_sync(0xffffffffu, key, 1);
   const bool head = (lane == 0) || (nv > 0 && (dirty || pkey == kDirtyKey || key != pkey));
@@ -817,28 +864,24 @@ __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *st
   return total;
 }
 
-// ---------------------------------------------------------------- phase A: the plan's sums
-// Chunk aggregates of a tile into sm.wa[s].  A plan unit (publish) also
-// publishes them, for the tile's run unit, and the tile's approximate sum --
-// or s0 plus it for the first tile of a sum -- for the scanner.
-__device__ __noinline__ void phase_a(const Params &p, Smem &sm, const unsigned char *stage, int s, int64_t t,
-                                     int64_t ntiles, bool publish) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const TileGeo g = tile_geo(p, t, ntiles);
-  const int64_t lstart = g.start + (int64_t)w * kChunkTerms + (int64_t)lane * kLaneTerms;
-  const int nv = (int)max((int64_t)0, min((int64_t)kLaneTerms, g.end - lstart));
-  uint64_t xs[kLaneTerms];
-  load_lane(p, stage, sm.tma[s] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, xs);
-  float sig = 0.0f, ab = 0.0f;
-  uint32_t orh = 0, orz = 0, mx = 0;
+// ---------------------------------------------------------------- streaming units
+// A streaming CTA has eight compute warps (warp w owns chunk w of every tile)
+// and a control warp.  Per stage two mbarriers: full (the tile's copy and,
+// for a run unit, its plan words have landed; the unit is described in
+// sm.tk/kind/tma) and done (the eight compute warps finished the unit).  The
+// control warp takes the tickets, issues the copies and runs each unit's
+// epilogue (publishing the plan's aggregates or the tile's header), so the
+// compute warps never wait for one another.
+enum : int { U_PLAN = 0, U_RUN = 1, U_END = 2 };
+
+// The plan's sums of this warp's chunk of tile t (fp32 images of the terms,
+// their sum and |x| sum) into sm.wa[k][w].
+__device__ __forceinline__ void chunk_sums_of(const uint64_t *xs, float &sig, float &ab) {
+  sig = 0.0f;
+  ab = 0.0f;
 #pragma unroll
   for (int i = 0; i < kLaneTerms; i++) {
-    const uint32_t hi = (uint32_t)(xs[i] >> 32);
-    const uint32_t mag = hi & 0x7FFFFFFFu;
-    orh |= hi;
-    orz |= mag | (uint32_t)xs[i];
-    mx = max(mx, mag);
-    const float f = approx_term_clamped(hi);
+    const float f = approx_term_clamped((uint32_t)(xs[i] >> 32));
     sig += f;
     ab += fabsf(f);
   }
@@ -846,94 +889,155 @@ __device__ __noinline__ void phase_a(const Params &p, Smem &sm, const unsigned c
   for (int o = 16; o > 0; o >>= 1) {
     sig += __shfl_xor_sync(0xffffffffu, sig, o);
     ab += __shfl_xor_sync(0xffffffffu, ab, o);
-    orh |= __shfl_xor_sync(0xffffffffu, orh, o);
-    orz |= __shfl_xor_sync(0xffffffffu, orz, o);
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  }
-  if (lane == 0) sm.wa[s][w] = WarpAgg{sig, ab, mx, ((orh >> 31) ? WA_NEG : 0u) | (orz ? WA_NZ : 0u)};
-  __syncthreads();
-  if (publish && w == 0) {
-    const bool ok = sq_ok(p, t >= 0 && t < p.cap_tiles, 6, t);
-    if (ok && lane < kWarps) publish_wagg(p.cagg + 2 * (t * kWarps + lane), sm.wa[s][lane], p.epoch);
-    DF agg = DF{0.0f, 0.0f};
-    float agga = 0.0f;
-#pragma unroll
-    for (int k = 0; k < kWarps; k++) { agg = df_addf(agg, sm.wa[s][k].sig); agga += sm.wa[s][k].ab; }
-    if (lane == 0 && ok) {
-      if (g.tile_in_sum != 0) {
-        publish_status(p.status + 2 * t, agg, agga, p.epoch, 0);
-      } else {                                   // the first tile of a sum: s0 + its sum at once
-        const DF ex = df_from_double(p.s0s ? p.s0s[g.sum] : p.s0);
-        publish_status(p.status + 2 * t, df_add(ex, agg), fabsf(ex.hi) + agga, p.epoch, 1);
-      }
-    }
   }
 }
-
-// Warp 0 of a streaming CTA: start copying a run unit's plan words -- its
-// chunk aggregates (lanes 0-7) and the prefix of the tile before it (lane 8)
-// -- into the stage's slots; completed by cp_async_wait_all before the
-// barrier that precedes the unit's runs.
-__device__ __forceinline__ void prefetch_plan(const Params &p, Smem &sm, int s, int64_t t) {
-  const int lane = threadIdx.x & 31;
-  if (lane < kWarps) cp_async16(sm.agg_raw[s][lane], p.cagg + 2 * (t * kWarps + lane));
-  else if (lane == kWarps && t > 0) cp_async16(sm.pre_raw[s], p.status + 2 * (t - 1));
-  cp_async_commit();
-  if (lane == 0) sm.raw_tile[s] = t;
-}
-
-// ---------------------------------------------------------------- phase B: runs of a tile
-__device__ __noinline__ void phase_b(const Params &p, Smem &sm, const unsigned char *stage, int s, int64_t t, int64_t ntiles) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  unsigned long long *st = sm.st;
+__device__ __noinline__ void chunk_aggregate(const Params &p, Smem &sm, const unsigned char *stage, int k,
+                                             int64_t t, int64_t ntiles) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const TileGeo g = tile_geo(p, t, ntiles);
-  // the plan words copied in ahead (else wait for the prefix / form the
-  // chunk aggregates from the tile itself)
-  const bool have = sm.raw_tile[s] == t;
-  bool agg_ok = true;
-  if (tid < kWarps) {
-    WarpAgg a;
-    agg_ok = have && decode_wagg(sm.agg_raw[s][tid][0], sm.agg_raw[s][tid][1], p.epoch, a);
-    if (agg_ok) sm.wa[s][tid] = a;
+  const int64_t lstart = g.start + (int64_t)w * kChunkTerms + (int64_t)lane * kLaneTerms;
+  const int nv = (int)max((int64_t)0, min((int64_t)kLaneTerms, g.end - lstart));
+  uint64_t xs[kLaneTerms];
+  load_lane(p, stage, sm.tma[k] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, xs);
+  float sig, ab;
+  chunk_sums_of(xs, sig, ab);
+  if (lane == 0) sm.wa[k][w] = WarpAgg{sig, ab, 0u, 0u};
+}
+
+// Control warp, after a plan unit: publish the tile's approximate sum (for
+// its run unit) and, for the scanner, the same sum -- or s0 plus it for the
+// first tile of a sum.
+__device__ __noinline__ void plan_epilogue(const Params &p, Smem &sm, int k, int64_t t, int64_t ntiles) {
+  const int lane = threadIdx.x & 31;
+  if (!sq_ok(p, t >= 0 && t < p.cap_tiles, 6, t)) return;
+  const TileGeo g = tile_geo(p, t, ntiles);
+  WarpAgg a = WarpAgg{0.0f, 0.0f, 0u, 0u};
+  if (lane < kWarps) a = sm.wa[k][lane];
+  DF agg = DF{a.sig, 0.0f};
+  float agga = a.ab;
+#pragma unroll
+  for (int o = kWarps / 2; o > 0; o >>= 1) {
+    agg = df_add(agg, shfl_xor_df(agg, o));
+    agga += __shfl_xor_sync(0xffffffffu, agga, o);
   }
-  if (tid == 0) {
-    const uint32_t tag = (p.epoch << 1) | 1u;
-    const uint64_t A = sm.pre_raw[s][0], B = sm.pre_raw[s][1];
-    if (t != g.first_tile && have && (uint32_t)(A & 0xFF) == tag && (uint32_t)B == tag) {
-      sm.ex = status_sum(A);
-      sm.ex_abs = status_abs(B);
+  if (lane == 0) {
+    publish_status(p.tagg + 2 * t, agg, agga, p.epoch, 0);     // the tile's own sum, for its run unit
+    if (g.tile_in_sum != 0) {
+      publish_status(p.status + 2 * t, agg, agga, p.epoch, 0);
     } else {
-      const uint64_t tl = globaltimer();
-      const Prefix pr = read_prefix(p, g.sum, g.first_tile, t, st);
-      sm.ex = pr.ex;
-      sm.ex_abs = pr.ex_abs;
-      atomicAdd(&st[S_NS_PREFIX_WAIT], globaltimer() - tl);
+      const DF ex = df_from_double(p.s0s ? p.s0s[g.sum] : p.s0);
+      publish_status(p.status + 2 * t, df_add(ex, agg), fabsf(ex.hi) + agga, p.epoch, 1);
     }
   }
-  if (!__syncthreads_and(agg_ok)) {
-    if (tid == 0) atomicAdd(&st[S_PLAN_LOCAL], 1ull);
-    phase_a(p, sm, stage, s, t, ntiles, false);
+}
+
+// Compute warp w, a run unit: the exact run (or items) of chunk w of tile t
+// under the binade its approximate prefix names; the chunk's record goes to
+// sm.chunk[k][w] for the control warp's header.
+__device__ __noinline__ void chunk_runs(const Params &p, Smem &sm, const unsigned char *stage, int k, int64_t t,
+                                        int64_t ntiles, uint32_t &sums_ph) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const unsigned full = 0xffffffffu;
+  unsigned int *st = sm.st;
+  const TileGeo g = tile_geo(p, t, ntiles);
+  const uint32_t tag0 = p.epoch << 1, tag1 = tag0 | 1u;
+  // ---- the plan words: the prefix before the tile and the tile's own sums
+  DF sp;
+  float ap;
+  if (t == g.first_tile) {
+    sp = df_from_double(p.s0s ? p.s0s[g.sum] : p.s0);
+    ap = fabsf(sp.hi);
+  } else {
+    const uint64_t A = sm.pre_raw[k][0], B = sm.pre_raw[k][1];
+    if ((uint32_t)(A & 0xFF) == tag1 && (uint32_t)B == tag1) {
+      sp = status_sum(A);
+      ap = status_abs(B);
+    } else {
+      Prefix pr{DF{0.0f, 0.0f}, 0.0f};
+      if (lane == 0) {
+        const uint64_t tl = globaltimer();
+        pr = read_prefix(p, g.sum, g.first_tile, t, st);
+        atomicAdd(&st[S_NS_PREFIX_WAIT], (unsigned)(globaltimer() - tl));
+      }
+      sp = DF{__shfl_sync(full, pr.ex.hi, 0), __shfl_sync(full, pr.ex.lo, 0)};
+      ap = __shfl_sync(full, pr.ex_abs, 0);
+    }
   }
-  // ---- plan of this warp's chunk
-  DF sc = sm.ex;
-  float ac = sm.ex_abs;
-  for (int k = 0; k < w; k++) { sc = df_addf(sc, sm.wa[s][k].sig); ac += sm.wa[s][k].ab; }
-  const WarpAgg me = sm.wa[s][w];
+  uint64_t TA = sm.tagg_raw[k][0], TB = sm.tagg_raw[k][1];
+  if (!((uint32_t)(TA & 0xFF) == tag0 && (uint32_t)TB == tag0)) {
+    // not copied in time: wait for the plan unit's word (bounded)
+    if (lane == 0) {
+      const uint64_t t0 = globaltimer();
+      while (true) {
+        ld_vol_v2(p.tagg + 2 * t, TA, TB);
+        if ((uint32_t)(TA & 0xFF) == tag0 && (uint32_t)TB == tag0) break;
+        if (globaltimer() - t0 > kWaitNs) {
+          note_timeout(p, ERR_PLAN_TIMEOUT, TO_TILESUM, (uint32_t)t, (uint32_t)((TA & 0xFF) | (p.epoch << 16)));
+          break;
+        }
+        __nanosleep(32);
+      }
+      atomicAdd(&st[S_NS_PREFIX_WAIT], (unsigned)(globaltimer() - t0));
+    }
+    TA = __shfl_sync(full, TA, 0);
+    TB = __shfl_sync(full, TB, 0);
+  }
+  const bool tagg_ok = (uint32_t)(TA & 0xFF) == tag0 && (uint32_t)TB == tag0;
+  // ---- this lane's terms and the chunk's exact stats (the fast runs'
+  // preconditions)
   const int64_t cstart = g.start + (int64_t)w * kChunkTerms;
   const int cnt_chunk = (int)max((int64_t)0, min((int64_t)kChunkTerms, g.end - cstart));
   const int64_t lstart = cstart + (int64_t)lane * kLaneTerms;
   const int nv = (int)max((int64_t)0, min((int64_t)kLaneTerms, g.end - lstart));
+  uint64_t xs[kLaneTerms];
+  load_lane(p, stage, sm.tma[k] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, xs);
+  WarpAgg me = WarpAgg{0.0f, 0.0f, 0u, 0u};
+  {
+    uint32_t orh = 0, orz = 0, mx = 0;
+#pragma unroll
+    for (int i = 0; i < kLaneTerms; i++) {
+      const uint32_t hi = (uint32_t)(xs[i] >> 32);
+      const uint32_t mag = hi & 0x7FFFFFFFu;
+      orh |= hi;
+      orz |= mag | (uint32_t)xs[i];
+      mx = max(mx, mag);
+    }
+    me.mx = __reduce_max_sync(full, mx);
+    me.flags = ((__reduce_or_sync(full, orh) >> 31) ? WA_NEG : 0u) | (__reduce_or_sync(full, orz) ? WA_NZ : 0u);
+  }
+  // ---- the binade: one for the whole tile when the prefix range of every
+  // term in it stays inside one (the common case); else chunk by chunk
+  DF sc = sp;
+  float ac = ap;
   int e = 0;
   bool clean;
   {
-    const float P = 0.5f * (me.ab + me.sig), N = 0.5f * (me.ab - me.sig);
+    const DF tsd = status_sum(TA);
+    const float c = sp.hi + sp.lo, ts = tsd.hi + tsd.lo, tab = status_abs(TB);
+    const float P = 0.5f * (tab + ts), N = 0.5f * (tab - ts);
+    const float delta = kEps * (ap + tab) + kRelF32 * (fabsf(c) + tab) + kTinyF;
+    clean = tagg_ok && p.plan_mode == 0 && one_binade_f(c - N - delta, c + P + delta, e);
+  }
+  if (!clean) {
+    // the same words reach every compute warp, so all of them come here;
+    // they trade their chunks' sums through a per-stage barrier (bounded)
+    float sig, ab;
+    chunk_sums_of(xs, sig, ab);
+    if (lane == 0) sm.wa[k][w] = WarpAgg{sig, ab, 0u, 0u};
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.sums[k]);
+    mbar_wait(p, &sm.sums[k], (sums_ph >> k) & 1u, ERR_PLAN_TIMEOUT, TO_SUMS, (uint32_t)t, (uint32_t)w);
+    sums_ph ^= 1u << k;
+    if (tid == 0) atomicAdd(&st[S_PLAN_LOCAL], 1u);
+    for (int j = 0; j < w; j++) { sc = df_addf(sc, sm.wa[k][j].sig); ac += sm.wa[k][j].ab; }
+    me.sig = sig;
+    me.ab = ab;
+    const float P = 0.5f * (ab + sig), N = 0.5f * (ab - sig);
     const float c = sc.hi + sc.lo;
-    const float delta = kEps * (ac + me.ab) + kRelF32 * (fabsf(c) + me.ab) + kTinyF;
+    const float delta = kEps * (ac + ab) + kRelF32 * (fabsf(c) + ab) + kTinyF;
     clean = one_binade_f(c - N - delta, c + P + delta, e);
     clean = plan_override(p.plan_mode, clean, e, (uint64_t)t, w, 0);
   }
-  uint64_t xs[kLaneTerms];
-  load_lane(p, stage, sm.tma[s] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, xs);
   Rec *area = p.items + t * kTileSlots;
   Rec crec;
   int nitems = 0;
@@ -995,7 +1099,7 @@ __device__ __noinline__ void phase_b(const Params &p, Smem &sm, const unsigned c
         }
       }
     }
-    if (general) r = lane_run_general(p, stage, sm.tma[s] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, e);
+    if (general) r = lane_run_general(p, stage, sm.tma[k] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, e);
     if (general_reduce) {
 #pragma unroll 1
       for (int off = 1; off < 32; off <<= 1) {
@@ -1004,9 +1108,9 @@ __device__ __noinline__ void phase_b(const Params &p, Smem &sm, const unsigned c
       }
     }
     crec = make_rec(r, (r.flags & F_ZERO) ? kZeroE : e, K_RUN, (uint32_t)cnt_chunk, (uint32_t)(w * kChunkTerms));
-    if (lane == 0) atomicAdd(&st[S_CHUNK_RUN], 1ull);
+    if (lane == 0) atomicAdd(&st[S_CHUNK_RUN], 1u);
   } else {
-    nitems = split_chunk(p, stage, sm.tma[s] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, sc, ac,
+    nitems = split_chunk(p, stage, sm.tma[k] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, sc, ac,
                          (uint64_t)t, area, st);
     if (nitems == 0) {
       Run fr = run_empty();
@@ -1014,74 +1118,78 @@ __device__ __noinline__ void phase_b(const Params &p, Smem &sm, const unsigned c
       crec = make_rec(fr, 0, K_FALLBACK, (uint32_t)cnt_chunk, (uint32_t)(w * kChunkTerms));
       if (lane == 0) {
         if (item_ok(p, area + w * kChunkSlots, 7)) stcg_rec(area + w * kChunkSlots, crec);
-        atomicAdd(&st[S_POOL_OVERFLOW], 1ull);
+        atomicAdd(&st[S_POOL_OVERFLOW], 1u);
       }
       nitems = 1;
     } else if (lane == 0) {
-      atomicAdd(&st[S_CHUNK_LIST], 1ull);
-      atomicAdd(&st[S_ITEMS], (unsigned long long)nitems);
+      atomicAdd(&st[S_CHUNK_LIST], 1u);
+      atomicAdd(&st[S_ITEMS], (unsigned)nitems);
     }
     crec.meta = rec_meta(0, 0, K_COMPLEX, 0);
   }
   if (lane == 0) {
-    sm.chunk[w] = crec;
-    sm.nitems[w] = nitems;
+    sm.chunk[k][w] = crec;
+    sm.nitems[k][w] = nitems;
   }
-  // the items every warp wrote are ordered before the header by this barrier
-  // and the publishing thread's device-scope fence (a fence is cumulative)
-  __syncthreads();
-  // ---- the tile's header (warp 0): one run when every chunk is a run of one
-  // binade (runs of zeros fit any), else the chunks' items in the item area
-  if (w == 0) {
-    const unsigned full = 0xffffffffu;
-    Rec c = make_rec(run_empty(), kZeroE, K_RUN, 0, 0);
-    int n = 0;
-    if (lane < kWarps) { c = sm.chunk[lane]; n = sm.nitems[lane]; }
-    const uint32_t kind = rec_kind(c.meta), flags = rec_flags(c.meta);
-    const bool nz_run = lane < kWarps && kind == K_RUN && !(flags & F_ZERO);
-    const uint32_t nzm = __ballot_sync(full, nz_run);
-    const int et = nzm ? __shfl_sync(full, (int)c.e, __ffs(nzm) - 1) : kZeroE;
-    const bool mixed = lane < kWarps && (kind != K_RUN || (nz_run && c.e != et));
-    Rec hd;
-    if (__ballot_sync(full, mixed) == 0) {
-      Run r = rec_run(c);
+}
+
+// Control warp, after a run unit: the tile's header -- one run when every
+// chunk is a run of one binade (runs of zeros fit any), else the chunks'
+// items in the tile's item area.
+__device__ __noinline__ void run_epilogue(const Params &p, Smem &sm, int k, int64_t t, int64_t ntiles) {
+  const int lane = threadIdx.x & 31;
+  unsigned int *st = sm.st;
+  const TileGeo g = tile_geo(p, t, ntiles);
+  Rec *area = p.items + t * kTileSlots;
+  const unsigned full = 0xffffffffu;
+  Rec c = make_rec(run_empty(), kZeroE, K_RUN, 0, 0);
+  int n = 0;
+  if (lane < kWarps) { c = sm.chunk[k][lane]; n = sm.nitems[k][lane]; }
+  const uint32_t kind = rec_kind(c.meta), flags = rec_flags(c.meta);
+  const bool nz_run = lane < kWarps && kind == K_RUN && !(flags & F_ZERO);
+  const uint32_t nzm = __ballot_sync(full, nz_run);
+  const int et = nzm ? __shfl_sync(full, (int)c.e, __ffs(nzm) - 1) : kZeroE;
+  const bool mixed = lane < kWarps && (kind != K_RUN || (nz_run && c.e != et));
+  Rec hd;
+  if (__ballot_sync(full, mixed) == 0) {
+    Run r = rec_run(c);
 #pragma unroll
-      for (int off = 1; off < kWarps; off <<= 1) {
-        const Run o = shfl_run<SH_DOWN>(r, off);
-        if ((lane & (2 * off - 1)) == 0) r = run_compose(r, o);
-      }
-      // the header alone holds the tile: nothing to order before it
-      hd = make_rec(r, (r.flags & F_ZERO) ? kZeroE : et, K_RUN, (uint32_t)(g.end - g.start), 0);
-    } else {
-      if (lane < kWarps && kind == K_RUN) {
-        n = 0;
-        if (c.count > 0) {
-          if (item_ok(p, area + lane * kChunkSlots, 8)) stcg_rec(area + lane * kChunkSlots, c);
-          n = 1;
-        }
-      }
-      const uint64_t mine = (lane < kWarps) ? (uint64_t)(uint32_t)n << (kCountBits * lane) : 0ull;
-      const uint64_t packed = ((uint64_t)__reduce_or_sync(full, (uint32_t)(mine >> 32)) << 32) |
-                              __reduce_or_sync(full, (uint32_t)mine);
-      const uint32_t orf = __reduce_or_sync(full, lane < kWarps ? flags : 0u);
-      Run z = run_empty();
-      z.inc = (int64_t)packed;
-      z.flags = orf & (F_HASINF_P | F_HASINF_N | F_HASNAN);
-      hd = make_rec(z, 0, K_COMPLEX, (uint32_t)(g.end - g.start), 0);
-      hd.inc = (int64_t)packed;
-      __syncwarp();
-      // the items (written before the tile barrier, and by this warp) are
-      // ordered before the header by this device-scope fence
-      if (lane == 0) {
-        __threadfence();
-        atomicAdd(&st[S_TILE_COMPLEX], 1ull);
+    for (int off = 1; off < kWarps; off <<= 1) {
+      const Run o = shfl_run<SH_DOWN>(r, off);
+      if ((lane & (2 * off - 1)) == 0) r = run_compose(r, o);
+    }
+    // the header alone holds the tile: nothing to order before it
+    hd = make_rec(r, (r.flags & F_ZERO) ? kZeroE : et, K_RUN, (uint32_t)(g.end - g.start), 0);
+  } else {
+    if (lane < kWarps && kind == K_RUN) {
+      n = 0;
+      if (c.count > 0) {
+        if (item_ok(p, area + lane * kChunkSlots, 8)) stcg_rec(area + lane * kChunkSlots, c);
+        n = 1;
       }
     }
+    const uint64_t mine = (lane < kWarps) ? (uint64_t)(uint32_t)n << (kCountBits * lane) : 0ull;
+    const uint64_t packed = ((uint64_t)__reduce_or_sync(full, (uint32_t)(mine >> 32)) << 32) |
+                            __reduce_or_sync(full, (uint32_t)mine);
+    const uint32_t orf = __reduce_or_sync(full, lane < kWarps ? flags : 0u);
+    Run z = run_empty();
+    z.inc = (int64_t)packed;
+    z.flags = orf & (F_HASINF_P | F_HASINF_N | F_HASNAN);
+    hd = make_rec(z, 0, K_COMPLEX, (uint32_t)(g.end - g.start), 0);
+    hd.inc = (int64_t)packed;
+    __syncwarp();
+    // the items the compute warps wrote (ordered before their arrival on
+    // the stage's done barrier) and this warp's are ordered before the
+    // header by this device-scope fence (a fence is cumulative)
     if (lane == 0) {
-      if (sq_ok(p, t >= 0 && t < p.cap_tiles, 9, t)) publish_header(p.hdr + t, hd, (p.epoch << 1) | 1u);
-      atomicMax(&p.stats[S_T_STREAM_END], (unsigned long long)globaltimer());
-      atomicAdd(&st[S_TILES], 1ull);
+      __threadfence();
+      atomicAdd(&st[S_TILE_COMPLEX], 1u);
     }
+  }
+  if (lane == 0) {
+    if (sq_ok(p, t >= 0 && t < p.cap_tiles, 9, t)) publish_header(p.hdr + t, hd, (p.epoch << 1) | 1u);
+    atomicMax(&p.stats[S_T_STREAM_END], (unsigned long long)globaltimer());
+    atomicAdd(&st[S_TILES], 1u);
   }
 }
 
@@ -1101,7 +1209,7 @@ __device__ __forceinline__ uint64_t absorb(uint64_t Sb, uint32_t flags) {
 
 // Term-by-term fallback over x[a, a + cnt), run by a whole warp; every lane
 // ends with the same S.  One __dadd_rn per term, in index order.
-__device__ uint64_t add_terms(const Params &p, uint64_t Sb, int64_t a, int64_t cnt, unsigned long long *st) {
+__device__ uint64_t add_terms(const Params &p, uint64_t Sb, int64_t a, int64_t cnt, unsigned int *st) {
   const int lane = threadIdx.x & 31;
   const uint64_t t0 = globaltimer();
   double S = bitsd(Sb);
@@ -1112,8 +1220,8 @@ __device__ uint64_t add_terms(const Params &p, uint64_t Sb, int64_t a, int64_t c
     for (int j = 0; j < m; j++) S = __dadd_rn(S, __shfl_sync(0xffffffffu, v, j));
   }
   if (lane == 0) {
-    atomicAdd(&st[S_TERMS_ADDED], (unsigned long long)cnt);
-    atomicAdd(&st[S_NS_WALK_ADDS], globaltimer() - t0);
+    atomicAdd(&st[S_TERMS_ADDED], (unsigned)cnt);
+    atomicAdd(&st[S_NS_WALK_ADDS], (unsigned)(globaltimer() - t0));
   }
   return dbits(S);
 }
@@ -1157,7 +1265,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
   uint32_t *elpos = reinterpret_cast<uint32_t *>(dyn + kWalkOffPos);
   unsigned char *head = dyn + kWalkOffHead;
   int *ends = reinterpret_cast<int *>(dyn + kWalkOffEnds);
-  unsigned long long *st = sm.st;
+  unsigned int *st = sm.st;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t tag = (p.epoch << 1) | 1u;
   constexpr int B = kWalkElems / kThreads;          // elements per thread in the scan
@@ -1166,15 +1274,15 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
   if (tid == 0) sm.S = dbits(s0);
   int64_t pos = tb;
   uint64_t t_work0 = 0;
-  __syncthreads();
+  wide_sync();
   while (pos < te) {
     // ---- 1. the contiguous ready prefix [pos, pos + m)
     const int want = (int)min((int64_t)kWalkTiles, te - pos);
     const uint64_t t0 = globaltimer();
-    if (tid == 0 && t_work0 != 0) atomicAdd(&st[S_NS_WALK_WORK], t0 - t_work0);
+    if (tid == 0 && t_work0 != 0) atomicAdd(&st[S_NS_WALK_WORK], (unsigned)(t0 - t_work0));
     while (true) {
       if (tid == 0) sm.m = want;
-      __syncthreads();
+      wide_sync();
       for (int i = tid; i < want; i += kThreads) {
         Rec h;
         const int rh = sq_ok(p, pos + i < p.cap_tiles, 11, pos + i) ? read_header(p.hdr + pos + i, tag, h) : 0;
@@ -1182,14 +1290,20 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
           hdrs[i] = h;
         } else {
           atomicMin(&sm.m, i);
-          if (rh < 0) atomicAdd(&st[S_TORN_HEADER], 1ull);
+          if (rh < 0) atomicAdd(&st[S_TORN_HEADER], 1u);
         }
       }
-      __syncthreads();
+      wide_sync();
       if (sm.m > 0) break;
-      if (globaltimer() - t0 > kWaitNs) {
-        if (tid == 0) { atomicOr(&p.ctr[C_ERR], ERR_WALK_TIMEOUT); p.outs[k] = __longlong_as_double(0x7FF8000000000000ll); }
-        __syncthreads();
+      // thread 0 alone decides whether to give up, so the CTA stays together
+      if (tid == 0) sm.restart = (globaltimer() - t0 > kWaitNs) ? 1 : 0;
+      wide_sync();
+      if (sm.restart) {
+        if (tid == 0) {
+          note_timeout(p, ERR_WALK_TIMEOUT, TO_WALK, (uint32_t)pos, (uint32_t)want);
+          p.outs[k] = __longlong_as_double(0x7FF8000000000000ll);
+        }
+        wide_sync();
         return;
       }
       __nanosleep(200);
@@ -1197,9 +1311,9 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
     int m = sm.m;
     __threadfence();
     if (tid == 0) {
-      atomicAdd(&st[S_WALK_BATCHES], 1ull);
+      atomicAdd(&st[S_WALK_BATCHES], 1u);
       t_work0 = globaltimer();
-      atomicAdd(&st[S_NS_WALK_WAIT], t_work0 - t0);
+      atomicAdd(&st[S_NS_WALK_WAIT], (unsigned)(t_work0 - t0));
       if (pos + m >= te) p.stats[S_T_WALK0] = t_work0;
     }
     // ---- 2. elements per tile and their prefix; the batch is cut where the
@@ -1231,9 +1345,9 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
       }
-      __syncthreads();
+      wide_sync();
       if (lane == 31) sm.wcnt[warp] = incl;
-      __syncthreads();
+      wide_sync();
       wbase = 0;
       for (int w = 0; w < warp; w++) wbase += sm.wcnt[w];
       if (pass == 1) break;
@@ -1244,11 +1358,11 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         if (i < m && off + cnt[q] > kWalkElems) atomicMin(&sm.m, i);
         off += cnt[q];
       }
-      __syncthreads();
+      wide_sync();
       m = sm.m;
     }
     uint64_t tsec = 0;
-    if (tid == 0) { tsec = globaltimer(); atomicAdd(&st[S_NS_WALK_COUNT], tsec - t_work0); }
+    if (tid == 0) { tsec = globaltimer(); atomicAdd(&st[S_NS_WALK_COUNT], (unsigned)(tsec - t_work0)); }
     // ---- 3. the flat element list: simple tiles by their thread; the items
     //         of complex tiles by the whole block, one item per thread
     {
@@ -1280,7 +1394,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       }
       if (tid == kThreads - 1) sm.nel = wbase + incl;
     }
-    __syncthreads();
+    wide_sync();
     for (int j = tid; j < sm.nel && j < kWalkElems; j += kThreads) {
       const uint32_t ep = elpos[j];
       if (ep & 0x80000000u) {
@@ -1298,7 +1412,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         }
       }
     }
-    __syncthreads();
+    wide_sync();
 #ifdef SEQSUM_CHECKS
     if (pos == tb) {
       for (int j = tid; j < sm.nel && j < 4000; j += kThreads) {
@@ -1312,7 +1426,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
     }
 #endif
     const int nel = min(sm.nel, kWalkElems);
-    if (tid == 0) { const uint64_t t2 = globaltimer(); atomicAdd(&st[S_NS_WALK_GATHER], t2 - tsec); tsec = t2; }
+    if (tid == 0) { const uint64_t t2 = globaltimer(); atomicAdd(&st[S_NS_WALK_GATHER], (unsigned)(t2 - tsec)); tsec = t2; }
     // ---- 4. segmented scan and serial application (restarted after a rejected run)
     int from = 0;
     while (from < nel) {
@@ -1325,7 +1439,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         }
         head[i] = hd ? 1 : 0;
       }
-      __syncthreads();
+      wide_sync();
       Run agg = run_empty();
       bool has_head = false;
       int first_head = B;
@@ -1349,7 +1463,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         if (lane >= o) { if (!f) v = run_compose(ov, v); f |= of; }
       }
       if (lane == 31) { sm.wagg[warp] = v; sm.wflag[warp] = f; }
-      __syncthreads();
+      wide_sync();
       Run ex = run_empty();
 #pragma unroll 1
       for (int w = 0; w < warp; w++) {
@@ -1379,7 +1493,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         if (lane >= o) inc2 += vv;
       }
       if (lane == 31) sm.wcnt[warp] = inc2;
-      __syncthreads();
+      wide_sync();
       int eb2 = 0;
       for (int w = 0; w < warp; w++) eb2 += sm.wcnt[w];
       const int epos = eb2 + inc2 - my;
@@ -1393,8 +1507,8 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         comp[epos + jj] = make_rec(incls[idx[jj]], q.e, rec_kind(q.meta), q.count, rec_tstart(q.meta));
       }
       if (tid == kThreads - 1) sm.nseg = epos + my;
-      __syncthreads();
-      if (tid == 0) { const uint64_t t2 = globaltimer(); atomicAdd(&st[S_NS_WALK_SCAN], t2 - tsec); tsec = t2; }
+      wide_sync();
+      if (tid == 0) { const uint64_t t2 = globaltimer(); atomicAdd(&st[S_NS_WALK_SCAN], (unsigned)(t2 - tsec)); tsec = t2; }
       // ---- serial part on warp 0
 #ifdef SEQSUM_CHECKS
       auto abs_start = [&](int j) -> int64_t {
@@ -1411,7 +1525,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
           const int ei = ends[sidx];
           const Rec c = comp[sidx];
           const uint32_t kind = rec_kind(c.meta);
-          if (lane == 0) atomicAdd(&st[S_WALK_SEGMENTS], 1ull);
+          if (lane == 0) atomicAdd(&st[S_WALK_SEGMENTS], 1u);
           if (nonfinite(Sb)) {
             Sb = absorb(Sb, rec_flags(c.meta));
             WALK_TRACE(abs_start(segstart), abs_start(ei) + el[ei].count, 6u, Sb);
@@ -1428,8 +1542,8 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
             if (nt > 2) S = __dadd_rn(S, bitsd((uint64_t)q.hi));
             Sb = dbits(S);
             if (lane == 0) {
-              atomicAdd(&st[S_TERMS_ADDED], (unsigned long long)nt);
-              atomicAdd(&st[S_NS_WALK_ADDS], globaltimer() - ta0);
+              atomicAdd(&st[S_TERMS_ADDED], (unsigned)nt);
+              atomicAdd(&st[S_NS_WALK_ADDS], (unsigned)(globaltimer() - ta0));
             }
             WALK_TRACE(abs_start(ei), abs_start(ei) + nt, 2u, Sb);
             segstart = ei + 1;
@@ -1439,7 +1553,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
             const uint32_t ep = elpos[ei];
             const TileGeo g = tile_geo(p, pos + (ep >> 12), ntiles);
             Sb = add_terms(p, Sb, g.start + (ep & 0xFFF), c.count, st);
-            if (lane == 0) atomicAdd(&st[S_CHUNK_FALLBACK], 1ull);
+            if (lane == 0) atomicAdd(&st[S_CHUNK_FALLBACK], 1u);
             WALK_TRACE(abs_start(ei), abs_start(ei) + c.count, 1u, Sb);
             segstart = ei + 1;
             continue;
@@ -1453,7 +1567,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
               continue;
             }
           }
-          if (lane == 0) atomicAdd(&st[S_RUN_REJECTED], 1ull);
+          if (lane == 0) atomicAdd(&st[S_RUN_REJECTED], 1u);
           // the first element of the segment whose prefix composite the
           // check rejects: the warp composes 32 prefixes at a time.  The
           // bounds of a composite depend on the shape of its tree, so this
@@ -1513,41 +1627,143 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
           sm.S = Sb;
           sm.restart = restart;
           const uint64_t t2 = globaltimer();
-          atomicAdd(&st[S_NS_WALK_SERIAL], t2 - tsec);
+          atomicAdd(&st[S_NS_WALK_SERIAL], (unsigned)(t2 - tsec));
           tsec = t2;
         }
       }
-      __syncthreads();
+      wide_sync();
       const int rs = sm.restart;
-      __syncthreads();
+      wide_sync();
       if (rs < 0) break;
       from = rs;
     }
     pos += m;
-    __syncthreads();
+    wide_sync();
   }
   if (tid == 0) {
     p.outs[k] = bitsd(sm.S);
     const uint64_t tend = globaltimer();
     p.stats[S_T_WALK1] = tend;
-    if (t_work0 != 0) atomicAdd(&st[S_NS_WALK_WORK], tend - t_work0);
+    if (t_work0 != 0) atomicAdd(&st[S_NS_WALK_WORK], (unsigned)(tend - t_work0));
   }
-  __syncthreads();
+  wide_sync();
+}
+
+// ---------------------------------------------------------------- the streaming loops
+
+// Compute warps: the units of the stages in turn, until the control warp
+// marks the end.
+__device__ __noinline__ void compute_loop(const Params &p, Smem &sm, const unsigned char *dyn, int64_t ntiles) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t ph = 0;                                       // bit k: parity of full[k]
+  uint32_t sums_ph = 0;                                  // bit k: parity of sums[k]
+  for (int j = 0;; j++) {
+    const int k = j % kStages;
+    const uint64_t tw = (tid == 0) ? globaltimer() : 0;
+    if (!mbar_wait(p, &sm.full[k], (ph >> k) & 1u, ERR_TMA_TIMEOUT, TO_FULL, (uint32_t)j,
+                   (uint32_t)(k | (tid >> 5) << 8 | blockIdx.x << 16)))
+      break;                                             // the call has failed
+    ph ^= 1u << k;
+    if (tid == 0) atomicAdd(&sm.st[S_NS_TMA_WAIT], (unsigned)(globaltimer() - tw));
+    const int kind = sm.kind[k];
+    if (kind == U_END) break;
+    const int64_t t = sm.tk[k];
+    const unsigned char *stage = dyn + k * kStageBytes;
+    const uint64_t tb = (tid == 0) ? globaltimer() : 0;
+    if (kind == U_PLAN) {
+      chunk_aggregate(p, sm, stage, k, t, ntiles);
+      if (tid == 0) atomicAdd(&sm.st[S_NS_PHASE_A], (unsigned)(globaltimer() - tb));
+    } else {
+      chunk_runs(p, sm, stage, k, t, ntiles, sums_ph);
+      if (tid == 0) atomicAdd(&sm.st[S_NS_PHASE_B], (unsigned)(globaltimer() - tb));
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.done[k]);
+  }
+}
+
+// The control warp: tickets, copies, plan words and epilogues.
+__device__ __noinline__ void control_loop(const Params &p, Smem &sm, unsigned char *dyn, const CUtensorMap *tmap,
+                                          int64_t ntiles) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nunits = 2 * ntiles;
+  uint32_t u_next = 0;                                   // lane 0: the next ticket, taken one unit ahead
+  if (lane == 0) u_next = atomicAdd(&p.ctr[C_TICKET], 1u);
+  uint32_t ph = 0;                                       // bit k: parity of done[k]
+  auto epilogue = [&](int k) -> bool {
+    const uint64_t tw = globaltimer();
+    if (!mbar_wait(p, &sm.done[k], (ph >> k) & 1u, ERR_TMA_TIMEOUT, TO_DONE, (uint32_t)sm.tk[k],
+                   (uint32_t)(k | sm.kind[k] << 8 | blockIdx.x << 16)))
+      return false;
+    ph ^= 1u << k;
+    if (lane == 0) atomicAdd(&sm.st[S_NS_CTRL_WAIT], (unsigned)(globaltimer() - tw));
+    if (sm.kind[k] == U_PLAN) plan_epilogue(p, sm, k, sm.tk[k], ntiles);
+    else run_epilogue(p, sm, k, sm.tk[k], ntiles);
+    return true;
+  };
+  for (int j = 0;; j++) {
+    const int k = j % kStages;
+    if (j >= kStages && !epilogue(k)) break;             // the unit that held this stage (else the call failed)
+    uint32_t u = 0;
+    if (lane == 0) {
+      u = u_next;
+      u_next = atomicAdd(&p.ctr[C_TICKET], 1u);          // used at the next unit: its latency overlaps
+    }
+    u = __shfl_sync(0xffffffffu, u, 0);
+    if ((int64_t)u >= nunits) {
+      if (lane == 0) {
+        sm.kind[k] = U_END;
+        mbar_arrive(&sm.full[k]);
+      }
+      for (int jj = max(j - kStages + 1, 0); jj < j; jj++)
+        if (!epilogue(jj % kStages)) break;
+      break;
+    }
+    int64_t t;
+    const bool plan = unit_of((int64_t)u, ntiles, p.wave, t);
+    const TileGeo g = tile_geo(p, t, ntiles);
+    const bool tma = p.tma_rows != 0 && (g.start & 15) == 0;
+    if (!plan) {
+      // a run unit's plan words: the tile's own sum and the prefix of the
+      // tile before; the stage's full barrier also waits for these copies
+      if (lane == 0) cp_async16(sm.tagg_raw[k], p.tagg + 2 * t);
+      else if (lane == 1 && t > 0) cp_async16(sm.pre_raw[k], p.status + 2 * (t - 1));
+      if (lane < 2) cp_async_mbar_arrive(&sm.full[k]);
+    }
+    __syncwarp();
+    if (lane == 0) {
+      sm.tk[k] = t;
+      sm.kind[k] = plan ? U_PLAN : U_RUN;
+      sm.tma[k] = tma ? 1 : 0;
+      if (tma) {
+        fence_proxy_async();                             // the compute warps' reads of this stage came first
+        mbar_arrive_expect_tx(&sm.full[k], (uint32_t)kStageBytes);
+        tma_load_box(dyn + k * kStageBytes, tmap, &sm.full[k], 0, (int32_t)(g.start >> 4));
+      } else {
+        mbar_arrive(&sm.full[k]);
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------- the kernel
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kBlockThreads, 2)
     seqsum_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmap) {
   extern __shared__ unsigned char dsm_raw[];
   unsigned char *dyn =
       reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
   __shared__ Smem sm;
   const int tid = threadIdx.x;
+  const int warp = tid >> 5;
   int64_t ntiles = (p.ntiles >= 0) ? p.ntiles : (int64_t)__ldcg(&p.ctr[C_NTILES]);
   if (ntiles > p.cap_tiles) ntiles = 0;                  // the set-up flagged ERR_CAPACITY
   if (tid < S_COUNT) sm.st[tid] = 0;
   if (tid == 0) {
-    for (int s = 0; s < kStages; s++) mbar_init(&sm.bar[s], 1);
+    for (int s = 0; s < kStages; s++) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.done[s], kWarps);
+      mbar_init(&sm.sums[s], kWarps);
+    }
     fence_mbar_init();
     if (blockIdx.x == 0) p.stats[S_T_START] = globaltimer();
     // roles go to CTAs in the order they start, so every waiting role is
@@ -1558,111 +1774,36 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int role = sm.role;
 
   if (role < p.nwalkers) {
-    // ---------------- walker CTA
-    if (p.offsets == nullptr) {
-      if (ntiles == 0) { if (tid == 0) p.outs[0] = p.s0; }
-      else walk_sum(p, sm, dyn, 0, 0, ntiles, ntiles);
-    } else {
-      while (true) {
-        if (tid == 0) sm.sum_k = (int)atomicAdd(&p.ctr[C_SUMTICKET], 1u);
-        __syncthreads();
-        const int k = sm.sum_k;
-        __syncthreads();
-        if (k >= p.nsums) break;
-        if (ntiles == 0) continue;                         // bad offsets or capacity: outputs already NaN
-        const int64_t tb = __ldcg(&p.tile_begin[k]), te = __ldcg(&p.tile_begin[k + 1]);
-        if (te > tb) walk_sum(p, sm, dyn, k, tb, te, ntiles);
+    // ---------------- walker CTA (its control warp idles)
+    if (warp < kWarps) {
+      if (p.offsets == nullptr) {
+        if (ntiles == 0) { if (tid == 0) p.outs[0] = p.s0; }
+        else walk_sum(p, sm, dyn, 0, 0, ntiles, ntiles);
+      } else {
+        while (true) {
+          if (tid == 0) sm.sum_k = (int)atomicAdd(&p.ctr[C_SUMTICKET], 1u);
+          wide_sync();
+          const int k = sm.sum_k;
+          wide_sync();
+          if (k >= p.nsums) break;
+          if (ntiles == 0) continue;                     // bad offsets or capacity: outputs already NaN
+          const int64_t tb = __ldcg(&p.tile_begin[k]), te = __ldcg(&p.tile_begin[k + 1]);
+          if (te > tb) walk_sum(p, sm, dyn, k, tb, te, ntiles);
+        }
       }
     }
   } else if (role == p.nwalkers) {
-    // ---------------- the plan's prefix scanner
-    if (ntiles > 0) scan_prefix(p, sm, ntiles);
+    // ---------------- the plan's prefix scanner (its control warp idles)
+    if (warp < kWarps && ntiles > 0) scan_prefix(p, sm, ntiles);
   } else {
-    // ---------------- streaming CTA: copy of unit i+2 | unit i+1: a plan
-    // unit's aggregates, or a run unit's plan words copied in | runs of unit i
-    const int warp = tid >> 5;
-    const int64_t nunits = 2 * ntiles;
-    uint32_t u_next = 0;                                 // thread 0: the next ticket, taken one issue ahead
-    auto issue = [&](int s) {                            // thread 0
-      const int64_t u = (int64_t)u_next;
-      u_next = atomicAdd(&p.ctr[C_TICKET], 1u);          // used at the next issue: its latency overlaps
-      sm.tma[s] = 0;
-      sm.plan[s] = 0;
-      if (u >= nunits) { sm.tk[s] = ntiles; return; }    // no units left
-      int64_t t;
-      sm.plan[s] = unit_of(u, ntiles, p.wave, t) ? 1 : 0;
-      sm.tk[s] = t;
-      if (p.tma_rows == 0) return;
-      const TileGeo g = tile_geo(p, t, ntiles);
-      if ((g.start & 15) != 0) return;
-      fence_proxy_async();
-      mbar_arrive_expect_tx(&sm.bar[s], (uint32_t)kStageBytes);
-      tma_load_box(dyn + s * kStageBytes, &tmap, &sm.bar[s], 0, (int32_t)(g.start >> 4));
-      sm.tma[s] = 1;
-    };
-    uint32_t phases = 0;                                 // bit s: parity of stage s's barrier
-    auto wait_stage = [&](int s) {
-      if (sm.tma[s]) {
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(&sm.bar[s], (phases >> s) & 1u)) {
-          if (globaltimer() - t0 > kWaitNs) { atomicOr(&p.ctr[C_ERR], ERR_TMA_TIMEOUT); break; }
-        }
-        phases ^= 1u << s;
-        if (tid == 0) atomicAdd(&sm.st[S_NS_TMA_WAIT], globaltimer() - t0);
-      }
-    };
-    if (tid < kStages) sm.raw_tile[tid] = -1;
-    if (tid == 0) {
-      u_next = atomicAdd(&p.ctr[C_TICKET], 1u);
-      issue(0);
-      issue(1);
-    }
-    __syncthreads();
-    if (sm.tk[0] < ntiles) {
-      wait_stage(0);
-      if (sm.plan[0]) {
-        phase_a(p, sm, dyn, 0, sm.tk[0], ntiles, true);
-      } else if (warp == 0) {
-        prefetch_plan(p, sm, 0, sm.tk[0]);
-        cp_async_wait_all();
-      }
-    }
-    __syncthreads();
-    for (int i = 0;; i++) {
-      const int s = i % kStages, s1 = (i + 1) % kStages, s2 = (i + 2) % kStages;
-      const int64_t t = sm.tk[s];
-      if (t >= ntiles) break;
-      const int64_t t1 = sm.tk[s1];
-      const bool run_s = sm.plan[s] == 0, plan_s1 = sm.plan[s1] != 0;
-      __syncthreads();
-      if (tid == 0) {
-        if (t1 < ntiles) issue(s2);
-        else { sm.tk[s2] = ntiles; sm.tma[s2] = 0; sm.plan[s2] = 0; }
-      }
-      if (t1 < ntiles) {
-        wait_stage(s1);
-        if (plan_s1) {
-          const uint64_t ta = globaltimer();
-          phase_a(p, sm, dyn + s1 * kStageBytes, s1, t1, ntiles, true);
-          if (tid == 0) atomicAdd(&sm.st[S_NS_PHASE_A], globaltimer() - ta);
-        } else if (warp == 0) {
-          prefetch_plan(p, sm, s1, t1);
-        }
-      }
-      __syncthreads();
-      if (run_s) {
-        const uint64_t tb = globaltimer();
-        phase_b(p, sm, dyn + s * kStageBytes, s, t, ntiles);
-        if (tid == 0) atomicAdd(&sm.st[S_NS_PHASE_B], globaltimer() - tb);
-      }
-      if (warp == 0) cp_async_wait_all();                // unit i+1's plan words have landed
-      __syncthreads();
-    }
+    // ---------------- streaming CTA
+    if (warp < kWarps) compute_loop(p, sm, dyn, ntiles);
+    else control_loop(p, sm, dyn, &tmap, ntiles);
   }
 
   // ---- statistics and the last CTA's reset of the shared counters
   __syncthreads();
-  if (tid < S_ACCUM_END && sm.st[tid]) atomicAdd(&p.stats[tid], sm.st[tid]);
+  if (tid < S_ACCUM_END && sm.st[tid]) atomicAdd(&p.stats[tid], (unsigned long long)sm.st[tid]);
   if (tid == 0) {
     __threadfence();
     if (atomicAdd(&p.ctr[C_EXIT], 1u) + 1 == gridDim.x) {
@@ -1731,7 +1872,7 @@ cudaError_t launch_seqsum(const Params &p, const CUtensorMap *tmap, int grid, cu
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  seqsum_kernel<<<grid, kThreads, kDynSmem, st>>>(p, *tmap);
+  seqsum_kernel<<<grid, kBlockThreads, kDynSmem, st>>>(p, *tmap);
   return cudaGetLastError();
 }
 
@@ -1743,7 +1884,7 @@ cudaError_t launch_setup(const Params &p, cudaStream_t st) {
 int kernel_max_blocks_per_sm() {
   cudaFuncSetAttribute(seqsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
   int nb = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, seqsum_kernel, kThreads, kDynSmem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, seqsum_kernel, kBlockThreads, kDynSmem) != cudaSuccess)
     return 1;
   return nb > 0 ? nb : 1;
 }
