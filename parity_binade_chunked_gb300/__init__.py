@@ -70,6 +70,8 @@ def lib():
             L.seqsum_debug_set_plan.restype = ctypes.c_int
             L.seqsum_debug_read.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), ctypes.c_int]
             L.seqsum_debug_read.restype = ctypes.c_int
+            L.seqsum_debug_heartbeat.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), ctypes.c_int]
+            L.seqsum_debug_heartbeat.restype = ctypes.c_int
             L.seqsum_version.argtypes = []
             L.seqsum_version.restype = ctypes.c_char_p
             _lib = L
@@ -169,6 +171,17 @@ def debug_read(n: int = 64) -> list:
     buf = (ctypes.c_ulonglong * n)()
     _check(lib().seqsum_debug_read(buf, n))
     return list(buf)
+
+
+def debug_heartbeat(nctas: int = 320) -> dict:
+    """Counters and per-CTA heartbeats of the most recent call, read without
+    waiting for it (diagnostics of a call that does not finish)."""
+    n = 16 + int(nctas)
+    buf = (ctypes.c_ulonglong * n)()
+    _check(lib().seqsum_debug_heartbeat(buf, n))
+    words = list(buf)
+    beats = [(i, w >> 56, (w >> 48) & 0xFF, w & 0xFFFFFFFFFFFF) for i, w in enumerate(words[16:]) if w]
+    return {"counters": words[:16], "beats": beats}
 
 
 def release_workspace():

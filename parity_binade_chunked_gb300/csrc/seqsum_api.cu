@@ -32,6 +32,7 @@ struct Workspace {
   int64_t *tile_begin = nullptr;
   unsigned long long *stats = nullptr;
   unsigned long long *dbg = nullptr;
+  unsigned long long *hb = nullptr;  // heartbeat words
   uint32_t epoch = 0;
   int64_t *h_pin = nullptr;          // pinned bounce for the batched size read-back
   // tensor map cache
@@ -83,6 +84,8 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
       return cuda_fail(e);
     if ((e = cudaMallocHost(&w->h_pin, 2 * sizeof(int64_t))) != cudaSuccess) return cuda_fail(e);
     if ((e = cudaMalloc(&w->dbg, 16384 * sizeof(unsigned long long))) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMalloc(&w->hb, sq::kHeartbeats * sizeof(unsigned long long))) != cudaSuccess) return cuda_fail(e);
+    cudaMemset(w->hb, 0, sq::kHeartbeats * sizeof(unsigned long long));
     cudaMemset(w->dbg, 0, 16384 * sizeof(unsigned long long));
     cudaMemset(w->ctr, 0, sq::C_COUNT * sizeof(uint32_t));
     cudaMemset(w->stats, 0, sq::S_COUNT * sizeof(unsigned long long));
@@ -183,6 +186,7 @@ void fill_ws(Params &p, Workspace *w) {
   p.cap_tiles = w->cap_tiles;
   p.stats = w->stats;
   p.dbg = w->dbg;
+  p.hb = w->hb;
 }
 
 int batched_impl(const double *x, int64_t x_len, const int64_t *offsets, int32_t nsums, const double *s0s,
@@ -381,6 +385,8 @@ void seqsum_release_workspace(void) {
     ws_free(w);
     cudaFree(w->ctr);
     cudaFree(w->stats);
+    cudaFree(w->dbg);
+    cudaFree(w->hb);
     cudaFreeHost(w->h_pin);
     delete w;
   }
@@ -397,6 +403,26 @@ int seqsum_debug_read(unsigned long long *out, int n) {
   if (e == cudaSuccess) e = cudaMemcpy(out, w->dbg, n * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemset(w->dbg, 0, 16384 * sizeof(unsigned long long));
   return e == cudaSuccess ? SEQSUM_OK : cuda_fail(e);
+}
+
+int seqsum_debug_heartbeat(unsigned long long *out, int n) {
+  // No lock: this is read while another thread may be blocked inside a call
+  // of this library (holding its lock).  A non-blocking stream lets the copy
+  // run next to a kernel that has not finished.
+  static cudaStream_t side = nullptr;
+  Workspace *w = g_last;
+  if (!w || !out || n < sq::C_COUNT || n > sq::C_COUNT + sq::kHeartbeats) return SEQSUM_EINVAL;
+  cudaError_t e = cudaSuccess;
+  if (!side) e = cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking);
+  uint32_t c[sq::C_COUNT];
+  if (e == cudaSuccess) e = cudaMemcpyAsync(c, w->ctr, sizeof c, cudaMemcpyDeviceToHost, side);
+  if (e == cudaSuccess && n > sq::C_COUNT)
+    e = cudaMemcpyAsync(out + sq::C_COUNT, w->hb, (n - sq::C_COUNT) * sizeof(unsigned long long),
+                        cudaMemcpyDeviceToHost, side);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(side);
+  if (e != cudaSuccess) return cuda_fail(e);
+  for (int i = 0; i < sq::C_COUNT; i++) out[i] = c[i];
+  return SEQSUM_OK;
 }
 
 int seqsum_debug_set_plan(int mode) {

@@ -22,6 +22,7 @@ constexpr int kTileSlots = kWarps * kChunkSlots;
 constexpr int kWalkTiles = 1024;                // tile headers per walk batch (32 KB)
 constexpr int kWalkElems = 1024;                // flat elements per walk batch (32 KB)
 constexpr int kMaxWalkers = 8;
+constexpr int kHeartbeats = 4096;               // CTAs with a heartbeat word (diagnostics of a stuck call)
 
 // ---- record kinds
 enum : uint32_t { K_RUN = 0, K_FALLBACK = 1, K_TERMS = 2, K_COMPLEX = 3 };
@@ -125,7 +126,8 @@ struct Params {
   int32_t nwalkers;            // CTA roles 0 .. nwalkers-1 walk, role nwalkers scans, the others stream
   int32_t pad2;
   int64_t wave;                // plan units run this many tiles ahead of run units
-  unsigned long long *dbg;     // self-checking builds: 64 diagnostic words
+  unsigned long long *dbg;     // self-checking builds: diagnostic words
+  unsigned long long *hb;      // kHeartbeats words: per CTA its role, what it waits for or does, where
   int64_t cap_tiles;           // tiles the workspace holds
   unsigned long long *stats;   // S_COUNT counters
 };

@@ -128,6 +128,18 @@ __device__ __forceinline__ void wide_sync() { named_sync(kBarWide, kThreads); }
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// Heartbeat of this CTA (one thread calls it): its role, what it waits for
+// or does (HB_*) and where (a unit, tile or position), read by the host
+// while a call runs.
+enum : uint32_t {
+  HB_START = 1, HB_WAIT_UNIT = 2, HB_UNIT = 3, HB_WAIT_DONE = 4, HB_EPILOGUE = 5, HB_WAIT_HEADERS = 6,
+  HB_BATCH = 7, HB_SERIAL = 8, HB_WAIT_SUMS = 9, HB_WINDOW = 10, HB_END = 15
+};
+__device__ __forceinline__ void beat(const Params &p, uint32_t role, uint32_t what, uint64_t where) {
+  if (blockIdx.x < (unsigned)kHeartbeats)
+    p.hb[blockIdx.x] = ((uint64_t)(role & 0xFFu) << 56) | ((uint64_t)(what & 0xFFu) << 48) | (where & 0xFFFFFFFFFFFFull);
+}
+
 // A bounded wait gave up: set its error bit and keep the first such site
 // with two words of context for the host.
 enum : uint32_t {
@@ -154,10 +166,10 @@ __device__ __forceinline__ bool mbar_wait(const Params &p, uint64_t *bar, uint32
   return true;
 }
 
-// the barrier's phase waits, besides its arrivals, for every earlier
-// cp.async of this thread
+// One of the barrier's expected arrivals, made when every earlier cp.async
+// of this thread has completed.
 __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
-  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // 16-byte asynchronous copy global -> shared through L2 (the prefetch of a
@@ -402,7 +414,7 @@ struct WarpAgg {
 };
 
 struct Smem {
-  uint64_t full[kStages];           // streaming: the unit's copy and plan words landed
+  uint64_t full[kStages];           // streaming: the unit's copy and plan words landed (3 arrivals)
   uint64_t done[kStages];           // streaming: the compute warps finished the unit
   uint64_t sums[kStages];           // streaming: the compute warps' chunk sums (a tile planned chunk by chunk)
   int64_t tk[kStages];              // the stage's tile
@@ -529,6 +541,7 @@ __device__ __noinline__ void scan_prefix(const Params &p, Smem &sm, int64_t ntil
   const uint64_t tbegin = tprog;
   uint64_t twait = 0;
   while (pos < ntiles) {
+    if (tid == 0) beat(p, sm.role, HB_WINDOW, (uint64_t)pos);
     uint64_t A[PER], B[PER];
 #pragma unroll
     for (int q = 0; q < PER; q++) {
@@ -1026,6 +1039,7 @@ __device__ __noinline__ void chunk_runs(const Params &p, Smem &sm, const unsigne
     if (lane == 0) sm.wa[k][w] = WarpAgg{sig, ab, 0u, 0u};
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.sums[k]);
+    if (tid == 0) beat(p, sm.role, HB_WAIT_SUMS, (uint64_t)t);
     mbar_wait(p, &sm.sums[k], (sums_ph >> k) & 1u, ERR_PLAN_TIMEOUT, TO_SUMS, (uint32_t)t, (uint32_t)w);
     sums_ph ^= 1u << k;
     if (tid == 0) atomicAdd(&st[S_PLAN_LOCAL], 1u);
@@ -1280,6 +1294,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
     const int want = (int)min((int64_t)kWalkTiles, te - pos);
     const uint64_t t0 = globaltimer();
     if (tid == 0 && t_work0 != 0) atomicAdd(&st[S_NS_WALK_WORK], (unsigned)(t0 - t_work0));
+    if (tid == 0) beat(p, sm.role, HB_WAIT_HEADERS, (uint64_t)pos);
     while (true) {
       if (tid == 0) sm.m = want;
       wide_sync();
@@ -1311,6 +1326,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
     int m = sm.m;
     __threadfence();
     if (tid == 0) {
+      beat(p, sm.role, HB_BATCH, ((uint64_t)m << 32) | (uint32_t)pos);
       atomicAdd(&st[S_WALK_BATCHES], 1u);
       t_work0 = globaltimer();
       atomicAdd(&st[S_NS_WALK_WAIT], (unsigned)(t_work0 - t0));
@@ -1660,6 +1676,7 @@ __device__ __noinline__ void compute_loop(const Params &p, Smem &sm, const unsig
   for (int j = 0;; j++) {
     const int k = j % kStages;
     const uint64_t tw = (tid == 0) ? globaltimer() : 0;
+    if (tid == 0) beat(p, sm.role, HB_WAIT_UNIT, (uint64_t)j);
     if (!mbar_wait(p, &sm.full[k], (ph >> k) & 1u, ERR_TMA_TIMEOUT, TO_FULL, (uint32_t)j,
                    (uint32_t)(k | (tid >> 5) << 8 | blockIdx.x << 16)))
       break;                                             // the call has failed
@@ -1670,6 +1687,7 @@ __device__ __noinline__ void compute_loop(const Params &p, Smem &sm, const unsig
     const int64_t t = sm.tk[k];
     const unsigned char *stage = dyn + k * kStageBytes;
     const uint64_t tb = (tid == 0) ? globaltimer() : 0;
+    if (tid == 0) beat(p, sm.role, HB_UNIT, ((uint64_t)j << 32) | (uint32_t)t);
     if (kind == U_PLAN) {
       chunk_aggregate(p, sm, stage, k, t, ntiles);
       if (tid == 0) atomicAdd(&sm.st[S_NS_PHASE_A], (unsigned)(globaltimer() - tb));
@@ -1692,6 +1710,7 @@ __device__ __noinline__ void control_loop(const Params &p, Smem &sm, unsigned ch
   uint32_t ph = 0;                                       // bit k: parity of done[k]
   auto epilogue = [&](int k) -> bool {
     const uint64_t tw = globaltimer();
+    if (lane == 0) beat(p, sm.role + 0x80u, HB_WAIT_DONE, ((uint64_t)k << 32) | (uint32_t)sm.tk[k]);
     if (!mbar_wait(p, &sm.done[k], (ph >> k) & 1u, ERR_TMA_TIMEOUT, TO_DONE, (uint32_t)sm.tk[k],
                    (uint32_t)(k | sm.kind[k] << 8 | blockIdx.x << 16)))
       return false;
@@ -1711,10 +1730,9 @@ __device__ __noinline__ void control_loop(const Params &p, Smem &sm, unsigned ch
     }
     u = __shfl_sync(0xffffffffu, u, 0);
     if ((int64_t)u >= nunits) {
-      if (lane == 0) {
-        sm.kind[k] = U_END;
-        mbar_arrive(&sm.full[k]);
-      }
+      if (lane == 0) sm.kind[k] = U_END;
+      __syncwarp();
+      if (lane < 3) mbar_arrive(&sm.full[k]);          // all three arrivals at once
       for (int jj = max(j - kStages + 1, 0); jj < j; jj++)
         if (!epilogue(jj % kStages)) break;
       break;
@@ -1723,13 +1741,14 @@ __device__ __noinline__ void control_loop(const Params &p, Smem &sm, unsigned ch
     const bool plan = unit_of((int64_t)u, ntiles, p.wave, t);
     const TileGeo g = tile_geo(p, t, ntiles);
     const bool tma = p.tma_rows != 0 && (g.start & 15) == 0;
+    // lanes 0 and 1 make two of the stage's three arrivals when their
+    // copies (a run unit's plan words: the tile's own sum and the prefix of
+    // the tile before; none for a plan unit) have landed
     if (!plan) {
-      // a run unit's plan words: the tile's own sum and the prefix of the
-      // tile before; the stage's full barrier also waits for these copies
       if (lane == 0) cp_async16(sm.tagg_raw[k], p.tagg + 2 * t);
       else if (lane == 1 && t > 0) cp_async16(sm.pre_raw[k], p.status + 2 * (t - 1));
-      if (lane < 2) cp_async_mbar_arrive(&sm.full[k]);
     }
+    if (lane < 2) cp_async_mbar_arrive(&sm.full[k]);
     __syncwarp();
     if (lane == 0) {
       sm.tk[k] = t;
@@ -1760,7 +1779,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
   if (tid < S_COUNT) sm.st[tid] = 0;
   if (tid == 0) {
     for (int s = 0; s < kStages; s++) {
-      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.full[s], 3);                         // control lanes 0 and 1 (copies) and lane 0 (unit)
       mbar_init(&sm.done[s], kWarps);
       mbar_init(&sm.sums[s], kWarps);
     }
@@ -1769,6 +1788,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
     // roles go to CTAs in the order they start, so every waiting role is
     // held by a running CTA
     sm.role = (int)atomicAdd(&p.ctr[C_ROLE], 1u);
+    beat(p, sm.role, HB_START, 0);
   }
   __syncthreads();
   const int role = sm.role;
@@ -1803,6 +1823,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
 
   // ---- statistics and the last CTA's reset of the shared counters
   __syncthreads();
+  if (tid == 0) beat(p, sm.role, HB_END, 0);
   if (tid < S_ACCUM_END && sm.st[tid]) atomicAdd(&p.stats[tid], (unsigned long long)sm.st[tid]);
   if (tid == 0) {
     __threadfence();

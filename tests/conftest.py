@@ -37,3 +37,32 @@ def oracle_mod():
     import oracle
     oracle.lib()
     return oracle
+
+
+# With SEQSUM_WATCHDOG=<seconds>, a GPU test still running after that long
+# prints the library's counters and per-CTA heartbeats (read without waiting
+# for the call) and ends the process, instead of leaving a call stuck.
+@pytest.fixture(autouse=True)
+def _watchdog(request):
+    limit = float(os.environ.get("SEQSUM_WATCHDOG", "0") or 0)
+    if limit <= 0 or request.node.get_closest_marker("gpu") is None:
+        yield
+        return
+    import threading
+
+    def fire():
+        try:
+            import parity_binade_chunked_gb300 as sq
+            d = sq.debug_heartbeat(320)
+            print(f"\nWATCHDOG {request.node.nodeid}: counters {d['counters']}", flush=True)
+            for beat in d["beats"]:
+                print("  cta %d role %d what %d where %#x" % beat, flush=True)
+        except Exception as e:          # diagnostics only
+            print("WATCHDOG failed:", e, flush=True)
+        os._exit(3)
+
+    timer = threading.Timer(limit, fire)
+    timer.daemon = True
+    timer.start()
+    yield
+    timer.cancel()
