@@ -46,7 +46,8 @@ enum {
   SEQSUM_ECUDA = -2,      /* a CUDA runtime call failed (see seqsum_last_cuda_error) */
   SEQSUM_ETIMEOUT = -3,   /* a device wait gave up (reported by seqsum_get_stats) */
   SEQSUM_ENOMEM = -4,     /* the workspace could not be allocated */
-  SEQSUM_ECAPACITY = -5,  /* a batched call needed more tiles than its workspace holds */
+  SEQSUM_ECAPACITY = -5,  /* a batched call needed more tiles than its workspace holds, or n is above
+                             SEQSUM_STATIC_MAX_TERMS for seqsum_f64_static */
   SEQSUM_EOFFSETS = -6    /* offsets out of order or out of range (seqsum_get_stats) */
 };
 
@@ -61,6 +62,24 @@ enum {
  *   stream CUDA stream the work is enqueued on
  * Returns SEQSUM_OK, SEQSUM_EINVAL, SEQSUM_ENOMEM or SEQSUM_ECUDA. */
 int seqsum_f64(const double *x, int64_t n, double s0, double *out, cudaStream_t stream);
+
+/* The largest n seqsum_f64_static accepts: 2^21 terms (512 tiles of 4096). */
+#define SEQSUM_STATIC_MAX_TERMS (1 << 21)
+
+/* As seqsum_f64, for n <= SEQSUM_STATIC_MAX_TERMS, on scratch held in
+ * fixed-size device arrays of the library: the call allocates nothing (no
+ * cudaMalloc, cudaFree or allocating library routine).  The pages describe no
+ * such call -- it has no counterpart in the method; it exists for callers that
+ * must not allocate.
+ *   x, n, s0, out, stream  as for seqsum_f64
+ * The first call on a device looks up the arrays' addresses and clears them
+ * on `stream`; make that first call before any stream capture.  Every call on
+ * a device shares the one scratch: calls that overlap in time (on different
+ * streams, or from several host threads) race and give wrong results; order
+ * them.  seqsum_get_stats() does not cover these calls.
+ * Returns SEQSUM_OK, SEQSUM_EINVAL, SEQSUM_ECAPACITY (n too large; nothing is
+ * enqueued) or SEQSUM_ECUDA. */
+int seqsum_f64_static(const double *x, int64_t n, double s0, double *out, cudaStream_t stream);
 
 /* nsums independent sequential sums over one concatenated plane: for each k,
  * outs[k] = s0s[k] + x[offsets[k]] + ... + x[offsets[k+1] - 1], in index order

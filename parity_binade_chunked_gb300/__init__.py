@@ -17,7 +17,7 @@ import threading
 
 from . import build as _build
 
-__all__ = ["seqsum_f64", "seqsum_f64_batched", "seqsum_f64_batched_sized", "get_stats",
+__all__ = ["seqsum_f64", "seqsum_f64_static", "seqsum_f64_batched", "seqsum_f64_batched_sized", "get_stats",
            "debug_set_plan", "release_workspace", "version", "lib", "SeqsumError"]
 
 _lock = threading.Lock()
@@ -54,6 +54,8 @@ def lib():
             vp, i64, i32, d = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_double
             L.seqsum_f64.argtypes = [vp, i64, d, vp, vp]
             L.seqsum_f64.restype = ctypes.c_int
+            L.seqsum_f64_static.argtypes = [vp, i64, d, vp, vp]
+            L.seqsum_f64_static.restype = ctypes.c_int
             L.seqsum_f64_batched.argtypes = [vp, vp, i32, vp, vp, vp]
             L.seqsum_f64_batched.restype = ctypes.c_int
             L.seqsum_f64_batched_sized.argtypes = [vp, i64, vp, i32, vp, vp, vp]
@@ -111,6 +113,24 @@ def seqsum_f64(x, s0: float = 0.0, out=None, stream=None):
     with torch.cuda.device(x.device):
         _check(lib().seqsum_f64(ctypes.c_void_p(x.data_ptr()), x.numel(), float(s0),
                                 ctypes.c_void_p(out.data_ptr()), _stream_handle(stream)))
+    return out
+
+
+STATIC_MAX_TERMS = 1 << 21
+
+
+def seqsum_f64_static(x, s0: float = 0.0, out=None, stream=None):
+    """As seqsum_f64 for at most STATIC_MAX_TERMS terms, on the library's
+    fixed-size device scratch: the call allocates nothing.  Calls that
+    overlap in time race (they share the scratch)."""
+    import torch
+    x = _dev_f64(x, "x").reshape(-1)
+    if out is None:
+        out = torch.empty(1, dtype=torch.float64, device=x.device)
+    _dev_f64(out, "out")
+    with torch.cuda.device(x.device):
+        _check(lib().seqsum_f64_static(ctypes.c_void_p(x.data_ptr()), x.numel(), float(s0),
+                                       ctypes.c_void_p(out.data_ptr()), _stream_handle(stream)))
     return out
 
 
