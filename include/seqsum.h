@@ -180,9 +180,9 @@ int seqsum_debug_set_plan(int mode);
 int seqsum_debug_read(unsigned long long *out, int n);
 
 /* Diagnostics of a call that does not finish: copies the device counters of
- * the most recent call's workspace into out[0..16) and, per CTA, a heartbeat
- * word into out[16..n) (role << 56 | what it waits for or does << 48 |
- * where).  It takes no lock and reads on a stream of its own, so it can run
+ * the most recent call's workspace into out[0..16) and, per warp (index
+ * CTA * 9 + warp), a heartbeat word into out[16..n) (role << 56 | what it
+ * waits for or does << 48 | where).  It takes no lock and reads on a stream of its own, so it can run
  * while another thread waits on that call.  16 <= n <= 16 + 4096. */
 int seqsum_debug_heartbeat(unsigned long long *out, int n);
 

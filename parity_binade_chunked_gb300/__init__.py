@@ -194,13 +194,14 @@ def debug_read(n: int = 64) -> list:
 
 
 def debug_heartbeat(nctas: int = 320) -> dict:
-    """Counters and per-CTA heartbeats of the most recent call, read without
-    waiting for it (diagnostics of a call that does not finish)."""
-    n = 16 + int(nctas)
+    """Counters and per-warp heartbeats (cta, warp, role, what, where) of the
+    most recent call, read without waiting for it (diagnostics of a call that
+    does not finish)."""
+    n = 16 + min(9 * int(nctas), 4096)
     buf = (ctypes.c_ulonglong * n)()
     _check(lib().seqsum_debug_heartbeat(buf, n))
     words = list(buf)
-    beats = [(i, w >> 56, (w >> 48) & 0xFF, w & 0xFFFFFFFFFFFF) for i, w in enumerate(words[16:]) if w]
+    beats = [(i // 9, i % 9, w >> 56, (w >> 48) & 0xFF, w & 0xFFFFFFFFFFFF) for i, w in enumerate(words[16:]) if w]
     return {"counters": words[:16], "beats": beats}
 
 

@@ -121,23 +121,32 @@ __device__ __forceinline__ void st_vol_v2(void *p, uint64_t a, uint64_t b) {
 // control warp takes no part).  Streaming CTAs synchronise through mbarriers
 // only, every wait bounded.
 constexpr int kBarWide = 1;
+// The non-aligned form: a warp's threads may arrive at it separately (code
+// before it is lane-divergent, and the compiler does not treat an asm barrier
+// as a point where the warp must be converged, which the aligned bar.sync
+// requires).
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
-__device__ __forceinline__ void wide_sync() { named_sync(kBarWide, kThreads); }
+struct Smem;
+__device__ __forceinline__ void wide_sync_at(const Params &p, Smem &sm, int site);
+#define wide_sync(p, sm, site) wide_sync_at((p), (sm), (site))
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 // Heartbeat of this CTA (one thread calls it): its role, what it waits for
 // or does (HB_*) and where (a unit, tile or position), read by the host
 // while a call runs.
+// One word per warp (index CTA * 9 + warp).
 enum : uint32_t {
   HB_START = 1, HB_WAIT_UNIT = 2, HB_UNIT = 3, HB_WAIT_DONE = 4, HB_EPILOGUE = 5, HB_WAIT_HEADERS = 6,
-  HB_BATCH = 7, HB_SERIAL = 8, HB_WAIT_SUMS = 9, HB_WINDOW = 10, HB_END = 15
+  HB_BATCH = 7, HB_SERIAL = 8, HB_WAIT_SUMS = 9, HB_WINDOW = 10, HB_COUNT = 11, HB_GATHER = 12, HB_SCAN = 13,
+  HB_RESTART = 14, HB_END = 15, HB_BARRIER = 16
 };
 __device__ __forceinline__ void beat(const Params &p, uint32_t role, uint32_t what, uint64_t where) {
-  if (blockIdx.x < (unsigned)kHeartbeats)
-    p.hb[blockIdx.x] = ((uint64_t)(role & 0xFFu) << 56) | ((uint64_t)(what & 0xFFu) << 48) | (where & 0xFFFFFFFFFFFFull);
+  const unsigned i = blockIdx.x * 9u + (threadIdx.x >> 5);
+  if (i < (unsigned)kHeartbeats)
+    p.hb[i] = ((uint64_t)(role & 0xFFu) << 56) | ((uint64_t)(what & 0xFFu) << 48) | (where & 0xFFFFFFFFFFFFull);
 }
 
 // A bounded wait gave up: set its error bit and keep the first such site
@@ -421,6 +430,7 @@ struct Smem {
   int tma[kStages];                 // its terms came by TMA (else from global memory)
   int kind[kStages];                // U_PLAN, U_RUN or U_END
   int role;
+  uint32_t barcnt[kWarps];          // walker/scanner: wide barriers passed per warp (heartbeat)
   // a run unit's plan words, copied in ahead of its runs: the tile's own
   // approximate sum and the prefix of the tile before (cp.async
   // destinations: 16-byte aligned)
@@ -450,6 +460,18 @@ static_assert(offsetof(Smem, tagg_raw) % 16 == 0 && offsetof(Smem, pre_raw) % 16
               "cp.async destinations must be 16-byte aligned");
 static_assert(offsetof(Smem, full) % 8 == 0 && offsetof(Smem, done) % 8 == 0 && offsetof(Smem, sums) % 8 == 0,
               "mbarriers are 8-byte aligned");
+
+// The 256-thread barrier of a walking or scanning CTA; each warp first
+// records the barrier's site and how many it has passed (its heartbeat).
+__device__ __forceinline__ void wide_sync_at(const Params &p, Smem &sm, int site) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    const uint32_t c = ++sm.barcnt[warp];
+    beat(p, sm.role, HB_BARRIER, ((uint64_t)site << 32) | c);
+  }
+  named_sync(kBarWide, kThreads);
+}
+
 
 // ---------------------------------------------------------------- the plan's prefix
 // Per tile two tagged 64-bit words, written and read as one 16-byte access:
@@ -560,7 +582,7 @@ __device__ __noinline__ void scan_prefix(const Params &p, Smem &sm, int64_t ntil
     // the published run [pos, pos + m): the first gap over the window
     const uint32_t wmin = __reduce_min_sync(full, myfirst < PER ? (uint32_t)(tid * PER + myfirst) : (uint32_t)WIN);
     if (lane == 0) sm.scan_m[warp] = (int)wmin;
-    wide_sync();
+    wide_sync(p, sm, 1);
     int m = WIN;
 #pragma unroll
     for (int w2 = 0; w2 < kWarps; w2++) m = min(m, sm.scan_m[w2]);
@@ -573,7 +595,7 @@ __device__ __noinline__ void scan_prefix(const Params &p, Smem &sm, int64_t ntil
       }
       __nanosleep(64);
       twait += globaltimer() - now;
-      wide_sync();                       // sm.scan_stop is set; sm.scan_m may be written again
+      wide_sync(p, sm, 2);                       // sm.scan_stop is set; sm.scan_m may be written again
       if (sm.scan_stop) break;
       continue;
     }
@@ -612,7 +634,7 @@ __device__ __noinline__ void scan_prefix(const Params &p, Smem &sm, int64_t ntil
       }
     }
     if (lane == 31) { sm.scan_v[warp] = wv; sm.scan_a[warp] = wab; sm.scan_f[warp] = wf; }
-    wide_sync();
+    wide_sync(p, sm, 3);
     DF ev = carry;
     float eab = carry_abs;
     for (int w2 = 0; w2 < warp; w2++) {
@@ -638,12 +660,12 @@ __device__ __noinline__ void scan_prefix(const Params &p, Smem &sm, int64_t ntil
         if (i == m - 1) { sm.carry = inc; sm.carry_abs = inca; }
       }
     }
-    wide_sync();
+    wide_sync(p, sm, 4);
     carry = sm.carry;
     carry_abs = sm.carry_abs;
     pos += m;
     if (tid == 0) atomicAdd(&st[S_SCAN_WINDOWS], 1u);
-    wide_sync();
+    wide_sync(p, sm, 5);
   }
   if (tid == 0) {
     atomicAdd(&st[S_NS_SCAN], (unsigned)(tprog - tbegin));
@@ -1039,7 +1061,7 @@ __device__ __noinline__ void chunk_runs(const Params &p, Smem &sm, const unsigne
     if (lane == 0) sm.wa[k][w] = WarpAgg{sig, ab, 0u, 0u};
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.sums[k]);
-    if (tid == 0) beat(p, sm.role, HB_WAIT_SUMS, (uint64_t)t);
+    if (lane == 0) beat(p, sm.role, HB_WAIT_SUMS, (uint64_t)t);
     mbar_wait(p, &sm.sums[k], (sums_ph >> k) & 1u, ERR_PLAN_TIMEOUT, TO_SUMS, (uint32_t)t, (uint32_t)w);
     sums_ph ^= 1u << k;
     if (tid == 0) atomicAdd(&st[S_PLAN_LOCAL], 1u);
@@ -1288,7 +1310,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
   if (tid == 0) sm.S = dbits(s0);
   int64_t pos = tb;
   uint64_t t_work0 = 0;
-  wide_sync();
+  wide_sync(p, sm, 6);
   while (pos < te) {
     // ---- 1. the contiguous ready prefix [pos, pos + m)
     const int want = (int)min((int64_t)kWalkTiles, te - pos);
@@ -1297,7 +1319,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
     if (tid == 0) beat(p, sm.role, HB_WAIT_HEADERS, (uint64_t)pos);
     while (true) {
       if (tid == 0) sm.m = want;
-      wide_sync();
+      wide_sync(p, sm, 7);
       for (int i = tid; i < want; i += kThreads) {
         Rec h;
         const int rh = sq_ok(p, pos + i < p.cap_tiles, 11, pos + i) ? read_header(p.hdr + pos + i, tag, h) : 0;
@@ -1308,17 +1330,17 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
           if (rh < 0) atomicAdd(&st[S_TORN_HEADER], 1u);
         }
       }
-      wide_sync();
+      wide_sync(p, sm, 8);
       if (sm.m > 0) break;
       // thread 0 alone decides whether to give up, so the CTA stays together
       if (tid == 0) sm.restart = (globaltimer() - t0 > kWaitNs) ? 1 : 0;
-      wide_sync();
+      wide_sync(p, sm, 9);
       if (sm.restart) {
         if (tid == 0) {
           note_timeout(p, ERR_WALK_TIMEOUT, TO_WALK, (uint32_t)pos, (uint32_t)want);
           p.outs[k] = __longlong_as_double(0x7FF8000000000000ll);
         }
-        wide_sync();
+        wide_sync(p, sm, 10);
         return;
       }
       __nanosleep(200);
@@ -1334,6 +1356,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
     }
     // ---- 2. elements per tile and their prefix; the batch is cut where the
     //         flat list would overflow, then the prefix is taken again
+    if (lane == 0) beat(p, sm.role, HB_COUNT, ((uint64_t)m << 32) | (uint32_t)pos);
     int cnt[BT];
     int mine = 0, wbase = 0, incl = 0;
     for (int pass = 0; pass < 2; pass++) {
@@ -1361,9 +1384,9 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
       }
-      wide_sync();
+      wide_sync(p, sm, 11);
       if (lane == 31) sm.wcnt[warp] = incl;
-      wide_sync();
+      wide_sync(p, sm, 12);
       wbase = 0;
       for (int w = 0; w < warp; w++) wbase += sm.wcnt[w];
       if (pass == 1) break;
@@ -1374,13 +1397,14 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         if (i < m && off + cnt[q] > kWalkElems) atomicMin(&sm.m, i);
         off += cnt[q];
       }
-      wide_sync();
+      wide_sync(p, sm, 13);
       m = sm.m;
     }
     uint64_t tsec = 0;
     if (tid == 0) { tsec = globaltimer(); atomicAdd(&st[S_NS_WALK_COUNT], (unsigned)(tsec - t_work0)); }
     // ---- 3. the flat element list: simple tiles by their thread; the items
     //         of complex tiles by the whole block, one item per thread
+    if (lane == 0) beat(p, sm.role, HB_GATHER, ((uint64_t)m << 32) | (uint32_t)pos);
     {
       int off = wbase + incl - mine;
 #pragma unroll 1
@@ -1410,7 +1434,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       }
       if (tid == kThreads - 1) sm.nel = wbase + incl;
     }
-    wide_sync();
+    wide_sync(p, sm, 14);
     for (int j = tid; j < sm.nel && j < kWalkElems; j += kThreads) {
       const uint32_t ep = elpos[j];
       if (ep & 0x80000000u) {
@@ -1428,7 +1452,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         }
       }
     }
-    wide_sync();
+    wide_sync(p, sm, 15);
 #ifdef SEQSUM_CHECKS
     if (pos == tb) {
       for (int j = tid; j < sm.nel && j < 4000; j += kThreads) {
@@ -1446,6 +1470,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
     // ---- 4. segmented scan and serial application (restarted after a rejected run)
     int from = 0;
     while (from < nel) {
+      if (lane == 0) beat(p, sm.role, HB_SCAN, ((uint64_t)nel << 32) | ((uint64_t)from << 16) | (uint32_t)(pos & 0xFFFF));
       for (int i = from + tid; i < nel; i += kThreads) {
         const Rec q = el[i];
         bool hd = (i == from) || elem_alone(q);
@@ -1455,7 +1480,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         }
         head[i] = hd ? 1 : 0;
       }
-      wide_sync();
+      wide_sync(p, sm, 16);
       Run agg = run_empty();
       bool has_head = false;
       int first_head = B;
@@ -1479,7 +1504,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         if (lane >= o) { if (!f) v = run_compose(ov, v); f |= of; }
       }
       if (lane == 31) { sm.wagg[warp] = v; sm.wflag[warp] = f; }
-      wide_sync();
+      wide_sync(p, sm, 17);
       Run ex = run_empty();
 #pragma unroll 1
       for (int w = 0; w < warp; w++) {
@@ -1509,7 +1534,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         if (lane >= o) inc2 += vv;
       }
       if (lane == 31) sm.wcnt[warp] = inc2;
-      wide_sync();
+      wide_sync(p, sm, 18);
       int eb2 = 0;
       for (int w = 0; w < warp; w++) eb2 += sm.wcnt[w];
       const int epos = eb2 + inc2 - my;
@@ -1523,7 +1548,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         comp[epos + jj] = make_rec(incls[idx[jj]], q.e, rec_kind(q.meta), q.count, rec_tstart(q.meta));
       }
       if (tid == kThreads - 1) sm.nseg = epos + my;
-      wide_sync();
+      wide_sync(p, sm, 19);
       if (tid == 0) { const uint64_t t2 = globaltimer(); atomicAdd(&st[S_NS_WALK_SCAN], (unsigned)(t2 - tsec)); tsec = t2; }
       // ---- serial part on warp 0
 #ifdef SEQSUM_CHECKS
@@ -1541,6 +1566,8 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
           const int ei = ends[sidx];
           const Rec c = comp[sidx];
           const uint32_t kind = rec_kind(c.meta);
+          if (lane == 0)
+            beat(p, sm.role, HB_SERIAL, ((uint64_t)kind << 40) | ((uint64_t)ns << 24) | ((uint64_t)ei << 12) | (uint32_t)sidx);
           if (lane == 0) atomicAdd(&st[S_WALK_SEGMENTS], 1u);
           if (nonfinite(Sb)) {
             Sb = absorb(Sb, rec_flags(c.meta));
@@ -1639,6 +1666,10 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
           if (kfail < ei) { restart = kfail + 1; break; }
           segstart = ei + 1;
         }
+        // every lane has read sm.S (at the top of the pass) before lane 0
+        // replaces it: the lanes of a warp do not run in lockstep, and a lane
+        // that reads the new value would walk the segments from the wrong sum
+        __syncwarp();
         if (lane == 0) {
           sm.S = Sb;
           sm.restart = restart;
@@ -1647,14 +1678,15 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
           tsec = t2;
         }
       }
-      wide_sync();
+      if (lane == 0) beat(p, sm.role, HB_RESTART, (uint64_t)from);
+      wide_sync(p, sm, 20);
       const int rs = sm.restart;
-      wide_sync();
+      wide_sync(p, sm, 21);
       if (rs < 0) break;
       from = rs;
     }
     pos += m;
-    wide_sync();
+    wide_sync(p, sm, 22);
   }
   if (tid == 0) {
     p.outs[k] = bitsd(sm.S);
@@ -1662,7 +1694,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
     p.stats[S_T_WALK1] = tend;
     if (t_work0 != 0) atomicAdd(&st[S_NS_WALK_WORK], (unsigned)(tend - t_work0));
   }
-  wide_sync();
+  wide_sync(p, sm, 23);
 }
 
 // ---------------------------------------------------------------- the streaming loops
@@ -1676,7 +1708,7 @@ __device__ __noinline__ void compute_loop(const Params &p, Smem &sm, const unsig
   for (int j = 0;; j++) {
     const int k = j % kStages;
     const uint64_t tw = (tid == 0) ? globaltimer() : 0;
-    if (tid == 0) beat(p, sm.role, HB_WAIT_UNIT, (uint64_t)j);
+    if (lane == 0) beat(p, sm.role, HB_WAIT_UNIT, (uint64_t)j);
     if (!mbar_wait(p, &sm.full[k], (ph >> k) & 1u, ERR_TMA_TIMEOUT, TO_FULL, (uint32_t)j,
                    (uint32_t)(k | (tid >> 5) << 8 | blockIdx.x << 16)))
       break;                                             // the call has failed
@@ -1687,7 +1719,7 @@ __device__ __noinline__ void compute_loop(const Params &p, Smem &sm, const unsig
     const int64_t t = sm.tk[k];
     const unsigned char *stage = dyn + k * kStageBytes;
     const uint64_t tb = (tid == 0) ? globaltimer() : 0;
-    if (tid == 0) beat(p, sm.role, HB_UNIT, ((uint64_t)j << 32) | (uint32_t)t);
+    if (lane == 0) beat(p, sm.role, HB_UNIT, ((uint64_t)j << 32) | (uint32_t)t);
     if (kind == U_PLAN) {
       chunk_aggregate(p, sm, stage, k, t, ntiles);
       if (tid == 0) atomicAdd(&sm.st[S_NS_PHASE_A], (unsigned)(globaltimer() - tb));
@@ -1777,6 +1809,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
   int64_t ntiles = (p.ntiles >= 0) ? p.ntiles : (int64_t)__ldcg(&p.ctr[C_NTILES]);
   if (ntiles > p.cap_tiles) ntiles = 0;                  // the set-up flagged ERR_CAPACITY
   if (tid < S_COUNT) sm.st[tid] = 0;
+  if (tid < kWarps) sm.barcnt[tid] = 0;
   if (tid == 0) {
     for (int s = 0; s < kStages; s++) {
       mbar_init(&sm.full[s], 3);                         // control lanes 0 and 1 (copies) and lane 0 (unit)
@@ -1788,9 +1821,9 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
     // roles go to CTAs in the order they start, so every waiting role is
     // held by a running CTA
     sm.role = (int)atomicAdd(&p.ctr[C_ROLE], 1u);
-    beat(p, sm.role, HB_START, 0);
   }
   __syncthreads();
+  if ((tid & 31) == 0) beat(p, sm.role, HB_START, 0);
   const int role = sm.role;
 
   if (role < p.nwalkers) {
@@ -1802,9 +1835,9 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
       } else {
         while (true) {
           if (tid == 0) sm.sum_k = (int)atomicAdd(&p.ctr[C_SUMTICKET], 1u);
-          wide_sync();
+          wide_sync(p, sm, 24);
           const int k = sm.sum_k;
-          wide_sync();
+          wide_sync(p, sm, 25);
           if (k >= p.nsums) break;
           if (ntiles == 0) continue;                     // bad offsets or capacity: outputs already NaN
           const int64_t tb = __ldcg(&p.tile_begin[k]), te = __ldcg(&p.tile_begin[k + 1]);
@@ -1822,8 +1855,8 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
   }
 
   // ---- statistics and the last CTA's reset of the shared counters
+  if ((tid & 31) == 0) beat(p, sm.role, HB_END, 0);
   __syncthreads();
-  if (tid == 0) beat(p, sm.role, HB_END, 0);
   if (tid < S_ACCUM_END && sm.st[tid]) atomicAdd(&p.stats[tid], (unsigned long long)sm.st[tid]);
   if (tid == 0) {
     __threadfence();

@@ -56,7 +56,7 @@ def _watchdog(request):
             d = sq.debug_heartbeat(320)
             print(f"\nWATCHDOG {request.node.nodeid}: counters {d['counters']}", flush=True)
             for beat in d["beats"]:
-                print("  cta %d role %d what %d where %#x" % beat, flush=True)
+                print("  cta %d warp %d role %d what %d where %#x" % beat, flush=True)
         except Exception as e:          # diagnostics only
             print("WATCHDOG failed:", e, flush=True)
         os._exit(3)
