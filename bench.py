@@ -58,6 +58,25 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def measured_traffic(config: str, height_mult: int):
+    """DRAM bytes per launch of the kernel from a committed ncu capture
+    (profiles/), or None when the kernel's sources changed since it was taken
+    or the workload differs."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", f"seqsum_kernel_{config}_traffic.json")) as f:
+            rec = json.load(f)
+        h = hashlib.sha256()
+        for src in rec["kernel_sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != rec["kernel_sources_sha256"] or height_mult != 1:
+            return None
+        return int(rec["dram_bytes_read_per_launch"]) + int(rec["dram_bytes_write_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def dist_init():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -274,8 +293,9 @@ def main():
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "parity_0ulp": parity and e2e_ok,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "peak_source": peak_src,
-                     "algorithmic_bytes_per_launch": 8 * n},
+                     "frac": achieved / peak, "traffic": measured_traffic(args.config, args.height_mult),
+                     "peak_source": peak_src, "algorithmic_bytes_per_launch": 8 * n,
+                     "traffic_source": "profiles/seqsum_kernel_%s_traffic.json (null if the kernel changed)" % args.config},
         "e2e": {"value": n / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": 8 * n,
                 "d2h_bytes_per_step": 8},
         "gpu_launches": args.steps,
