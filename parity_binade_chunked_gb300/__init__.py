@@ -47,9 +47,10 @@ def lib():
     with _lock:
         if _lib is None:
             checks = os.environ.get("SEQSUM_CHECKS", "") == "1"
-            path = _build.CHECK_LIB if checks else _build.LIB
+            profile = os.environ.get("SEQSUM_PROFILE", "") == "1"
+            path = _build.CHECK_LIB if checks else (_build.PROFILE_LIB if profile else _build.LIB)
             if not os.path.exists(path):
-                path = _build.build(checks=checks)
+                path = _build.build(checks=checks, profile=profile)
             L = ctypes.CDLL(path)
             vp, i64, i32, d = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_double
             L.seqsum_f64.argtypes = [vp, i64, d, vp, vp]

@@ -41,10 +41,18 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, extra_flags=(), verbose: bool = False, checks: bool = False) -> str:
-    bdir, lib = (CHECK_BUILD, CHECK_LIB) if checks else (BUILD, LIB)
+# cycle-profiling variant (-DSEQSUM_PROFILE): the walk's sections summed into the diagnostic words
+PROFILE_BUILD = os.path.join(BUILD, "profile")
+PROFILE_LIB = os.path.join(PROFILE_BUILD, "libseqsum.so")
+
+
+def build(force: bool = False, extra_flags=(), verbose: bool = False, checks: bool = False,
+          profile: bool = False) -> str:
+    bdir, lib = (CHECK_BUILD, CHECK_LIB) if checks else ((PROFILE_BUILD, PROFILE_LIB) if profile else (BUILD, LIB))
     if checks:
         extra_flags = tuple(extra_flags) + ("-DSEQSUM_CHECKS",)
+    if profile:
+        extra_flags = tuple(extra_flags) + ("-DSEQSUM_PROFILE",)
     os.makedirs(bdir, exist_ok=True)
     inc = os.path.join(os.path.dirname(HERE), "include")
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(inc, "seqsum.h"), __file__]

@@ -60,13 +60,11 @@ static_assert(((uint64_t)kChunkSlots << (kCountBits * (kWarps - 1))) < (1ull << 
               "packed item counts must fit a tagged 56-bit word");
 constexpr int kWalkOffEl = 32768;              // walker layout in the dynamic shared memory
 constexpr int kWalkOffPos = 65536;
-constexpr int kWalkOffHead = 69632;
-constexpr int kWalkOffEnds = 70656;
+constexpr int kWalkOffEnds = 69632;
 static_assert(kWalkTiles * (int)sizeof(Rec) <= kWalkOffEl, "walk headers overlap the element list");
 static_assert(kWalkElems * (int)sizeof(Rec) <= kWalkOffEl, "segment composites overlap the element list");
 static_assert(kWalkOffEl + kWalkElems * (int)sizeof(Rec) <= kWalkOffPos, "element list overlaps positions");
-static_assert(kWalkOffPos + kWalkElems * 4 <= kWalkOffHead, "positions overlap head flags");
-static_assert(kWalkOffHead + kWalkElems <= kWalkOffEnds, "head flags overlap segment ends");
+static_assert(kWalkOffPos + kWalkElems * 4 <= kWalkOffEnds, "positions overlap segment ends");
 static_assert(kWalkOffEnds + kWalkElems * 4 <= kStages * kStageBytes, "walk buffers exceed the stages");
 static_assert(kWalkElems % kThreads == 0 && kWalkTiles % kThreads == 0, "walk batch split");
 
@@ -129,7 +127,7 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 struct Smem;
-__device__ __forceinline__ void wide_sync_at(const Params &p, Smem &sm, int site);
+__device__ __noinline__ void wide_sync_at(const Params &p, Smem &sm, int site);
 #define wide_sync(p, sm, site) wide_sync_at((p), (sm), (site))
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -443,6 +441,7 @@ struct Smem {
   // walker
   uint64_t S;
   int m, nel, restart, nseg;
+  int walk_m[kWarps];
   int wflag[kWarps];
   Run wagg[kWarps];
   int wcnt[kWarps];
@@ -463,7 +462,7 @@ static_assert(offsetof(Smem, full) % 8 == 0 && offsetof(Smem, done) % 8 == 0 && 
 
 // The 256-thread barrier of a walking or scanning CTA; each warp first
 // records the barrier's site and how many it has passed (its heartbeat).
-__device__ __forceinline__ void wide_sync_at(const Params &p, Smem &sm, int site) {
+__device__ __noinline__ void wide_sync_at(const Params &p, Smem &sm, int site) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) {
     const uint32_t c = ++sm.barcnt[warp];
@@ -1245,7 +1244,7 @@ __device__ __forceinline__ uint64_t absorb(uint64_t Sb, uint32_t flags) {
 
 // Term-by-term fallback over x[a, a + cnt), run by a whole warp; every lane
 // ends with the same S.  One __dadd_rn per term, in index order.
-__device__ uint64_t add_terms(const Params &p, uint64_t Sb, int64_t a, int64_t cnt, unsigned int *st) {
+__device__ __noinline__ uint64_t add_terms(const Params &p, uint64_t Sb, int64_t a, int64_t cnt, unsigned int *st) {
   const int lane = threadIdx.x & 31;
   const uint64_t t0 = globaltimer();
   double S = bitsd(Sb);
@@ -1285,68 +1284,183 @@ __device__ __forceinline__ int elem_key(const Rec &q) {
   return (rec_flags(q.meta) & F_ZERO) ? kZeroE : (int)q.e;
 }
 
-// Walk sum k over its tiles [tb, te), as the headers appear.  Whole CTA; the
-// serial part runs on warp 0.  The dynamic shared memory of a walking CTA
-// (it never copies tiles) holds:
-//   [0, 32K)       tile headers of the batch, later the segment composites
-//   [32K, 64K)     the batch's flat list of elements (headers and items)
-//   [64K, 68K)     per element: tile offset in the batch << 12 | first term
-//   [68K, 69K)     per element: segment head flag
-//   [69K, 73K)     segment ends
+// The in-order pass met a segment whose composite the check refused: find the
+// first element whose prefix composite the check refuses (the warp composes 32
+// prefixes at a time), apply the prefix before it, and add that element's
+// terms one by one.  The bounds of a composite depend on the shape of its
+// tree, so this composition may accept what the scan's refused; then the whole
+// segment is applied as composed here and -1 returned.  Else returns the
+// element added term by term; Sb is the exact sum after it.  Whole warp.
+__device__ __noinline__ int resolve_rejection(const Params &p, const Rec *el, const uint32_t *elpos, int segstart,
+                                              int ei, int e, int64_t pos, int64_t ntiles, unsigned int *st,
+                                              uint64_t &Sb) {
+  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  int kfail = -1;
+  Run racc = run_empty(), before = run_empty();
+  for (int c0 = segstart; c0 <= ei; c0 += 32) {
+    const int i = c0 + lane;
+    Run r = (i <= ei) ? rec_run(el[i]) : run_empty();
+#pragma unroll 1
+    for (int o = 1; o < 32; o <<= 1) {
+      const Run ov = shfl_run<SH_UP>(r, o);
+      if (lane >= o) r = run_compose(ov, r);
+    }
+    const Run pre = run_compose(racc, r);
+    bool bad = false;
+    if (i <= ei) { uint64_t T = Sb; bad = run_apply(T, pre, e) != APPLY_OK; }
+    const uint32_t bm = __ballot_sync(full, bad);
+    if (bm) {
+      kfail = c0 + __ffs(bm) - 1;
+      const int src = kfail - 1 - c0;
+      before = shfl_run<SH_IDX>(pre, src < 0 ? 0 : src);
+      if (src < 0) before = racc;
+      break;
+    }
+    racc = shfl_run<SH_IDX>(pre, 31);
+  }
+  if (kfail < 0) {
+    uint64_t T = Sb;
+    if (run_apply(T, racc, e) == APPLY_OK) {
+      Sb = T;
+      return -1;
+    }
+    kfail = segstart;                                  // not reached: the last prefix passed
+  } else if (kfail > segstart) {
+    uint64_t T = Sb;
+    if (run_apply(T, before, e) == APPLY_OK) Sb = T;
+    else kfail = segstart;                             // not reached: that prefix passed
+  }
+  const uint32_t ep = elpos[kfail];
+  const TileGeo g = tile_geo(p, pos + (ep >> 12), ntiles);
+  Sb = add_terms(p, Sb, g.start + (ep & 0xFFF), el[kfail].count, st);
+  return kfail;
+}
+
+#ifdef SEQSUM_PROFILE
+// Cycle profile of the walk (profiling builds): cycles since the previous
+// point, summed per point, for thread 0 and for thread 224 (warp 7).
+#define WALK_PT(id)                                                                        \
+  do {                                                                                     \
+    if (tid == 0 || tid == 224) {                                                          \
+      const long long now_ = clock64();                                                    \
+      atomicAdd(&p.dbg[15000 + 2 * (id) + (tid ? 1 : 0)], (unsigned long long)(now_ - prof_t)); \
+      prof_t = now_;                                                                       \
+    }                                                                                      \
+  } while (0)
+#else
+#define WALK_PT(id) do { } while (0)
+#endif
+
+// Walk sum k over its tiles [tb, te), as the headers appear.  Whole CTA (256
+// threads); the in-order pass runs on warp 0.  Per batch of up to 1024 ready
+// tiles: the headers are staged, the elements (simple tile headers, the items
+// of complex tiles) listed in order, every maximal run of same-binade run
+// elements composed by a segmented scan, and the segments applied in order.
+// The dynamic shared memory of a walking CTA (it never copies tiles) holds:
+//   [0, 32K)       the batch's headers (thread t: tiles 4t..4t+3), later the
+//                  segment composites
+//   [32K, 64K)     the batch's elements in order
+//   [64K, 68K)     per element: its tile in the batch << 12 | its first term
+//   [68K, 72K)     segment ends
 __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *dyn, int k, int64_t tb, int64_t te,
-                         int64_t ntiles) {
+                                      int64_t ntiles) {
+  constexpr int PT = kWalkTiles / kThreads;         // tiles, then elements, per thread
+  static_assert(kWalkTiles == kThreads * PT && kWalkElems == kThreads * PT, "walk batch shape");
   Rec *hdrs = reinterpret_cast<Rec *>(dyn);
   Rec *comp = hdrs;
   Rec *el = reinterpret_cast<Rec *>(dyn + kWalkOffEl);
   uint32_t *elpos = reinterpret_cast<uint32_t *>(dyn + kWalkOffPos);
-  unsigned char *head = dyn + kWalkOffHead;
   int *ends = reinterpret_cast<int *>(dyn + kWalkOffEnds);
   unsigned int *st = sm.st;
+  const unsigned full = 0xffffffffu;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t tag = (p.epoch << 1) | 1u;
-  constexpr int B = kWalkElems / kThreads;          // elements per thread in the scan
-  constexpr int BT = kWalkTiles / kThreads;         // tiles per thread
-  const double s0 = p.s0s ? p.s0s[k] : p.s0;
-  if (tid == 0) sm.S = dbits(s0);
+  if (tid == 0) sm.S = dbits(p.s0s ? p.s0s[k] : p.s0);
   int64_t pos = tb;
   uint64_t t_work0 = 0;
+#ifdef SEQSUM_PROFILE
+  long long prof_t = clock64();
+#endif
   wide_sync(p, sm, 6);
   while (pos < te) {
-    // ---- 1. the contiguous ready prefix [pos, pos + m)
+    // ---- A. the ready run of headers [pos, pos + m)
     const int want = (int)min((int64_t)kWalkTiles, te - pos);
     const uint64_t t0 = globaltimer();
-    if (tid == 0 && t_work0 != 0) atomicAdd(&st[S_NS_WALK_WORK], (unsigned)(t0 - t_work0));
-    if (tid == 0) beat(p, sm.role, HB_WAIT_HEADERS, (uint64_t)pos);
+    if (tid == 0) {
+      if (t_work0 != 0) atomicAdd(&st[S_NS_WALK_WORK], (unsigned)(t0 - t_work0));
+      beat(p, sm.role, HB_WAIT_HEADERS, (uint64_t)pos);
+    }
+    int m;
     while (true) {
-      if (tid == 0) sm.m = want;
-      wide_sync(p, sm, 7);
-      for (int i = tid; i < want; i += kThreads) {
-        Rec h;
-        const int rh = sq_ok(p, pos + i < p.cap_tiles, 11, pos + i) ? read_header(p.hdr + pos + i, tag, h) : 0;
-        if (rh > 0) {
-          hdrs[i] = h;
-        } else {
-          atomicMin(&sm.m, i);
-          if (rh < 0) atomicAdd(&st[S_TORN_HEADER], 1u);
+      uint64_t w[PT][4];
+#pragma unroll
+      for (int q = 0; q < PT; q++) {
+        const int i = PT * tid + q;
+        w[q][0] = w[q][1] = w[q][2] = w[q][3] = 0;
+        if (i < want && sq_ok(p, pos + i < p.cap_tiles, 11, pos + i)) {
+          ld_vol_v2(p.hdr + pos + i, w[q][0], w[q][1]);
+          ld_vol_v2(reinterpret_cast<const char *>(p.hdr + pos + i) + 16, w[q][2], w[q][3]);
         }
       }
-      wide_sync(p, sm, 8);
-      if (sm.m > 0) break;
-      // thread 0 alone decides whether to give up, so the CTA stays together
+      int gap = want;                                  // this thread's first tile not (fully) published
+#pragma unroll
+      for (int q = PT - 1; q >= 0; q--) {
+        const int i = PT * tid + q;
+        const int nt = ((uint32_t)(w[q][0] >> 56) == tag) + ((uint32_t)(w[q][1] >> 56) == tag) +
+                       ((uint32_t)(w[q][2] >> 56) == tag) + ((uint32_t)((w[q][3] >> 24) & 0xFFu) == tag);
+        if (i < want && nt != 4) {
+          gap = i;
+          if (nt != 0) atomicAdd(&st[S_TORN_HEADER], 1u);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < PT; q++) {
+        const int i = PT * tid + q;
+        if (i < gap) {
+          Rec h;
+          h.inc = untag56(w[q][0]);
+          h.lo = untag56(w[q][1]);
+          h.hi = untag56(w[q][2]);
+          h.meta = (uint32_t)w[q][3] & 0x00FFFFFFu;
+          h.e = (int16_t)(uint16_t)(w[q][3] >> 32);
+          h.count = (uint16_t)(w[q][3] >> 48);
+          hdrs[i] = h;
+        }
+      }
+      const int wm = (int)__reduce_min_sync(full, (uint32_t)gap);
+      if (lane == 0) sm.walk_m[warp] = wm;
+      wide_sync(p, sm, 7);
+      m = want;
+#pragma unroll
+      for (int w2 = 0; w2 < kWarps; w2++) m = min(m, sm.walk_m[w2]);
+      // a batch costs about the same whatever its size (its steps are
+      // latency-bound), so the walk takes full batches: 1024 tiles, or the
+      // rest of the sum
+      if (m == want) break;
+      // not all ready yet; thread 0 alone decides whether to give up
       if (tid == 0) sm.restart = (globaltimer() - t0 > kWaitNs) ? 1 : 0;
-      wide_sync(p, sm, 9);
+      wide_sync(p, sm, 8);
       if (sm.restart) {
         if (tid == 0) {
           note_timeout(p, ERR_WALK_TIMEOUT, TO_WALK, (uint32_t)pos, (uint32_t)want);
           p.outs[k] = __longlong_as_double(0x7FF8000000000000ll);
         }
-        wide_sync(p, sm, 10);
+        wide_sync(p, sm, 9);
         return;
       }
-      __nanosleep(200);
+      __nanosleep(500);
     }
-    int m = sm.m;
-    __threadfence();
+    WALK_PT(1);                                        // waiting for headers
+    {
+      // a thread that saw a complex header orders the tile's items (read
+      // later, after barriers, by any thread) after it
+      bool saw_complex = false;
+#pragma unroll
+      for (int q = 0; q < PT; q++)
+        if (PT * tid + q < m && rec_kind(hdrs[PT * tid + q].meta) == K_COMPLEX) saw_complex = true;
+      if (saw_complex) __threadfence();
+    }
     if (tid == 0) {
       beat(p, sm.role, HB_BATCH, ((uint64_t)m << 32) | (uint32_t)pos);
       atomicAdd(&st[S_WALK_BATCHES], 1u);
@@ -1354,21 +1468,21 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       atomicAdd(&st[S_NS_WALK_WAIT], (unsigned)(t_work0 - t0));
       if (pos + m >= te) p.stats[S_T_WALK0] = t_work0;
     }
-    // ---- 2. elements per tile and their prefix; the batch is cut where the
-    //         flat list would overflow, then the prefix is taken again
-    if (lane == 0) beat(p, sm.role, HB_COUNT, ((uint64_t)m << 32) | (uint32_t)pos);
-    int cnt[BT];
-    int mine = 0, wbase = 0, incl = 0;
+    // ---- B. elements per tile and their offsets; a batch whose elements do
+    //         not fit is cut before the first tile that overflows
+    int cnt[PT];
+    int off0 = 0, nel = 0;
     for (int pass = 0; pass < 2; pass++) {
-      mine = 0;
-#pragma unroll 1
-      for (int q = 0; q < BT; q++) {
-        const int i = tid * BT + q;
+      int mine = 0;
+#pragma unroll
+      for (int q = 0; q < PT; q++) {
+        const int i = PT * tid + q;
         int c = 0;
         if (i < m) {
           const Rec &h = hdrs[i];
           if (rec_kind(h.meta) == K_COMPLEX) {
             const uint64_t packed = (uint64_t)h.inc;
+#pragma unroll
             for (int cc = 0; cc < kWarps; cc++) c += (int)((packed >> (kCountBits * cc)) & kCountMask);
           } else {
             c = 1;
@@ -1378,64 +1492,77 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         cnt[q] = c;
         mine += c;
       }
-      incl = mine;
-#pragma unroll 1
+      int incl = mine;
+#pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        const int v = __shfl_up_sync(full, incl, o);
         if (lane >= o) incl += v;
       }
-      wide_sync(p, sm, 11);
       if (lane == 31) sm.wcnt[warp] = incl;
-      wide_sync(p, sm, 12);
-      wbase = 0;
-      for (int w = 0; w < warp; w++) wbase += sm.wcnt[w];
-      if (pass == 1) break;
-      int off = wbase + incl - mine;
-#pragma unroll 1
-      for (int q = 0; q < BT; q++) {
-        const int i = tid * BT + q;
-        if (i < m && off + cnt[q] > kWalkElems) atomicMin(&sm.m, i);
-        off += cnt[q];
+      wide_sync(p, sm, 10);
+      int wbase = 0;
+      nel = 0;
+#pragma unroll
+      for (int w2 = 0; w2 < kWarps; w2++) {
+        const int v = sm.wcnt[w2];
+        wbase += (w2 < warp) ? v : 0;
+        nel += v;
       }
-      wide_sync(p, sm, 13);
-      m = sm.m;
+      off0 = wbase + incl - mine;
+      if (nel <= kWalkElems) break;
+      // (rare) the first tile whose elements would not fit ends the batch
+      int cut = m, o = off0;
+#pragma unroll
+      for (int q = 0; q < PT; q++) {
+        const int i = PT * tid + q;
+        if (i < m && o + cnt[q] > kWalkElems && cut == m) cut = i;
+        o += cnt[q];
+      }
+      const int wc = (int)__reduce_min_sync(full, (uint32_t)cut);
+      wide_sync(p, sm, 11);                            // every thread has read sm.wcnt
+      if (lane == 0) sm.walk_m[warp] = wc;
+      wide_sync(p, sm, 12);
+#pragma unroll
+      for (int w2 = 0; w2 < kWarps; w2++) m = min(m, sm.walk_m[w2]);
     }
+    WALK_PT(2);                                        // counts and offsets
     uint64_t tsec = 0;
     if (tid == 0) { tsec = globaltimer(); atomicAdd(&st[S_NS_WALK_COUNT], (unsigned)(tsec - t_work0)); }
-    // ---- 3. the flat element list: simple tiles by their thread; the items
-    //         of complex tiles by the whole block, one item per thread
-    if (lane == 0) beat(p, sm.role, HB_GATHER, ((uint64_t)m << 32) | (uint32_t)pos);
+    // ---- C. the ordered elements: simple headers by their thread; for a
+    //         complex tile its thread marks the items' places, and the block
+    //         loads the items, one per thread
     {
-      int off = wbase + incl - mine;
-#pragma unroll 1
-      for (int q = 0; q < BT; q++) {
-        const int i = tid * BT + q;
-        if (i >= m) break;
-        const Rec h = hdrs[i];
-        if (rec_kind(h.meta) != K_COMPLEX) {
-          if (sq_ok(p, off >= 0 && off < kWalkElems, 12, off)) {
-            el[off] = h;
-            elpos[off] = (uint32_t)i << 12;
-          }
-        } else {
-          // mark: elpos holds (tile << 12 | chunk << 8 | item) + a flag bit, filled below
-          const uint64_t packed = (uint64_t)h.inc;
-          int o2 = off;
-          for (int cc = 0; cc < kWarps; cc++) {
-            const int n = (int)((packed >> (kCountBits * cc)) & kCountMask);
-            for (int u = 0; u < n; u++) {
-              if (sq_ok(p, o2 >= 0 && o2 < kWalkElems && u < kChunkSlots, 13, ((int64_t)o2 << 32) | (u << 8) | cc))
-                elpos[o2] = 0x80000000u | ((uint32_t)i << 12) | ((uint32_t)cc << 8) | (uint32_t)u;
-              o2++;
+      int off = off0;
+#pragma unroll
+      for (int q = 0; q < PT; q++) {
+        const int i = PT * tid + q;
+        if (i < m) {
+          const Rec h = hdrs[i];
+          if (rec_kind(h.meta) != K_COMPLEX) {
+            if (sq_ok(p, off >= 0 && off < kWalkElems, 12, off)) {
+              el[off] = h;
+              elpos[off] = (uint32_t)i << 12;
+            }
+          } else {
+            const uint64_t packed = (uint64_t)h.inc;
+            int o2 = off;
+            for (int cc = 0; cc < kWarps; cc++) {
+              const int n = (int)((packed >> (kCountBits * cc)) & kCountMask);
+              for (int u = 0; u < n; u++) {
+                if (sq_ok(p, o2 >= 0 && o2 < kWalkElems && u < kChunkSlots, 13, ((int64_t)o2 << 32) | (u << 8) | cc))
+                  elpos[o2] = 0x80000000u | ((uint32_t)i << 12) | ((uint32_t)cc << 8) | (uint32_t)u;
+                o2++;
+              }
             }
           }
         }
         off += cnt[q];
       }
-      if (tid == kThreads - 1) sm.nel = wbase + incl;
     }
-    wide_sync(p, sm, 14);
-    for (int j = tid; j < sm.nel && j < kWalkElems; j += kThreads) {
+    WALK_PT(3);                                        // placing elements
+    wide_sync(p, sm, 13);
+    WALK_PT(4);
+    for (int j = tid; j < nel; j += kThreads) {
       const uint32_t ep = elpos[j];
       if (ep & 0x80000000u) {
         const uint32_t i = (ep >> 12) & 0x7FFFFu, cc = (ep >> 8) & 0xFu, u = ep & 0xFFu;
@@ -1452,105 +1579,130 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         }
       }
     }
-    wide_sync(p, sm, 15);
-#ifdef SEQSUM_CHECKS
-    if (pos == tb) {
-      for (int j = tid; j < sm.nel && j < 4000; j += kThreads) {
-        const Rec q = el[j];
-        p.dbg[8192 + j] = (unsigned long long)rec_kind(q.meta) | ((unsigned long long)q.count << 8) |
-                          ((unsigned long long)rec_tstart(q.meta) << 24) | ((unsigned long long)elpos[j] << 36) |
-                          ((unsigned long long)(q.e & 0xFFF) << 52);
-      }
-      for (int i = tid; i < m && i < 64; i += kThreads) p.dbg[12800 + i] = (unsigned long long)hdrs[i].inc;
-      if (tid == 0) p.dbg[12799] = (unsigned long long)sm.nel;
-    }
-#endif
-    const int nel = min(sm.nel, kWalkElems);
+    WALK_PT(5);                                        // loading items
+    wide_sync(p, sm, 14);
+    WALK_PT(6);
     if (tid == 0) { const uint64_t t2 = globaltimer(); atomicAdd(&st[S_NS_WALK_GATHER], (unsigned)(t2 - tsec)); tsec = t2; }
-    // ---- 4. segmented scan and serial application (restarted after a rejected run)
+    // ---- D. segmented scan of elements [from, nel) and E. the in-order
+    //         pass (again from the element after a rejected run's failure)
     int from = 0;
     while (from < nel) {
       if (lane == 0) beat(p, sm.role, HB_SCAN, ((uint64_t)nel << 32) | ((uint64_t)from << 16) | (uint32_t)(pos & 0xFFFF));
-      for (int i = from + tid; i < nel; i += kThreads) {
-        const Rec q = el[i];
-        bool hd = (i == from) || elem_alone(q);
-        if (!hd) {
-          const Rec pq = el[i - 1];
-          hd = elem_alone(pq) || elem_key(pq) != elem_key(q);
-        }
-        head[i] = hd ? 1 : 0;
+      const int j0 = PT * tid;
+      // pass 1: this thread's elements in order -- heads (an element alone,
+      // or a binade change, starts a segment) and the composite since the
+      // last head
+      int pkey = 0;
+      bool palone = true;
+      if (j0 - 1 >= from && j0 - 1 < nel) {
+        const Rec pq = el[j0 - 1];
+        pkey = elem_key(pq);
+        palone = elem_alone(pq);
       }
-      wide_sync(p, sm, 16);
-      Run agg = run_empty();
-      bool has_head = false;
-      int first_head = B;
-      Run incls[B];
+      Run acc = run_empty();
+      uint32_t hdmask = 0, valmask = 0;                // bit q: element j0 + q starts a segment / is walked
+      int lastkey = 0;
+      bool lastalone = true;
 #pragma unroll 1
-      for (int jj = 0; jj < B; jj++) {
-        const int i = tid * B + jj;
-        incls[jj] = run_empty();
-        if (i < from || i >= nel) continue;
-        const Run r = rec_run(el[i]);
-        if (head[i]) { agg = r; if (!has_head) first_head = jj; has_head = true; }
-        else agg = run_compose(agg, r);
-        incls[jj] = agg;
+      for (int q = 0; q < PT; q++) {
+        const int j = j0 + q;
+        if (j < from || j >= nel) continue;
+        const Rec x = el[j];
+        const int kx = elem_key(x);
+        const bool ax = elem_alone(x);
+        const int kp = (q == 0 || !(valmask & 1u << (q - 1))) ? pkey : lastkey;
+        const bool ap = (q == 0 || !(valmask & 1u << (q - 1))) ? palone : lastalone;
+        const bool h = (j == from) || ax || ap || kp != kx;
+        const Run r = rec_run(x);
+        acc = h ? r : run_compose(acc, r);
+        valmask |= 1u << q;
+        if (h) hdmask |= 1u << q;
+        lastkey = kx;
+        lastalone = ax;
       }
-      Run v = agg;
-      int f = has_head ? 1 : 0;
+      // segment ends: the last element, or one whose successor starts a segment
+      const int nhd0 = __shfl_down_sync(full, (int)(hdmask & 1u), 1);
+      bool next_head_last = true;
+      if (lane < 31) {
+        next_head_last = nhd0 != 0;
+      } else if (j0 + PT < nel) {
+        const Rec xn = el[j0 + PT];
+        next_head_last = elem_alone(xn) || lastalone || elem_key(xn) != lastkey;
+      }
+      uint32_t endmask = 0;
+#pragma unroll 1
+      for (int q = 0; q < PT; q++) {
+        const int j = j0 + q;
+        const bool nh = (q + 1 < PT) ? ((hdmask >> (q + 1)) & 1u) != 0 : next_head_last;
+        if ((valmask >> q) & 1u && (j == nel - 1 || nh)) endmask |= 1u << q;
+      }
+      const int my = __popc(endmask);
+      // across the warp: (head seen, composite) and the end counts
+      Run v = acc;
+      int f = hdmask ? 1 : 0;
+      int ie = my;
 #pragma unroll 1
       for (int o = 1; o < 32; o <<= 1) {
         const Run ov = shfl_run<SH_UP>(v, o);
-        const int of = __shfl_up_sync(0xffffffffu, f, o);
-        if (lane >= o) { if (!f) v = run_compose(ov, v); f |= of; }
+        const int of = __shfl_up_sync(full, f, o);
+        const int oe = __shfl_up_sync(full, ie, o);
+        if (lane >= o) {
+          if (!f) v = run_compose(ov, v);
+          f |= of;
+          ie += oe;
+        }
       }
-      if (lane == 31) { sm.wagg[warp] = v; sm.wflag[warp] = f; }
-      wide_sync(p, sm, 17);
+      if (lane == 31) { sm.wagg[warp] = v; sm.wflag[warp] = f; sm.wcnt[warp] = ie; }
+      WALK_PT(7);                                      // local and warp composition
+      wide_sync(p, sm, 15);
+      WALK_PT(8);
+      // the composite before this thread's first element: earlier warps, then
+      // earlier lanes of this warp
       Run ex = run_empty();
+      int eb = 0, nseg = 0;
 #pragma unroll 1
-      for (int w = 0; w < warp; w++) {
-        if (sm.wflag[w]) ex = sm.wagg[w];
-        else ex = run_compose(ex, sm.wagg[w]);
+      for (int w2 = 0; w2 < kWarps; w2++) {
+        if (w2 < warp) {
+          if (sm.wflag[w2]) ex = sm.wagg[w2];
+          else ex = run_compose(ex, sm.wagg[w2]);
+          eb += sm.wcnt[w2];
+        }
+        nseg += sm.wcnt[w2];
       }
       {
         const Run lv = shfl_run<SH_UP>(v, 1);
-        const int lf = __shfl_up_sync(0xffffffffu, f, 1);
-        if (lane >= 1) { if (lf) ex = lv; else ex = run_compose(ex, lv); }
+        const int lf = __shfl_up_sync(full, f, 1);
+        if (lane >= 1) {
+          if (lf) ex = lv;
+          else ex = run_compose(ex, lv);
+        }
       }
+      // pass 2: each segment end's composite (again in order from the
+      // thread's first element), in order into the segment list
+      int epos = eb + ie - my;
+      Run cur = ex;
 #pragma unroll 1
-      for (int jj = 0; jj < B; jj++)
-        if (jj < first_head) incls[jj] = run_compose(ex, incls[jj]);
-      // segment ends, compacted in order, with their composites
-      int my = 0;
-      int idx[B];
-#pragma unroll 1
-      for (int jj = 0; jj < B; jj++) {
-        const int i = tid * B + jj;
-        if (i >= from && i < nel && (i == nel - 1 || head[i + 1])) idx[my++] = jj;
+      for (int q = 0; q < PT; q++) {
+        const int j = j0 + q;
+        if (!((valmask >> q) & 1u)) continue;
+        const Rec x = el[j];
+        const Run r = rec_run(x);
+        cur = ((hdmask >> q) & 1u) ? r : run_compose(cur, r);
+        if ((endmask >> q) & 1u) {
+          if (sq_ok(p, epos < kWalkElems, 15, epos)) {
+            ends[epos] = j;
+            comp[epos] = make_rec(cur, x.e, rec_kind(x.meta), x.count, rec_tstart(x.meta));
+          }
+          epos++;
+        }
       }
-      int inc2 = my;
-#pragma unroll 1
-      for (int o = 1; o < 32; o <<= 1) {
-        const int vv = __shfl_up_sync(0xffffffffu, inc2, o);
-        if (lane >= o) inc2 += vv;
-      }
-      if (lane == 31) sm.wcnt[warp] = inc2;
-      wide_sync(p, sm, 18);
-      int eb2 = 0;
-      for (int w = 0; w < warp; w++) eb2 += sm.wcnt[w];
-      const int epos = eb2 + inc2 - my;
-#pragma unroll 1
-      for (int jj = 0; jj < B; jj++) {
-        if (jj >= my) break;
-        const int i = tid * B + idx[jj];
-        const Rec q = el[i];
-        if (!sq_ok(p, epos + jj < kWalkElems, 15, epos + jj)) break;
-        ends[epos + jj] = i;
-        comp[epos + jj] = make_rec(incls[idx[jj]], q.e, rec_kind(q.meta), q.count, rec_tstart(q.meta));
-      }
-      if (tid == kThreads - 1) sm.nseg = epos + my;
-      wide_sync(p, sm, 19);
+      WALK_PT(9);                                      // cross-warp prefix, segment list
+      WALK_PT(10);
+      WALK_PT(11);
+      wide_sync(p, sm, 17);
+      WALK_PT(12);
       if (tid == 0) { const uint64_t t2 = globaltimer(); atomicAdd(&st[S_NS_WALK_SCAN], (unsigned)(t2 - tsec)); tsec = t2; }
-      // ---- serial part on warp 0
+      // ---- E. the in-order pass (warp 0)
 #ifdef SEQSUM_CHECKS
       auto abs_start = [&](int j) -> int64_t {
         const uint32_t ep = elpos[j];
@@ -1561,14 +1713,11 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         uint64_t Sb = sm.S;
         int restart = -1;
         int segstart = from;
-        const int ns = sm.nseg;
-        for (int sidx = 0; sidx < ns; sidx++) {
+        unsigned nterms = 0, nrej = 0;
+        for (int sidx = 0; sidx < nseg; sidx++) {
           const int ei = ends[sidx];
           const Rec c = comp[sidx];
           const uint32_t kind = rec_kind(c.meta);
-          if (lane == 0)
-            beat(p, sm.role, HB_SERIAL, ((uint64_t)kind << 40) | ((uint64_t)ns << 24) | ((uint64_t)ei << 12) | (uint32_t)sidx);
-          if (lane == 0) atomicAdd(&st[S_WALK_SEGMENTS], 1u);
           if (nonfinite(Sb)) {
             Sb = absorb(Sb, rec_flags(c.meta));
             WALK_TRACE(abs_start(segstart), abs_start(ei) + el[ei].count, 6u, Sb);
@@ -1576,7 +1725,6 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
             continue;
           }
           if (kind == K_TERMS) {
-            const uint64_t ta0 = globaltimer();
             const Rec q = el[ei];
             double S = bitsd(Sb);
             const int nt = (int)q.count;
@@ -1584,10 +1732,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
             if (nt > 1) S = __dadd_rn(S, bitsd((uint64_t)q.lo));
             if (nt > 2) S = __dadd_rn(S, bitsd((uint64_t)q.hi));
             Sb = dbits(S);
-            if (lane == 0) {
-              atomicAdd(&st[S_TERMS_ADDED], (unsigned)nt);
-              atomicAdd(&st[S_NS_WALK_ADDS], (unsigned)(globaltimer() - ta0));
-            }
+            nterms += (unsigned)nt;
             WALK_TRACE(abs_start(ei), abs_start(ei) + nt, 2u, Sb);
             segstart = ei + 1;
             continue;
@@ -1610,58 +1755,11 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
               continue;
             }
           }
-          if (lane == 0) atomicAdd(&st[S_RUN_REJECTED], 1u);
-          // the first element of the segment whose prefix composite the
-          // check rejects: the warp composes 32 prefixes at a time.  The
-          // bounds of a composite depend on the shape of its tree, so this
-          // composition may accept what the scan's rejected: then the whole
-          // segment is applied as composed here.
-          int kfail = -1;
-          Run acc = run_empty(), before = run_empty();
-          for (int c0 = segstart; c0 <= ei; c0 += 32) {
-            const int i = c0 + lane;
-            Run r = (i <= ei) ? rec_run(el[i]) : run_empty();
-      #pragma unroll 1
-      for (int o = 1; o < 32; o <<= 1) {
-              const Run ov = shfl_run<SH_UP>(r, o);
-              if (lane >= o) r = run_compose(ov, r);
-            }
-            const Run pre = run_compose(acc, r);
-            bool bad = false;
-            if (i <= ei) { uint64_t T = Sb; bad = run_apply(T, pre, c.e) != APPLY_OK; }
-            const uint32_t bm = __ballot_sync(0xffffffffu, bad);
-            if (bm) {
-              kfail = c0 + __ffs(bm) - 1;
-              const int src = kfail - 1 - c0;
-              before = shfl_run<SH_IDX>(pre, src < 0 ? 0 : src);
-              if (src < 0) before = acc;
-              break;
-            }
-            acc = shfl_run<SH_IDX>(pre, 31);
-          }
-          if (kfail < 0) {
-            uint64_t T = Sb;
-            if (run_apply(T, acc, c.e) == APPLY_OK) {
-              Sb = T;
-              WALK_TRACE(abs_start(segstart), abs_start(ei) + el[ei].count, 3u, Sb);
-              segstart = ei + 1;
-              continue;
-            }
-            kfail = segstart;                            // not reached: the last prefix passed
-          } else if (kfail > segstart) {
-            uint64_t T = Sb;
-            if (run_apply(T, before, c.e) == APPLY_OK) {
-              Sb = T;
-              WALK_TRACE(abs_start(segstart), abs_start(kfail), 4u, Sb);
-            } else {
-              kfail = segstart;                          // not reached: that prefix passed
-            }
-          }
-          {
-            const uint32_t ep = elpos[kfail];
-            const TileGeo g = tile_geo(p, pos + (ep >> 12), ntiles);
-            Sb = add_terms(p, Sb, g.start + (ep & 0xFFF), el[kfail].count, st);
-            WALK_TRACE(abs_start(kfail), abs_start(kfail) + el[kfail].count, 5u, Sb);
+          nrej++;
+          const int kfail = resolve_rejection(p, el, elpos, segstart, ei, c.e, pos, ntiles, st, Sb);
+          if (kfail < 0) {                             // the segment applied as composed here
+            segstart = ei + 1;
+            continue;
           }
           if (kfail < ei) { restart = kfail + 1; break; }
           segstart = ei + 1;
@@ -1673,20 +1771,24 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
         if (lane == 0) {
           sm.S = Sb;
           sm.restart = restart;
+          atomicAdd(&st[S_WALK_SEGMENTS], (unsigned)nseg);
+          if (nterms) atomicAdd(&st[S_TERMS_ADDED], nterms);
+          if (nrej) atomicAdd(&st[S_RUN_REJECTED], nrej);
           const uint64_t t2 = globaltimer();
           atomicAdd(&st[S_NS_WALK_SERIAL], (unsigned)(t2 - tsec));
           tsec = t2;
         }
       }
-      if (lane == 0) beat(p, sm.role, HB_RESTART, (uint64_t)from);
-      wide_sync(p, sm, 20);
+      WALK_PT(13);                                     // the in-order pass (warp 0)
+      wide_sync(p, sm, 18);
+      WALK_PT(14);
       const int rs = sm.restart;
-      wide_sync(p, sm, 21);
       if (rs < 0) break;
       from = rs;
     }
     pos += m;
-    wide_sync(p, sm, 22);
+    wide_sync(p, sm, 19);
+    WALK_PT(15);
   }
   if (tid == 0) {
     p.outs[k] = bitsd(sm.S);
@@ -1694,7 +1796,7 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
     p.stats[S_T_WALK1] = tend;
     if (t_work0 != 0) atomicAdd(&st[S_NS_WALK_WORK], (unsigned)(tend - t_work0));
   }
-  wide_sync(p, sm, 23);
+  wide_sync(p, sm, 20);
 }
 
 // ---------------------------------------------------------------- the streaming loops
