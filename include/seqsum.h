@@ -125,8 +125,8 @@ typedef struct {
   int64_t walk_batches;      /* batches of tile headers the walk took */
   int64_t ns_tma_wait;       /* nanoseconds, summed over CTAs: compute warps waiting for a unit */
   int64_t ns_prefix_wait;    /* ... run units waiting for the plan's prefix of their tile */
-  int64_t ns_phase_a;        /* ... compute warps on plan units */
-  int64_t ns_phase_b;        /* ... compute warps on run units (the prefix wait included) */
+  int64_t ns_phase_a;        /* ... compute warps on plan units (the fixed-point sums of a tile) */
+  int64_t ns_phase_b;        /* ... compute warps on run units (runs and items) */
   int64_t ns_walk_wait;      /* ... the walk waiting for tile headers */
   int64_t ns_walk_work;      /* ... the walk working */
   int64_t torn_header_reads; /* tile-header reads that saw words of two publications (retried) */
@@ -137,9 +137,11 @@ typedef struct {
   int64_t ns_walk_scan;      /* ... composing same-binade segments in parallel */
   int64_t ns_walk_serial;    /* ... the in-order pass over the segments */
   int64_t ns_walk_adds;      /* ... of which term-by-term fp64 adds */
-  int64_t plan_local;        /* tiles whose prefix range spans two binades (planned chunk by chunk) */
+  int64_t chunks_dirty;      /* chunks whose prefix range spans two binades (placed lane by lane) */
   int64_t ns_ctrl_wait;      /* nanoseconds, summed: control warps waiting for their compute warps */
   int64_t ns_scan_wait;      /* nanoseconds: the prefix scanner waiting for tiles' sums */
+  int64_t ns_verdict;        /* nanoseconds, summed: run units forming their chunks' verdicts */
+  int64_t ns_verdict_wait;   /* nanoseconds, summed: run units reading plan words not copied in time */
   int64_t t_stream_ns;       /* latest call: kernel start to the last tile header */
   int64_t t_walk_tail_ns;    /* latest call: last tile header to the end of the walk */
   int64_t t_total_ns;        /* latest call: kernel start to the end of the walk */
@@ -174,14 +176,14 @@ void seqsum_release_workspace(void);
  * plan cannot make the result wrong, only slower.  Returns the old mode. */
 int seqsum_debug_set_plan(int mode);
 
-/* Test hook: copies up to 16384 diagnostic words that self-checking builds
- * of the library record (a trace of the walk; zeros otherwise) and clears
- * them. */
+/* Test hook: copies up to 65536 diagnostic words that self-checking and
+ * profiling builds of the library record (a trace of the walk, a timeline of
+ * the units; zeros otherwise) and clears them. */
 int seqsum_debug_read(unsigned long long *out, int n);
 
 /* Diagnostics of a call that does not finish: copies the device counters of
  * the most recent call's workspace into out[0..16) and, per warp (index
- * CTA * 9 + warp), a heartbeat word into out[16..n) (role << 56 | what it
+ * CTA * 10 + warp), a heartbeat word into out[16..n) (role << 56 | what it
  * waits for or does << 48 | where).  It takes no lock and reads on a stream of its own, so it can run
  * while another thread waits on that call.  16 <= n <= 16 + 4096. */
 int seqsum_debug_heartbeat(unsigned long long *out, int n);

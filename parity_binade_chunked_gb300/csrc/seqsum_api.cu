@@ -25,7 +25,7 @@ struct Workspace {
   cudaStream_t stream = nullptr;
   int64_t cap_tiles = 0, cap_sums = 0;
   uint64_t *status = nullptr;        // the plan's prefix words, 2 per tile
-  uint64_t *tagg = nullptr;          // the plan's tile sums, 2 words per tile
+  uint64_t *cplan = nullptr;         // the plan's chunk sums, 4 words per chunk
   Rec *hdr = nullptr;                // one header per tile
   Rec *items = nullptr;              // kTileSlots items per tile
   uint32_t *ctr = nullptr;
@@ -46,9 +46,9 @@ std::map<std::pair<int, cudaStream_t>, Workspace *> g_ws;
 Workspace *g_last = nullptr;
 int g_last_cuda = 0;
 int g_plan_mode = 0;
-int64_t g_wave = 0;                  // tiles plan units run ahead of run units (0: not yet read)
 int g_blocks_per_sm = 0;
 int g_num_sms[64] = {0};
+int64_t g_wave = 0;                  // tiles plan units run ahead of run units (0: not yet read)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int cuda_fail(cudaError_t e) {
@@ -58,11 +58,11 @@ int cuda_fail(cudaError_t e) {
 
 void ws_free(Workspace *w) {
   cudaFree(w->status);
-  cudaFree(w->tagg);
+  cudaFree(w->cplan);
   cudaFree(w->hdr);
   cudaFree(w->items);
   cudaFree(w->tile_begin);
-  w->status = w->tagg = nullptr;
+  w->status = w->cplan = nullptr;
   w->hdr = w->items = nullptr;
   w->tile_begin = nullptr;
   w->cap_tiles = w->cap_sums = 0;
@@ -83,10 +83,10 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
     if ((e = cudaMalloc(&w->stats, sq::S_COUNT * sizeof(unsigned long long))) != cudaSuccess)
       return cuda_fail(e);
     if ((e = cudaMallocHost(&w->h_pin, 2 * sizeof(int64_t))) != cudaSuccess) return cuda_fail(e);
-    if ((e = cudaMalloc(&w->dbg, 16384 * sizeof(unsigned long long))) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMalloc(&w->dbg, sq::kDbgAlloc * sizeof(unsigned long long))) != cudaSuccess) return cuda_fail(e);
     if ((e = cudaMalloc(&w->hb, sq::kHeartbeats * sizeof(unsigned long long))) != cudaSuccess) return cuda_fail(e);
     cudaMemset(w->hb, 0, sq::kHeartbeats * sizeof(unsigned long long));
-    cudaMemset(w->dbg, 0, 16384 * sizeof(unsigned long long));
+    cudaMemset(w->dbg, 0, sq::kDbgAlloc * sizeof(unsigned long long));
     cudaMemset(w->ctr, 0, sq::C_COUNT * sizeof(uint32_t));
     cudaMemset(w->stats, 0, sq::S_COUNT * sizeof(unsigned long long));
   }
@@ -97,7 +97,7 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
     const int64_t cs = sums > w->cap_sums ? sums + 16 : w->cap_sums;
     ws_free(w);
     if (cudaMalloc(&w->status, ct * 2 * sizeof(uint64_t)) != cudaSuccess ||
-        cudaMalloc(&w->tagg, ct * 2 * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMalloc(&w->cplan, ct * sq::kWarps * 4 * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&w->hdr, ct * sizeof(Rec)) != cudaSuccess ||
         cudaMalloc(&w->items, ct * sq::kTileSlots * sizeof(Rec)) != cudaSuccess ||
         cudaMalloc(&w->tile_begin, (cs + 1) * sizeof(int64_t)) != cudaSuccess) {
@@ -106,7 +106,7 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
       return SEQSUM_ENOMEM;
     }
     cudaMemset(w->status, 0, ct * 2 * sizeof(uint64_t));
-    cudaMemset(w->tagg, 0, ct * 2 * sizeof(uint64_t));
+    cudaMemset(w->cplan, 0, ct * sq::kWarps * 4 * sizeof(uint64_t));
     cudaMemset(w->hdr, 0, ct * sizeof(Rec));
     w->cap_tiles = ct;
     w->cap_sums = cs;
@@ -144,14 +144,14 @@ int ensure_device_info() {
   return SEQSUM_OK;
 }
 
-// Next epoch for the tags (1..127); every tagged word (the plan's prefixes
-// and tile sums, the tile headers) is cleared whenever the tag wraps, so a
-// stale word can never carry a current tag.
+// Next epoch for the tags (1..127); every tagged word (the plan's sums and
+// prefixes, the tile headers) is cleared whenever the tag wraps, so a stale
+// word can never carry a current tag.
 void next_epoch(Workspace *w, cudaStream_t stream) {
   w->epoch++;
   if (w->epoch > 127) {
     cudaMemsetAsync(w->status, 0, w->cap_tiles * 2 * sizeof(uint64_t), stream);
-    cudaMemsetAsync(w->tagg, 0, w->cap_tiles * 2 * sizeof(uint64_t), stream);
+    cudaMemsetAsync(w->cplan, 0, w->cap_tiles * sq::kWarps * 4 * sizeof(uint64_t), stream);
     cudaMemsetAsync(w->hdr, 0, w->cap_tiles * sizeof(Rec), stream);
     w->epoch = 1;
   }
@@ -178,7 +178,7 @@ int64_t tensor_map(Workspace *w, const double *x, int64_t n_total) {
 
 void fill_ws(Params &p, Workspace *w) {
   p.status = w->status;
-  p.tagg = w->tagg;
+  p.cplan = w->cplan;
   p.hdr = w->hdr;
   p.items = w->items;
   p.ctr = w->ctr;
@@ -234,7 +234,7 @@ int batched_impl(const double *x, int64_t x_len, const int64_t *offsets, int32_t
   cudaError_t e = sq::launch_setup(p, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   int grid = g_num_sms[w->device] * g_blocks_per_sm;
-  if (grid < p.nwalkers + 2) grid = p.nwalkers + 2;     // walkers, the scanner, a streamer
+  if (grid < p.nwalkers + 2) grid = p.nwalkers + 2;     // walkers, the scanner, at least one streamer
   static CUtensorMap dummy;
   e = sq::launch_seqsum(p, p.tma_rows ? &w->tmap : &dummy, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -343,9 +343,11 @@ int seqsum_get_stats(seqsum_stats *st) {
   st->ns_walk_scan = (int64_t)s[sq::S_NS_WALK_SCAN];
   st->ns_walk_serial = (int64_t)s[sq::S_NS_WALK_SERIAL];
   st->ns_walk_adds = (int64_t)s[sq::S_NS_WALK_ADDS];
-  st->plan_local = (int64_t)s[sq::S_PLAN_LOCAL];
+  st->chunks_dirty = (int64_t)s[sq::S_CHUNK_DIRTY];
   st->ns_ctrl_wait = (int64_t)s[sq::S_NS_CTRL_WAIT];
   st->ns_scan_wait = (int64_t)s[sq::S_NS_SCAN_WAIT];
+  st->ns_verdict = (int64_t)s[sq::S_NS_VERDICT];
+  st->ns_verdict_wait = (int64_t)s[sq::S_NS_VERDICT_WAIT];
   st->t_stream_ns = (int64_t)(s[sq::S_T_STREAM_END] - s[sq::S_T_START]);
   st->t_walk_tail_ns = (int64_t)(s[sq::S_T_WALK1] - s[sq::S_T_STREAM_END]);
   st->t_total_ns = (int64_t)(s[sq::S_T_WALK1] - s[sq::S_T_START]);
@@ -398,10 +400,10 @@ void seqsum_release_workspace(void) {
 int seqsum_debug_read(unsigned long long *out, int n) {
   std::lock_guard<std::mutex> lk(g_mu);
   Workspace *w = g_last;
-  if (!w || !out || n < 0 || n > 16384) return SEQSUM_EINVAL;
+  if (!w || !out || n < 0 || n > sq::kDbgAlloc) return SEQSUM_EINVAL;
   cudaError_t e = cudaStreamSynchronize(w->stream);
   if (e == cudaSuccess) e = cudaMemcpy(out, w->dbg, n * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess) e = cudaMemset(w->dbg, 0, 16384 * sizeof(unsigned long long));
+  if (e == cudaSuccess) e = cudaMemset(w->dbg, 0, sq::kDbgAlloc * sizeof(unsigned long long));
   return e == cudaSuccess ? SEQSUM_OK : cuda_fail(e);
 }
 

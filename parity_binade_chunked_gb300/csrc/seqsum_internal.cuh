@@ -8,11 +8,13 @@ namespace sq {
 // ---- geometry (a lane owns one 128-byte row of 16 consecutive terms)
 constexpr int kLaneTerms = 16;
 constexpr int kWarps = 8;                       // warps per CTA = chunks per tile
-constexpr int kThreads = kWarps * 32;           // compute threads of a CTA (the walker's and scanner's width)
-constexpr int kBlockThreads = kThreads + 32;    // + the control warp of a streaming CTA
+constexpr int kThreads = kWarps * 32;           // compute threads of a CTA (the walker's width)
+constexpr int kCtrlWarp = kWarps;               // a streaming CTA's control warp (tickets, copies, tile headers)
+constexpr int kBlockThreads = kThreads + 32;
+constexpr int kBlockWarps = kBlockThreads / 32;
 constexpr int kChunkTerms = 32 * kLaneTerms;    // 512 terms: one warp's chunk
 constexpr int kTileTerms = kWarps * kChunkTerms;// 4096 terms = 32 KB: one TMA box
-constexpr int kStages = 3;                      // copy of tile i+2 | plan of i+1 | runs of i
+constexpr int kStages = 3;                      // units a streaming CTA holds: copied, worked on, epilogue
 constexpr int kStageBytes = kTileTerms * 8;
 constexpr int kDynSmem = kStages * kStageBytes + 1024;   // + alignment slack
 constexpr int kChunkSlots = 32;                 // item slots per chunk in a tile's item area
@@ -23,6 +25,7 @@ constexpr int kWalkTiles = 1024;                // tile headers per walk batch (
 constexpr int kWalkElems = 1024;                // flat elements per walk batch (32 KB)
 constexpr int kMaxWalkers = 8;
 constexpr int kHeartbeats = 4096;               // CTAs with a heartbeat word (diagnostics of a stuck call)
+constexpr int kDbgAlloc = 65536;                // diagnostic words: checks, walk trace, profiling timeline
 
 // ---- record kinds
 enum : uint32_t { K_RUN = 0, K_FALLBACK = 1, K_TERMS = 2, K_COMPLEX = 3 };
@@ -86,13 +89,15 @@ enum : int {
   S_TORN_HEADER,       // header reads that mixed words of two publications (retried)
   S_TORN_STATUS,       // prefix reads that mixed words of two publications (retried)
   S_NS_SCAN,           // the scanner's time from its first to its last window
-  S_PLAN_LOCAL,        // run units whose tile spans two binades (planned chunk by chunk)
+  S_CHUNK_DIRTY,       // chunks whose prefix range spans two binades (placed lane by lane)
   S_NS_CTRL_WAIT,      // control warps waiting for their compute warps
   S_NS_SCAN_WAIT,      // the scanner waiting for tiles' sums to be published
   // the walk's work by section (nanoseconds): counting a batch's elements,
   // gathering them, the segmented scan, the in-order pass, and within that
   // pass the term-by-term adds
   S_NS_WALK_COUNT, S_NS_WALK_GATHER, S_NS_WALK_SCAN, S_NS_WALK_SERIAL, S_NS_WALK_ADDS,
+  S_NS_VERDICT,        // run units: forming the chunks' verdicts from the plan words
+  S_NS_VERDICT_WAIT,   // run units: plan words read again from global memory (not copied in time)
   S_ACCUM_END,         // counters above are summed; below are timestamps of the latest call
   S_T_START = 40,      // block 0 started (timestamps follow the summed counters)
   S_T_WALK0 = 41,      // the walk's last batch of headers was ready
@@ -117,8 +122,8 @@ struct Params {
   int32_t plan_mode;           // 0 normal; >0 forced plans for tests
   int32_t pad;
   // workspace
-  uint64_t *status;            // 2 words per tile: tagged approximate prefix
-  uint64_t *tagg;              // 2 words per tile: its own approximate sum (tagged like status)
+  uint64_t *status;            // 2 words per tile: tagged approximate sum, then inclusive prefix
+  uint64_t *cplan;             // 4 tagged words per chunk: the plan's fixed-point sums of the chunk
   Rec *hdr;                    // one header per tile
   Rec *items;                  // kTileSlots items per tile
   uint32_t *ctr;               // C_COUNT counters

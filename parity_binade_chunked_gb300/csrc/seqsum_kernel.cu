@@ -1,28 +1,32 @@
 // The device path of the exact sequential fp64 sum (sm_103a).
 //
-// One persistent kernel.  CTAs 0 .. nwalkers-1 walk; every other CTA streams
-// tiles of 4096 terms (32 KB, one TMA box) taken in ticket order, in a
-// three-stage pipeline: the copy of tile i+2 is in flight while the plan of
-// tile i+1 and the runs of tile i are formed.
+// One persistent kernel.  CTAs 0 .. nwalkers-1 walk, the next one scans the
+// plan's tile sums; every other CTA streams
+// tiles of 4096 terms (32 KB, one TMA box) taken in ticket order, each read
+// from HBM once, in a three-stage pipeline: while one tile is copied, the
+// next is planned and the one before is formed into runs.
 //
-//  * Plan (Research-1424, section 3: "a first pass can add each row on its own
-//    and a prefix over the rows gives S at each row start ... which names the
-//    binade except next to a power of two"; Research-1433, finding 5 and the
-//    open question "compute the plan's prefix with a scan across the lanes"):
-//    every term's fp32 image is built from its bits with integer operations,
-//    a tile's approximate sum is published as soon as the tile has landed,
-//    and a decoupled look-back over the published sums, 256 tiles per read,
-//    gives each tile its approximate starting value in double-float.  No
-//    fp64 instruction is used for the plan.
+//  * Plan (Research-1424, section 3: a first pass that adds each row on its
+//    own and a prefix over the rows give the sum at every row start, which
+//    names the binade except next to a power of two; Research-1433, finding 5
+//    and the open question "compute the plan's prefix with a scan"): as soon
+//    as a tile lands, its terms are summed in fixed point (their 32 leading
+//    significant bits, by integer shifts) and the tile's approximate sum is
+//    published; a scanner CTA scans the published sums in order, in windows
+//    of up to 1024 tiles, and publishes every tile's inclusive prefix; each
+//    streaming CTA's prefix warp reads the prefix of the tile before its own
+//    and gives every chunk of the tile its approximate starting value in
+//    double-float and a verdict: inside one binade, all zeros, or spanning a
+//    power of two.
 //  * Runs (finding 2 "Inside a binade the loop is an integer sum", finding 3
 //    "Ties need the parity of the running integer"): a chunk of 512 terms
 //    whose whole range lies inside one binade is turned into its increment
 //    by integer shifts (binade_math.cuh) and composed: each lane's 16 terms
 //    in order, then the warp's 32 lanes in a fixed shuffle tree (finding 6).
-//  * A chunk the plan cannot place in one binade is split: lanes that fit a
-//    binade become runs, and inside the other lanes each term is placed on
-//    its own; only the terms whose approximate prefix lies next to a power of
-//    two are carried, as values, to be added one by one (finding 4).
+//  * A chunk spanning a power of two is split: lanes that fit a binade become
+//    runs, and inside the other lanes each term is placed on its own; only
+//    the terms whose prefix range touches a power of two are carried, as
+//    values, to be added one by one (finding 4).
 //  * The walk (finding 4; open question "compose runs of chunks that share a
 //    binade so that the walk steps over 64 or 1024 chunks at a time") runs
 //    at the same time as the stream: it reads tile headers as they appear,
@@ -44,17 +48,10 @@
 namespace sq {
 
 // ---------------------------------------------------------------- constants
-// Relative error allowance of the plan against the running sum of |x|: fp32
-// term images keep 20 fraction bits (truncated), fp32 sums of 16 and 32
-// values, double-float across chunks and tiles.  The plan only chooses where
-// to look; a wrong guess costs a fallback, never a wrong bit.
-constexpr float kEps = 0x1p-18f;
-constexpr float kRelF32 = 0x1p-21f;            // rounding of one fp32 prefix value
-constexpr float kTinyF = 0x1p-120f;
+constexpr float kTinyF = 0x1p-120f;            // floor of the plan's error allowance
 constexpr int kZeroE = -2000;                  // binade key of a run of zeros
 constexpr int kDirtyKey = -3000;               // merge key of a lane placed term by term
 constexpr uint64_t kWaitNs = 2000000000ull;    // bounded device waits: 2 s
-constexpr uint32_t kMagLo = 896u << 20;        // exponent 896 = 2^-127
 constexpr uint64_t kCountMask = (1u << kCountBits) - 1;
 static_assert(((uint64_t)kChunkSlots << (kCountBits * (kWarps - 1))) < (1ull << 55),
               "packed item counts must fit a tagged 56-bit word");
@@ -99,6 +96,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of an mbarrier phase (for polling several barriers).
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // 2-D tiled TMA load of one box (16 terms x 256 rows) into shared memory.
 __device__ __forceinline__ void tma_load_box(void *dst, const CUtensorMap *map, uint64_t *bar, int32_t c0,
                                              int32_t c1) {
@@ -135,14 +142,14 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 // Heartbeat of this CTA (one thread calls it): its role, what it waits for
 // or does (HB_*) and where (a unit, tile or position), read by the host
 // while a call runs.
-// One word per warp (index CTA * 9 + warp).
+// One word per warp (index CTA * kBlockWarps + warp).
 enum : uint32_t {
-  HB_START = 1, HB_WAIT_UNIT = 2, HB_UNIT = 3, HB_WAIT_DONE = 4, HB_EPILOGUE = 5, HB_WAIT_HEADERS = 6,
-  HB_BATCH = 7, HB_SERIAL = 8, HB_WAIT_SUMS = 9, HB_WINDOW = 10, HB_COUNT = 11, HB_GATHER = 12, HB_SCAN = 13,
-  HB_RESTART = 14, HB_END = 15, HB_BARRIER = 16
+  HB_START = 1, HB_WAIT_UNIT = 2, HB_UNIT = 3, HB_WAIT_DONE = 4, HB_WAIT_HEADERS = 6,
+  HB_BATCH = 7, HB_SERIAL = 8, HB_COUNT = 11, HB_GATHER = 12, HB_SCAN = 13,
+  HB_RESTART = 14, HB_END = 15, HB_BARRIER = 16, HB_WINDOW = 17
 };
 __device__ __forceinline__ void beat(const Params &p, uint32_t role, uint32_t what, uint64_t where) {
-  const unsigned i = blockIdx.x * 9u + (threadIdx.x >> 5);
+  const unsigned i = blockIdx.x * (unsigned)kBlockWarps + (threadIdx.x >> 5);
   if (i < (unsigned)kHeartbeats)
     p.hb[i] = ((uint64_t)(role & 0xFFu) << 56) | ((uint64_t)(what & 0xFFu) << 48) | (where & 0xFFFFFFFFFFFFull);
 }
@@ -150,7 +157,7 @@ __device__ __forceinline__ void beat(const Params &p, uint32_t role, uint32_t wh
 // A bounded wait gave up: set its error bit and keep the first such site
 // with two words of context for the host.
 enum : uint32_t {
-  TO_FULL = 1, TO_DONE = 2, TO_SUMS = 3, TO_PREFIX = 4, TO_TILESUM = 5, TO_SCAN = 6, TO_WALK = 7
+  TO_FULL = 1, TO_DONE = 2, TO_PLANNED = 3, TO_PREFIX = 4, TO_VERDICT = 5, TO_SCAN = 6, TO_WALK = 7
 };
 __device__ __noinline__ void note_timeout(const Params &p, uint32_t err, uint32_t site, uint32_t a, uint32_t b) {
   atomicOr(&p.ctr[C_ERR], err);
@@ -211,6 +218,24 @@ __device__ __forceinline__ bool item_ok(const Params &p, const Rec *q, uint32_t 
   return sq_ok(p, q >= p.items && q < p.items + p.cap_tiles * kTileSlots, site, (int64_t)(q - p.items));
 }
 
+// Timeline of a call (profiling builds): per tile and unit kind eight words
+// from kTraceUnits on (its copy issued, the compute warps' start and end, the
+// epilogue's end, the CTA and ticket), per walk batch four words.
+#ifdef SEQSUM_PROFILE
+constexpr int kTraceUnits = 16384;
+constexpr int kTraceBatches = 61440;
+__device__ __forceinline__ void trace_word(const Params &p, int base, int limit, int64_t idx, int stride, int field,
+                                           unsigned long long v) {
+  const int64_t i = base + idx * stride + field;
+  if (idx >= 0 && i < limit) p.dbg[i] = v;
+}
+#define TRACE_UNIT(t, kind, field, v) trace_word(p, kTraceUnits, kTraceBatches, 2 * (t) + (kind), 8, (field), (v))
+#define TRACE_BATCH(b, field, v) trace_word(p, kTraceBatches, kDbgAlloc, (b), 4, (field), (v))
+#else
+#define TRACE_UNIT(t, kind, field, v) do { } while (0)
+#define TRACE_BATCH(b, field, v) do { } while (0)
+#endif
+
 // ---------------------------------------------------------------- double-float
 // (hi + lo) pairs of fp32 for the plan's prefix; every op is one rounded fp32
 // add (no contraction in this translation unit).
@@ -236,31 +261,6 @@ __device__ __forceinline__ DF df_from_double(double v) {
 }
 __device__ __forceinline__ DF shfl_xor_df(DF v, int m) {
   return DF{__shfl_xor_sync(0xffffffffu, v.hi, m), __shfl_xor_sync(0xffffffffu, v.lo, m)};
-}
-
-// ---------------------------------------------------------------- the plan's term image
-// fp32 image of a term from its high word: 20 fraction bits (truncated), the
-// exponent moved to the fp32 bias; magnitudes below 2^-127 give 0.  Terms of
-// 2^128 and above need the clamped form.
-__device__ __forceinline__ float approx_term(uint32_t hi) {
-  const uint32_t v = max(hi & 0x7FFFFFFFu, kMagLo);
-  return __uint_as_float(((v - kMagLo) * 8u) | (hi & 0x80000000u));
-}
-__device__ __forceinline__ float approx_term_clamped(uint32_t hi) {
-  const uint32_t v = min(max(hi & 0x7FFFFFFFu, kMagLo), (1150u << 20) | 0xFFFFFu);
-  return __uint_as_float(((v - kMagLo) * 8u) | (hi & 0x80000000u));
-}
-
-// Binade (unbiased exponent) shared by all of [lo, hi] (fp32), or false.
-__device__ __forceinline__ bool one_binade_f(float lo, float hi, int &e) {
-  float a, b;
-  if (lo > 0.0f) { a = lo; b = hi; }
-  else if (hi < 0.0f) { a = -hi; b = -lo; }
-  else return false;
-  const int ea = (int)((__float_as_uint(a) >> 23) & 0xFF), eb = (int)((__float_as_uint(b) >> 23) & 0xFF);
-  if (ea != eb || ea == 0 || ea == 0xFF) return false;
-  e = ea - 127;
-  return true;
 }
 
 __device__ __forceinline__ uint32_t hash3(uint64_t a, uint32_t b, uint32_t c) {
@@ -411,32 +411,61 @@ __device__ __forceinline__ TileGeo tile_geo(const Params &p, int64_t t, int64_t 
 }
 
 // ---------------------------------------------------------------- shared memory
-// A chunk's aggregates: the sum and |x| sum of its terms' fp32 images (the
-// plan), the largest magnitude word and whether any term has its sign bit set
-// or any term is non-zero (the exact preconditions of the fast runs).
-enum : uint32_t { WA_NEG = 1u, WA_NZ = 2u };
-struct WarpAgg {
-  float sig, ab;
-  uint32_t mx, flags;
+// Flags of a chunk's terms: one with the sign bit set, one with it clear, one
+// that is not zero.
+enum : uint32_t { WA_NEG = 1u, WA_POS = 2u, WA_NZ = 4u };
+
+// The plan of one chunk, formed by its compute warp as soon as the tile has
+// landed: the magnitudes of its non-negative terms (P) and of its negative
+// terms (N), each summed in fixed point in units of 2^(L - 1054), where L is
+// the largest biased exponent among the chunk's terms.
+struct ChunkPlan {
+  uint64_t P, N;
+  int32_t L;
+  uint32_t mx;        // largest magnitude high word among the chunk's terms
+  uint32_t flags;     // WA_*
+  uint32_t pad;
+};
+
+// The look-back warp's verdict on one chunk.
+enum : int { CP_CLEAN = 0, CP_ZERO = 1, CP_DIRTY = 2 };
+struct ChunkPre {
+  DF c;               // approximate running sum before the chunk
+  float ab;           // approximate |s0| + sum of |x| before the chunk
+  float delta;        // the plan's error allowance inside the chunk
+  int32_t e;          // CP_CLEAN: the binade of every prefix inside the chunk
+  int32_t mode;       // CP_*
+};
+
+enum : int { U_PLAN = 0, U_RUN = 1, U_END = 2 };
+// The unit a stage holds, written by the control warp before its copy starts.
+struct StageGeo {
+  int64_t t;          // tile index
+  int64_t start, end; // its terms [start, end) in x
+  int64_t first_tile; // the first tile of its sum
+  int64_t sum_start;  // the first term of its sum
+  int32_t sum;        // which sum
+  int32_t kind;       // U_PLAN, U_RUN, or U_END: no more units
+  int32_t tma;        // its terms came by TMA (else they are read from global memory)
+  int32_t pad;
 };
 
 struct Smem {
-  uint64_t full[kStages];           // streaming: the unit's copy and plan words landed (3 arrivals)
-  uint64_t done[kStages];           // streaming: the compute warps finished the unit
-  uint64_t sums[kStages];           // streaming: the compute warps' chunk sums (a tile planned chunk by chunk)
-  int64_t tk[kStages];              // the stage's tile
-  int tma[kStages];                 // its terms came by TMA (else from global memory)
-  int kind[kStages];                // U_PLAN, U_RUN or U_END
-  int role;
-  uint32_t barcnt[kWarps];          // walker/scanner: wide barriers passed per warp (heartbeat)
-  // a run unit's plan words, copied in ahead of its runs: the tile's own
-  // approximate sum and the prefix of the tile before (cp.async
-  // destinations: 16-byte aligned)
-  alignas(16) uint64_t tagg_raw[kStages][2];
+  uint64_t full[kStages];           // the unit's copy and plan words landed, or the end marker (kFullArrivals)
+  uint64_t done[kStages];           // the compute warps finished the unit (kWarps arrivals)
+  StageGeo geo[kStages];            // the unit's tile and kind (U_PLAN, U_RUN, U_END)
+  // a run unit's plan words, copied in ahead of its runs: the prefix of the
+  // tile before and the tile's chunk plans (cp.async destinations: 16-byte
+  // aligned)
   alignas(16) uint64_t pre_raw[kStages][2];
-  WarpAgg wa[kStages][kWarps];
+  alignas(16) uint64_t cplan_raw[kStages][kWarps * 4];
+  ChunkPlan plan[kStages][kWarps];  // a plan unit's chunk plans
   Rec chunk[kStages][kWarps];       // a run unit's chunk records
   int nitems[kStages][kWarps];      // >0: a split chunk's items in the tile's item area
+  int plan_cnt[kStages];            // chunks of a plan unit's tile planned so far
+  Rec stg[kWarps][kChunkSlots];     // a split chunk's items, staged in order before they are written out
+  int role;
+  uint32_t barcnt[kWarps];          // walker and scanner: wide barriers passed per warp (heartbeat)
   unsigned int st[S_COUNT];         // per-CTA statistics of one call (32-bit: native shared atomics)
   // walker
   uint64_t S;
@@ -455,13 +484,17 @@ struct Smem {
   DF carry;
   float carry_abs;
 };
-static_assert(offsetof(Smem, tagg_raw) % 16 == 0 && offsetof(Smem, pre_raw) % 16 == 0,
+static_assert(offsetof(Smem, pre_raw) % 16 == 0 && offsetof(Smem, cplan_raw) % 16 == 0,
               "cp.async destinations must be 16-byte aligned");
-static_assert(offsetof(Smem, full) % 8 == 0 && offsetof(Smem, done) % 8 == 0 && offsetof(Smem, sums) % 8 == 0,
-              "mbarriers are 8-byte aligned");
+// a run unit's copies: lane 0 the prefix word pair, lanes 1..16 the chunk
+// plans (16 bytes each); every one of those lanes makes one arrival when its
+// copy has landed, and lane 0 one more for the tile's own copy
+constexpr int kCopyLanes = 1 + kWarps * 2;
+constexpr uint32_t kFullArrivals = kCopyLanes + 1;
+static_assert(offsetof(Smem, full) % 8 == 0 && offsetof(Smem, done) % 8 == 0, "mbarriers are 8-byte aligned");
 
-// The 256-thread barrier of a walking or scanning CTA; each warp first
-// records the barrier's site and how many it has passed (its heartbeat).
+// The 256-thread barrier of a walking or scanning CTA; each warp first records the
+// barrier's site and how many it has passed (its heartbeat).
 __device__ __noinline__ void wide_sync_at(const Params &p, Smem &sm, int site) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) {
@@ -471,8 +504,106 @@ __device__ __noinline__ void wide_sync_at(const Params &p, Smem &sm, int site) {
   named_sync(kBarWide, kThreads);
 }
 
+// ---------------------------------------------------------------- the plan
+// The plan (Research-1424, section 3: a first pass that adds each row on its
+// own and a prefix over the rows give the sum at every row start, and so its
+// binade except next to a power of two; Research-1433, finding 5: the plan
+// only chooses where the walk looks, so an error in it costs time, never a
+// bit).  Every term enters it as its 32 leading significant bits in fixed
+// point, by integer shifts; chunk sums become double-float values; a scanner
+// CTA turns the tiles' published sums into inclusive prefixes.
+//
+// Error of the plan, relative to the running sum of |x|: a term loses less
+// than one unit of its lane's scale (2^-31 of the lane's largest term), a lane
+// less than one unit of its chunk's scale; with the double-float sums that is
+// below 2^-25.  The sequential fp64 sum itself drifts from the exact sum by
+// at most 2^-53 of |s0| + sum |x| per add.  The allowance kPlanEps covers the
+// first with a margin, and the walk's drift term is added per chunk.
+constexpr float kPlanEps = 0x1p-24f;
 
-// ---------------------------------------------------------------- the plan's prefix
+// The 32 leading significant bits of a normal term (0 for zeros and
+// subnormals, too small to matter to the plan): the term is about
+// m * 2^(E - 1054).
+__device__ __forceinline__ uint32_t lead32(uint32_t hi, uint32_t lo, uint32_t E) {
+  const uint32_t m = __funnelshift_l(lo, hi, 11) | 0x80000000u;
+  return E ? m : 0u;
+}
+// The lane's terms in fixed point at scale 2^(Lm - 1054), Lm the largest
+// biased exponent among them: `all` sums every magnitude, `neg` those of the
+// terms with the sign bit set.  Each term loses less than one unit.
+__device__ __forceinline__ void lane_fixed(const uint64_t *xs, uint32_t Lm, uint64_t &all, uint64_t &neg) {
+  all = 0;
+  neg = 0;
+#pragma unroll
+  for (int i = 0; i < kLaneTerms; i++) {
+    const uint32_t hi = (uint32_t)(xs[i] >> 32), lo = (uint32_t)xs[i];
+    const uint32_t E = (hi >> 20) & 0x7FFu;
+    const uint32_t v = __funnelshift_rc(lead32(hi, lo, E), 0u, Lm - E);   // shifts of 32 or more give 0
+    all += v;
+    neg += (hi >> 31) ? v : 0u;
+  }
+}
+// Sum over the warp of values below 2^36 (16-bit low parts and the rest
+// summed apart, so that each 32-bit reduction stays exact).
+__device__ __forceinline__ uint64_t warp_sum36(uint64_t v) {
+  const uint32_t lo = __reduce_add_sync(0xffffffffu, (uint32_t)v & 0xFFFFu);
+  const uint32_t hi = __reduce_add_sync(0xffffffffu, (uint32_t)(v >> 16));
+  return ((uint64_t)hi << 16) + lo;
+}
+// 2^q as a float: 0 below 2^-126, infinity above 2^127 (the plan then only
+// gets worse).
+__device__ __forceinline__ float pow2f(int q) {
+  if (q < -126) return 0.0f;
+  if (q > 127) return __uint_as_float(0x7F800000u);
+  return __uint_as_float((uint32_t)(q + 127) << 23);
+}
+// Integers as double-float or float values, from exact 16-bit pieces (32-bit
+// conversions and fp32 adds only): |v| < 2^48.
+__device__ __forceinline__ DF df_from_u48(uint64_t v) {
+  const float a = __fmul_rn(__uint2float_rn((uint32_t)(v >> 32) & 0xFFFFu), 0x1p32f);
+  const float b = __fmul_rn(__uint2float_rn((uint32_t)v >> 16), 0x1p16f);
+  const float c = __uint2float_rn((uint32_t)v & 0xFFFFu);
+  return df_addf(two_sum(a, b), c);
+}
+__device__ __forceinline__ DF df_from_i48(int64_t v) {
+  const DF m = df_from_u48((uint64_t)(v < 0 ? -v : v));
+  return v < 0 ? DF{-m.hi, -m.lo} : m;
+}
+__device__ __forceinline__ float f_from_u48(uint64_t v) {
+  return __fadd_rn(__fmul_rn(__uint2float_rn((uint32_t)(v >> 32) & 0xFFFFu), 0x1p32f), __uint2float_rn((uint32_t)v));
+}
+__device__ __forceinline__ float f_from_i48(int64_t v) {
+  const float m = f_from_u48((uint64_t)(v < 0 ? -v : v));
+  return v < 0 ? -m : m;
+}
+// v * 2^(L - 1054) as a double-float or a float (|v| < 2^48).
+__device__ __forceinline__ DF df_fixed(int64_t v, int L) {
+  const DF m = df_from_i48(v);
+  const float s = pow2f(L - 1054);
+  return DF{__fmul_rn(m.hi, s), __fmul_rn(m.lo, s)};
+}
+__device__ __forceinline__ float f_fixed(uint64_t v, int L) { return __fmul_rn(f_from_u48(v), pow2f(L - 1054)); }
+
+// Binade of a positive double-float value: its high part's, one less when
+// the high part is a power of two and the low part pulls the value below it.
+// (The fp32 biased exponent; 0 for subnormal, 255 for inf and NaN.)
+__device__ __forceinline__ int df_exp_pos(DF v) {
+  const uint32_t b = __float_as_uint(v.hi);
+  const int e = (int)((b >> 23) & 0xFFu);
+  return e - (((b & 0x7FFFFFu) == 0u && v.lo < 0.0f) ? 1 : 0);
+}
+// The binade (unbiased exponent) shared by every value in [lo, hi], or false.
+__device__ __forceinline__ bool one_binade_df(DF lo, DF hi, int &e) {
+  DF a, b;
+  if (lo.hi > 0.0f) { a = lo; b = hi; }
+  else if (hi.hi < 0.0f) { a = DF{-hi.hi, -hi.lo}; b = DF{-lo.hi, -lo.lo}; }
+  else return false;                                   // zero inside, or NaN
+  const int ea = df_exp_pos(a), eb = df_exp_pos(b);
+  if (ea != eb || ea <= 0 || ea >= 0xFF) return false;
+  e = ea - 127;
+  return true;
+}
+
 // Per tile two tagged 64-bit words, written and read as one 16-byte access:
 //   A = sum.hi (fp32) << 32 | sum.lo (fp32) with its low 8 bits replaced by the tag
 //   B = |x| sum (fp32) << 32 | tag;   tag = epoch << 1 | kind,
@@ -490,64 +621,163 @@ __device__ __forceinline__ DF status_sum(uint64_t A) {
 }
 __device__ __forceinline__ float status_abs(uint64_t B) { return __uint_as_float((uint32_t)(B >> 32)); }
 
-struct Prefix {
-  DF ex;
-  float ex_abs;
-};
-
-// Units of work.  Every tile has a plan unit (copy it, publish its approximate
-// sum) and a run unit (copy it again, form its runs from the prefix the
-// scanner published for the tile before it).  Tickets hand out the plan units
-// of the first `wave` tiles, then a run unit and a plan unit in turn, then the
-// remaining run units: the plan of tile t always precedes the run of tile
-// t + 1 by about `wave` tiles, so a run unit's prefix is normally published
-// long before it is read, and its tile is still in L2.  Returns true for a
-// plan unit.
-__device__ __forceinline__ bool unit_of(int64_t u, int64_t ntiles, int64_t wave, int64_t &tile) {
-  const int64_t w = min(wave, ntiles);
-  if (u < w) { tile = u; return true; }
-  const int64_t v = u - w, rest = ntiles - w;
-  if (v < 2 * rest) {
-    tile = (v & 1) ? w + (v >> 1) : (v >> 1);
-    return (v & 1) != 0;
+// Warp-uniform test of an mbarrier phase.  When it reports the phase
+// complete, every lane has itself observed the completion (and so sees what
+// was written before it).
+__device__ __forceinline__ bool mbar_test_warp(uint64_t *bar, uint32_t parity) {
+  if (!__any_sync(0xffffffffu, mbar_test(bar, parity))) return false;
+  for (int i = 0; i < (1 << 20) && !mbar_test(bar, parity); i++) {
   }
-  tile = rest + (v - 2 * rest);
-  return false;
+  return true;
 }
-
-// The approximate exclusive prefix of tile t: s0 for the first tile of a sum,
-// else the inclusive prefix the scanner published for tile t - 1 (a bounded
-// wait; on a timeout the plan is only worse, the result stays exact).  One
-// thread.
-__device__ __forceinline__ Prefix read_prefix(const Params &p, int sum, int64_t first_tile, int64_t t,
-                                              unsigned int *st) {
-  if (t == first_tile) {
-    const DF ex = df_from_double(p.s0s ? p.s0s[sum] : p.s0);
-    return Prefix{ex, fabsf(ex.hi)};
-  }
-  const uint32_t tag = (p.epoch << 1) | 1u;
+// A bounded, warp-uniform wait on an mbarrier phase; false (for every lane)
+// on timeout.
+__device__ __forceinline__ bool mbar_wait_warp(const Params &p, uint64_t *bar, uint32_t parity, uint32_t err,
+                                               uint32_t site, uint32_t a, uint32_t b) {
+  if (mbar_test_warp(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  if (!sq_ok(p, t >= 1 && t - 1 < p.cap_tiles, 1, t)) return Prefix{DF{0.0f, 0.0f}, 0.0f};
+  uint32_t nap = 32;
   while (true) {
-    uint64_t A, B;
-    ld_vol_v2(p.status + 2 * (t - 1), A, B);
-    const uint32_t ta = (uint32_t)(A & 0xFF), tb = (uint32_t)B;
-    if (ta == tag && tb == tag) return Prefix{status_sum(A), status_abs(B)};
-    if (ta != tb && ((ta >> 1) == p.epoch || (tb >> 1) == p.epoch)) atomicAdd(&st[S_TORN_STATUS], 1u);
-    if (globaltimer() - t0 > kWaitNs) {
-      note_timeout(p, ERR_PLAN_TIMEOUT, TO_PREFIX, (uint32_t)t, (uint32_t)(ta | (tb << 8) | (p.epoch << 16)));
-      return Prefix{DF{0.0f, 0.0f}, 0.0f};
+    // one potentially blocking wait, then the warp-uniform test; between
+    // tests the warp sleeps (backoff), so that it takes no issue slots
+    (void)mbar_try_wait(bar, parity);
+    if (mbar_test_warp(bar, parity)) break;
+    __nanosleep(nap);
+    nap = min(nap * 2u, 256u);
+    if (__any_sync(0xffffffffu, globaltimer() - t0 > kWaitNs)) {
+      if ((threadIdx.x & 31) == 0) note_timeout(p, err, site, a, b);
+      return false;
     }
-    __nanosleep(32);
+  }
+  return true;
+}
+
+#ifdef SEQSUM_PROFILE
+// Cycle profiles (profiling builds): cycles since the previous point, summed
+// per point, and the number of times each point is passed (split chunks from
+// word 15200 on, plans from 15300).
+#define PROF_START long long prof_t = clock64()
+#define PROF_PT(base, id)                                                                  \
+  do {                                                                                     \
+    if ((threadIdx.x & 31) == 0) {                                                         \
+      const long long now_ = clock64();                                                    \
+      atomicAdd(&p.dbg[(base) + 2 * (id)], (unsigned long long)(now_ - prof_t));           \
+      atomicAdd(&p.dbg[(base) + 1 + 2 * (id)], 1ull);                                      \
+      prof_t = now_;                                                                       \
+    }                                                                                      \
+  } while (0)
+#else
+#define PROF_START do { } while (0)
+#define PROF_PT(base, id) do { } while (0)
+#endif
+#define SPLIT_PT(id) PROF_PT(15200, id)
+#define PLAN_PT(id) PROF_PT(15300, id)
+
+// The plan of chunk w of the stage's tile (by whichever compute warp claimed
+// it).  The warp that completes the tile's plan publishes the tile's
+// approximate sum (for a sum's first tile: s0 plus it, as an inclusive
+// prefix) and signals the look-back.
+__device__ __noinline__ void publish_tile_plan(const Params &p, Smem &sm, int k);
+__device__ __forceinline__ void load_lane(const Params &p, const unsigned char *stage, bool use_tma, int64_t row,
+                                          int64_t lstart, int nv, int w, int lane, uint64_t *xs);
+__device__ __noinline__ void plan_chunk(const Params &p, Smem &sm, const unsigned char *stage, int k, int w) {
+  const int lane = threadIdx.x & 31;
+  const unsigned full = 0xffffffffu;
+  PROF_START;
+  const StageGeo &g = sm.geo[k];
+  const int64_t lstart = g.start + (int64_t)w * kChunkTerms + (int64_t)lane * kLaneTerms;
+  const int nv = (int)max((int64_t)0, min((int64_t)kLaneTerms, g.end - lstart));
+  uint64_t xs[kLaneTerms];
+  load_lane(p, stage, g.tma != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, xs);
+  PLAN_PT(0);                                                 // loads
+  uint32_t mx = 0, orz = 0, orh = 0, andh = 0xFFFFFFFFu;
+#pragma unroll
+  for (int i = 0; i < kLaneTerms; i++) {
+    const uint32_t hi = (uint32_t)(xs[i] >> 32), lo = (uint32_t)xs[i];
+    const uint32_t mag = hi & 0x7FFFFFFFu;
+    mx = max(mx, mag);
+    orz |= mag | lo;
+    if (i < nv) { orh |= hi; andh &= hi; }
+  }
+  const uint32_t Lm = mx >> 20;
+  PLAN_PT(1);                                                 // lane stats
+  uint64_t all, neg;
+  lane_fixed(xs, Lm, all, neg);
+  PLAN_PT(2);                                                 // fixed point
+  const uint32_t Lc = __reduce_max_sync(full, Lm);
+  const uint32_t sh = min(Lc - Lm, 63u);
+  const uint64_t Pc = warp_sum36((all - neg) >> sh), Nc = warp_sum36(neg >> sh);
+  const uint32_t fl = __reduce_or_sync(full, ((orh >> 31) ? WA_NEG : 0u) | ((andh >> 31) ? 0u : WA_POS) |
+                                                 (orz ? WA_NZ : 0u));
+  const uint32_t mxc = __reduce_max_sync(full, mx);
+  PLAN_PT(3);                                                 // warp reductions
+  int last = 0;
+  if (lane == 0) {
+    sm.plan[k][w] = ChunkPlan{Pc, Nc, (int32_t)Lc, mxc, fl, 0u};
+    __threadfence_block();
+    last = atomicAdd(&sm.plan_cnt[k], 1) == kWarps - 1;
+  }
+  PLAN_PT(4);                                                 // count
+  if (__shfl_sync(full, last, 0)) {
+    __threadfence_block();
+    publish_tile_plan(p, sm, k);
+    PLAN_PT(5);                                               // publish (last warp)
   }
 }
 
-// The scanner (a whole CTA): takes, from where it stands, the longest run of
+// The chunk plans in global memory, four words per chunk, the tag in the top
+// byte of every word (an 8-byte access is single-copy atomic, a 16-byte one
+// need not be): P, N, L | flags << 16, mx.
+__device__ __forceinline__ void publish_cplan(uint64_t *dst, const ChunkPlan &c, uint32_t tag) {
+  const uint64_t tg = (uint64_t)tag << 56;
+  st_vol_v2(dst, c.P | tg, c.N | tg);
+  st_vol_v2(dst + 2, (uint64_t)(uint32_t)c.L | ((uint64_t)c.flags << 16) | tg, (uint64_t)c.mx | tg);
+}
+// The chunk plan in four words, when all of them carry `tag`.
+__device__ __forceinline__ bool cplan_of(uint64_t w0, uint64_t w1, uint64_t w2, uint64_t w3, uint32_t tag,
+                                        ChunkPlan &c) {
+  if ((uint32_t)(w0 >> 56) != tag || (uint32_t)(w1 >> 56) != tag || (uint32_t)(w2 >> 56) != tag ||
+      (uint32_t)(w3 >> 56) != tag)
+    return false;
+  c.P = w0 & kLow56;
+  c.N = w1 & kLow56;
+  c.L = (int32_t)(w2 & 0xFFFFu);
+  c.flags = (uint32_t)(w2 >> 16) & 0xFFu;
+  c.mx = (uint32_t)w3;
+  c.pad = 0u;
+  return true;
+}
+
+__device__ __noinline__ void publish_tile_plan(const Params &p, Smem &sm, int k) {
+  const int lane = threadIdx.x & 31;
+  const StageGeo &g = sm.geo[k];
+  ChunkPlan cp{0ull, 0ull, 0, 0u, 0u, 0u};
+  if (lane < kWarps) cp = sm.plan[k][lane];
+  const bool in = sq_ok(p, g.t >= 0 && g.t < p.cap_tiles, 6, g.t);
+  if (lane < kWarps && in) publish_cplan(p.cplan + (g.t * kWarps + lane) * 4, cp, (p.epoch << 1) | 1u);
+  DF s = df_fixed((int64_t)cp.P - (int64_t)cp.N, cp.L);
+  float a = f_fixed(cp.P + cp.N, cp.L);
+#pragma unroll
+  for (int o = kWarps / 2; o > 0; o >>= 1) {
+    s = df_add(s, shfl_xor_df(s, o));
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+  }
+  if (lane == 0 && in) {
+    if (g.t == g.first_tile) {
+      const DF s0 = df_from_double(p.s0s ? p.s0s[g.sum] : p.s0);
+      publish_status(p.status + 2 * g.t, df_add(s0, s), fabsf(s0.hi) + a, p.epoch, 1);
+    } else {
+      publish_status(p.status + 2 * g.t, s, a, p.epoch, 0);
+    }
+  }
+}
+
+// The scanner (a whole CTA, Research-1424 section 3: a prefix over the row
+// sums gives the sum at every row start; Research-1433, open question "the
+// plan's prefix as a scan"): from where it stands it takes the longest run of
 // tiles whose approximate sums are published (up to 1024 tiles), scans it --
-// a tile published as kind 1 starts a sum and already holds s0 plus its own
-// sum -- and publishes every other tile's inclusive prefix as kind 1
-// (Research-1424, section 3: a prefix over the row sums gives S at each row
-// start; Research-1433, open question: the plan's prefix as a scan).
+// a tile published as an inclusive prefix starts a sum and already holds s0
+// plus its own sum -- and publishes every other tile's inclusive prefix.
 __device__ __noinline__ void scan_prefix(const Params &p, Smem &sm, int64_t ntiles) {
   constexpr int PER = 4;
   constexpr int WIN = kThreads * PER;
@@ -561,6 +791,7 @@ __device__ __noinline__ void scan_prefix(const Params &p, Smem &sm, int64_t ntil
   uint64_t tprog = globaltimer();
   const uint64_t tbegin = tprog;
   uint64_t twait = 0;
+  uint32_t nap = 32;
   while (pos < ntiles) {
     if (tid == 0) beat(p, sm.role, HB_WINDOW, (uint64_t)pos);
     uint64_t A[PER], B[PER];
@@ -592,14 +823,16 @@ __device__ __noinline__ void scan_prefix(const Params &p, Smem &sm, int64_t ntil
         sm.scan_stop = (now - tprog > kWaitNs) ? 1 : 0;
         if (sm.scan_stop) note_timeout(p, ERR_PLAN_TIMEOUT, TO_SCAN, (uint32_t)pos, (uint32_t)ntiles);
       }
-      __nanosleep(64);
+      __nanosleep(nap);
+      nap = min(nap * 2u, 256u);
       twait += globaltimer() - now;
       wide_sync(p, sm, 2);                       // sm.scan_stop is set; sm.scan_m may be written again
       if (sm.scan_stop) break;
       continue;
     }
+    nap = 32;
     tprog = globaltimer();
-    // this thread's elements, scanned in order; a kind-1 tile restarts the sum
+    // this thread's elements, scanned in order; an inclusive prefix restarts the sum
     DF v[PER];
     float a[PER];
     bool f[PER];
@@ -672,6 +905,76 @@ __device__ __noinline__ void scan_prefix(const Params &p, Smem &sm, int64_t ntil
   }
 }
 
+// The inclusive prefix the scanner published for tile t - 1 (a bounded wait
+// with backoff; on a timeout the plan is only worse).  Whole warp.
+__device__ __noinline__ void read_prefix(const Params &p, Smem &sm, int64_t t, DF &ex, float &exab) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t tag1 = (p.epoch << 1) | 1u;
+  const uint64_t t0 = globaltimer();
+  uint32_t nap = 32;
+  uint64_t A = 0, B = 0;
+  while (true) {
+    if (lane == 0 && sq_ok(p, t >= 1 && t - 1 < p.cap_tiles, 1, t)) ld_vol_v2(p.status + 2 * (t - 1), A, B);
+    A = __shfl_sync(0xffffffffu, A, 0);
+    B = __shfl_sync(0xffffffffu, B, 0);
+    const uint32_t ta = (uint32_t)(A & 0xFF), tb = (uint32_t)B;
+    if (ta == tag1 && tb == tag1) break;
+    if (lane == 0 && ta != tb && ((ta >> 1) == p.epoch || (tb >> 1) == p.epoch)) atomicAdd(&sm.st[S_TORN_STATUS], 1u);
+    if (__any_sync(0xffffffffu, globaltimer() - t0 > kWaitNs)) {
+      if (lane == 0) note_timeout(p, ERR_PLAN_TIMEOUT, TO_PREFIX, (uint32_t)t, (uint32_t)(ta | tb << 8));
+      A = 0;
+      B = 0;
+      break;
+    }
+    __nanosleep(nap);
+    nap = min(nap * 2u, 256u);
+  }
+  ex = status_sum(A);
+  exab = status_abs(B);
+}
+
+// A run unit's verdict on chunk w of its tile (every compute warp forms its
+// own): the chunk's approximate starting value -- the prefix before the tile
+// plus the plans of the tile's earlier chunks, lane j holding chunk j's --,
+// its error allowance, and whether every prefix inside it stays in one
+// binade.  Whole warp; returns the verdict and the chunk's largest magnitude
+// word and flags.
+__device__ __forceinline__ ChunkPre chunk_verdict(const StageGeo &g, int w, DF ex, float exab, const ChunkPlan &cp,
+                                                  uint32_t &cmx, uint32_t &cflags) {
+  const int lane = threadIdx.x & 31;
+  const unsigned full = 0xffffffffu;
+  const DF sig = df_fixed((int64_t)cp.P - (int64_t)cp.N, cp.L);
+  const float ab = f_fixed(cp.P + cp.N, cp.L);
+  DF s = sig;
+  float sa = ab;
+#pragma unroll
+  for (int o = 1; o < kWarps; o <<= 1) {
+    const DF os = DF{__shfl_up_sync(full, s.hi, o), __shfl_up_sync(full, s.lo, o)};
+    const float oa = __shfl_up_sync(full, sa, o);
+    if (lane >= o) { s = df_add(os, s); sa += oa; }
+  }
+  // the sums of chunks 0 .. w-1 (lane w - 1's inclusive value)
+  const int src = w > 0 ? w - 1 : 0;
+  DF es = DF{__shfl_sync(full, s.hi, src), __shfl_sync(full, s.lo, src)};
+  float ea = __shfl_sync(full, sa, src);
+  if (w == 0) { es = DF{0.0f, 0.0f}; ea = 0.0f; }
+  const uint64_t P = __shfl_sync(full, cp.P, w), N = __shfl_sync(full, cp.N, w);
+  const int L = __shfl_sync(full, cp.L, w);
+  cmx = __shfl_sync(full, cp.mx, w);
+  cflags = __shfl_sync(full, cp.flags, w);
+  const DF c = df_add(ex, es);
+  const float cab = exab + ea;
+  const float abw = f_fixed(P + N, L);
+  const float nb = (float)(g.start - g.sum_start + (int64_t)(w + 1) * kChunkTerms);
+  const float delta = __fmaf_rn(nb, 0x1p-53f, kPlanEps) * (cab + abw) + kTinyF;
+  const float Pf = f_fixed(P, L), Nf = f_fixed(N, L);
+  int e = 0, mode;
+  if (!(cflags & WA_NZ)) mode = CP_ZERO;
+  else if (one_binade_df(df_addf(c, -(Nf + delta)), df_addf(c, Pf + delta), e)) mode = CP_CLEAN;
+  else mode = CP_DIRTY;
+  return ChunkPre{c, cab, delta, e, mode};
+}
+
 // ---------------------------------------------------------------- lanes
 __device__ __forceinline__ void load_lane(const Params &p, const unsigned char *stage, bool use_tma,
                                           int64_t row, int64_t lstart, int nv, int w, int lane, uint64_t *xs) {
@@ -695,6 +998,17 @@ __device__ __forceinline__ void load_lane(const Params &p, const unsigned char *
   }
 }
 
+// Term i of a lane: from its 128-byte row of the stage (16-byte chunk i/2,
+// swizzled by the row), or from global memory.
+__device__ __forceinline__ uint64_t lane_term(bool from_stage, const unsigned char *rp,
+                                              const unsigned long long *gp, int lane, int i) {
+  if (from_stage) {
+    const uint2 v = *reinterpret_cast<const uint2 *>(rp + ((((i >> 1) ^ (lane & 7)) << 4) | ((i & 1) << 3)));
+    return ((uint64_t)v.y << 32) | v.x;
+  }
+  return __ldg(gp + i);
+}
+
 // Exact run of a lane's terms under binade e (the general path: ties,
 // signed terms whose bounds need every prefix, binades outside the fast
 // path's range).  Kept out of line, with the lane's terms loaded again, so
@@ -708,14 +1022,7 @@ __device__ __noinline__ Run lane_run_general(const Params &p, const unsigned cha
   Run r = run_empty();
 #pragma unroll 1
   for (int i = 0; i < nv; i++) {
-    uint64_t x;
-    if (from_stage) {
-      // term i of the lane's 128-byte row: 16-byte chunk i/2, swizzled by the row
-      const uint2 v = *reinterpret_cast<const uint2 *>(rp + ((((i >> 1) ^ (lane & 7)) << 4) | ((i & 1) << 3)));
-      x = ((uint64_t)v.y << 32) | v.x;
-    } else {
-      x = __ldg(gp + i);
-    }
+    const uint64_t x = lane_term(from_stage, rp, gp, lane, i);
     int64_t re;
     int32_t d;
     const bool poison = term_inc(x, e, re, d);
@@ -724,417 +1031,403 @@ __device__ __noinline__ Run lane_run_general(const Params &p, const unsigned cha
   return r;
 }
 
-// Items of one lane the plan could not place in a binade, term by term: runs
-// of terms whose approximate prefix stays inside one binade, and up to three
-// carried terms per item where it does not.  With out == nullptr only counts.
-__device__ __noinline__ int lane_items(const Params &p, const uint64_t *xs, int nv, float A, float dbase, uint64_t t, int w,
-                          int lane, Rec *out) {
-  float a = A;
-  int cur = 0, cur_e = 0, nterms = 0, cstart = 0, n = 0;
-  Run rr = run_empty();
-  int64_t vals[3] = {0, 0, 0};
-  uint32_t tf_or = 0;
-  const uint32_t tbase = (uint32_t)(w * kChunkTerms + lane * kLaneTerms);
-  for (int i = 0; i <= nv; i++) {
-    int kind = 0, ei = 0;
-    int64_t re = 0;
-    int32_t dd = 0;
-    if (i < nv) {
-      const float a1 = a + approx_term_clamped((uint32_t)(xs[i] >> 32));
-      const float d = dbase + kRelF32 * fmaxf(fabsf(a), fabsf(a1));
-      bool ok = one_binade_f(fminf(a, a1) - d, fmaxf(a, a1) + d, ei);
-      ok = plan_override(p.plan_mode, ok, ei, t, w, 100 + lane * 16 + i);
-      if (ok && term_inc(xs[i], ei, re, dd)) ok = false;
-      kind = ok ? 1 : 2;
-      a = a1;
-    }
-    // close the open item when this term does not extend it
-    const bool extend = (i < nv) && ((kind == 1 && cur == 1 && cur_e == ei) || (kind == 2 && cur == 2 && nterms < 3));
-    if (!extend && cur != 0) {
-      if (out && item_ok(p, out + n, 4)) {
-        if (cur == 1) {
-          stcg_rec(out + n, make_rec(rr, cur_e, K_RUN, (uint32_t)(i - cstart), tbase + (uint32_t)cstart));
-        } else {
-          Run tr = run_empty();
-          tr.inc = vals[0]; tr.lo = vals[1]; tr.hi = vals[2]; tr.d = 0;
-          tr.flags = tf_or & (F_HASINF_P | F_HASINF_N | F_HASNAN);
-          stcg_rec(out + n, make_rec(tr, 0, K_TERMS, (uint32_t)nterms, tbase + (uint32_t)cstart));
-        }
-      }
-      n++;
-      cur = 0;
-    }
-    if (i == nv) break;
-    if (cur == 0) {
-      cur = kind;
-      cstart = i;
-      rr = run_empty();
-      nterms = 0;
-      tf_or = 0;
-      cur_e = ei;
-    }
-    if (kind == 1) {
-      run_push(rr, re, dd, term_flags(xs[i]));
-    } else {
-      vals[nterms++] = (int64_t)xs[i];
-      tf_or |= term_flags(xs[i]);
-    }
-  }
-  return n;
+// The run of a lane's terms from their increments summed apart by sign (no
+// tie among them): P for the terms with the sign bit clear, N for the others;
+// or and and of the valid terms' high words give the sign flags.
+__device__ __forceinline__ Run lane_pn_run(uint64_t P, uint64_t N, uint32_t orl, uint32_t andl, int nv) {
+  if (nv == 0) return run_empty();
+  Run r;
+  r.inc = (int64_t)(P - N);
+  r.lo = -(int64_t)N;
+  r.hi = (int64_t)P;
+  r.d = 0;
+  r.flags = ((orl >> 31) ? 0u : F_NONNEG) | ((andl >> 31) ? F_NONPOS : 0u);
+  return r;
 }
-
-// A chunk the plan could not place in one binade.  Lanes that fit one become
-// runs (neighbouring runs of one binade merge); the other lanes are placed
-// term by term.  Writes the items for chunk w into the tile's item area and
-// returns their number, or 0 when they do not fit (the caller then records
-// the chunk as one fallback).
-__device__ __noinline__ int split_chunk(const Params &p, const unsigned char *stage, bool use_tma, int64_t row,
-                                       int64_t lstart, int nv, int w, int lane, DF sc, float ac, uint64_t t,
-                                       Rec *area, unsigned int *st) {
-  uint64_t xs[kLaneTerms];
-  load_lane(p, stage, use_tma, row, lstart, nv, w, lane, xs);
-  float sig = 0.0f, ab = 0.0f;
-  uint32_t orz = 0;
+// Increments of a lane's terms under the fast rule (binade_math.cuh,
+// term_inc_fast; c = 64 - (e + 1023)) summed apart by sign, whether any of
+// them ties, and the sign flags of the valid terms.
+__device__ __forceinline__ void lane_fast(const uint64_t *xs, int nv, int c, uint64_t &P, uint64_t &N, bool &anytie,
+                                          uint32_t &orl, uint32_t &andl) {
+  P = 0; N = 0; anytie = false; orl = 0; andl = 0xFFFFFFFFu;
 #pragma unroll
   for (int i = 0; i < kLaneTerms; i++) {
     const uint32_t hi = (uint32_t)(xs[i] >> 32);
-    const float f = approx_term_clamped(hi);
-    sig += f;
-    ab += fabsf(f);
-    orz |= (hi & 0x7FFFFFFFu) | (uint32_t)xs[i];
+    uint64_t ri;
+    bool tie;
+    term_inc_fast(hi, (uint32_t)xs[i], c, ri, tie);
+    if (hi >> 31) N += ri; else P += ri;
+    anytie |= tie;
+    if (i < nv) { orl |= hi; andl &= hi; }
   }
-  float isig = sig, iab = ab;
+}
+// The fast rule applies to binade e for terms whose largest magnitude word
+// is mx: e in range and every term below 2^e.
+__device__ __forceinline__ bool fast_ok(int e, uint32_t mx) {
+  return e >= -969 && e <= 1023 && (int)(mx >> 20) < e + 1023;
+}
+
+// A lane's run under binade e (a cold path: rolled loops over the terms read
+// from the stage or global memory, kept small): the fast rule when no term
+// ties, else the general path.
+__device__ __noinline__ Run lane_run_any(const Params &p, bool from_stage, const unsigned char *rp,
+                                         const unsigned long long *gp, int nv, int lane, int e) {
+  uint32_t mx = 0;
+#pragma unroll 1
+  for (int i = 0; i < nv; i++) mx = max(mx, (uint32_t)(lane_term(from_stage, rp, gp, lane, i) >> 32) & 0x7FFFFFFFu);
+  if (nv > 0 && fast_ok(e, mx)) {
+    const int c = 64 - (e + 1023);
+    uint64_t P = 0, N = 0;
+    bool anytie = false;
+    uint32_t orl = 0, andl = 0xFFFFFFFFu;
+#pragma unroll 1
+    for (int i = 0; i < nv; i++) {
+      const uint64_t x = lane_term(from_stage, rp, gp, lane, i);
+      const uint32_t hi = (uint32_t)(x >> 32);
+      uint64_t ri;
+      bool tie;
+      term_inc_fast(hi, (uint32_t)x, c, ri, tie);
+      if (hi >> 31) N += ri; else P += ri;
+      anytie |= tie;
+      orl |= hi;
+      andl &= hi;
+    }
+    if (!anytie) return lane_pn_run(P, N, orl, andl, nv);
+  }
+  Run r = run_empty();
+#pragma unroll 1
+  for (int i = 0; i < nv; i++) {
+    const uint64_t x = lane_term(from_stage, rp, gp, lane, i);
+    int64_t re;
+    int32_t d;
+    const bool poison = term_inc(x, e, re, d);
+    run_push(r, re, d, term_flags(x) | (poison ? F_POISON : 0u));
+  }
+  return r;
+}
+
+// The items of dirty lane d of this warp's chunk (Research-1433, finding 4),
+// its sixteen terms spread over lanes 0..15: lane i takes term i, its exact
+// fixed-point prefix inside the lane (a scan), its prefix range (the lane's
+// starting value cl plus the prefixes before and after the term, widened by
+// dl) and so its key -- the binade the range stays in, or "carried" -- and its
+// increment for that binade.  A segmented scan composes the runs of one key;
+// each carried term becomes an item of its own, added one by one by the walk.
+// Writes the items below `room` to out (shared memory) and returns their
+// number (at most 16).  Whole warp; the arguments are warp-uniform.
+constexpr int kCarryKey = -4000;
+__device__ __noinline__ int place_lane(const Params &p, const unsigned char *stage, bool from_stage, int64_t lstart,
+                                       int nv, int w, int d, DF cl, uint32_t Lm, float dl, uint64_t t, Rec *out,
+                                       int room) {
+  const int lane = threadIdx.x & 31;
+  const unsigned full = 0xffffffffu;
+  const bool act = lane < nv;
+  uint64_t x = 0;
+  if (act) {
+    if (from_stage) {
+      const unsigned char *rp = stage + (w * 32 + d) * 128;
+      const uint2 v = *reinterpret_cast<const uint2 *>(rp + ((((lane >> 1) ^ (d & 7)) << 4) | ((lane & 1) << 3)));
+      x = ((uint64_t)v.y << 32) | v.x;
+    } else if (sq_ok(p, lstart >= 0 && lstart + nv <= p.n, 3, lstart)) {
+      x = __ldg(reinterpret_cast<const unsigned long long *>(p.x) + lstart + lane);
+    }
+  }
+  const uint32_t hi = (uint32_t)(x >> 32), lo = (uint32_t)x, E = (hi >> 20) & 0x7FFu;
+  const int64_t mag = (int64_t)__funnelshift_rc(lead32(hi, lo, E), 0u, Lm - E);
+  const int64_t v = (hi >> 31) ? -mag : mag;
+  int64_t incl = v;
+#pragma unroll
+  for (int o = 1; o < kLaneTerms; o <<= 1) {
+    const int64_t u = __shfl_up_sync(full, incl, o);
+    if (lane >= o) incl += u;
+  }
+  const float sc = pow2f((int)Lm - 1054);
+  const DF a0 = df_addf(cl, __fmul_rn(f_from_i48(incl - v), sc));
+  const DF a1 = df_addf(cl, __fmul_rn(f_from_i48(incl), sc));
+  const bool up = v >= 0;
+  int ei = 0;
+  bool ok = act && one_binade_df(df_addf(up ? a0 : a1, -dl), df_addf(up ? a1 : a0, dl), ei);
+  ok = act && plan_override(p.plan_mode, ok, ei, t, w, 100 + d * 16 + lane);
+  // a term with |x| >= 2^ei, inf or NaN can never be in a run for ei
+  const int xe = E ? (int)E - 1023 : -1022;
+  if (E == 0x7FFu || xe >= ei) ok = false;
+  const int key = ok ? ei : kCarryKey;
+  Run r = run_empty();
+  if (ok) {
+    int64_t re;
+    int32_t dd;
+    term_inc(x, key, re, dd);
+    run_push(r, re, dd, term_flags(x));
+  }
+  // segments: a head where the key changes; every carried term stands alone
+  const int pkey = __shfl_up_sync(full, key, 1);
+  const bool head = act && (lane == 0 || key != pkey || key == kCarryKey);
+  Run s = r;
+  int f = head ? 1 : 0;
+#pragma unroll 1
+  for (int o = 1; o < kLaneTerms; o <<= 1) {
+    const Run os = shfl_run<SH_UP>(s, o);
+    const int of = __shfl_up_sync(full, f, o);
+    if (lane >= o) { if (!f) s = run_compose(os, s); f |= of; }
+  }
+  const uint32_t heads = __ballot_sync(full, head);
+  const bool end = act && (lane == nv - 1 || ((heads >> (lane + 1)) & 1u));
+  const uint32_t ends = __ballot_sync(full, end);
+  const int idx = __popc(ends & ((1u << lane) - 1u));
+  if (end && idx < room) {
+    const uint32_t tbase = (uint32_t)(w * kChunkTerms + d * kLaneTerms);
+    if (key == kCarryKey) {
+      Run tr = run_empty();
+      tr.inc = (int64_t)x; tr.lo = 0; tr.hi = 0; tr.d = 0;
+      tr.flags = term_flags(x) & (F_HASINF_P | F_HASINF_N | F_HASNAN);
+      out[idx] = make_rec(tr, 0, K_TERMS, 1u, tbase + (uint32_t)lane);
+    } else {
+      const int hl = 31 - __clz(heads & ((2u << lane) - 1u));
+      out[idx] = make_rec(s, key, K_RUN, (uint32_t)(lane - hl + 1), tbase + (uint32_t)hl);
+    }
+  }
+  return __popc(ends);
+}
+
+
+// A chunk the plan could not place in one binade.  Each lane's starting value
+// is the chunk's plus the fixed-point sums of the earlier lanes; a lane whose
+// own range stays in one binade becomes one run (neighbouring runs of one
+// binade merge), the others are placed term by term.  Writes the items for
+// chunk w into the tile's item area and returns their number, or 0 when they
+// do not fit (the caller then records the chunk as one fallback).
+__device__ __noinline__ int split_chunk(const Params &p, const unsigned char *stage, const StageGeo &g, int w,
+                                        int lane, int nv, int64_t lstart, const ChunkPre &pre, Rec *area,
+                                        Rec *stg, unsigned int *st) {
+  const unsigned full = 0xffffffffu;
+  const bool use_tma = g.tma != 0;
+  const int64_t row = (g.start >> 4) + w * 32 + lane;
+  const uint64_t t = (uint64_t)g.t;
+  PROF_START;
+  const bool from_stage = use_tma && row < p.tma_rows;
+  const unsigned char *rp = stage + (w * 32 + lane) * 128;
+  const unsigned long long *gp = reinterpret_cast<const unsigned long long *>(p.x) + lstart;
+  if (!from_stage && !sq_ok(p, nv == 0 || (lstart >= 0 && lstart + nv <= p.n), 3, lstart)) nv = 0;
+  uint32_t mx = 0, orz = 0, andh = 0xFFFFFFFFu;
+#pragma unroll 1
+  for (int i = 0; i < nv; i++) {
+    const uint64_t x = lane_term(from_stage, rp, gp, lane, i);
+    const uint32_t mag = (uint32_t)(x >> 32) & 0x7FFFFFFFu;
+    mx = max(mx, mag);
+    orz |= mag | (uint32_t)x;
+    andh &= (uint32_t)(x >> 32);
+  }
+  const uint32_t Lm = mx >> 20;
+  uint64_t all = 0, neg = 0;
+#pragma unroll 1
+  for (int i = 0; i < nv; i++) {
+    const uint64_t x = lane_term(from_stage, rp, gp, lane, i);
+    const uint32_t hi = (uint32_t)(x >> 32), E = (hi >> 20) & 0x7FFu;
+    const uint32_t v = __funnelshift_rc(lead32(hi, (uint32_t)x, E), 0u, Lm - E);
+    all += v;
+    neg += (hi >> 31) ? v : 0u;
+  }
+  const uint32_t Lc = __reduce_max_sync(full, Lm), sh = min(Lc - Lm, 63u);
+  const int64_t sv = (int64_t)((all - neg) >> sh) - (int64_t)(neg >> sh);
+  // the earlier lanes' signed sum, at the chunk's scale
+  int64_t is = sv;
 #pragma unroll 1
   for (int o = 1; o < 32; o <<= 1) {
-    const float a = __shfl_up_sync(0xffffffffu, isig, o);
-    const float b = __shfl_up_sync(0xffffffffu, iab, o);
-    if (lane >= o) { isig += a; iab += b; }
+    const int64_t v = __shfl_up_sync(full, is, o);
+    if (lane >= o) is += v;
   }
-  const DF A0 = df_addf(sc, isig - sig);
-  const float A = A0.hi + A0.lo;
-  const float P = 0.5f * (ab + sig), N = 0.5f * (ab - sig);
-  const float dbase = kEps * (ac + (iab - ab) + ab) + kTinyF;
-  const float dl = dbase + kRelF32 * (fabsf(A) + ab);
+  const DF cl = df_add(pre.c, df_fixed(is - sv, (int)Lc));
+  const float Pl = f_fixed(all - neg, (int)Lm), Nl = f_fixed(neg, (int)Lm);
+  const float dl = pre.delta;
   int e_l = 0;
-  bool clean = one_binade_f(A - N - dl, A + P + dl, e_l);
+  bool clean = one_binade_df(df_addf(cl, -(Nl + dl)), df_addf(cl, Pl + dl), e_l);
   clean = plan_override(p.plan_mode, clean, e_l, t, w, lane + 1);
   const bool zl = (orz == 0);
   const bool dirty = !clean && !zl && nv > 0;
-  Run r = run_empty();
-  if (!dirty) r = lane_run_general(p, stage, use_tma, row, lstart, nv, w, lane, clean ? e_l : 0);
+  SPLIT_PT(0);                                                // lane sums, prefixes, verdicts
+  Run r = run_empty();                                       // a lane of zeros: a run of zeros
+  if (zl && !(andh >> 31)) r.flags &= ~F_ALLNEGZ;             // (all -0 only if every term is -0)
+  if (clean && !zl) r = lane_run_any(p, from_stage, rp, gp, nv, lane, e_l);
+  __syncwarp();
+  SPLIT_PT(1);                                                // clean lanes' runs
   const int key = dirty ? kDirtyKey : (clean ? e_l : kZeroE);
-  const int ndirty = dirty ? lane_items(p, xs, nv, A, dbase, t, w, lane, nullptr) : 0;
   if (dirty) atomicAdd(&st[S_LANE_DIRTY], 1u);
   // merge neighbouring runs of one key (lanes past the end join the previous)
-  const int pkey = __shfl_up_sync(0xffffffffu, key, 1);
+  const int pkey = __shfl_up_sync(full, key, 1);
   const bool head = (lane == 0) || (nv > 0 && (dirty || pkey == kDirtyKey || key != pkey));
   Run v = r;
   int fl = head ? 1 : 0;
 #pragma unroll 1
   for (int o = 1; o < 32; o <<= 1) {
     const Run ov = shfl_run<SH_UP>(v, o);
-    const int of = __shfl_up_sync(0xffffffffu, fl, o);
+    const int of = __shfl_up_sync(full, fl, o);
     if (lane >= o) { if (!fl) v = run_compose(ov, v); fl |= of; }
   }
-  const uint32_t heads = __ballot_sync(0xffffffffu, head);
+  const uint32_t heads = __ballot_sync(full, head);
   const bool end = (lane == 31) || ((heads >> (lane + 1)) & 1u);
-  const uint32_t le = heads & ((lane == 31) ? 0xffffffffu : ((2u << lane) - 1u));
+  const uint32_t le = heads & ((lane == 31) ? full : ((2u << lane) - 1u));
   const int hlane = 31 - __clz(le);
-  const int hkey = __shfl_sync(0xffffffffu, key, hlane);
+  const int hkey = __shfl_sync(full, key, hlane);
   // terms before each lane, for the item counts
   int csum = nv;
 #pragma unroll 1
   for (int o = 1; o < 32; o <<= 1) {
-    const int vv = __shfl_up_sync(0xffffffffu, csum, o);
+    const int vv = __shfl_up_sync(full, csum, o);
     if (lane >= o) csum += vv;
   }
-  const int before_head = __shfl_sync(0xffffffffu, csum - nv, hlane);
-  // items per lane: a merged run at its end lane, or the dirty lane's own
-  // items; if they do not fit, each dirty lane becomes one fallback item
-  bool lane_fb = false;
-  int myitems = dirty ? ndirty : ((end && hkey != kDirtyKey) ? 1 : 0);
-  int ioff = 0, total = 0;
-  for (int attempt = 0; attempt < 2; attempt++) {
-    ioff = myitems;
+  const int before_head = __shfl_sync(full, csum - nv, hlane);
+  // the chunk's items in lane order, staged in shared memory: a merged run at
+  // its end lane, a dirty lane's own items; if they do not fit, each dirty
+  // lane becomes one fallback item instead
+  SPLIT_PT(2);                                                // merges and counts
+  const uint32_t dirtym = __ballot_sync(full, dirty);
+  const uint32_t cleanm = __ballot_sync(full, !dirty && end && hkey != kDirtyKey);
+  const Rec myrun = make_rec(v, hkey, K_RUN, (uint32_t)(csum - before_head), (uint32_t)(w * kChunkTerms + hlane * kLaneTerms));
+  const uint32_t below = (1u << lane) - 1u;
+  int n = 0;
+  uint32_t emitted = 0;                                // lanes whose items are staged
+  for (uint32_t m = dirtym; m; m &= m - 1) {
+    const int d = __ffs(m) - 1;
+    const uint32_t cm = cleanm & ((1u << d) - 1u) & ~emitted;
+    if (((cm >> lane) & 1u) && n + __popc(cm & below) < kChunkSlots) stg[n + __popc(cm & below)] = myrun;
+    n += __popc(cm);
+    emitted |= (2u << d) - 1u;
+    const DF cd = DF{__shfl_sync(full, cl.hi, d), __shfl_sync(full, cl.lo, d)};
+    const bool fs = use_tma && (g.start >> 4) + w * 32 + d < p.tma_rows;
+    SPLIT_PT(3);                                              // between dirty lanes
+    n += place_lane(p, stage, fs, __shfl_sync(full, lstart, d), __shfl_sync(full, nv, d), w, d, cd,
+                    __shfl_sync(full, Lm, d), dl, t, stg + min(n, kChunkSlots), max(kChunkSlots - n, 0));
+    SPLIT_PT(4);                                              // one dirty lane placed
+  }
+  {
+    const uint32_t cm = cleanm & ~emitted;
+    if (((cm >> lane) & 1u) && n + __popc(cm & below) < kChunkSlots) stg[n + __popc(cm & below)] = myrun;
+    n += __popc(cm);
+  }
+  if (n > kChunkSlots) {
+    // one item per clean end lane and per dirty lane (at most 32)
+    const uint32_t em = cleanm | dirtym;
+    n = __popc(em);
+    __syncwarp();
+    if ((em >> lane) & 1u) {
+      if (dirty) {
+        Run fr = run_empty();
+        uint32_t tf = 0;
 #pragma unroll 1
-    for (int o = 1; o < 32; o <<= 1) {
-      const int vv = __shfl_up_sync(0xffffffffu, ioff, o);
-      if (lane >= o) ioff += vv;
+        for (int i = 0; i < nv; i++) tf |= term_flags(lane_term(from_stage, rp, gp, lane, i));
+        fr.flags = tf & (F_HASINF_P | F_HASINF_N | F_HASNAN);
+        stg[__popc(em & below)] = make_rec(fr, 0, K_FALLBACK, (uint32_t)nv, (uint32_t)(w * kChunkTerms + lane * kLaneTerms));
+      } else {
+        stg[__popc(em & below)] = myrun;
+      }
     }
-    total = __shfl_sync(0xffffffffu, ioff, 31);
-    ioff -= myitems;
-    if (total <= kChunkSlots) break;
-    lane_fb = true;
-    myitems = dirty ? 1 : ((end && hkey != kDirtyKey) ? 1 : 0);
   }
-#ifdef SEQSUM_CHECKS
-  if (t == 0 && w == 0) {
-    p.dbg[14000 + lane] = (unsigned long long)dirty | ((unsigned long long)clean << 1) | ((unsigned long long)zl << 2) |
-                          ((unsigned long long)head << 3) | ((unsigned long long)end << 4) |
-                          ((unsigned long long)lane_fb << 5) | ((unsigned long long)(hlane & 63) << 8) |
-                          ((unsigned long long)(myitems & 255) << 16) | ((unsigned long long)(ioff & 255) << 24) |
-                          ((unsigned long long)(total & 255) << 32) | ((unsigned long long)(ndirty & 255) << 40) |
-                          ((unsigned long long)(uint16_t)(int16_t)key << 48);
-    p.dbg[14040 + lane] = (unsigned long long)__float_as_uint(A) | ((unsigned long long)__float_as_uint(dl) << 32);
-    p.dbg[14080 + lane] = (unsigned long long)__float_as_uint(P) | ((unsigned long long)__float_as_uint(N) << 32);
-  }
-#endif
-  if (total > kChunkSlots) return 0;
+  __syncwarp();
   Rec *out = area + w * kChunkSlots;
-  if (!dirty && myitems && item_ok(p, out + ioff, 5))
-    stcg_rec(out + ioff, make_rec(v, hkey, K_RUN, (uint32_t)(csum - before_head),
-                                  (uint32_t)(w * kChunkTerms + hlane * kLaneTerms)));
-  if (dirty && lane_fb) {
-    if (item_ok(p, out + ioff, 16)) {
-      Run fr = run_empty();
-      uint32_t tf = 0;
-      for (int i = 0; i < nv; i++) tf |= term_flags(xs[i]);
-      fr.flags = tf & (F_HASINF_P | F_HASINF_N | F_HASNAN);
-      stcg_rec(out + ioff, make_rec(fr, 0, K_FALLBACK, (uint32_t)nv, (uint32_t)(w * kChunkTerms + lane * kLaneTerms)));
-    }
-  } else if (dirty) {
-    lane_items(p, xs, nv, A, dbase, t, w, lane, out + ioff);
-  }
+  if (lane < n && item_ok(p, out + lane, 5)) stcg_rec(out + lane, stg[lane]);
+  const int total = n;
+  SPLIT_PT(5);                                                // staging written out
   return total;
 }
 
-// ---------------------------------------------------------------- streaming units
-// A streaming CTA has eight compute warps (warp w owns chunk w of every tile)
-// and a control warp.  Per stage two mbarriers: full (the tile's copy and,
-// for a run unit, its plan words have landed; the unit is described in
-// sm.tk/kind/tma) and done (the eight compute warps finished the unit).  The
-// control warp takes the tickets, issues the copies and runs each unit's
-// epilogue (publishing the plan's aggregates or the tile's header), so the
-// compute warps never wait for one another.
-enum : int { U_PLAN = 0, U_RUN = 1, U_END = 2 };
-
-// The plan's sums of this warp's chunk of tile t (fp32 images of the terms,
-// their sum and |x| sum) into sm.wa[k][w].
-__device__ __forceinline__ void chunk_sums_of(const uint64_t *xs, float &sig, float &ab) {
-  sig = 0.0f;
-  ab = 0.0f;
-#pragma unroll
-  for (int i = 0; i < kLaneTerms; i++) {
-    const float f = approx_term_clamped((uint32_t)(xs[i] >> 32));
-    sig += f;
-    ab += fabsf(f);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    sig += __shfl_xor_sync(0xffffffffu, sig, o);
-    ab += __shfl_xor_sync(0xffffffffu, ab, o);
-  }
-}
-__device__ __noinline__ void chunk_aggregate(const Params &p, Smem &sm, const unsigned char *stage, int k,
-                                             int64_t t, int64_t ntiles) {
+// ---------------------------------------------------------------- a tile's runs
+// Compute warp w, a run unit: the verdict on chunk w of the tile from the
+// plan words, then the exact run (or items) of chunk w (Research-1433, finding 2 "Inside a binade the loop is an integer
+// sum", finding 3 "Ties need the parity of the running integer"); the chunk's
+// record goes to sm.chunk[k][w] for the control warp's header.
+__device__ __noinline__ void run_chunk(const Params &p, Smem &sm, const unsigned char *stage, int k) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const TileGeo g = tile_geo(p, t, ntiles);
-  const int64_t lstart = g.start + (int64_t)w * kChunkTerms + (int64_t)lane * kLaneTerms;
-  const int nv = (int)max((int64_t)0, min((int64_t)kLaneTerms, g.end - lstart));
-  uint64_t xs[kLaneTerms];
-  load_lane(p, stage, sm.tma[k] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, xs);
-  float sig, ab;
-  chunk_sums_of(xs, sig, ab);
-  if (lane == 0) sm.wa[k][w] = WarpAgg{sig, ab, 0u, 0u};
-}
-
-// Control warp, after a plan unit: publish the tile's approximate sum (for
-// its run unit) and, for the scanner, the same sum -- or s0 plus it for the
-// first tile of a sum.
-__device__ __noinline__ void plan_epilogue(const Params &p, Smem &sm, int k, int64_t t, int64_t ntiles) {
-  const int lane = threadIdx.x & 31;
-  if (!sq_ok(p, t >= 0 && t < p.cap_tiles, 6, t)) return;
-  const TileGeo g = tile_geo(p, t, ntiles);
-  WarpAgg a = WarpAgg{0.0f, 0.0f, 0u, 0u};
-  if (lane < kWarps) a = sm.wa[k][lane];
-  DF agg = DF{a.sig, 0.0f};
-  float agga = a.ab;
-#pragma unroll
-  for (int o = kWarps / 2; o > 0; o >>= 1) {
-    agg = df_add(agg, shfl_xor_df(agg, o));
-    agga += __shfl_xor_sync(0xffffffffu, agga, o);
-  }
-  if (lane == 0) {
-    publish_status(p.tagg + 2 * t, agg, agga, p.epoch, 0);     // the tile's own sum, for its run unit
-    if (g.tile_in_sum != 0) {
-      publish_status(p.status + 2 * t, agg, agga, p.epoch, 0);
-    } else {
-      const DF ex = df_from_double(p.s0s ? p.s0s[g.sum] : p.s0);
-      publish_status(p.status + 2 * t, df_add(ex, agg), fabsf(ex.hi) + agga, p.epoch, 1);
-    }
-  }
-}
-
-// Compute warp w, a run unit: the exact run (or items) of chunk w of tile t
-// under the binade its approximate prefix names; the chunk's record goes to
-// sm.chunk[k][w] for the control warp's header.
-__device__ __noinline__ void chunk_runs(const Params &p, Smem &sm, const unsigned char *stage, int k, int64_t t,
-                                        int64_t ntiles, uint32_t &sums_ph) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const unsigned full = 0xffffffffu;
   unsigned int *st = sm.st;
-  const TileGeo g = tile_geo(p, t, ntiles);
-  const uint32_t tag0 = p.epoch << 1, tag1 = tag0 | 1u;
-  // ---- the plan words: the prefix before the tile and the tile's own sums
-  DF sp;
-  float ap;
-  if (t == g.first_tile) {
-    sp = df_from_double(p.s0s ? p.s0s[g.sum] : p.s0);
-    ap = fabsf(sp.hi);
+  const StageGeo &g = sm.geo[k];
+  // ---- the plan words, copied in with the tile (else read again from
+  // global memory, bounded): the prefix before the tile and its chunk plans
+  const uint32_t tag = (p.epoch << 1) | 1u;
+  const uint64_t tv = globaltimer();
+  DF ex;
+  float exab;
+  if (g.t == g.first_tile) {
+    ex = df_from_double(p.s0s ? p.s0s[g.sum] : p.s0);
+    exab = fabsf(ex.hi);
   } else {
     const uint64_t A = sm.pre_raw[k][0], B = sm.pre_raw[k][1];
-    if ((uint32_t)(A & 0xFF) == tag1 && (uint32_t)B == tag1) {
-      sp = status_sum(A);
-      ap = status_abs(B);
+    if ((uint32_t)(A & 0xFF) == tag && (uint32_t)B == tag) {
+      ex = status_sum(A);
+      exab = status_abs(B);
     } else {
-      Prefix pr{DF{0.0f, 0.0f}, 0.0f};
-      if (lane == 0) {
-        const uint64_t tl = globaltimer();
-        pr = read_prefix(p, g.sum, g.first_tile, t, st);
-        atomicAdd(&st[S_NS_PREFIX_WAIT], (unsigned)(globaltimer() - tl));
-      }
-      sp = DF{__shfl_sync(full, pr.ex.hi, 0), __shfl_sync(full, pr.ex.lo, 0)};
-      ap = __shfl_sync(full, pr.ex_abs, 0);
+      read_prefix(p, sm, g.t, ex, exab);
     }
   }
-  uint64_t TA = sm.tagg_raw[k][0], TB = sm.tagg_raw[k][1];
-  if (!((uint32_t)(TA & 0xFF) == tag0 && (uint32_t)TB == tag0)) {
-    // not copied in time: wait for the plan unit's word (bounded)
-    if (lane == 0) {
-      const uint64_t t0 = globaltimer();
-      while (true) {
-        ld_vol_v2(p.tagg + 2 * t, TA, TB);
-        if ((uint32_t)(TA & 0xFF) == tag0 && (uint32_t)TB == tag0) break;
-        if (globaltimer() - t0 > kWaitNs) {
-          note_timeout(p, ERR_PLAN_TIMEOUT, TO_TILESUM, (uint32_t)t, (uint32_t)((TA & 0xFF) | (p.epoch << 16)));
-          break;
-        }
-        __nanosleep(32);
-      }
-      atomicAdd(&st[S_NS_PREFIX_WAIT], (unsigned)(globaltimer() - t0));
-    }
-    TA = __shfl_sync(full, TA, 0);
-    TB = __shfl_sync(full, TB, 0);
+  ChunkPlan cp{0ull, 0ull, 0, 0u, 0u, 0u};
+  bool have = true;
+  if (lane < kWarps) {
+    const uint64_t *q = &sm.cplan_raw[k][4 * lane];
+    have = cplan_of(q[0], q[1], q[2], q[3], tag, cp);
   }
-  const bool tagg_ok = (uint32_t)(TA & 0xFF) == tag0 && (uint32_t)TB == tag0;
-  // ---- this lane's terms and the chunk's exact stats (the fast runs'
-  // preconditions)
+  if (!__all_sync(full, have)) {
+    const uint64_t t0 = globaltimer();
+    uint32_t nap = 32;
+    while (!__all_sync(full, have)) {
+      if (!have) {
+        uint64_t w0, w1, w2, w3;
+        const uint64_t *q = p.cplan + (g.t * kWarps + lane) * 4;
+        ld_vol_v2(q, w0, w1);
+        ld_vol_v2(q + 2, w2, w3);
+        have = cplan_of(w0, w1, w2, w3, tag, cp);
+      }
+      if (__any_sync(full, globaltimer() - t0 > kWaitNs)) {
+        if (lane == 0) note_timeout(p, ERR_PLAN_TIMEOUT, TO_PLANNED, (uint32_t)g.t, (uint32_t)w);
+        cp = ChunkPlan{0ull, 0ull, 0, 0u, WA_NZ | WA_NEG | WA_POS, 0u};    // no plan: every chunk is split
+        break;
+      }
+      __nanosleep(nap);
+      nap = min(nap * 2u, 256u);
+    }
+    if (lane == 0) atomicAdd(&st[S_NS_VERDICT_WAIT], (unsigned)(globaltimer() - t0));
+  }
+  uint32_t cmx, cflags;
+  const ChunkPre pre = chunk_verdict(g, w, ex, exab, cp, cmx, cflags);
+  if (lane == 0) atomicAdd(&st[S_NS_VERDICT], (unsigned)(globaltimer() - tv));
   const int64_t cstart = g.start + (int64_t)w * kChunkTerms;
   const int cnt_chunk = (int)max((int64_t)0, min((int64_t)kChunkTerms, g.end - cstart));
   const int64_t lstart = cstart + (int64_t)lane * kLaneTerms;
   const int nv = (int)max((int64_t)0, min((int64_t)kLaneTerms, g.end - lstart));
-  uint64_t xs[kLaneTerms];
-  load_lane(p, stage, sm.tma[k] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, xs);
-  WarpAgg me = WarpAgg{0.0f, 0.0f, 0u, 0u};
-  {
-    uint32_t orh = 0, orz = 0, mx = 0;
-#pragma unroll
-    for (int i = 0; i < kLaneTerms; i++) {
-      const uint32_t hi = (uint32_t)(xs[i] >> 32);
-      const uint32_t mag = hi & 0x7FFFFFFFu;
-      orh |= hi;
-      orz |= mag | (uint32_t)xs[i];
-      mx = max(mx, mag);
-    }
-    me.mx = __reduce_max_sync(full, mx);
-    me.flags = ((__reduce_or_sync(full, orh) >> 31) ? WA_NEG : 0u) | (__reduce_or_sync(full, orz) ? WA_NZ : 0u);
-  }
-  // ---- the binade: one for the whole tile when the prefix range of every
-  // term in it stays inside one (the common case); else chunk by chunk
-  DF sc = sp;
-  float ac = ap;
-  int e = 0;
-  bool clean;
-  {
-    const DF tsd = status_sum(TA);
-    const float c = sp.hi + sp.lo, ts = tsd.hi + tsd.lo, tab = status_abs(TB);
-    const float P = 0.5f * (tab + ts), N = 0.5f * (tab - ts);
-    const float delta = kEps * (ap + tab) + kRelF32 * (fabsf(c) + tab) + kTinyF;
-    clean = tagg_ok && p.plan_mode == 0 && one_binade_f(c - N - delta, c + P + delta, e);
-  }
-  if (!clean) {
-    // the same words reach every compute warp, so all of them come here;
-    // they trade their chunks' sums through a per-stage barrier (bounded)
-    float sig, ab;
-    chunk_sums_of(xs, sig, ab);
-    if (lane == 0) sm.wa[k][w] = WarpAgg{sig, ab, 0u, 0u};
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.sums[k]);
-    if (lane == 0) beat(p, sm.role, HB_WAIT_SUMS, (uint64_t)t);
-    mbar_wait(p, &sm.sums[k], (sums_ph >> k) & 1u, ERR_PLAN_TIMEOUT, TO_SUMS, (uint32_t)t, (uint32_t)w);
-    sums_ph ^= 1u << k;
-    if (tid == 0) atomicAdd(&st[S_PLAN_LOCAL], 1u);
-    for (int j = 0; j < w; j++) { sc = df_addf(sc, sm.wa[k][j].sig); ac += sm.wa[k][j].ab; }
-    me.sig = sig;
-    me.ab = ab;
-    const float P = 0.5f * (ab + sig), N = 0.5f * (ab - sig);
-    const float c = sc.hi + sc.lo;
-    const float delta = kEps * (ac + ab) + kRelF32 * (fabsf(c) + ab) + kTinyF;
-    clean = one_binade_f(c - N - delta, c + P + delta, e);
-    clean = plan_override(p.plan_mode, clean, e, (uint64_t)t, w, 0);
-  }
-  Rec *area = p.items + t * kTileSlots;
+  const int64_t row = (g.start >> 4) + w * 32 + lane;
+  int mode = pre.mode, e = pre.e;
+  if (p.plan_mode != 0 && mode != CP_ZERO)
+    mode = plan_override(p.plan_mode, mode == CP_CLEAN, e, (uint64_t)g.t, w, 0) ? CP_CLEAN : CP_DIRTY;
+  Rec *area = p.items + g.t * kTileSlots;
   Rec crec;
   int nitems = 0;
-  const bool zero_chunk = (me.flags & WA_NZ) == 0;
-  if (clean || zero_chunk) {
-    if (zero_chunk) e = 0;
-    const int eb = e + 1023;
-    const bool fast = !zero_chunk && e >= -969 && e <= 1023 && (int)(me.mx >> 20) < eb;
+  if (mode == CP_ZERO) {
+    // every term is +0 or -0: a run of zeros (all -0 keeps a -0 sum at -0)
+    Run z = run_empty();
+    if (cflags & WA_POS) z.flags &= ~F_ALLNEGZ;
+    crec = make_rec(z, kZeroE, K_RUN, (uint32_t)cnt_chunk, (uint32_t)(w * kChunkTerms));
+    if (lane == 0) atomicAdd(&st[S_CHUNK_RUN], 1u);
+  } else if (mode == CP_CLEAN) {
+    uint64_t xs[kLaneTerms];
+    load_lane(p, stage, g.tma != 0, row, lstart, nv, w, lane, xs);
     Run r;
     bool general = true, general_reduce = true;
-    if (fast) {
-      const int c = 64 - eb;
-      if ((me.flags & WA_NEG) == 0) {
-        // non-negative terms: the run is a plain sum of increments
-        uint64_t a = 0;
-        bool anytie = false;
+    if (fast_ok(e, cmx)) {
+      uint64_t P, N;
+      bool anytie;
+      uint32_t orl, andl;
+      lane_fast(xs, nv, 64 - (e + 1023), P, N, anytie, orl, andl);
+      if ((cflags & WA_NEG) == 0 && __ballot_sync(full, anytie) == 0) {
+        // non-negative terms and no tie: the run is a plain sum of increments
 #pragma unroll
-        for (int i = 0; i < kLaneTerms; i++) {
-          uint64_t ri;
-          bool tie;
-          term_inc_fast((uint32_t)(xs[i] >> 32), (uint32_t)xs[i], c, ri, tie);
-          a += ri;
-          anytie |= tie;
-        }
-        if (__ballot_sync(0xffffffffu, anytie) == 0) {
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-          r.inc = (int64_t)a; r.lo = 0; r.hi = (int64_t)a; r.d = 0; r.flags = F_NONNEG;
-          general = general_reduce = false;
-        } else if (!anytie) {
-          r.inc = (int64_t)a; r.lo = 0; r.hi = (int64_t)a; r.d = 0;
-          r.flags = F_NONNEG | (nv == 0 ? (F_NONPOS | F_ZERO | F_ALLNEGZ) : 0u);
-          general = false;
-        }
-      } else {
-        // signed terms: positive and negative increments summed apart give
-        // bounds for every prefix
-        uint64_t P = 0, Nn = 0;
-        bool anytie = false;
-        uint32_t orl = 0, andl = 0xFFFFFFFFu;
-#pragma unroll
-        for (int i = 0; i < kLaneTerms; i++) {
-          const uint32_t hi = (uint32_t)(xs[i] >> 32);
-          uint64_t ri;
-          bool tie;
-          term_inc_fast(hi, (uint32_t)xs[i], c, ri, tie);
-          if (hi >> 31) Nn += ri; else P += ri;
-          anytie |= tie;
-          if (i < nv) { orl |= hi; andl &= hi; }
-        }
-        if (!anytie) {
-          if (nv == 0) {
-            r = run_empty();
-          } else {
-            r.inc = (int64_t)(P - Nn); r.lo = -(int64_t)Nn; r.hi = (int64_t)P; r.d = 0;
-            r.flags = ((orl >> 31) ? 0u : F_NONNEG) | ((andl >> 31) ? F_NONPOS : 0u);
-          }
-          general = false;
-        }
+        for (int o = 16; o > 0; o >>= 1) P += __shfl_xor_sync(full, P, o);
+        r.inc = (int64_t)P; r.lo = 0; r.hi = (int64_t)P; r.d = 0; r.flags = F_NONNEG;
+        general = general_reduce = false;
+      } else if (!anytie) {
+        // positive and negative increments summed apart bound every prefix
+        r = lane_pn_run(P, N, orl, andl, nv);
+        general = false;
       }
     }
-    if (general) r = lane_run_general(p, stage, sm.tma[k] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, e);
+    if (general) r = lane_run_general(p, stage, g.tma != 0, row, lstart, nv, w, lane, e);
     if (general_reduce) {
 #pragma unroll 1
       for (int off = 1; off < 32; off <<= 1) {
@@ -1145,11 +1438,11 @@ __device__ __noinline__ void chunk_runs(const Params &p, Smem &sm, const unsigne
     crec = make_rec(r, (r.flags & F_ZERO) ? kZeroE : e, K_RUN, (uint32_t)cnt_chunk, (uint32_t)(w * kChunkTerms));
     if (lane == 0) atomicAdd(&st[S_CHUNK_RUN], 1u);
   } else {
-    nitems = split_chunk(p, stage, sm.tma[k] != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, sc, ac,
-                         (uint64_t)t, area, st);
+    if (lane == 0) atomicAdd(&st[S_CHUNK_DIRTY], 1u);
+    nitems = split_chunk(p, stage, g, w, lane, nv, lstart, pre, area, sm.stg[w], st);
     if (nitems == 0) {
       Run fr = run_empty();
-      fr.flags = ((me.mx >= 0x7FF00000u) ? (F_HASINF_P | F_HASINF_N | F_HASNAN) : 0u);
+      fr.flags = ((cmx >= 0x7FF00000u) ? (F_HASINF_P | F_HASINF_N | F_HASNAN) : 0u);
       crec = make_rec(fr, 0, K_FALLBACK, (uint32_t)cnt_chunk, (uint32_t)(w * kChunkTerms));
       if (lane == 0) {
         if (item_ok(p, area + w * kChunkSlots, 7)) stcg_rec(area + w * kChunkSlots, crec);
@@ -1168,13 +1461,14 @@ __device__ __noinline__ void chunk_runs(const Params &p, Smem &sm, const unsigne
   }
 }
 
-// Control warp, after a run unit: the tile's header -- one run when every
+// Control warp, after a tile's runs: the tile's header -- one run when every
 // chunk is a run of one binade (runs of zeros fit any), else the chunks'
 // items in the tile's item area.
-__device__ __noinline__ void run_epilogue(const Params &p, Smem &sm, int k, int64_t t, int64_t ntiles) {
+__device__ __noinline__ void run_epilogue(const Params &p, Smem &sm, int k) {
   const int lane = threadIdx.x & 31;
   unsigned int *st = sm.st;
-  const TileGeo g = tile_geo(p, t, ntiles);
+  const StageGeo &g = sm.geo[k];
+  const int64_t t = g.t;
   Rec *area = p.items + t * kTileSlots;
   const unsigned full = 0xffffffffu;
   Rec c = make_rec(run_empty(), kZeroE, K_RUN, 0, 0);
@@ -1352,6 +1646,7 @@ __device__ __noinline__ int resolve_rejection(const Params &p, const Rec *el, co
 #define WALK_PT(id) do { } while (0)
 #endif
 
+
 // Walk sum k over its tiles [tb, te), as the headers appear.  Whole CTA (256
 // threads); the in-order pass runs on warp 0.  Per batch of up to 1024 ready
 // tiles: the headers are staged, the elements (simple tile headers, the items
@@ -1379,6 +1674,8 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
   if (tid == 0) sm.S = dbits(p.s0s ? p.s0s[k] : p.s0);
   int64_t pos = tb;
   uint64_t t_work0 = 0;
+  int nbatch = 0;
+  (void)nbatch;
 #ifdef SEQSUM_PROFILE
   long long prof_t = clock64();
 #endif
@@ -1465,6 +1762,8 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       beat(p, sm.role, HB_BATCH, ((uint64_t)m << 32) | (uint32_t)pos);
       atomicAdd(&st[S_WALK_BATCHES], 1u);
       t_work0 = globaltimer();
+      TRACE_BATCH(nbatch, 0, t_work0);
+      TRACE_BATCH(nbatch, 2, ((unsigned long long)m << 32) | (uint64_t)pos);
       atomicAdd(&st[S_NS_WALK_WAIT], (unsigned)(t_work0 - t0));
       if (pos + m >= te) p.stats[S_T_WALK0] = t_work0;
     }
@@ -1787,6 +2086,8 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       from = rs;
     }
     pos += m;
+    if (tid == 0) { TRACE_BATCH(nbatch, 1, globaltimer()); TRACE_BATCH(nbatch, 3, (unsigned long long)nel); }
+    nbatch++;
     wide_sync(p, sm, 19);
     WALK_PT(15);
   }
@@ -1800,41 +2101,107 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
 }
 
 // ---------------------------------------------------------------- the streaming loops
+// A streaming CTA has eight compute warps (warp w owns chunk w of every
+// tile), a control warp and a look-back warp.  Per stage four mbarriers:
+// full (the tile's copy landed; the tile is described in sm.geo), planned
+// (the tile's approximate sum is published), prefix (the look-back's
+// verdicts are in), done (the compute warps' records are in).  A compute
+// warp plans the next tile while the look-back of the current one is still
+// running, so no tile's plan waits for another tile's prefix.
+
+// The tile a ticket names, found by the control warp (a 32-way search over
+// the sums' first tiles for a batched call).
+__device__ __noinline__ StageGeo stage_geo(const Params &p, int64_t t) {
+  const int lane = threadIdx.x & 31;
+  const unsigned full = 0xffffffffu;
+  StageGeo g;
+  g.t = t;
+  g.kind = U_PLAN;
+  g.pad = 0;
+  if (p.offsets == nullptr) {
+    g.sum = 0;
+    g.first_tile = 0;
+    g.sum_start = 0;
+    g.start = t * kTileTerms;
+    g.end = min(p.n, g.start + kTileTerms);
+  } else {
+    // the last sum k with tile_begin[k] <= t; empty sums share their
+    // successor's tile_begin, and the search lands on the non-empty one
+    // (invariant: tile_begin[lo] <= t < tile_begin[hi])
+    int lo = 0, hi = p.nsums;
+    while (hi - lo > 1) {
+      const int step = (hi - lo + 31) / 32;
+      const int idx = lo + lane * step;
+      const bool le = idx < hi && __ldcg(&p.tile_begin[idx]) <= t;
+      const uint32_t m = __ballot_sync(full, le);          // lane 0 (idx = lo) always
+      lo += (31 - __clz(m)) * step;
+      hi = min(hi, lo + step);
+    }
+    g.sum = lo;
+    g.first_tile = __ldcg(&p.tile_begin[lo]);
+    g.sum_start = p.offsets[lo];
+    g.start = g.sum_start + (t - g.first_tile) * kTileTerms;
+    g.end = min(p.offsets[lo + 1], g.start + kTileTerms);
+  }
+  g.tma = (p.tma_rows != 0 && (g.start & 15) == 0) ? 1 : 0;
+  return g;
+}
+
+// Units of work.  Every tile has a plan unit (copy it, publish its chunks'
+// fixed-point sums and the tile's approximate sum) and a run unit (copy it
+// again, form its runs under the verdicts that its prefix and chunk sums give).
+// Tickets hand out the plan units of the first `wave` tiles, then a run unit
+// and a plan unit in turn, then the remaining run units: the plan of tile t
+// precedes the run of tile t + 1 by about `wave` tiles, so a run unit's prefix
+// is normally published long before it is needed, and its tile is still in L2.
+// Returns true for a plan unit.
+__device__ __forceinline__ bool unit_of(int64_t u, int64_t ntiles, int64_t wave, int64_t &tile) {
+  const int64_t w = min(wave, ntiles);
+  if (u < w) { tile = u; return true; }
+  const int64_t v = u - w, rest = ntiles - w;
+  if (v < 2 * rest) {
+    tile = (v & 1) ? w + (v >> 1) : (v >> 1);
+    return (v & 1) != 0;
+  }
+  tile = rest + (v - 2 * rest);
+  return false;
+}
 
 // Compute warps: the units of the stages in turn, until the control warp
 // marks the end.
-__device__ __noinline__ void compute_loop(const Params &p, Smem &sm, const unsigned char *dyn, int64_t ntiles) {
-  const int tid = threadIdx.x, lane = tid & 31;
+__device__ __noinline__ void compute_loop(const Params &p, Smem &sm, const unsigned char *dyn) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  unsigned int *st = sm.st;
   uint32_t ph = 0;                                       // bit k: parity of full[k]
-  uint32_t sums_ph = 0;                                  // bit k: parity of sums[k]
   for (int j = 0;; j++) {
     const int k = j % kStages;
     const uint64_t tw = (tid == 0) ? globaltimer() : 0;
     if (lane == 0) beat(p, sm.role, HB_WAIT_UNIT, (uint64_t)j);
-    if (!mbar_wait(p, &sm.full[k], (ph >> k) & 1u, ERR_TMA_TIMEOUT, TO_FULL, (uint32_t)j,
-                   (uint32_t)(k | (tid >> 5) << 8 | blockIdx.x << 16)))
+    if (!mbar_wait_warp(p, &sm.full[k], (ph >> k) & 1u, ERR_TMA_TIMEOUT, TO_FULL, (uint32_t)j,
+                        (uint32_t)(k | w << 8 | blockIdx.x << 16)))
       break;                                             // the call has failed
     ph ^= 1u << k;
-    if (tid == 0) atomicAdd(&sm.st[S_NS_TMA_WAIT], (unsigned)(globaltimer() - tw));
-    const int kind = sm.kind[k];
+    if (tid == 0) atomicAdd(&st[S_NS_TMA_WAIT], (unsigned)(globaltimer() - tw));
+    const int kind = sm.geo[k].kind;
     if (kind == U_END) break;
-    const int64_t t = sm.tk[k];
+    const int64_t t = sm.geo[k].t;
     const unsigned char *stage = dyn + k * kStageBytes;
     const uint64_t tb = (tid == 0) ? globaltimer() : 0;
     if (lane == 0) beat(p, sm.role, HB_UNIT, ((uint64_t)j << 32) | (uint32_t)t);
-    if (kind == U_PLAN) {
-      chunk_aggregate(p, sm, stage, k, t, ntiles);
-      if (tid == 0) atomicAdd(&sm.st[S_NS_PHASE_A], (unsigned)(globaltimer() - tb));
-    } else {
-      chunk_runs(p, sm, stage, k, t, ntiles, sums_ph);
-      if (tid == 0) atomicAdd(&sm.st[S_NS_PHASE_B], (unsigned)(globaltimer() - tb));
+    if (tid == 0) TRACE_UNIT(t, kind, 1, tb);
+    if (kind == U_PLAN) plan_chunk(p, sm, stage, k, w);
+    else run_chunk(p, sm, stage, k);
+    if (tid == 0) {
+      const uint64_t te = globaltimer();
+      atomicAdd(&st[kind == U_PLAN ? S_NS_PHASE_A : S_NS_PHASE_B], (unsigned)(te - tb));
+      TRACE_UNIT(t, kind, 2, te);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.done[k]);
   }
 }
 
-// The control warp: tickets, copies, plan words and epilogues.
+// The control warp: tickets, copies, plan words and tile headers.
 __device__ __noinline__ void control_loop(const Params &p, Smem &sm, unsigned char *dyn, const CUtensorMap *tmap,
                                           int64_t ntiles) {
   const int lane = threadIdx.x & 31;
@@ -1844,14 +2211,14 @@ __device__ __noinline__ void control_loop(const Params &p, Smem &sm, unsigned ch
   uint32_t ph = 0;                                       // bit k: parity of done[k]
   auto epilogue = [&](int k) -> bool {
     const uint64_t tw = globaltimer();
-    if (lane == 0) beat(p, sm.role + 0x80u, HB_WAIT_DONE, ((uint64_t)k << 32) | (uint32_t)sm.tk[k]);
-    if (!mbar_wait(p, &sm.done[k], (ph >> k) & 1u, ERR_TMA_TIMEOUT, TO_DONE, (uint32_t)sm.tk[k],
-                   (uint32_t)(k | sm.kind[k] << 8 | blockIdx.x << 16)))
+    if (lane == 0) beat(p, sm.role + 0x80u, HB_WAIT_DONE, ((uint64_t)k << 32) | (uint32_t)sm.geo[k].t);
+    if (!mbar_wait_warp(p, &sm.done[k], (ph >> k) & 1u, ERR_TMA_TIMEOUT, TO_DONE, (uint32_t)sm.geo[k].t,
+                        (uint32_t)(k | sm.geo[k].kind << 8 | blockIdx.x << 16)))
       return false;
     ph ^= 1u << k;
     if (lane == 0) atomicAdd(&sm.st[S_NS_CTRL_WAIT], (unsigned)(globaltimer() - tw));
-    if (sm.kind[k] == U_PLAN) plan_epilogue(p, sm, k, sm.tk[k], ntiles);
-    else run_epilogue(p, sm, k, sm.tk[k], ntiles);
+    if (sm.geo[k].kind == U_RUN) run_epilogue(p, sm, k);   // a plan unit's last warp has published it
+    if (lane == 0) TRACE_UNIT(sm.geo[k].t, sm.geo[k].kind, 3, globaltimer());
     return true;
   };
   for (int j = 0;; j++) {
@@ -1864,31 +2231,34 @@ __device__ __noinline__ void control_loop(const Params &p, Smem &sm, unsigned ch
     }
     u = __shfl_sync(0xffffffffu, u, 0);
     if ((int64_t)u >= nunits) {
-      if (lane == 0) sm.kind[k] = U_END;
+      if (lane == 0) sm.geo[k].kind = U_END;
       __syncwarp();
-      if (lane < 3) mbar_arrive(&sm.full[k]);          // all three arrivals at once
+      if (lane < kCopyLanes) cp_async_mbar_arrive(&sm.full[k]);     // all the stage's arrivals at once
+      if (lane == 0) mbar_arrive(&sm.full[k]);
       for (int jj = max(j - kStages + 1, 0); jj < j; jj++)
         if (!epilogue(jj % kStages)) break;
       break;
     }
     int64_t t;
     const bool plan = unit_of((int64_t)u, ntiles, p.wave, t);
-    const TileGeo g = tile_geo(p, t, ntiles);
-    const bool tma = p.tma_rows != 0 && (g.start & 15) == 0;
-    // lanes 0 and 1 make two of the stage's three arrivals when their
-    // copies (a run unit's plan words: the tile's own sum and the prefix of
-    // the tile before; none for a plan unit) have landed
-    if (!plan) {
-      if (lane == 0) cp_async16(sm.tagg_raw[k], p.tagg + 2 * t);
-      else if (lane == 1 && t > 0) cp_async16(sm.pre_raw[k], p.status + 2 * (t - 1));
+    StageGeo g = stage_geo(p, t);
+    g.kind = plan ? U_PLAN : U_RUN;
+    if (lane == 0) {
+      sm.geo[k] = g;
+      sm.plan_cnt[k] = 0;
+      TRACE_UNIT(t, g.kind, 0, globaltimer());
+      TRACE_UNIT(t, g.kind, 4, ((unsigned long long)blockIdx.x << 32) | u);
     }
-    if (lane < 2) cp_async_mbar_arrive(&sm.full[k]);
+    // a run unit's plan words (the prefix before the tile, the tile's chunk
+    // plans); each copying lane arrives once its copy has landed
+    if (!plan && sq_ok(p, t < p.cap_tiles, 22, t)) {
+      if (lane == 0 && t > g.first_tile) cp_async16(sm.pre_raw[k], p.status + 2 * (t - 1));
+      if (lane >= 1 && lane < kCopyLanes) cp_async16(&sm.cplan_raw[k][2 * (lane - 1)], p.cplan + t * kWarps * 4 + 2 * (lane - 1));
+    }
+    if (lane < kCopyLanes) cp_async_mbar_arrive(&sm.full[k]);
     __syncwarp();
     if (lane == 0) {
-      sm.tk[k] = t;
-      sm.kind[k] = plan ? U_PLAN : U_RUN;
-      sm.tma[k] = tma ? 1 : 0;
-      if (tma) {
+      if (g.tma) {
         fence_proxy_async();                             // the compute warps' reads of this stage came first
         mbar_arrive_expect_tx(&sm.full[k], (uint32_t)kStageBytes);
         tma_load_box(dyn + k * kStageBytes, tmap, &sm.full[k], 0, (int32_t)(g.start >> 4));
@@ -1901,12 +2271,19 @@ __device__ __noinline__ void control_loop(const Params &p, Smem &sm, unsigned ch
 
 // ---------------------------------------------------------------- the kernel
 __global__ void __launch_bounds__(kBlockThreads, 2)
-    seqsum_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmap) {
+    seqsum_kernel(const __grid_constant__ Params pk, const __grid_constant__ CUtensorMap tmap) {
   extern __shared__ unsigned char dsm_raw[];
   unsigned char *dyn =
       reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
   __shared__ Smem sm;
+  // the parameters, copied to shared memory: the out-of-line functions take
+  // them by reference, and a reference into the kernel's parameter space is
+  // read through slow generic loads
+  __shared__ Params ps;
   const int tid = threadIdx.x;
+  if (tid == 0) ps = pk;
+  __syncthreads();
+  const Params &p = ps;
   const int warp = tid >> 5;
   int64_t ntiles = (p.ntiles >= 0) ? p.ntiles : (int64_t)__ldcg(&p.ctr[C_NTILES]);
   if (ntiles > p.cap_tiles) ntiles = 0;                  // the set-up flagged ERR_CAPACITY
@@ -1914,9 +2291,9 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
   if (tid < kWarps) sm.barcnt[tid] = 0;
   if (tid == 0) {
     for (int s = 0; s < kStages; s++) {
-      mbar_init(&sm.full[s], 3);                         // control lanes 0 and 1 (copies) and lane 0 (unit)
+      mbar_init(&sm.full[s], kFullArrivals);             // the copying lanes and the tile's copy
       mbar_init(&sm.done[s], kWarps);
-      mbar_init(&sm.sums[s], kWarps);
+      sm.plan_cnt[s] = 0;
     }
     fence_mbar_init();
     if (blockIdx.x == 0) p.stats[S_T_START] = globaltimer();
@@ -1952,7 +2329,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
     if (warp < kWarps && ntiles > 0) scan_prefix(p, sm, ntiles);
   } else {
     // ---------------- streaming CTA
-    if (warp < kWarps) compute_loop(p, sm, dyn, ntiles);
+    if (warp < kWarps) compute_loop(p, sm, dyn);
     else control_loop(p, sm, dyn, &tmap, ntiles);
   }
 

@@ -20,13 +20,13 @@ using sq::Rec;
 
 constexpr int64_t kStaticTiles = SEQSUM_STATIC_MAX_TERMS / sq::kTileTerms;
 static_assert(kStaticTiles * sq::kTileTerms == SEQSUM_STATIC_MAX_TERMS, "whole tiles");
-constexpr int kDbgWords = 16384;
+constexpr int kDbgWords = sq::kDbgAlloc;
 
 // the scratch: tagged plan words and tile headers (zero at the start and
 // after every tag wrap), items, counters and statistics (zero at the start;
 // the kernel leaves its counters at zero when it ends)
 static __device__ __align__(256) uint64_t s_status[kStaticTiles * 2];
-static __device__ __align__(256) uint64_t s_tagg[kStaticTiles * 2];
+static __device__ __align__(256) uint64_t s_cplan[kStaticTiles * sq::kWarps * 4];
 static __device__ __align__(256) Rec s_hdr[kStaticTiles];
 static __device__ __align__(256) Rec s_items[kStaticTiles * sq::kTileSlots];
 static __device__ __align__(256) uint32_t s_ctr[sq::C_COUNT];
@@ -37,7 +37,7 @@ static __device__ __align__(256) unsigned long long s_hb[sq::kHeartbeats];
 
 struct DeviceScratch {
   bool ready = false;
-  uint64_t *status = nullptr, *tagg = nullptr;
+  uint64_t *status = nullptr, *cplan = nullptr;
   Rec *hdr = nullptr, *items = nullptr;
   uint32_t *ctr = nullptr;
   unsigned long long *stats = nullptr, *dbg = nullptr, *hb = nullptr;
@@ -67,7 +67,7 @@ cudaError_t symbol(T **out, const void *sym) {
 cudaError_t setup(DeviceScratch &d, int dev, cudaStream_t stream) {
   cudaError_t e;
   if ((e = symbol(&d.status, s_status)) != cudaSuccess) return e;
-  if ((e = symbol(&d.tagg, s_tagg)) != cudaSuccess) return e;
+  if ((e = symbol(&d.cplan, s_cplan)) != cudaSuccess) return e;
   if ((e = symbol(&d.hdr, s_hdr)) != cudaSuccess) return e;
   if ((e = symbol(&d.items, s_items)) != cudaSuccess) return e;
   if ((e = symbol(&d.ctr, s_ctr)) != cudaSuccess) return e;
@@ -86,7 +86,7 @@ cudaError_t setup(DeviceScratch &d, int dev, cudaStream_t stream) {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   if ((e = cudaMemsetAsync(d.status, 0, sizeof s_status, stream)) != cudaSuccess) return e;
-  if ((e = cudaMemsetAsync(d.tagg, 0, sizeof s_tagg, stream)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(d.cplan, 0, sizeof s_cplan, stream)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(d.hdr, 0, sizeof s_hdr, stream)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(d.ctr, 0, sizeof s_ctr, stream)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(d.stats, 0, sizeof s_stats, stream)) != cudaSuccess) return e;
@@ -129,7 +129,7 @@ extern "C" int seqsum_f64_static(const double *x, int64_t n, double s0, double *
   // the next tag (1..127); the tagged arrays are cleared when it wraps
   if (++d.epoch > 127) {
     if (cudaMemsetAsync(d.status, 0, sizeof s_status, stream) != cudaSuccess ||
-        cudaMemsetAsync(d.tagg, 0, sizeof s_tagg, stream) != cudaSuccess ||
+        cudaMemsetAsync(d.cplan, 0, sizeof s_cplan, stream) != cudaSuccess ||
         cudaMemsetAsync(d.hdr, 0, sizeof s_hdr, stream) != cudaSuccess)
       return SEQSUM_ECUDA;
     d.epoch = 1;
@@ -145,7 +145,7 @@ extern "C" int seqsum_f64_static(const double *x, int64_t n, double s0, double *
   p.nsums = 1;
   p.epoch = d.epoch;
   p.status = d.status;
-  p.tagg = d.tagg;
+  p.cplan = d.cplan;
   p.hdr = d.hdr;
   p.items = d.items;
   p.ctr = d.ctr;
