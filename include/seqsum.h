@@ -142,6 +142,8 @@ typedef struct {
   int64_t ns_scan_wait;      /* nanoseconds: the prefix scanner waiting for tiles' sums */
   int64_t ns_verdict;        /* nanoseconds, summed: run units forming their chunks' verdicts */
   int64_t ns_verdict_wait;   /* nanoseconds, summed: run units reading plan words not copied in time */
+  int64_t ns_group_count;    /* nanoseconds, summed: control warps counting tiles in their groups */
+  int64_t ns_compose;        /* nanoseconds, summed: control warps composing groups for the walk */
   int64_t t_stream_ns;       /* latest call: kernel start to the last tile header */
   int64_t t_walk_tail_ns;    /* latest call: last tile header to the end of the walk */
   int64_t t_total_ns;        /* latest call: kernel start to the end of the walk */
@@ -183,7 +185,7 @@ int seqsum_debug_read(unsigned long long *out, int n);
 
 /* Diagnostics of a call that does not finish: copies the device counters of
  * the most recent call's workspace into out[0..16) and, per warp (index
- * CTA * 10 + warp), a heartbeat word into out[16..n) (role << 56 | what it
+ * CTA * 9 + warp: 8 compute warps, then the control warp), a heartbeat word into out[16..n) (role << 56 | what it
  * waits for or does << 48 | where).  It takes no lock and reads on a stream of its own, so it can run
  * while another thread waits on that call.  16 <= n <= 16 + 4096. */
 int seqsum_debug_heartbeat(unsigned long long *out, int n);

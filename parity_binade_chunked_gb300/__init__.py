@@ -34,7 +34,7 @@ class _Stats(ctypes.Structure):
         "runs_rejected", "terms_added", "items", "pool_overflow", "tiles_complex",
         "scan_windows", "walk_batches", "ns_tma_wait", "ns_prefix_wait", "ns_phase_a", "ns_phase_b",
         "ns_walk_wait", "ns_walk_work", "torn_header_reads", "torn_status_reads", "ns_scan", "ns_walk_count", "ns_walk_gather",
-        "ns_walk_scan", "ns_walk_serial", "ns_walk_adds", "chunks_dirty", "ns_ctrl_wait", "ns_scan_wait", "ns_verdict", "ns_verdict_wait", "t_stream_ns", "t_walk_tail_ns", "t_total_ns")] + [
+        "ns_walk_scan", "ns_walk_serial", "ns_walk_adds", "chunks_dirty", "ns_ctrl_wait", "ns_scan_wait", "ns_verdict", "ns_verdict_wait", "ns_group_count", "ns_compose", "t_stream_ns", "t_walk_tail_ns", "t_total_ns")] + [
         ("device_status", ctypes.c_int32), ("device_error_bits", ctypes.c_int32),
         ("check_site", ctypes.c_int32), ("check_pad", ctypes.c_int32), ("check_value", ctypes.c_int64),
         ("timeout_site", ctypes.c_int32), ("timeout_pad", ctypes.c_int32), ("timeout_a", ctypes.c_int64),
@@ -194,15 +194,18 @@ def debug_read(n: int = 64) -> list:
     return list(buf)
 
 
+_BLOCK_WARPS = 9   # warps per CTA: 8 compute warps and a control warp
+
+
 def debug_heartbeat(nctas: int = 320) -> dict:
     """Counters and per-warp heartbeats (cta, warp, role, what, where) of the
     most recent call, read without waiting for it (diagnostics of a call that
     does not finish)."""
-    n = 16 + min(10 * int(nctas), 4096)
+    n = 16 + min(_BLOCK_WARPS * int(nctas), 4096)
     buf = (ctypes.c_ulonglong * n)()
     _check(lib().seqsum_debug_heartbeat(buf, n))
     words = list(buf)
-    beats = [(i // 10, i % 10, w >> 56, (w >> 48) & 0xFF, w & 0xFFFFFFFFFFFF) for i, w in enumerate(words[16:]) if w]
+    beats = [(i // _BLOCK_WARPS, i % _BLOCK_WARPS, w >> 56, (w >> 48) & 0xFF, w & 0xFFFFFFFFFFFF) for i, w in enumerate(words[16:]) if w]
     return {"counters": words[:16], "beats": beats}
 
 

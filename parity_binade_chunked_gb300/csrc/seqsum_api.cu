@@ -26,6 +26,10 @@ struct Workspace {
   int64_t cap_tiles = 0, cap_sums = 0;
   uint64_t *status = nullptr;        // the plan's prefix words, 2 per tile
   uint64_t *cplan = nullptr;         // the plan's chunk sums, 4 words per chunk
+  uint32_t *grp_cnt = nullptr;       // composed groups of tiles: counters, headers, segments
+  uint64_t *grp_hdr = nullptr;
+  Rec *grp_seg = nullptr;
+  uint16_t *grp_stile = nullptr;
   Rec *hdr = nullptr;                // one header per tile
   Rec *items = nullptr;              // kTileSlots items per tile
   uint32_t *ctr = nullptr;
@@ -59,6 +63,14 @@ int cuda_fail(cudaError_t e) {
 void ws_free(Workspace *w) {
   cudaFree(w->status);
   cudaFree(w->cplan);
+  cudaFree(w->grp_cnt);
+  cudaFree(w->grp_hdr);
+  cudaFree(w->grp_seg);
+  cudaFree(w->grp_stile);
+  w->grp_cnt = nullptr;
+  w->grp_hdr = nullptr;
+  w->grp_seg = nullptr;
+  w->grp_stile = nullptr;
   cudaFree(w->hdr);
   cudaFree(w->items);
   cudaFree(w->tile_begin);
@@ -98,6 +110,10 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
     ws_free(w);
     if (cudaMalloc(&w->status, ct * 2 * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&w->cplan, ct * sq::kWarps * 4 * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMalloc(&w->grp_cnt, (ct / sq::kGroupTiles + 1) * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMalloc(&w->grp_hdr, (ct / sq::kGroupTiles + 1) * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMalloc(&w->grp_seg, (ct / sq::kGroupTiles + 1) * sq::kGroupSegs * sizeof(Rec)) != cudaSuccess ||
+        cudaMalloc(&w->grp_stile, (ct / sq::kGroupTiles + 1) * sq::kGroupSegs * sizeof(uint16_t)) != cudaSuccess ||
         cudaMalloc(&w->hdr, ct * sizeof(Rec)) != cudaSuccess ||
         cudaMalloc(&w->items, ct * sq::kTileSlots * sizeof(Rec)) != cudaSuccess ||
         cudaMalloc(&w->tile_begin, (cs + 1) * sizeof(int64_t)) != cudaSuccess) {
@@ -107,6 +123,8 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
     }
     cudaMemset(w->status, 0, ct * 2 * sizeof(uint64_t));
     cudaMemset(w->cplan, 0, ct * sq::kWarps * 4 * sizeof(uint64_t));
+    cudaMemset(w->grp_cnt, 0, (ct / sq::kGroupTiles + 1) * sizeof(uint32_t));
+    cudaMemset(w->grp_hdr, 0, (ct / sq::kGroupTiles + 1) * sizeof(uint64_t));
     cudaMemset(w->hdr, 0, ct * sizeof(Rec));
     w->cap_tiles = ct;
     w->cap_sums = cs;
@@ -152,6 +170,8 @@ void next_epoch(Workspace *w, cudaStream_t stream) {
   if (w->epoch > 127) {
     cudaMemsetAsync(w->status, 0, w->cap_tiles * 2 * sizeof(uint64_t), stream);
     cudaMemsetAsync(w->cplan, 0, w->cap_tiles * sq::kWarps * 4 * sizeof(uint64_t), stream);
+    cudaMemsetAsync(w->grp_cnt, 0, (w->cap_tiles / sq::kGroupTiles + 1) * sizeof(uint32_t), stream);
+    cudaMemsetAsync(w->grp_hdr, 0, (w->cap_tiles / sq::kGroupTiles + 1) * sizeof(uint64_t), stream);
     cudaMemsetAsync(w->hdr, 0, w->cap_tiles * sizeof(Rec), stream);
     w->epoch = 1;
   }
@@ -179,6 +199,10 @@ int64_t tensor_map(Workspace *w, const double *x, int64_t n_total) {
 void fill_ws(Params &p, Workspace *w) {
   p.status = w->status;
   p.cplan = w->cplan;
+  p.grp_cnt = w->grp_cnt;
+  p.grp_hdr = w->grp_hdr;
+  p.grp_seg = w->grp_seg;
+  p.grp_stile = w->grp_stile;
   p.hdr = w->hdr;
   p.items = w->items;
   p.ctr = w->ctr;
@@ -348,6 +372,8 @@ int seqsum_get_stats(seqsum_stats *st) {
   st->ns_scan_wait = (int64_t)s[sq::S_NS_SCAN_WAIT];
   st->ns_verdict = (int64_t)s[sq::S_NS_VERDICT];
   st->ns_verdict_wait = (int64_t)s[sq::S_NS_VERDICT_WAIT];
+  st->ns_group_count = (int64_t)s[sq::S_NS_GCOUNT];
+  st->ns_compose = (int64_t)s[sq::S_NS_COMPOSE];
   st->t_stream_ns = (int64_t)(s[sq::S_T_STREAM_END] - s[sq::S_T_START]);
   st->t_walk_tail_ns = (int64_t)(s[sq::S_T_WALK1] - s[sq::S_T_STREAM_END]);
   st->t_total_ns = (int64_t)(s[sq::S_T_WALK1] - s[sq::S_T_START]);

@@ -24,6 +24,8 @@ constexpr int kTileSlots = kWarps * kChunkSlots;
 constexpr int kWalkTiles = 1024;                // tile headers per walk batch (32 KB)
 constexpr int kWalkElems = 1024;                // flat elements per walk batch (32 KB)
 constexpr int kMaxWalkers = 8;
+constexpr int kGroupTiles = 32;                 // tiles whose records one streaming CTA composes for the walk
+constexpr int kGroupSegs = 96;                  // records and segments a composed group holds (more: the walk takes its tiles)
 constexpr int kHeartbeats = 4096;               // CTAs with a heartbeat word (diagnostics of a stuck call)
 constexpr int kDbgAlloc = 65536;                // diagnostic words: checks, walk trace, profiling timeline
 
@@ -98,6 +100,8 @@ enum : int {
   S_NS_WALK_COUNT, S_NS_WALK_GATHER, S_NS_WALK_SCAN, S_NS_WALK_SERIAL, S_NS_WALK_ADDS,
   S_NS_VERDICT,        // run units: forming the chunks' verdicts from the plan words
   S_NS_VERDICT_WAIT,   // run units: plan words read again from global memory (not copied in time)
+  S_NS_GCOUNT,         // control warps counting their tiles in the tiles' groups
+  S_NS_COMPOSE,        // control warps composing groups for the walk
   S_ACCUM_END,         // counters above are summed; below are timestamps of the latest call
   S_T_START = 40,      // block 0 started (timestamps follow the summed counters)
   S_T_WALK0 = 41,      // the walk's last batch of headers was ready
@@ -124,6 +128,10 @@ struct Params {
   // workspace
   uint64_t *status;            // 2 words per tile: tagged approximate sum, then inclusive prefix
   uint64_t *cplan;             // 4 tagged words per chunk: the plan's fixed-point sums of the chunk
+  uint32_t *grp_cnt;           // per group of kGroupTiles tiles: epoch << 24 | tiles whose header is published
+  uint64_t *grp_hdr;           // per group: tag << 56 | raw << 16 | segments
+  Rec *grp_seg;                // per group: kGroupSegs composed segments
+  uint16_t *grp_stile;         // per group segment: its first tile within the group
   Rec *hdr;                    // one header per tile
   Rec *items;                  // kTileSlots items per tile
   uint32_t *ctr;               // C_COUNT counters

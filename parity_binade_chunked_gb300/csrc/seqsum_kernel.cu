@@ -55,6 +55,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;    // bounded device waits: 2 s
 constexpr uint64_t kCountMask = (1u << kCountBits) - 1;
 static_assert(((uint64_t)kChunkSlots << (kCountBits * (kWarps - 1))) < (1ull << 55),
               "packed item counts must fit a tagged 56-bit word");
+constexpr int kWalkMinTiles = 256;             // smallest walk batch (unless the sum ends sooner)
 constexpr int kWalkOffEl = 32768;              // walker layout in the dynamic shared memory
 constexpr int kWalkOffPos = 65536;
 constexpr int kWalkOffEnds = 69632;
@@ -194,6 +195,14 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// An atomic add with acquire and release semantics at GPU scope: the writes
+// before it are visible to whoever observes its result, and the reads after
+// it see what was visible to the writers of the values it observed.
+__device__ __forceinline__ uint32_t add_acq_rel(uint32_t *a, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ uint64_t dbits(double v) { return (uint64_t)__double_as_longlong(v); }
 __device__ __forceinline__ double bitsd(uint64_t b) { return __longlong_as_double((long long)b); }
 
@@ -464,12 +473,15 @@ struct Smem {
   int nitems[kStages][kWarps];      // >0: a split chunk's items in the tile's item area
   int plan_cnt[kStages];            // chunks of a plan unit's tile planned so far
   Rec stg[kWarps][kChunkSlots];     // a split chunk's items, staged in order before they are written out
+  Rec gel[kGroupSegs];              // control warp: a group's records in order, for its composition
+  uint16_t gtile[kGroupSegs];       // ... and the tile (in the group) of each
   int role;
   uint32_t barcnt[kWarps];          // walker and scanner: wide barriers passed per warp (heartbeat)
   unsigned int st[S_COUNT];         // per-CTA statistics of one call (32-bit: native shared atomics)
   // walker
   uint64_t S;
   int m, nel, restart, nseg;
+  int64_t wpos0, wpos1;             // the walk's helper command: tiles [wpos0, wpos1)
   int walk_m[kWarps];
   int wflag[kWarps];
   Run wagg[kWarps];
@@ -655,7 +667,7 @@ __device__ __forceinline__ bool mbar_wait_warp(const Params &p, uint64_t *bar, u
 #ifdef SEQSUM_PROFILE
 // Cycle profiles (profiling builds): cycles since the previous point, summed
 // per point, and the number of times each point is passed (split chunks from
-// word 15200 on, plans from 15300).
+// word 15200 on).
 #define PROF_START long long prof_t = clock64()
 #define PROF_PT(base, id)                                                                  \
   do {                                                                                     \
@@ -671,7 +683,6 @@ __device__ __forceinline__ bool mbar_wait_warp(const Params &p, uint64_t *bar, u
 #define PROF_PT(base, id) do { } while (0)
 #endif
 #define SPLIT_PT(id) PROF_PT(15200, id)
-#define PLAN_PT(id) PROF_PT(15300, id)
 
 // The plan of chunk w of the stage's tile (by whichever compute warp claimed
 // it).  The warp that completes the tile's plan publishes the tile's
@@ -683,13 +694,11 @@ __device__ __forceinline__ void load_lane(const Params &p, const unsigned char *
 __device__ __noinline__ void plan_chunk(const Params &p, Smem &sm, const unsigned char *stage, int k, int w) {
   const int lane = threadIdx.x & 31;
   const unsigned full = 0xffffffffu;
-  PROF_START;
   const StageGeo &g = sm.geo[k];
   const int64_t lstart = g.start + (int64_t)w * kChunkTerms + (int64_t)lane * kLaneTerms;
   const int nv = (int)max((int64_t)0, min((int64_t)kLaneTerms, g.end - lstart));
   uint64_t xs[kLaneTerms];
   load_lane(p, stage, g.tma != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, xs);
-  PLAN_PT(0);                                                 // loads
   uint32_t mx = 0, orz = 0, orh = 0, andh = 0xFFFFFFFFu;
 #pragma unroll
   for (int i = 0; i < kLaneTerms; i++) {
@@ -700,28 +709,23 @@ __device__ __noinline__ void plan_chunk(const Params &p, Smem &sm, const unsigne
     if (i < nv) { orh |= hi; andh &= hi; }
   }
   const uint32_t Lm = mx >> 20;
-  PLAN_PT(1);                                                 // lane stats
   uint64_t all, neg;
   lane_fixed(xs, Lm, all, neg);
-  PLAN_PT(2);                                                 // fixed point
   const uint32_t Lc = __reduce_max_sync(full, Lm);
   const uint32_t sh = min(Lc - Lm, 63u);
   const uint64_t Pc = warp_sum36((all - neg) >> sh), Nc = warp_sum36(neg >> sh);
   const uint32_t fl = __reduce_or_sync(full, ((orh >> 31) ? WA_NEG : 0u) | ((andh >> 31) ? 0u : WA_POS) |
                                                  (orz ? WA_NZ : 0u));
   const uint32_t mxc = __reduce_max_sync(full, mx);
-  PLAN_PT(3);                                                 // warp reductions
   int last = 0;
   if (lane == 0) {
     sm.plan[k][w] = ChunkPlan{Pc, Nc, (int32_t)Lc, mxc, fl, 0u};
     __threadfence_block();
     last = atomicAdd(&sm.plan_cnt[k], 1) == kWarps - 1;
   }
-  PLAN_PT(4);                                                 // count
   if (__shfl_sync(full, last, 0)) {
     __threadfence_block();
     publish_tile_plan(p, sm, k);
-    PLAN_PT(5);                                               // publish (last warp)
   }
 }
 
@@ -1067,69 +1071,43 @@ __device__ __forceinline__ bool fast_ok(int e, uint32_t mx) {
   return e >= -969 && e <= 1023 && (int)(mx >> 20) < e + 1023;
 }
 
-// A lane's run under binade e (a cold path: rolled loops over the terms read
-// from the stage or global memory, kept small): the fast rule when no term
-// ties, else the general path.
-__device__ __noinline__ Run lane_run_any(const Params &p, bool from_stage, const unsigned char *rp,
-                                         const unsigned long long *gp, int nv, int lane, int e) {
-  uint32_t mx = 0;
-#pragma unroll 1
-  for (int i = 0; i < nv; i++) mx = max(mx, (uint32_t)(lane_term(from_stage, rp, gp, lane, i) >> 32) & 0x7FFFFFFFu);
-  if (nv > 0 && fast_ok(e, mx)) {
-    const int c = 64 - (e + 1023);
-    uint64_t P = 0, N = 0;
-    bool anytie = false;
-    uint32_t orl = 0, andl = 0xFFFFFFFFu;
-#pragma unroll 1
-    for (int i = 0; i < nv; i++) {
-      const uint64_t x = lane_term(from_stage, rp, gp, lane, i);
-      const uint32_t hi = (uint32_t)(x >> 32);
-      uint64_t ri;
-      bool tie;
-      term_inc_fast(hi, (uint32_t)x, c, ri, tie);
-      if (hi >> 31) N += ri; else P += ri;
-      anytie |= tie;
-      orl |= hi;
-      andl &= hi;
-    }
-    if (!anytie) return lane_pn_run(P, N, orl, andl, nv);
-  }
-  Run r = run_empty();
-#pragma unroll 1
-  for (int i = 0; i < nv; i++) {
-    const uint64_t x = lane_term(from_stage, rp, gp, lane, i);
-    int64_t re;
-    int32_t d;
-    const bool poison = term_inc(x, e, re, d);
-    run_push(r, re, d, term_flags(x) | (poison ? F_POISON : 0u));
-  }
-  return r;
-}
-
-// The items of dirty lane d of this warp's chunk (Research-1433, finding 4),
-// its sixteen terms spread over lanes 0..15: lane i takes term i, its exact
-// fixed-point prefix inside the lane (a scan), its prefix range (the lane's
-// starting value cl plus the prefixes before and after the term, widened by
-// dl) and so its key -- the binade the range stays in, or "carried" -- and its
-// increment for that binade.  A segmented scan composes the runs of one key;
-// each carried term becomes an item of its own, added one by one by the walk.
-// Writes the items below `room` to out (shared memory) and returns their
-// number (at most 16).  Whole warp; the arguments are warp-uniform.
+// The items of up to two dirty lanes of this warp's chunk (Research-1433,
+// finding 4), each lane's sixteen terms spread over a half-warp: lane i of a
+// half takes term i, its exact fixed-point prefix inside the dirty lane (a
+// scan), its prefix range (the dirty lane's starting value cl plus the
+// prefixes before and after the term, widened by dl) and so its key -- the
+// binade the range stays in, or "carried" -- and its increment for that
+// binade.  A segmented scan composes the runs of one key; each carried term
+// becomes an item of its own, added one by one by the walk.  The arguments
+// are those of the lane's own half (d < 0: no dirty lane for this half).
+// Items go to out[base + i] (shared memory) below kChunkSlots, where half 1's
+// base is its own base plus half 0's count.  Returns half 0's count | half
+// 1's count << 8.  Whole warp.
 constexpr int kCarryKey = -4000;
-__device__ __noinline__ int place_lane(const Params &p, const unsigned char *stage, bool from_stage, int64_t lstart,
-                                       int nv, int w, int d, DF cl, uint32_t Lm, float dl, uint64_t t, Rec *out,
-                                       int room) {
-  const int lane = threadIdx.x & 31;
+__device__ __forceinline__ Run shfl_run_up16(const Run &r, int arg) {
+  Run o;
   const unsigned full = 0xffffffffu;
-  const bool act = lane < nv;
+  o.inc = __shfl_up_sync(full, r.inc, arg, 16);
+  o.lo = __shfl_up_sync(full, r.lo, arg, 16);
+  o.hi = __shfl_up_sync(full, r.hi, arg, 16);
+  o.d = __shfl_up_sync(full, r.d, arg, 16);
+  o.flags = __shfl_up_sync(full, r.flags, arg, 16);
+  return o;
+}
+__device__ __noinline__ int place_pair(const Params &p, const unsigned char *stage, bool from_stage, int64_t lstart,
+                                       int nv, int w, int d, DF cl, uint32_t Lm, float dl, uint64_t t, Rec *out,
+                                       int base) {
+  const int lane = threadIdx.x & 31, hl = lane & 15, half = lane >> 4;
+  const unsigned full = 0xffffffffu;
+  const bool act = d >= 0 && hl < nv;
   uint64_t x = 0;
   if (act) {
     if (from_stage) {
       const unsigned char *rp = stage + (w * 32 + d) * 128;
-      const uint2 v = *reinterpret_cast<const uint2 *>(rp + ((((lane >> 1) ^ (d & 7)) << 4) | ((lane & 1) << 3)));
+      const uint2 v = *reinterpret_cast<const uint2 *>(rp + ((((hl >> 1) ^ (d & 7)) << 4) | ((hl & 1) << 3)));
       x = ((uint64_t)v.y << 32) | v.x;
     } else if (sq_ok(p, lstart >= 0 && lstart + nv <= p.n, 3, lstart)) {
-      x = __ldg(reinterpret_cast<const unsigned long long *>(p.x) + lstart + lane);
+      x = __ldg(reinterpret_cast<const unsigned long long *>(p.x) + lstart + hl);
     }
   }
   const uint32_t hi = (uint32_t)(x >> 32), lo = (uint32_t)x, E = (hi >> 20) & 0x7FFu;
@@ -1138,8 +1116,8 @@ __device__ __noinline__ int place_lane(const Params &p, const unsigned char *sta
   int64_t incl = v;
 #pragma unroll
   for (int o = 1; o < kLaneTerms; o <<= 1) {
-    const int64_t u = __shfl_up_sync(full, incl, o);
-    if (lane >= o) incl += u;
+    const int64_t u = __shfl_up_sync(full, incl, o, 16);
+    if (hl >= o) incl += u;
   }
   const float sc = pow2f((int)Lm - 1054);
   const DF a0 = df_addf(cl, __fmul_rn(f_from_i48(incl - v), sc));
@@ -1147,7 +1125,7 @@ __device__ __noinline__ int place_lane(const Params &p, const unsigned char *sta
   const bool up = v >= 0;
   int ei = 0;
   bool ok = act && one_binade_df(df_addf(up ? a0 : a1, -dl), df_addf(up ? a1 : a0, dl), ei);
-  ok = act && plan_override(p.plan_mode, ok, ei, t, w, 100 + d * 16 + lane);
+  ok = act && plan_override(p.plan_mode, ok, ei, t, w, 100 + (d < 0 ? 0 : d) * 16 + hl);
   // a term with |x| >= 2^ei, inf or NaN can never be in a run for ei
   const int xe = E ? (int)E - 1023 : -1022;
   if (E == 0x7FFu || xe >= ei) ok = false;
@@ -1160,35 +1138,36 @@ __device__ __noinline__ int place_lane(const Params &p, const unsigned char *sta
     run_push(r, re, dd, term_flags(x));
   }
   // segments: a head where the key changes; every carried term stands alone
-  const int pkey = __shfl_up_sync(full, key, 1);
-  const bool head = act && (lane == 0 || key != pkey || key == kCarryKey);
+  const int pkey = __shfl_up_sync(full, key, 1, 16);
+  const bool head = act && (hl == 0 || key != pkey || key == kCarryKey);
   Run s = r;
   int f = head ? 1 : 0;
 #pragma unroll 1
   for (int o = 1; o < kLaneTerms; o <<= 1) {
-    const Run os = shfl_run<SH_UP>(s, o);
-    const int of = __shfl_up_sync(full, f, o);
-    if (lane >= o) { if (!f) s = run_compose(os, s); f |= of; }
+    const Run os = shfl_run_up16(s, o);
+    const int of = __shfl_up_sync(full, f, o, 16);
+    if (hl >= o) { if (!f) s = run_compose(os, s); f |= of; }
   }
-  const uint32_t heads = __ballot_sync(full, head);
-  const bool end = act && (lane == nv - 1 || ((heads >> (lane + 1)) & 1u));
-  const uint32_t ends = __ballot_sync(full, end);
-  const int idx = __popc(ends & ((1u << lane) - 1u));
-  if (end && idx < room) {
+  const uint32_t heads = (__ballot_sync(full, head) >> (half * 16)) & 0xFFFFu;
+  const bool end = act && (hl == nv - 1 || ((heads >> (hl + 1)) & 1u));
+  const uint32_t ends = (__ballot_sync(full, end) >> (half * 16)) & 0xFFFFu;
+  const int cnt = __popc(ends);
+  const int cnt0 = __shfl_sync(full, cnt, 0), cnt1 = __shfl_sync(full, cnt, 16);
+  const int idx = base + (half ? cnt0 : 0) + __popc(ends & ((1u << hl) - 1u));
+  if (end && idx < kChunkSlots) {
     const uint32_t tbase = (uint32_t)(w * kChunkTerms + d * kLaneTerms);
     if (key == kCarryKey) {
       Run tr = run_empty();
       tr.inc = (int64_t)x; tr.lo = 0; tr.hi = 0; tr.d = 0;
       tr.flags = term_flags(x) & (F_HASINF_P | F_HASINF_N | F_HASNAN);
-      out[idx] = make_rec(tr, 0, K_TERMS, 1u, tbase + (uint32_t)lane);
+      out[idx] = make_rec(tr, 0, K_TERMS, 1u, tbase + (uint32_t)hl);
     } else {
-      const int hl = 31 - __clz(heads & ((2u << lane) - 1u));
-      out[idx] = make_rec(s, key, K_RUN, (uint32_t)(lane - hl + 1), tbase + (uint32_t)hl);
+      const int hlead = 31 - __clz(heads & ((2u << hl) - 1u));
+      out[idx] = make_rec(s, key, K_RUN, (uint32_t)(hl - hlead + 1), tbase + (uint32_t)hlead);
     }
   }
-  return __popc(ends);
+  return cnt0 | (cnt1 << 8);
 }
-
 
 // A chunk the plan could not place in one binade.  Each lane's starting value
 // is the chunk's plus the fixed-point sums of the earlier lanes; a lane whose
@@ -1204,29 +1183,20 @@ __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *st
   const int64_t row = (g.start >> 4) + w * 32 + lane;
   const uint64_t t = (uint64_t)g.t;
   PROF_START;
-  const bool from_stage = use_tma && row < p.tma_rows;
-  const unsigned char *rp = stage + (w * 32 + lane) * 128;
-  const unsigned long long *gp = reinterpret_cast<const unsigned long long *>(p.x) + lstart;
-  if (!from_stage && !sq_ok(p, nv == 0 || (lstart >= 0 && lstart + nv <= p.n), 3, lstart)) nv = 0;
+  uint64_t xs[kLaneTerms];
+  load_lane(p, stage, use_tma, row, lstart, nv, w, lane, xs);
   uint32_t mx = 0, orz = 0, andh = 0xFFFFFFFFu;
-#pragma unroll 1
-  for (int i = 0; i < nv; i++) {
-    const uint64_t x = lane_term(from_stage, rp, gp, lane, i);
-    const uint32_t mag = (uint32_t)(x >> 32) & 0x7FFFFFFFu;
+#pragma unroll
+  for (int i = 0; i < kLaneTerms; i++) {
+    const uint32_t hi = (uint32_t)(xs[i] >> 32);
+    const uint32_t mag = hi & 0x7FFFFFFFu;
     mx = max(mx, mag);
-    orz |= mag | (uint32_t)x;
-    andh &= (uint32_t)(x >> 32);
+    orz |= mag | (uint32_t)xs[i];
+    if (i < nv) andh &= hi;
   }
   const uint32_t Lm = mx >> 20;
-  uint64_t all = 0, neg = 0;
-#pragma unroll 1
-  for (int i = 0; i < nv; i++) {
-    const uint64_t x = lane_term(from_stage, rp, gp, lane, i);
-    const uint32_t hi = (uint32_t)(x >> 32), E = (hi >> 20) & 0x7FFu;
-    const uint32_t v = __funnelshift_rc(lead32(hi, (uint32_t)x, E), 0u, Lm - E);
-    all += v;
-    neg += (hi >> 31) ? v : 0u;
-  }
+  uint64_t all, neg;
+  lane_fixed(xs, Lm, all, neg);
   const uint32_t Lc = __reduce_max_sync(full, Lm), sh = min(Lc - Lm, 63u);
   const int64_t sv = (int64_t)((all - neg) >> sh) - (int64_t)(neg >> sh);
   // the earlier lanes' signed sum, at the chunk's scale
@@ -1247,7 +1217,17 @@ __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *st
   SPLIT_PT(0);                                                // lane sums, prefixes, verdicts
   Run r = run_empty();                                       // a lane of zeros: a run of zeros
   if (zl && !(andh >> 31)) r.flags &= ~F_ALLNEGZ;             // (all -0 only if every term is -0)
-  if (clean && !zl) r = lane_run_any(p, from_stage, rp, gp, nv, lane, e_l);
+  if (clean && !zl) {
+    bool done = false;
+    if (fast_ok(e_l, mx)) {
+      uint64_t P, N;
+      bool anytie;
+      uint32_t orl, andl;
+      lane_fast(xs, nv, 64 - (e_l + 1023), P, N, anytie, orl, andl);
+      if (!anytie) { r = lane_pn_run(P, N, orl, andl, nv); done = true; }
+    }
+    if (!done) r = lane_run_general(p, stage, use_tma, row, lstart, nv, w, lane, e_l);
+  }
   __syncwarp();
   SPLIT_PT(1);                                                // clean lanes' runs
   const int key = dirty ? kDirtyKey : (clean ? e_l : kZeroE);
@@ -1286,18 +1266,32 @@ __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *st
   const uint32_t below = (1u << lane) - 1u;
   int n = 0;
   uint32_t emitted = 0;                                // lanes whose items are staged
-  for (uint32_t m = dirtym; m; m &= m - 1) {
-    const int d = __ffs(m) - 1;
-    const uint32_t cm = cleanm & ((1u << d) - 1u) & ~emitted;
-    if (((cm >> lane) & 1u) && n + __popc(cm & below) < kChunkSlots) stg[n + __popc(cm & below)] = myrun;
-    n += __popc(cm);
-    emitted |= (2u << d) - 1u;
-    const DF cd = DF{__shfl_sync(full, cl.hi, d), __shfl_sync(full, cl.lo, d)};
-    const bool fs = use_tma && (g.start >> 4) + w * 32 + d < p.tma_rows;
-    SPLIT_PT(3);                                              // between dirty lanes
-    n += place_lane(p, stage, fs, __shfl_sync(full, lstart, d), __shfl_sync(full, nv, d), w, d, cd,
-                    __shfl_sync(full, Lm, d), dl, t, stg + min(n, kChunkSlots), max(kChunkSlots - n, 0));
-    SPLIT_PT(4);                                              // one dirty lane placed
+  // dirty lanes two at a time (one per half-warp), each pair preceded by the
+  // merged runs of the clean lanes before it
+  for (uint32_t m = dirtym; m;) {
+    const int d0 = __ffs(m) - 1;
+    m &= m - 1;
+    const int d1 = m ? __ffs(m) - 1 : -1;
+    if (m) m &= m - 1;
+    const uint32_t c0 = cleanm & ((1u << d0) - 1u) & ~emitted;
+    if (((c0 >> lane) & 1u) && n + __popc(c0 & below) < kChunkSlots) stg[n + __popc(c0 & below)] = myrun;
+    n += __popc(c0);
+    // the clean items between d0 and d1 go between their items
+    const uint32_t gapm = d1 >= 0 ? (cleanm & ((1u << d1) - 1u) & ~((2u << d0) - 1u)) : 0u;
+    const int gap = __popc(gapm);
+    const int dd = (lane >> 4) ? d1 : d0;
+    const int ds = dd < 0 ? 0 : dd;
+    const DF cd = DF{__shfl_sync(full, cl.hi, ds), __shfl_sync(full, cl.lo, ds)};
+    const int64_t ls = __shfl_sync(full, lstart, ds);
+    const int nvd = __shfl_sync(full, nv, ds);
+    const uint32_t Lmd = __shfl_sync(full, Lm, ds);
+    const bool fs = use_tma && (g.start >> 4) + w * 32 + ds < p.tma_rows;
+    const int cc = place_pair(p, stage, fs, ls, nvd, w, dd, cd, Lmd, dl, t, stg, (lane >> 4) ? n + gap : n);
+    const int cnt0 = cc & 0xFF, cnt1 = cc >> 8;
+    if (((gapm >> lane) & 1u) && n + cnt0 + __popc(gapm & below) < kChunkSlots)
+      stg[n + cnt0 + __popc(gapm & below)] = myrun;
+    n += cnt0 + gap + cnt1;
+    emitted |= (2u << (d1 >= 0 ? d1 : d0)) - 1u;
   }
   {
     const uint32_t cm = cleanm & ~emitted;
@@ -1313,8 +1307,8 @@ __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *st
       if (dirty) {
         Run fr = run_empty();
         uint32_t tf = 0;
-#pragma unroll 1
-        for (int i = 0; i < nv; i++) tf |= term_flags(lane_term(from_stage, rp, gp, lane, i));
+#pragma unroll
+        for (int i = 0; i < kLaneTerms; i++) tf |= (i < nv) ? term_flags(xs[i]) : 0u;
         fr.flags = tf & (F_HASINF_P | F_HASINF_N | F_HASNAN);
         stg[__popc(em & below)] = make_rec(fr, 0, K_FALLBACK, (uint32_t)nv, (uint32_t)(w * kChunkTerms + lane * kLaneTerms));
       } else {
@@ -1464,7 +1458,8 @@ __device__ __noinline__ void run_chunk(const Params &p, Smem &sm, const unsigned
 // Control warp, after a tile's runs: the tile's header -- one run when every
 // chunk is a run of one binade (runs of zeros fit any), else the chunks'
 // items in the tile's item area.
-__device__ __noinline__ void run_epilogue(const Params &p, Smem &sm, int k) {
+__device__ __noinline__ void group_done(const Params &p, Smem &sm, int64_t t, int64_t ntiles);
+__device__ __noinline__ void run_epilogue(const Params &p, Smem &sm, int k, int64_t ntiles) {
   const int lane = threadIdx.x & 31;
   unsigned int *st = sm.st;
   const StageGeo &g = sm.geo[k];
@@ -1520,6 +1515,9 @@ __device__ __noinline__ void run_epilogue(const Params &p, Smem &sm, int k) {
     atomicMax(&p.stats[S_T_STREAM_END], (unsigned long long)globaltimer());
     atomicAdd(&st[S_TILES], 1u);
   }
+  __syncwarp();
+  if (lane == 0) TRACE_UNIT(t, 1, 6, globaltimer());
+  group_done(p, sm, t, ntiles);
 }
 
 // ---------------------------------------------------------------- the walk
@@ -1571,8 +1569,12 @@ __device__ __forceinline__ void walk_trace(const Params &p, int64_t a, int64_t b
   }
 }
 #define WALK_TRACE(a, b, what, Sb) do { if (lane == 0) walk_trace(p, (a), (b), (what), (Sb)); } while (0)
+// a whole batch of uniform tiles [pos, pos + m) applied as one composite
+#define WALK_TRACE_T0(p, pos, m, Sb)                                                                  \
+  walk_trace((p), tile_geo((p), (pos), ntiles).start, tile_geo((p), (pos) + (m) - 1, ntiles).end, 7u, (Sb))
 #else
 #define WALK_TRACE(a, b, what, Sb) do { } while (0)
+#define WALK_TRACE_T0(p, pos, m, Sb) do { } while (0)
 #endif
 __device__ __forceinline__ int elem_key(const Rec &q) {
   return (rec_flags(q.meta) & F_ZERO) ? kZeroE : (int)q.e;
@@ -1658,8 +1660,8 @@ __device__ __noinline__ int resolve_rejection(const Params &p, const Rec *el, co
 //   [32K, 64K)     the batch's elements in order
 //   [64K, 68K)     per element: its tile in the batch << 12 | its first term
 //   [68K, 72K)     segment ends
-__device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *dyn, int k, int64_t tb, int64_t te,
-                                      int64_t ntiles) {
+__device__ __noinline__ void walk_batch(const Params &p, Smem &sm, unsigned char *dyn, int k, int64_t tb,
+                                        int64_t te, int64_t ntiles) {
   constexpr int PT = kWalkTiles / kThreads;         // tiles, then elements, per thread
   static_assert(kWalkTiles == kThreads * PT && kWalkElems == kThreads * PT, "walk batch shape");
   Rec *hdrs = reinterpret_cast<Rec *>(dyn);
@@ -1671,7 +1673,6 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
   const unsigned full = 0xffffffffu;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t tag = (p.epoch << 1) | 1u;
-  if (tid == 0) sm.S = dbits(p.s0s ? p.s0s[k] : p.s0);
   int64_t pos = tb;
   uint64_t t_work0 = 0;
   int nbatch = 0;
@@ -1731,10 +1732,10 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       m = want;
 #pragma unroll
       for (int w2 = 0; w2 < kWarps; w2++) m = min(m, sm.walk_m[w2]);
-      // a batch costs about the same whatever its size (its steps are
-      // latency-bound), so the walk takes full batches: 1024 tiles, or the
-      // rest of the sum
-      if (m == want) break;
+      // a batch has a fixed cost of a few microseconds, so the walk takes at
+      // least kWalkMinTiles ready tiles (or the rest of the sum); early
+      // batches overlap with the stream
+      if (m >= min(want, kWalkMinTiles)) break;
       // not all ready yet; thread 0 alone decides whether to give up
       if (tid == 0) sm.restart = (globaltimer() - t0 > kWaitNs) ? 1 : 0;
       wide_sync(p, sm, 8);
@@ -1766,6 +1767,64 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       TRACE_BATCH(nbatch, 2, ((unsigned long long)m << 32) | (uint64_t)pos);
       atomicAdd(&st[S_NS_WALK_WAIT], (unsigned)(t_work0 - t0));
       if (pos + m >= te) p.stats[S_T_WALK0] = t_work0;
+    }
+    // ---- the common case: every header of the batch is a run of one binade
+    //      (or every one a run of zeros); they compose in order, by a tree
+    //      over the threads, and the walk applies the one composite.  If its
+    //      check refuses it, the batch takes the general path below.
+    {
+      int k0 = kZeroE - 1;                             // "not uniform" unless header 0 is a run
+      if (rec_kind(hdrs[0].meta) == K_RUN) k0 = elem_key(hdrs[0]);
+      bool uni = k0 != kZeroE - 1;
+      Run r = run_empty();
+#pragma unroll
+      for (int q = 0; q < PT; q++) {
+        const int i = PT * tid + q;
+        if (i < m) {
+          const Rec h = hdrs[i];
+          uni = uni && rec_kind(h.meta) == K_RUN && elem_key(h) == k0;
+          r = run_compose(r, rec_run(h));
+        }
+      }
+#pragma unroll 1
+      for (int off = 1; off < 32; off <<= 1) {
+        const Run o = shfl_run<SH_DOWN>(r, off);
+        if ((lane & (2 * off - 1)) == 0) r = run_compose(r, o);
+      }
+      const bool wuni = __all_sync(full, uni);
+      if (lane == 0) { sm.wagg[warp] = r; sm.wflag[warp] = wuni ? 1 : 0; }
+      wide_sync(p, sm, 26);
+      if (tid == 0) {
+        bool all = true;
+        Run c = run_empty();
+        for (int w2 = 0; w2 < kWarps; w2++) {
+          all = all && sm.wflag[w2] != 0;
+          c = run_compose(c, sm.wagg[w2]);
+        }
+        sm.restart = 0;
+        if (all) {
+          uint64_t Sb = sm.S;
+          if (nonfinite(Sb)) {
+            sm.S = absorb(Sb, c.flags);
+            sm.restart = 1;
+          } else if (run_apply(Sb, c, k0) == APPLY_OK) {
+            sm.S = Sb;
+            sm.restart = 1;
+          }
+          if (sm.restart) {
+            atomicAdd(&st[S_WALK_SEGMENTS], 1u);
+            WALK_TRACE_T0(p, pos, m, sm.S);
+          }
+        }
+      }
+      wide_sync(p, sm, 27);
+      if (sm.restart) {
+        pos += m;
+        if (tid == 0) { TRACE_BATCH(nbatch, 1, globaltimer()); TRACE_BATCH(nbatch, 3, (unsigned long long)m); }
+        nbatch++;
+        wide_sync(p, sm, 28);                          // sm.restart and the batch buffers may be reused
+        continue;
+      }
     }
     // ---- B. elements per tile and their offsets; a batch whose elements do
     //         not fit is cut before the first tile that overflows
@@ -2091,13 +2150,332 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
     wide_sync(p, sm, 19);
     WALK_PT(15);
   }
-  if (tid == 0) {
-    p.outs[k] = bitsd(sm.S);
+  (void)t_work0;
+  wide_sync(p, sm, 21);
+}
+
+// ---------------------------------------------------------------- composed groups
+// Groups of kGroupTiles consecutive tiles.  The streaming CTA that publishes
+// the last header of a group composes the group for the walk (Research-1433,
+// open question "compose runs of chunks that share a binade so that the walk
+// steps over 64 or 1024 chunks at a time"): the group's records are listed in
+// order (simple tile headers, the items of complex tiles), every maximal
+// stretch of runs of one binade is composed into one segment, and the walk
+// then only applies the segments.  A group with more than kGroupSegs records
+// is published "raw": the walk takes its tiles one by one.
+
+// The group's records composed into segments (control warp).  Every header of
+// the group is published.
+__device__ __noinline__ void compose_group(const Params &p, Smem &sm, int64_t g, int nt, int64_t ntiles) {
+  const int lane = threadIdx.x & 31;
+  const unsigned full = 0xffffffffu;
+  const uint32_t tag = (p.epoch << 1) | 1u;
+  const int64_t t0 = g * kGroupTiles;
+  Rec h;
+  int cnt = 0;
+  bool okh = true, first = false;
+  if (lane < nt) {
+    okh = read_header(p.hdr + t0 + lane, tag, h) == 1;
+    if (okh) {
+      if (rec_kind(h.meta) == K_COMPLEX) {
+        const uint64_t packed = (uint64_t)h.inc;
+#pragma unroll
+        for (int cc = 0; cc < kWarps; cc++) cnt += (int)((packed >> (kCountBits * cc)) & kCountMask);
+      } else {
+        cnt = 1;
+      }
+    }
+    // a tile that starts a sum starts a segment (batched calls)
+    first = (p.offsets == nullptr) ? (t0 + lane == 0) : (tile_geo(p, t0 + lane, ntiles).first_tile == t0 + lane);
+  }
+  int off = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(full, off, o);
+    if (lane >= o) off += v;
+  }
+  const int E = __shfl_sync(full, off, 31);
+  off -= cnt;
+  const bool raw = !__all_sync(full, okh) || E > kGroupSegs;
+  if (!raw) {
+    // simple tiles: their header; complex tiles: their items, loaded by the
+    // whole warp at once (lane j the tile's item j, in chunk order)
+    const bool cplx = lane < nt && rec_kind(h.meta) == K_COMPLEX;
+    if (lane < nt && !cplx) {
+      sm.gel[off] = h;
+      sm.gtile[off] = (uint16_t)(lane | (first ? 0x100 : 0));   // 0x100: the record starts a sum
+    }
+    for (uint32_t m = __ballot_sync(full, cplx); m; m &= m - 1) {
+      const int c = __ffs(m) - 1;
+      const uint64_t packed = (uint64_t)__shfl_sync(full, h.inc, c);
+      const int base = __shfl_sync(full, off, c), n = __shfl_sync(full, cnt, c);
+      const bool fc = __shfl_sync(full, first, c);
+      const Rec *src = p.items + (t0 + c) * kTileSlots;
+      for (int j = lane; j < n; j += 32) {
+        // item j of the tile: the chunk whose running count passes j
+        int cc = 0, before = 0;
+        for (; cc < kWarps; cc++) {
+          const int nc = (int)((packed >> (kCountBits * cc)) & kCountMask);
+          if (j < before + nc) break;
+          before += nc;
+        }
+        Rec it = make_rec(run_empty(), kZeroE, K_RUN, 0, 0);
+        const Rec *q = src + cc * kChunkSlots + (j - before);
+        if (cc < kWarps && item_ok(p, q, 23)) it = ldcg_rec(q);
+        sm.gel[base + j] = it;
+        sm.gtile[base + j] = (uint16_t)(c | ((fc && j == 0) ? 0x100 : 0));
+      }
+    }
+  }
+  __syncwarp();
+  int nseg = 0;
+  if (!raw) {
+    // rounds of 32 records: a segmented scan of the runs, carried over
+    Run carry = run_empty();
+    bool carry_open = false;
+    int key_prev = 0;
+    bool alone_prev = true;
+    for (int rnd = 0; rnd * 32 < E; rnd++) {
+      const int j = rnd * 32 + lane;
+      const bool valid = j < E;
+      Rec x = make_rec(run_empty(), kZeroE, K_RUN, 0, 0);
+      if (valid) x = sm.gel[j];
+      const int key = elem_key(x);
+      const bool alone = elem_alone(x);
+      int kp = __shfl_up_sync(full, key, 1);
+      bool ap = __shfl_up_sync(full, alone, 1);
+      if (lane == 0) { kp = key_prev; ap = alone_prev; }
+      const bool head = valid && (j == 0 || alone || ap || key != kp || (sm.gtile[j] & 0x100));
+      Run v = rec_run(x);
+      int f = head ? 1 : 0;
+#pragma unroll 1
+      for (int o = 1; o < 32; o <<= 1) {
+        const Run ov = shfl_run<SH_UP>(v, o);
+        const int of = __shfl_up_sync(full, f, o);
+        if (lane >= o) { if (!f) v = run_compose(ov, v); f |= of; }
+      }
+      // the open segment of the previous round continues into this one's lanes before the first head
+      if (!f && valid && carry_open) v = run_compose(carry, v);
+      const uint32_t heads = __ballot_sync(full, head);
+      // an end: the last record, or one followed by a head (for the round's
+      // last lane, the next round's first record decides)
+      bool nexthead = (heads >> (lane + 1)) & 1u;
+      if (lane == 31 && valid && j < E - 1) {
+        const Rec xn = sm.gel[j + 1];
+        nexthead = elem_alone(xn) || alone || elem_key(xn) != key || (sm.gtile[j + 1] & 0x100);
+      }
+      const bool end = valid && (j == E - 1 || nexthead);
+      const uint32_t ends = __ballot_sync(full, end);
+      const int s = nseg + __popc(ends & ((1u << lane) - 1u));
+      if (end && s < kGroupSegs) {
+        stcg_rec(p.grp_seg + g * kGroupSegs + s, alone ? x : make_rec(v, key, K_RUN, 0u, 0u));
+        p.grp_stile[g * kGroupSegs + s] = sm.gtile[j] & 0xFFu;
+      }
+      nseg += __popc(ends);
+      // carry the open segment (the last lane's composite when it did not end)
+      const bool open31 = __shfl_sync(full, valid && !end, 31);
+      const Run v31 = shfl_run<SH_IDX>(v, 31);
+      carry = v31;
+      carry_open = open31;
+      key_prev = __shfl_sync(full, key, 31);
+      alone_prev = __shfl_sync(full, alone, 31);
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();                                   // the segments before the group's header
+    const uint64_t hw = ((uint64_t)tag << 56) | ((uint64_t)(raw ? 1u : 0u) << 16) | (uint64_t)(raw ? 0 : nseg);
+    *reinterpret_cast<volatile uint64_t *>(p.grp_hdr + g) = hw;
+  }
+}
+
+// After tile t's header is published (control warp): count the tile in its
+// group; the CTA that completes the group composes it.
+__device__ __noinline__ void group_done(const Params &p, Smem &sm, int64_t t, int64_t ntiles) {
+  const int lane = threadIdx.x & 31;
+  const int64_t g = t / kGroupTiles;
+  const int nt = (int)min((int64_t)kGroupTiles, ntiles - g * kGroupTiles);
+  int last = 0;
+  const uint64_t tc = globaltimer();
+  if (lane == 0) {
+    // release: this tile's header (and items) before its count; acquire:
+    // the other tiles' headers after their counts, for the composer.  The
+    // composer puts the counter back to 0 for the next call.
+    last = (int)add_acq_rel(p.grp_cnt + g, 1u) + 1 == nt;
+    atomicAdd(&sm.st[S_NS_GCOUNT], (unsigned)(globaltimer() - tc));
+  }
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  const uint64_t t1 = globaltimer();
+  if (lane == 0) p.grp_cnt[g] = 0u;                   // every tile of the group has counted
+  compose_group(p, sm, g, nt, ntiles);
+  if (lane == 0) atomicAdd(&sm.st[S_NS_COMPOSE], (unsigned)(globaltimer() - t1));
+}
+
+// Warp 0 of the walk: apply the staged segments of one group whose tile lies
+// in [lo, hi) (tile offsets in the group) to the exact running sum Sb, in
+// order.  False when the exact check refuses one: Sb is then unchanged and
+// the walk takes the group's tiles one by one.  Counts segments and terms.
+__device__ __forceinline__ bool apply_segments(const Params &p, uint64_t &Sb0, const Rec *seg, const uint16_t *stile,
+                                               int nseg, int64_t g0, int lo, int hi, int64_t ntiles, unsigned int *st,
+                                               unsigned &napplied, unsigned &nterms) {
+  const int lane = threadIdx.x & 31;
+  uint64_t Sb = Sb0;
+  unsigned na = 0, nt = 0;
+  for (int s = 0; s < nseg; s++) {
+    const int ti = stile[s];
+    if (ti < lo || ti >= hi) continue;
+    const Rec c = seg[s];
+    const uint32_t kind = rec_kind(c.meta);
+    na++;
+    if (nonfinite(Sb)) { Sb = absorb(Sb, rec_flags(c.meta)); continue; }
+    if (kind == K_RUN) {
+      uint64_t T = Sb;
+      if (run_apply(T, rec_run(c), c.e) != APPLY_OK) return false;
+      Sb = T;
+    } else if (kind == K_TERMS) {
+      double S = bitsd(Sb);
+      const int n = (int)c.count;
+      if (n > 0) S = __dadd_rn(S, bitsd((uint64_t)c.inc));
+      if (n > 1) S = __dadd_rn(S, bitsd((uint64_t)c.lo));
+      if (n > 2) S = __dadd_rn(S, bitsd((uint64_t)c.hi));
+      Sb = dbits(S);
+      nt += (unsigned)n;
+    } else {                                            // K_FALLBACK
+      const TileGeo tg = tile_geo(p, g0 + ti, ntiles);
+      Sb = add_terms(p, Sb, tg.start + rec_tstart(c.meta), c.count, st);
+      if (lane == 0) atomicAdd(&st[S_CHUNK_FALLBACK], 1u);
+    }
+  }
+  Sb0 = Sb;
+  napplied += na;
+  nterms += nt;
+  return true;
+}
+
+// Walk sum k over its tiles [tb, te) group by group, as the groups are
+// composed.  Warp 0 reads ahead the headers of up to 32 groups, stages their
+// segments in shared memory and applies them in order; the other warps wait
+// at a barrier and join only to walk the tiles of a group that is raw or
+// whose segments the check refuses (walk_batch).
+constexpr int kWalkStageSegs = 512;                   // staged segments (after the batch buffers)
+constexpr int kWalkOffStage = 73728;
+static_assert(kWalkOffStage + kWalkStageSegs * ((int)sizeof(Rec) + 2) <= kStages * kStageBytes, "walk staging");
+__device__ __noinline__ void walk_batch(const Params &p, Smem &sm, unsigned char *dyn, int k, int64_t tb,
+                                        int64_t te, int64_t ntiles);
+__device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *dyn, int k, int64_t tb, int64_t te,
+                                      int64_t ntiles) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned full = 0xffffffffu;
+  const uint32_t tag = (p.epoch << 1) | 1u;
+  unsigned int *st = sm.st;
+  Rec *seg = reinterpret_cast<Rec *>(dyn + kWalkOffStage);
+  uint16_t *stile = reinterpret_cast<uint16_t *>(dyn + kWalkOffStage + kWalkStageSegs * sizeof(Rec));
+  if (tid == 0) sm.S = dbits(p.s0s ? p.s0s[k] : p.s0);
+  wide_sync(p, sm, 6);
+  if (warp != 0) {
+    // the helpers: a command from warp 0 (a range of tiles to walk), or the end
+    while (true) {
+      wide_sync(p, sm, 32);
+      const int cmd = sm.nseg;
+      const int64_t a = sm.wpos0, b = sm.wpos1;
+      wide_sync(p, sm, 33);
+      if (cmd == 0) break;
+      walk_batch(p, sm, dyn, k, a, b, ntiles);
+    }
+    return;
+  }
+  uint64_t twait = 0;
+  const uint64_t tbeg = globaltimer();
+  const int64_t gend = (te - 1) / kGroupTiles + 1;
+  uint64_t Sb = sm.S;                                  // the exact running sum (every lane of warp 0)
+  unsigned napplied = 0, nterms = 0;
+  int nround = 0;
+  (void)nround;
+  bool failed = false;
+  for (int64_t g = tb / kGroupTiles; g < gend && !failed;) {
+    // the ready groups g .. g + r - 1 (bounded wait for group g)
+    const uint64_t t0 = globaltimer();
+    if (lane == 0) beat(p, sm.role, HB_WAIT_HEADERS, (uint64_t)(g * kGroupTiles));
+    uint32_t nap = 32;
+    uint64_t hw = 0;
+    int r = 0;
+    while (true) {
+      const int64_t gi = g + lane;
+      hw = gi < gend ? *reinterpret_cast<const volatile uint64_t *>(p.grp_hdr + gi) : 0ull;
+      const uint32_t rm = __ballot_sync(full, gi < gend && (uint32_t)(hw >> 56) == tag);
+      r = (~rm == 0u) ? 32 : __ffs(~rm) - 1;
+      if (r > 0) break;
+      if (__any_sync(full, globaltimer() - t0 > kWaitNs)) {
+        if (lane == 0) note_timeout(p, ERR_WALK_TIMEOUT, TO_WALK, (uint32_t)(g * kGroupTiles), (uint32_t)te);
+        failed = true;
+        break;
+      }
+      __nanosleep(nap);
+      nap = min(nap * 2u, 256u);
+    }
+    twait += globaltimer() - t0;
+    if (failed) break;
+    // stage the segments of the ready groups that fit
+    const bool mine = lane < r;
+    const int raw = mine ? (int)((hw >> 16) & 1u) : 0;
+    const int ns = (mine && !raw) ? (int)(hw & 0xFFFFu) : 0;
+    int off = ns;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(full, off, o);
+      if (lane >= o) off += v;
+    }
+    off -= ns;
+    const uint32_t fits = __ballot_sync(full, mine && off + ns <= kWalkStageSegs);
+    r = (~fits == 0u) ? 32 : __ffs(~fits) - 1;        // at least group g fits (at most kGroupSegs)
+    if (lane < r) {
+      const int64_t gi = g + lane;
+      for (int s2 = 0; s2 < ns; s2++) {
+        seg[off + s2] = ldcg_rec(p.grp_seg + gi * kGroupSegs + s2);
+        stile[off + s2] = p.grp_stile[gi * kGroupSegs + s2];
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      TRACE_BATCH(256 + nround, 0, globaltimer());
+      TRACE_BATCH(256 + nround, 2, ((unsigned long long)r << 32) | (uint64_t)g);
+    }
+    // apply them group by group, in order
+    for (int i = 0; i < r; i++) {
+      const int64_t gi = g + i, g0 = gi * kGroupTiles;
+      const int lo = (int)(max(g0, tb) - g0), hi = (int)(min(g0 + kGroupTiles, te) - g0);
+      const int rawi = __shfl_sync(full, raw, i), nsi = __shfl_sync(full, ns, i), offi = __shfl_sync(full, off, i);
+      const bool ok = !rawi && apply_segments(p, Sb, seg + offi, stile + offi, nsi, g0, lo, hi, ntiles, st, napplied, nterms);
+      if (!ok) {
+        // the whole CTA walks the group's tiles from the sum so far
+        if (lane == 0) { sm.S = Sb; sm.nseg = 1; sm.wpos0 = g0 + lo; sm.wpos1 = g0 + hi; }
+        if (lane == 0 && !rawi) atomicAdd(&st[S_RUN_REJECTED], 1u);
+        wide_sync(p, sm, 32);
+        wide_sync(p, sm, 33);
+        walk_batch(p, sm, dyn, k, g0 + lo, g0 + hi, ntiles);
+        Sb = sm.S;
+      }
+    }
+    if (lane == 0) TRACE_BATCH(256 + nround, 1, globaltimer());
+    nround++;
+    g += r;
+  }
+  // release the helpers
+  if (lane == 0) {
+    sm.nseg = 0;
+    sm.S = Sb;
+    atomicAdd(&st[S_WALK_SEGMENTS], napplied);
+    if (nterms) atomicAdd(&st[S_TERMS_ADDED], nterms);
+  }
+  wide_sync(p, sm, 32);
+  wide_sync(p, sm, 33);
+  if (lane == 0) {
+    p.outs[k] = failed ? __longlong_as_double(0x7FF8000000000000ll) : bitsd(Sb);
     const uint64_t tend = globaltimer();
     p.stats[S_T_WALK1] = tend;
-    if (t_work0 != 0) atomicAdd(&st[S_NS_WALK_WORK], (unsigned)(tend - t_work0));
+    atomicAdd(&st[S_NS_WALK_WAIT], (unsigned)twait);
+    atomicAdd(&st[S_NS_WALK_WORK], (unsigned)(tend - tbeg - twait));
   }
-  wide_sync(p, sm, 20);
 }
 
 // ---------------------------------------------------------------- the streaming loops
@@ -2216,8 +2594,11 @@ __device__ __noinline__ void control_loop(const Params &p, Smem &sm, unsigned ch
                         (uint32_t)(k | sm.geo[k].kind << 8 | blockIdx.x << 16)))
       return false;
     ph ^= 1u << k;
-    if (lane == 0) atomicAdd(&sm.st[S_NS_CTRL_WAIT], (unsigned)(globaltimer() - tw));
-    if (sm.geo[k].kind == U_RUN) run_epilogue(p, sm, k);   // a plan unit's last warp has published it
+    if (lane == 0) {
+      atomicAdd(&sm.st[S_NS_CTRL_WAIT], (unsigned)(globaltimer() - tw));
+      TRACE_UNIT(sm.geo[k].t, sm.geo[k].kind, 5, globaltimer());
+    }
+    if (sm.geo[k].kind == U_RUN) run_epilogue(p, sm, k, ntiles);   // a plan unit's last warp has published it
     if (lane == 0) TRACE_UNIT(sm.geo[k].t, sm.geo[k].kind, 3, globaltimer());
     return true;
   };
@@ -2340,6 +2721,9 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
   if (tid == 0) {
     __threadfence();
     if (atomicAdd(&p.ctr[C_EXIT], 1u) + 1 == gridDim.x) {
+      // a call that failed may have left group counters short of complete
+      if (__ldcg(&p.ctr[C_ERR]) != 0u)
+        for (int64_t g = 0; g <= ntiles / kGroupTiles; g++) p.grp_cnt[g] = 0u;
       p.ctr[C_TICKET] = 0;
       p.ctr[C_SUMTICKET] = 0;
       p.ctr[C_ROLE] = 0;

@@ -27,6 +27,11 @@ constexpr int kDbgWords = sq::kDbgAlloc;
 // the kernel leaves its counters at zero when it ends)
 static __device__ __align__(256) uint64_t s_status[kStaticTiles * 2];
 static __device__ __align__(256) uint64_t s_cplan[kStaticTiles * sq::kWarps * 4];
+constexpr int64_t kStaticGroups = kStaticTiles / sq::kGroupTiles + 1;
+static __device__ __align__(256) uint32_t s_grp_cnt[kStaticGroups];
+static __device__ __align__(256) uint64_t s_grp_hdr[kStaticGroups];
+static __device__ __align__(256) Rec s_grp_seg[kStaticGroups * sq::kGroupSegs];
+static __device__ __align__(256) uint16_t s_grp_stile[kStaticGroups * sq::kGroupSegs];
 static __device__ __align__(256) Rec s_hdr[kStaticTiles];
 static __device__ __align__(256) Rec s_items[kStaticTiles * sq::kTileSlots];
 static __device__ __align__(256) uint32_t s_ctr[sq::C_COUNT];
@@ -37,7 +42,10 @@ static __device__ __align__(256) unsigned long long s_hb[sq::kHeartbeats];
 
 struct DeviceScratch {
   bool ready = false;
-  uint64_t *status = nullptr, *cplan = nullptr;
+  uint64_t *status = nullptr, *cplan = nullptr, *grp_hdr = nullptr;
+  uint32_t *grp_cnt = nullptr;
+  Rec *grp_seg = nullptr;
+  uint16_t *grp_stile = nullptr;
   Rec *hdr = nullptr, *items = nullptr;
   uint32_t *ctr = nullptr;
   unsigned long long *stats = nullptr, *dbg = nullptr, *hb = nullptr;
@@ -68,6 +76,10 @@ cudaError_t setup(DeviceScratch &d, int dev, cudaStream_t stream) {
   cudaError_t e;
   if ((e = symbol(&d.status, s_status)) != cudaSuccess) return e;
   if ((e = symbol(&d.cplan, s_cplan)) != cudaSuccess) return e;
+  if ((e = symbol(&d.grp_cnt, s_grp_cnt)) != cudaSuccess) return e;
+  if ((e = symbol(&d.grp_hdr, s_grp_hdr)) != cudaSuccess) return e;
+  if ((e = symbol(&d.grp_seg, s_grp_seg)) != cudaSuccess) return e;
+  if ((e = symbol(&d.grp_stile, s_grp_stile)) != cudaSuccess) return e;
   if ((e = symbol(&d.hdr, s_hdr)) != cudaSuccess) return e;
   if ((e = symbol(&d.items, s_items)) != cudaSuccess) return e;
   if ((e = symbol(&d.ctr, s_ctr)) != cudaSuccess) return e;
@@ -87,6 +99,8 @@ cudaError_t setup(DeviceScratch &d, int dev, cudaStream_t stream) {
   }
   if ((e = cudaMemsetAsync(d.status, 0, sizeof s_status, stream)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(d.cplan, 0, sizeof s_cplan, stream)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(d.grp_cnt, 0, sizeof s_grp_cnt, stream)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(d.grp_hdr, 0, sizeof s_grp_hdr, stream)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(d.hdr, 0, sizeof s_hdr, stream)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(d.ctr, 0, sizeof s_ctr, stream)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(d.stats, 0, sizeof s_stats, stream)) != cudaSuccess) return e;
@@ -130,6 +144,8 @@ extern "C" int seqsum_f64_static(const double *x, int64_t n, double s0, double *
   if (++d.epoch > 127) {
     if (cudaMemsetAsync(d.status, 0, sizeof s_status, stream) != cudaSuccess ||
         cudaMemsetAsync(d.cplan, 0, sizeof s_cplan, stream) != cudaSuccess ||
+        cudaMemsetAsync(d.grp_cnt, 0, sizeof s_grp_cnt, stream) != cudaSuccess ||
+        cudaMemsetAsync(d.grp_hdr, 0, sizeof s_grp_hdr, stream) != cudaSuccess ||
         cudaMemsetAsync(d.hdr, 0, sizeof s_hdr, stream) != cudaSuccess)
       return SEQSUM_ECUDA;
     d.epoch = 1;
@@ -146,6 +162,10 @@ extern "C" int seqsum_f64_static(const double *x, int64_t n, double s0, double *
   p.epoch = d.epoch;
   p.status = d.status;
   p.cplan = d.cplan;
+  p.grp_cnt = d.grp_cnt;
+  p.grp_hdr = d.grp_hdr;
+  p.grp_seg = d.grp_seg;
+  p.grp_stile = d.grp_stile;
   p.hdr = d.hdr;
   p.items = d.items;
   p.ctr = d.ctr;
