@@ -71,6 +71,7 @@ enum : int {
   C_TO_SITE = 11,    // first bounded wait that gave up: its site and two words of context
   C_TO_A = 12,
   C_TO_B = 13,
+  C_WALK_SM = 14,    // 1 + the SM of walker 0 and 1: a streaming CTA on one of them stops early
   C_COUNT = 16
 };
 enum : uint32_t {

@@ -70,6 +70,11 @@ static_assert(kWalkElems % kThreads == 0 && kWalkTiles % kThreads == 0, "walk ba
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
+__device__ __forceinline__ uint32_t smid() {
+  uint32_t v;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(v));
+  return v;
+}
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -240,7 +245,14 @@ __device__ __forceinline__ void trace_word(const Params &p, int base, int limit,
 }
 #define TRACE_UNIT(t, kind, field, v) trace_word(p, kTraceUnits, kTraceBatches, 2 * (t) + (kind), 8, (field), (v))
 #define TRACE_BATCH(b, field, v) trace_word(p, kTraceBatches, kDbgAlloc, (b), 4, (field), (v))
+// the largest value offered (the slowest chunk of a unit)
+#define TRACE_UNIT_MAX(t, kind, field, v)                                                      \
+  do {                                                                                       \
+    const int64_t i_ = kTraceUnits + (2 * (t) + (kind)) * 8 + (field);                       \
+    if (i_ < kTraceBatches) atomicMax(&p.dbg[i_], (unsigned long long)(v));                  \
+  } while (0)
 #else
+#define TRACE_UNIT_MAX(t, kind, field, v) do { } while (0)
 #define TRACE_UNIT(t, kind, field, v) do { } while (0)
 #define TRACE_BATCH(b, field, v) do { } while (0)
 #endif
@@ -472,6 +484,9 @@ struct Smem {
   Rec chunk[kStages][kWarps];       // a run unit's chunk records
   int nitems[kStages][kWarps];      // >0: a split chunk's items in the tile's item area
   int plan_cnt[kStages];            // chunks of a plan unit's tile planned so far
+  // per stage the claim word of its unit: use << 8 | chunks claimed (the
+  // use counts the units the stage has held; bit 7 marks the end marker)
+  uint32_t cnext[kStages];
   Rec stg[kWarps][kChunkSlots];     // a split chunk's items, staged in order before they are written out
   Rec gel[kGroupSegs];              // control warp: a group's records in order, for its composition
   uint16_t gtile[kGroupSegs];       // ... and the tile (in the group) of each
@@ -1329,8 +1344,8 @@ __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *st
 // plan words, then the exact run (or items) of chunk w (Research-1433, finding 2 "Inside a binade the loop is an integer
 // sum", finding 3 "Ties need the parity of the running integer"); the chunk's
 // record goes to sm.chunk[k][w] for the control warp's header.
-__device__ __noinline__ void run_chunk(const Params &p, Smem &sm, const unsigned char *stage, int k) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+__device__ __noinline__ void run_chunk(const Params &p, Smem &sm, const unsigned char *stage, int k, int w) {
+  const int lane = threadIdx.x & 31;
   const unsigned full = 0xffffffffu;
   unsigned int *st = sm.st;
   const StageGeo &g = sm.geo[k];
@@ -1433,7 +1448,7 @@ __device__ __noinline__ void run_chunk(const Params &p, Smem &sm, const unsigned
     if (lane == 0) atomicAdd(&st[S_CHUNK_RUN], 1u);
   } else {
     if (lane == 0) atomicAdd(&st[S_CHUNK_DIRTY], 1u);
-    nitems = split_chunk(p, stage, g, w, lane, nv, lstart, pre, area, sm.stg[w], st);
+    nitems = split_chunk(p, stage, g, w, lane, nv, lstart, pre, area, sm.stg[threadIdx.x >> 5], st);
     if (nitems == 0) {
       Run fr = run_empty();
       fr.flags = ((cmx >= 0x7FF00000u) ? (F_HASINF_P | F_HASINF_N | F_HASNAN) : 0u);
@@ -2322,7 +2337,7 @@ __device__ __forceinline__ bool apply_segments(const Params &p, uint64_t &Sb0, c
   uint64_t Sb = Sb0;
   unsigned na = 0, nt = 0;
   for (int s = 0; s < nseg; s++) {
-    const int ti = stile[s];
+    const int ti = stile[s] & 0xFF;
     if (ti < lo || ti >= hi) continue;
     const Rec c = seg[s];
     const uint32_t kind = rec_kind(c.meta);
@@ -2342,6 +2357,107 @@ __device__ __forceinline__ bool apply_segments(const Params &p, uint64_t &Sb0, c
       nt += (unsigned)n;
     } else {                                            // K_FALLBACK
       const TileGeo tg = tile_geo(p, g0 + ti, ntiles);
+      Sb = add_terms(p, Sb, tg.start + rec_tstart(c.meta), c.count, st);
+      if (lane == 0) atomicAdd(&st[S_CHUNK_FALLBACK], 1u);
+    }
+  }
+  Sb0 = Sb;
+  napplied += na;
+  nterms += nt;
+  return true;
+}
+
+// Warp 0 of the walk, the fast path of a round: the staged segments of
+// groups g, g + 1, ... (segment i in seg[i], its group in the round and tile
+// in the group in code[i] = group << 8 | tile) that lie in the sum's tiles
+// [tb, te) are composed once more -- consecutive runs of one binade across
+// the groups merge, every other record stands alone -- and the composites
+// applied in order (run composition is associative: Research-1433, finding
+// 2).  The composites overwrite the staged segments.  False, with Sb
+// unchanged, when the check refuses one.
+__device__ __noinline__ bool walk_fast(const Params &p, uint64_t &Sb0, Rec *seg, uint16_t *code, int total,
+                                       int64_t g, int64_t tb, int64_t te, int64_t ntiles, unsigned int *st,
+                                       unsigned &napplied, unsigned &nterms) {
+  const int lane = threadIdx.x & 31;
+  const unsigned full = 0xffffffffu;
+  Run carry = run_empty();
+  bool carry_open = false, alone_prev = true, valid_prev = false;
+  int key_prev = 0, nc = 0;
+  for (int base = 0; base < total; base += 32) {
+    const int j = base + lane;
+    Rec x = make_rec(run_empty(), kZeroE, K_RUN, 0, 0);
+    uint32_t cj = 0;
+    bool valid = false;
+    if (j < total) {
+      x = seg[j];
+      cj = code[j];
+      const int64_t t = (g + (cj >> 8)) * kGroupTiles + (cj & 0xFFu);
+      valid = t >= tb && t < te;
+    }
+    const int key = elem_key(x);
+    const bool alone = elem_alone(x);
+    int kp = __shfl_up_sync(full, key, 1);
+    bool ap = __shfl_up_sync(full, alone, 1), vp = __shfl_up_sync(full, valid, 1);
+    if (lane == 0) { kp = key_prev; ap = alone_prev; vp = valid_prev; }
+    const bool head = valid && (j == 0 || !vp || alone || ap || key != kp);
+    Run v = rec_run(x);
+    int f = head ? 1 : 0;
+#pragma unroll 1
+    for (int o = 1; o < 32; o <<= 1) {
+      const Run ov = shfl_run<SH_UP>(v, o);
+      const int of = __shfl_up_sync(full, f, o);
+      if (lane >= o) { if (!f) v = run_compose(ov, v); f |= of; }
+    }
+    if (!f && valid && carry_open) v = run_compose(carry, v);
+    // an end: followed by a head, an invalid record or nothing (for the
+    // round's last lane the next round's first record decides)
+    const uint32_t heads = __ballot_sync(full, head), valids = __ballot_sync(full, valid);
+    bool nexthead = (heads >> (lane + 1)) & 1u, nextvalid = (valids >> (lane + 1)) & 1u;
+    if (lane == 31 && valid && j + 1 < total) {
+      const Rec xn = seg[j + 1];
+      const uint32_t cn = code[j + 1];
+      const int64_t tn = (g + (cn >> 8)) * kGroupTiles + (cn & 0xFFu);
+      nextvalid = tn >= tb && tn < te;
+      nexthead = elem_alone(xn) || alone || elem_key(xn) != key;
+    }
+    const bool end = valid && (j == total - 1 || !nextvalid || nexthead);
+    const uint32_t ends = __ballot_sync(full, end);
+    const int o = nc + __popc(ends & ((1u << lane) - 1u));
+    __syncwarp();                                      // every record read before any is overwritten
+    if (end) {
+      seg[o] = alone ? x : make_rec(v, key, K_RUN, 0u, 0u);
+      code[o] = (uint16_t)cj;
+    }
+    nc += __popc(ends);
+    carry_open = __shfl_sync(full, valid && !end, 31);
+    carry = shfl_run<SH_IDX>(v, 31);
+    key_prev = __shfl_sync(full, key, 31);
+    alone_prev = __shfl_sync(full, alone, 31);
+    valid_prev = __shfl_sync(full, valid, 31);
+    __syncwarp();
+  }
+  uint64_t Sb = Sb0;
+  unsigned na = 0, nt = 0;
+  for (int s = 0; s < nc; s++) {
+    const Rec c = seg[s];
+    const uint32_t kind = rec_kind(c.meta);
+    na++;
+    if (nonfinite(Sb)) { Sb = absorb(Sb, rec_flags(c.meta)); continue; }
+    if (kind == K_RUN) {
+      uint64_t T = Sb;
+      if (run_apply(T, rec_run(c), c.e) != APPLY_OK) return false;
+      Sb = T;
+    } else if (kind == K_TERMS) {
+      double S = bitsd(Sb);
+      const int n = (int)c.count;
+      if (n > 0) S = __dadd_rn(S, bitsd((uint64_t)c.inc));
+      if (n > 1) S = __dadd_rn(S, bitsd((uint64_t)c.lo));
+      if (n > 2) S = __dadd_rn(S, bitsd((uint64_t)c.hi));
+      Sb = dbits(S);
+      nt += (unsigned)n;
+    } else {                                            // K_FALLBACK
+      const uint32_t cs = code[s];
+      const TileGeo tg = tile_geo(p, (g + (cs >> 8)) * kGroupTiles + (cs & 0xFFu), ntiles);
       Sb = add_terms(p, Sb, tg.start + rec_tstart(c.meta), c.count, st);
       if (lane == 0) atomicAdd(&st[S_CHUNK_FALLBACK], 1u);
     }
@@ -2428,20 +2544,48 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
     off -= ns;
     const uint32_t fits = __ballot_sync(full, mine && off + ns <= kWalkStageSegs);
     r = (~fits == 0u) ? 32 : __ffs(~fits) - 1;        // at least group g fits (at most kGroupSegs)
-    if (lane < r) {
-      const int64_t gi = g + lane;
-      for (int s2 = 0; s2 < ns; s2++) {
-        seg[off + s2] = ldcg_rec(p.grp_seg + gi * kGroupSegs + s2);
-        stile[off + s2] = p.grp_stile[gi * kGroupSegs + s2];
+    const int total = __shfl_sync(full, off + ns, r - 1);
+    auto stage_segments = [&]() {
+      // the whole warp loads them, lane l element l, l + 32, ...: element
+      // idx belongs to the last group whose offset is at most idx
+      for (int base = 0; base < total; base += 32) {
+        const int idx = base + lane;
+        int gl = 0;
+#pragma unroll
+        for (int step = 16; step > 0; step >>= 1) {
+          const int cand = gl + step;
+          const int oc = __shfl_sync(full, off, min(cand, 31));
+          if (cand < r && oc <= idx) gl = cand;
+        }
+        const int og = __shfl_sync(full, off, gl);
+        if (idx < total) {
+          const int64_t gi = g + gl;
+          seg[idx] = ldcg_rec(p.grp_seg + gi * kGroupSegs + (idx - og));
+          stile[idx] = (uint16_t)((gl << 8) | (p.grp_stile[gi * kGroupSegs + (idx - og)] & 0xFF));
+        }
       }
-    }
+    };
+    stage_segments();
     __syncwarp();
     if (lane == 0) {
       TRACE_BATCH(256 + nround, 0, globaltimer());
       TRACE_BATCH(256 + nround, 2, ((unsigned long long)r << 32) | (uint64_t)g);
     }
-    // apply them group by group, in order
-    for (int i = 0; i < r; i++) {
+#ifdef SEQSUM_PROFILE
+    const long long c_apply0 = clock64();
+    const unsigned na_before = napplied;
+#endif
+    // the fast path: the round's segments composed across groups (unless a
+    // group is raw); when the check refuses a composite, the round again
+    // from its start, group by group
+    bool fast = !__any_sync(full, raw != 0) &&
+                walk_fast(p, Sb, seg, stile, total, g, tb, te, ntiles, st, napplied, nterms);
+    if (!fast && !__any_sync(full, raw != 0)) {
+      __syncwarp();
+      stage_segments();
+      __syncwarp();
+    }
+    for (int i = 0; i < r && !fast; i++) {
       const int64_t gi = g + i, g0 = gi * kGroupTiles;
       const int lo = (int)(max(g0, tb) - g0), hi = (int)(min(g0 + kGroupTiles, te) - g0);
       const int rawi = __shfl_sync(full, raw, i), nsi = __shfl_sync(full, ns, i), offi = __shfl_sync(full, off, i);
@@ -2457,6 +2601,9 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
       }
     }
     if (lane == 0) TRACE_BATCH(256 + nround, 1, globaltimer());
+#ifdef SEQSUM_PROFILE
+    if (lane == 0) TRACE_BATCH(256 + nround, 3, ((unsigned long long)(clock64() - c_apply0) << 20) | (napplied - na_before) | ((unsigned long long)smid() << 12));
+#endif
     nround++;
     g += r;
   }
@@ -2545,37 +2692,94 @@ __device__ __forceinline__ bool unit_of(int64_t u, int64_t ntiles, int64_t wave,
   return false;
 }
 
-// Compute warps: the units of the stages in turn, until the control warp
-// marks the end.
+// Claim words of the stages.  A unit's chunks go to whichever compute warps
+// claim them first, so that a chunk that takes long (a split) holds up only
+// its own unit, not the same chunk of the CTA's next units.
+constexpr uint32_t kClaimEnd = 0x80u;
+__device__ __forceinline__ uint32_t claim_word(uint32_t use, bool end) { return (use << 8) | (end ? kClaimEnd : 0u); }
+__device__ __forceinline__ uint32_t read_claim(const Smem &sm, int k) {
+  return __shfl_sync(0xffffffffu, *reinterpret_cast<const volatile uint32_t *>(&sm.cnext[k]), 0);
+}
+// Whether use m of stage k can be claimed from: 1 once its copy has landed
+// and the stage still holds it, 0 when the stage has moved on to a later use
+// (every chunk of use m was claimed and finished), -1 when the wait gave up.
+// Warp-uniform and bounded.
+__device__ __forceinline__ int unit_ready(const Params &p, Smem &sm, int k, uint32_t m, int j) {
+  const uint32_t par = m & 1u;
+  const uint64_t t0 = globaltimer();
+  uint32_t nap = 32;
+  while (true) {
+    if ((int32_t)((read_claim(sm, k) >> 8) - m) > 0) return 0;
+    if (mbar_test_warp(&sm.full[k], par)) {
+      // the phase that completed may already be a later use's
+      return (read_claim(sm, k) >> 8) == m ? 1 : 0;
+    }
+    (void)mbar_try_wait(&sm.full[k], par);
+    __nanosleep(nap);
+    nap = min(nap * 2u, 256u);
+    if (__any_sync(0xffffffffu, globaltimer() - t0 > kWaitNs)) {
+      if ((threadIdx.x & 31) == 0)
+        note_timeout(p, ERR_TMA_TIMEOUT, TO_FULL, (uint32_t)j, (uint32_t)(k | (threadIdx.x >> 5) << 8 | blockIdx.x << 16));
+      return -1;
+    }
+  }
+}
+// Claim the next chunk of use m of stage k: its index, -1 when none is left,
+// -2 at the end marker.  Warp-uniform.
+__device__ __forceinline__ int claim_chunk(Smem &sm, int k, uint32_t m) {
+  int r = -1;
+  if ((threadIdx.x & 31) == 0) {
+    uint32_t c = *reinterpret_cast<volatile uint32_t *>(&sm.cnext[k]);
+    while (true) {
+      if ((c >> 8) != m) break;
+      if (c & kClaimEnd) { r = -2; break; }
+      if ((c & 0xFFu) >= (uint32_t)kWarps) break;
+      const uint32_t prev = atomicCAS(&sm.cnext[k], c, c + 1u);
+      if (prev == c) { r = (int)(c & 0xFFu); break; }
+      c = prev;
+    }
+  }
+  return __shfl_sync(0xffffffffu, r, 0);
+}
+
+// Compute warps: the units of the stages in turn, claiming their chunks,
+// until the end marker.
 __device__ __noinline__ void compute_loop(const Params &p, Smem &sm, const unsigned char *dyn) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   unsigned int *st = sm.st;
-  uint32_t ph = 0;                                       // bit k: parity of full[k]
   for (int j = 0;; j++) {
     const int k = j % kStages;
+    const uint32_t m = (uint32_t)(j / kStages);
     const uint64_t tw = (tid == 0) ? globaltimer() : 0;
     if (lane == 0) beat(p, sm.role, HB_WAIT_UNIT, (uint64_t)j);
-    if (!mbar_wait_warp(p, &sm.full[k], (ph >> k) & 1u, ERR_TMA_TIMEOUT, TO_FULL, (uint32_t)j,
-                        (uint32_t)(k | w << 8 | blockIdx.x << 16)))
-      break;                                             // the call has failed
-    ph ^= 1u << k;
+    const int ready = unit_ready(p, sm, k, m, j);
+    if (ready < 0) break;                                // the call has failed
     if (tid == 0) atomicAdd(&st[S_NS_TMA_WAIT], (unsigned)(globaltimer() - tw));
-    const int kind = sm.geo[k].kind;
-    if (kind == U_END) break;
-    const int64_t t = sm.geo[k].t;
-    const unsigned char *stage = dyn + k * kStageBytes;
-    const uint64_t tb = (tid == 0) ? globaltimer() : 0;
-    if (lane == 0) beat(p, sm.role, HB_UNIT, ((uint64_t)j << 32) | (uint32_t)t);
-    if (tid == 0) TRACE_UNIT(t, kind, 1, tb);
-    if (kind == U_PLAN) plan_chunk(p, sm, stage, k, w);
-    else run_chunk(p, sm, stage, k);
-    if (tid == 0) {
-      const uint64_t te = globaltimer();
-      atomicAdd(&st[kind == U_PLAN ? S_NS_PHASE_A : S_NS_PHASE_B], (unsigned)(te - tb));
-      TRACE_UNIT(t, kind, 2, te);
+    if (ready == 0) continue;
+    bool end = false;
+    while (true) {
+      const int c = claim_chunk(sm, k, m);
+      if (c == -2) { end = true; break; }
+      if (c < 0) break;
+      const int kind = sm.geo[k].kind;
+      const int64_t t = sm.geo[k].t;
+      const unsigned char *stage = dyn + k * kStageBytes;
+      const uint64_t tb = (lane == 0) ? globaltimer() : 0;
+      if (lane == 0) beat(p, sm.role, HB_UNIT, ((uint64_t)j << 32) | (uint32_t)t);
+      if (c == 0 && lane == 0) TRACE_UNIT(t, kind, 1, tb);
+      if (kind == U_PLAN) plan_chunk(p, sm, stage, k, c);
+      else run_chunk(p, sm, stage, k, c);
+      if (c == 0 && lane == 0) {
+        const uint64_t te = globaltimer();
+        atomicAdd(&st[kind == U_PLAN ? S_NS_PHASE_A : S_NS_PHASE_B], (unsigned)(te - tb));
+        TRACE_UNIT(t, kind, 2, te);
+      }
+      if (lane == 0 && kind == U_RUN)
+        TRACE_UNIT_MAX(t, kind, 7, ((globaltimer() - tb) << 20) | ((uint64_t)(sm.nitems[k][c] & 0xFFF) << 8) | (uint64_t)c);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.done[k]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.done[k]);
+    if (end) break;
   }
 }
 
@@ -2584,8 +2788,7 @@ __device__ __noinline__ void control_loop(const Params &p, Smem &sm, unsigned ch
                                           int64_t ntiles) {
   const int lane = threadIdx.x & 31;
   const int64_t nunits = 2 * ntiles;
-  uint32_t u_next = 0;                                   // lane 0: the next ticket, taken one unit ahead
-  if (lane == 0) u_next = atomicAdd(&p.ctr[C_TICKET], 1u);
+  bool beside_walker = false;                            // lane 0
   uint32_t ph = 0;                                       // bit k: parity of done[k]
   auto epilogue = [&](int k) -> bool {
     const uint64_t tw = globaltimer();
@@ -2605,14 +2808,27 @@ __device__ __noinline__ void control_loop(const Params &p, Smem &sm, unsigned ch
   for (int j = 0;; j++) {
     const int k = j % kStages;
     if (j >= kStages && !epilogue(k)) break;             // the unit that held this stage (else the call failed)
+    // a ticket only once the stage is free: a CTA held up by a long unit
+    // takes none that it cannot start; none at all once the CTA has found
+    // that it shares its SM with a walker
     uint32_t u = 0;
     if (lane == 0) {
-      u = u_next;
-      u_next = atomicAdd(&p.ctr[C_TICKET], 1u);          // used at the next unit: its latency overlaps
+      if (j == kStages) {
+        const uint32_t me = smid() + 1u;
+        for (int i = 0; i < min(p.nwalkers, 2); i++)
+          if (*reinterpret_cast<const volatile uint32_t *>(&p.ctr[C_WALK_SM + i]) == me) {
+            beside_walker = true;
+#ifdef SEQSUM_PROFILE
+            p.dbg[16000 + i] = ((unsigned long long)me << 32) | (blockIdx.x + 1u);
+#endif
+          }
+      }
+      u = beside_walker ? 0xFFFFFFFFu : atomicAdd(&p.ctr[C_TICKET], 1u);
     }
     u = __shfl_sync(0xffffffffu, u, 0);
+    const uint32_t use = (uint32_t)(j / kStages);
     if ((int64_t)u >= nunits) {
-      if (lane == 0) sm.geo[k].kind = U_END;
+      if (lane == 0) { sm.geo[k].kind = U_END; sm.cnext[k] = claim_word(use, true); }
       __syncwarp();
       if (lane < kCopyLanes) cp_async_mbar_arrive(&sm.full[k]);     // all the stage's arrivals at once
       if (lane == 0) mbar_arrive(&sm.full[k]);
@@ -2627,6 +2843,7 @@ __device__ __noinline__ void control_loop(const Params &p, Smem &sm, unsigned ch
     if (lane == 0) {
       sm.geo[k] = g;
       sm.plan_cnt[k] = 0;
+      sm.cnext[k] = claim_word(use, false);
       TRACE_UNIT(t, g.kind, 0, globaltimer());
       TRACE_UNIT(t, g.kind, 4, ((unsigned long long)blockIdx.x << 32) | u);
     }
@@ -2675,12 +2892,16 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
       mbar_init(&sm.full[s], kFullArrivals);             // the copying lanes and the tile's copy
       mbar_init(&sm.done[s], kWarps);
       sm.plan_cnt[s] = 0;
+      sm.cnext[s] = 0u;
     }
     fence_mbar_init();
     if (blockIdx.x == 0) p.stats[S_T_START] = globaltimer();
     // roles go to CTAs in the order they start, so every waiting role is
     // held by a running CTA
     sm.role = (int)atomicAdd(&p.ctr[C_ROLE], 1u);
+    // the first two walkers' SMs: the streaming CTAs that share them stop
+    // early, so that each walk's serial chain has its SM's pipes to itself
+    if (sm.role < min(p.nwalkers, 2)) atomicExch(&p.ctr[C_WALK_SM + sm.role], smid() + 1u);
   }
   __syncthreads();
   if ((tid & 31) == 0) beat(p, sm.role, HB_START, 0);
@@ -2728,6 +2949,8 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
       p.ctr[C_SUMTICKET] = 0;
       p.ctr[C_ROLE] = 0;
       p.ctr[C_EXIT] = 0;
+      p.ctr[C_WALK_SM] = 0;
+      p.ctr[C_WALK_SM + 1] = 0;
       __threadfence();
     }
   }
