@@ -474,6 +474,7 @@ struct StageGeo {
 struct Smem {
   uint64_t full[kStages];           // the unit's copy and plan words landed, or the end marker (kFullArrivals)
   uint64_t done[kStages];           // the compute warps finished the unit (kWarps arrivals)
+  uint64_t used[kStages];           // the unit's chunks have read their terms from the stage (kWarps arrivals)
   StageGeo geo[kStages];            // the unit's tile and kind (U_PLAN, U_RUN, U_END)
   // a run unit's plan words, copied in ahead of its runs: the prefix of the
   // tile before and the tile's chunk plans (cp.async destinations: 16-byte
@@ -487,12 +488,16 @@ struct Smem {
   // per stage the claim word of its unit: use << 8 | chunks claimed (the
   // use counts the units the stage has held; bit 7 marks the end marker)
   uint32_t cnext[kStages];
+  int slow[kStages];                // a chunk of the stage's unit is being split (it ends late)
   Rec stg[kWarps][kChunkSlots];     // a split chunk's items, staged in order before they are written out
   Rec gel[kGroupSegs];              // control warp: a group's records in order, for its composition
   uint16_t gtile[kGroupSegs];       // ... and the tile (in the group) of each
   int role;
   uint32_t barcnt[kWarps];          // walker and scanner: wide barriers passed per warp (heartbeat)
   unsigned int st[S_COUNT];         // per-CTA statistics of one call (32-bit: native shared atomics)
+#ifdef SEQSUM_PROFILE
+  unsigned int prof[40];            // cycle profile of the run chunks
+#endif
   // walker
   uint64_t S;
   int m, nel, restart, nseg;
@@ -515,10 +520,12 @@ static_assert(offsetof(Smem, pre_raw) % 16 == 0 && offsetof(Smem, cplan_raw) % 1
               "cp.async destinations must be 16-byte aligned");
 // a run unit's copies: lane 0 the prefix word pair, lanes 1..16 the chunk
 // plans (16 bytes each); every one of those lanes makes one arrival when its
-// copy has landed, and lane 0 one more for the tile's own copy
+// copy has landed, lane 0 one more for the tile's own copy, and one more once
+// the unit's description (sm.geo, the claim word) is written
 constexpr int kCopyLanes = 1 + kWarps * 2;
-constexpr uint32_t kFullArrivals = kCopyLanes + 1;
-static_assert(offsetof(Smem, full) % 8 == 0 && offsetof(Smem, done) % 8 == 0, "mbarriers are 8-byte aligned");
+constexpr uint32_t kFullArrivals = kCopyLanes + 2;
+static_assert(offsetof(Smem, full) % 8 == 0 && offsetof(Smem, done) % 8 == 0 && offsetof(Smem, used) % 8 == 0,
+              "mbarriers are 8-byte aligned");
 
 // The 256-thread barrier of a walking or scanning CTA; each warp first records the
 // barrier's site and how many it has passed (its heartbeat).
@@ -698,6 +705,24 @@ __device__ __forceinline__ bool mbar_wait_warp(const Params &p, uint64_t *bar, u
 #define PROF_PT(base, id) do { } while (0)
 #endif
 #define SPLIT_PT(id) PROF_PT(15200, id)
+// Per-CTA cycle profile of the run chunks (profiling builds): cycles since
+// the previous point and passes, summed in shared memory, added to the
+// diagnostic words from 15300 on when the CTA ends.
+#ifdef SEQSUM_PROFILE
+#define CPROF_START long long cprof_t = clock64()
+#define CPROF_PT(id)                                                                       \
+  do {                                                                                     \
+    if ((threadIdx.x & 31) == 0) {                                                         \
+      const long long n_ = clock64();                                                      \
+      atomicAdd(&sm.prof[2 * (id)], (unsigned)(n_ - cprof_t));                             \
+      atomicAdd(&sm.prof[2 * (id) + 1], 1u);                                               \
+      cprof_t = n_;                                                                        \
+    }                                                                                      \
+  } while (0)
+#else
+#define CPROF_START do { } while (0)
+#define CPROF_PT(id) do { } while (0)
+#endif
 
 // The plan of chunk w of the stage's tile (by whichever compute warp claimed
 // it).  The warp that completes the tile's plan publishes the tile's
@@ -706,6 +731,13 @@ __device__ __forceinline__ bool mbar_wait_warp(const Params &p, uint64_t *bar, u
 __device__ __noinline__ void publish_tile_plan(const Params &p, Smem &sm, int k);
 __device__ __forceinline__ void load_lane(const Params &p, const unsigned char *stage, bool use_tma, int64_t row,
                                           int64_t lstart, int nv, int w, int lane, uint64_t *xs);
+// A chunk is done with the stage's terms (every lane has them in registers):
+// the control warp may copy the next unit's terms into the stage.  Once per
+// chunk and use of the stage.
+__device__ __forceinline__ void release_stage(Smem &sm, int k) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&sm.used[k]);
+}
 __device__ __noinline__ void plan_chunk(const Params &p, Smem &sm, const unsigned char *stage, int k, int w) {
   const int lane = threadIdx.x & 31;
   const unsigned full = 0xffffffffu;
@@ -714,6 +746,7 @@ __device__ __noinline__ void plan_chunk(const Params &p, Smem &sm, const unsigne
   const int nv = (int)max((int64_t)0, min((int64_t)kLaneTerms, g.end - lstart));
   uint64_t xs[kLaneTerms];
   load_lane(p, stage, g.tma != 0, (g.start >> 4) + w * 32 + lane, lstart, nv, w, lane, xs);
+  release_stage(sm, k);
   uint32_t mx = 0, orz = 0, orh = 0, andh = 0xFFFFFFFFu;
 #pragma unroll
   for (int i = 0; i < kLaneTerms; i++) {
@@ -1080,6 +1113,28 @@ __device__ __forceinline__ void lane_fast(const uint64_t *xs, int nv, int c, uin
     if (i < nv) { orl |= hi; andl &= hi; }
   }
 }
+// The same, reading the lane's terms from its row of the stage two at a
+// time (a rolled loop: the instructions of a chunk's run stay few, so that
+// the warps of an SM keep them cached).
+__device__ __forceinline__ void lane_fast_stage(const unsigned char *rp, int sw, int nv, int c, uint64_t &P,
+                                                uint64_t &N, bool &anytie, uint32_t &orl, uint32_t &andl) {
+  P = 0; N = 0; anytie = false; orl = 0; andl = 0xFFFFFFFFu;
+#pragma unroll 1
+  for (int q = 0; q < kLaneTerms / 2; q++) {
+    const uint4 v = *reinterpret_cast<const uint4 *>(rp + ((q ^ sw) << 4));
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+      const bool in = 2 * q + h < nv;
+      const uint32_t hi = in ? (h ? v.w : v.y) : 0u, lo = in ? (h ? v.z : v.x) : 0u;
+      uint64_t ri;
+      bool tie;
+      term_inc_fast(hi, lo, c, ri, tie);
+      if (hi >> 31) N += ri; else P += ri;
+      anytie |= tie;
+      if (in) { orl |= hi; andl &= hi; }
+    }
+  }
+}
 // The fast rule applies to binade e for terms whose largest magnitude word
 // is mx: e in range and every term below 2^e.
 __device__ __forceinline__ bool fast_ok(int e, uint32_t mx) {
@@ -1194,7 +1249,9 @@ __device__ __noinline__ int split_chunk(const Params &p, const unsigned char *st
                                         int lane, int nv, int64_t lstart, const ChunkPre &pre, Rec *area,
                                         Rec *stg, unsigned int *st) {
   const unsigned full = 0xffffffffu;
-  const bool use_tma = g.tma != 0;
+  // the stage may already hold the next unit's terms: this chunk's come
+  // from global memory
+  const bool use_tma = false;
   const int64_t row = (g.start >> 4) + w * 32 + lane;
   const uint64_t t = (uint64_t)g.t;
   PROF_START;
@@ -1353,6 +1410,7 @@ __device__ __noinline__ void run_chunk(const Params &p, Smem &sm, const unsigned
   // global memory, bounded): the prefix before the tile and its chunk plans
   const uint32_t tag = (p.epoch << 1) | 1u;
   const uint64_t tv = globaltimer();
+  CPROF_START;
   DF ex;
   float exab;
   if (g.t == g.first_tile) {
@@ -1395,7 +1453,9 @@ __device__ __noinline__ void run_chunk(const Params &p, Smem &sm, const unsigned
     if (lane == 0) atomicAdd(&st[S_NS_VERDICT_WAIT], (unsigned)(globaltimer() - t0));
   }
   uint32_t cmx, cflags;
+  CPROF_PT(0);                                        // prefix and plan words
   const ChunkPre pre = chunk_verdict(g, w, ex, exab, cp, cmx, cflags);
+  CPROF_PT(1);                                        // the verdict
   if (lane == 0) atomicAdd(&st[S_NS_VERDICT], (unsigned)(globaltimer() - tv));
   const int64_t cstart = g.start + (int64_t)w * kChunkTerms;
   const int cnt_chunk = (int)max((int64_t)0, min((int64_t)kChunkTerms, g.end - cstart));
@@ -1408,6 +1468,12 @@ __device__ __noinline__ void run_chunk(const Params &p, Smem &sm, const unsigned
   Rec *area = p.items + g.t * kTileSlots;
   Rec crec;
   int nitems = 0;
+  if (mode != CP_CLEAN) {
+    // a zero chunk reads no terms; a split one reads them from global memory
+    // (and ends late: the control warp takes no unit for the stage early)
+    if (mode == CP_DIRTY && lane == 0) sm.slow[k] = 1;
+    release_stage(sm, k);
+  }
   if (mode == CP_ZERO) {
     // every term is +0 or -0: a run of zeros (all -0 keeps a -0 sum at -0)
     Run z = run_empty();
@@ -1415,15 +1481,18 @@ __device__ __noinline__ void run_chunk(const Params &p, Smem &sm, const unsigned
     crec = make_rec(z, kZeroE, K_RUN, (uint32_t)cnt_chunk, (uint32_t)(w * kChunkTerms));
     if (lane == 0) atomicAdd(&st[S_CHUNK_RUN], 1u);
   } else if (mode == CP_CLEAN) {
-    uint64_t xs[kLaneTerms];
-    load_lane(p, stage, g.tma != 0, row, lstart, nv, w, lane, xs);
+    CPROF_PT(2);
     Run r;
     bool general = true, general_reduce = true;
-    if (fast_ok(e, cmx)) {
+    // a chunk with terms past the tensor map's rows (the ragged end of x)
+    // takes the general path, from global memory (warp-uniform: the fast
+    // rule's reductions need the whole warp)
+    const bool from_stage = __all_sync(full, g.tma != 0 && row < p.tma_rows);
+    if (fast_ok(e, cmx) && from_stage) {
       uint64_t P, N;
       bool anytie;
       uint32_t orl, andl;
-      lane_fast(xs, nv, 64 - (e + 1023), P, N, anytie, orl, andl);
+      lane_fast_stage(stage + (w * 32 + lane) * 128, lane & 7, nv, 64 - (e + 1023), P, N, anytie, orl, andl);
       if ((cflags & WA_NEG) == 0 && __ballot_sync(full, anytie) == 0) {
         // non-negative terms and no tie: the run is a plain sum of increments
 #pragma unroll
@@ -1436,7 +1505,9 @@ __device__ __noinline__ void run_chunk(const Params &p, Smem &sm, const unsigned
         general = false;
       }
     }
-    if (general) r = lane_run_general(p, stage, g.tma != 0, row, lstart, nv, w, lane, e);
+    release_stage(sm, k);
+    CPROF_PT(3);                                      // the fast rule
+    if (general) r = lane_run_general(p, stage, false, row, lstart, nv, w, lane, e);   // terms from global memory
     if (general_reduce) {
 #pragma unroll 1
       for (int off = 1; off < 32; off <<= 1) {
@@ -1444,8 +1515,10 @@ __device__ __noinline__ void run_chunk(const Params &p, Smem &sm, const unsigned
         if ((lane & (2 * off - 1)) == 0) r = run_compose(r, o);
       }
     }
+    CPROF_PT(4);                                      // general path and reduction
     crec = make_rec(r, (r.flags & F_ZERO) ? kZeroE : e, K_RUN, (uint32_t)cnt_chunk, (uint32_t)(w * kChunkTerms));
     if (lane == 0) atomicAdd(&st[S_CHUNK_RUN], 1u);
+    CPROF_PT(5);                                      // the record
   } else {
     if (lane == 0) atomicAdd(&st[S_CHUNK_DIRTY], 1u);
     nitems = split_chunk(p, stage, g, w, lane, nv, lstart, pre, area, sm.stg[threadIdx.x >> 5], st);
@@ -2708,12 +2781,30 @@ __device__ __forceinline__ int unit_ready(const Params &p, Smem &sm, int k, uint
   const uint32_t par = m & 1u;
   const uint64_t t0 = globaltimer();
   uint32_t nap = 32;
+#ifdef SEQSUM_PROFILE
+  const long long c0 = clock64();
+  int npoll = 0;
+#endif
   while (true) {
     if ((int32_t)((read_claim(sm, k) >> 8) - m) > 0) return 0;
     if (mbar_test_warp(&sm.full[k], par)) {
+#ifdef SEQSUM_PROFILE
+      if ((threadIdx.x & 31) == 0) {
+        atomicAdd(&sm.prof[npoll ? 32 : 34], (unsigned)(clock64() - c0));
+        atomicAdd(&sm.prof[npoll ? 33 : 35], 1u);
+        // the earliest time a waiting warp saw the unit's copies complete
+        if (npoll) {
+          const int64_t ti = sm.geo[k].t * 2 + sm.geo[k].kind;
+          if (ti >= 0 && 54100 + ti < 61440) atomicMax(&p.dbg[54100 + ti], ~0ull - globaltimer());
+        }
+      }
+#endif
       // the phase that completed may already be a later use's
       return (read_claim(sm, k) >> 8) == m ? 1 : 0;
     }
+#ifdef SEQSUM_PROFILE
+    npoll++;
+#endif
     (void)mbar_try_wait(&sm.full[k], par);
     __nanosleep(nap);
     nap = min(nap * 2u, 256u);
@@ -2747,15 +2838,20 @@ __device__ __forceinline__ int claim_chunk(Smem &sm, int k, uint32_t m) {
 __device__ __noinline__ void compute_loop(const Params &p, Smem &sm, const unsigned char *dyn) {
   const int tid = threadIdx.x, lane = tid & 31;
   unsigned int *st = sm.st;
+  CPROF_START;
   for (int j = 0;; j++) {
     const int k = j % kStages;
     const uint32_t m = (uint32_t)(j / kStages);
     const uint64_t tw = (tid == 0) ? globaltimer() : 0;
     if (lane == 0) beat(p, sm.role, HB_WAIT_UNIT, (uint64_t)j);
+#ifdef SEQSUM_PROFILE
+    const bool armed0 = (read_claim(sm, k) >> 8) == m;
+#endif
     const int ready = unit_ready(p, sm, k, m, j);
     if (ready < 0) break;                                // the call has failed
     if (tid == 0) atomicAdd(&st[S_NS_TMA_WAIT], (unsigned)(globaltimer() - tw));
     if (ready == 0) continue;
+    CPROF_PT(sm.geo[k].kind == U_RUN ? (armed0 ? 6 : 7) : (armed0 ? 16 : 17));   // waited for a run / plan unit, armed or not
     bool end = false;
     while (true) {
       const int c = claim_chunk(sm, k, m);
@@ -2767,8 +2863,10 @@ __device__ __noinline__ void compute_loop(const Params &p, Smem &sm, const unsig
       const uint64_t tb = (lane == 0) ? globaltimer() : 0;
       if (lane == 0) beat(p, sm.role, HB_UNIT, ((uint64_t)j << 32) | (uint32_t)t);
       if (c == 0 && lane == 0) TRACE_UNIT(t, kind, 1, tb);
+      CPROF_PT(kind == U_PLAN ? 8 : 9);                 // waiting and claiming before a plan / run chunk
       if (kind == U_PLAN) plan_chunk(p, sm, stage, k, c);
       else run_chunk(p, sm, stage, k, c);
+      CPROF_PT(kind == U_PLAN ? 10 : 11);               // the plan chunk / the run chunk
       if (c == 0 && lane == 0) {
         const uint64_t te = globaltimer();
         atomicAdd(&st[kind == U_PLAN ? S_NS_PHASE_A : S_NS_PHASE_B], (unsigned)(te - tb));
@@ -2790,6 +2888,7 @@ __device__ __noinline__ void control_loop(const Params &p, Smem &sm, unsigned ch
   const int64_t nunits = 2 * ntiles;
   bool beside_walker = false;                            // lane 0
   uint32_t ph = 0;                                       // bit k: parity of done[k]
+  CPROF_START;
   auto epilogue = [&](int k) -> bool {
     const uint64_t tw = globaltimer();
     if (lane == 0) beat(p, sm.role + 0x80u, HB_WAIT_DONE, ((uint64_t)k << 32) | (uint32_t)sm.geo[k].t);
@@ -2801,16 +2900,16 @@ __device__ __noinline__ void control_loop(const Params &p, Smem &sm, unsigned ch
       atomicAdd(&sm.st[S_NS_CTRL_WAIT], (unsigned)(globaltimer() - tw));
       TRACE_UNIT(sm.geo[k].t, sm.geo[k].kind, 5, globaltimer());
     }
+    CPROF_PT(12);                                        // control: waiting for a unit's chunks
     if (sm.geo[k].kind == U_RUN) run_epilogue(p, sm, k, ntiles);   // a plan unit's last warp has published it
+    CPROF_PT(13);                                        // control: the epilogue
     if (lane == 0) TRACE_UNIT(sm.geo[k].t, sm.geo[k].kind, 3, globaltimer());
     return true;
   };
-  for (int j = 0;; j++) {
-    const int k = j % kStages;
-    if (j >= kStages && !epilogue(k)) break;             // the unit that held this stage (else the call failed)
-    // a ticket only once the stage is free: a CTA held up by a long unit
-    // takes none that it cannot start; none at all once the CTA has found
-    // that it shares its SM with a walker
+  uint32_t uph = 0;                                      // bit k: parity of used[k]
+  // lane 0: the next ticket; none at all once the CTA has found that it
+  // shares its SM with a walker
+  auto ticket = [&](int j) -> uint32_t {
     uint32_t u = 0;
     if (lane == 0) {
       if (j == kStages) {
@@ -2825,30 +2924,15 @@ __device__ __noinline__ void control_loop(const Params &p, Smem &sm, unsigned ch
       }
       u = beside_walker ? 0xFFFFFFFFu : atomicAdd(&p.ctr[C_TICKET], 1u);
     }
-    u = __shfl_sync(0xffffffffu, u, 0);
-    const uint32_t use = (uint32_t)(j / kStages);
-    if ((int64_t)u >= nunits) {
-      if (lane == 0) { sm.geo[k].kind = U_END; sm.cnext[k] = claim_word(use, true); }
-      __syncwarp();
-      if (lane < kCopyLanes) cp_async_mbar_arrive(&sm.full[k]);     // all the stage's arrivals at once
-      if (lane == 0) mbar_arrive(&sm.full[k]);
-      for (int jj = max(j - kStages + 1, 0); jj < j; jj++)
-        if (!epilogue(jj % kStages)) break;
-      break;
-    }
-    int64_t t;
-    const bool plan = unit_of((int64_t)u, ntiles, p.wave, t);
-    StageGeo g = stage_geo(p, t);
-    g.kind = plan ? U_PLAN : U_RUN;
-    if (lane == 0) {
-      sm.geo[k] = g;
-      sm.plan_cnt[k] = 0;
-      sm.cnext[k] = claim_word(use, false);
-      TRACE_UNIT(t, g.kind, 0, globaltimer());
-      TRACE_UNIT(t, g.kind, 4, ((unsigned long long)blockIdx.x << 32) | u);
-    }
-    // a run unit's plan words (the prefix before the tile, the tile's chunk
-    // plans); each copying lane arrives once its copy has landed
+    return __shfl_sync(0xffffffffu, u, 0);
+  };
+  // the copies of a unit into stage k: a run unit's plan words (the prefix
+  // before the tile, the tile's chunk plans; each copying lane arrives once
+  // its copy has landed) and the tile's terms
+  auto copy_in = [&](int k, const StageGeo &g, int64_t t, bool plan) {
+#ifdef SEQSUM_PROFILE
+    if (lane == 0 && 50000 + 2 * t + (plan ? 0 : 1) < 54100) p.dbg[50000 + 2 * t + (plan ? 0 : 1)] = globaltimer();
+#endif
     if (!plan && sq_ok(p, t < p.cap_tiles, 22, t)) {
       if (lane == 0 && t > g.first_tile) cp_async16(sm.pre_raw[k], p.status + 2 * (t - 1));
       if (lane >= 1 && lane < kCopyLanes) cp_async16(&sm.cplan_raw[k][2 * (lane - 1)], p.cplan + t * kWarps * 4 + 2 * (lane - 1));
@@ -2864,6 +2948,67 @@ __device__ __noinline__ void control_loop(const Params &p, Smem &sm, unsigned ch
         mbar_arrive(&sm.full[k]);
       }
     }
+  };
+  for (int j = 0;; j++) {
+    const int k = j % kStages;
+    const uint32_t use = (uint32_t)(j / kStages);
+    uint32_t u = 0;
+    bool have_u = false, copied = false;
+    int64_t t = 0;
+    bool plan = false;
+    StageGeo g;
+    if (j >= kStages) {
+      // once the stage's unit has read its plan words and terms, the next
+      // unit's can be copied in while that unit still computes -- unless a
+      // chunk of it is being split: then the CTA takes no ticket that it
+      // would hold until the split ends
+      if (!mbar_wait_warp(p, &sm.used[k], (uph >> k) & 1u, ERR_TMA_TIMEOUT, TO_DONE, (uint32_t)j,
+                          (uint32_t)(k | blockIdx.x << 16)))
+        break;
+      uph ^= 1u << k;
+      if (!sm.slow[k]) {
+        u = ticket(j);
+        have_u = true;
+        if ((int64_t)u < nunits) {
+          plan = unit_of((int64_t)u, ntiles, p.wave, t);
+          g = stage_geo(p, t);
+          copy_in(k, g, t, plan);
+          copied = true;
+        }
+      }
+      if (!epilogue(k)) break;                           // the unit that held this stage (else the call failed)
+    }
+    CPROF_PT(14);                                        // control: waits, the early copies, the epilogue
+#ifdef SEQSUM_PROFILE
+    if (lane == 0 && j >= kStages) atomicAdd(&sm.prof[copied ? 36 : 38], 1u);
+#endif
+    if (!have_u) u = ticket(j);
+    if ((int64_t)u >= nunits) {
+      if (lane == 0) { sm.geo[k].kind = U_END; sm.cnext[k] = claim_word(use, true); }
+      __syncwarp();
+      if (lane < kCopyLanes) cp_async_mbar_arrive(&sm.full[k]);     // all the stage's arrivals at once
+      if (lane == 0) { mbar_arrive(&sm.full[k]); mbar_arrive(&sm.full[k]); }
+      for (int jj = max(j - kStages + 1, 0); jj < j; jj++)
+        if (!epilogue(jj % kStages)) break;
+      break;
+    }
+    if (!copied) {
+      plan = unit_of((int64_t)u, ntiles, p.wave, t);
+      g = stage_geo(p, t);
+    }
+    g.kind = plan ? U_PLAN : U_RUN;
+    if (lane == 0) {
+      sm.geo[k] = g;
+      sm.plan_cnt[k] = 0;
+      sm.slow[k] = 0;
+      sm.cnext[k] = claim_word(use, false);
+      TRACE_UNIT(t, g.kind, 0, globaltimer());
+      TRACE_UNIT(t, g.kind, 4, ((unsigned long long)blockIdx.x << 32) | u);
+    }
+    if (!copied) copy_in(k, g, t, plan);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.full[k]);             // the unit's description is written
+    CPROF_PT(15);                                        // control: arming the stage
   }
 }
 
@@ -2886,13 +3031,18 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
   int64_t ntiles = (p.ntiles >= 0) ? p.ntiles : (int64_t)__ldcg(&p.ctr[C_NTILES]);
   if (ntiles > p.cap_tiles) ntiles = 0;                  // the set-up flagged ERR_CAPACITY
   if (tid < S_COUNT) sm.st[tid] = 0;
+#ifdef SEQSUM_PROFILE
+  if (tid < 40) sm.prof[tid] = 0u;
+#endif
   if (tid < kWarps) sm.barcnt[tid] = 0;
   if (tid == 0) {
     for (int s = 0; s < kStages; s++) {
       mbar_init(&sm.full[s], kFullArrivals);             // the copying lanes and the tile's copy
       mbar_init(&sm.done[s], kWarps);
+      mbar_init(&sm.used[s], kWarps);
       sm.plan_cnt[s] = 0;
       sm.cnext[s] = 0u;
+      sm.slow[s] = 0;
     }
     fence_mbar_init();
     if (blockIdx.x == 0) p.stats[S_T_START] = globaltimer();
@@ -2939,6 +3089,9 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
   if ((tid & 31) == 0) beat(p, sm.role, HB_END, 0);
   __syncthreads();
   if (tid < S_ACCUM_END && sm.st[tid]) atomicAdd(&p.stats[tid], (unsigned long long)sm.st[tid]);
+#ifdef SEQSUM_PROFILE
+  if (tid < 40 && sm.prof[tid]) atomicAdd(&p.dbg[15300 + tid], (unsigned long long)sm.prof[tid]);
+#endif
   if (tid == 0) {
     __threadfence();
     if (atomicAdd(&p.ctr[C_EXIT], 1u) + 1 == gridDim.x) {
