@@ -482,6 +482,11 @@ struct Smem {
   alignas(16) uint64_t pre_raw[kStages][2];
   alignas(16) uint64_t cplan_raw[kStages][kWarps * 4];
   ChunkPlan plan[kStages][kWarps];  // a plan unit's chunk plans
+  // a run unit's chunk verdicts, formed by the first warp that reaches the
+  // unit (vtile: its tile + 1 once they are in)
+  ChunkPre vpre[kStages][kWarps];
+  uint32_t vmx[kStages][kWarps], vfl[kStages][kWarps];
+  int64_t vtile[kStages];
   Rec chunk[kStages][kWarps];       // a run unit's chunk records
   int nitems[kStages][kWarps];      // >0: a split chunk's items in the tile's item area
   int plan_cnt[kStages];            // chunks of a plan unit's tile planned so far
@@ -516,6 +521,8 @@ struct Smem {
   DF carry;
   float carry_abs;
 };
+// two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
+static_assert(sizeof(Smem) + sizeof(Params) + 64 + kDynSmem + 1024 <= 233472 / 2, "two CTAs per SM");
 static_assert(offsetof(Smem, pre_raw) % 16 == 0 && offsetof(Smem, cplan_raw) % 16 == 0,
               "cp.async destinations must be 16-byte aligned");
 // a run unit's copies: lane 0 the prefix word pair, lanes 1..16 the chunk
@@ -985,14 +992,10 @@ __device__ __noinline__ void read_prefix(const Params &p, Smem &sm, int64_t t, D
   exab = status_abs(B);
 }
 
-// A run unit's verdict on chunk w of its tile (every compute warp forms its
-// own): the chunk's approximate starting value -- the prefix before the tile
-// plus the plans of the tile's earlier chunks, lane j holding chunk j's --,
-// its error allowance, and whether every prefix inside it stays in one
-// binade.  Whole warp; returns the verdict and the chunk's largest magnitude
-// word and flags.
-__device__ __forceinline__ ChunkPre chunk_verdict(const StageGeo &g, int w, DF ex, float exab, const ChunkPlan &cp,
-                                                  uint32_t &cmx, uint32_t &cflags) {
+// The verdicts of all chunks of the tile at once: lane j (j < kWarps) the
+// verdict on chunk j, its largest magnitude word and flags.  Whole warp.
+__device__ __forceinline__ ChunkPre chunk_verdicts(const StageGeo &g, DF ex, float exab, const ChunkPlan &cp,
+                                                   uint32_t &cmx, uint32_t &cflags) {
   const int lane = threadIdx.x & 31;
   const unsigned full = 0xffffffffu;
   const DF sig = df_fixed((int64_t)cp.P - (int64_t)cp.N, cp.L);
@@ -1005,21 +1008,17 @@ __device__ __forceinline__ ChunkPre chunk_verdict(const StageGeo &g, int w, DF e
     const float oa = __shfl_up_sync(full, sa, o);
     if (lane >= o) { s = df_add(os, s); sa += oa; }
   }
-  // the sums of chunks 0 .. w-1 (lane w - 1's inclusive value)
-  const int src = w > 0 ? w - 1 : 0;
-  DF es = DF{__shfl_sync(full, s.hi, src), __shfl_sync(full, s.lo, src)};
-  float ea = __shfl_sync(full, sa, src);
-  if (w == 0) { es = DF{0.0f, 0.0f}; ea = 0.0f; }
-  const uint64_t P = __shfl_sync(full, cp.P, w), N = __shfl_sync(full, cp.N, w);
-  const int L = __shfl_sync(full, cp.L, w);
-  cmx = __shfl_sync(full, cp.mx, w);
-  cflags = __shfl_sync(full, cp.flags, w);
+  // the sums of the chunks before lane j's (exclusive)
+  DF es = DF{__shfl_up_sync(full, s.hi, 1), __shfl_up_sync(full, s.lo, 1)};
+  float ea = __shfl_up_sync(full, sa, 1);
+  if (lane == 0) { es = DF{0.0f, 0.0f}; ea = 0.0f; }
+  cmx = cp.mx;
+  cflags = cp.flags;
   const DF c = df_add(ex, es);
   const float cab = exab + ea;
-  const float abw = f_fixed(P + N, L);
-  const float nb = (float)(g.start - g.sum_start + (int64_t)(w + 1) * kChunkTerms);
-  const float delta = __fmaf_rn(nb, 0x1p-53f, kPlanEps) * (cab + abw) + kTinyF;
-  const float Pf = f_fixed(P, L), Nf = f_fixed(N, L);
+  const float nb = (float)(g.start - g.sum_start + (int64_t)(lane + 1) * kChunkTerms);
+  const float delta = __fmaf_rn(nb, 0x1p-53f, kPlanEps) * (cab + ab) + kTinyF;
+  const float Pf = f_fixed(cp.P, cp.L), Nf = f_fixed(cp.N, cp.L);
   int e = 0, mode;
   if (!(cflags & WA_NZ)) mode = CP_ZERO;
   else if (one_binade_df(df_addf(c, -(Nf + delta)), df_addf(c, Pf + delta), e)) mode = CP_CLEAN;
@@ -1406,56 +1405,80 @@ __device__ __noinline__ void run_chunk(const Params &p, Smem &sm, const unsigned
   const unsigned full = 0xffffffffu;
   unsigned int *st = sm.st;
   const StageGeo &g = sm.geo[k];
-  // ---- the plan words, copied in with the tile (else read again from
-  // global memory, bounded): the prefix before the tile and its chunk plans
-  const uint32_t tag = (p.epoch << 1) | 1u;
   const uint64_t tv = globaltimer();
   CPROF_START;
-  DF ex;
-  float exab;
-  if (g.t == g.first_tile) {
-    ex = df_from_double(p.s0s ? p.s0s[g.sum] : p.s0);
-    exab = fabsf(ex.hi);
-  } else {
-    const uint64_t A = sm.pre_raw[k][0], B = sm.pre_raw[k][1];
-    if ((uint32_t)(A & 0xFF) == tag && (uint32_t)B == tag) {
-      ex = status_sum(A);
-      exab = status_abs(B);
-    } else {
-      read_prefix(p, sm, g.t, ex, exab);
-    }
-  }
-  ChunkPlan cp{0ull, 0ull, 0, 0u, 0u, 0u};
-  bool have = true;
-  if (lane < kWarps) {
-    const uint64_t *q = &sm.cplan_raw[k][4 * lane];
-    have = cplan_of(q[0], q[1], q[2], q[3], tag, cp);
-  }
-  if (!__all_sync(full, have)) {
-    const uint64_t t0 = globaltimer();
-    uint32_t nap = 32;
-    while (!__all_sync(full, have)) {
-      if (!have) {
-        uint64_t w0, w1, w2, w3;
-        const uint64_t *q = p.cplan + (g.t * kWarps + lane) * 4;
-        ld_vol_v2(q, w0, w1);
-        ld_vol_v2(q + 2, w2, w3);
-        have = cplan_of(w0, w1, w2, w3, tag, cp);
-      }
-      if (__any_sync(full, globaltimer() - t0 > kWaitNs)) {
-        if (lane == 0) note_timeout(p, ERR_PLAN_TIMEOUT, TO_PLANNED, (uint32_t)g.t, (uint32_t)w);
-        cp = ChunkPlan{0ull, 0ull, 0, 0u, WA_NZ | WA_NEG | WA_POS, 0u};    // no plan: every chunk is split
-        break;
-      }
-      __nanosleep(nap);
-      nap = min(nap * 2u, 256u);
-    }
-    if (lane == 0) atomicAdd(&st[S_NS_VERDICT_WAIT], (unsigned)(globaltimer() - t0));
-  }
+  ChunkPre pre;
   uint32_t cmx, cflags;
-  CPROF_PT(0);                                        // prefix and plan words
-  const ChunkPre pre = chunk_verdict(g, w, ex, exab, cp, cmx, cflags);
-  CPROF_PT(1);                                        // the verdict
+  const int formed = *reinterpret_cast<const volatile int64_t *>(&sm.vtile[k]) == g.t + 1;
+  if (__shfl_sync(full, formed, 0)) {
+    // another warp formed the unit's verdicts
+    __threadfence_block();
+    pre = sm.vpre[k][w];
+    cmx = sm.vmx[k][w];
+    cflags = sm.vfl[k][w];
+  } else {
+    // ---- the plan words, copied in with the tile (else read again from
+    // global memory, bounded): the prefix before the tile and its chunk plans
+    const uint32_t tag = (p.epoch << 1) | 1u;
+    DF ex;
+    float exab;
+    if (g.t == g.first_tile) {
+      ex = df_from_double(p.s0s ? p.s0s[g.sum] : p.s0);
+      exab = fabsf(ex.hi);
+    } else {
+      const uint64_t A = sm.pre_raw[k][0], B = sm.pre_raw[k][1];
+      if ((uint32_t)(A & 0xFF) == tag && (uint32_t)B == tag) {
+        ex = status_sum(A);
+        exab = status_abs(B);
+      } else {
+        read_prefix(p, sm, g.t, ex, exab);
+      }
+    }
+    ChunkPlan cp{0ull, 0ull, 0, 0u, 0u, 0u};
+    bool have = true;
+    if (lane < kWarps) {
+      const uint64_t *q = &sm.cplan_raw[k][4 * lane];
+      have = cplan_of(q[0], q[1], q[2], q[3], tag, cp);
+    }
+    if (!__all_sync(full, have)) {
+      const uint64_t t0 = globaltimer();
+      uint32_t nap = 32;
+      while (!__all_sync(full, have)) {
+        if (!have) {
+          uint64_t w0, w1, w2, w3;
+          const uint64_t *q = p.cplan + (g.t * kWarps + lane) * 4;
+          ld_vol_v2(q, w0, w1);
+          ld_vol_v2(q + 2, w2, w3);
+          have = cplan_of(w0, w1, w2, w3, tag, cp);
+        }
+        if (__any_sync(full, globaltimer() - t0 > kWaitNs)) {
+          if (lane == 0) note_timeout(p, ERR_PLAN_TIMEOUT, TO_PLANNED, (uint32_t)g.t, (uint32_t)w);
+          cp = ChunkPlan{0ull, 0ull, 0, 0u, WA_NZ | WA_NEG | WA_POS, 0u};    // no plan: every chunk is split
+          break;
+        }
+        __nanosleep(nap);
+        nap = min(nap * 2u, 256u);
+      }
+      if (lane == 0) atomicAdd(&st[S_NS_VERDICT_WAIT], (unsigned)(globaltimer() - t0));
+    }
+    CPROF_PT(0);                                        // prefix and plan words
+    uint32_t lmx, lfl;
+    const ChunkPre lp = chunk_verdicts(g, ex, exab, cp, lmx, lfl);
+    if (lane < kWarps) { sm.vpre[k][lane] = lp; sm.vmx[k][lane] = lmx; sm.vfl[k][lane] = lfl; }
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      *reinterpret_cast<volatile int64_t *>(&sm.vtile[k]) = g.t + 1;
+    }
+    pre.c = DF{__shfl_sync(full, lp.c.hi, w), __shfl_sync(full, lp.c.lo, w)};
+    pre.ab = __shfl_sync(full, lp.ab, w);
+    pre.delta = __shfl_sync(full, lp.delta, w);
+    pre.e = __shfl_sync(full, lp.e, w);
+    pre.mode = __shfl_sync(full, lp.mode, w);
+    cmx = __shfl_sync(full, lmx, w);
+    cflags = __shfl_sync(full, lfl, w);
+    CPROF_PT(1);                                        // the verdict
+  }
   if (lane == 0) atomicAdd(&st[S_NS_VERDICT], (unsigned)(globaltimer() - tv));
   const int64_t cstart = g.start + (int64_t)w * kChunkTerms;
   const int cnt_chunk = (int)max((int64_t)0, min((int64_t)kChunkTerms, g.end - cstart));
@@ -3043,6 +3066,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2)
       sm.plan_cnt[s] = 0;
       sm.cnext[s] = 0u;
       sm.slow[s] = 0;
+      sm.vtile[s] = 0;
     }
     fence_mbar_init();
     if (blockIdx.x == 0) p.stats[S_T_START] = globaltimer();
