@@ -2534,28 +2534,66 @@ __device__ __noinline__ bool walk_fast(const Params &p, uint64_t &Sb0, Rec *seg,
   }
   uint64_t Sb = Sb0;
   unsigned na = 0, nt = 0;
-  for (int s = 0; s < nc; s++) {
-    const Rec c = seg[s];
-    const uint32_t kind = rec_kind(c.meta);
-    na++;
-    if (nonfinite(Sb)) { Sb = absorb(Sb, rec_flags(c.meta)); continue; }
-    if (kind == K_RUN) {
-      uint64_t T = Sb;
-      if (run_apply(T, rec_run(c), c.e) != APPLY_OK) return false;
-      Sb = T;
-    } else if (kind == K_TERMS) {
-      double S = bitsd(Sb);
-      const int n = (int)c.count;
-      if (n > 0) S = __dadd_rn(S, bitsd((uint64_t)c.inc));
-      if (n > 1) S = __dadd_rn(S, bitsd((uint64_t)c.lo));
-      if (n > 2) S = __dadd_rn(S, bitsd((uint64_t)c.hi));
-      Sb = dbits(S);
-      nt += (unsigned)n;
-    } else {                                            // K_FALLBACK
-      const uint32_t cs = code[s];
-      const TileGeo tg = tile_geo(p, (g + (cs >> 8)) * kGroupTiles + (cs & 0xFFu), ntiles);
-      Sb = add_terms(p, Sb, tg.start + rec_tstart(c.meta), c.count, st);
-      if (lane == 0) atomicAdd(&st[S_CHUNK_FALLBACK], 1u);
+  for (int base = 0; base < nc; base += 32) {
+    const int nb = min(32, nc - base);
+    // lane j prepares composite base + j for a positive normal sum: the
+    // exponent field it needs and, per parity of the significand m, its
+    // increment and the range of m that run_apply accepts -- so that the
+    // in-order step is a few operations and three shuffles
+    Rec cj = make_rec(run_empty(), kZeroE, K_RUN, 0, 0);
+    if (lane < nb) cj = seg[base + lane];
+    const uint32_t fj = rec_flags(cj.meta);
+    const bool simple = lane < nb && rec_kind(cj.meta) == K_RUN && !(fj & (F_ZERO | F_POISON));
+    const uint32_t Ej = (uint32_t)(cj.e + 1023);
+    const int64_t inc0 = cj.inc, inc1 = cj.inc + rec_d(cj.meta);
+    int64_t lo0, lo1, hi0, hi1;
+    if (fj & F_NONNEG) {                               // m + inc <= 2^53
+      lo0 = lo1 = kTwo52;
+      hi0 = kTwo53 - inc0;
+      hi1 = kTwo53 - inc1;
+    } else {                                           // m + lo - p >= 2^52 + 1, m + hi + p <= 2^53 - 1
+      lo0 = kTwo52 + 1 - cj.lo;
+      lo1 = kTwo52 + 2 - cj.lo;
+      hi0 = kTwo53 - 1 - cj.hi;
+      hi1 = kTwo53 - 2 - cj.hi;
+    }
+    const uint32_t simple_m = __ballot_sync(full, simple);
+    for (int sl = 0; sl < nb; sl++) {
+      const int s = base + sl;
+      const uint32_t Es = __shfl_sync(full, Ej, sl);
+      const uint64_t mag = Sb & ~kSignBit;
+      if (((simple_m >> sl) & 1u) && !(Sb >> 63) && (uint32_t)(mag >> 52) == Es) {
+        const int64_t m = (int64_t)((mag & kFracMask) | kHidden);
+        const bool odd = (m & 1) != 0;
+        const int64_t inc = __shfl_sync(full, odd ? inc1 : inc0, sl);
+        const int64_t L = __shfl_sync(full, odd ? lo1 : lo0, sl), H = __shfl_sync(full, odd ? hi1 : hi0, sl);
+        na++;
+        if (m < L || m > H) return false;
+        Sb = mag + (uint64_t)inc;                      // m stays in [2^52, 2^53]: the bits follow
+        continue;
+      }
+      const Rec c = seg[s];
+      const uint32_t kind = rec_kind(c.meta);
+      na++;
+      if (nonfinite(Sb)) { Sb = absorb(Sb, rec_flags(c.meta)); continue; }
+      if (kind == K_RUN) {
+        uint64_t T = Sb;
+        if (run_apply(T, rec_run(c), c.e) != APPLY_OK) return false;
+        Sb = T;
+      } else if (kind == K_TERMS) {
+        double S = bitsd(Sb);
+        const int n = (int)c.count;
+        if (n > 0) S = __dadd_rn(S, bitsd((uint64_t)c.inc));
+        if (n > 1) S = __dadd_rn(S, bitsd((uint64_t)c.lo));
+        if (n > 2) S = __dadd_rn(S, bitsd((uint64_t)c.hi));
+        Sb = dbits(S);
+        nt += (unsigned)n;
+      } else {                                            // K_FALLBACK
+        const uint32_t cs = code[s];
+        const TileGeo tg = tile_geo(p, (g + (cs >> 8)) * kGroupTiles + (cs & 0xFFu), ntiles);
+        Sb = add_terms(p, Sb, tg.start + rec_tstart(c.meta), c.count, st);
+        if (lane == 0) atomicAdd(&st[S_CHUNK_FALLBACK], 1u);
+      }
     }
   }
   Sb0 = Sb;
