@@ -25,7 +25,7 @@ constexpr int kWalkTiles = 1024;                // tile headers per walk batch (
 constexpr int kWalkElems = 1024;                // flat elements per walk batch (32 KB)
 constexpr int kMaxWalkers = 8;
 constexpr int kGroupTiles = 32;                 // tiles whose records one streaming CTA composes for the walk
-constexpr int kGroupSegs = 96;                  // records and segments a composed group holds (more: the walk takes its tiles)
+constexpr int kGroupSegs = 256;                 // segments a composed group holds (more: the walk takes its tiles)
 constexpr int kHeartbeats = 4096;               // CTAs with a heartbeat word (diagnostics of a stuck call)
 constexpr int kDbgAlloc = 65536;                // diagnostic words: checks, walk trace, profiling timeline
 

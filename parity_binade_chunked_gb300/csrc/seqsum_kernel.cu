@@ -495,8 +495,6 @@ struct Smem {
   uint32_t cnext[kStages];
   int slow[kStages];                // a chunk of the stage's unit is being split (it ends late)
   Rec stg[kWarps][kChunkSlots];     // a split chunk's items, staged in order before they are written out
-  Rec gel[kGroupSegs];              // control warp: a group's records in order, for its composition
-  uint16_t gtile[kGroupSegs];       // ... and the tile (in the group) of each
   int role;
   uint32_t barcnt[kWarps];          // walker and scanner: wide barriers passed per warp (heartbeat)
   unsigned int st[S_COUNT];         // per-CTA statistics of one call (32-bit: native shared atomics)
@@ -2272,17 +2270,19 @@ __device__ __noinline__ void walk_batch(const Params &p, Smem &sm, unsigned char
 // steps over 64 or 1024 chunks at a time"): the group's records are listed in
 // order (simple tile headers, the items of complex tiles), every maximal
 // stretch of runs of one binade is composed into one segment, and the walk
-// then only applies the segments.  A group with more than kGroupSegs records
-// is published "raw": the walk takes its tiles one by one.
+// then only applies the segments.  A group that composes into more than
+// kGroupSegs segments is published "raw": the walk takes its tiles one by one.
 
-// The group's records composed into segments (control warp).  Every header of
-// the group is published.
+// The group's records composed into segments (one warp).  Every header of the
+// group is published.
 __device__ __noinline__ void compose_group(const Params &p, Smem &sm, int64_t g, int nt, int64_t ntiles) {
   const int lane = threadIdx.x & 31;
   const unsigned full = 0xffffffffu;
   const uint32_t tag = (p.epoch << 1) | 1u;
   const int64_t t0 = g * kGroupTiles;
-  Rec h;
+  // lane c: tile c's header, its number of records (one, or a complex
+  // tile's items), whether it starts a sum, and its first record's index
+  Rec h = make_rec(run_empty(), kZeroE, K_RUN, 0, 0);
   int cnt = 0;
   bool okh = true, first = false;
   if (lane < nt) {
@@ -2307,56 +2307,69 @@ __device__ __noinline__ void compose_group(const Params &p, Smem &sm, int64_t g,
   }
   const int E = __shfl_sync(full, off, 31);
   off -= cnt;
-  const bool raw = !__all_sync(full, okh) || E > kGroupSegs;
-  if (!raw) {
-    // simple tiles: their header; complex tiles: their items, loaded by the
-    // whole warp at once (lane j the tile's item j, in chunk order)
-    const bool cplx = lane < nt && rec_kind(h.meta) == K_COMPLEX;
-    if (lane < nt && !cplx) {
-      sm.gel[off] = h;
-      sm.gtile[off] = (uint16_t)(lane | (first ? 0x100 : 0));   // 0x100: the record starts a sum
-    }
-    for (uint32_t m = __ballot_sync(full, cplx); m; m &= m - 1) {
-      const int c = __ffs(m) - 1;
-      const uint64_t packed = (uint64_t)__shfl_sync(full, h.inc, c);
-      const int base = __shfl_sync(full, off, c), n = __shfl_sync(full, cnt, c);
-      const bool fc = __shfl_sync(full, first, c);
-      const Rec *src = p.items + (t0 + c) * kTileSlots;
-      for (int j = lane; j < n; j += 32) {
-        // item j of the tile: the chunk whose running count passes j
-        int cc = 0, before = 0;
-        for (; cc < kWarps; cc++) {
-          const int nc = (int)((packed >> (kCountBits * cc)) & kCountMask);
-          if (j < before + nc) break;
-          before += nc;
-        }
-        Rec it = make_rec(run_empty(), kZeroE, K_RUN, 0, 0);
-        const Rec *q = src + cc * kChunkSlots + (j - before);
-        if (cc < kWarps && item_ok(p, q, 23)) it = ldcg_rec(q);
-        sm.gel[base + j] = it;
-        sm.gtile[base + j] = (uint16_t)(c | ((fc && j == 0) ? 0x100 : 0));
-      }
-    }
-  }
-  __syncwarp();
+  bool raw = !__all_sync(full, okh);
   int nseg = 0;
   if (!raw) {
-    // rounds of 32 records: a segmented scan of the runs, carried over
-    Run carry = run_empty();
-    bool carry_open = false;
-    int key_prev = 0;
-    bool alone_prev = true;
-    for (int rnd = 0; rnd * 32 < E; rnd++) {
-      const int j = rnd * 32 + lane;
+    // rounds of 32 records read straight from the headers and item areas
+    // (lane j record base + j), composed by a segmented scan; the last lane's
+    // open segment is carried into the next round, and emitted there when
+    // that round starts a new one
+    Run cv = run_empty();
+    Rec cx = h;
+    int ckey = 0;
+    bool calone = true, copen = false;
+    uint32_t ctile = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int j = base + lane;
       const bool valid = j < E;
-      Rec x = make_rec(run_empty(), kZeroE, K_RUN, 0, 0);
-      if (valid) x = sm.gel[j];
+      // the record's tile: the last tile whose first record is at or before j
+      int c = 0;
+#pragma unroll
+      for (int step = 16; step > 0; step >>= 1) {
+        const int cand = c + step;
+        const int oc = __shfl_sync(full, off, min(cand, 31));
+        if (cand < nt && oc <= j) c = cand;
+      }
+      const int oc = __shfl_sync(full, off, c);
+      Rec x;
+      x.inc = __shfl_sync(full, h.inc, c);
+      x.lo = __shfl_sync(full, h.lo, c);
+      x.hi = __shfl_sync(full, h.hi, c);
+      x.meta = __shfl_sync(full, h.meta, c);
+      x.e = (int16_t)__shfl_sync(full, (int)h.e, c);
+      x.count = (uint16_t)__shfl_sync(full, (int)h.count, c);
+      const bool fc = __shfl_sync(full, first, c);
+      if (valid && rec_kind(x.meta) == K_COMPLEX) {
+        // item j - oc of the tile: the chunk whose running count passes it
+        const uint64_t packed = (uint64_t)x.inc;
+        const int i = j - oc;
+        int cc = 0, before = 0;
+        for (; cc < kWarps; cc++) {
+          const int n = (int)((packed >> (kCountBits * cc)) & kCountMask);
+          if (i < before + n) break;
+          before += n;
+        }
+        x = make_rec(run_empty(), kZeroE, K_RUN, 0, 0);
+        const Rec *q = p.items + (t0 + c) * kTileSlots + cc * kChunkSlots + (i - before);
+        if (cc < kWarps && item_ok(p, q, 23)) x = ldcg_rec(q);
+      }
+      if (!valid) x = make_rec(run_empty(), kZeroE, K_RUN, 0, 0);
+      const uint32_t tinfo = (uint32_t)c | ((fc && j == oc) ? 0x100u : 0u);   // 0x100: the record starts a sum
       const int key = elem_key(x);
       const bool alone = elem_alone(x);
       int kp = __shfl_up_sync(full, key, 1);
       bool ap = __shfl_up_sync(full, alone, 1);
-      if (lane == 0) { kp = key_prev; ap = alone_prev; }
-      const bool head = valid && (j == 0 || alone || ap || key != kp || (sm.gtile[j] & 0x100));
+      if (lane == 0) { kp = ckey; ap = calone; }
+      const bool head = valid && (j == 0 || alone || ap || key != kp || (tinfo & 0x100u));
+      // the carried segment ends where this round starts a new one
+      const bool carry_ends = copen && __shfl_sync(full, head, 0);
+      if (carry_ends) {
+        if (lane == 0 && nseg < kGroupSegs) {
+          stcg_rec(p.grp_seg + g * kGroupSegs + nseg, calone ? cx : make_rec(cv, ckey, K_RUN, 0u, 0u));
+          p.grp_stile[g * kGroupSegs + nseg] = (uint16_t)(ctile & 0xFFu);
+        }
+        nseg++;
+      }
       Run v = rec_run(x);
       int f = head ? 1 : 0;
 #pragma unroll 1
@@ -2365,32 +2378,32 @@ __device__ __noinline__ void compose_group(const Params &p, Smem &sm, int64_t g,
         const int of = __shfl_up_sync(full, f, o);
         if (lane >= o) { if (!f) v = run_compose(ov, v); f |= of; }
       }
-      // the open segment of the previous round continues into this one's lanes before the first head
-      if (!f && valid && carry_open) v = run_compose(carry, v);
+      if (!f && valid && copen && !carry_ends) v = run_compose(cv, v);
+      // an end: the group's last record, or one followed by a head in this
+      // round (the round's last lane stays open until the next round)
       const uint32_t heads = __ballot_sync(full, head);
-      // an end: the last record, or one followed by a head (for the round's
-      // last lane, the next round's first record decides)
-      bool nexthead = (heads >> (lane + 1)) & 1u;
-      if (lane == 31 && valid && j < E - 1) {
-        const Rec xn = sm.gel[j + 1];
-        nexthead = elem_alone(xn) || alone || elem_key(xn) != key || (sm.gtile[j + 1] & 0x100);
-      }
-      const bool end = valid && (j == E - 1 || nexthead);
+      const bool end = valid && (j == E - 1 || (lane < 31 && ((heads >> (lane + 1)) & 1u)));
       const uint32_t ends = __ballot_sync(full, end);
-      const int s = nseg + __popc(ends & ((1u << lane) - 1u));
-      if (end && s < kGroupSegs) {
-        stcg_rec(p.grp_seg + g * kGroupSegs + s, alone ? x : make_rec(v, key, K_RUN, 0u, 0u));
-        p.grp_stile[g * kGroupSegs + s] = sm.gtile[j] & 0xFFu;
+      const int sidx = nseg + __popc(ends & ((1u << lane) - 1u));
+      if (end && sidx < kGroupSegs) {
+        stcg_rec(p.grp_seg + g * kGroupSegs + sidx, alone ? x : make_rec(v, key, K_RUN, 0u, 0u));
+        p.grp_stile[g * kGroupSegs + sidx] = (uint16_t)(tinfo & 0xFFu);
       }
       nseg += __popc(ends);
-      // carry the open segment (the last lane's composite when it did not end)
-      const bool open31 = __shfl_sync(full, valid && !end, 31);
-      const Run v31 = shfl_run<SH_IDX>(v, 31);
-      carry = v31;
-      carry_open = open31;
-      key_prev = __shfl_sync(full, key, 31);
-      alone_prev = __shfl_sync(full, alone, 31);
+      // carry the last lane's segment when it did not end
+      copen = __shfl_sync(full, valid && !end, 31);
+      cv = shfl_run<SH_IDX>(v, 31);
+      cx.inc = __shfl_sync(full, x.inc, 31);
+      cx.lo = __shfl_sync(full, x.lo, 31);
+      cx.hi = __shfl_sync(full, x.hi, 31);
+      cx.meta = __shfl_sync(full, x.meta, 31);
+      cx.e = (int16_t)__shfl_sync(full, (int)x.e, 31);
+      cx.count = (uint16_t)__shfl_sync(full, (int)x.count, 31);
+      ckey = __shfl_sync(full, key, 31);
+      calone = __shfl_sync(full, alone, 31);
+      ctile = __shfl_sync(full, tinfo, 31);
     }
+    raw = nseg > kGroupSegs;                           // more segments than a group holds: the walk takes its tiles
   }
   __syncwarp();
   if (lane == 0) {
