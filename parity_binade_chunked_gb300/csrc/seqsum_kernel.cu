@@ -448,7 +448,8 @@ struct ChunkPlan {
   uint32_t pad;
 };
 
-// The look-back warp's verdict on one chunk.
+// A run unit's verdict on one chunk: every term zero, every prefix in one
+// binade (clean), or the prefix range spanning a power of two (dirty).
 enum : int { CP_CLEAN = 0, CP_ZERO = 1, CP_DIRTY = 2 };
 struct ChunkPre {
   DF c;               // approximate running sum before the chunk
@@ -730,9 +731,9 @@ __device__ __forceinline__ bool mbar_wait_warp(const Params &p, uint64_t *bar, u
 #endif
 
 // The plan of chunk w of the stage's tile (by whichever compute warp claimed
-// it).  The warp that completes the tile's plan publishes the tile's
-// approximate sum (for a sum's first tile: s0 plus it, as an inclusive
-// prefix) and signals the look-back.
+// it).  The warp that completes the tile's plan publishes the chunk plans and
+// the tile's approximate sum (for a sum's first tile: s0 plus it, as an
+// inclusive prefix) for the scanner.
 __device__ __noinline__ void publish_tile_plan(const Params &p, Smem &sm, int k);
 __device__ __forceinline__ void load_lane(const Params &p, const unsigned char *stage, bool use_tma, int64_t row,
                                           int64_t lstart, int nv, int w, int lane, uint64_t *xs);
@@ -2773,13 +2774,12 @@ __device__ __noinline__ void walk_sum(const Params &p, Smem &sm, unsigned char *
 }
 
 // ---------------------------------------------------------------- the streaming loops
-// A streaming CTA has eight compute warps (warp w owns chunk w of every
-// tile), a control warp and a look-back warp.  Per stage four mbarriers:
-// full (the tile's copy landed; the tile is described in sm.geo), planned
-// (the tile's approximate sum is published), prefix (the look-back's
-// verdicts are in), done (the compute warps' records are in).  A compute
-// warp plans the next tile while the look-back of the current one is still
-// running, so no tile's plan waits for another tile's prefix.
+// A streaming CTA has eight compute warps and a control warp, and three
+// stages.  Per stage three mbarriers: full (the unit's copies landed and its
+// description -- sm.geo, the claim word -- is written), used (its chunks have
+// read their terms: the stage may take the next unit's copies) and done (its
+// chunks are finished: the control warp's epilogue).  A unit's eight chunks go
+// to whichever compute warps claim them.
 
 // The tile a ticket names, found by the control warp (a 32-way search over
 // the sums' first tiles for a batched call).
