@@ -207,6 +207,21 @@ def test_stream_and_repeats(sq):
         assert_same(o.item(), wants[k], f"repeat plane {k}")
 
 
+def test_group_too_fragmented_is_walked_tile_by_tile(sq):
+    """A running sum that crosses a power of two at every term (1.0, 0.5,
+    1.0, ...): every lane is dirty, every chunk overflows its item slots, and
+    each group of 32 tiles needs far more segments than a composed group
+    holds -- the walk takes those groups tile by tile, and the bits still
+    match the loop's."""
+    n = 32 * 4096 * 2
+    x = np.empty(n)
+    x[0] = 1.0
+    x[1::2] = -0.5
+    x[2::2] = 0.5
+    st = check(sq, x, 0.0, "alternating crossings")
+    assert st["walk_batches"] > 0, st
+
+
 # ------------------------------------------------------------ plan independence
 
 @pytest.mark.parametrize("mode", [1, 2, 3, 4, 5])
