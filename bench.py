@@ -162,6 +162,35 @@ def cpu_baseline(x, s0, budget_s):
                       f"(the sequential loop cannot use more cores without changing its bits)"}
 
 
+def cpu_batched_all_cores(x, offsets, s0s, reps=3):
+    """The oracle's loop for every sum of a batched workload, the sums spread
+    over all host cores (one sum per thread, largest first; each sum is still
+    one sequential loop, so its bits do not change).  Returns the baseline
+    record and the sums of the last pass."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    import oracle
+    oracle.lib()
+    n = len(offsets) - 1
+    order = sorted(range(n), key=lambda k: -(int(offsets[k + 1]) - int(offsets[k])))
+    cores = os.cpu_count() or 1
+    outs = np.empty(n)
+
+    def one(k):
+        outs[k] = oracle.seqsum(x[int(offsets[k]):int(offsets[k + 1])], float(s0s[k]))
+
+    times = []
+    with ThreadPoolExecutor(cores) as ex:
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            list(ex.map(one, order))
+            times.append(time.perf_counter() - t0)
+    best = min(times)
+    return {"value": len(x) / best / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"all {n} sums ({len(x)} terms), best of {reps} passes, one sum per thread "
+                      f"on {cores} host threads"}, outs
+
+
 def reference_arm(args, ws, rank):
     """The oracle as the reference arm: same metric, config and unit."""
     if rank != 0:
@@ -349,6 +378,11 @@ def main():
         extra["c4"] = {"n_terms": len(w4.x), "nsums": w4.nsums, "ms_per_step": m4,
                        "Gterms/s": len(w4.x) / (m4 * 1e-3) / 1e9,
                        "frac_hbm": 8 * len(w4.x) / (m4 * 1e-3) / 1e9 / peak, "parity_0ulp": bool(ok4)}
+        if not args.quick:
+            cpu4, cpu_outs = cpu_batched_all_cores(w4.x, w4.offsets, w4.s0)
+            cpu4["bits_match_oracle"] = bool(np.array_equal(
+                cpu_outs.view(np.uint64), oracle.seqsum_batched(w4.x, w4.offsets, w4.s0).view(np.uint64)))
+            extra["c4"]["cpu_baseline_all_cores"] = cpu4
         line["other_configs"] = extra
 
     if rank == 0:
