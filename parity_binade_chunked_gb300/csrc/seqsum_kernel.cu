@@ -172,19 +172,6 @@ __device__ __noinline__ void note_timeout(const Params &p, uint32_t err, uint32_
     p.ctr[C_TO_B] = b;
   }
 }
-// A bounded wait on an mbarrier phase; false on timeout.
-__device__ __forceinline__ bool mbar_wait(const Params &p, uint64_t *bar, uint32_t parity, uint32_t err,
-                                          uint32_t site, uint32_t a, uint32_t b) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitNs) {
-      note_timeout(p, err, site, a, b);
-      return false;
-    }
-  }
-  return true;
-}
 
 // One of the barrier's expected arrivals, made when every earlier cp.async
 // of this thread has completed.
@@ -197,7 +184,6 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // An atomic add with acquire and release semantics at GPU scope: the writes
