@@ -115,16 +115,16 @@ typedef struct {
   int64_t chunks_list;       /* chunks the plan split into several items */
   int64_t chunks_fallback;   /* chunks added term by term as a whole */
   int64_t lanes_dirty;       /* 16-term lanes the plan could not place */
-  int64_t walk_segments;     /* segments the in-order walk applied */
+  int64_t walk_segments;     /* composites the in-order walk applied (same-binade runs composed across groups) */
   int64_t runs_rejected;     /* runs the walk's exact check refused (fell back) */
   int64_t terms_added;       /* terms the walk added one by one in fp64 */
   int64_t items;             /* items written for split chunks */
   int64_t pool_overflow;     /* split chunks that found no room and fell back */
-  int64_t tiles_complex;     /* tiles the walk descended into */
+  int64_t tiles_complex;     /* tiles published with an item list (a split chunk, or chunks of several binades) */
   int64_t scan_windows;      /* windows of tile sums the plan's prefix scanner took */
-  int64_t walk_batches;      /* batches of tile headers the walk took */
+  int64_t walk_batches;      /* batches the walk took tile by tile (groups too fragmented to compose, or refused) */
   int64_t ns_tma_wait;       /* nanoseconds, summed over CTAs: compute warps waiting for a unit */
-  int64_t ns_prefix_wait;    /* ... run units waiting for the plan's prefix of their tile */
+  int64_t ns_prefix_wait;    /* not counted (always 0): a run unit's wait for a late prefix is in ns_verdict */
   int64_t ns_phase_a;        /* ... compute warps on plan units (the fixed-point sums of a tile) */
   int64_t ns_phase_b;        /* ... compute warps on run units (runs and items) */
   int64_t ns_walk_wait;      /* ... the walk waiting for tile headers */
@@ -132,7 +132,7 @@ typedef struct {
   int64_t torn_header_reads; /* tile-header reads that saw words of two publications (retried) */
   int64_t torn_status_reads; /* prefix reads that saw words of two publications (retried) */
   int64_t ns_scan;           /* the prefix scanner's time from its first to its last window */
-  int64_t ns_walk_count;     /* the walk's work by section: counting a batch's elements */
+  int64_t ns_walk_count;     /* the tile-by-tile walk's work by section: counting a batch's elements */
   int64_t ns_walk_gather;    /* ... gathering headers and items into one list */
   int64_t ns_walk_scan;      /* ... composing same-binade segments in parallel */
   int64_t ns_walk_serial;    /* ... the in-order pass over the segments */
@@ -143,7 +143,7 @@ typedef struct {
   int64_t ns_verdict;        /* nanoseconds, summed: run units forming their chunks' verdicts */
   int64_t ns_verdict_wait;   /* nanoseconds, summed: run units reading plan words not copied in time */
   int64_t ns_group_count;    /* nanoseconds, summed: control warps counting tiles in their groups */
-  int64_t ns_compose;        /* nanoseconds, summed: control warps composing groups for the walk */
+  int64_t ns_compose;        /* nanoseconds, summed: control warps composing the groups they completed */
   int64_t t_stream_ns;       /* latest call: kernel start to the last tile header */
   int64_t t_walk_tail_ns;    /* latest call: last tile header to the end of the walk */
   int64_t t_total_ns;        /* latest call: kernel start to the end of the walk */
