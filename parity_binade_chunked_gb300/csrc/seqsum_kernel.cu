@@ -44,6 +44,7 @@
 
 #include "binade_math.cuh"
 #include "seqsum_internal.cuh"
+#include "units.cuh"
 
 namespace sq {
 
@@ -2813,53 +2814,7 @@ __device__ __noinline__ StageGeo stage_geo(const Params &p, int64_t t) {
 // precedes the run of tile t + 1 by about `wave` tiles, so a run unit's prefix
 // is normally published long before it is needed, and its tile is still in L2.
 // Returns true for a plan unit.
-// Ticket order.  The run unit of tile t follows the plan unit of tile
-// lag(t): for the first kHeadTiles tiles that is tile P (about kHeadAfter
-// plan units in: early, so that the walk can start early, yet late enough
-// for their prefixes to be published); for the others, tile t + wave (a wave
-// behind, so that their prefixes are ready and their terms still in L2).
-// Every run unit's ticket is larger than those of the plan units it depends
-// on (its tile's and the tiles' before it).  Batched calls start no head
-// (every run a wave behind, unit_of_wave).  The plan of tile q has ticket
-// q + the runs placed before it; a ticket is decoded piece by piece.
-constexpr int64_t kHeadTiles = 128;
-constexpr int64_t kHeadAfter = 1024;
-__device__ __forceinline__ int64_t plan_ticket(int64_t q, int64_t H, int64_t W, int64_t P) {
-  return q + (q > P ? H : 0) + max((int64_t)0, q - W - H);
-}
-// Without a head: the plans of the first `wave` tiles, then a run and a plan
-// in turn, then the remaining runs (decoded directly).
-__device__ __forceinline__ bool unit_of_wave(int64_t u, int64_t ntiles, int64_t wave, int64_t &tile) {
-  const int64_t w = min(wave, ntiles);
-  if (u < w) { tile = u; return true; }
-  const int64_t v = u - w, rest = ntiles - w;
-  if (v < 2 * rest) {
-    tile = (v & 1) ? w + (v >> 1) : (v >> 1);
-    return (v & 1) != 0;
-  }
-  tile = rest + (v - 2 * rest);
-  return false;
-}
-__device__ __forceinline__ bool unit_of(int64_t u, int64_t ntiles, int64_t wave, int64_t head, int64_t &tile) {
-  if (head == 0) return unit_of_wave(u, ntiles, wave, tile);
-  const int64_t n = ntiles, H = min(head, n), W = min(wave, n);
-  const int64_t P = min(min(max(kHeadAfter, H - 1), n - 1), H + W - 1);
-  if (u <= P) { tile = u; return true; }               // the first plans
-  if (u <= P + H) { tile = u - P - 1; return false; }  // the head's runs
-  const int64_t tlast = plan_ticket(n - 1, H, W, P);
-  if (u < tlast) {
-    if (u - H <= H + W - 1) { tile = u - H; return true; }   // plans with no run between them
-    const int64_t v = u + W;                           // then a plan and a run a wave behind in turn
-    if ((v & 1) == 0) { tile = v >> 1; return true; }
-    tile = ((v - 1) >> 1) - W;
-    return false;
-  }
-  if (u == tlast) { tile = n - 1; return true; }
-  int64_t k = u - tlast - 1;                           // the runs after the last plan
-  if (P == n - 1) k -= H;
-  tile = max(H, n - 1 - W) + k;
-  return false;
-}
+// The ticket order (units.cuh): plan and run units of the tiles.
 
 // Claim words of the stages.  A unit's chunks go to whichever compute warps
 // claim them first, so that a chunk that takes long (a split) holds up only
