@@ -89,6 +89,22 @@ def dist_init():
     return ws, rank, local
 
 
+def job_rate(ms_local: float, terms_local: int, ws: int, device="cpu"):
+    """Whole-job rate of the replicas: the terms of every rank over the
+    slowest rank's time per step (the maximum over ranks).  Returns
+    (Gterms/s, ms).  With ws > 1 the process group must be initialised."""
+    ms, terms = float(ms_local), float(terms_local)
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        u = torch.tensor([terms], device=device, dtype=torch.float64)
+        dist.all_reduce(u, op=dist.ReduceOp.SUM)
+        ms, terms = t.item(), u.item()
+    return terms / (ms * 1e-3) / 1e9, ms
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -282,12 +298,7 @@ def main():
         t_wall = time.perf_counter() - t_wall0
     torch.cuda.synchronize()
     stats = sq.get_stats()
-    ms = sum(times) / len(times)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = t.item()
-    value = ws * n / (ms * 1e-3) / 1e9
+    value, ms = job_rate(sum(times) / len(times), n, ws, dev)
     peak, peak_src = peaks()
     achieved = 8.0 * n / (ms * 1e-3) / 1e9          # GB/s, algorithmic bytes (8 per term read once)
 
