@@ -254,6 +254,33 @@ def time_kernel(sq, torch, xd, s0, out, steps, warmup, flush, stream):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def read_peak(torch, xd, flush, stream, reps=20):
+    """A read-only streaming peak measured in the same run: torch's sum of the
+    same device plane (8 bytes per term read once), with the same L2 flush
+    before each step, timed with CUDA events on the stream (median GB/s).  A
+    reference for the roofline beside the measured copy peak; None if it
+    cannot be taken."""
+    try:
+        n = xd.numel()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                flush.fill_(1)
+                xd.sum()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            for a, b in ev:
+                flush.fill_(1)
+                a.record(stream)
+                xd.sum()
+                b.record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        return 8.0 * n / (ms * 1e-3) / 1e9
+    except Exception:
+        return None
+
+
 def main():
     args = parse()
     ws, rank, local = dist_init()
@@ -324,6 +351,8 @@ def main():
     e2e_ms = a.elapsed_time(b) / e2e_steps
     e2e_ok = bool(np.float64(hout.item()).view(np.uint64) == np.float64(want).view(np.uint64))
 
+    rpeak = read_peak(torch, xd, flush, stream)
+
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -335,7 +364,9 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": measured_traffic(args.config, args.height_mult),
                      "peak_source": peak_src, "algorithmic_bytes_per_launch": 8 * n,
-                     "traffic_source": "profiles/seqsum_kernel_%s_traffic.json (null if the kernel changed)" % args.config},
+                     "traffic_source": "profiles/seqsum_kernel_%s_traffic.json (null if the kernel changed)" % args.config,
+                     "read_peak_gbs": rpeak, "frac_of_read_peak": (achieved / rpeak) if rpeak else None,
+                     "read_peak_source": "torch sum of the same plane, L2 flushed before each step, this run"},
         "e2e": {"value": n / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": 8 * n,
                 "d2h_bytes_per_step": 8},
         "gpu_launches": args.steps,
