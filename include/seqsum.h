@@ -76,7 +76,9 @@ int seqsum_f64(const double *x, int64_t n, double s0, double *out, cudaStream_t 
  * on `stream`; make that first call before any stream capture.  Every call on
  * a device shares the one scratch: calls that overlap in time (on different
  * streams, or from several host threads) race and give wrong results; order
- * them.  seqsum_get_stats() does not cover these calls.
+ * them.  seqsum_get_stats() does not cover these calls, and the test hooks
+ * (seqsum_debug_set_plan, seqsum_debug_set_fault) do not reach them: a
+ * device-side failure (a bounded wait that gave up) shows only as NaN in *out.
  * Returns SEQSUM_OK, SEQSUM_EINVAL, SEQSUM_ECAPACITY (n too large; nothing is
  * enqueued) or SEQSUM_ECUDA. */
 int seqsum_f64_static(const double *x, int64_t n, double s0, double *out, cudaStream_t stream);
@@ -111,39 +113,16 @@ int seqsum_f64_batched_sized(const double *x, int64_t x_len, const int64_t *offs
  * recent call of this process. */
 typedef struct {
   int64_t tiles;             /* tiles of 4096 terms processed */
-  int64_t chunks_run;        /* 512-term chunks that became one run */
-  int64_t chunks_list;       /* chunks the plan split into several items */
-  int64_t chunks_fallback;   /* chunks added term by term as a whole */
-  int64_t lanes_dirty;       /* 16-term lanes the plan could not place */
-  int64_t walk_segments;     /* composites the in-order walk applied (same-binade runs composed across groups) */
-  int64_t runs_rejected;     /* runs the walk's exact check refused (fell back) */
-  int64_t terms_added;       /* terms the walk added one by one in fp64 */
-  int64_t items;             /* items written for split chunks */
-  int64_t pool_overflow;     /* split chunks that found no room and fell back */
-  int64_t tiles_complex;     /* tiles published with an item list (a split chunk, or chunks of several binades) */
-  int64_t scan_windows;      /* windows of tile sums the plan's prefix scanner took */
-  int64_t walk_batches;      /* batches the walk took tile by tile (groups too fragmented to compose, or refused) */
-  int64_t ns_tma_wait;       /* nanoseconds, summed over CTAs: compute warps waiting for a unit */
-  int64_t ns_prefix_wait;    /* not counted (always 0): a run unit's wait for a late prefix is in ns_verdict */
-  int64_t ns_phase_a;        /* ... compute warps on plan units (the fixed-point sums of a tile) */
-  int64_t ns_phase_b;        /* ... compute warps on run units (runs and items) */
-  int64_t ns_walk_wait;      /* ... the walk waiting for tile headers */
-  int64_t ns_walk_work;      /* ... the walk working */
-  int64_t torn_header_reads; /* tile-header reads that saw words of two publications (retried) */
-  int64_t torn_status_reads; /* prefix reads that saw words of two publications (retried) */
-  int64_t ns_scan;           /* the prefix scanner's time from its first to its last window */
-  int64_t ns_walk_count;     /* the tile-by-tile walk's work by section: counting a batch's elements */
-  int64_t ns_walk_gather;    /* ... gathering headers and items into one list */
-  int64_t ns_walk_scan;      /* ... composing same-binade segments in parallel */
-  int64_t ns_walk_serial;    /* ... the in-order pass over the segments */
-  int64_t ns_walk_adds;      /* ... of which term-by-term fp64 adds */
-  int64_t chunks_dirty;      /* chunks whose prefix range spans two binades (placed lane by lane) */
-  int64_t ns_ctrl_wait;      /* nanoseconds, summed: control warps waiting for their compute warps */
-  int64_t ns_scan_wait;      /* nanoseconds: the prefix scanner waiting for tiles' sums */
-  int64_t ns_verdict;        /* nanoseconds, summed: run units forming their chunks' verdicts */
-  int64_t ns_verdict_wait;   /* nanoseconds, summed: run units reading plan words not copied in time */
-  int64_t ns_group_count;    /* nanoseconds, summed: control warps counting tiles in their groups */
-  int64_t ns_compose;        /* nanoseconds, summed: control warps composing the groups they completed */
+  int64_t tiles_complex;     /* tiles published as a list of items (rows of several binades, raw rows, ties) */
+  int64_t tiles_overflow;    /* tiles whose items did not fit their area (the walk read their terms) */
+  int64_t lanes_raw;         /* 16-term rows whose plan range crossed a power of two (added by the walk) */
+  int64_t lanes_raw2;        /* ... of which published with prefix tables for one crossing */
+  int64_t lanes_tie;         /* rows with a tie, composed in order by the even/odd rule */
+  int64_t walk_batches;      /* batches of tile headers the walk read */
+  int64_t walk_segments;     /* composites the walk applied (same-binade runs composed across tiles) */
+  int64_t runs_rejected;     /* runs the walk's exact check refused (their terms were added one by one) */
+  int64_t terms_dadd;        /* terms the walk added with a hardware fp64 add */
+  int64_t raw_rounds;        /* warp rounds of the walk's term-by-term resolution */
   int64_t t_stream_ns;       /* latest call: kernel start to the last tile header */
   int64_t t_walk_tail_ns;    /* latest call: last tile header to the end of the walk */
   int64_t t_total_ns;        /* latest call: kernel start to the end of the walk */
@@ -152,9 +131,10 @@ typedef struct {
   int32_t check_site;        /* self-checking builds: first failed check (0: none) */
   int32_t check_pad;
   int64_t check_value;       /* self-checking builds: the value that failed it */
-  int32_t timeout_site;      /* first bounded device wait that gave up (0: none) and its context */
+  int32_t timeout_site;      /* first bounded device wait that gave up (0: none): 1 plan look-back, 2 TMA copy,
+                                3 walk header */
   int32_t timeout_pad;
-  int64_t timeout_a;
+  int64_t timeout_a;         /* its context: the tile */
   int64_t timeout_b;
 } seqsum_stats;
 
@@ -178,17 +158,22 @@ void seqsum_release_workspace(void);
  * plan cannot make the result wrong, only slower.  Returns the old mode. */
 int seqsum_debug_set_plan(int mode);
 
-/* Test hook: copies up to 65536 diagnostic words that self-checking and
- * profiling builds of the library record (a trace of the walk, a timeline of
- * the units; zeros otherwise) and clears them. */
+/* Test hook: copies up to 4096 diagnostic words that self-checking builds
+ * of the library record (zeros otherwise) and clears them. */
 int seqsum_debug_read(unsigned long long *out, int n);
 
-/* Diagnostics of a call that does not finish: copies the device counters of
- * the most recent call's workspace into out[0..16) and, per warp (index
- * CTA * 9 + warp: 8 compute warps, then the control warp), a heartbeat word into out[16..n) (role << 56 | what it
- * waits for or does << 48 | where).  It takes no lock and reads on a stream of its own, so it can run
- * while another thread waits on that call.  16 <= n <= 16 + 4096. */
-int seqsum_debug_heartbeat(unsigned long long *out, int n);
+/* Diagnostics of a call that does not finish: copies the first n (1..16)
+ * device counters of the most recent call's workspace (tickets, roles, exits,
+ * error bits, tag) into out.  It takes no lock and reads on a stream of its
+ * own, so it can run while another thread waits on that call. */
+int seqsum_debug_counters(unsigned long long *out, int n);
+
+/* Test hook for the bounded waits: mode 1 withholds the header of tile `arg`
+ * in later calls (the walk's wait for it must give up, write NaN and report
+ * SEQSUM_ETIMEOUT, site 3); mode 0 restores normal calls.  wait_ns > 0 sets
+ * the limit of every bounded device wait of later calls (0: the default, 2 s).
+ * Returns SEQSUM_OK or SEQSUM_EINVAL. */
+int seqsum_debug_set_fault(int mode, int64_t arg, int64_t wait_ns);
 
 /* Library version string. */
 const char *seqsum_version(void);

@@ -18,7 +18,8 @@ import threading
 from . import build as _build
 
 __all__ = ["seqsum_f64", "seqsum_f64_static", "seqsum_f64_batched", "seqsum_f64_batched_sized", "get_stats",
-           "debug_set_plan", "release_workspace", "version", "lib", "SeqsumError"]
+           "debug_set_plan", "debug_set_fault", "debug_counters", "release_workspace", "version", "lib",
+           "SeqsumError"]
 
 _lock = threading.Lock()
 _lib = None
@@ -30,11 +31,9 @@ class SeqsumError(RuntimeError):
 
 class _Stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
-        "tiles", "chunks_run", "chunks_list", "chunks_fallback", "lanes_dirty", "walk_segments",
-        "runs_rejected", "terms_added", "items", "pool_overflow", "tiles_complex",
-        "scan_windows", "walk_batches", "ns_tma_wait", "ns_prefix_wait", "ns_phase_a", "ns_phase_b",
-        "ns_walk_wait", "ns_walk_work", "torn_header_reads", "torn_status_reads", "ns_scan", "ns_walk_count", "ns_walk_gather",
-        "ns_walk_scan", "ns_walk_serial", "ns_walk_adds", "chunks_dirty", "ns_ctrl_wait", "ns_scan_wait", "ns_verdict", "ns_verdict_wait", "ns_group_count", "ns_compose", "t_stream_ns", "t_walk_tail_ns", "t_total_ns")] + [
+        "tiles", "tiles_complex", "tiles_overflow", "lanes_raw", "lanes_raw2", "lanes_tie", "walk_batches",
+        "walk_segments", "runs_rejected", "terms_dadd", "raw_rounds", "t_stream_ns", "t_walk_tail_ns",
+        "t_total_ns")] + [
         ("device_status", ctypes.c_int32), ("device_error_bits", ctypes.c_int32),
         ("check_site", ctypes.c_int32), ("check_pad", ctypes.c_int32), ("check_value", ctypes.c_int64),
         ("timeout_site", ctypes.c_int32), ("timeout_pad", ctypes.c_int32), ("timeout_a", ctypes.c_int64),
@@ -73,8 +72,10 @@ def lib():
             L.seqsum_debug_set_plan.restype = ctypes.c_int
             L.seqsum_debug_read.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), ctypes.c_int]
             L.seqsum_debug_read.restype = ctypes.c_int
-            L.seqsum_debug_heartbeat.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), ctypes.c_int]
-            L.seqsum_debug_heartbeat.restype = ctypes.c_int
+            L.seqsum_debug_counters.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), ctypes.c_int]
+            L.seqsum_debug_counters.restype = ctypes.c_int
+            L.seqsum_debug_set_fault.argtypes = [ctypes.c_int, i64, i64]
+            L.seqsum_debug_set_fault.restype = ctypes.c_int
             L.seqsum_version.argtypes = []
             L.seqsum_version.restype = ctypes.c_char_p
             _lib = L
@@ -194,19 +195,22 @@ def debug_read(n: int = 64) -> list:
     return list(buf)
 
 
-_BLOCK_WARPS = 9   # warps per CTA: 8 compute warps and a control warp
+def debug_set_fault(mode: int, arg: int = 0, wait_ns: int = 0) -> None:
+    """Test hook for the bounded device waits: mode 1 withholds the header of
+    tile `arg` in later calls; wait_ns > 0 shortens every wait (0: 2 s)."""
+    _check(lib().seqsum_debug_set_fault(int(mode), int(arg), int(wait_ns)))
 
 
-def debug_heartbeat(nctas: int = 320) -> dict:
-    """Counters and per-warp heartbeats (cta, warp, role, what, where) of the
-    most recent call, read without waiting for it (diagnostics of a call that
-    does not finish)."""
-    n = 16 + min(_BLOCK_WARPS * int(nctas), 4096)
-    buf = (ctypes.c_ulonglong * n)()
-    _check(lib().seqsum_debug_heartbeat(buf, n))
-    words = list(buf)
-    beats = [(i // _BLOCK_WARPS, i % _BLOCK_WARPS, w >> 56, (w >> 48) & 0xFF, w & 0xFFFFFFFFFFFF) for i, w in enumerate(words[16:]) if w]
-    return {"counters": words[:16], "beats": beats}
+_COUNTER_NAMES = ["ticket", "role", "exit", "sum_ticket", "err", "epoch", "ntiles", "skip", "check_site",
+                  "check_lo", "check_hi", "timeout_site", "timeout_a", "timeout_b", "pad14", "pad15"]
+
+
+def debug_counters() -> dict:
+    """The device counters of the most recent call, read without waiting for
+    it (diagnostics of a call that does not finish)."""
+    buf = (ctypes.c_ulonglong * 16)()
+    _check(lib().seqsum_debug_counters(buf, 16))
+    return dict(zip(_COUNTER_NAMES, list(buf)))
 
 
 def release_workspace():

@@ -20,7 +20,7 @@ LIB = os.path.join(BUILD, "libseqsum.so")
 CHECK_BUILD = os.path.join(BUILD, "check")
 CHECK_LIB = os.path.join(CHECK_BUILD, "libseqsum.so")
 SOURCES = ["seqsum_kernel.cu", "seqsum_api.cu", "seqsum_static.cu"]
-HEADERS = ["binade_math.cuh", "seqsum_internal.cuh", "units.cuh"]
+HEADERS = ["binade_math.cuh", "seqsum_internal.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "--fmad=false", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-fno-fast-math", "-Xcompiler", "-ffp-contract=off",

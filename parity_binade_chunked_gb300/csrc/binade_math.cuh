@@ -183,6 +183,31 @@ SQ_HD void term_inc_fast(uint32_t hi, uint32_t lo, int c, uint64_t &r, bool &tie
   r = f + (up ? 1u : 0u);
 }
 
+// The magnitude increment of one term rounded half up, with a tie detector,
+// for the streaming pass: the same two multiplies as term_inc_fast, but the
+// round-up decision is the top remainder bit alone and the tie test folds
+// into one word.  hi/lo are the term's halves (the sign bit is ignored), c =
+// 64 - (e + 1023) with e >= -969.  Returns r = round-half-up(|x| / 2^(e-52));
+// `t` is zero exactly when the shifted-out bits are one half (a tie, where
+// the correct increment depends on the parity and is r or r - 1).  When
+// |x| >= 2^e the result is meaningless and the caller flags the term.
+SQ_HD uint64_t term_mag_halfup(uint32_t hi, uint32_t lo, int c, uint32_t &t) {
+  const uint32_t E = (hi >> 20) & 0x7FFu;
+  const uint32_t mh = (hi & 0xFFFFFu) | 0x100000u;
+  int j = (int)E + c;
+  j = j < 0 ? 0 : j;
+  const uint32_t w = 1u << (j & 31);
+  const bool J = j >= 32;
+  const uint64_t A = (uint64_t)lo * w, B = (uint64_t)mh * w;
+  const uint32_t A0 = (uint32_t)A, A1 = (uint32_t)(A >> 32), B0 = (uint32_t)B, B1 = (uint32_t)(B >> 32);
+  const uint32_t P = B0 | A1;
+  const uint32_t Rh = J ? A0 : P;
+  const uint32_t X = J ? 0u : A0;
+  t = (Rh ^ 0x80000000u) | X;
+  const uint64_t f = J ? (((uint64_t)B1 << 32) | P) : (uint64_t)B1;
+  return f + (Rh >> 31);
+}
+
 SQ_HD int64_t sq_min(int64_t a, int64_t b) { return a < b ? a : b; }
 SQ_HD int64_t sq_max(int64_t a, int64_t b) { return a > b ? a : b; }
 

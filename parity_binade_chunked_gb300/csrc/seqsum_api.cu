@@ -24,20 +24,13 @@ struct Workspace {
   int device = 0;
   cudaStream_t stream = nullptr;
   int64_t cap_tiles = 0, cap_sums = 0;
-  uint64_t *status = nullptr;        // the plan's prefix words, 2 per tile
-  uint64_t *cplan = nullptr;         // the plan's chunk sums, 4 words per chunk
-  uint32_t *grp_cnt = nullptr;       // composed groups of tiles: counters, headers, segments
-  uint64_t *grp_hdr = nullptr;
-  Rec *grp_seg = nullptr;
-  uint16_t *grp_stile = nullptr;
+  uint4 *status = nullptr;           // the plan's per-tile words
   Rec *hdr = nullptr;                // one header per tile
-  Rec *items = nullptr;              // kTileSlots items per tile
+  Rec *items = nullptr;              // kItemSlots item slots per tile
   uint32_t *ctr = nullptr;
   int64_t *tile_begin = nullptr;
   unsigned long long *stats = nullptr;
   unsigned long long *dbg = nullptr;
-  unsigned long long *hb = nullptr;  // heartbeat words
-  uint32_t epoch = 0;
   int64_t *h_pin = nullptr;          // pinned bounce for the batched size read-back
   // tensor map cache
   const void *tm_ptr = nullptr;
@@ -50,9 +43,11 @@ std::map<std::pair<int, cudaStream_t>, Workspace *> g_ws;
 Workspace *g_last = nullptr;
 int g_last_cuda = 0;
 int g_plan_mode = 0;
+int g_fault_mode = 0;
+int64_t g_fault_arg = 0;
+uint64_t g_wait_ns = 2000000000ull;   // every bounded device wait gives up after 2 s
 int g_blocks_per_sm = 0;
 int g_num_sms[64] = {0};
-int64_t g_wave = 0;                  // tiles plan units run ahead of run units (0: not yet read)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int cuda_fail(cudaError_t e) {
@@ -62,19 +57,10 @@ int cuda_fail(cudaError_t e) {
 
 void ws_free(Workspace *w) {
   cudaFree(w->status);
-  cudaFree(w->cplan);
-  cudaFree(w->grp_cnt);
-  cudaFree(w->grp_hdr);
-  cudaFree(w->grp_seg);
-  cudaFree(w->grp_stile);
-  w->grp_cnt = nullptr;
-  w->grp_hdr = nullptr;
-  w->grp_seg = nullptr;
-  w->grp_stile = nullptr;
   cudaFree(w->hdr);
   cudaFree(w->items);
   cudaFree(w->tile_begin);
-  w->status = w->cplan = nullptr;
+  w->status = nullptr;
   w->hdr = w->items = nullptr;
   w->tile_begin = nullptr;
   w->cap_tiles = w->cap_sums = 0;
@@ -95,10 +81,8 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
     if ((e = cudaMalloc(&w->stats, sq::S_COUNT * sizeof(unsigned long long))) != cudaSuccess)
       return cuda_fail(e);
     if ((e = cudaMallocHost(&w->h_pin, 2 * sizeof(int64_t))) != cudaSuccess) return cuda_fail(e);
-    if ((e = cudaMalloc(&w->dbg, sq::kDbgAlloc * sizeof(unsigned long long))) != cudaSuccess) return cuda_fail(e);
-    if ((e = cudaMalloc(&w->hb, sq::kHeartbeats * sizeof(unsigned long long))) != cudaSuccess) return cuda_fail(e);
-    cudaMemset(w->hb, 0, sq::kHeartbeats * sizeof(unsigned long long));
-    cudaMemset(w->dbg, 0, sq::kDbgAlloc * sizeof(unsigned long long));
+    if ((e = cudaMalloc(&w->dbg, sq::kDbgWords * sizeof(unsigned long long))) != cudaSuccess) return cuda_fail(e);
+    cudaMemset(w->dbg, 0, sq::kDbgWords * sizeof(unsigned long long));
     cudaMemset(w->ctr, 0, sq::C_COUNT * sizeof(uint32_t));
     cudaMemset(w->stats, 0, sq::S_COUNT * sizeof(unsigned long long));
   }
@@ -108,27 +92,20 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
     const int64_t ct = tiles > w->cap_tiles ? tiles + tiles / 4 + 16 : w->cap_tiles;
     const int64_t cs = sums > w->cap_sums ? sums + 16 : w->cap_sums;
     ws_free(w);
-    if (cudaMalloc(&w->status, ct * 2 * sizeof(uint64_t)) != cudaSuccess ||
-        cudaMalloc(&w->cplan, ct * sq::kWarps * 4 * sizeof(uint64_t)) != cudaSuccess ||
-        cudaMalloc(&w->grp_cnt, (ct / sq::kGroupTiles + 1) * sizeof(uint32_t)) != cudaSuccess ||
-        cudaMalloc(&w->grp_hdr, (ct / sq::kGroupTiles + 1) * sizeof(uint64_t)) != cudaSuccess ||
-        cudaMalloc(&w->grp_seg, (ct / sq::kGroupTiles + 1) * sq::kGroupSegs * sizeof(Rec)) != cudaSuccess ||
-        cudaMalloc(&w->grp_stile, (ct / sq::kGroupTiles + 1) * sq::kGroupSegs * sizeof(uint16_t)) != cudaSuccess ||
+    if (cudaMalloc(&w->status, ct * sizeof(uint4)) != cudaSuccess ||
         cudaMalloc(&w->hdr, ct * sizeof(Rec)) != cudaSuccess ||
-        cudaMalloc(&w->items, ct * sq::kTileSlots * sizeof(Rec)) != cudaSuccess ||
+        cudaMalloc(&w->items, ct * sq::kItemSlots * sizeof(Rec)) != cudaSuccess ||
         cudaMalloc(&w->tile_begin, (cs + 1) * sizeof(int64_t)) != cudaSuccess) {
       ws_free(w);
       g_last_cuda = (int)cudaGetLastError();
       return SEQSUM_ENOMEM;
     }
-    cudaMemset(w->status, 0, ct * 2 * sizeof(uint64_t));
-    cudaMemset(w->cplan, 0, ct * sq::kWarps * 4 * sizeof(uint64_t));
-    cudaMemset(w->grp_cnt, 0, (ct / sq::kGroupTiles + 1) * sizeof(uint32_t));
-    cudaMemset(w->grp_hdr, 0, (ct / sq::kGroupTiles + 1) * sizeof(uint64_t));
+    // fresh tagged words and a fresh tag sequence (the counters' epoch word)
+    cudaMemset(w->status, 0, ct * sizeof(uint4));
     cudaMemset(w->hdr, 0, ct * sizeof(Rec));
+    cudaMemset(w->ctr, 0, sq::C_COUNT * sizeof(uint32_t));
     w->cap_tiles = ct;
     w->cap_sums = cs;
-    w->epoch = 0;
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e);
   }
   *out = w;
@@ -143,15 +120,7 @@ int ensure_device_info() {
     cudaError_t e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  if (g_blocks_per_sm == 0) g_blocks_per_sm = sq::kernel_max_blocks_per_sm();
-  if (g_wave == 0) {
-    // 2048 tiles (64 MB): far more than the units a full grid holds in
-    // flight, so the scanner is well ahead of the run units, and little
-    // enough that a tile is still in L2 (129 MB) when its run unit reads it.
-    g_wave = 2048;
-    const char *ev = getenv("SEQSUM_WAVE");
-    if (ev && atoll(ev) > 0) g_wave = atoll(ev);
-  }
+  if (g_blocks_per_sm == 0) g_blocks_per_sm = sq::kernel_blocks_per_sm();
   if (!g_encode) {
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -162,21 +131,6 @@ int ensure_device_info() {
   return SEQSUM_OK;
 }
 
-// Next epoch for the tags (1..127); every tagged word (the plan's sums and
-// prefixes, the tile headers) is cleared whenever the tag wraps, so a stale
-// word can never carry a current tag.
-void next_epoch(Workspace *w, cudaStream_t stream) {
-  w->epoch++;
-  if (w->epoch > 127) {
-    cudaMemsetAsync(w->status, 0, w->cap_tiles * 2 * sizeof(uint64_t), stream);
-    cudaMemsetAsync(w->cplan, 0, w->cap_tiles * sq::kWarps * 4 * sizeof(uint64_t), stream);
-    cudaMemsetAsync(w->grp_cnt, 0, (w->cap_tiles / sq::kGroupTiles + 1) * sizeof(uint32_t), stream);
-    cudaMemsetAsync(w->grp_hdr, 0, (w->cap_tiles / sq::kGroupTiles + 1) * sizeof(uint64_t), stream);
-    cudaMemsetAsync(w->hdr, 0, w->cap_tiles * sizeof(Rec), stream);
-    w->epoch = 1;
-  }
-}
-
 // The 2-D view [rows][16] of the plane, 128-byte swizzled boxes of 256 rows.
 // Returns the rows covered (0 when x is not 16-byte aligned: no TMA).
 int64_t tensor_map(Workspace *w, const double *x, int64_t n_total) {
@@ -185,12 +139,16 @@ int64_t tensor_map(Workspace *w, const double *x, int64_t n_total) {
   if (w->tm_ptr == x && w->tm_rows == rows) return rows;
   cuuint64_t dims[2] = {16, (cuuint64_t)rows};
   cuuint64_t strides[1] = {16 * sizeof(double)};
-  cuuint32_t box[2] = {16, 256};
+  cuuint32_t box[2] = {16, (cuuint32_t)sq::kTileRows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(&w->tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT64, 2, const_cast<double *>(x), dims, strides, box,
                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) { w->tm_ptr = nullptr; w->tm_rows = -1; return 0; }
+  if (r != CUDA_SUCCESS) {
+    w->tm_ptr = nullptr;
+    w->tm_rows = -1;
+    return 0;
+  }
   w->tm_ptr = x;
   w->tm_rows = rows;
   return rows;
@@ -198,11 +156,6 @@ int64_t tensor_map(Workspace *w, const double *x, int64_t n_total) {
 
 void fill_ws(Params &p, Workspace *w) {
   p.status = w->status;
-  p.cplan = w->cplan;
-  p.grp_cnt = w->grp_cnt;
-  p.grp_hdr = w->grp_hdr;
-  p.grp_seg = w->grp_seg;
-  p.grp_stile = w->grp_stile;
   p.hdr = w->hdr;
   p.items = w->items;
   p.ctr = w->ctr;
@@ -210,7 +163,10 @@ void fill_ws(Params &p, Workspace *w) {
   p.cap_tiles = w->cap_tiles;
   p.stats = w->stats;
   p.dbg = w->dbg;
-  p.hb = w->hb;
+  p.plan_mode = g_plan_mode;
+  p.fault_mode = g_fault_mode;
+  p.fault_arg = g_fault_arg;
+  p.wait_ns = g_wait_ns;
 }
 
 int batched_impl(const double *x, int64_t x_len, const int64_t *offsets, int32_t nsums, const double *s0s,
@@ -236,31 +192,29 @@ int batched_impl(const double *x, int64_t x_len, const int64_t *offsets, int32_t
   }
   if (x_len < 0) return SEQSUM_EINVAL;
   if (x_len > 0 && !x) return SEQSUM_EINVAL;
-  const int64_t tiles = x_len / sq::kTileTerms + nsums + 1;
+  // every sum adds at most two tiles beyond its share of x (row alignment, a ragged end)
+  const int64_t tiles = x_len / sq::kTileTerms + 2 * (int64_t)nsums + 1;
   rc = get_ws(stream, tiles, nsums, &w);
   if (rc) return rc;
-  next_epoch(w, stream);
   Params p;
   memset(&p, 0, sizeof p);
   p.x = x;
-  p.n = x_len;
+  p.x_len = x_len;
   p.offsets = offsets;
   p.s0s = s0s;
   p.outs = outs;
   p.ntiles = -1;
   p.nsums = nsums;
-  p.epoch = w->epoch;
-  p.plan_mode = g_plan_mode;
   fill_ws(p, w);
   p.tma_rows = tensor_map(w, x, x_len);
   p.nwalkers = nsums < sq::kMaxWalkers ? nsums : sq::kMaxWalkers;
-  p.wave = g_wave;
   cudaError_t e = sq::launch_setup(p, stream);
   if (e != cudaSuccess) return cuda_fail(e);
-  int grid = g_num_sms[w->device] * g_blocks_per_sm;
-  if (grid < p.nwalkers + 2) grid = p.nwalkers + 2;     // walkers, the scanner, at least one streamer
+  int64_t grid = (int64_t)g_num_sms[w->device] * g_blocks_per_sm;
+  if (p.nwalkers + tiles < grid) grid = p.nwalkers + tiles;
+  if (grid < p.nwalkers + 1) grid = p.nwalkers + 1;
   static CUtensorMap dummy;
-  e = sq::launch_seqsum(p, p.tma_rows ? &w->tmap : &dummy, grid, stream);
+  e = sq::launch_seqsum(p, p.tma_rows ? &w->tmap : &dummy, (int)grid, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   g_last = w;
   return SEQSUM_OK;
@@ -279,24 +233,21 @@ int seqsum_f64(const double *x, int64_t n, double s0, double *out, cudaStream_t 
   Workspace *w = nullptr;
   rc = get_ws(stream, tiles > 0 ? tiles : 1, 1, &w);
   if (rc) return rc;
-  next_epoch(w, stream);
   Params p;
   memset(&p, 0, sizeof p);
   p.x = x;
+  p.x_len = n;
   p.outs = out;
   p.s0 = s0;
   p.n = n;
   p.ntiles = tiles;
   p.nsums = 1;
-  p.epoch = w->epoch;
-  p.plan_mode = g_plan_mode;
   fill_ws(p, w);
   p.tma_rows = n > 0 ? tensor_map(w, x, n) : 0;
   p.nwalkers = 1;
-  p.wave = g_wave;
   const int dev = w->device;
   int64_t grid = (int64_t)g_num_sms[dev] * g_blocks_per_sm;
-  if (2 * tiles + 2 < grid) grid = 2 * tiles + 2;     // the walker, the scanner, one streamer per unit
+  if (tiles + 1 < grid) grid = tiles + 1;     // the walker and at most one streaming CTA per tile
   static CUtensorMap dummy;
   cudaError_t e = sq::launch_seqsum(p, p.tma_rows ? &w->tmap : &dummy, (int)grid, stream);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -333,55 +284,32 @@ int seqsum_get_stats(seqsum_stats *st) {
   if (e == cudaSuccess && err) e = cudaMemset(w->ctr + sq::C_ERR, 0, sizeof(uint32_t));
   if (e == cudaSuccess && c[sq::C_CHECK_SITE]) e = cudaMemset(w->ctr + sq::C_CHECK_SITE, 0, 3 * sizeof(uint32_t));
   if (e == cudaSuccess && c[sq::C_TO_SITE]) e = cudaMemset(w->ctr + sq::C_TO_SITE, 0, 3 * sizeof(uint32_t));
+  cudaSetDevice(prev);
+  if (e != cudaSuccess) return cuda_fail(e);
   st->timeout_site = (int32_t)c[sq::C_TO_SITE];
   st->timeout_a = (int64_t)c[sq::C_TO_A];
   st->timeout_b = (int64_t)c[sq::C_TO_B];
   st->check_site = (int32_t)c[sq::C_CHECK_SITE];
   st->check_value = (int64_t)(((uint64_t)c[sq::C_CHECK_HI] << 32) | c[sq::C_CHECK_LO]);
-  cudaSetDevice(prev);
-  if (e != cudaSuccess) return cuda_fail(e);
   st->tiles = (int64_t)s[sq::S_TILES];
-  st->chunks_run = (int64_t)s[sq::S_CHUNK_RUN];
-  st->chunks_list = (int64_t)s[sq::S_CHUNK_LIST];
-  st->chunks_fallback = (int64_t)s[sq::S_CHUNK_FALLBACK];
-  st->lanes_dirty = (int64_t)s[sq::S_LANE_DIRTY];
+  st->tiles_complex = (int64_t)s[sq::S_TILE_COMPLEX];
+  st->tiles_overflow = (int64_t)s[sq::S_TILE_OVERFLOW];
+  st->lanes_raw = (int64_t)s[sq::S_LANE_RAW];
+  st->lanes_raw2 = (int64_t)s[sq::S_LANE_RAW2];
+  st->lanes_tie = (int64_t)s[sq::S_LANE_TIE];
+  st->walk_batches = (int64_t)s[sq::S_WALK_BATCHES];
   st->walk_segments = (int64_t)s[sq::S_WALK_SEGMENTS];
   st->runs_rejected = (int64_t)s[sq::S_RUN_REJECTED];
-  st->terms_added = (int64_t)s[sq::S_TERMS_ADDED];
-  st->items = (int64_t)s[sq::S_ITEMS];
-  st->pool_overflow = (int64_t)s[sq::S_POOL_OVERFLOW];
-  st->tiles_complex = (int64_t)s[sq::S_TILE_COMPLEX];
-  st->scan_windows = (int64_t)s[sq::S_SCAN_WINDOWS];
-  st->walk_batches = (int64_t)s[sq::S_WALK_BATCHES];
-  st->ns_tma_wait = (int64_t)s[sq::S_NS_TMA_WAIT];
-  st->ns_prefix_wait = (int64_t)s[sq::S_NS_PREFIX_WAIT];
-  st->ns_phase_a = (int64_t)s[sq::S_NS_PHASE_A];
-  st->ns_phase_b = (int64_t)s[sq::S_NS_PHASE_B];
-  st->ns_walk_wait = (int64_t)s[sq::S_NS_WALK_WAIT];
-  st->ns_walk_work = (int64_t)s[sq::S_NS_WALK_WORK];
-  st->torn_header_reads = (int64_t)s[sq::S_TORN_HEADER];
-  st->torn_status_reads = (int64_t)s[sq::S_TORN_STATUS];
-  st->ns_scan = (int64_t)s[sq::S_NS_SCAN];
-  st->ns_walk_count = (int64_t)s[sq::S_NS_WALK_COUNT];
-  st->ns_walk_gather = (int64_t)s[sq::S_NS_WALK_GATHER];
-  st->ns_walk_scan = (int64_t)s[sq::S_NS_WALK_SCAN];
-  st->ns_walk_serial = (int64_t)s[sq::S_NS_WALK_SERIAL];
-  st->ns_walk_adds = (int64_t)s[sq::S_NS_WALK_ADDS];
-  st->chunks_dirty = (int64_t)s[sq::S_CHUNK_DIRTY];
-  st->ns_ctrl_wait = (int64_t)s[sq::S_NS_CTRL_WAIT];
-  st->ns_scan_wait = (int64_t)s[sq::S_NS_SCAN_WAIT];
-  st->ns_verdict = (int64_t)s[sq::S_NS_VERDICT];
-  st->ns_verdict_wait = (int64_t)s[sq::S_NS_VERDICT_WAIT];
-  st->ns_group_count = (int64_t)s[sq::S_NS_GCOUNT];
-  st->ns_compose = (int64_t)s[sq::S_NS_COMPOSE];
-  st->t_stream_ns = (int64_t)(s[sq::S_T_STREAM_END] - s[sq::S_T_START]);
-  st->t_walk_tail_ns = (int64_t)(s[sq::S_T_WALK1] - s[sq::S_T_STREAM_END]);
-  st->t_total_ns = (int64_t)(s[sq::S_T_WALK1] - s[sq::S_T_START]);
+  st->terms_dadd = (int64_t)s[sq::S_TERMS_DADD];
+  st->raw_rounds = (int64_t)s[sq::S_RAW_ROUNDS];
+  const int64_t t0 = (int64_t)s[sq::S_T_START], t1 = (int64_t)s[sq::S_T_STREAM_END], t2 = (int64_t)s[sq::S_T_WALK_END];
+  st->t_stream_ns = (t0 && t1) ? t1 - t0 : 0;
+  st->t_walk_tail_ns = (t1 && t2) ? t2 - t1 : 0;
+  st->t_total_ns = (t0 && t2) ? t2 - t0 : 0;
   st->device_error_bits = (int32_t)err;
   if (err & sq::ERR_CAPACITY) st->device_status = SEQSUM_ECAPACITY;
   else if (err & sq::ERR_BAD_OFFSETS) st->device_status = SEQSUM_EOFFSETS;
   else if (err & (sq::ERR_TMA_TIMEOUT | sq::ERR_WALK_TIMEOUT)) st->device_status = SEQSUM_ETIMEOUT;
-  else if (err & 32u) st->device_status = SEQSUM_EINVAL;
   else st->device_status = SEQSUM_OK;   // a plan timeout alone leaves results exact
   return SEQSUM_OK;
 }
@@ -393,7 +321,7 @@ const char *seqsum_strerror(int code) {
     case SEQSUM_ECUDA: return "CUDA runtime error";
     case SEQSUM_ETIMEOUT: return "a bounded device wait gave up";
     case SEQSUM_ENOMEM: return "workspace allocation failed";
-    case SEQSUM_ECAPACITY: return "batched call exceeded its promised size";
+    case SEQSUM_ECAPACITY: return "more tiles than the scratch holds";
     case SEQSUM_EOFFSETS: return "offsets are not non-decreasing";
     default: return "unknown error";
   }
@@ -414,7 +342,6 @@ void seqsum_release_workspace(void) {
     cudaFree(w->ctr);
     cudaFree(w->stats);
     cudaFree(w->dbg);
-    cudaFree(w->hb);
     cudaFreeHost(w->h_pin);
     delete w;
   }
@@ -426,30 +353,27 @@ void seqsum_release_workspace(void) {
 int seqsum_debug_read(unsigned long long *out, int n) {
   std::lock_guard<std::mutex> lk(g_mu);
   Workspace *w = g_last;
-  if (!w || !out || n < 0 || n > sq::kDbgAlloc) return SEQSUM_EINVAL;
+  if (!w || !out || n < 0 || n > sq::kDbgWords) return SEQSUM_EINVAL;
   cudaError_t e = cudaStreamSynchronize(w->stream);
   if (e == cudaSuccess) e = cudaMemcpy(out, w->dbg, n * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess) e = cudaMemset(w->dbg, 0, sq::kDbgAlloc * sizeof(unsigned long long));
+  if (e == cudaSuccess) e = cudaMemset(w->dbg, 0, sq::kDbgWords * sizeof(unsigned long long));
   return e == cudaSuccess ? SEQSUM_OK : cuda_fail(e);
 }
 
-int seqsum_debug_heartbeat(unsigned long long *out, int n) {
+int seqsum_debug_counters(unsigned long long *out, int n) {
   // No lock: this is read while another thread may be blocked inside a call
   // of this library (holding its lock).  A non-blocking stream lets the copy
   // run next to a kernel that has not finished.
   static cudaStream_t side = nullptr;
   Workspace *w = g_last;
-  if (!w || !out || n < sq::C_COUNT || n > sq::C_COUNT + sq::kHeartbeats) return SEQSUM_EINVAL;
+  if (!w || !out || n < 1 || n > sq::C_COUNT) return SEQSUM_EINVAL;
   cudaError_t e = cudaSuccess;
   if (!side) e = cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking);
   uint32_t c[sq::C_COUNT];
   if (e == cudaSuccess) e = cudaMemcpyAsync(c, w->ctr, sizeof c, cudaMemcpyDeviceToHost, side);
-  if (e == cudaSuccess && n > sq::C_COUNT)
-    e = cudaMemcpyAsync(out + sq::C_COUNT, w->hb, (n - sq::C_COUNT) * sizeof(unsigned long long),
-                        cudaMemcpyDeviceToHost, side);
   if (e == cudaSuccess) e = cudaStreamSynchronize(side);
   if (e != cudaSuccess) return cuda_fail(e);
-  for (int i = 0; i < sq::C_COUNT; i++) out[i] = c[i];
+  for (int i = 0; i < n; i++) out[i] = c[i];
   return SEQSUM_OK;
 }
 
@@ -460,6 +384,15 @@ int seqsum_debug_set_plan(int mode) {
   return old;
 }
 
-const char *seqsum_version(void) { return "seqsum 0.1 (sm_103a)"; }
+int seqsum_debug_set_fault(int mode, int64_t arg, int64_t wait_ns) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (mode < 0 || mode > 1 || wait_ns < 0) return SEQSUM_EINVAL;
+  g_fault_mode = mode;
+  g_fault_arg = arg;
+  g_wait_ns = wait_ns > 0 ? (uint64_t)wait_ns : 2000000000ull;
+  return SEQSUM_OK;
+}
+
+const char *seqsum_version(void) { return "seqsum 0.2 (sm_103a)"; }
 
 }  // extern "C"

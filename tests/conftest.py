@@ -40,8 +40,8 @@ def oracle_mod():
 
 
 # With SEQSUM_WATCHDOG=<seconds>, a GPU test still running after that long
-# prints the library's counters and per-CTA heartbeats (read without waiting
-# for the call) and ends the process, instead of leaving a call stuck.
+# prints the library's device counters (read without waiting for the call)
+# and ends the process, instead of leaving a call stuck.
 @pytest.fixture(autouse=True)
 def _watchdog(request):
     limit = float(os.environ.get("SEQSUM_WATCHDOG", "0") or 0)
@@ -53,10 +53,7 @@ def _watchdog(request):
     def fire():
         try:
             import parity_binade_chunked_gb300 as sq
-            d = sq.debug_heartbeat(320)
-            print(f"\nWATCHDOG {request.node.nodeid}: counters {d['counters']}", flush=True)
-            for beat in d["beats"]:
-                print("  cta %d warp %d role %d what %d where %#x" % beat, flush=True)
+            print(f"\nWATCHDOG {request.node.nodeid}: counters {sq.debug_counters()}", flush=True)
         except Exception as e:          # diagnostics only
             print("WATCHDOG failed:", e, flush=True)
         os._exit(3)

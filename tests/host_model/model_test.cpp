@@ -5,12 +5,18 @@
 //   1. the one-term rule: applying the increment of one term to S gives
 //      exactly S + x whenever the walk's check accepts it, on random and
 //      adversarial pairs (ties, binade edges, negative S, subnormal terms);
-//   2. the whole pipeline in the kernels' layout (lanes of 16 terms, warps of
-//      32 lanes composed in a tree, tiles of 8 warps), walked with the
-//      term-by-term fallback, against the plain loop, under several plans:
-//      the true binade, one binade too high, all "zero", one fixed binade,
-//      all chunks term by term, and random (Research-1433, finding 5
-//      "The plan cannot make the result wrong").
+//   2. the streaming kernel's fast rule: half-up increments with a one-word
+//      tie detector (term_mag_halfup) against term_inc;
+//   3. the whole pipeline in the kernels' layout (lanes of 16 terms, warps of
+//      32 lanes composed in a tree), walked with the term-by-term fallback,
+//      against the plain loop, under several plans: the true binade, one
+//      binade too high, all "zero", one fixed binade, all chunks term by term,
+//      and random (Research-1433, finding 5 "The plan cannot make the result
+//      wrong");
+//   4. the streaming kernel's composition: rows of 16 terms by the fast rule
+//      (signed rows bounded by their negative and positive parts, rows with a
+//      tie by the exact rule), a tile of rows of one binade composed by plain
+//      sums, walked with row and term fallbacks under the same plans.
 //
 // Built with -DSEQSUM_MUTATE=k it must FAIL (exit status != 0) for each
 // planted mistake k (Research-1433, "Tests": always round a tie up, drop the
@@ -134,6 +140,47 @@ static void test_fast_increment(long count) {
     }
   }
   printf("fast increment: %ld checked\n", n);
+}
+
+// ----------------------------------------------------- half-up increment
+// term_mag_halfup (the streaming pass) against term_inc: away from a tie the
+// two agree; at a tie (t == 0) the half-up value is the floor plus one, and
+// term_inc's even-start value and odd-start difference follow from the floor.
+static void test_halfup_increment(long count) {
+  long n = 0, ties = 0;
+  for (long i = 0; i < count; i++) {
+    const int e = (int)(rnd() % 1990) - 969;
+    double x;
+    const uint64_t c = rnd() % 8;
+    if (c == 0) x = 0.0;
+    else if (c == 1) x = dbl(rnd() % (1ull << 52));                                  // subnormal
+    else if (c == 2) x = ldexp((double)(rnd() % 4096) + 0.5, e - 52 - (int)(rnd() % 12));
+    else if (c == 3) x = mk(e - 1, rnd(), false);                                      // just below 2^e
+    else if (c == 4) x = ldexp((double)(rnd() % (1ull << 40)), e - 52 - (int)(rnd() % 50));
+    else x = mk(e - 1 - (int)(rnd() % 80), rnd(), false);
+    if (rnd() & 1) x = -x;
+    if (!(fabs(x) < ldexp(1.0, e))) continue;
+    const uint64_t b = bits(x);
+    int64_t re; int32_t d;
+    if (term_inc(b & ~kSignBit, e, re, d)) continue;       // the magnitude's increment
+    uint32_t t;
+    const uint64_t r = term_mag_halfup((uint32_t)(b >> 32), (uint32_t)b, 64 - (e + 1023), t);
+    bool ok;
+    if (t != 0) ok = (d == 0) && ((int64_t)r == re);
+    else {
+      ties++;
+      const uint64_t f = r - 1;
+      ok = (re == (int64_t)(f + (f & 1))) && (d == ((f & 1) ? -1 : 1));
+    }
+    n++;
+    if (!ok) {
+      if (g_fail < 10)
+        fprintf(stderr, "half-up increment mismatch: x=%a e=%d r=%llu t=%u re=%lld d=%d\n", x, e,
+                (unsigned long long)r, t, (long long)re, d);
+      g_fail++;
+    }
+  }
+  printf("half-up increment: %ld checked, %ld ties\n", n, ties);
 }
 
 // ------------------------------------------------------------- short runs
@@ -293,12 +340,150 @@ static void test_pipeline() {
   printf("pipeline: %ld sums, %ld chunk fallbacks\n", total, fb);
 }
 
+// ----------------------------------------------- the streaming composition
+// A row as the streaming kernel forms it: all zeros exactly; else the fast
+// rule (half-up increments, signed rows bounded by [-negatives, positives]),
+// or the exact rule when a tie is detected.
+static Run row_kernel(const double *x, int n, int e, bool &tie) {
+  tie = false;
+  bool zero = true, allneg = true;
+  for (int i = 0; i < n; i++) {
+    zero = zero && (bits(x[i]) << 1) == 0;
+    allneg = allneg && (bits(x[i]) >> 63);
+  }
+  if (zero) {
+    Run r = run_empty();
+    r.lo = r.hi = 0;
+    r.flags = F_NONNEG | F_NONPOS | F_ZERO | (allneg ? F_ALLNEGZ : 0u);
+    return r;
+  }
+  uint64_t tot = 0, ng = 0;
+  uint32_t tmin = ~0u, emax = 0;
+  bool anyneg = false;
+  for (int i = 0; i < n; i++) {
+    const uint64_t b = bits(x[i]);
+    const uint32_t hi = (uint32_t)(b >> 32);
+    uint32_t t;
+    const uint64_t r = term_mag_halfup(hi, (uint32_t)b, 64 - (e + 1023), t);
+    tmin = t < tmin ? t : tmin;
+    const uint32_t E = (hi >> 20) & 0x7FFu;
+    emax = E > emax ? E : emax;
+    const uint64_t sm = (hi >> 31) ? ~0ull : 0ull;
+    anyneg = anyneg || (hi >> 31);
+    tot += r;
+    ng += r & sm;
+  }
+  if (tmin == 0) {
+    tie = true;
+    return lane_run(x, n, e);
+  }
+  Run r;
+  r.inc = (int64_t)(tot - 2 * ng);
+  r.lo = -(int64_t)ng;
+  r.hi = (int64_t)(tot - ng);
+  r.d = 0;
+  r.flags = (anyneg ? 0u : (uint32_t)F_NONNEG) | (emax >= (uint32_t)(e + 1023) ? (uint32_t)F_POISON : 0u);
+  const int64_t lim = (int64_t)1 << 54;
+  if (r.inc > lim || r.inc < -lim || r.hi > lim || r.lo < -lim) r.flags |= F_POISON;
+  return r;
+}
+
+static uint64_t add_terms(uint64_t S, const double *x, int n) {
+  double s = dbl(S);
+  for (int i = 0; i < n; i++) s = seq_add(s, x[i]);
+  return bits(s);
+}
+
+static uint64_t walk_kernel(const std::vector<double> &x, double s0, int plan_kind, long &fast_tiles) {
+  const int ROWS = 8, TT = ROWS * LANE;
+  uint64_t S = bits(s0);
+  double approx = s0;
+  const size_t n = x.size();
+  for (size_t t0 = 0; t0 < n; t0 += TT) {
+    int e[ROWS];
+    Run rr[ROWS];
+    bool tie[ROWS], ok_rows = true;
+    int nr = 0;
+    for (int r = 0; r < ROWS && t0 + (size_t)r * LANE < n; r++, nr++) {
+      const size_t a = t0 + (size_t)r * LANE;
+      const int m = (int)((n - a) < (size_t)LANE ? (n - a) : LANE);
+      switch (plan_kind) {
+        case 0: e[r] = binade_of_bits(bits(approx)); break;
+        case 1: e[r] = binade_of_bits(bits(approx)) + 1; break;
+        case 2: e[r] = -200; break;
+        case 3: e[r] = 3; break;
+        case 4: e[r] = 99999; break;
+        default: e[r] = binade_of_bits(bits(approx)) + (int)(rnd() % 3) - 1; break;
+      }
+      for (int i = 0; i < m; i++) approx += x[a + i];
+      if (e[r] < -900 || e[r] > 1000) { ok_rows = false; continue; }
+      rr[r] = row_kernel(&x[a], m, e[r], tie[r]);
+      if (tie[r] || e[r] != e[0]) ok_rows = false;
+    }
+    if (ok_rows && plan_kind != 4) {
+      // one run for the tile: plain sums of the rows, flags combined
+      Run h;
+      h.inc = h.lo = h.hi = 0;
+      h.d = 0;
+      uint32_t fand = 0xFF, fo = 0;
+      for (int r = 0; r < nr; r++) {
+        h.inc += rr[r].inc;
+        h.lo += rr[r].lo;
+        h.hi += rr[r].hi;
+        fand &= rr[r].flags & (F_NONNEG | F_NONPOS | F_ZERO | F_ALLNEGZ);
+        fo |= rr[r].flags & F_POISON;
+      }
+      h.flags = fand | fo;
+      uint64_t T = S;
+      if (run_apply(T, h, e[0]) == APPLY_OK) {
+        fast_tiles++;
+        S = T;
+        continue;
+      }
+    }
+    for (int r = 0; r < nr; r++) {
+      const size_t a = t0 + (size_t)r * LANE;
+      const int m = (int)((n - a) < (size_t)LANE ? (n - a) : LANE);
+      uint64_t T = S;
+      if (plan_kind != 4 && e[r] >= -900 && e[r] <= 1000 && run_apply(T, rr[r], e[r]) == APPLY_OK) S = T;
+      else S = add_terms(S, &x[a], m);
+    }
+  }
+  return S;
+}
+
+static void test_kernel_composition() {
+  const double starts[] = {0.0, -0.0, 1.0, -1.0, 12345.678, 0x1p-1070, -3.0e9};
+  long total = 0, fast = 0;
+  for (int kind = 0; kind < 10; kind++)
+    for (int plan = 0; plan < 6; plan++)
+      for (int rep = 0; rep < 4; rep++) {
+        size_t n = 1 + (size_t)(rnd() % 6000);
+        std::vector<double> x = gen(kind, n);
+        double s0 = starts[rnd() % 7];
+        double want = s0;
+        for (size_t i = 0; i < n; i++) want = seq_add(want, x[i]);
+        uint64_t got = walk_kernel(x, s0, plan, fast);
+        total++;
+        bool same = (got == bits(want)) || (want != want && dbl(got) != dbl(got));
+        if (!same) {
+          if (g_fail < 10)
+            fprintf(stderr, "kernel composition mismatch kind=%d plan=%d n=%zu got=%a want=%a\n",
+                    kind, plan, n, dbl(got), want);
+          g_fail++;
+        }
+      }
+  printf("kernel composition: %ld sums, %ld tiles applied as one run\n", total, fast);
+}
+
 int main(int argc, char **argv) {
   long count = argc > 1 ? atol(argv[1]) : 2000000;
   test_one_term(count);
   test_fast_increment(count);
+  test_halfup_increment(count);
   test_short_runs(count / 2);
   test_pipeline();
+  test_kernel_composition();
   printf("mutation=%d failures=%ld\n", kMutate, g_fail);
   return g_fail ? 1 : 0;
 }

@@ -182,6 +182,18 @@ def test_negative_and_cancelling_sums(sq):
     check(sq, z, 0.0, "up, down, up")
 
 
+def test_walk_batch_ends_where_staged_items_run_out(sq):
+    """A signed random walk crosses zero again and again, so most tiles carry
+    item lists; a walk batch then stages more item slots than its shared
+    memory holds and must end before the first tile that does not fit (and
+    take that tile in the next batch, once).  Prefixes of several lengths,
+    ragged tails included."""
+    rng = np.random.default_rng(4)
+    y = rng.standard_normal(200000) * np.ldexp(1.0, rng.integers(-10, 10, 200000))
+    for n in [188284, 188285, 150000, 200000, 4096 * 40, 4096 * 40 + 1]:
+        check(sq, y[:n], 0.0, f"random walk prefix {n}")
+
+
 def test_wide_exponent_mix(sq):
     rng = np.random.default_rng(5)
     x = np.ldexp(rng.random(100000), rng.integers(-1074, 1000, 100000)) * np.where(
@@ -190,7 +202,7 @@ def test_wide_exponent_mix(sq):
 
 
 def test_stream_and_repeats(sq):
-    """Many calls on a side stream, across the look-back tag wrap (127)."""
+    """Many calls on a side stream, across the tag wrap (255 calls)."""
     s = torch.cuda.Stream()
     rng = np.random.default_rng(6)
     planes = [W.plane_c2(int(n), 1, seed=int(n)) for n in rng.integers(1, 40000, 12)]
@@ -207,19 +219,18 @@ def test_stream_and_repeats(sq):
         assert_same(o.item(), wants[k], f"repeat plane {k}")
 
 
-def test_group_too_fragmented_is_walked_tile_by_tile(sq):
+def test_crossing_at_every_term_overflows_the_item_area(sq):
     """A running sum that crosses a power of two at every term (1.0, 0.5,
-    1.0, ...): every lane is dirty, every chunk overflows its item slots, and
-    each group of 32 tiles needs far more segments than a composed group
-    holds -- the walk takes those groups tile by tile, and the bits still
-    match the loop's."""
+    1.0, ...): every row's plan range spans a power of two, so every row is
+    raw and no tile's items fit its area -- the walk reads those tiles' terms
+    itself, and the bits still match the loop's."""
     n = 32 * 4096 * 2
     x = np.empty(n)
     x[0] = 1.0
     x[1::2] = -0.5
     x[2::2] = 0.5
     st = check(sq, x, 0.0, "alternating crossings")
-    assert st["walk_batches"] > 0, st
+    assert st["tiles_overflow"] > 0, st
 
 
 # ------------------------------------------------------------ plan independence

@@ -36,15 +36,3 @@ def test_planted_mistake_fails(mutate):
     exe = _build(mutate)
     r = subprocess.run([exe, "400000"], capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutation {mutate} was not caught:\n{r.stdout}"
-
-
-def test_ticket_order_on_host():
-    """The ticket order of the streaming CTAs (csrc/units.cuh): every tile's
-    plan and run unit named once, in the order of its definition, each run
-    after the plans it depends on, over 4710 (size, wave, head) cases."""
-    os.makedirs(OUT, exist_ok=True)
-    exe = os.path.join(OUT, "units")
-    subprocess.check_call(["g++", *FLAGS, "-o", exe, os.path.join(ROOT, "tests", "host_model", "units_test.cpp")])
-    r = subprocess.run([exe], capture_output=True, text=True, timeout=600)
-    assert r.returncode == 0, r.stdout + r.stderr
-    assert "failures=0" in r.stdout
