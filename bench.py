@@ -9,8 +9,9 @@ U in [-40, 0], 1% zeros), result bit-checked against the oracle before timing.
 
 Prints one JSON line.  `value` is Gterms/s (terms / device time), timed with
 CUDA events on the launching stream around each call, the L2 flushed before
-every step by writing a 256 MB buffer (the plane itself is 66 MB, under the
-129 MB L2).  Multi-GPU runs (torchrun) are independent replicas, one per rank:
+every step by writing one 256 MB buffer and then reading another (so the L2
+holds clean lines of the second buffer and the timed call writes nothing
+back; the plane itself is 66 MB, under the 129 MB L2).  Multi-GPU runs (torchrun) are independent replicas, one per rank:
 a single sequential sum has no data-parallel split without an exchange step.
 """
 from __future__ import annotations
@@ -236,49 +237,36 @@ def reference_arm(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+class Flush:
+    """Leaves the L2 holding clean lines that the timed call does not use: a
+    256 MB write, then a read of another 256 MB buffer (twice the 129 MB L2)."""
+
+    def __init__(self, torch, dev):
+        self.a = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.b = torch.ones(32 << 20, dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        self.a.fill_(1)
+        self.b.sum()
+
+
 def time_kernel(sq, torch, xd, s0, out, steps, warmup, flush, stream):
     """Per-step CUDA events on the launching stream around one call; the L2
-    is flushed (a 256 MB write) before each step, outside the events."""
-    for _ in range(warmup):
-        flush.fill_(1)
-        sq.seqsum_f64(xd, s0, out=out, stream=stream)
+    is flushed before each step, outside the events."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush()
+            sq.seqsum_f64(xd, s0, out=out, stream=stream)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     with torch.cuda.stream(stream):
         for a, b in ev:
-            flush.fill_(1)
+            flush()
             a.record(stream)
             sq.seqsum_f64(xd, s0, out=out, stream=stream)
             b.record(stream)
     torch.cuda.synchronize()
     return [a.elapsed_time(b) for a, b in ev]
-
-
-def read_peak(torch, xd, flush, stream, reps=20):
-    """A read-only streaming peak measured in the same run: torch's sum of the
-    same device plane (8 bytes per term read once), with the same L2 flush
-    before each step, timed with CUDA events on the stream (median GB/s).  A
-    reference for the roofline beside the measured copy peak; None if it
-    cannot be taken."""
-    try:
-        n = xd.numel()
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                flush.fill_(1)
-                xd.sum()
-        torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-        with torch.cuda.stream(stream):
-            for a, b in ev:
-                flush.fill_(1)
-                a.record(stream)
-                xd.sum()
-                b.record(stream)
-        torch.cuda.synchronize()
-        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
-        return 8.0 * n / (ms * 1e-3) / 1e9
-    except Exception:
-        return None
 
 
 def main():
@@ -305,7 +293,7 @@ def main():
     s0 = float(wl.s0[0])
     xd = torch.from_numpy(x).to(dev)
     out = torch.empty(1, dtype=torch.float64, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = Flush(torch, dev)
 
     # parity before timing (0 ULP)
     want = oracle.seqsum(x, s0)
@@ -351,22 +339,18 @@ def main():
     e2e_ms = a.elapsed_time(b) / e2e_steps
     e2e_ok = bool(np.float64(hout.item()).view(np.uint64) == np.float64(want).view(np.uint64))
 
-    rpeak = read_peak(torch, xd, flush, stream)
-
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{args.config} {wl.shape[0][0]}x{wl.shape[0][1]} single sum ({n} terms)", "n_terms": n,
-                   "recipe": wl.recipe, "l2": "flushed before every step (256 MB write)",
+                   "recipe": wl.recipe, "l2": "flushed before every step (256 MB write, then a 256 MB read of another buffer)",
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "parity_0ulp": parity and e2e_ok,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": measured_traffic(args.config, args.height_mult),
                      "peak_source": peak_src, "algorithmic_bytes_per_launch": 8 * n,
-                     "traffic_source": "profiles/seqsum_kernel_%s_traffic.json (null if the kernel changed)" % args.config,
-                     "read_peak_gbs": rpeak, "frac_of_read_peak": (achieved / rpeak) if rpeak else None,
-                     "read_peak_source": "torch sum of the same plane, L2 flushed before each step, this run"},
+                     "traffic_source": "profiles/seqsum_kernel_%s_traffic.json (null if the kernel changed)" % args.config},
         "e2e": {"value": n / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": 8 * n,
                 "d2h_bytes_per_step": 8},
         "gpu_launches": args.steps,
@@ -407,7 +391,7 @@ def main():
                              oracle.seqsum_batched(w4.x, w4.offsets, w4.s0).view(np.uint64))
         ts = []
         for i in range(30):
-            flush.fill_(1)
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             with torch.cuda.stream(stream):
                 a.record(stream)

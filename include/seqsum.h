@@ -114,15 +114,26 @@ int seqsum_f64_batched_sized(const double *x, int64_t x_len, const int64_t *offs
 typedef struct {
   int64_t tiles;             /* tiles of 4096 terms processed */
   int64_t tiles_complex;     /* tiles published as a list of items (rows of several binades, raw rows, ties) */
-  int64_t tiles_overflow;    /* tiles whose items did not fit their area (the walk read their terms) */
+  int64_t ranges_from_x;     /* walk ranges of 128 tiles whose steps did not fit (the walk read their terms) */
   int64_t lanes_raw;         /* 16-term rows whose plan range crossed a power of two (added by the walk) */
   int64_t lanes_raw2;        /* ... of which published with prefix tables for one crossing */
   int64_t lanes_tie;         /* rows with a tie, composed in order by the even/odd rule */
-  int64_t walk_batches;      /* batches of tile headers the walk read */
+  int64_t walk_batches;      /* walk ranges (128 tiles each) applied in order */
   int64_t walk_segments;     /* composites the walk applied (same-binade runs composed across tiles) */
   int64_t runs_rejected;     /* runs the walk's exact check refused (their terms were added one by one) */
   int64_t terms_dadd;        /* terms the walk added with a hardware fp64 add */
   int64_t raw_rounds;        /* warp rounds of the walk's term-by-term resolution */
+  int64_t cy_walk_wait;      /* SM cycles the walk's producer warps waited for tile headers (summed) */
+  int64_t cy_walk_serial;    /* SM cycles of the walk's in-order warp applying steps */
+  int64_t cy_walk_raw;       /* ... of which resolving raw terms */
+  int64_t cy_tma_wait;       /* SM cycles summed over the streaming warps: waiting for a unit's copy */
+  int64_t cy_plan;           /* ... plan units (the tiles' sums) */
+  int64_t cy_pfx_wait;       /* ... run units waiting for a prefix the copy did not bring */
+  int64_t cy_run;            /* ... run units (the rows' runs and the tile's header) */
+  int64_t scan_windows;      /* windows of tiles' prefixes the scanner published */
+  int64_t scan_polls;        /* scanner polls that found no new tile sums */
+  int64_t pfx_late;          /* run units whose prefix was not yet published when their copy landed */
+  int64_t ctas_alone;        /* streaming CTAs that left their SM to the walker or the scanner */
   int64_t t_stream_ns;       /* latest call: kernel start to the last tile header */
   int64_t t_walk_tail_ns;    /* latest call: last tile header to the end of the walk */
   int64_t t_total_ns;        /* latest call: kernel start to the end of the walk */

@@ -31,9 +31,10 @@ class SeqsumError(RuntimeError):
 
 class _Stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
-        "tiles", "tiles_complex", "tiles_overflow", "lanes_raw", "lanes_raw2", "lanes_tie", "walk_batches",
-        "walk_segments", "runs_rejected", "terms_dadd", "raw_rounds", "t_stream_ns", "t_walk_tail_ns",
-        "t_total_ns")] + [
+        "tiles", "tiles_complex", "ranges_from_x", "lanes_raw", "lanes_raw2", "lanes_tie", "walk_batches",
+        "walk_segments", "runs_rejected", "terms_dadd", "raw_rounds", "cy_walk_wait", "cy_walk_serial",
+        "cy_walk_raw", "cy_tma_wait", "cy_plan", "cy_pfx_wait", "cy_run", "scan_windows", "scan_polls", "pfx_late", "ctas_alone",
+        "t_stream_ns", "t_walk_tail_ns", "t_total_ns")] + [
         ("device_status", ctypes.c_int32), ("device_error_bits", ctypes.c_int32),
         ("check_site", ctypes.c_int32), ("check_pad", ctypes.c_int32), ("check_value", ctypes.c_int64),
         ("timeout_site", ctypes.c_int32), ("timeout_pad", ctypes.c_int32), ("timeout_a", ctypes.c_int64),

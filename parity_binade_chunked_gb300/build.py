@@ -41,7 +41,7 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-# cycle-profiling variant (-DSEQSUM_PROFILE): the walk's sections summed into the diagnostic words
+# profiling variant (-DSEQSUM_PROFILE): a timeline of two streaming CTAs and the walk's phases in the diagnostic words
 PROFILE_BUILD = os.path.join(BUILD, "profile")
 PROFILE_LIB = os.path.join(PROFILE_BUILD, "libseqsum.so")
 

@@ -24,7 +24,8 @@ struct Workspace {
   int device = 0;
   cudaStream_t stream = nullptr;
   int64_t cap_tiles = 0, cap_sums = 0;
-  uint4 *status = nullptr;           // the plan's per-tile words
+  uint4 *status = nullptr;           // per tile: its sums, published by its plan unit
+  uint4 *prec = nullptr;             // per tile: its prefix (the scanner) and its warps' sums (the plan)
   Rec *hdr = nullptr;                // one header per tile
   Rec *items = nullptr;              // kItemSlots item slots per tile
   uint32_t *ctr = nullptr;
@@ -47,6 +48,7 @@ int g_fault_mode = 0;
 int64_t g_fault_arg = 0;
 uint64_t g_wait_ns = 2000000000ull;   // every bounded device wait gives up after 2 s
 int g_blocks_per_sm = 0;
+int64_t g_wave = 0;                   // plan units run this many tiles ahead of run units (0: not yet read)
 int g_num_sms[64] = {0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -57,6 +59,8 @@ int cuda_fail(cudaError_t e) {
 
 void ws_free(Workspace *w) {
   cudaFree(w->status);
+  cudaFree(w->prec);
+  w->prec = nullptr;
   cudaFree(w->hdr);
   cudaFree(w->items);
   cudaFree(w->tile_begin);
@@ -93,6 +97,7 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
     const int64_t cs = sums > w->cap_sums ? sums + 16 : w->cap_sums;
     ws_free(w);
     if (cudaMalloc(&w->status, ct * sizeof(uint4)) != cudaSuccess ||
+        cudaMalloc(&w->prec, ct * sq::kPrecWords * sizeof(uint4)) != cudaSuccess ||
         cudaMalloc(&w->hdr, ct * sizeof(Rec)) != cudaSuccess ||
         cudaMalloc(&w->items, ct * sq::kItemSlots * sizeof(Rec)) != cudaSuccess ||
         cudaMalloc(&w->tile_begin, (cs + 1) * sizeof(int64_t)) != cudaSuccess) {
@@ -102,6 +107,7 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
     }
     // fresh tagged words and a fresh tag sequence (the counters' epoch word)
     cudaMemset(w->status, 0, ct * sizeof(uint4));
+    cudaMemset(w->prec, 0, ct * sq::kPrecWords * sizeof(uint4));
     cudaMemset(w->hdr, 0, ct * sizeof(Rec));
     cudaMemset(w->ctr, 0, sq::C_COUNT * sizeof(uint32_t));
     w->cap_tiles = ct;
@@ -121,6 +127,14 @@ int ensure_device_info() {
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (g_blocks_per_sm == 0) g_blocks_per_sm = sq::kernel_blocks_per_sm();
+  if (g_wave == 0) {
+    // far enough ahead that the scanner has published a tile's prefix when
+    // its run unit starts, near enough that the tile is still in L2 (1024
+    // tiles = 32 MB of the 129 MB)
+    g_wave = 1024;
+    const char *ev = getenv("SEQSUM_WAVE");
+    if (ev && atoll(ev) > 0) g_wave = atoll(ev);
+  }
   if (!g_encode) {
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -156,6 +170,8 @@ int64_t tensor_map(Workspace *w, const double *x, int64_t n_total) {
 
 void fill_ws(Params &p, Workspace *w) {
   p.status = w->status;
+  p.prec = w->prec;
+  p.wave = g_wave;
   p.hdr = w->hdr;
   p.items = w->items;
   p.ctr = w->ctr;
@@ -210,9 +226,10 @@ int batched_impl(const double *x, int64_t x_len, const int64_t *offsets, int32_t
   p.nwalkers = nsums < sq::kMaxWalkers ? nsums : sq::kMaxWalkers;
   cudaError_t e = sq::launch_setup(p, stream);
   if (e != cudaSuccess) return cuda_fail(e);
+  // the walkers, the scanner, and streaming CTAs (at most one per unit)
   int64_t grid = (int64_t)g_num_sms[w->device] * g_blocks_per_sm;
-  if (p.nwalkers + tiles < grid) grid = p.nwalkers + tiles;
-  if (grid < p.nwalkers + 1) grid = p.nwalkers + 1;
+  if (p.nwalkers + 1 + 2 * tiles < grid) grid = p.nwalkers + 1 + 2 * tiles;
+  if (grid < p.nwalkers + 2) grid = p.nwalkers + 2;
   static CUtensorMap dummy;
   e = sq::launch_seqsum(p, p.tma_rows ? &w->tmap : &dummy, (int)grid, stream);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -247,7 +264,8 @@ int seqsum_f64(const double *x, int64_t n, double s0, double *out, cudaStream_t 
   p.nwalkers = 1;
   const int dev = w->device;
   int64_t grid = (int64_t)g_num_sms[dev] * g_blocks_per_sm;
-  if (tiles + 1 < grid) grid = tiles + 1;     // the walker and at most one streaming CTA per tile
+  if (2 * tiles + 2 < grid) grid = 2 * tiles + 2;     // the walker, the scanner, at most one streaming CTA per unit
+  if (grid < 3) grid = 3;
   static CUtensorMap dummy;
   cudaError_t e = sq::launch_seqsum(p, p.tma_rows ? &w->tmap : &dummy, (int)grid, stream);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -293,7 +311,7 @@ int seqsum_get_stats(seqsum_stats *st) {
   st->check_value = (int64_t)(((uint64_t)c[sq::C_CHECK_HI] << 32) | c[sq::C_CHECK_LO]);
   st->tiles = (int64_t)s[sq::S_TILES];
   st->tiles_complex = (int64_t)s[sq::S_TILE_COMPLEX];
-  st->tiles_overflow = (int64_t)s[sq::S_TILE_OVERFLOW];
+  st->ranges_from_x = (int64_t)s[sq::S_RANGE_X];
   st->lanes_raw = (int64_t)s[sq::S_LANE_RAW];
   st->lanes_raw2 = (int64_t)s[sq::S_LANE_RAW2];
   st->lanes_tie = (int64_t)s[sq::S_LANE_TIE];
@@ -302,6 +320,17 @@ int seqsum_get_stats(seqsum_stats *st) {
   st->runs_rejected = (int64_t)s[sq::S_RUN_REJECTED];
   st->terms_dadd = (int64_t)s[sq::S_TERMS_DADD];
   st->raw_rounds = (int64_t)s[sq::S_RAW_ROUNDS];
+  st->cy_walk_wait = (int64_t)s[sq::S_CY_WALK_WAIT];
+  st->cy_walk_serial = (int64_t)s[sq::S_CY_WALK_SERIAL];
+  st->cy_walk_raw = (int64_t)s[sq::S_CY_WALK_RAW];
+  st->cy_tma_wait = (int64_t)s[sq::S_CY_TMA_WAIT];
+  st->cy_plan = (int64_t)s[sq::S_CY_PLAN];
+  st->cy_pfx_wait = (int64_t)s[sq::S_CY_PFX_WAIT];
+  st->cy_run = (int64_t)s[sq::S_CY_RUN];
+  st->scan_windows = (int64_t)s[sq::S_SCAN_WINDOWS];
+  st->scan_polls = (int64_t)s[sq::S_SCAN_POLLS];
+  st->pfx_late = (int64_t)s[sq::S_PFX_LATE];
+  st->ctas_alone = (int64_t)s[sq::S_ALONE];
   const int64_t t0 = (int64_t)s[sq::S_T_START], t1 = (int64_t)s[sq::S_T_STREAM_END], t2 = (int64_t)s[sq::S_T_WALK_END];
   st->t_stream_ns = (t0 && t1) ? t1 - t0 : 0;
   st->t_walk_tail_ns = (t1 && t2) ? t2 - t1 : 0;

@@ -8,20 +8,21 @@ namespace sq {
 
 // ---- geometry
 // A lane owns one 128-byte row: 16 consecutive terms.  A tile is 256 rows
-// (4096 terms, 32 KB), one TMA box; a CTA has 8 warps, one row per thread.
+// (4096 terms, 32 KB), one TMA box.  A CTA has 8 compute warps (one row per
+// thread) and a ninth warp: a streaming CTA's producer.
 constexpr int kLaneTerms = 16;
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
+constexpr int kBlockWarps = kWarps + 1;          // + a streaming CTA's producer warp (tickets and copies)
+constexpr int kBlockThreads = kBlockWarps * 32;
 constexpr int kTileRows = kThreads;
 constexpr int kTileTerms = kTileRows * kLaneTerms;
 constexpr int kStages = 3;                       // TMA stages of a streaming CTA
 constexpr int kStageBytes = kTileTerms * 8;
 constexpr int kDynSmem = kStages * kStageBytes + 1024;   // + alignment slack for the 128-byte swizzle
-constexpr int kItemSlots = 256;                  // 32-byte slots in a tile's item area (8 KB)
+constexpr int kWarpSlots = 32;                   // 32-byte item slots of one warp's region (one per row)
+constexpr int kItemSlots = kWarps * kWarpSlots;  // a tile's item area (8 KB): one region per compute warp
 constexpr int kMaxWalkers = 8;
-constexpr int kBatch = kThreads;                 // tile headers a walk batch reads (one per thread)
-constexpr int kBatchSlots = 2048;                // item slots a walk batch stages in shared memory (64 KB)
-static_assert(kBatchSlots * 32 + kBatch * 32 <= kDynSmem, "walker staging fits the dynamic shared memory");
 
 // ---- records
 // A tile header or an item: four 64-bit words.  A header carries the call's
@@ -31,20 +32,25 @@ static_assert(kBatchSlots * 32 + kBatch * 32 <= kDynSmem, "walker staging fits t
 //   w[0] inc, w[1] lo, w[2] hi: 56-bit two's complement
 //   w[3] meta: kind (3 bits), biased binade (11 bits, 0 = none), d + 1 (2 bits),
 //        flags (8 bits), count (13 bits), start (13 bits)
+// A K_COMPLEX header carries instead, in w[0], the number of the tile's items:
+// records from slot 0 of its item area, in the order of their terms, runs of
+// one binade that touch already composed; a raw row's terms stay in x.  (While
+// a tile is formed, warp k writes its own items from slot 32 k.)
 struct __align__(16) Rec {
   uint64_t w[4];
 };
 
 enum : uint32_t {
   K_RUN = 0,       // a run of adds inside binade eb (or a run of zeros)
-  K_RAW = 1,       // item: 16 terms the walk adds itself; the terms follow in 4 slots
-  K_COMPLEX = 2,   // header: the tile's records are `count` item slots
+  K_RAW = 1,       // item: a row of 16 terms the walk adds itself
+  K_COMPLEX = 2,   // header: the tile's records are its warps' item regions
   K_OVERFLOW = 3,  // header: the tile's items did not fit; the walk reads its terms from x
-  K_RAW2 = 4       // item: 16 terms across one power of two, with prefix tables (13 slots)
+  K_RAW2 = 4       // item: a raw row across one power of two, from binade eb to eb + 1, all of its
+                   // terms of one sign (w[0]: 1 if negative); the walk builds prefix tables for it
 };
 
-constexpr int kRawSlots = 5;      // K_RAW: descriptor + 16 terms
-constexpr int kRaw2Slots = 13;    // K_RAW2: descriptor + 16 terms + 16 prefixes + 16 suffixes
+constexpr int kPrecWords = 5;     // a tile's plan record: its exclusive prefix, then its warps' float sums (5 x 16 B)
+constexpr int kScanTiles = 4 * kThreads;   // tiles the scanner takes per window
 
 // ---- counters in the workspace (32-bit words)
 enum : int {
@@ -62,6 +68,8 @@ enum : int {
   C_TO_SITE = 11,    // first bounded wait that gave up: its site and two words of context
   C_TO_A = 12,
   C_TO_B = 13,
+  C_WALK_SM = 14,    // 1 + the SM of the (first) walker: a streaming CTA there takes no units
+  C_SCAN_SM = 15,    // 1 + the SM of the scanner: likewise
   C_COUNT = 16
 };
 enum : uint32_t {
@@ -74,17 +82,28 @@ enum : uint32_t {
 
 // ---- statistics (accumulated on the device, read and cleared by the host)
 enum : int {
-  S_TILES = 0,        // tiles processed
+  S_TILES = 0,        // tiles whose runs were formed
   S_TILE_COMPLEX,     // tiles published with an item list
-  S_TILE_OVERFLOW,    // tiles whose items did not fit (walked from x)
-  S_LANE_RAW,         // 16-term lanes published as raw terms (plan range across a power of two)
-  S_LANE_RAW2,        // ... of which with prefix tables for one crossing
-  S_LANE_TIE,         // lanes with a tie, composed in order
-  S_WALK_BATCHES,     // header batches the walk read
+  S_RANGE_X,          // walk ranges whose steps did not fit their slot (read from x)
+  S_LANE_RAW,         // 16-term rows published as raw terms (plan range across a power of two)
+  S_LANE_RAW2,        // ... of which published with prefix tables for one crossing
+  S_LANE_TIE,         // rows with a tie, composed in order
+  S_WALK_BATCHES,     // walk ranges applied in order
   S_WALK_SEGMENTS,    // composites the walk applied
   S_RUN_REJECTED,     // runs the walk's exact check refused (their terms were added one by one)
   S_TERMS_DADD,       // terms the walk added with a hardware fp64 add
   S_RAW_ROUNDS,       // warp rounds of the walk's raw-term resolution
+  S_CY_WALK_WAIT,     // SM cycles the walk's producer warps waited for tile headers
+  S_CY_WALK_SERIAL,   // SM cycles of the walk's in-order warp applying steps
+  S_CY_WALK_RAW,      // SM cycles of the walk's raw-term resolution (within the in-order passes)
+  S_CY_TMA_WAIT,      // SM cycles, summed over warps: waiting for a unit's copy
+  S_CY_PLAN,          // ... plan units (from the copy to the tile's sums published)
+  S_CY_PFX_WAIT,      // ... run units waiting for a prefix that the copy did not bring
+  S_CY_RUN,           // ... run units (from the prefix to the tile's header)
+  S_SCAN_WINDOWS,     // windows the scanner published
+  S_SCAN_POLLS,       // scanner polls of tiles' sums
+  S_PFX_LATE,         // run units whose prefix came after their copy
+  S_ALONE,            // streaming CTAs that left their SM to the walker or the scanner
   S_ACCUM_END,
   S_T_START = 24,     // timestamps of the latest call (globaltimer): first CTA start
   S_T_STREAM_END,     // last tile header published (max over CTAs)
@@ -110,8 +129,10 @@ struct Params {
   int32_t fault_mode;          // 0 none; 1 the header of tile fault_arg is withheld (tests)
   int64_t fault_arg;
   uint64_t wait_ns;            // limit of every bounded device wait
+  int64_t wave;                // plan units run this many tiles ahead of run units
   // workspace
-  uint4 *status;               // per tile: the plan's aggregate or inclusive prefix (16 bytes)
+  uint4 *status;               // per tile: the tile's own sums, published by its plan unit (16 bytes)
+  uint4 *prec;                 // per tile: kPrecWords words -- the exclusive prefix (the scanner), the warp sums (the plan)
   Rec *hdr;                    // per tile: its header
   Rec *items;                  // kItemSlots per tile
   uint32_t *ctr;               // C_COUNT counters

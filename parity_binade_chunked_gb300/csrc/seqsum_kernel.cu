@@ -84,23 +84,31 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
       "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
 }
+// Words other CTAs of the same launch write or read while it runs: relaxed
+// accesses at GPU scope (volatile ones would be system scope, which on a
+// CPU-coherent node costs a round trip far longer than the L2's).
 __device__ __forceinline__ uint4 ld_vol_v4(const uint4 *p) {
   uint4 v;
-  asm volatile("ld.volatile.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p)
                : "memory");
   return v;
 }
 __device__ __forceinline__ void st_vol_v4(uint4 *p, uint4 v) {
-  asm volatile("st.volatile.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+  asm volatile("st.relaxed.gpu.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
 __device__ __forceinline__ void ld_vol_v2(const void *p, uint64_t &a, uint64_t &b) {
-  asm volatile("ld.volatile.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 __device__ __forceinline__ void st_vol_v2(void *p, uint64_t a, uint64_t b) {
-  asm volatile("st.volatile.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+  asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 __device__ __forceinline__ void fence_acq_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ uint64_t dbits(double v) { return (uint64_t)__double_as_longlong(v); }
@@ -127,6 +135,37 @@ __device__ __noinline__ void note_timeout(const Params &p, uint32_t err, uint32_
     p.ctr[C_TO_B] = b;
   }
 }
+
+// profiling builds: a timeline of the units of four streaming CTAs (globaltimer
+// stamps of compute warp 0 and of the producer) in the diagnostic words
+#ifdef SEQSUM_PROFILE
+__device__ __forceinline__ void tl_mark(const Params &p, int role, int who, uint32_t u, int k) {
+  const int c = role - p.nwalkers - 1;
+  if (c < 0 || c >= 2 || u >= 96) return;
+  p.dbg[(c * 2 + who) * 512 + u * 5 + k] = gtimer();
+}
+#define TL(p, role, who, u, k) tl_mark((p), (role), (who), (u), (k))
+// the walk's phases: SM cycles per phase, summed over batches (thread 0)
+#define WPH(k)                                              \
+  do {                                                      \
+    if (threadIdx.x == 0) {                                 \
+      const uint64_t now_ = clock64();                      \
+      atomicAdd(&p.dbg[2048 + (k)], now_ - wph_last);       \
+      wph_last = now_;                                      \
+    }                                                       \
+  } while (0)
+#define WPH_INIT uint64_t wph_last = clock64()
+// the walk's ranges: globaltimer stamps (headers in, slot handed over, slot taken, range applied)
+#define WRT(r, k)                                                       \
+  do {                                                                  \
+    if ((threadIdx.x & 31) == 0 && (r) < 64) p.dbg[2100 + 4 * (r) + (k)] = gtimer(); \
+  } while (0)
+#else
+#define WRT(r, k) ((void)0)
+#define TL(p, role, who, u, k) ((void)0)
+#define WPH(k) ((void)0)
+#define WPH_INIT ((void)0)
+#endif
 
 // ------------------------------------------------------------------ double-float (two floats)
 struct DF {
@@ -158,6 +197,7 @@ struct Item {
   Run r;
   uint32_t kind, eb, count, start;
 };
+constexpr uint32_t kNoKey = 0xFFFFFFFFu;   // the binade key of a record that is not a run (it never merges)
 
 __device__ __forceinline__ uint64_t pack_meta(uint32_t kind, uint32_t eb, int32_t d, uint32_t flags, uint32_t count,
                                               uint32_t start) {
@@ -225,40 +265,59 @@ __device__ __forceinline__ Run shfl_run_idx(const Run &r, int src) {
 }
 
 // ------------------------------------------------------------------ shared memory
+// One stage of a streaming CTA: the copy of a unit's tile, and what the
+// producer warp wrote about the unit (read by the compute warps before they
+// release the stage).
+struct __align__(16) StageSm {
+  uint4 prec[kPrecWords];       // run units: the tile's prefix and warp sums, copied beside the tile
+  int64_t tile;                 // -1: none (the compute warps stop)
+  int64_t geo[5];               // row0, g_lo, g_hi, t_first, sum
+  uint32_t tma;                 // the tile comes by TMA
+  int plan;                     // a plan unit (else a run unit)
+};
+
+// The combining state of a unit while its warps finish it (a ring of 4: a
+// warp can be at most three units ahead of the slowest).  The last warp to
+// finish is found with a shared atomic counter.
+constexpr int kUnitSlots = 4;
+struct UnitSm {
+  int done_cnt;                     // warps done with the unit
+  float wfs[kWarps], wfa[kWarps];   // plan units: the warps' sums
+  long long wred[kWarps][3];        // run units: the warps' runs when each is one run: inc, lo, hi
+  int32_t wd[kWarps];               // ... and its odd-start adjustment (non-zero only with a tie)
+  uint32_t wflags[kWarps];
+  int32_t wkey[kWarps];             // the warp's binade key (one run), or -1 (items)
+  uint32_t wcnt[kWarps];            // the warp's items (when it is not one run)
+};
+
 struct Smem {
-  uint64_t full[kStages];            // TMA mbarriers, one per stage
-  int64_t st_tile[kStages];          // the stage's tile (-1: none)
-  int64_t st_geo[kStages][5];        // row0, g_lo, g_hi, t_first, sum
-  uint32_t st_flags[kStages];        // bit 0: the tile came by TMA
-  float wfs[kWarps], wfa[kWarps];    // warp totals of the plan sums
-  DF excl;                           // the prefix before the tile
-  float excl_abs;
-  int32_t web[kWarps];
-  int32_t wok[kWarps];
-  uint32_t wslots[kWarps];
-  long long wred[kWarps][3];
-  uint32_t wfl_and[kWarps], wfl_or[kWarps];
+  uint64_t full[kStages];            // a stage's copy landed (and the producer's words about it)
+  uint64_t empty[kStages];           // the compute warps have read the stage (8 arrivals)
+  StageSm st[kStages];
+  UnitSm us[kUnitSlots];
   int role;
+  int alone;                         // a streaming CTA on the walker's or the scanner's SM
   uint32_t tag;
   int64_t ntiles;
   int fail;
   int broken;                        // this streaming CTA stopped using TMA after a timeout
   int count;
-  int nseg;
   int wk;
   uint64_t S;                        // the walk's running value (bits)
+  uint32_t prof_i;                   // profiling builds: how a raw row with tables ended
   uint64_t t_stream_end;
-  // walker block scan
-  Run wtot[kWarps];
-  int wtot_head[kWarps];
-  int wstart[kWarps];
-  int whead0[kWarps + 1];
-  uint32_t wtails[kWarps];
-  unsigned long long stat[S_ACCUM_END];
+  // the walk's slots: handed over by mbarriers, their uses counted on each side
+  uint64_t wfull[kWarps];
+  uint64_t wempty[kWarps];
+  uint32_t wuse_p[kWarps];
+  uint32_t wuse_c[kWarps];
+  unsigned long long stat[kBlockWarps][S_ACCUM_END];   // per warp (written by one lane of it)
 };
 
+// Counters: each warp adds to its own row (one lane of the warp at a time);
+// the rows are summed when the CTA ends.
 __device__ __forceinline__ void stat_add(Smem &sm, int which, unsigned long long v) {
-  atomicAdd(&sm.stat[which], v);
+  sm.stat[threadIdx.x >> 5][which] += v;
 }
 
 // ------------------------------------------------------------------ tile geometry
@@ -296,74 +355,6 @@ __device__ __forceinline__ Geo tile_geo(const Params &p, int64_t t) {
   return g;
 }
 
-// ------------------------------------------------------------------ the plan's look-back
-// status[t] = {hi, lo, abs, tag << 8 | flag} (flag 1: the tile's own sum,
-// 2: the inclusive prefix through the tile).  Run by one warp.  Returns the
-// exclusive prefix of tile t (not the first of its sum) and publishes t's
-// inclusive prefix.
-__device__ __noinline__ void lookback(const Params &p, int64_t t, int64_t t_first, DF agg, float agg_abs, uint32_t tag,
-                                      DF &excl, float &excl_abs) {
-  const int lane = threadIdx.x & 31;
-  if (lane == 0)
-    st_vol_v4(&p.status[t], make_uint4(__float_as_uint(agg.hi), __float_as_uint(agg.lo), __float_as_uint(agg_abs),
-                                       (tag << 8) | 1u));
-  float acc = 0.0f, acc_abs = 0.0f;
-  DF incl = DF{0.0f, 0.0f};
-  int64_t base = t - 1;
-  const uint64_t t0 = gtimer();
-  bool timed_out = false;
-  while (true) {
-    const int64_t idx = base - lane;
-    const bool inrange = idx >= t_first;
-    uint4 st = make_uint4(0, 0, 0, 0);
-    int first_incl = 32;
-    uint32_t spin = 0;
-    while (true) {
-      if (inrange) st = ld_vol_v4(&p.status[idx]);
-      const bool valid = inrange && (st.w >> 8) == tag && (st.w & 3u) != 0u;
-      const bool inc = valid && (st.w & 3u) == 2u;
-      const uint32_t bi = __ballot_sync(kFull, inc);
-      const uint32_t bv = __ballot_sync(kFull, valid);
-      first_incl = bi ? __ffs(bi) - 1 : 32;
-      const uint32_t need = first_incl >= 31 ? kFull : ((2u << first_incl) - 1u);
-      if ((bv & need) == need) break;
-      // the decision to give up is the warp's (a lane alone must not leave the ballots)
-      if (__any_sync(kFull, (++spin & 63u) == 0u && gtimer() - t0 > p.wait_ns)) {
-        timed_out = true;
-        break;
-      }
-      __nanosleep(32);
-    }
-    if (timed_out) {
-      if (lane == 0) note_timeout(p, ERR_PLAN_TIMEOUT, 1, (uint32_t)t, (uint32_t)base);
-      break;
-    }
-    // the tiles' own sums before the first inclusive prefix, and every abs up to it
-    float v = (lane < first_incl) ? __fadd_rn(__uint_as_float(st.x), __uint_as_float(st.y)) : 0.0f;
-    float va = (lane <= first_incl) ? __uint_as_float(st.z) : 0.0f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      v += __shfl_xor_sync(kFull, v, o);
-      va += __shfl_xor_sync(kFull, va, o);
-    }
-    acc += v;
-    acc_abs += va;
-    if (first_incl < 32) {
-      incl.hi = __uint_as_float(__shfl_sync(kFull, st.x, first_incl));
-      incl.lo = __uint_as_float(__shfl_sync(kFull, st.y, first_incl));
-      break;
-    }
-    base -= 32;
-  }
-  excl = df_add(incl, DF{acc, 0.0f});
-  excl_abs = acc_abs;
-  if (lane == 0) {
-    const DF in = df_add(excl, agg);
-    st_vol_v4(&p.status[t], make_uint4(__float_as_uint(in.hi), __float_as_uint(in.lo),
-                                       __float_as_uint(excl_abs + agg_abs), (tag << 8) | 2u));
-  }
-}
-
 // ------------------------------------------------------------------ forced plans (tests)
 __device__ __forceinline__ uint32_t hash3(uint64_t a, uint32_t b) {
   uint64_t z = a * 0x9E3779B97F4A7C15ull + b * 0xBF58476D1CE4E5B9ull;
@@ -396,25 +387,287 @@ __device__ __forceinline__ void saturate(Run &r) {
   }
 }
 
-// ------------------------------------------------------------------ one tile of a streaming CTA
+// ------------------------------------------------------------------ units of the streaming CTAs
+// Ticket k names a unit: the plan of a tile (its float sums published), or
+// the runs of a tile, W tiles behind the plans, once the scanner has turned
+// the sums into the tile's prefix.  Every unit depends only on units with
+// smaller tickets, so the smallest unfinished unit can always proceed.
+__device__ __forceinline__ int64_t unit_of(int64_t k, int64_t P, int64_t W, bool &plan) {
+  plan = false;
+  if (k < 0) return -1;
+  if (W >= P) {
+    plan = k < P;
+    return plan ? k : (k < 2 * P ? k - P : -1);
+  }
+  if (k < W) {
+    plan = true;
+    return k;
+  }
+  const int64_t j = k - W;
+  if (j < 2 * (P - W)) {
+    plan = (j & 1) == 0;
+    return plan ? W + (j >> 1) : (j >> 1);
+  }
+  const int64_t r = (P - W) + (j - 2 * (P - W));
+  return r < P ? r : -1;
+}
+
 __device__ __forceinline__ int float_binade(float f) { return (int)((__float_as_uint(f) >> 23) & 0xFFu); }
+__device__ __forceinline__ int vload(const int *p) { return *reinterpret_cast<const volatile int *>(p); }
 
-__device__ __forceinline__ void process_tile(const Params &p, Smem &sm, const uint64_t (&v)[kLaneTerms], int64_t t,
-                                          const Geo &g, uint32_t tag) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+__device__ __forceinline__ Geo stage_geo(const StageSm &st) {
+  Geo g;
+  g.row0 = st.geo[0];
+  g.g_lo = st.geo[1];
+  g.g_hi = st.geo[2];
+  g.t_first = st.geo[3];
+  g.sum = (int32_t)st.geo[4];
+  return g;
+}
 
-  // ---- plan sums of the row
-  float fs = 0.0f, fa = 0.0f;
-  uint32_t mx = 0;
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Stage s takes unit k (one thread): its tile's copy, and for a run unit the
+// tile's plan record (prefix and warp sums) beside it.  The stage's per-unit
+// state is cleared first; the mbarrier completion publishes it to the warps.
+__device__ __forceinline__ void stage_fill(const Params &p, Smem &sm, unsigned char *stages, const CUtensorMap *tmap,
+                                           int s, int64_t k, int64_t ntiles) {
+  StageSm &st = sm.st[s];
+  bool plan = false;
+  const int64_t t = unit_of(k, ntiles, p.wave, plan);
+  if (t < 0) {
+    st.tile = -1;
+    st.tma = 0;
+    mbar_arrive(&sm.full[s]);
+    return;
+  }
+  const Geo g = tile_geo(p, t);
+  st.tile = t;
+  st.plan = plan ? 1 : 0;
+  st.geo[0] = g.row0;
+  st.geo[1] = g.g_lo;
+  st.geo[2] = g.g_hi;
+  st.geo[3] = g.t_first;
+  st.geo[4] = g.sum;
+  const bool tma = p.tma_rows > 0 && g.row0 < p.tma_rows;
+  st.tma = tma ? 1u : 0u;
+  const uint32_t side = plan ? 0u : (uint32_t)(kPrecWords * sizeof(uint4));
+  if (tma || side) {
+    mbar_expect_tx(&sm.full[s], (tma ? (uint32_t)kStageBytes : 0u) + side);
+    if (tma) tma_load_2d(stages + s * kStageBytes, tmap, &sm.full[s], 0, (int32_t)g.row0);
+    if (side) bulk_load(st.prec, p.prec + t * kPrecWords, side, &sm.full[s]);
+  } else {
+    mbar_arrive(&sm.full[s]);
+  }
+}
+
+// A warp waits (bounded) for use `ph` of stage s.  Returns whether the copy
+// landed; a copy that did not is recorded, and the warp reads its rows from x.
+__device__ __forceinline__ bool stage_wait(const Params &p, Smem &sm, int s, uint32_t ph) {
+  const int lane = threadIdx.x & 31;
+  int ok = 1;
+  if (lane == 0) {
+    const uint64_t c0 = clock64();
+    uint64_t t0 = 0;
+    uint32_t spin = 0;
+    while (!mbar_try_wait(&sm.full[s], ph)) {
+      if ((++spin & 255u) == 0u) {
+        const uint64_t now = gtimer();
+        if (!t0) t0 = now;
+        else if (now - t0 > p.wait_ns) {
+          ok = 0;
+          break;
+        }
+      }
+    }
+    if (!ok) {
+      // the copy may still land: wait once more (bounded) so that it cannot
+      // write into the stage after it is reused
+      note_timeout(p, ERR_TMA_TIMEOUT, 2, (uint32_t)s, ph);
+      sm.broken = 1;
+      const uint64_t t1 = gtimer();
+      while (!mbar_try_wait(&sm.full[s], ph) && gtimer() - t1 < p.wait_ns) {
+      }
+    }
+    stat_add(sm, S_CY_TMA_WAIT, clock64() - c0);
+  }
+  ok = __shfl_sync(kFull, ok, 0);
+  if (ok) {
+    // every lane's own wait on the completed phase makes the copy's writes visible to it
+    for (uint32_t k = 0; k < (1u << 20) && !mbar_try_wait(&sm.full[s], ph); k++) {
+    }
+  }
+  return ok != 0;
+}
+
+__device__ __forceinline__ void load_row(const Params &p, const unsigned char *stage, bool lane_tma, int64_t row,
+                                         const Geo &g, uint64_t (&v)[kLaneTerms]) {
+  const int rw = threadIdx.x;   // the row within the tile
+  const bool full = g.row0 * kLaneTerms >= g.g_lo && (g.row0 + kTileRows) * kLaneTerms <= g.g_hi;
+  if (lane_tma) {
+    const unsigned char *rp = stage + rw * 128;
+    const int sw = rw & 7;
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+      const uint4 d = *reinterpret_cast<const uint4 *>(rp + ((q ^ sw) << 4));
+      v[2 * q] = ((uint64_t)d.y << 32) | d.x;
+      v[2 * q + 1] = ((uint64_t)d.w << 32) | d.z;
+    }
+    if (!full) {
+      const int64_t g0 = row * kLaneTerms;
+#pragma unroll
+      for (int j = 0; j < kLaneTerms; j++) {
+        const int64_t gi = g0 + j;
+        if (gi < g.g_lo || gi >= g.g_hi) v[j] = kNegZero;
+      }
+    }
+  } else {
+    const int64_t g0 = row * kLaneTerms;
+    const unsigned long long *xp = reinterpret_cast<const unsigned long long *>(p.x);
+#pragma unroll
+    for (int j = 0; j < kLaneTerms; j++) {
+      const int64_t gi = g0 + j;
+      v[j] = (gi >= g.g_lo && gi < g.g_hi) ? (uint64_t)__ldg(xp + gi) : kNegZero;
+    }
+  }
+}
+
+// A term as a float for the plan, from its bits with integer operations
+// only (this GPU's fp64 pipe, which a conversion instruction would use, is a
+// small fraction of its integer and fp32 rate): the significand truncated to
+// 24 bits; magnitudes below 2^-126 become 0, those of 2^128 and above (and
+// inf, NaN) inf.  The plan only steers the walk: an inexact plan cannot make
+// a result wrong.
+__device__ __forceinline__ float plan_f32(uint64_t b) {
+  const uint32_t hi = (uint32_t)(b >> 32), lo = (uint32_t)b;
+  const uint32_t E = (hi >> 20) & 0x7FFu;
+  uint32_t f = (__funnelshift_l(lo, hi, 3) & 0x7FFFFFu) | ((E - 896u) << 23);
+  f = E <= 896u ? 0u : (E >= 1151u ? 0x7F800000u : f);
+  return __uint_as_float(f | (hi & 0x80000000u));
+}
+
+// The row's plan sums: its terms as floats summed, their magnitudes summed,
+// and the largest high word (sign included).
+__device__ __forceinline__ void row_sums(const uint64_t (&v)[kLaneTerms], float &fs, float &fa, uint32_t &mx) {
+  fs = 0.0f;
+  fa = 0.0f;
+  mx = 0;
 #pragma unroll
   for (int j = 0; j < kLaneTerms; j++) {
-    const uint32_t hi = (uint32_t)(v[j] >> 32);
-    mx = max(mx, hi);
-    const float f = __double2float_rn(bitsd(v[j]));
+    mx = max(mx, (uint32_t)(v[j] >> 32));
+    const float f = plan_f32(v[j]);
     fs = __fadd_rn(fs, f);
     fa = __fadd_rn(fa, fabsf(f));
   }
-  // warp inclusive scans
+}
+
+// A plan unit, one warp's 32 rows (already loaded): the warp's float sums;
+// the last warp publishes the warps' sums beside the tile's prefix, and the
+// tile's sums for the scanner.  (No fence orders the two: they only steer
+// the plan, which cannot make a result wrong.)
+__device__ __forceinline__ void plan_unit(const Params &p, Smem &sm, UnitSm &us, int64_t t,
+                                          const uint64_t (&v)[kLaneTerms], uint32_t tag) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  float fs, fa;
+  uint32_t mx;
+  row_sums(v, fs, fa, mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    fs = __fadd_rn(fs, __shfl_xor_sync(kFull, fs, o));
+    fa = __fadd_rn(fa, __shfl_xor_sync(kFull, fa, o));
+  }
+  int last = 0;
+  if (lane == 0) {
+    us.wfs[w] = fs;
+    us.wfa[w] = fa;
+    __threadfence_block();
+    last = atomicAdd(&us.done_cnt, 1) == kWarps - 1;
+  }
+  last = __shfl_sync(kFull, last, 0);
+  if (!last) return;
+  __threadfence_block();
+  if (lane < 2 * kWarps / 4) {
+    // the warps' sums (4 floats a lane) beside the tile's prefix
+    const float *src = lane < kWarps / 4 ? &us.wfs[4 * lane] : &us.wfa[4 * (lane - kWarps / 4)];
+    st_vol_v4(&p.prec[t * kPrecWords + 1 + lane], make_uint4(__float_as_uint(src[0]), __float_as_uint(src[1]),
+                                                             __float_as_uint(src[2]), __float_as_uint(src[3])));
+  }
+  if (lane == 0) {
+    DF agg = DF{0.0f, 0.0f};
+    float agg_abs = 0.0f;
+    for (int k = 0; k < kWarps; k++) {
+      agg = df_add(agg, DF{us.wfs[k], 0.0f});
+      agg_abs = __fadd_rn(agg_abs, us.wfa[k]);
+    }
+    st_vol_v4(&p.status[t], make_uint4(__float_as_uint(agg.hi), __float_as_uint(agg.lo), __float_as_uint(agg_abs),
+                                       (tag << 8) | 1u));
+  }
+}
+
+// A run unit, one warp's 32 rows (already loaded): each row's binade from
+// its prefix range, the rows' runs and the warp's record; the last warp
+// publishes the tile's header.  pf is the tile's prefix as the copy brought
+// it, bs/ba the sums of the warps before this one.
+__device__ __forceinline__ void run_unit(const Params &p, Smem &sm, UnitSm &us, int64_t t, const Geo &g,
+                                         const uint64_t (&v)[kLaneTerms], uint4 pf, float bs, float ba,
+                                         uint32_t tag) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, tid = threadIdx.x;
+  if (!((pf.w >> 8) == tag && (pf.w & 3u) == 2u)) {
+    // the scanner had not published the prefix when the copy ran: poll it
+    const uint64_t c0 = clock64();
+    int ok = 0;
+    if (lane == 0) {
+      uint64_t t0 = 0;
+      for (uint32_t spin = 0;; spin++) {
+        pf = ld_vol_v4(&p.prec[t * kPrecWords]);
+        if ((pf.w >> 8) == tag && (pf.w & 3u) == 2u) {
+          ok = 1;
+          break;
+        }
+        if ((spin & 15u) == 15u) {
+          const uint64_t now = gtimer();
+          if (!t0) t0 = now;
+          else if (now - t0 > p.wait_ns) break;
+        }
+        __nanosleep(64);
+      }
+      if (!ok) note_timeout(p, ERR_PLAN_TIMEOUT, 5, (uint32_t)t, 0);
+      stat_add(sm, S_PFX_LATE, 1);
+      stat_add(sm, S_CY_PFX_WAIT, clock64() - c0);
+    }
+    ok = __shfl_sync(kFull, ok, 0);
+    pf.x = __shfl_sync(kFull, pf.x, 0);
+    pf.y = __shfl_sync(kFull, pf.y, 0);
+    pf.z = __shfl_sync(kFull, pf.z, 0);
+    if (!ok) pf = make_uint4(0, 0, 0, 0);   // the plan only: a prefix taken as 0
+    fence_acq_rel();
+    // the warps' sums, read again after the prefix
+    bs = ba = 0.0f;
+    if (lane < kWarps) {
+      const float *ws = reinterpret_cast<const float *>(&p.prec[t * kPrecWords + 1]);
+      const float a = lane < w ? ws[lane] : 0.0f, b = lane < w ? ws[kWarps + lane] : 0.0f;
+      bs = a;
+      ba = b;
+    }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) {
+      bs = __fadd_rn(bs, __shfl_xor_sync(kFull, bs, o));
+      ba = __fadd_rn(ba, __shfl_xor_sync(kFull, ba, o));
+    }
+    bs = __shfl_sync(kFull, bs, 0);
+    ba = __shfl_sync(kFull, ba, 0);
+  }
+  const uint64_t c0 = clock64();
+  const DF ex = DF{__uint_as_float(pf.x), __uint_as_float(pf.y)};
+  const float ex_abs = __uint_as_float(pf.z);
+  float fs, fa;
+  uint32_t mx;
+  row_sums(v, fs, fa, mx);
   float is = fs, ia = fa;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -424,53 +677,14 @@ __device__ __forceinline__ void process_tile(const Params &p, Smem &sm, const ui
       ia = __fadd_rn(ia, b);
     }
   }
-  if (lane == 31) {
-    sm.wfs[w] = is;
-    sm.wfa[w] = ia;
-  }
   float xs = __shfl_up_sync(kFull, is, 1), xa = __shfl_up_sync(kFull, ia, 1);
   if (lane == 0) xs = xa = 0.0f;
-  __syncthreads();
-  float bs = 0.0f, ba = 0.0f;
-  for (int k = 0; k < w; k++) {
-    bs = __fadd_rn(bs, sm.wfs[k]);
-    ba = __fadd_rn(ba, sm.wfa[k]);
-  }
   xs = __fadd_rn(bs, xs);
   xa = __fadd_rn(ba, xa);
 
-  // ---- the prefix before the tile
-  if (w == 0) {
-    DF agg = DF{0.0f, 0.0f};
-    float agg_abs = 0.0f;
-    for (int k = 0; k < kWarps; k++) {
-      agg = df_add(agg, DF{sm.wfs[k], 0.0f});
-      agg_abs = __fadd_rn(agg_abs, sm.wfa[k]);
-    }
-    DF ex;
-    float ex_abs;
-    if (t == g.t_first) {
-      ex = df_of_double(p.offsets ? p.s0s[g.sum] : p.s0);
-      ex_abs = fabsf(ex.hi);
-      if (lane == 0) {
-        const DF in = df_add(ex, agg);
-        st_vol_v4(&p.status[t], make_uint4(__float_as_uint(in.hi), __float_as_uint(in.lo),
-                                           __float_as_uint(__fadd_rn(ex_abs, agg_abs)), (tag << 8) | 2u));
-      }
-    } else {
-      lookback(p, t, g.t_first, agg, agg_abs, tag, ex, ex_abs);
-    }
-    if (lane == 0) {
-      sm.excl = ex;
-      sm.excl_abs = ex_abs;
-    }
-  }
-  __syncthreads();
-
-  // ---- the row's binade
-  const DF ex = sm.excl;
+  // ---- the row's binade: its prefix range inside one binade, with an allowance
   const float Pf = __fadd_rn(ex.hi, __fadd_rn(ex.lo, xs));
-  const float A = __fadd_rn(__fadd_rn(sm.excl_abs, xa), fa);
+  const float A = __fadd_rn(__fadd_rn(ex_abs, xa), fa);
   const float marg = __fadd_rn(__fmul_rn(A, 4.76837158203125e-7f /* 2^-21 */), 1e-30f);
   const float pos = __fmul_rn(0.5f, __fadd_rn(fa, fs)), neg = __fmul_rn(0.5f, __fsub_rn(fa, fs));
   const float lo_ = __fsub_rn(__fsub_rn(Pf, neg), marg), hi_ = __fadd_rn(__fadd_rn(Pf, pos), marg);
@@ -560,17 +774,6 @@ __device__ __forceinline__ void process_tile(const Params &p, Smem &sm, const ui
     r.flags = F_NONNEG | F_NONPOS | F_ZERO | (allneg ? (uint32_t)F_ALLNEGZ : 0u);
   }
   const uint32_t key = raw ? 0xFFFFFFFFu : eb;   // zero rows keep the plan's binade (0 where it has none)
-
-  // ---- one header, or a list of items
-  const uint32_t key0 = __shfl_sync(kFull, key, 0);
-  const bool same = __all_sync(kFull, !raw && !general && key == key0);
-  if (lane == 0) {
-    sm.wok[w] = same;
-    sm.web[w] = (int32_t)key;
-  }
-  __syncthreads();
-  bool fast = true;
-  for (int k = 0; k < kWarps; k++) fast = fast && sm.wok[k] && sm.web[k] == sm.web[0];
   const uint32_t nraw = __popc(__ballot_sync(kFull, raw));
   const uint32_t ntie = __popc(__ballot_sync(kFull, general));
   if (lane == 0) {
@@ -578,7 +781,27 @@ __device__ __forceinline__ void process_tile(const Params &p, Smem &sm, const ui
     if (ntie) stat_add(sm, S_LANE_TIE, ntie);
   }
 
-  if (fast) {
+  // ---- the warp's record: one run, or its items in its region of the tile's item area
+  const uint32_t key0 = __shfl_sync(kFull, key, 0);
+  const bool samekey = __all_sync(kFull, !raw && key == key0);
+  if (samekey && ntie != 0) {
+    // one binade with a tie: the rows' runs composed in order (the even/odd rule)
+    Run seg = r;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const Run q = shfl_run_up(seg, o);
+      if (lane >= o) seg = run_compose(q, seg);
+    }
+    if (lane == 31) {
+      us.wred[w][0] = seg.inc;
+      us.wred[w][1] = seg.lo;
+      us.wred[w][2] = seg.hi;
+      us.wd[w] = seg.d;
+      us.wflags[w] = seg.flags;
+      us.wkey[w] = (int32_t)key0;
+      us.wcnt[w] = 1;
+    }
+  } else if (samekey) {
     long long a = r.inc, b = r.lo, d = r.hi;
     uint32_t fand = r.flags & (F_NONNEG | F_NONPOS | F_ZERO | F_ALLNEGZ), fo = r.flags & F_POISON;
 #pragma unroll
@@ -590,251 +813,570 @@ __device__ __forceinline__ void process_tile(const Params &p, Smem &sm, const ui
     fand = __reduce_and_sync(kFull, fand);
     fo = __reduce_or_sync(kFull, fo);
     if (lane == 0) {
-      sm.wred[w][0] = a;
-      sm.wred[w][1] = b;
-      sm.wred[w][2] = d;
-      sm.wfl_and[w] = fand;
-      sm.wfl_or[w] = fo;
+      us.wred[w][0] = a;
+      us.wred[w][1] = b;
+      us.wred[w][2] = d;
+      us.wflags[w] = fand | fo;
+      us.wd[w] = 0;
+      us.wkey[w] = (int32_t)key0;
+      us.wcnt[w] = 1;
     }
-    __syncthreads();
-    if (tid == 0) {
+  } else {
+    const uint32_t pkey = __shfl_up_sync(kFull, key, 1);
+    const bool praw = __shfl_up_sync(kFull, raw, 1);
+    const bool head = lane == 0 || raw || praw || key != pkey;
+    int sstart = head ? lane : 0;
+    Run seg = r;
+    bool hf = head;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const Run q = shfl_run_up(seg, o);
+      const bool qh = __shfl_up_sync(kFull, hf, o);
+      const int qs = __shfl_up_sync(kFull, sstart, o);
+      if (lane >= o) {
+        if (!hf) seg = run_compose(q, seg);
+        hf = hf || qh;
+        sstart = max(sstart, qs);
+      }
+    }
+    const bool nhead = __shfl_down_sync(kFull, head, 1);
+    const bool tail = (lane == 31) || nhead;
+    // a raw row whose plan range crosses one power of two, all of its terms
+    // of the range's sign, carries prefix tables for the two binades
+    bool raw2 = false, rneg = false;
+    uint32_t ea = 0;
+    if (raw) {
+      uint32_t hmin = 0xFFFFFFFFu;
+#pragma unroll
+      for (int j = 0; j < kLaneTerms; j++)
+        hmin = min(hmin, (v[j] << 1) == 0 ? 0xFFFFFFFFu : (uint32_t)(v[j] >> 32));
+      int a = 0, b = 0;
+      if (lo_ > 0.0f && mx < 0x80000000u) {
+        a = float_binade(lo_);
+        b = float_binade(hi_);
+      } else if (hi_ < 0.0f && hmin >= 0x80000000u) {
+        a = float_binade(-hi_);
+        b = float_binade(-lo_);
+        rneg = true;
+      }
+      ea = (uint32_t)(a - 127 + 1023);
+      raw2 = a >= 1 && (b == a || b == a + 1) && ea >= 54u && ea + 1u <= 2046u;
+    }
+    // the warp's region: one descriptor per item, in the order of their terms
+    // (a warp has at most one item per row: it always fits)
+    const uint32_t mdesc = __ballot_sync(kFull, raw || tail);
+    const uint32_t total = __popc(mdesc);
+    const uint32_t nraw2 = __popc(__ballot_sync(kFull, raw2));
+    if (lane == 0 && nraw2) stat_add(sm, S_LANE_RAW2, nraw2);
+    const uint32_t at = __popc(mdesc & ((1u << lane) - 1u));
+    {
+      Rec *area = p.items + t * kItemSlots + w * kWarpSlots;
+      if (raw) {
+        Item it;
+        it.r = run_empty();
+        it.kind = raw2 ? K_RAW2 : K_RAW;
+        it.eb = raw2 ? ea : 0u;
+        it.count = kLaneTerms;
+        it.start = (uint32_t)tid * kLaneTerms;
+        Rec q = pack_item(it, 0);
+        q.w[0] = rneg ? 1u : 0u;
+        st_rec(&area[at], q);
+      } else if (tail) {
+        Item it;
+        it.r = seg;
+        it.kind = K_RUN;
+        it.eb = key;
+        it.count = (uint32_t)(lane - sstart + 1) * kLaneTerms;
+        it.start = (uint32_t)(w * 32 + sstart) * kLaneTerms;
+        st_rec(&area[at], pack_item(it, 0));
+      }
+      __threadfence();   // the items before the header that publishes them
+    }
+    if (lane == 0) {
+      us.wkey[w] = -1;
+      us.wcnt[w] = total;
+    }
+  }
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) {
+    __threadfence_block();
+    last = atomicAdd(&us.done_cnt, 1) == kWarps - 1;
+  }
+  last = __shfl_sync(kFull, last, 0);
+  if (!last) return;
+
+  // ---- the last warp: the tile's header, then the stage's next tile
+  __threadfence_block();
+  const int32_t k0 = us.wkey[0];
+  bool one = true;
+  for (int k = 0; k < kWarps; k++) one = one && us.wkey[k] >= 0 && us.wkey[k] == k0;
+  if (one) {
+    if (lane == 0) {
       Item h;
       h.r.inc = h.r.lo = h.r.hi = 0;
       h.r.d = 0;
-      uint32_t fa2 = 0xFFu, fo2 = 0;
+      uint32_t fand = 0xFFu, fo = 0;
+      bool tie = false;
       for (int k = 0; k < kWarps; k++) {
-        h.r.inc += sm.wred[k][0];
-        h.r.lo += sm.wred[k][1];
-        h.r.hi += sm.wred[k][2];
-        fa2 &= sm.wfl_and[k];
-        fo2 |= sm.wfl_or[k];
+        h.r.inc += us.wred[k][0];
+        h.r.lo += us.wred[k][1];
+        h.r.hi += us.wred[k][2];
+        fand &= us.wflags[k];
+        fo |= us.wflags[k];
+        tie = tie || us.wd[k] != 0;
       }
-      h.r.flags = fa2 | fo2;
+      h.r.flags = (fand & (F_NONNEG | F_NONPOS | F_ZERO | F_ALLNEGZ)) | (fo & F_POISON);
+      if (tie) {
+        // a warp with a tie: the warps' runs composed in order
+        h.r = run_empty();
+        for (int k = 0; k < kWarps; k++) {
+          Run q;
+          q.inc = us.wred[k][0];
+          q.lo = us.wred[k][1];
+          q.hi = us.wred[k][2];
+          q.d = us.wd[k];
+          q.flags = us.wflags[k];
+          h.r = k == 0 ? q : run_compose(h.r, q);
+        }
+      }
       saturate(h.r);
       h.kind = K_RUN;
-      h.eb = (uint32_t)sm.web[0];
+      h.eb = (uint32_t)k0;
       h.count = kTileTerms;
       h.start = 0;
       if (!(p.fault_mode == 1 && t == p.fault_arg)) st_rec_vol(&p.hdr[t], pack_item(h, tag));
     }
-    return;
-  }
-
-  // ---- items: each warp's maximal runs of one binade, and raw rows
-  const uint32_t pkey = __shfl_up_sync(kFull, key, 1);
-  const bool praw = __shfl_up_sync(kFull, raw, 1);
-  bool head = lane == 0 || raw || praw || key != pkey;
-  int sstart = head ? lane : 0;
-  Run s = r;
-  bool hf = head;
+  } else {
+    // a complex tile: the warps' items in the order of their terms (a warp
+    // that is one run gives its run), consecutive runs of one binade composed,
+    // written compactly from slot 0 of the tile's item area.  The tile's item
+    // i lies at slot 32 k + j >= i (a warp has at most 32), so every write
+    // lands on a slot already read.
+    uint32_t ck = 0;
+    if (lane < kWarps) ck = us.wkey[lane] >= 0 ? 1u : us.wcnt[lane];
+    uint32_t cex = ck;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const Run q = shfl_run_up(s, o);
-    const bool qh = __shfl_up_sync(kFull, hf, o);
-    const int qs = __shfl_up_sync(kFull, sstart, o);
-    if (lane >= o) {
-      if (!hf) s = run_compose(q, s);
-      hf = hf || qh;
-      sstart = max(sstart, qs);
+    for (int o = 1; o < kWarps; o <<= 1) {
+      const uint32_t q = __shfl_up_sync(kFull, cex, o);
+      if (lane >= o) cex += q;
     }
-  }
-  const bool nhead = __shfl_down_sync(kFull, head, 1);
-  const bool tail = (lane == 31) || nhead;
-  const uint32_t my = raw ? (uint32_t)kRawSlots : ((tail && !raw) ? 1u : 0u);
-  uint32_t ex_sl = my;
+    const int T = (int)__shfl_sync(kFull, cex, kWarps - 1);
+    cex -= ck;
+    Rec *area = p.items + t * kItemSlots;
+    const uint32_t lt = (1u << lane) - 1u;
+    int M = 0;
+    Run carry = run_empty();                 // the open run at the end of the chunk before
+    uint32_t ckey = kNoKey, cstart = 0, cend = 0;
+    bool pending = false;
+    for (int c = 0; c < T; c += 32) {
+      const int i = c + lane;
+      const bool in = i < T;
+      // the warp whose items hold item i
+      int k = 0;
+      uint32_t kex = 0;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t q = __shfl_up_sync(kFull, ex_sl, o);
-    if (lane >= o) ex_sl += q;
-  }
-  if (lane == 31) sm.wslots[w] = ex_sl;
-  ex_sl -= my;
-  __syncthreads();
-  uint32_t base = 0, total = 0;
-  for (int k = 0; k < kWarps; k++) {
-    if (k < w) base += sm.wslots[k];
-    total += sm.wslots[k];
-  }
-  if (total > (uint32_t)kItemSlots) {
-    if (tid == 0) {
-      Item h;
-      h.r = run_empty();
-      h.kind = K_OVERFLOW;
-      h.eb = 0;
-      h.count = 0;
-      h.start = 0;
-      stat_add(sm, S_TILE_OVERFLOW, 1);
-      if (!(p.fault_mode == 1 && t == p.fault_arg)) st_rec_vol(&p.hdr[t], pack_item(h, tag));
-    }
-    return;
-  }
-  Rec *area = p.items + t * kItemSlots;
-  const uint32_t at = base + ex_sl;
-  const uint32_t row_start = (uint32_t)(w * 32 + lane) * kLaneTerms;
-  if (raw) {
-    if (SQ_OK(p, at + kRawSlots <= (uint32_t)kItemSlots, 11, at)) {
+      for (int q = 0; q < kWarps; q++) {
+        const uint32_t e = __shfl_sync(kFull, cex, q), n = __shfl_sync(kFull, ck, q);
+        if (in && e <= (uint32_t)i && (uint32_t)i < e + n) {
+          k = q;
+          kex = e;
+        }
+      }
       Item it;
       it.r = run_empty();
-      it.kind = K_RAW;
+      it.kind = K_OVERFLOW;
       it.eb = 0;
-      it.count = kLaneTerms;
-      it.start = row_start;
-      st_rec(&area[at], pack_item(it, 0));
-      uint4 *dst = reinterpret_cast<uint4 *>(&area[at + 1]);
+      it.start = it.count = 0;
+      if (in) {
+        if (us.wkey[k] >= 0) {
+          it.r.inc = us.wred[k][0];
+          it.r.lo = us.wred[k][1];
+          it.r.hi = us.wred[k][2];
+          it.r.d = us.wd[k];
+          it.r.flags = us.wflags[k];
+          saturate(it.r);
+          it.kind = K_RUN;
+          it.eb = (uint32_t)us.wkey[k];
+          it.count = 32 * kLaneTerms;
+          it.start = (uint32_t)k * 32 * kLaneTerms;
+        } else {
+          it = unpack_item(ld_rec_vol(&area[k * kWarpSlots + (i - (int)kex)]));
+        }
+      }
+      const uint32_t key = (in && it.kind == K_RUN) ? it.eb : kNoKey;
+      uint32_t pkey = __shfl_up_sync(kFull, key, 1);
+      if (lane == 0) pkey = ckey;
+      const bool head = in && (i == 0 || key == kNoKey || pkey == kNoKey || key != pkey);
+      // the open run of the chunk before ends if this chunk begins with a head
+      const bool close_prev = __shfl_sync(kFull, head, 0) && pending;
+      Run rr = it.r;
+      bool f = head;
+      uint32_t from = head ? it.start : 0u;
+      if (lane == 0 && in && !head) {
+        rr = run_compose(carry, rr);
+        from = cstart;
+        f = true;
+      }
 #pragma unroll
-      for (int j = 0; j < kLaneTerms; j += 2)
-        dst[j / 2] = make_uint4((uint32_t)v[j], (uint32_t)(v[j] >> 32), (uint32_t)v[j + 1], (uint32_t)(v[j + 1] >> 32));
+      for (int o = 1; o < 32; o <<= 1) {
+        const Run q = shfl_run_up(rr, o);
+        const bool qh = __shfl_up_sync(kFull, f, o);
+        const uint32_t qf = __shfl_up_sync(kFull, from, o);
+        if (lane >= o) {
+          if (!f) rr = run_compose(q, rr);
+          f = f || qh;
+          from = max(from, qf);
+        }
+      }
+      const uint32_t nkey = __shfl_down_sync(kFull, key, 1);
+      const bool tail = in && (key == kNoKey || i == T - 1 || (lane < 31 && (nkey == kNoKey || nkey != key)));
+      const uint32_t tb = __ballot_sync(kFull, tail);
+      __syncwarp();   // every read of the chunk before any write
+      if (close_prev) {
+        if (lane == 0) {
+          Item m;
+          m.r = carry;
+          saturate(m.r);
+          m.kind = K_RUN;
+          m.eb = ckey;
+          m.start = cstart;
+          m.count = cend - cstart;
+          st_rec(&area[M], pack_item(m, 0));
+        }
+        M++;
+      }
+      if (tail) {
+        Item m = it;
+        if (it.kind == K_RUN) {
+          m.r = rr;
+          saturate(m.r);
+          m.start = from;
+          m.count = it.start + it.count - from;
+        }
+        st_rec(&area[M + __popc(tb & lt)], pack_item(m, 0));
+      }
+      M += __popc(tb);
+      carry = shfl_run_idx(rr, 31);
+      ckey = __shfl_sync(kFull, key, 31);
+      cstart = __shfl_sync(kFull, from, 31);
+      cend = __shfl_sync(kFull, it.start + it.count, 31);
+      pending = __shfl_sync(kFull, in && !tail, 31);
     }
-  } else if (tail) {
-    if (SQ_OK(p, at < (uint32_t)kItemSlots, 12, at)) {
-      Item it;
-      it.r = s;
-      it.kind = K_RUN;
-      it.eb = key;
-      it.count = (uint32_t)(lane - sstart + 1) * kLaneTerms;
-      it.start = (uint32_t)(w * 32 + sstart) * kLaneTerms;
-      st_rec(&area[at], pack_item(it, 0));
+    __threadfence();   // the items before the header that publishes them
+    if (lane == 0) {
+      Rec q;
+      q.w[0] = ((uint64_t)M & kPay56) | ((uint64_t)tag << 56);
+      q.w[1] = (uint64_t)tag << 56;
+      q.w[2] = (uint64_t)tag << 56;
+      q.w[3] = pack_meta(K_COMPLEX, 0, 0, 0, 0, 0) | ((uint64_t)tag << 56);
+      stat_add(sm, S_TILE_COMPLEX, 1);
+      if (!(p.fault_mode == 1 && t == p.fault_arg)) st_rec_vol(&p.hdr[t], q);
     }
   }
-  __threadfence();   // each writer's items before the header that publishes them
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    Item h;
-    h.r = run_empty();
-    h.kind = K_COMPLEX;
-    h.eb = 0;
-    h.count = total;
-    h.start = 0;
-    stat_add(sm, S_TILE_COMPLEX, 1);
-    if (!(p.fault_mode == 1 && t == p.fault_arg)) st_rec_vol(&p.hdr[t], pack_item(h, tag));
+  if (lane == 0) {
+    stat_add(sm, S_TILES, 1);
+    stat_add(sm, S_CY_RUN, clock64() - c0);
   }
 }
 
-// ------------------------------------------------------------------ the streaming loop
-__device__ __forceinline__ void load_row(const Params &p, const unsigned char *stage, bool lane_tma, int64_t row,
-                                         const Geo &g, bool full, uint64_t (&v)[kLaneTerms]) {
-  const int tid = threadIdx.x;
-  if (lane_tma) {
-    const unsigned char *rp = stage + tid * 128;
-    const int sw = tid & 7;
-#pragma unroll
-    for (int q = 0; q < 8; q++) {
-      const uint4 d = *reinterpret_cast<const uint4 *>(rp + ((q ^ sw) << 4));
-      v[2 * q] = ((uint64_t)d.y << 32) | d.x;
-      v[2 * q + 1] = ((uint64_t)d.w << 32) | d.z;
-    }
-  } else {
-    const int64_t g0 = row * kLaneTerms;
-    const unsigned long long *xp = reinterpret_cast<const unsigned long long *>(p.x);
-#pragma unroll
-    for (int j = 0; j < kLaneTerms; j++) {
-      const int64_t gi = g0 + j;
-      v[j] = (gi >= g.g_lo && gi < g.g_hi) ? (uint64_t)__ldg(xp + gi) : kNegZero;
-    }
-    return;
-  }
-  if (!full) {
-    const int64_t g0 = row * kLaneTerms;
-#pragma unroll
-    for (int j = 0; j < kLaneTerms; j++) {
-      const int64_t gi = g0 + j;
-      if (gi < g.g_lo || gi >= g.g_hi) v[j] = kNegZero;
-    }
-  }
-}
-
-// Takes the next ticket for stage s and starts its copy (thread 0).
-__device__ __forceinline__ void refill(const Params &p, Smem &sm, unsigned char *stages, const CUtensorMap *tmap,
-                                       int s, int64_t ntiles) {
-  const int64_t t = sm.broken ? ntiles : (int64_t)atomicAdd(&p.ctr[C_TICKET], 1u);
-  if (t >= ntiles) {
-    sm.st_tile[s] = -1;
-    return;
-  }
-  const Geo g = tile_geo(p, t);
-  sm.st_tile[s] = t;
-  sm.st_geo[s][0] = g.row0;
-  sm.st_geo[s][1] = g.g_lo;
-  sm.st_geo[s][2] = g.g_hi;
-  sm.st_geo[s][3] = g.t_first;
-  sm.st_geo[s][4] = g.sum;
-  const bool tma = p.tma_rows > 0 && g.row0 < p.tma_rows;
-  sm.st_flags[s] = tma ? 1u : 0u;
-  if (tma) {
-    mbar_expect_tx(&sm.full[s], kStageBytes);
-    tma_load_2d(stages + s * kStageBytes, tmap, &sm.full[s], 0, (int32_t)g.row0);
-  } else {
-    mbar_arrive(&sm.full[s]);
-  }
-}
-
-__device__ __noinline__ void stream_loop(const Params &p, Smem &sm, unsigned char *stages, const CUtensorMap *tmap,
-                                         int64_t ntiles, uint32_t tag) {
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    for (int s = 0; s < kStages; s++) mbar_init(&sm.full[s], 1);
-    fence_mbar_init();
-    sm.broken = 0;
-    sm.t_stream_end = 0;
-    for (int s = 0; s < kStages; s++) refill(p, sm, stages, tmap, s, ntiles);
-  }
-  __syncthreads();
-  for (uint32_t it = 0;; it++) {
-    const int s = (int)(it % kStages);
-    const uint32_t ph = (it / kStages) & 1u;
-    const int64_t t = sm.st_tile[s];
+// A compute warp of a streaming CTA: units in the order the producer puts
+// them into the stages; the rows (and, for a run unit, the prefix the copy
+// brought) are read, the stage released, then the unit's work done.
+__device__ __noinline__ void compute_warp(const Params &p, Smem &sm, const unsigned char *stages) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const uint32_t tag = sm.tag;
+  for (uint32_t u = 0;; u++) {
+    const int s = (int)(u % kStages);
+    if (w == 0 && lane == 0) TL(p, sm.role, 0, u, 0);
+    const bool landed = stage_wait(p, sm, s, (u / kStages) & 1u);
+    const StageSm &st = sm.st[s];
+    const int64_t t = st.tile;
+    if (w == 0 && lane == 0) TL(p, sm.role, 0, u, 1);
     if (t < 0) break;
-    Geo g;
-    g.row0 = sm.st_geo[s][0];
-    g.g_lo = sm.st_geo[s][1];
-    g.g_hi = sm.st_geo[s][2];
-    g.t_first = sm.st_geo[s][3];
-    g.sum = (int32_t)sm.st_geo[s][4];
-    const bool tma = sm.st_flags[s] & 1u;
-    // wait for the copy (bounded; one thread decides for the CTA)
-    if (tid == 0) {
+    const bool plan = st.plan != 0;
+    const Geo g = stage_geo(st);
+    const int64_t row = g.row0 + threadIdx.x;
+    uint64_t v[kLaneTerms];
+    load_row(p, stages + s * kStageBytes, landed && st.tma && row < p.tma_rows, row, g, v);
+    uint4 pf = make_uint4(0, 0, 0, 0);
+    float bs = 0.0f, ba = 0.0f;
+    if (!plan && landed) {
+      pf = st.prec[0];
+      const float *ws = reinterpret_cast<const float *>(&st.prec[1]);
+      for (int k = 0; k < w; k++) {
+        bs = __fadd_rn(bs, ws[k]);
+        ba = __fadd_rn(ba, ws[kWarps + k]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[s]);   // this warp is done with the stage
+    if (w == 0 && lane == 0) TL(p, sm.role, 0, u, 2);
+    UnitSm &us = sm.us[u % kUnitSlots];
+    if (plan) {
+      const uint64_t c0 = clock64();
+      plan_unit(p, sm, us, t, v, tag);
+      if (lane == 0) stat_add(sm, S_CY_PLAN, clock64() - c0);
+    } else {
+      run_unit(p, sm, us, t, g, v, pf, bs, ba, tag);
+    }
+    if (w == 0 && lane == 0) TL(p, sm.role, 0, u, 3);
+    if (w == 0 && lane == 0) TL(p, sm.role, 0, u, 4 - (plan ? 0 : 0));
+  }
+}
+
+// The producer warp of a streaming CTA (lane 0): takes units by ticket and
+// starts their copies.  Unit u goes to stage u mod 3 once the compute warps
+// have released unit u - depth: depth 3 keeps three units in flight (the
+// next ticket taken while the stage is still busy, so the atomic's round
+// trip overlaps the work); depth 1, for calls with few units per CTA, takes
+// a ticket only when the CTA is ready for it.
+__device__ __noinline__ void producer_warp(const Params &p, Smem &sm, unsigned char *stages, const CUtensorMap *tmap,
+                                           int64_t ntiles) {
+  if ((threadIdx.x & 31) != 0) return;
+  const int64_t nstream = (int64_t)gridDim.x - p.nwalkers - 1, units = 2 * ntiles;
+  const bool deep = units > 2 * nstream;
+  const uint32_t depth = deep ? (uint32_t)kStages : 1u;
+  int64_t hand = -1;
+  for (uint32_t u = 0;; u++) {
+    const int s = (int)(u % kStages);
+    TL(p, sm.role, 1, u, 0);
+    if (u >= depth) {
+      // unit u - depth released (bounded; a stuck compute warp ends the CTA's units)
+      const uint32_t r = u - depth;
+      const uint32_t ph = (r / kStages) & 1u;
       const uint64_t t0 = gtimer();
       uint32_t spin = 0;
-      int ok = 1;
-      while (!mbar_try_wait(&sm.full[s], ph)) {
+      bool ok = true;
+      while (!mbar_try_wait(&sm.empty[r % kStages], ph)) {
         if ((++spin & 255u) == 0u && gtimer() - t0 > p.wait_ns) {
-          ok = 0;
+          ok = false;
           break;
         }
       }
       if (!ok) {
-        // the copy may still land: wait once more (bounded) so that it cannot
-        // write into the stage after it is reused; the tile is read from x
-        note_timeout(p, ERR_TMA_TIMEOUT, 2, (uint32_t)t, (uint32_t)s);
+        note_timeout(p, ERR_TMA_TIMEOUT, 7, u, 0);
         sm.broken = 1;
-        const uint64_t t1 = gtimer();
-        while (!mbar_try_wait(&sm.full[s], ph) && gtimer() - t1 < p.wait_ns) {
-        }
-      }
-      sm.fail = ok ? 0 : 1;
-    }
-    __syncthreads();
-    const bool tma_ok = tma && !sm.fail;
-    if (tma_ok && tid != 0) {
-      // the phase is complete (thread 0 saw it); each thread's own wait makes the copy's writes visible to it
-      for (uint32_t k = 0; k < (1u << 20) && !mbar_try_wait(&sm.full[s], ph); k++) {
       }
     }
-    const int64_t row = g.row0 + tid;
-    const bool full = g.row0 * kLaneTerms >= g.g_lo && (g.row0 + kTileRows) * kLaneTerms <= g.g_hi;
-    const bool lane_tma = tma_ok && row < p.tma_rows;
-    uint64_t v[kLaneTerms];
-    load_row(p, stages + s * kStageBytes, lane_tma, row, g, full, v);
-    __syncthreads();
-    if (tid == 0) refill(p, sm, stages, tmap, s, ntiles);
-    process_tile(p, sm, v, t, g, tag);
-    if (tid == 0) {
-      stat_add(sm, S_TILES, 1);
-      sm.t_stream_end = gtimer();
+    TL(p, sm.role, 1, u, 1);
+    int64_t k = hand >= 0 ? hand : (int64_t)atomicAdd(&p.ctr[C_TICKET], 1u);
+    const bool valid = k < units && !sm.broken;
+    TL(p, sm.role, 1, u, 2);
+    sm.us[u % kUnitSlots].done_cnt = 0;
+    stage_fill(p, sm, stages, tmap, s, valid ? k : -1, ntiles);
+    TL(p, sm.role, 1, u, 3);
+#ifdef SEQSUM_PROFILE
+    if (sm.role - p.nwalkers - 1 >= 0 && sm.role - p.nwalkers - 1 < 4 && u < 96)
+      p.dbg[((sm.role - p.nwalkers - 1) * 2 + 1) * 512 + u * 5 + 4] = (uint64_t)k;
+#endif
+    if (!valid) break;
+    hand = deep ? (int64_t)atomicAdd(&p.ctr[C_TICKET], 1u) : -1;
+  }
+}
+
+// A streaming CTA: 8 compute warps and a producer warp, no CTA barriers
+// after the start (the last warp to finish a unit publishes it).
+__device__ __noinline__ void stream_cta(const Params &p, Smem &sm, unsigned char *stages, const CUtensorMap *tmap,
+                                        int64_t ntiles) {
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    sm.broken = 0;
+    sm.t_stream_end = 0;
+    for (int s = 0; s < kStages; s++) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], kWarps);
     }
+    fence_mbar_init();
   }
   __syncthreads();
+  if ((tid >> 5) < kWarps) compute_warp(p, sm, stages);
+  else producer_warp(p, sm, stages, tmap, ntiles);
+  __syncthreads();
+  if (tid == 0) sm.t_stream_end = gtimer();   // this CTA's last header is published
+}
+
+// ------------------------------------------------------------------ the scanner
+// One CTA turns the tiles' sums into every tile's exclusive prefix, in order
+// (the first tile of a sum starts from s0), a window of up to 1024 tiles at a
+// time as the plan units publish them (double-float sums).
+__device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const uint32_t tag = sm.tag;
+  __shared__ DF s_wtot[kWarps];
+  __shared__ float s_wabs[kWarps];
+  __shared__ int s_whead[kWarps];
+  __shared__ int s_ready, s_giveup;
+  DF carry = DF{0.0f, 0.0f};
+  float carry_abs = 0.0f;
+  int64_t pos = 0;
+  uint64_t t_wait = 0;
+  while (pos < ntiles) {
+    // this thread's four consecutive tiles of the window
+    const int64_t t0 = pos + 4 * tid;
+    uint4 v[4];
+    bool rd[4];
+    if (tid == 0) s_ready = kScanTiles;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const int64_t t = t0 + j;
+      rd[j] = false;
+      v[j] = make_uint4(0, 0, 0, 0);
+      if (t < ntiles) {
+        v[j] = ld_vol_v4(&p.status[t]);
+        rd[j] = (v[j].w >> 8) == tag && (v[j].w & 3u) == 1u;
+      }
+    }
+    int my_first = kScanTiles;
+#pragma unroll
+    for (int j = 3; j >= 0; j--)
+      if (t0 + j < ntiles && !rd[j]) my_first = 4 * tid + j;
+    if (my_first < kScanTiles) atomicMin(&s_ready, my_first);
+    __syncthreads();
+    const int nready = (int)min((int64_t)s_ready, ntiles - pos);
+    if (nready == 0) {
+      // nothing new yet: thread 0 decides for the CTA whether to keep waiting
+      if (tid == 0) {
+        stat_add(sm, S_SCAN_POLLS, 1);
+        s_giveup = 0;
+        if (!t_wait) t_wait = gtimer();
+        else if (gtimer() - t_wait > p.wait_ns) {
+          note_timeout(p, ERR_PLAN_TIMEOUT, 6, (uint32_t)pos, 0);
+          s_giveup = 1;   // the run units will give up waiting too (their plans only)
+        }
+      }
+      __syncthreads();
+      if (s_giveup) break;
+      __nanosleep(128);
+      continue;
+    }
+    t_wait = 0;
+    // This thread's tiles, in order: loc[j] is the inclusive sum from the
+    // thread's first tile (or from the last sum start among them, which
+    // restarts at its s0); hup[j] says whether a sum started at or before j.
+    DF loc[4], s0d[4];
+    float loca[4];
+    bool head[4], hup[4];
+    DF acc = DF{0.0f, 0.0f};
+    float acca = 0.0f;
+    bool seen = false;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const int64_t t = t0 + j;
+      head[j] = false;
+      s0d[j] = DF{0.0f, 0.0f};
+      if (4 * tid + j < nready) {
+        const DF a = DF{__uint_as_float(v[j].x), __uint_as_float(v[j].y)};
+        const float aa = __uint_as_float(v[j].z);
+        const Geo g = tile_geo(p, t);
+        if (t == g.t_first) {
+          head[j] = true;
+          s0d[j] = df_of_double(p.offsets ? p.s0s[g.sum] : p.s0);
+          acc = df_add(s0d[j], a);
+          acca = __fadd_rn(fabsf(s0d[j].hi), aa);
+          seen = true;
+        } else {
+          acc = df_add(acc, a);
+          acca = __fadd_rn(acca, aa);
+        }
+      }
+      loc[j] = acc;
+      loca[j] = acca;
+      hup[j] = seen;
+    }
+    // segmented scan of the threads' totals across the warp ...
+    DF x = acc;
+    float xa = acca;
+    bool hx = seen;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      DF y;
+      y.hi = __shfl_up_sync(kFull, x.hi, o);
+      y.lo = __shfl_up_sync(kFull, x.lo, o);
+      const float ya = __shfl_up_sync(kFull, xa, o);
+      const bool hy = __shfl_up_sync(kFull, hx, o);
+      if (lane >= o) {
+        if (!hx) {
+          x = df_add(y, x);
+          xa = __fadd_rn(ya, xa);
+        }
+        hx = hx || hy;
+      }
+    }
+    if (lane == 31) {
+      s_wtot[w] = x;
+      s_wabs[w] = xa;
+      s_whead[w] = hx;
+    }
+    DF xl;
+    xl.hi = __shfl_up_sync(kFull, x.hi, 1);
+    xl.lo = __shfl_up_sync(kFull, x.lo, 1);
+    const float xla = __shfl_up_sync(kFull, xa, 1);
+    const bool hl = __shfl_up_sync(kFull, hx, 1);
+    __syncthreads();
+    // ... and across the warps, after the carry of the earlier windows:
+    // `before` is the inclusive prefix just before this thread's first tile
+    DF before = carry;
+    float before_a = carry_abs;
+    for (int k = 0; k < w; k++) {
+      if (s_whead[k]) {
+        before = s_wtot[k];
+        before_a = s_wabs[k];
+      } else {
+        before = df_add(before, s_wtot[k]);
+        before_a = __fadd_rn(before_a, s_wabs[k]);
+      }
+    }
+    if (lane > 0) {
+      if (hl) {
+        before = xl;
+        before_a = xla;
+      } else {
+        before = df_add(before, xl);
+        before_a = __fadd_rn(before_a, xla);
+      }
+    }
+    // each tile's exclusive prefix: its s0 at a sum start, else the inclusive
+    // prefix of the tile before it
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      if (4 * tid + j < nready) {
+        DF e;
+        float ea;
+        if (head[j]) {
+          e = s0d[j];
+          ea = fabsf(s0d[j].hi);
+        } else if (j == 0) {
+          e = before;
+          ea = before_a;
+        } else if (hup[j - 1]) {
+          e = loc[j - 1];
+          ea = loca[j - 1];
+        } else {
+          e = df_add(before, loc[j - 1]);
+          ea = __fadd_rn(before_a, loca[j - 1]);
+        }
+        st_vol_v4(&p.prec[(t0 + j) * kPrecWords], make_uint4(__float_as_uint(e.hi), __float_as_uint(e.lo),
+                                                             __float_as_uint(ea), (tag << 8) | 2u));
+      }
+    }
+    // the carry into the next window: the inclusive prefix of its last tile
+    __syncthreads();
+    {
+      const int j = nready - 1 - 4 * tid;
+      if (j >= 0 && j < 4) {
+        s_wtot[0] = hup[j] ? loc[j] : df_add(before, loc[j]);
+        s_wabs[0] = hup[j] ? loca[j] : __fadd_rn(before_a, loca[j]);
+      }
+    }
+    __syncthreads();
+    carry = s_wtot[0];
+    carry_abs = s_wabs[0];
+    __syncthreads();
+    if (tid == 0) stat_add(sm, S_SCAN_WINDOWS, 1);
+    pos += nready;
+  }
 }
 
 // ------------------------------------------------------------------ the walk: raw terms
@@ -845,13 +1387,46 @@ __device__ __noinline__ void stream_loop(const Params &p, Smem &sm, unsigned cha
 // applied at once, and the term after it (which leaves the binade) is added
 // with the hardware add.  A zero, subnormal, tiny or non-finite Sb takes one
 // hardware add per term.
-__device__ __noinline__ uint64_t raw_chunk(Smem &sm, uint64_t Sb, uint64_t t, int n) {
+__device__ __noinline__ uint64_t raw_chunk(Smem &sm, uint64_t Sb, uint64_t t, int i, int n) {
   const int lane = threadIdx.x & 31;
-  int i = 0;
+  const uint64_t t_in = clock64();
   uint32_t rounds = 0, dadds = 0;
   while (i < n) {
     const uint32_t Eb = (uint32_t)(Sb >> 52) & 0x7FFu;
     if (Eb >= 64u && Eb < 0x7FFu) {
+      // the common case: no term of the other sign, no tie -- the magnitudes'
+      // increments simply add, and the check of a prefix is m + P <= 2^53
+      const bool inr = lane >= i && lane < n;
+      const uint32_t hi = (uint32_t)(t >> 32);
+      const uint32_t E = (hi >> 20) & 0x7FFu;
+      const bool opp = inr && (hi >> 31) != (uint32_t)(Sb >> 63) && (t << 1) != 0;
+      const bool big = inr && E >= Eb;   // |t| >= 2^e, inf or NaN: never inside this binade
+      uint32_t tt = 1;
+      const uint64_t rr = inr ? term_mag_halfup(hi, (uint32_t)t, 64 - (int)Eb, tt) : 0ull;
+      if (!__any_sync(kFull, opp || (inr && !big && tt == 0u))) {
+        uint64_t P = big ? (1ull << 57) : rr;   // a term that cannot be added ends every prefix through it
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint64_t q = __shfl_up_sync(kFull, P, o);
+          if (lane >= o) P += q;
+        }
+        const uint64_t m = (Sb & kFracMask) | kHidden;
+        const bool ok = inr && m + P <= (uint64_t)kTwo53;
+        const uint32_t okm = __ballot_sync(kFull, ok);
+        const uint32_t inrange = (n >= 32 ? kFull : ((1u << n) - 1u)) & ~((1u << i) - 1u);
+        const uint32_t fail = ~okm & inrange;
+        int j = fail ? __ffs(fail) - 1 : n;
+        if (j > i) Sb += __shfl_sync(kFull, P, j - 1);   // the magnitude grows by P; a count of 2^53 is 2^(e+1)
+        if (j < n) {
+          const uint64_t tj = __shfl_sync(kFull, t, j);
+          Sb = dbits(__dadd_rn(bitsd(Sb), bitsd(tj)));
+          j++;
+          dadds++;
+        }
+        rounds++;
+        i = j;
+        continue;
+      }
       const int e = (int)Eb - 1023;
       Run r = run_empty();
       if (lane >= i && lane < n) {
@@ -890,6 +1465,7 @@ __device__ __noinline__ uint64_t raw_chunk(Smem &sm, uint64_t Sb, uint64_t t, in
   if (lane == 0) {
     stat_add(sm, S_RAW_ROUNDS, rounds);
     stat_add(sm, S_TERMS_DADD, dadds);
+    stat_add(sm, S_CY_WALK_RAW, clock64() - t_in);
   }
   return Sb;
 }
@@ -901,12 +1477,92 @@ __device__ __noinline__ uint64_t raw_from_x(const Params &p, Smem &sm, uint64_t 
   for (int64_t g = a; g < b; g += 32) {
     const int n = (int)min((int64_t)32, b - g);
     const uint64_t t = lane < n ? (uint64_t)__ldg(xp + g + lane) : kNegZero;
-    Sb = raw_chunk(sm, Sb, t, n);
+    Sb = raw_chunk(sm, Sb, t, 0, n);
   }
   return Sb;
 }
 
-// ------------------------------------------------------------------ the walk: one batch of tile headers
+// A raw row with prefix tables for the binades ea and ea + 1 (one warp; every
+// lane computes the same S): data holds its 16 terms, then the two tables,
+// lims where each table stops being usable (5 bits each).  While S is in one of them, of the row's sign,
+// and the table holds: the longest prefix whose increments keep the count
+// within the binade (m + P <= 2^53) is added at once, and the term after it
+// with the hardware add.  The rest goes term by term (raw_chunk).
+__device__ __noinline__ uint64_t raw2_row(Smem &sm, uint64_t S, const uint64_t *data, uint32_t lims, uint32_t ea,
+                                          uint64_t neg) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t t_in = clock64();
+  const int la = (int)(lims & 31u), lb = (int)((lims >> 5) & 31u);
+  const uint64_t t = lane < kLaneTerms ? data[lane] : kNegZero;
+  const uint64_t pa = lane < kLaneTerms ? data[kLaneTerms + lane] : 0ull;
+  const uint64_t pb = lane < kLaneTerms ? data[2 * kLaneTerms + lane] : 0ull;
+  int i = 0;
+  uint32_t rounds = 0, dadds = 0;
+  if (((uint32_t)(S >> 52) & 0x7FFu) == ea && (S >> 63) == neg && la == kLaneTerms && lb == kLaneTerms) {
+    // the common row: S in the lower binade, both tables whole.  The
+    // increments are non-negative, so the terms that keep the count within
+    // the binade are a prefix; the term after it crosses (the hardware add)
+    // and the rest is one check and one add in the upper binade.
+    const uint64_t m = (S & kFracMask) | kHidden;
+    const uint32_t okm = __ballot_sync(kFull, lane < kLaneTerms && m + pa <= (uint64_t)kTwo53) & 0xFFFFu;
+    const int k = __ffs(~okm) - 1;   // 16: no crossing
+    const uint64_t pk = __shfl_sync(kFull, pa, (k - 1) & 31);
+    const uint64_t xk = __shfl_sync(kFull, t, k & 15);
+    const uint64_t pbk = __shfl_sync(kFull, pb, k & 15), pb15 = __shfl_sync(kFull, pb, kLaneTerms - 1);
+    if (k > 0) S += pk;   // a count of 2^53 is 2^(e+1)
+    rounds = 1;
+    i = k;
+    if (k < kLaneTerms) {
+      S = dbits(__dadd_rn(bitsd(S), bitsd(xk)));
+      dadds = 1;
+      i = k + 1;
+      const uint64_t rest = pb15 - pbk, m2 = (S & kFracMask) | kHidden;
+      if (i < kLaneTerms && ((uint32_t)(S >> 52) & 0x7FFu) == ea + 1u && (S >> 63) == neg &&
+          m2 + rest <= (uint64_t)kTwo53) {
+        S += rest;
+        i = kLaneTerms;
+        rounds = 2;
+      }
+    }
+  }
+  while (i < kLaneTerms) {
+    const uint32_t Eb = (uint32_t)(S >> 52) & 0x7FFu;
+    const bool use_a = Eb == ea && i < la, use_b = Eb == ea + 1u && i < lb;
+    if ((S >> 63) != neg || !(use_a || use_b)) break;
+    const uint64_t P = use_a ? pa : pb;
+    const int lim = use_a ? la : lb;
+    const uint64_t base = i > 0 ? __shfl_sync(kFull, P, i - 1) : 0ull;
+    const uint64_t m = (S & kFracMask) | kHidden;
+    const bool ok = lane >= i && lane < lim && m + (P - base) <= (uint64_t)kTwo53;
+    const uint32_t inr = ((1u << lim) - 1u) & ~((1u << i) - 1u);
+    const uint32_t fail = ~__ballot_sync(kFull, ok) & inr;
+    const int k = fail ? __ffs(fail) - 1 : lim;
+    if (k > i) S += __shfl_sync(kFull, P, k - 1) - base;   // the magnitude grows; a count of 2^53 is 2^(e+1)
+    rounds++;
+    i = k;
+    if (k == lim) break;   // the table ends here (or the row does)
+    S = dbits(__dadd_rn(bitsd(S), bitsd(__shfl_sync(kFull, t, k))));
+    dadds++;
+    i = k + 1;
+  }
+  if (lane == 0) {
+    stat_add(sm, S_RAW_ROUNDS, rounds);
+    stat_add(sm, S_TERMS_DADD, dadds);
+    stat_add(sm, S_CY_WALK_RAW, clock64() - t_in);
+  }
+#ifdef SEQSUM_PROFILE
+  if (lane == 0) sm.prof_i = (uint32_t)i | (rounds << 8) | (dadds << 16) | (((uint32_t)(S >> 52) & 0x7FFu) << 20);
+#endif
+  if (i < kLaneTerms) S = raw_chunk(sm, S, t, i, kLaneTerms);
+  return S;
+}
+
+// ------------------------------------------------------------------ the walk: ranges of tiles
+// A walker CTA: eight producer warps and one in-order warp.  The tiles of a
+// sum are cut into ranges of kRangeTiles; producer warp k takes ranges k,
+// k + 8, ... and writes each, composed into steps, to its own slot; the
+// in-order warp takes the slots in range order and applies their steps to
+// the exact running value.  A slot's full and empty mbarriers hand it over.
 struct WalkSum {
   int64_t tb, te;        // the sum's tiles
   int64_t row_base;      // the sum's first row
@@ -920,247 +1576,491 @@ __device__ __forceinline__ void clip(const WalkSum &ws, int64_t tile, uint32_t s
   b = min(g0 + (int64_t)start + (int64_t)count, ws.g_hi);
 }
 
-// Applies one run (lane 0 decides) and, if the check refuses it, adds the
-// run's terms from x.  Warp 0.
-__device__ __forceinline__ uint64_t apply_or_raw(const Params &p, Smem &sm, uint64_t Sb, const Run &r, uint32_t eb,
-                                                 const WalkSum &ws, int64_t tile, uint32_t start, uint32_t count) {
-  const int lane = threadIdx.x & 31;
-  uint64_t nb = Sb;
-  int ok = 0;
-  if (lane == 0) ok = run_apply(nb, r, (int)eb - 1023) == APPLY_OK;
-  ok = __shfl_sync(kFull, ok, 0);
-  if (ok) return __shfl_sync(kFull, nb, 0);
-  if (lane == 0) stat_add(sm, S_RUN_REJECTED, 1);
-  int64_t a, b;
-  clip(ws, tile, start, count, a, b);
-  return raw_from_x(p, sm, Sb, a, b);
+
+// One step of the in-order pass: a composite of consecutive runs of one
+// binade, a raw row, or a range of terms read from x.
+enum : uint32_t { ST_RUN = 0, ST_RAW = 1, ST_RAW2 = 2, ST_X = 3 };
+struct __align__(16) Step {
+  int64_t inc, lo, hi;   // a composite's run; a raw row: its place among the slot's fetched rows (in inc)
+  uint64_t meta;         // kind (2 bits), biased binade (11), d + 1 (2), flags (8), then its terms:
+                         // first tile (7) and row (9), last tile (7) and row after it (9), within the range
+};
+__device__ __forceinline__ uint64_t step_meta(uint32_t kind, uint32_t eb, int32_t d, uint32_t flags, uint32_t from,
+                                              uint32_t to) {
+  return (uint64_t)(kind & 3u) | ((uint64_t)(eb & 0x7FFu) << 2) | ((uint64_t)((d + 1) & 3) << 13) |
+         ((uint64_t)(flags & 0xFFu) << 15) | ((uint64_t)(from & 0xFFFFu) << 23) | ((uint64_t)(to & 0xFFFFu) << 39);
+}
+// a position in a range: tile (7 bits) and row (9 bits); positions compare as numbers
+__device__ __forceinline__ uint32_t rpos(uint32_t tile, uint32_t row) { return (tile << 9) | row; }
+
+constexpr int kRangeTiles = 4 * 32;   // tiles of a walk range (four per lane of a producer warp)
+constexpr int kRangeSteps = 64;       // steps a slot holds (more: the range is read from x)
+constexpr int kRangeRaw = 24;         // raw rows a slot holds with their terms and tables
+struct RangeSlot {
+  Step steps[kRangeSteps];
+  uint64_t raw[kRangeRaw][3 * kLaneTerms];   // a raw row's terms, then its two prefix tables
+  uint32_t rawlim[kRangeRaw];                // where each table stops being usable (5 bits each)
+  uint32_t rawpos[kRangeRaw];                // its first term: position in the range, with tables (bit 16), binade
+  int nsteps;                                // -1: the steps did not fit
+  int fail;                                  // a header never came
+};
+static_assert(sizeof(RangeSlot) % 16 == 0, "slots stay 16-byte aligned");
+static_assert(kWarps * sizeof(RangeSlot) <= kDynSmem - 1024, "the walk's slots fit the dynamic shared memory");
+
+// An element of a range, in the order of its terms: a tile's run (its
+// header), an item of a complex tile (a run or a raw row), or terms read from
+// x (a region or a tile without items).
+enum : uint32_t { EK_RUN = 0, EK_RAW = 1, EK_RAW2 = 2, EK_X = 3 };
+struct Elem {
+  Run r;
+  uint32_t kind, key;    // key: the run's biased binade; kNoKey for the others
+  uint32_t from, to;     // its terms: positions in the range
+  uint32_t eb, neg;      // a raw row with tables: the lower binade and the sign
+};
+
+// The number of items of a complex tile's compact list (0: none usable, the
+// tile is read from x).
+__device__ __forceinline__ uint32_t complex_items(const Rec &h) {
+  const uint64_t m = h.w[0] & kPay56;
+  return (m >= 1 && m <= (uint64_t)kItemSlots) ? (uint32_t)m : 0u;
 }
 
-__device__ __noinline__ uint64_t apply_items(const Params &p, Smem &sm, uint64_t Sb, const Rec *slots, uint32_t nsl,
-                                             const WalkSum &ws, int64_t tile) {
-  const int lane = threadIdx.x & 31;
-  uint32_t s = 0;
-  while (s < nsl) {
-    const Item it = unpack_item(slots[s]);
-    if (it.kind == K_RAW && s + kRawSlots <= nsl) {
-      const uint64_t *terms = reinterpret_cast<const uint64_t *>(&slots[s + 1]);
-      const uint64_t t = lane < kLaneTerms ? terms[lane] : kNegZero;
-      Sb = raw_chunk(sm, Sb, t, kLaneTerms);
-      s += kRawSlots;
-    } else if (it.kind == K_RUN) {
-      Sb = apply_or_raw(p, sm, Sb, it.r, it.eb, ws, tile, it.start, it.count);
-      if (lane == 0) stat_add(sm, S_WALK_SEGMENTS, 1);
-      s += 1;
-    } else {
-      // an item this walk does not know: the tile's terms from x
-      int64_t a, b;
-      clip(ws, tile, 0, kTileTerms, a, b);
-      Sb = raw_from_x(p, sm, Sb, a, b);
-      break;
+// Element E of the range (every lane of the warp calls it; in: E < n).
+// off: this lane's first element; eo: the first elements of its four tiles;
+// direct: every tile is one element (element E is tile E).
+__device__ __forceinline__ Elem range_elem(const Params &p, const Rec (&hl)[4], int64_t ta, int E, bool in,
+                                           uint32_t off, const uint32_t (&eo)[4], bool direct) {
+  uint32_t tt = (uint32_t)E, kk = 0;
+  if (!direct) {
+    // the lane whose tiles hold E: the last with off <= E
+    int o = 0;
+#pragma unroll
+    for (int step = 16; step > 0; step >>= 1) {
+      const uint32_t v = __shfl_sync(kFull, off, o + step);
+      if (in && v <= (uint32_t)E) o += step;
+    }
+    const uint32_t e0 = __shfl_sync(kFull, eo[0], o), e1 = __shfl_sync(kFull, eo[1], o),
+                   e2 = __shfl_sync(kFull, eo[2], o), e3 = __shfl_sync(kFull, eo[3], o);
+    const uint32_t j = (uint32_t)E >= e3 ? 3u : ((uint32_t)E >= e2 ? 2u : ((uint32_t)E >= e1 ? 1u : 0u));
+    kk = (uint32_t)E - (j == 3u ? e3 : (j == 2u ? e2 : (j == 1u ? e1 : e0)));
+    tt = 4u * (uint32_t)o + j;
+  }
+  Elem el;
+  el.r = run_empty();
+  el.kind = EK_X;
+  el.key = kNoKey;
+  el.eb = el.neg = 0;
+  el.from = rpos(tt, 0);
+  el.to = rpos(tt, kTileRows);
+  // the tile's header, from the lane that read it
+  Rec h;
+  h.w[0] = h.w[1] = h.w[2] = h.w[3] = 0;
+  const int src = (int)(tt >> 2) & 31, jt = (int)(tt & 3u);
+#pragma unroll
+  for (int j = 0; j < 4; j++) {
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      const uint64_t v = (uint64_t)__shfl_sync(kFull, (long long)hl[j].w[q], src);
+      if (j == jt) h.w[q] = v;
     }
   }
-  return Sb;
+  if (!in) return el;
+  const uint32_t hk = (uint32_t)(h.w[3] & 7u);
+  if (hk == K_RUN) {
+    const Item it = unpack_item(h);
+    el.r = it.r;
+    el.kind = EK_RUN;
+    el.key = it.eb;
+    return el;
+  }
+  if (hk != K_COMPLEX || complex_items(h) == 0) return el;   // a tile read from x
+  const Rec q = ld_rec_vol(&p.items[(ta + tt) * kItemSlots + kk]);
+  const Item it = unpack_item(q);
+  el.from = rpos(tt, it.start / kLaneTerms);
+  el.to = rpos(tt, (it.start + it.count) / kLaneTerms);
+  if (it.kind == K_RUN) {
+    el.r = it.r;
+    el.kind = EK_RUN;
+    el.key = it.eb;
+  } else if (it.kind == K_RAW || it.kind == K_RAW2) {
+    el.kind = it.kind == K_RAW ? EK_RAW : EK_RAW2;
+    el.eb = it.eb;
+    el.neg = (uint32_t)(q.w[0] & 1u);
+  }
+  return el;
+}
+
+// Waits (bounded) for phase `ph` of an mbarrier; false if the limit passed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t ph, uint64_t limit_ns) {
+  uint64_t t0 = 0;
+  for (uint32_t spin = 0; !mbar_try_wait(bar, ph); spin++) {
+    if ((spin & 63u) == 63u) {
+      const uint64_t now = gtimer();
+      if (!t0) t0 = now;
+      else if (now - t0 > limit_ns) return false;
+    }
+  }
+  return true;
+}
+
+// A producer warp: the ranges pw, pw + 8, ... of one sum into slot pw.
+__device__ __noinline__ void walk_producer(const Params &p, Smem &sm, RangeSlot &rs, const WalkSum &ws, int nranges,
+                                           int pw, uint32_t tag) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t lt = (1u << lane) - 1u;
+  bool failed_all = false;
+  for (int r = pw; r < nranges; r += kWarps) {
+    // the slot's previous use must have been applied
+    const uint32_t use = sm.wuse_p[pw];
+    bool ok = !failed_all;
+    if (use > 0) ok = mbar_wait_bounded(&sm.wempty[pw], (use - 1) & 1u, 4 * p.wait_ns);
+    const int64_t ta = ws.tb + (int64_t)r * kRangeTiles;
+    const int tn = (int)min((int64_t)kRangeTiles, ws.te - ta);
+    // ---- the range's headers (four a lane), as they arrive
+    Rec h[4];
+    uint32_t need = 0;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      h[j].w[0] = h[j].w[1] = h[j].w[2] = h[j].w[3] = 0;
+      if (4 * lane + j < tn) need |= 1u << j;
+    }
+    const uint64_t c0 = clock64();
+    uint64_t t0 = 0;
+    for (uint32_t spin = 0; ok; spin++) {
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        if (need & (1u << j)) {
+          h[j] = ld_rec_vol(&p.hdr[ta + 4 * lane + j]);
+          if (tags_ok(h[j], tag)) need &= ~(1u << j);
+        }
+      }
+      if (__all_sync(kFull, need == 0u)) break;
+      const uint64_t now = gtimer();
+      if (!t0) t0 = now;
+      else if (now - t0 > p.wait_ns) {
+        if (lane == 0) note_timeout(p, ERR_WALK_TIMEOUT, 3, (uint32_t)ta, (uint32_t)ws.te);
+        ok = false;
+      }
+      __nanosleep(200);
+    }
+    ok = __all_sync(kFull, ok);
+    if (lane == 0) stat_add(sm, S_CY_WALK_WAIT, clock64() - c0);
+    WRT(r, 0);
+    fence_acq_rel();
+    // ---- its elements: a run or overflow tile is one, a complex tile one per item
+    uint32_t eo[4], n = 0;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      eo[j] = n;
+      if (4 * lane + j < tn) {
+        const uint32_t hk = (uint32_t)(h[j].w[3] & 7u);
+        n += (hk == K_COMPLEX && complex_items(h[j]) > 0) ? complex_items(h[j]) : 1u;
+      }
+    }
+    uint32_t off = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t q = __shfl_up_sync(kFull, off, o);
+      if (lane >= o) off += q;
+    }
+    const int N = ok ? (int)__shfl_sync(kFull, off, 31) : 0;
+    const bool direct = N == tn;   // every tile one element
+    off -= n;
+#pragma unroll
+    for (int j = 0; j < 4; j++) eo[j] += off;
+    __syncwarp();
+    // ---- the segmented scan, 32 elements at a time; steps at the tails
+    int nsteps = 0, nraw = 0;
+    bool over = false;
+    Run carry = run_empty();      // the composite of the open segment (since its head)
+    uint32_t ckey = kNoKey, cfrom = 0, cto = 0;
+    bool pending = false;         // the chunk before ended inside a segment
+    for (int c = 0; c < N; c += 32) {
+      const int E = c + lane;
+      const bool in = E < N;
+      const Elem el = range_elem(p, h, ta, E, in, off, eo, direct);
+      const uint32_t key = in ? el.key : kNoKey;
+      uint32_t pkey = __shfl_up_sync(kFull, key, 1);
+      if (lane == 0) pkey = ckey;
+      const bool head = in && (E == 0 || key == kNoKey || pkey == kNoKey || key != pkey);
+      // the open segment of the chunk before ends if this chunk begins with a head
+      const bool close_prev = __shfl_sync(kFull, head, 0) && pending;
+      if (close_prev && lane == 0 && nsteps < kRangeSteps) {
+        Step st;
+        st.inc = carry.inc;
+        st.lo = carry.lo;
+        st.hi = carry.hi;
+        st.meta = step_meta(ST_RUN, ckey, carry.d, carry.flags, cfrom, cto);
+        rs.steps[nsteps] = st;
+      }
+      if (close_prev) nsteps++;
+      // the common chunk: runs of one binade, non-negative, without a tie,
+      // no head after its first element -- their increments simply add
+      const uint32_t key0 = __shfl_sync(kFull, key, 0);
+      const bool plain = __all_sync(kFull, !in || (el.kind == EK_RUN && el.r.d == 0 && (el.r.flags & F_NONNEG) &&
+                                                   key == key0 && (lane == 0 || !head)));
+      if (plain) {
+        long long a = in ? (long long)el.r.inc : 0ll;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(kFull, a, o);
+        const uint32_t fand = __reduce_and_sync(
+            kFull, in ? (el.r.flags & (F_NONNEG | F_NONPOS | F_ZERO | F_ALLNEGZ)) : (uint32_t)(F_NONNEG | F_NONPOS | F_ZERO | F_ALLNEGZ));
+        const uint32_t fo = __reduce_or_sync(kFull, in ? (el.r.flags & ~(uint32_t)(F_NONNEG | F_NONPOS | F_ZERO | F_ALLNEGZ)) : 0u);
+        Run ch;
+        ch.inc = a;
+        ch.lo = 0;
+        ch.hi = a;
+        ch.d = 0;
+        ch.flags = fand | fo;
+        saturate(ch);
+        const bool h0 = __shfl_sync(kFull, head, 0);
+        const Run comp = h0 ? ch : run_compose(carry, ch);
+        const uint32_t from0 = h0 ? __shfl_sync(kFull, el.from, 0) : cfrom;
+        const int lastl = min(31, N - 1 - c);
+        const uint32_t to = __shfl_sync(kFull, el.to, lastl);
+        if (c + 32 >= N) {
+          // the range's last element: the segment ends here
+          if (lane == 0 && nsteps < kRangeSteps) {
+            Step st;
+            st.inc = comp.inc;
+            st.lo = comp.lo;
+            st.hi = comp.hi;
+            st.meta = step_meta(ST_RUN, key0, comp.d, comp.flags, from0, to);
+            rs.steps[nsteps] = st;
+          }
+          nsteps++;
+          pending = false;
+        } else {
+          pending = true;
+        }
+        carry = comp;
+        ckey = key0;
+        cfrom = from0;
+        cto = to;
+        continue;
+      }
+      Run rr = el.r;
+      bool f = head;
+      uint32_t from = head ? el.from : 0u;
+      if (lane == 0 && in && !head) {
+        rr = run_compose(carry, rr);
+        from = cfrom;
+        f = true;   // the carry stands for its head
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const Run q = shfl_run_up(rr, o);
+        const bool qh = __shfl_up_sync(kFull, f, o);
+        const uint32_t qf = __shfl_up_sync(kFull, from, o);
+        if (lane >= o) {
+          if (!f) rr = run_compose(q, rr);
+          f = f || qh;
+          from = max(from, qf);
+        }
+      }
+      // tails: the next element is a head (lane 31 decides with the next chunk)
+      const uint32_t nkey = __shfl_down_sync(kFull, key, 1);
+      const bool last = E == N - 1;
+      const bool tail = in && (key == kNoKey || last || (lane < 31 && (nkey == kNoKey || nkey != key)));
+      const uint32_t tb = __ballot_sync(kFull, tail);
+      const uint32_t rb = __ballot_sync(kFull, tail && (el.kind == EK_RAW || el.kind == EK_RAW2));
+      if (tail) {
+        const int at = nsteps + __popc(tb & lt);
+        if (at < kRangeSteps) {
+          Step st;
+          if (el.kind == EK_RUN) {
+            st.inc = rr.inc;
+            st.lo = rr.lo;
+            st.hi = rr.hi;
+            st.meta = step_meta(ST_RUN, key, rr.d, rr.flags, from, el.to);
+          } else {
+            const uint32_t q = (uint32_t)nraw + __popc(rb & lt);
+            st.inc = (int64_t)q;
+            if (q < (uint32_t)kRangeRaw)
+              rs.rawpos[q] = el.from | (el.kind == EK_RAW2 ? 1u << 16 : 0u) | ((el.eb & 0x7FFu) << 17);
+            st.lo = st.hi = 0;
+            const uint32_t sk = el.kind == EK_RAW ? ST_RAW : (el.kind == EK_RAW2 ? ST_RAW2 : ST_X);
+            st.meta = step_meta(sk, el.eb, 0, el.neg, el.from, el.to);
+          }
+          rs.steps[at] = st;
+        }
+      }
+      nsteps += __popc(tb);
+      nraw += __popc(rb);
+      // the open segment at the end of the chunk
+      carry = shfl_run_idx(rr, 31);
+      ckey = __shfl_sync(kFull, key, 31);
+      cfrom = __shfl_sync(kFull, from, 31);
+      cto = __shfl_sync(kFull, el.to, 31);
+      pending = __shfl_sync(kFull, in && !tail, 31);
+    }
+    over = nsteps > kRangeSteps;
+    __syncwarp();
+    // ---- the raw rows' terms from x (all loads at once), then their prefix tables
+    const int nfetch = over ? 0 : min(nraw, kRangeRaw);
+    for (int w0 = lane; w0 < nfetch * kLaneTerms; w0 += 32) {
+      const uint32_t pos = rs.rawpos[w0 / kLaneTerms] & 0xFFFFu;
+      const int64_t gi = (ws.row_base + (ta + (pos >> 9) - ws.tb) * kTileRows + (pos & 511u)) * kLaneTerms +
+                         (w0 & (kLaneTerms - 1));
+      rs.raw[w0 / kLaneTerms][w0 & (kLaneTerms - 1)] =
+          (gi >= ws.g_lo && gi < ws.g_hi) ? (uint64_t)__ldg(reinterpret_cast<const unsigned long long *>(p.x) + gi)
+                                          : kNegZero;
+    }
+    __syncwarp();
+    for (int q = 0; q < nfetch; q++) {
+      const uint32_t rp = rs.rawpos[q];
+      if (!(rp & (1u << 16))) continue;
+      // lanes 0..15 the lower binade, 16..31 the upper one
+      const int jj = lane & (kLaneTerms - 1);
+      const uint64_t t = rs.raw[q][jj];
+      const uint32_t E = (rp >> 17) + (uint32_t)(lane >> 4);
+      const uint32_t hi = (uint32_t)(t >> 32);
+      uint32_t tt;
+      uint64_t P = term_mag_halfup(hi, (uint32_t)t, 64 - (int)E, tt);
+      const uint32_t bad = __ballot_sync(kFull, tt == 0u || ((hi >> 20) & 0x7FFu) >= E);
+#pragma unroll
+      for (int o = 1; o < kLaneTerms; o <<= 1) {
+        const uint64_t v = __shfl_up_sync(kFull, P, o, kLaneTerms);
+        if (jj >= o) P += v;
+      }
+      rs.raw[q][kLaneTerms + lane] = P;
+      if (lane == 0) {
+        const uint32_t ba = bad & 0xFFFFu, bb = bad >> 16;
+        rs.rawlim[q] = (ba ? (uint32_t)(__ffs(ba) - 1) : (uint32_t)kLaneTerms) |
+                       ((bb ? (uint32_t)(__ffs(bb) - 1) : (uint32_t)kLaneTerms) << 5);
+      }
+    }
+    // ---- hand the slot over
+    if (lane == 0) {
+      rs.nsteps = over ? -1 : nsteps;
+      rs.fail = ok ? 0 : 1;
+      sm.wuse_p[pw] = use + 1;
+    }
+    __syncwarp();
+    WRT(r, 1);
+    if (lane == 0) mbar_arrive(&sm.wfull[pw]);
+    // after a failure the later ranges are handed over failed, without waiting
+    if (!ok) failed_all = true;
+  }
+}
+
+// The in-order warp: the slots of one sum in range order, their steps
+// applied to the exact running value S.  Returns S (NaN if a header never
+// came or a slot was not handed over in time).
+__device__ __noinline__ uint64_t walk_serial(const Params &p, Smem &sm, RangeSlot *slots, const WalkSum &ws,
+                                             int nranges, uint64_t S) {
+  const int lane = threadIdx.x & 31;
+  bool failed = false;
+  uint32_t nrun = 0;
+  for (int r = 0; r < nranges; r++) {
+    const int pw = r % kWarps;
+    RangeSlot &rs = slots[pw];
+    const uint32_t use = sm.wuse_c[pw];
+    const uint64_t c0 = clock64();
+    const bool got = mbar_wait_bounded(&sm.wfull[pw], use & 1u, 8 * p.wait_ns);
+    const uint64_t c1 = clock64();
+    WRT(r, 2);
+    if (!got || rs.fail) failed = true;
+    const int64_t ta = ws.tb + (int64_t)r * kRangeTiles;
+    if (got && !failed) {
+      const int ns = rs.nsteps;
+      if (ns < 0) {
+        // the steps did not fit: the range's terms one by one
+        if (lane == 0) stat_add(sm, S_RANGE_X, 1);
+        int64_t a, b;
+        clip(ws, ta, 0, (uint32_t)min((int64_t)kRangeTiles, ws.te - ta) * kTileTerms, a, b);
+        S = raw_from_x(p, sm, S, a, b);
+      }
+      for (int i = 0; i < ns; i++) {
+        const Step st = rs.steps[i];
+        const uint32_t kind = (uint32_t)(st.meta & 3u);
+#ifdef SEQSUM_PROFILE
+        const uint64_t t_seg = clock64();
+#endif
+        const uint32_t eb = (uint32_t)(st.meta >> 2) & 0x7FFu;
+        const uint32_t from = (uint32_t)(st.meta >> 23) & 0xFFFFu, to = (uint32_t)(st.meta >> 39) & 0xFFFFu;
+        bool done = false;
+        if (kind == ST_RUN) {
+          Run q;
+          q.inc = st.inc;
+          q.lo = st.lo;
+          q.hi = st.hi;
+          q.d = (int32_t)((st.meta >> 13) & 3u) - 1;
+          q.flags = (uint32_t)(st.meta >> 15) & 0xFFu;
+          uint64_t nb = S;
+          if (run_apply(nb, q, (int)eb - 1023) == APPLY_OK) {
+            S = nb;
+            done = true;
+          } else if (lane == 0) {
+            stat_add(sm, S_RUN_REJECTED, 1);
+          }
+          nrun++;
+        } else if ((kind == ST_RAW || kind == ST_RAW2) && st.inc < kRangeRaw) {
+          const uint64_t *data = rs.raw[st.inc];
+          if (kind == ST_RAW) S = raw_chunk(sm, S, lane < kLaneTerms ? data[lane] : kNegZero, 0, kLaneTerms);
+          else S = raw2_row(sm, S, data, rs.rawlim[st.inc], eb, (st.meta >> 15) & 1u);
+          done = true;
+        }
+        if (!done) {
+          // read from x: a refused composite, a region without items, a raw row beyond the fetched ones
+          const int64_t r0 = ws.row_base + (ta + (from >> 9) - ws.tb) * kTileRows + (from & 511u);
+          const int64_t r1 = ws.row_base + (ta + (to >> 9) - ws.tb) * kTileRows + (to & 511u);
+          const int64_t a = max(r0 * kLaneTerms, ws.g_lo), b = min(r1 * kLaneTerms, ws.g_hi);
+          if (b > a) S = raw_from_x(p, sm, S, a, b);
+        }
+#ifdef SEQSUM_PROFILE
+        if (lane == 0) {
+          // the walk's steps: kind and cycles (taken before the counter's round trip)
+          const uint64_t cy = clock64() - t_seg;
+          const unsigned long long slot = atomicAdd(&p.dbg[4095], 1ull);
+          const uint64_t info = kind == ST_RAW2 ? (uint64_t)sm.prof_i | ((uint64_t)eb << 31) : (uint64_t)i;
+          if (slot < 1000) p.dbg[4096 - 1000 - 1 + slot] = ((uint64_t)kind << 60) | ((info & 0xFFFFFFFFFFull) << 20) | (cy & 0xFFFFF);
+        }
+#endif
+      }
+    }
+    WRT(r, 3);
+    if (lane == 0) {
+      sm.wuse_c[pw] = use + 1;
+      stat_add(sm, S_WALK_BATCHES, 1);
+      stat_add(sm, S_CY_WALK_SERIAL, clock64() - c1);
+    }
+    __syncwarp();
+    if (got && lane == 0) mbar_arrive(&sm.wempty[pw]);
+    if (!got) break;   // the slot may still be written: stop using them
+  }
+  if (lane == 0) stat_add(sm, S_WALK_SEGMENTS, nrun);
+  return failed ? 0x7FF8000000000000ull : S;
 }
 
 // Walks the tiles [ws.tb, ws.te) of one sum from the start value Sb.
-// Returns the sum's bits; NaN if a header never came.
 __device__ __noinline__ uint64_t walk_sum(const Params &p, Smem &sm, unsigned char *dyn, const WalkSum &ws,
-                                         uint64_t Sb, uint32_t tag) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  Rec *bh = reinterpret_cast<Rec *>(dyn);                                   // kBatch headers
-  Rec *slots = bh + kBatch;                                                 // kBatchSlots item slots
-  Run *comp = reinterpret_cast<Run *>(dyn + (kBatch + kBatchSlots) * 32);   // composites at segment tails
-  int16_t *seg_tail = reinterpret_cast<int16_t *>(comp + kBatch);
-  int16_t *seg_start = seg_tail + kBatch;
-  int16_t *sl_off = seg_start + kBatch;
-  int16_t *sl_cnt = sl_off + kBatch;
-  if (tid == 0) {
-    sm.S = Sb;
-    sm.fail = 0;
+                                         uint64_t Sb) {
+  const int w = threadIdx.x >> 5;
+  RangeSlot *slots = reinterpret_cast<RangeSlot *>(dyn);
+  const int nranges = (int)((ws.te - ws.tb + kRangeTiles - 1) / kRangeTiles);
+  if (w < kWarps) {
+    walk_producer(p, sm, slots[w], ws, nranges, w, sm.tag);
+  } else {
+    const uint64_t S = walk_serial(p, sm, slots, ws, nranges, Sb);
+    if ((threadIdx.x & 31) == 0) sm.S = S;
   }
   __syncthreads();
-  int64_t pos = ws.tb;
-  while (pos < ws.te) {
-    const int nb = (int)min((int64_t)kBatch, ws.te - pos);
-    if (tid == 0) {
-      const uint64_t t0 = gtimer();
-      uint32_t spin = 0;
-      sm.fail = 0;
-      while (true) {
-        const Rec q = ld_rec_vol(&p.hdr[pos]);
-        if (tags_ok(q, tag)) break;
-        if ((++spin & 63u) == 0u && gtimer() - t0 > p.wait_ns) {
-          note_timeout(p, ERR_WALK_TIMEOUT, 3, (uint32_t)pos, (uint32_t)ws.te);
-          sm.fail = 1;
-          break;
-        }
-        __nanosleep(64);
-      }
-      sm.count = nb;
-    }
-    __syncthreads();
-    if (sm.fail) break;
-    Rec h;
-    h.w[0] = h.w[1] = h.w[2] = h.w[3] = 0;
-    bool ready = false;
-    if (tid < nb) {
-      h = ld_rec_vol(&p.hdr[pos + tid]);
-      ready = tags_ok(h, tag);
-    }
-    if (tid < nb && !ready) atomicMin(&sm.count, tid);
-    __syncthreads();
-    int count = sm.count;
-    fence_acq_rel();
-    const Item it = unpack_item(h);
-    // item slots of the complex tiles, packed in order
-    uint32_t my = (tid < count && it.kind == K_COMPLEX) ? it.count : 0u;
-    uint32_t inc = my;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t q = __shfl_up_sync(kFull, inc, o);
-      if (lane >= o) inc += q;
-    }
-    if (lane == 31) sm.wslots[w] = inc;
-    __syncthreads();
-    uint32_t base = 0;
-    for (int k = 0; k < w; k++) base += sm.wslots[k];
-    const uint32_t off = base + inc - my;
-    if (tid < count && off + my > (uint32_t)kBatchSlots) atomicMin(&sm.count, tid);
-    __syncthreads();
-    count = sm.count;   // the batch ends before the first tile whose items do not fit
-    const bool mine = tid < count;
-    if (tid < count) {
-      bh[tid] = h;
-      sl_off[tid] = (int16_t)off;
-      sl_cnt[tid] = (int16_t)my;
-    }
-    __syncthreads();
-    const uint32_t total = count > 0 ? (uint32_t)sl_off[count - 1] + (uint32_t)sl_cnt[count - 1] : 0u;
-    for (uint32_t q = tid; q < total; q += kThreads) {
-      int lo = 0, hi = count;   // the tile whose slots hold q: sl_off[lo] <= q < sl_off[lo] + sl_cnt[lo]
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if ((uint32_t)sl_off[mid] <= q) lo = mid;
-        else hi = mid;
-      }
-      const uint32_t k = q - (uint32_t)sl_off[lo];
-      if (SQ_OK(p, k < (uint32_t)kItemSlots && q < (uint32_t)kBatchSlots, 21, q))
-        slots[q] = p.items[(pos + lo) * kItemSlots + k];
-    }
-    // ---- segmented scan of the runs over the batch's headers
-    const Item me = mine ? unpack_item(bh[tid]) : it;
-    const bool isrun = mine && me.kind == K_RUN;
-    Run r = isrun ? me.r : run_empty();
-    const uint32_t key = isrun ? me.eb : 0xFFFFFFFFu;
-    const uint32_t pkey0 = __shfl_up_sync(kFull, key, 1);
-    const bool prun0 = __shfl_up_sync(kFull, isrun, 1);
-    if (lane == 0) sm.whead0[w] = 0;
-    __syncthreads();
-    // the previous element of lane 0 is the last lane of the previous warp
-    uint32_t pkey = pkey0;
-    bool prun = prun0;
-    if (lane == 0 && w > 0) {
-      const Item pv = unpack_item(bh[tid - 1]);
-      prun = (tid - 1 < count) && pv.kind == K_RUN;
-      pkey = prun ? pv.eb : 0xFFFFFFFFu;
-    }
-    const bool head = mine && (tid == 0 || !isrun || !prun || key != pkey);
-    bool hf = head;
-    int st = head ? tid : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const Run q = shfl_run_up(r, o);
-      const bool qh = __shfl_up_sync(kFull, hf, o);
-      const int qs = __shfl_up_sync(kFull, st, o);
-      if (lane >= o) {
-        if (!hf) r = run_compose(q, r);
-        hf = hf || qh;
-        st = max(st, qs);
-      }
-    }
-    if (lane == 31) {
-      sm.wtot[w] = r;
-      sm.wtot_head[w] = hf;
-      sm.wstart[w] = st;
-    }
-    if (lane == 0) sm.whead0[w] = head;
-    __syncthreads();
-    if (!hf) {
-      // the segment began in an earlier warp: compose the carry in
-      Run cr = run_empty();
-      int cs = 0;
-      for (int k = 0; k < w; k++) {
-        cr = sm.wtot_head[k] ? sm.wtot[k] : run_compose(cr, sm.wtot[k]);
-        cs = max(cs, sm.wstart[k]);
-      }
-      r = run_compose(cr, r);
-      st = max(st, cs);
-    }
-    const bool sd = __shfl_down_sync(kFull, head, 1);
-    const bool nxhead = (lane < 31) ? sd : (w + 1 < kWarps ? (sm.whead0[w + 1] != 0) : true);
-    const bool tl = mine && (tid == count - 1 || nxhead || !isrun);
-    const uint32_t tb = __ballot_sync(kFull, tl);
-    if (lane == 0) sm.wtails[w] = __popc(tb);
-    __syncthreads();
-    uint32_t tbase = 0;
-    for (int k = 0; k < w; k++) tbase += sm.wtails[k];
-    if (tl) {
-      const uint32_t j = tbase + __popc(tb & ((1u << lane) - 1u));
-      seg_tail[j] = (int16_t)tid;
-      seg_start[j] = (int16_t)(isrun ? st : tid);
-      comp[j] = r;
-    }
-    if (tid == 0) {
-      uint32_t nseg = 0;
-      for (int k = 0; k < kWarps; k++) nseg += sm.wtails[k];
-      sm.nseg = (int)nseg;
-    }
-    __syncthreads();
-    // ---- the in-order pass (warp 0)
-    if (w == 0) {
-      uint64_t S = sm.S;
-      const int nseg = sm.nseg;
-      for (int j = 0; j < nseg; j++) {
-        const int i = seg_tail[j];
-        const Item e = unpack_item(bh[i]);
-        if (e.kind == K_RUN) {
-          uint64_t nb2 = S;
-          int ok = 0;
-          if (lane == 0) ok = run_apply(nb2, comp[j], (int)e.eb - 1023) == APPLY_OK;
-          ok = __shfl_sync(kFull, ok, 0);
-          if (ok) {
-            S = __shfl_sync(kFull, nb2, 0);
-          } else {
-            for (int ii = seg_start[j]; ii <= i; ii++) {
-              const Item e2 = unpack_item(bh[ii]);
-              S = apply_or_raw(p, sm, S, e2.r, e2.eb, ws, pos + ii, 0, kTileTerms);
-            }
-          }
-          if (lane == 0) stat_add(sm, S_WALK_SEGMENTS, 1);
-        } else if (e.kind == K_COMPLEX) {
-          S = apply_items(p, sm, S, slots + sl_off[i], (uint32_t)sl_cnt[i], ws, pos + i);
-        } else {
-          int64_t a, b;
-          clip(ws, pos + i, 0, kTileTerms, a, b);
-          S = raw_from_x(p, sm, S, a, b);
-        }
-      }
-      if (lane == 0) {
-        sm.S = S;
-        stat_add(sm, S_WALK_BATCHES, 1);
-      }
-    }
-    __syncthreads();
-    pos += count;
-  }
-  __syncthreads();
-  const uint64_t out = sm.fail ? 0x7FF8000000000000ull : sm.S;
+  const uint64_t out = sm.S;
   __syncthreads();
   return out;
 }
 
-__device__ __noinline__ void walk_loop(const Params &p, Smem &sm, unsigned char *dyn, int64_t ntiles, uint32_t tag) {
+__device__ __noinline__ void walk_loop(const Params &p, Smem &sm, unsigned char *dyn, int64_t ntiles) {
   const int tid = threadIdx.x;
+  if (tid < kWarps) {
+    mbar_init(&sm.wfull[tid], 1);
+    mbar_init(&sm.wempty[tid], 1);
+    sm.wuse_p[tid] = 0;
+    sm.wuse_c[tid] = 0;
+  }
+  fence_mbar_init();
+  __syncthreads();
   while (true) {
     if (tid == 0) sm.wk = p.offsets ? (int)atomicAdd(&p.ctr[C_SUMTICKET], 1u) : (sm.wk == 0 ? 0 : 1);
     __syncthreads();
@@ -1183,7 +2083,7 @@ __device__ __noinline__ void walk_loop(const Params &p, Smem &sm, unsigned char 
       ws.row_base = 0;
       s0 = p.s0;
     }
-    const uint64_t S = walk_sum(p, sm, dyn, ws, dbits(s0), tag);
+    const uint64_t S = walk_sum(p, sm, dyn, ws, dbits(s0));
     if (tid == 0) {
       p.outs[k] = bitsd(S);
       if (!p.offsets) sm.wk = 1;
@@ -1193,18 +2093,39 @@ __device__ __noinline__ void walk_loop(const Params &p, Smem &sm, unsigned char 
 }
 
 // ------------------------------------------------------------------ the kernel
-__global__ void __launch_bounds__(kThreads, 2) seqsum_kernel(const Params p, const __grid_constant__ CUtensorMap tmap) {
+__global__ void __launch_bounds__(kBlockThreads, 2) seqsum_kernel(const Params p, const __grid_constant__ CUtensorMap tmap) {
   extern __shared__ unsigned char dyn_raw[];
   unsigned char *dyn = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Smem sm;
   const int tid = threadIdx.x;
-  if (tid < S_ACCUM_END) sm.stat[tid] = 0;
+  for (int i = tid; i < kBlockWarps * S_ACCUM_END; i += kBlockThreads) (&sm.stat[0][0])[i] = 0;
   if (tid == 0) {
     sm.role = (int)atomicAdd(&p.ctr[C_ROLE], 1u);
-    const uint32_t e = *reinterpret_cast<volatile uint32_t *>(&p.ctr[C_EPOCH]);
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    // the walker and the scanner are latency-bound: a streaming CTA that finds
+    // itself on their SM leaves it to them.  Both roles are taken by CTAs
+    // already running, which write their SM right after taking the role; a
+    // streaming CTA waits for both words (bounded: past the limit it streams)
+    if (sm.role == 0) atomicExch(&p.ctr[C_WALK_SM], smid + 1);
+    if (sm.role == p.nwalkers) atomicExch(&p.ctr[C_SCAN_SM], smid + 1);
+    sm.alone = 0;
+    if (sm.role > p.nwalkers) {
+      uint32_t ws = 0, ss = 0;
+      const uint64_t t0 = gtimer();
+      for (;;) {
+        ws = ld_relaxed_u32(&p.ctr[C_WALK_SM]);
+        ss = ld_relaxed_u32(&p.ctr[C_SCAN_SM]);
+        if ((ws != 0u && ss != 0u) || gtimer() - t0 > 20000ull) break;
+        __nanosleep(64);
+      }
+      sm.alone = ws == smid + 1 || ss == smid + 1;
+      if (sm.alone) sm.stat[kWarps][S_ALONE] += 1;
+    }
+    const uint32_t e = ld_relaxed_u32(&p.ctr[C_EPOCH]);
     sm.tag = e == 0 ? 1u : e;
-    sm.ntiles = p.offsets ? (int64_t)*reinterpret_cast<volatile uint32_t *>(&p.ctr[C_NTILES]) : p.ntiles;
-    sm.fail = *reinterpret_cast<volatile uint32_t *>(&p.ctr[C_SKIP]) != 0u && p.offsets;
+    sm.ntiles = p.offsets ? (int64_t)ld_relaxed_u32(&p.ctr[C_NTILES]) : p.ntiles;
+    sm.fail = ld_relaxed_u32(&p.ctr[C_SKIP]) != 0u && p.offsets;
     sm.wk = 0;
     if (sm.role == 0) p.stats[S_T_START] = gtimer();
   }
@@ -1214,16 +2135,24 @@ __global__ void __launch_bounds__(kThreads, 2) seqsum_kernel(const Params p, con
   const bool skip = sm.fail;
   __syncthreads();
   if (!skip) {
+    // roles in the order the CTAs start: the walkers, the scanner, then the
+    // streaming CTAs (every waiting role is held by a CTA already running)
     if (sm.role < p.nwalkers) {
-      walk_loop(p, sm, dyn, ntiles, tag);
+      walk_loop(p, sm, dyn, ntiles);
       if (tid == 0) atomicMax(&p.stats[S_T_WALK_END], (unsigned long long)gtimer());
-    } else {
-      stream_loop(p, sm, dyn, &tmap, ntiles, tag);
+    } else if (sm.role == p.nwalkers) {
+      scan_cta(p, sm, ntiles);
+    } else if (!sm.alone) {
+      stream_cta(p, sm, dyn, &tmap, ntiles);
       if (tid == 0 && sm.t_stream_end) atomicMax(&p.stats[S_T_STREAM_END], (unsigned long long)sm.t_stream_end);
     }
   }
   __syncthreads();
-  if (tid < S_ACCUM_END && sm.stat[tid]) atomicAdd(&p.stats[tid], sm.stat[tid]);
+  if (tid < S_ACCUM_END) {
+    unsigned long long v = 0;
+    for (int k = 0; k < kBlockWarps; k++) v += sm.stat[k][tid];
+    if (v) atomicAdd(&p.stats[tid], v);
+  }
   if (tid == 0) {
     __threadfence();
     const uint32_t done = atomicAdd(&p.ctr[C_EXIT], 1u);
@@ -1237,8 +2166,9 @@ __global__ void __launch_bounds__(kThreads, 2) seqsum_kernel(const Params p, con
     __threadfence();
     const uint32_t next = tag + 1;
     if (next > 255u) {
-      for (int64_t i = tid; i < p.cap_tiles; i += kThreads) {
+      for (int64_t i = tid; i < p.cap_tiles; i += kBlockThreads) {
         p.status[i] = make_uint4(0, 0, 0, 0);
+        p.prec[i * kPrecWords] = make_uint4(0, 0, 0, 0);
         Rec z;
         z.w[0] = z.w[1] = z.w[2] = z.w[3] = 0;
         st_rec(&p.hdr[i], z);
@@ -1250,6 +2180,8 @@ __global__ void __launch_bounds__(kThreads, 2) seqsum_kernel(const Params p, con
       p.ctr[C_TICKET] = 0;
       p.ctr[C_ROLE] = 0;
       p.ctr[C_SUMTICKET] = 0;
+      p.ctr[C_WALK_SM] = 0;
+      p.ctr[C_SCAN_SM] = 0;
       p.ctr[C_EPOCH] = next > 255u ? 1u : next;
       __threadfence();
       p.ctr[C_EXIT] = 0;
@@ -1327,7 +2259,7 @@ __global__ void __launch_bounds__(kThreads) setup_kernel(const Params p) {
 int kernel_blocks_per_sm() {
   int n = 0;
   cudaFuncSetAttribute(seqsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, seqsum_kernel, kThreads, kDynSmem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, seqsum_kernel, kBlockThreads, kDynSmem);
   return n > 0 ? n : 1;
 }
 
@@ -1338,7 +2270,7 @@ cudaError_t launch_seqsum(const Params &p, const CUtensorMap *tmap, int grid, cu
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  seqsum_kernel<<<grid, kThreads, kDynSmem, st>>>(p, *tmap);
+  seqsum_kernel<<<grid, kBlockThreads, kDynSmem, st>>>(p, *tmap);
   return cudaGetLastError();
 }
 

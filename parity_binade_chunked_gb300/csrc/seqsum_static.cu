@@ -25,6 +25,7 @@ static_assert(kStaticTiles * sq::kTileTerms == SEQSUM_STATIC_MAX_TERMS, "whole t
 // at zero; the kernel keeps them consistent from call to call (it advances
 // the tag itself and clears the tagged words when the tag wraps).
 static __device__ __align__(256) uint4 s_status[kStaticTiles];
+static __device__ __align__(256) uint4 s_prec[kStaticTiles * sq::kPrecWords];
 static __device__ __align__(256) Rec s_hdr[kStaticTiles];
 static __device__ __align__(256) Rec s_items[kStaticTiles * sq::kItemSlots];
 static __device__ __align__(256) uint32_t s_ctr[sq::C_COUNT];
@@ -34,7 +35,7 @@ static __device__ __align__(256) int64_t s_tile_begin[2];
 
 struct DeviceScratch {
   bool ready = false;
-  uint4 *status = nullptr;
+  uint4 *status = nullptr, *prec = nullptr;
   Rec *hdr = nullptr, *items = nullptr;
   uint32_t *ctr = nullptr;
   unsigned long long *stats = nullptr, *dbg = nullptr;
@@ -64,6 +65,7 @@ cudaError_t symbol(T **out, const void *sym) {
 cudaError_t setup(DeviceScratch &d, int dev, cudaStream_t stream) {
   cudaError_t e;
   if ((e = symbol(&d.status, s_status)) != cudaSuccess) return e;
+  if ((e = symbol(&d.prec, s_prec)) != cudaSuccess) return e;
   if ((e = symbol(&d.hdr, s_hdr)) != cudaSuccess) return e;
   if ((e = symbol(&d.items, s_items)) != cudaSuccess) return e;
   if ((e = symbol(&d.ctr, s_ctr)) != cudaSuccess) return e;
@@ -81,6 +83,7 @@ cudaError_t setup(DeviceScratch &d, int dev, cudaStream_t stream) {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   if ((e = cudaMemsetAsync(d.status, 0, sizeof s_status, stream)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(d.prec, 0, sizeof s_prec, stream)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(d.hdr, 0, sizeof s_hdr, stream)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(d.ctr, 0, sizeof s_ctr, stream)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(d.stats, 0, sizeof s_stats, stream)) != cudaSuccess) return e;
@@ -134,6 +137,8 @@ extern "C" int seqsum_f64_static(const double *x, int64_t n, double s0, double *
   p.ntiles = tiles;
   p.nsums = 1;
   p.status = d.status;
+  p.prec = d.prec;
+  p.wave = 1024;
   p.hdr = d.hdr;
   p.items = d.items;
   p.ctr = d.ctr;
@@ -145,7 +150,8 @@ extern "C" int seqsum_f64_static(const double *x, int64_t n, double s0, double *
   p.tma_rows = n > 0 ? tensor_map(d, x, n) : 0;
   p.nwalkers = 1;
   int64_t grid = (int64_t)d.num_sms * g_blocks_per_sm;
-  if (tiles + 1 < grid) grid = tiles + 1;
+  if (2 * tiles + 2 < grid) grid = 2 * tiles + 2;
+  if (grid < 3) grid = 3;
   static CUtensorMap dummy;
   e = sq::launch_seqsum(p, p.tma_rows ? &d.tmap : &dummy, (int)grid, stream);
   return e == cudaSuccess ? SEQSUM_OK : SEQSUM_ECUDA;

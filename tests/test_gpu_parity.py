@@ -182,12 +182,11 @@ def test_negative_and_cancelling_sums(sq):
     check(sq, z, 0.0, "up, down, up")
 
 
-def test_walk_batch_ends_where_staged_items_run_out(sq):
+def test_walk_ranges_full_of_items(sq):
     """A signed random walk crosses zero again and again, so most tiles carry
-    item lists; a walk batch then stages more item slots than its shared
-    memory holds and must end before the first tile that does not fit (and
-    take that tile in the next batch, once).  Prefixes of several lengths,
-    ragged tails included."""
+    item lists and a walk range can hold more steps than its slot (the range
+    is then read from x).  Prefixes of several lengths, ragged tails and a
+    partial last range included."""
     rng = np.random.default_rng(4)
     y = rng.standard_normal(200000) * np.ldexp(1.0, rng.integers(-10, 10, 200000))
     for n in [188284, 188285, 150000, 200000, 4096 * 40, 4096 * 40 + 1]:
@@ -219,18 +218,19 @@ def test_stream_and_repeats(sq):
         assert_same(o.item(), wants[k], f"repeat plane {k}")
 
 
-def test_crossing_at_every_term_overflows_the_item_area(sq):
+def test_crossing_at_every_term_reads_the_range_from_x(sq):
     """A running sum that crosses a power of two at every term (1.0, 0.5,
     1.0, ...): every row's plan range spans a power of two, so every row is
-    raw and no tile's items fit its area -- the walk reads those tiles' terms
-    itself, and the bits still match the loop's."""
+    a raw item and a walk range holds more steps than its slot -- the walk
+    reads that range's terms from x itself, and the bits still match the
+    loop's."""
     n = 32 * 4096 * 2
     x = np.empty(n)
     x[0] = 1.0
     x[1::2] = -0.5
     x[2::2] = 0.5
     st = check(sq, x, 0.0, "alternating crossings")
-    assert st["tiles_overflow"] > 0, st
+    assert st["ranges_from_x"] > 0, st
 
 
 # ------------------------------------------------------------ plan independence
