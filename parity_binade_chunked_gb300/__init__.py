@@ -18,7 +18,7 @@ import threading
 from . import build as _build
 
 __all__ = ["seqsum_f64", "seqsum_f64_static", "seqsum_f64_batched", "seqsum_f64_batched_sized", "get_stats",
-           "debug_set_plan", "debug_set_fault", "debug_counters", "release_workspace", "version", "lib",
+           "debug_set_plan", "debug_set_fault", "debug_counters", "release_workspace", "version", "lib", "lib_path",
            "SeqsumError"]
 
 _lock = threading.Lock()
@@ -79,8 +79,14 @@ def lib():
             L.seqsum_debug_set_fault.restype = ctypes.c_int
             L.seqsum_version.argtypes = []
             L.seqsum_version.restype = ctypes.c_char_p
+            L._path = path
             _lib = L
         return _lib
+
+
+def lib_path() -> str:
+    """The file of the loaded library (the plain, self-checking or profiling build)."""
+    return lib()._path
 
 
 def _check(rc: int):

@@ -869,7 +869,7 @@ __device__ __forceinline__ void run_unit(const Params &p, Smem &sm, UnitSm &us, 
     const uint32_t nraw2 = __popc(__ballot_sync(kFull, raw2));
     if (lane == 0 && nraw2) stat_add(sm, S_LANE_RAW2, nraw2);
     const uint32_t at = __popc(mdesc & ((1u << lane) - 1u));
-    {
+    if (SQ_OK(p, total <= (uint32_t)kWarpSlots, 1, total)) {
       Rec *area = p.items + t * kItemSlots + w * kWarpSlots;
       if (raw) {
         Item it;
@@ -1034,7 +1034,7 @@ __device__ __forceinline__ void run_unit(const Params &p, Smem &sm, UnitSm &us, 
       const uint32_t tb = __ballot_sync(kFull, tail);
       __syncwarp();   // every read of the chunk before any write
       if (close_prev) {
-        if (lane == 0) {
+        if (lane == 0 && SQ_OK(p, M < c, 2, M)) {
           Item m;
           m.r = carry;
           saturate(m.r);
@@ -1054,7 +1054,8 @@ __device__ __forceinline__ void run_unit(const Params &p, Smem &sm, UnitSm &us, 
           m.start = from;
           m.count = it.start + it.count - from;
         }
-        st_rec(&area[M + __popc(tb & lt)], pack_item(m, 0));
+        const int at = M + __popc(tb & lt);
+        if (SQ_OK(p, at <= i && at < kItemSlots, 2, at)) st_rec(&area[at], pack_item(m, 0));
       }
       M += __popc(tb);
       carry = shfl_run_idx(rr, 31);
@@ -1674,6 +1675,7 @@ __device__ __forceinline__ Elem range_elem(const Params &p, const Rec (&hl)[4], 
     return el;
   }
   if (hk != K_COMPLEX || complex_items(h) == 0) return el;   // a tile read from x
+  if (!SQ_OK(p, kk < complex_items(h), 3, kk)) return el;
   const Rec q = ld_rec_vol(&p.items[(ta + tt) * kItemSlots + kk]);
   const Item it = unpack_item(q);
   el.from = rpos(tt, it.start / kLaneTerms);
@@ -1765,6 +1767,7 @@ __device__ __noinline__ void walk_producer(const Params &p, Smem &sm, RangeSlot 
     }
     const int N = ok ? (int)__shfl_sync(kFull, off, 31) : 0;
     const bool direct = N == tn;   // every tile one element
+    if (ok && lane == 0) (void)SQ_OK(p, N >= tn, 4, N);
     off -= n;
 #pragma unroll
     for (int j = 0; j < 4; j++) eo[j] += off;
@@ -1895,6 +1898,7 @@ __device__ __noinline__ void walk_producer(const Params &p, Smem &sm, RangeSlot 
       pending = __shfl_sync(kFull, in && !tail, 31);
     }
     over = nsteps > kRangeSteps;
+    if (lane == 0 && N > 0) (void)SQ_OK(p, nsteps >= 1, 6, N);
     __syncwarp();
     // ---- the raw rows' terms from x (all loads at once), then their prefix tables
     const int nfetch = over ? 0 : min(nraw, kRangeRaw);
@@ -1979,6 +1983,7 @@ __device__ __noinline__ uint64_t walk_serial(const Params &p, Smem &sm, RangeSlo
 #endif
         const uint32_t eb = (uint32_t)(st.meta >> 2) & 0x7FFu;
         const uint32_t from = (uint32_t)(st.meta >> 23) & 0xFFFFu, to = (uint32_t)(st.meta >> 39) & 0xFFFFu;
+        if (lane == 0) (void)SQ_OK(p, from < to, 5, ((int64_t)from << 16) | to);
         bool done = false;
         if (kind == ST_RUN) {
           Run q;

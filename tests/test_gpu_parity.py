@@ -50,6 +50,7 @@ def gpu_sum(sq, x, s0=0.0, offset=0):
 
 def check(sq, x, s0=0.0, what="", offset=0):
     want = oracle.seqsum(x, s0)
+    sq.get_stats()   # counters of earlier calls out of the way
     got = gpu_sum(sq, x, s0, offset)
     assert_same(got, want, what)
     st = sq.get_stats()
@@ -102,6 +103,45 @@ def test_config_c4_full_size(sq):
     assert st["device_status"] == 0
     got2 = _batched(sq, wl, False)
     assert np.array_equal(got.view(np.uint64), got2.view(np.uint64))
+
+
+@pytest.mark.parametrize("name", ["c3", "c5"])
+@pytest.mark.parametrize("mult", [2, 4])
+def test_single_sums_above_the_wave(sq, name, mult):
+    """One sum of 2x and 4x the plane's height: more tiles than the wave the
+    plan units run ahead of the run units (2048), so plan and run units mix
+    and the walk takes ranges while tiles are still being formed."""
+    wl = W.config(name, height_mult=mult)
+    st = check(sq, wl.x, float(wl.s0[0]), f"{name} x{mult}")
+    assert st["tiles"] == (len(wl.x) + 4095) // 4096
+
+
+def test_single_sum_one_term_past_2048_tiles(sq):
+    """2048 * 4096 + 1 terms: the last tile holds one term, one past the wave."""
+    x = W.plane_c2(2048 * 4096 + 1, 1, seed=31)
+    st = check(sq, x, 0.125, "2048 tiles + 1 term")
+    assert st["tiles"] == 2049
+
+
+# ------------------------------------------------------------ bounded waits
+
+def test_withheld_header_times_out_then_recovers(sq):
+    """A tile header that never comes (the fault hook withholds it): the
+    walk's bounded wait gives up, the call writes NaN and reports
+    SEQSUM_ETIMEOUT at site 3 (a walk header), and the next call -- on the
+    same workspace -- is exact again."""
+    x = W.plane_c2(4096 * 40 + 5, 1, seed=3)
+    sq.debug_set_fault(1, 17, 3_000_000)   # tile 17's header withheld; every wait gives up after 3 ms
+    try:
+        got = gpu_sum(sq, x, 0.0)
+        st = sq.get_stats()
+    finally:
+        sq.debug_set_fault(0, 0, 0)
+    assert got != got, got
+    assert st["device_status"] == -3, st
+    assert st["timeout_site"] == 3, st
+    check(sq, x, 0.0, "the call after a timeout")
+    check(sq, W.config("c1").x, 0.0, "c1 after a timeout")
 
 
 # ------------------------------------------------------------ edge cases

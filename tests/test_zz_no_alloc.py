@@ -47,3 +47,31 @@ def test_static_matches_seqsum_f64_two_calls_in_a_row():
         torch.cuda.synchronize()
         got = [bits(v.item()) for v in (ref, a, b)]
         assert got == [bits(want)] * 3, (len(x), s0, got, bits(want))
+
+
+@pytest.mark.gpu
+def test_static_many_calls_misaligned_and_no_device_allocation():
+    """130 calls in a row (past the 255-call tag cycle when the session's
+    other calls are counted), a plane that starts one double past an aligned
+    address (no tensor map: the rows are read with plain loads), and the
+    device's free memory unchanged across all of them."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import parity_binade_chunked_gb300 as sq
+    x = W.plane_c3(512, 300, seed=25, zero_rows=4)
+    buf = torch.zeros(len(x) + 1, dtype=torch.float64, device="cuda")
+    buf[1:] = torch.from_numpy(x)
+    xv = buf[1:]                                       # 8 bytes past a 256-byte aligned start
+    assert xv.data_ptr() % 16 == 8
+    want = bits(oracle.seqsum(x, 0.5))
+    outs = torch.empty(130, dtype=torch.float64, device="cuda")
+    sq.seqsum_f64_static(xv, 0.5, out=outs[0:1])      # the first call sets the scratch up
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for i in range(130):
+        sq.seqsum_f64_static(xv, 0.5, out=outs[i:i + 1])
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    got = outs.cpu().numpy().view(np.uint64)
+    assert all(int(g) == want for g in got), [hex(int(g)) for g in got[:4]]
+    assert free1 == free0, (free0, free1)
