@@ -160,8 +160,20 @@ __device__ __forceinline__ void tl_mark(const Params &p, int role, int who, uint
   do {                                                                  \
     if ((threadIdx.x & 31) == 0 && (r) < 64) p.dbg[2100 + 4 * (r) + (k)] = gtimer(); \
   } while (0)
+// the scanner's windows: globaltimer at the poll that found them, their first tile and size, when published
+#define SCW(k, v)                                                              \
+  do {                                                                         \
+    if (threadIdx.x == 0 && nwin < 64) p.dbg[2400 + 4 * nwin + (k)] = (v);     \
+  } while (0)
+// range 0's producer phases (stamps)
+#define WR0(r, k)                                                            \
+  do {                                                                       \
+    if ((threadIdx.x & 31) == 0 && (r) == 4 && (k) < 40) p.dbg[2360 + (k)] = gtimer(); \
+  } while (0)
 #else
 #define WRT(r, k) ((void)0)
+#define WR0(r, k) ((void)0)
+#define SCW(k, v) ((void)0)
 #define TL(p, role, who, u, k) ((void)0)
 #define WPH(k) ((void)0)
 #define WPH_INIT ((void)0)
@@ -305,6 +317,7 @@ struct Smem {
   int wk;
   uint64_t S;                        // the walk's running value (bits)
   uint32_t prof_i;                   // profiling builds: how a raw row with tables ended
+  uint32_t prof_n;                   // profiling builds: walk steps logged
   uint64_t t_stream_end;
   // the walk's slots: handed over by mbarriers, their uses counted on each side
   uint64_t wfull[kWarps];
@@ -424,6 +437,12 @@ __device__ __forceinline__ Geo stage_geo(const StageSm &st) {
   g.sum = (int32_t)st.geo[4];
   return g;
 }
+
+// 16 bytes global -> shared, asynchronously (this thread waits for its own copies with cp_async_wait)
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -1212,8 +1231,10 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
   float carry_abs = 0.0f;
   int64_t pos = 0;
   uint64_t t_wait = 0;
+  int nwin = 0;
   while (pos < ntiles) {
     // this thread's four consecutive tiles of the window
+    const uint64_t t_poll = gtimer();
     const int64_t t0 = pos + 4 * tid;
     uint4 v[4];
     bool rd[4];
@@ -1253,6 +1274,9 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
       continue;
     }
     t_wait = 0;
+    SCW(0, t_poll);
+    SCW(1, (uint64_t)pos);
+    SCW(2, (uint64_t)nready);
     // This thread's tiles, in order: loc[j] is the inclusive sum from the
     // thread's first tile (or from the last sum start among them, which
     // restarts at its s0); hup[j] says whether a sum started at or before j.
@@ -1376,11 +1400,28 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
     carry_abs = s_wabs[0];
     __syncthreads();
     if (tid == 0) stat_add(sm, S_SCAN_WINDOWS, 1);
+    SCW(3, gtimer());
+    nwin++;
     pos += nready;
   }
 }
 
 // ------------------------------------------------------------------ the walk: raw terms
+// Terms i..n-1 of a row (lane l holds term l) added to Sb one by one with the
+// hardware add, in order (one warp; every lane computes the same value).  For
+// a row of 16 this is shorter than a round of prefix checks per crossing.
+__device__ __noinline__ uint64_t row_dadd(Smem &sm, uint64_t Sb, uint64_t t, int i, int n) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t t_in = clock64();
+  double S = bitsd(Sb);
+  for (int j = i; j < n; j++) S = __dadd_rn(S, bitsd(__shfl_sync(kFull, t, j)));
+  if (lane == 0) {
+    stat_add(sm, S_TERMS_DADD, (unsigned long long)max(0, n - i));
+    stat_add(sm, S_CY_WALK_RAW, clock64() - t_in);
+  }
+  return dbits(S);
+}
+
 // One warp adds up to 32 terms (lane l holds term l; lanes >= n hold -0) to
 // the exact running value Sb, in order: while Sb is a normal number (with
 // e >= -959), every term's run under Sb's binade is scanned in order and
@@ -1489,7 +1530,7 @@ __device__ __noinline__ uint64_t raw_from_x(const Params &p, Smem &sm, uint64_t 
 // and the table holds: the longest prefix whose increments keep the count
 // within the binade (m + P <= 2^53) is added at once, and the term after it
 // with the hardware add.  The rest goes term by term (raw_chunk).
-__device__ __noinline__ uint64_t raw2_row(Smem &sm, uint64_t S, const uint64_t *data, uint32_t lims, uint32_t ea,
+__device__ __forceinline__ uint64_t raw2_row(Smem &sm, uint64_t S, const uint64_t *data, uint32_t lims, uint32_t ea,
                                           uint64_t neg) {
   const int lane = threadIdx.x & 31;
   const uint64_t t_in = clock64();
@@ -1554,16 +1595,18 @@ __device__ __noinline__ uint64_t raw2_row(Smem &sm, uint64_t S, const uint64_t *
 #ifdef SEQSUM_PROFILE
   if (lane == 0) sm.prof_i = (uint32_t)i | (rounds << 8) | (dadds << 16) | (((uint32_t)(S >> 52) & 0x7FFu) << 20);
 #endif
-  if (i < kLaneTerms) S = raw_chunk(sm, S, t, i, kLaneTerms);
+  if (i < kLaneTerms) S = row_dadd(sm, S, t, i, kLaneTerms);
   return S;
 }
 
 // ------------------------------------------------------------------ the walk: ranges of tiles
 // A walker CTA: eight producer warps and one in-order warp.  The tiles of a
-// sum are cut into ranges of kRangeTiles; producer warp k takes ranges k,
-// k + 8, ... and writes each, composed into steps, to its own slot; the
-// in-order warp takes the slots in range order and applies their steps to
-// the exact running value.  A slot's full and empty mbarriers hand it over.
+// sum are cut into ranges -- small at the sum's start, where a sum that
+// starts near zero crosses many binades, then kRangeTiles; producer warp k
+// takes ranges k, k + 8, ... and writes each, composed into steps, to its own
+// slot; the in-order warp takes the slots in range order and applies their
+// steps to the exact running value.  A slot's full and empty mbarriers hand
+// it over.
 struct WalkSum {
   int64_t tb, te;        // the sum's tiles
   int64_t row_base;      // the sum's first row
@@ -1584,17 +1627,31 @@ enum : uint32_t { ST_RUN = 0, ST_RAW = 1, ST_RAW2 = 2, ST_X = 3 };
 struct __align__(16) Step {
   int64_t inc, lo, hi;   // a composite's run; a raw row: its place among the slot's fetched rows (in inc)
   uint64_t meta;         // kind (2 bits), biased binade (11), d + 1 (2), flags (8), then its terms:
-                         // first tile (7) and row (9), last tile (7) and row after it (9), within the range
+                         // first tile (7) and row (9), last tile (7) and row after it (9), within the range;
+                         // bit 56: a plain run (non-negative, no tie, no poison)
 };
 __device__ __forceinline__ uint64_t step_meta(uint32_t kind, uint32_t eb, int32_t d, uint32_t flags, uint32_t from,
                                               uint32_t to) {
+  const bool plain = kind == 0u && d == 0 && (flags & F_NONNEG) && !(flags & F_POISON);
   return (uint64_t)(kind & 3u) | ((uint64_t)(eb & 0x7FFu) << 2) | ((uint64_t)((d + 1) & 3) << 13) |
-         ((uint64_t)(flags & 0xFFu) << 15) | ((uint64_t)(from & 0xFFFFu) << 23) | ((uint64_t)(to & 0xFFFFu) << 39);
+         ((uint64_t)(flags & 0xFFu) << 15) | ((uint64_t)(from & 0xFFFFu) << 23) | ((uint64_t)(to & 0xFFFFu) << 39) |
+         ((uint64_t)(plain ? 1u : 0u) << 56);
 }
 // a position in a range: tile (7 bits) and row (9 bits); positions compare as numbers
 __device__ __forceinline__ uint32_t rpos(uint32_t tile, uint32_t row) { return (tile << 9) | row; }
 
 constexpr int kRangeTiles = 4 * 32;   // tiles of a walk range (four per lane of a producer warp)
+// Ranges 0..7 hold 8, 8, 16, 16, 32, 32, 64, 64 tiles (240 in all), the later ones kRangeTiles.
+__device__ __forceinline__ int64_t range_start(int r) {
+  if (r >= 8) return 240 + (int64_t)(r - 8) * kRangeTiles;
+  return (int64_t)(8 << (r >> 1)) * (2 + (r & 1)) - 16;
+}
+__device__ __forceinline__ int range_count(int64_t tiles) {
+  if (tiles > 240) return 8 + (int)((tiles - 240 + kRangeTiles - 1) / kRangeTiles);
+  int r = 0;
+  while (range_start(r) < tiles) r++;
+  return r;
+}
 constexpr int kRangeSteps = 64;       // steps a slot holds (more: the range is read from x)
 constexpr int kRangeRaw = 24;         // raw rows a slot holds with their terms and tables
 struct RangeSlot {
@@ -1626,11 +1683,21 @@ __device__ __forceinline__ uint32_t complex_items(const Rec &h) {
   return (m >= 1 && m <= (uint64_t)kItemSlots) ? (uint32_t)m : 0u;
 }
 
-// Element E of the range (every lane of the warp calls it; in: E < n).
+// Element E of the range, in two parts so that the record of the next chunk
+// can be in flight while this one is composed.  range_fetch (every lane of
+// the warp calls it; in: E < n) finds the element's tile and takes the
+// tile's header from the lane that read it, or starts the load of the
+// element's item; range_decode reads the element from that record.
 // off: this lane's first element; eo: the first elements of its four tiles;
 // direct: every tile is one element (element E is tile E).
-__device__ __forceinline__ Elem range_elem(const Params &p, const Rec (&hl)[4], int64_t ta, int E, bool in,
-                                           uint32_t off, const uint32_t (&eo)[4], bool direct) {
+struct ElemRec {
+  Rec q;          // the tile's header (a run or a tile read from x) or the item
+  uint32_t tt;    // the tile in the range
+  uint32_t what;  // 0: q is a run header; 1: q is an item; 2: the tile is read from x
+  bool in;
+};
+__device__ __forceinline__ ElemRec range_fetch(const Params &p, const Rec (&hl)[4], int64_t ta, int E, bool in,
+                                               uint32_t off, const uint32_t (&eo)[4], bool direct) {
   uint32_t tt = (uint32_t)E, kk = 0;
   if (!direct) {
     // the lane whose tiles hold E: the last with off <= E
@@ -1646,13 +1713,10 @@ __device__ __forceinline__ Elem range_elem(const Params &p, const Rec (&hl)[4], 
     kk = (uint32_t)E - (j == 3u ? e3 : (j == 2u ? e2 : (j == 1u ? e1 : e0)));
     tt = 4u * (uint32_t)o + j;
   }
-  Elem el;
-  el.r = run_empty();
-  el.kind = EK_X;
-  el.key = kNoKey;
-  el.eb = el.neg = 0;
-  el.from = rpos(tt, 0);
-  el.to = rpos(tt, kTileRows);
+  ElemRec er;
+  er.tt = tt;
+  er.in = in;
+  er.what = 2;
   // the tile's header, from the lane that read it
   Rec h;
   h.w[0] = h.w[1] = h.w[2] = h.w[3] = 0;
@@ -1665,29 +1729,39 @@ __device__ __forceinline__ Elem range_elem(const Params &p, const Rec (&hl)[4], 
       if (j == jt) h.w[q] = v;
     }
   }
-  if (!in) return el;
+  er.q = h;
+  if (!in) return er;
   const uint32_t hk = (uint32_t)(h.w[3] & 7u);
   if (hk == K_RUN) {
-    const Item it = unpack_item(h);
-    el.r = it.r;
-    el.kind = EK_RUN;
-    el.key = it.eb;
-    return el;
+    er.what = 0;
+  } else if (hk == K_COMPLEX && complex_items(h) > 0 && SQ_OK(p, kk < complex_items(h), 3, kk)) {
+    er.q = ld_rec_vol(&p.items[(ta + tt) * kItemSlots + kk]);
+    er.what = 1;
   }
-  if (hk != K_COMPLEX || complex_items(h) == 0) return el;   // a tile read from x
-  if (!SQ_OK(p, kk < complex_items(h), 3, kk)) return el;
-  const Rec q = ld_rec_vol(&p.items[(ta + tt) * kItemSlots + kk]);
-  const Item it = unpack_item(q);
-  el.from = rpos(tt, it.start / kLaneTerms);
-  el.to = rpos(tt, (it.start + it.count) / kLaneTerms);
+  return er;
+}
+__device__ __forceinline__ Elem range_decode(const ElemRec &er) {
+  Elem el;
+  el.r = run_empty();
+  el.kind = EK_X;
+  el.key = kNoKey;
+  el.eb = el.neg = 0;
+  el.from = rpos(er.tt, 0);
+  el.to = rpos(er.tt, kTileRows);
+  if (!er.in || er.what == 2) return el;
+  const Item it = unpack_item(er.q);
+  if (er.what == 1) {
+    el.from = rpos(er.tt, it.start / kLaneTerms);
+    el.to = rpos(er.tt, (it.start + it.count) / kLaneTerms);
+  }
   if (it.kind == K_RUN) {
     el.r = it.r;
     el.kind = EK_RUN;
     el.key = it.eb;
-  } else if (it.kind == K_RAW || it.kind == K_RAW2) {
+  } else if (er.what == 1 && (it.kind == K_RAW || it.kind == K_RAW2)) {
     el.kind = it.kind == K_RAW ? EK_RAW : EK_RAW2;
     el.eb = it.eb;
-    el.neg = (uint32_t)(q.w[0] & 1u);
+    el.neg = (uint32_t)(er.q.w[0] & 1u);
   }
   return el;
 }
@@ -1711,13 +1785,14 @@ __device__ __noinline__ void walk_producer(const Params &p, Smem &sm, RangeSlot 
   const int lane = threadIdx.x & 31;
   const uint32_t lt = (1u << lane) - 1u;
   bool failed_all = false;
+  const bool x16 = (reinterpret_cast<uintptr_t>(p.x) & 15u) == 0;   // rows can be copied 16 bytes at a time
   for (int r = pw; r < nranges; r += kWarps) {
     // the slot's previous use must have been applied
     const uint32_t use = sm.wuse_p[pw];
     bool ok = !failed_all;
     if (use > 0) ok = mbar_wait_bounded(&sm.wempty[pw], (use - 1) & 1u, 4 * p.wait_ns);
-    const int64_t ta = ws.tb + (int64_t)r * kRangeTiles;
-    const int tn = (int)min((int64_t)kRangeTiles, ws.te - ta);
+    const int64_t ta = ws.tb + range_start(r);
+    const int tn = (int)min(range_start(r + 1) - range_start(r), ws.te - ta);
     // ---- the range's headers (four a lane), as they arrive
     Rec h[4];
     uint32_t need = 0;
@@ -1767,6 +1842,7 @@ __device__ __noinline__ void walk_producer(const Params &p, Smem &sm, RangeSlot 
     }
     const int N = ok ? (int)__shfl_sync(kFull, off, 31) : 0;
     const bool direct = N == tn;   // every tile one element
+    WR0(r, 0);
     if (ok && lane == 0) (void)SQ_OK(p, N >= tn, 4, N);
     off -= n;
 #pragma unroll
@@ -1778,10 +1854,14 @@ __device__ __noinline__ void walk_producer(const Params &p, Smem &sm, RangeSlot 
     Run carry = run_empty();      // the composite of the open segment (since its head)
     uint32_t ckey = kNoKey, cfrom = 0, cto = 0;
     bool pending = false;         // the chunk before ended inside a segment
+    ElemRec nx = range_fetch(p, h, ta, lane, lane < N, off, eo, direct);
     for (int c = 0; c < N; c += 32) {
       const int E = c + lane;
       const bool in = E < N;
-      const Elem el = range_elem(p, h, ta, E, in, off, eo, direct);
+      const ElemRec cur = nx;
+      if (c + 32 < N) nx = range_fetch(p, h, ta, E + 32, E + 32 < N, off, eo, direct);   // in flight meanwhile
+      const Elem el = range_decode(cur);
+      WR0(r, 2 + 2 * (c / 32));
       const uint32_t key = in ? el.key : kNoKey;
       uint32_t pkey = __shfl_up_sync(kFull, key, 1);
       if (lane == 0) pkey = ckey;
@@ -1840,25 +1920,64 @@ __device__ __noinline__ void walk_producer(const Params &p, Smem &sm, RangeSlot 
         ckey = key0;
         cfrom = from0;
         cto = to;
+        WR0(r, 3 + 2 * (c / 32));
         continue;
       }
       Run rr = el.r;
       bool f = head;
       uint32_t from = head ? el.from : 0u;
-      if (lane == 0 && in && !head) {
-        rr = run_compose(carry, rr);
-        from = cfrom;
-        f = true;   // the carry stands for its head
-      }
+      // every run of the chunk (and the open one before it) plain: a segmented
+      // sum of the increments, an AND of the flags
+      const bool cplain = carry.d == 0 && (carry.flags & F_NONNEG) && !(carry.flags & F_POISON);
+      const bool splain = __all_sync(kFull, el.kind != EK_RUN || (el.r.d == 0 && (el.r.flags & F_NONNEG) &&
+                                                                   !(el.r.flags & F_POISON))) &&
+                          (__shfl_sync(kFull, head, 0) || cplain);
+      if (splain) {
+        long long a = el.kind == EK_RUN ? (long long)el.r.inc : 0ll;
+        uint32_t fl = el.kind == EK_RUN ? el.r.flags : 0u;
+        if (lane == 0 && in && !head) {
+          a += (long long)carry.inc;
+          fl &= carry.flags;
+          from = cfrom;
+          f = true;
+        }
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const Run q = shfl_run_up(rr, o);
-        const bool qh = __shfl_up_sync(kFull, f, o);
-        const uint32_t qf = __shfl_up_sync(kFull, from, o);
-        if (lane >= o) {
-          if (!f) rr = run_compose(q, rr);
-          f = f || qh;
-          from = max(from, qf);
+        for (int o = 1; o < 32; o <<= 1) {
+          const long long qa = __shfl_up_sync(kFull, a, o);
+          const uint32_t qfl = __shfl_up_sync(kFull, fl, o);
+          const bool qh = __shfl_up_sync(kFull, f, o);
+          const uint32_t qf = __shfl_up_sync(kFull, from, o);
+          if (lane >= o) {
+            if (!f) {
+              a += qa;
+              fl &= qfl;
+            }
+            f = f || qh;
+            from = max(from, qf);
+          }
+        }
+        rr.inc = a;
+        rr.lo = 0;
+        rr.hi = a;
+        rr.d = 0;
+        rr.flags = fl;
+        saturate(rr);
+      } else {
+        if (lane == 0 && in && !head) {
+          rr = run_compose(carry, rr);
+          from = cfrom;
+          f = true;   // the carry stands for its head
+        }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const Run q = shfl_run_up(rr, o);
+          const bool qh = __shfl_up_sync(kFull, f, o);
+          const uint32_t qf = __shfl_up_sync(kFull, from, o);
+          if (lane >= o) {
+            if (!f) rr = run_compose(q, rr);
+            f = f || qh;
+            from = max(from, qf);
+          }
         }
       }
       // tails: the next element is a head (lane 31 decides with the next chunk)
@@ -1879,8 +1998,18 @@ __device__ __noinline__ void walk_producer(const Params &p, Smem &sm, RangeSlot 
           } else {
             const uint32_t q = (uint32_t)nraw + __popc(rb & lt);
             st.inc = (int64_t)q;
-            if (q < (uint32_t)kRangeRaw)
-              rs.rawpos[q] = el.from | (el.kind == EK_RAW2 ? 1u << 16 : 0u) | ((el.eb & 0x7FFu) << 17);
+            if (q < (uint32_t)kRangeRaw) {
+              // the row's terms, copied now: they land while the range is composed
+              const int64_t g0 = (ws.row_base + (ta + (el.from >> 9) - ws.tb) * kTileRows + (el.from & 511u)) * kLaneTerms;
+              const bool pre = x16 && g0 >= ws.g_lo && g0 + kLaneTerms <= ws.g_hi;
+              if (pre) {
+                const double *src = p.x + g0;
+#pragma unroll
+                for (int k = 0; k < kLaneTerms / 2; k++) cp_async16(&rs.raw[q][2 * k], src + 2 * k);
+              }
+              rs.rawpos[q] = el.from | (el.kind == EK_RAW2 ? 1u << 16 : 0u) | ((el.eb & 0x7FFu) << 17) |
+                             (pre ? 1u << 28 : 0u);
+            }
             st.lo = st.hi = 0;
             const uint32_t sk = el.kind == EK_RAW ? ST_RAW : (el.kind == EK_RAW2 ? ST_RAW2 : ST_X);
             st.meta = step_meta(sk, el.eb, 0, el.neg, el.from, el.to);
@@ -1896,14 +2025,20 @@ __device__ __noinline__ void walk_producer(const Params &p, Smem &sm, RangeSlot 
       cfrom = __shfl_sync(kFull, from, 31);
       cto = __shfl_sync(kFull, el.to, 31);
       pending = __shfl_sync(kFull, in && !tail, 31);
+      WR0(r, 3 + 2 * (c / 32));
     }
+    WR0(r, 30);
     over = nsteps > kRangeSteps;
     if (lane == 0 && N > 0) (void)SQ_OK(p, nsteps >= 1, 6, N);
     __syncwarp();
-    // ---- the raw rows' terms from x (all loads at once), then their prefix tables
+    // ---- the raw rows' terms (the copies issued at the tails; the rest now),
+    // then their prefix tables, two rows at a time
     const int nfetch = over ? 0 : min(nraw, kRangeRaw);
+    cp_async_wait();
     for (int w0 = lane; w0 < nfetch * kLaneTerms; w0 += 32) {
-      const uint32_t pos = rs.rawpos[w0 / kLaneTerms] & 0xFFFFu;
+      const uint32_t rp = rs.rawpos[w0 / kLaneTerms];
+      if (rp & (1u << 28)) continue;
+      const uint32_t pos = rp & 0xFFFFu;
       const int64_t gi = (ws.row_base + (ta + (pos >> 9) - ws.tb) * kTileRows + (pos & 511u)) * kLaneTerms +
                          (w0 & (kLaneTerms - 1));
       rs.raw[w0 / kLaneTerms][w0 & (kLaneTerms - 1)] =
@@ -1911,29 +2046,39 @@ __device__ __noinline__ void walk_producer(const Params &p, Smem &sm, RangeSlot 
                                           : kNegZero;
     }
     __syncwarp();
-    for (int q = 0; q < nfetch; q++) {
-      const uint32_t rp = rs.rawpos[q];
-      if (!(rp & (1u << 16))) continue;
-      // lanes 0..15 the lower binade, 16..31 the upper one
-      const int jj = lane & (kLaneTerms - 1);
-      const uint64_t t = rs.raw[q][jj];
-      const uint32_t E = (rp >> 17) + (uint32_t)(lane >> 4);
-      const uint32_t hi = (uint32_t)(t >> 32);
-      uint32_t tt;
-      uint64_t P = term_mag_halfup(hi, (uint32_t)t, 64 - (int)E, tt);
-      const uint32_t bad = __ballot_sync(kFull, tt == 0u || ((hi >> 20) & 0x7FFu) >= E);
+    WR0(r, 31);
+    for (int q0 = 0; q0 < nfetch; q0 += 2) {
+      // lanes 0..15 row q0, 16..31 row q0 + 1; both binades each
+      const int q = q0 + (lane >> 4), jj = lane & (kLaneTerms - 1);
+      const uint32_t rp = q < nfetch ? rs.rawpos[q] : 0u;
+      const bool has = (rp & (1u << 16)) != 0;
+      const uint64_t t = has ? rs.raw[q][jj] : 0ull;
+      const uint32_t E = has ? (rp >> 17) & 0x7FFu : 1023u;
+      const uint32_t hi = (uint32_t)(t >> 32), Et = (hi >> 20) & 0x7FFu;
+      uint32_t ta_, tb_;
+      uint64_t Pa = term_mag_halfup(hi, (uint32_t)t, 64 - (int)E, ta_);
+      uint64_t Pb = term_mag_halfup(hi, (uint32_t)t, 63 - (int)E, tb_);
+      const uint32_t bada = __ballot_sync(kFull, ta_ == 0u || Et >= E);
+      const uint32_t badb = __ballot_sync(kFull, tb_ == 0u || Et >= E + 1u);
 #pragma unroll
       for (int o = 1; o < kLaneTerms; o <<= 1) {
-        const uint64_t v = __shfl_up_sync(kFull, P, o, kLaneTerms);
-        if (jj >= o) P += v;
+        const uint64_t va = __shfl_up_sync(kFull, Pa, o, kLaneTerms), vb = __shfl_up_sync(kFull, Pb, o, kLaneTerms);
+        if (jj >= o) {
+          Pa += va;
+          Pb += vb;
+        }
       }
-      rs.raw[q][kLaneTerms + lane] = P;
-      if (lane == 0) {
-        const uint32_t ba = bad & 0xFFFFu, bb = bad >> 16;
-        rs.rawlim[q] = (ba ? (uint32_t)(__ffs(ba) - 1) : (uint32_t)kLaneTerms) |
-                       ((bb ? (uint32_t)(__ffs(bb) - 1) : (uint32_t)kLaneTerms) << 5);
+      if (has) {
+        rs.raw[q][kLaneTerms + jj] = Pa;
+        rs.raw[q][2 * kLaneTerms + jj] = Pb;
+        if (jj == 0) {
+          const uint32_t ma = (bada >> (lane & 16)) & 0xFFFFu, mb = (badb >> (lane & 16)) & 0xFFFFu;
+          rs.rawlim[q] = (ma ? (uint32_t)(__ffs(ma) - 1) : (uint32_t)kLaneTerms) |
+                         ((mb ? (uint32_t)(__ffs(mb) - 1) : (uint32_t)kLaneTerms) << 5);
+        }
       }
     }
+    WR0(r, 32);
     // ---- hand the slot over
     if (lane == 0) {
       rs.nsteps = over ? -1 : nsteps;
@@ -1965,14 +2110,14 @@ __device__ __noinline__ uint64_t walk_serial(const Params &p, Smem &sm, RangeSlo
     const uint64_t c1 = clock64();
     WRT(r, 2);
     if (!got || rs.fail) failed = true;
-    const int64_t ta = ws.tb + (int64_t)r * kRangeTiles;
+    const int64_t ta = ws.tb + range_start(r);
     if (got && !failed) {
       const int ns = rs.nsteps;
       if (ns < 0) {
         // the steps did not fit: the range's terms one by one
         if (lane == 0) stat_add(sm, S_RANGE_X, 1);
         int64_t a, b;
-        clip(ws, ta, 0, (uint32_t)min((int64_t)kRangeTiles, ws.te - ta) * kTileTerms, a, b);
+        clip(ws, ta, 0, (uint32_t)min(range_start(r + 1) - range_start(r), ws.te - ta) * kTileTerms, a, b);
         S = raw_from_x(p, sm, S, a, b);
       }
       for (int i = 0; i < ns; i++) {
@@ -1985,7 +2130,13 @@ __device__ __noinline__ uint64_t walk_serial(const Params &p, Smem &sm, RangeSlo
         const uint32_t from = (uint32_t)(st.meta >> 23) & 0xFFFFu, to = (uint32_t)(st.meta >> 39) & 0xFFFFu;
         if (lane == 0) (void)SQ_OK(p, from < to, 5, ((int64_t)from << 16) | to);
         bool done = false;
-        if (kind == ST_RUN) {
+        const uint64_t m0 = (S & kFracMask) | kHidden;
+        if (kind == ST_RUN && ((st.meta >> 56) & 1u) && (S >> 52) == eb && m0 + (uint64_t)st.inc <= (uint64_t)kTwo53) {
+          // a plain run on a positive S of its binade: the count grows by inc
+          S += (uint64_t)st.inc;
+          done = true;
+          nrun++;
+        } else if (kind == ST_RUN) {
           Run q;
           q.inc = st.inc;
           q.lo = st.lo;
@@ -2002,7 +2153,7 @@ __device__ __noinline__ uint64_t walk_serial(const Params &p, Smem &sm, RangeSlo
           nrun++;
         } else if ((kind == ST_RAW || kind == ST_RAW2) && st.inc < kRangeRaw) {
           const uint64_t *data = rs.raw[st.inc];
-          if (kind == ST_RAW) S = raw_chunk(sm, S, lane < kLaneTerms ? data[lane] : kNegZero, 0, kLaneTerms);
+          if (kind == ST_RAW) S = row_dadd(sm, S, lane < kLaneTerms ? data[lane] : kNegZero, 0, kLaneTerms);
           else S = raw2_row(sm, S, data, rs.rawlim[st.inc], eb, (st.meta >> 15) & 1u);
           done = true;
         }
@@ -2015,9 +2166,10 @@ __device__ __noinline__ uint64_t walk_serial(const Params &p, Smem &sm, RangeSlo
         }
 #ifdef SEQSUM_PROFILE
         if (lane == 0) {
-          // the walk's steps: kind and cycles (taken before the counter's round trip)
+          // the walk's steps: kind and cycles (one in-order warp: a plain count)
           const uint64_t cy = clock64() - t_seg;
-          const unsigned long long slot = atomicAdd(&p.dbg[4095], 1ull);
+          const unsigned long long slot = sm.prof_n++;
+          p.dbg[4095] = slot + 1;
           const uint64_t info = kind == ST_RAW2 ? (uint64_t)sm.prof_i | ((uint64_t)eb << 31) : (uint64_t)i;
           if (slot < 1000) p.dbg[4096 - 1000 - 1 + slot] = ((uint64_t)kind << 60) | ((info & 0xFFFFFFFFFFull) << 20) | (cy & 0xFFFFF);
         }
@@ -2043,7 +2195,7 @@ __device__ __noinline__ uint64_t walk_sum(const Params &p, Smem &sm, unsigned ch
                                          uint64_t Sb) {
   const int w = threadIdx.x >> 5;
   RangeSlot *slots = reinterpret_cast<RangeSlot *>(dyn);
-  const int nranges = (int)((ws.te - ws.tb + kRangeTiles - 1) / kRangeTiles);
+  const int nranges = range_count(ws.te - ws.tb);
   if (w < kWarps) {
     walk_producer(p, sm, slots[w], ws, nranges, w, sm.tag);
   } else {
@@ -2058,6 +2210,7 @@ __device__ __noinline__ uint64_t walk_sum(const Params &p, Smem &sm, unsigned ch
 
 __device__ __noinline__ void walk_loop(const Params &p, Smem &sm, unsigned char *dyn, int64_t ntiles) {
   const int tid = threadIdx.x;
+  if (tid == 0) sm.prof_n = 0;
   if (tid < kWarps) {
     mbar_init(&sm.wfull[tid], 1);
     mbar_init(&sm.wempty[tid], 1);
