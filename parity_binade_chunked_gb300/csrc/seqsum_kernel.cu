@@ -160,6 +160,13 @@ __device__ __forceinline__ void tl_mark(const Params &p, int role, int who, uint
   do {                                                                  \
     if ((threadIdx.x & 31) == 0 && (r) < 64) p.dbg[2100 + 4 * (r) + (k)] = gtimer(); \
   } while (0)
+// the scanner's phases, summed over windows (cycles, thread 0)
+#define SCP(k)                                                        \
+  do {                                                                \
+    const uint64_t n_ = clock64();                                    \
+    scp_acc[k] += n_ - scp_last;                                      \
+    scp_last = n_;                                                    \
+  } while (0)
 // the scanner's windows: globaltimer at the poll that found them, their first tile and size, when published
 #define SCW(k, v)                                                              \
   do {                                                                         \
@@ -174,6 +181,7 @@ __device__ __forceinline__ void tl_mark(const Params &p, int role, int who, uint
 #define WRT(r, k) ((void)0)
 #define WR0(r, k) ((void)0)
 #define SCW(k, v) ((void)0)
+#define SCP(k) ((void)0)
 #define TL(p, role, who, u, k) ((void)0)
 #define WPH(k) ((void)0)
 #define WPH_INIT ((void)0)
@@ -342,7 +350,9 @@ struct Geo {
   int32_t sum;
 };
 
-__device__ __forceinline__ Geo tile_geo(const Params &p, int64_t t) {
+// hint: a sum at or before the tile's (a caller that walks tiles upwards
+// keeps it; most calls then read one or two starts instead of searching).
+__device__ __forceinline__ Geo tile_geo(const Params &p, int64_t t, int *hint = nullptr) {
   Geo g;
   if (!p.offsets) {
     g.row0 = t * kTileRows;
@@ -354,11 +364,21 @@ __device__ __forceinline__ Geo tile_geo(const Params &p, int64_t t) {
   }
   // the sum k with tile_begin[k] <= t < tile_begin[k+1] (the last such k: empty sums share a start)
   int lo = 0, hi = p.nsums;   // invariant: tile_begin[lo] <= t < tile_begin[hi]
+  if (hint && *hint >= 0 && *hint < p.nsums && __ldg(&p.tile_begin[*hint]) <= t) {
+    lo = *hint;
+    int k = 0;
+    while (k < 4 && lo + 1 < hi && __ldg(&p.tile_begin[lo + 1]) <= t) {
+      lo++;
+      k++;
+    }
+    if (k < 4) hi = lo + 1;   // found by walking up; else search above
+  }
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (__ldg(&p.tile_begin[mid]) <= t) lo = mid;
     else hi = mid;
   }
+  if (hint) *hint = lo;
   const int64_t off = __ldg(&p.offsets[lo]);
   g.t_first = __ldg(&p.tile_begin[lo]);
   g.row0 = (off >> 4) + (t - g.t_first) * kTileRows;
@@ -455,7 +475,7 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 // tile's plan record (prefix and warp sums) beside it.  The stage's per-unit
 // state is cleared first; the mbarrier completion publishes it to the warps.
 __device__ __forceinline__ void stage_fill(const Params &p, Smem &sm, unsigned char *stages, const CUtensorMap *tmap,
-                                           int s, int64_t k, int64_t ntiles) {
+                                           int s, int64_t k, int64_t ntiles, int (&hint)[2]) {
   StageSm &st = sm.st[s];
   bool plan = false;
   const int64_t t = unit_of(k, ntiles, p.wave, plan);
@@ -465,7 +485,7 @@ __device__ __forceinline__ void stage_fill(const Params &p, Smem &sm, unsigned c
     mbar_arrive(&sm.full[s]);
     return;
   }
-  const Geo g = tile_geo(p, t);
+  const Geo g = tile_geo(p, t, &hint[plan ? 0 : 1]);
   st.tile = t;
   st.plan = plan ? 1 : 0;
   st.geo[0] = g.row0;
@@ -628,13 +648,145 @@ __device__ __forceinline__ void plan_unit(const Params &p, Smem &sm, UnitSm &us,
   }
 }
 
+// The last warp of a complex tile's run unit: the tile's items merged and
+// its header published (out of line: rare, and kept out of the units' loop).
+__device__ __noinline__ void complex_merge(const Params &p, Smem &sm, UnitSm &us, int64_t t, uint32_t tag) {
+  const int lane = threadIdx.x & 31;
+  // a complex tile: the warps' items in the order of their terms (a warp
+  // that is one run gives its run), consecutive runs of one binade composed,
+  // written compactly from slot 0 of the tile's item area.  The tile's item
+  // i lies at slot 32 k + j >= i (a warp has at most 32), so every write
+  // lands on a slot already read.
+  uint32_t ck = 0;
+  if (lane < kWarps) ck = us.wkey[lane] >= 0 ? 1u : us.wcnt[lane];
+  uint32_t cex = ck;
+#pragma unroll
+  for (int o = 1; o < kWarps; o <<= 1) {
+    const uint32_t q = __shfl_up_sync(kFull, cex, o);
+    if (lane >= o) cex += q;
+  }
+  const int T = (int)__shfl_sync(kFull, cex, kWarps - 1);
+  cex -= ck;
+  Rec *area = p.items + t * kItemSlots;
+  const uint32_t lt = (1u << lane) - 1u;
+  int M = 0;
+  Run carry = run_empty();                 // the open run at the end of the chunk before
+  uint32_t ckey = kNoKey, cstart = 0, cend = 0;
+  bool pending = false;
+  for (int c = 0; c < T; c += 32) {
+    const int i = c + lane;
+    const bool in = i < T;
+    // the warp whose items hold item i
+    int k = 0;
+    uint32_t kex = 0;
+#pragma unroll
+    for (int q = 0; q < kWarps; q++) {
+      const uint32_t e = __shfl_sync(kFull, cex, q), n = __shfl_sync(kFull, ck, q);
+      if (in && e <= (uint32_t)i && (uint32_t)i < e + n) {
+        k = q;
+        kex = e;
+      }
+    }
+    Item it;
+    it.r = run_empty();
+    it.kind = K_OVERFLOW;
+    it.eb = 0;
+    it.start = it.count = 0;
+    if (in) {
+      if (us.wkey[k] >= 0) {
+        it.r.inc = us.wred[k][0];
+        it.r.lo = us.wred[k][1];
+        it.r.hi = us.wred[k][2];
+        it.r.d = us.wd[k];
+        it.r.flags = us.wflags[k];
+        saturate(it.r);
+        it.kind = K_RUN;
+        it.eb = (uint32_t)us.wkey[k];
+        it.count = 32 * kLaneTerms;
+        it.start = (uint32_t)k * 32 * kLaneTerms;
+      } else {
+        it = unpack_item(ld_rec_vol(&area[k * kWarpSlots + (i - (int)kex)]));
+      }
+    }
+    const uint32_t key = (in && it.kind == K_RUN) ? it.eb : kNoKey;
+    uint32_t pkey = __shfl_up_sync(kFull, key, 1);
+    if (lane == 0) pkey = ckey;
+    const bool head = in && (i == 0 || key == kNoKey || pkey == kNoKey || key != pkey);
+    // the open run of the chunk before ends if this chunk begins with a head
+    const bool close_prev = __shfl_sync(kFull, head, 0) && pending;
+    Run rr = it.r;
+    bool f = head;
+    uint32_t from = head ? it.start : 0u;
+    if (lane == 0 && in && !head) {
+      rr = run_compose(carry, rr);
+      from = cstart;
+      f = true;
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const Run q = shfl_run_up(rr, o);
+      const bool qh = __shfl_up_sync(kFull, f, o);
+      const uint32_t qf = __shfl_up_sync(kFull, from, o);
+      if (lane >= o) {
+        if (!f) rr = run_compose(q, rr);
+        f = f || qh;
+        from = max(from, qf);
+      }
+    }
+    const uint32_t nkey = __shfl_down_sync(kFull, key, 1);
+    const bool tail = in && (key == kNoKey || i == T - 1 || (lane < 31 && (nkey == kNoKey || nkey != key)));
+    const uint32_t tb = __ballot_sync(kFull, tail);
+    __syncwarp();   // every read of the chunk before any write
+    if (close_prev) {
+      if (lane == 0 && SQ_OK(p, M < c, 2, M)) {
+        Item m;
+        m.r = carry;
+        saturate(m.r);
+        m.kind = K_RUN;
+        m.eb = ckey;
+        m.start = cstart;
+        m.count = cend - cstart;
+        st_rec(&area[M], pack_item(m, 0));
+      }
+      M++;
+    }
+    if (tail) {
+      Item m = it;
+      if (it.kind == K_RUN) {
+        m.r = rr;
+        saturate(m.r);
+        m.start = from;
+        m.count = it.start + it.count - from;
+      }
+      const int at = M + __popc(tb & lt);
+      if (SQ_OK(p, at <= i && at < kItemSlots, 2, at)) st_rec(&area[at], pack_item(m, 0));
+    }
+    M += __popc(tb);
+    carry = shfl_run_idx(rr, 31);
+    ckey = __shfl_sync(kFull, key, 31);
+    cstart = __shfl_sync(kFull, from, 31);
+    cend = __shfl_sync(kFull, it.start + it.count, 31);
+    pending = __shfl_sync(kFull, in && !tail, 31);
+  }
+  __threadfence();   // the items before the header that publishes them
+  if (lane == 0) {
+    Rec q;
+    q.w[0] = ((uint64_t)M & kPay56) | ((uint64_t)tag << 56);
+    q.w[1] = (uint64_t)tag << 56;
+    q.w[2] = (uint64_t)tag << 56;
+    q.w[3] = pack_meta(K_COMPLEX, 0, 0, 0, 0, 0) | ((uint64_t)tag << 56);
+    stat_add(sm, S_TILE_COMPLEX, 1);
+    if (!(p.fault_mode == 1 && t == p.fault_arg)) st_rec_vol(&p.hdr[t], q);
+  }
+}
+
 // A run unit, one warp's 32 rows (already loaded): each row's binade from
 // its prefix range, the rows' runs and the warp's record; the last warp
 // publishes the tile's header.  pf is the tile's prefix as the copy brought
 // it, bs/ba the sums of the warps before this one.
 __device__ __forceinline__ void run_unit(const Params &p, Smem &sm, UnitSm &us, int64_t t, const Geo &g,
-                                         const uint64_t (&v)[kLaneTerms], uint4 pf, float bs, float ba,
-                                         uint32_t tag) {
+                                         const uint64_t (&v)[kLaneTerms], uint4 pf, float bs, float ba, float wfs,
+                                         float wfa, uint32_t tag) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, tid = threadIdx.x;
   if (!((pf.w >> 8) == tag && (pf.w & 3u) == 2u)) {
     // the scanner had not published the prefix when the copy ran: poll it
@@ -664,28 +816,39 @@ __device__ __forceinline__ void run_unit(const Params &p, Smem &sm, UnitSm &us, 
     pf.y = __shfl_sync(kFull, pf.y, 0);
     pf.z = __shfl_sync(kFull, pf.z, 0);
     if (!ok) pf = make_uint4(0, 0, 0, 0);   // the plan only: a prefix taken as 0
-    fence_acq_rel();
-    // the warps' sums, read again after the prefix
-    bs = ba = 0.0f;
-    if (lane < kWarps) {
-      const float *ws = reinterpret_cast<const float *>(&p.prec[t * kPrecWords + 1]);
-      const float a = lane < w ? ws[lane] : 0.0f, b = lane < w ? ws[kWarps + lane] : 0.0f;
-      bs = a;
-      ba = b;
-    }
-#pragma unroll
-    for (int o = 4; o > 0; o >>= 1) {
-      bs = __fadd_rn(bs, __shfl_xor_sync(kFull, bs, o));
-      ba = __fadd_rn(ba, __shfl_xor_sync(kFull, ba, o));
-    }
-    bs = __shfl_sync(kFull, bs, 0);
-    ba = __shfl_sync(kFull, ba, 0);
+    // (the warps' sums came with the copy: a stale copy can make the plan
+    // worse, never the result)
   }
   const uint64_t c0 = clock64();
   const DF ex = DF{__uint_as_float(pf.x), __uint_as_float(pf.y)};
   const float ex_abs = __uint_as_float(pf.z);
-  float fs, fa;
-  uint32_t mx;
+  // the warp's range -- its prefix and its own plan sums, with the allowance
+  // -- inside one binade: every row's range is inside it too, and the rows'
+  // own sums are not needed
+  int fbw = 0;
+  if (p.plan_mode == 0) {
+    const float P0 = __fadd_rn(ex.hi, __fadd_rn(ex.lo, bs));
+    const float Aw = __fadd_rn(__fadd_rn(ex_abs, ba), wfa);
+    const float mw = __fadd_rn(__fmul_rn(Aw, 4.76837158203125e-7f /* 2^-21 */), 1e-30f);
+    const float posw = __fmul_rn(0.5f, __fadd_rn(wfa, wfs)), negw = __fmul_rn(0.5f, __fsub_rn(wfa, wfs));
+    const float low = __fsub_rn(__fsub_rn(P0, negw), mw), hiw = __fadd_rn(__fadd_rn(P0, posw), mw);
+    if (low > 0.0f) {
+      const int a = float_binade(low), b = float_binade(hiw);
+      if (a == b && a >= 1 && a <= 254) fbw = a;
+    } else if (hiw < 0.0f) {
+      const int a = float_binade(-hiw), b = float_binade(-low);
+      if (a == b && a >= 1 && a <= 254) fbw = a;
+    }
+  }
+  float fs = 0.0f, fa = 0.0f, lo_ = 0.0f, hi_ = 0.0f;
+  uint32_t mx = 0, eb = 0;
+  bool zero = false, allneg = false;
+  if (fbw) {
+    // (a row of zeros is then a run of zero increments: S is not zero there)
+#pragma unroll
+    for (int j = 0; j < kLaneTerms; j++) mx = max(mx, (uint32_t)(v[j] >> 32));
+    eb = (uint32_t)(fbw - 127 + 1023);
+  } else {
   row_sums(v, fs, fa, mx);
   float is = fs, ia = fa;
 #pragma unroll
@@ -706,7 +869,8 @@ __device__ __forceinline__ void run_unit(const Params &p, Smem &sm, UnitSm &us, 
   const float A = __fadd_rn(__fadd_rn(ex_abs, xa), fa);
   const float marg = __fadd_rn(__fmul_rn(A, 4.76837158203125e-7f /* 2^-21 */), 1e-30f);
   const float pos = __fmul_rn(0.5f, __fadd_rn(fa, fs)), neg = __fmul_rn(0.5f, __fsub_rn(fa, fs));
-  const float lo_ = __fsub_rn(__fsub_rn(Pf, neg), marg), hi_ = __fadd_rn(__fadd_rn(Pf, pos), marg);
+  lo_ = __fsub_rn(__fsub_rn(Pf, neg), marg);
+  hi_ = __fadd_rn(__fadd_rn(Pf, pos), marg);
   int fb = 0;   // float biased exponent of the binade, 0: the row's range is not inside one binade
   if (lo_ > 0.0f) {
     const int a = float_binade(lo_), b = float_binade(hi_);
@@ -715,7 +879,7 @@ __device__ __forceinline__ void run_unit(const Params &p, Smem &sm, UnitSm &us, 
     const int a = float_binade(-hi_), b = float_binade(-lo_);
     if (a == b && a >= 1 && a <= 254) fb = a;
   }
-  uint32_t eb = fb ? (uint32_t)(fb - 127 + 1023) : 0u;   // double biased exponent
+  eb = fb ? (uint32_t)(fb - 127 + 1023) : 0u;   // double biased exponent
   // forced plans (tests): the walk must still give the loop's bits
   if (p.plan_mode) {
     const uint32_t h = hash3((uint64_t)t, (uint32_t)tid);
@@ -726,7 +890,6 @@ __device__ __forceinline__ void run_unit(const Params &p, Smem &sm, UnitSm &us, 
     else if (p.plan_mode == 5 && eb) eb = eb + (h % 3u) - 1u;
   }
   // exact zero rows: a no-op on any non-zero sum, the sign rule on a zero one
-  bool zero = false, allneg = false;
   if (fa == 0.0f) {
     uint64_t o = 0, a = kNegZero;
 #pragma unroll
@@ -736,6 +899,7 @@ __device__ __forceinline__ void run_unit(const Params &p, Smem &sm, UnitSm &us, 
     }
     zero = (o == 0);
     allneg = (a != 0);
+  }
   }
   const bool raw = !zero && (eb == 0 || p.plan_mode == 4);
   const bool runrow = !zero && !raw;
@@ -967,132 +1131,7 @@ __device__ __forceinline__ void run_unit(const Params &p, Smem &sm, UnitSm &us, 
       if (!(p.fault_mode == 1 && t == p.fault_arg)) st_rec_vol(&p.hdr[t], pack_item(h, tag));
     }
   } else {
-    // a complex tile: the warps' items in the order of their terms (a warp
-    // that is one run gives its run), consecutive runs of one binade composed,
-    // written compactly from slot 0 of the tile's item area.  The tile's item
-    // i lies at slot 32 k + j >= i (a warp has at most 32), so every write
-    // lands on a slot already read.
-    uint32_t ck = 0;
-    if (lane < kWarps) ck = us.wkey[lane] >= 0 ? 1u : us.wcnt[lane];
-    uint32_t cex = ck;
-#pragma unroll
-    for (int o = 1; o < kWarps; o <<= 1) {
-      const uint32_t q = __shfl_up_sync(kFull, cex, o);
-      if (lane >= o) cex += q;
-    }
-    const int T = (int)__shfl_sync(kFull, cex, kWarps - 1);
-    cex -= ck;
-    Rec *area = p.items + t * kItemSlots;
-    const uint32_t lt = (1u << lane) - 1u;
-    int M = 0;
-    Run carry = run_empty();                 // the open run at the end of the chunk before
-    uint32_t ckey = kNoKey, cstart = 0, cend = 0;
-    bool pending = false;
-    for (int c = 0; c < T; c += 32) {
-      const int i = c + lane;
-      const bool in = i < T;
-      // the warp whose items hold item i
-      int k = 0;
-      uint32_t kex = 0;
-#pragma unroll
-      for (int q = 0; q < kWarps; q++) {
-        const uint32_t e = __shfl_sync(kFull, cex, q), n = __shfl_sync(kFull, ck, q);
-        if (in && e <= (uint32_t)i && (uint32_t)i < e + n) {
-          k = q;
-          kex = e;
-        }
-      }
-      Item it;
-      it.r = run_empty();
-      it.kind = K_OVERFLOW;
-      it.eb = 0;
-      it.start = it.count = 0;
-      if (in) {
-        if (us.wkey[k] >= 0) {
-          it.r.inc = us.wred[k][0];
-          it.r.lo = us.wred[k][1];
-          it.r.hi = us.wred[k][2];
-          it.r.d = us.wd[k];
-          it.r.flags = us.wflags[k];
-          saturate(it.r);
-          it.kind = K_RUN;
-          it.eb = (uint32_t)us.wkey[k];
-          it.count = 32 * kLaneTerms;
-          it.start = (uint32_t)k * 32 * kLaneTerms;
-        } else {
-          it = unpack_item(ld_rec_vol(&area[k * kWarpSlots + (i - (int)kex)]));
-        }
-      }
-      const uint32_t key = (in && it.kind == K_RUN) ? it.eb : kNoKey;
-      uint32_t pkey = __shfl_up_sync(kFull, key, 1);
-      if (lane == 0) pkey = ckey;
-      const bool head = in && (i == 0 || key == kNoKey || pkey == kNoKey || key != pkey);
-      // the open run of the chunk before ends if this chunk begins with a head
-      const bool close_prev = __shfl_sync(kFull, head, 0) && pending;
-      Run rr = it.r;
-      bool f = head;
-      uint32_t from = head ? it.start : 0u;
-      if (lane == 0 && in && !head) {
-        rr = run_compose(carry, rr);
-        from = cstart;
-        f = true;
-      }
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const Run q = shfl_run_up(rr, o);
-        const bool qh = __shfl_up_sync(kFull, f, o);
-        const uint32_t qf = __shfl_up_sync(kFull, from, o);
-        if (lane >= o) {
-          if (!f) rr = run_compose(q, rr);
-          f = f || qh;
-          from = max(from, qf);
-        }
-      }
-      const uint32_t nkey = __shfl_down_sync(kFull, key, 1);
-      const bool tail = in && (key == kNoKey || i == T - 1 || (lane < 31 && (nkey == kNoKey || nkey != key)));
-      const uint32_t tb = __ballot_sync(kFull, tail);
-      __syncwarp();   // every read of the chunk before any write
-      if (close_prev) {
-        if (lane == 0 && SQ_OK(p, M < c, 2, M)) {
-          Item m;
-          m.r = carry;
-          saturate(m.r);
-          m.kind = K_RUN;
-          m.eb = ckey;
-          m.start = cstart;
-          m.count = cend - cstart;
-          st_rec(&area[M], pack_item(m, 0));
-        }
-        M++;
-      }
-      if (tail) {
-        Item m = it;
-        if (it.kind == K_RUN) {
-          m.r = rr;
-          saturate(m.r);
-          m.start = from;
-          m.count = it.start + it.count - from;
-        }
-        const int at = M + __popc(tb & lt);
-        if (SQ_OK(p, at <= i && at < kItemSlots, 2, at)) st_rec(&area[at], pack_item(m, 0));
-      }
-      M += __popc(tb);
-      carry = shfl_run_idx(rr, 31);
-      ckey = __shfl_sync(kFull, key, 31);
-      cstart = __shfl_sync(kFull, from, 31);
-      cend = __shfl_sync(kFull, it.start + it.count, 31);
-      pending = __shfl_sync(kFull, in && !tail, 31);
-    }
-    __threadfence();   // the items before the header that publishes them
-    if (lane == 0) {
-      Rec q;
-      q.w[0] = ((uint64_t)M & kPay56) | ((uint64_t)tag << 56);
-      q.w[1] = (uint64_t)tag << 56;
-      q.w[2] = (uint64_t)tag << 56;
-      q.w[3] = pack_meta(K_COMPLEX, 0, 0, 0, 0, 0) | ((uint64_t)tag << 56);
-      stat_add(sm, S_TILE_COMPLEX, 1);
-      if (!(p.fault_mode == 1 && t == p.fault_arg)) st_rec_vol(&p.hdr[t], q);
-    }
+    complex_merge(p, sm, us, t, tag);
   }
   if (lane == 0) {
     stat_add(sm, S_TILES, 1);
@@ -1120,7 +1159,7 @@ __device__ __noinline__ void compute_warp(const Params &p, Smem &sm, const unsig
     uint64_t v[kLaneTerms];
     load_row(p, stages + s * kStageBytes, landed && st.tma && row < p.tma_rows, row, g, v);
     uint4 pf = make_uint4(0, 0, 0, 0);
-    float bs = 0.0f, ba = 0.0f;
+    float bs = 0.0f, ba = 0.0f, wfs = 0.0f, wfa = 0.0f;
     if (!plan && landed) {
       pf = st.prec[0];
       const float *ws = reinterpret_cast<const float *>(&st.prec[1]);
@@ -1128,6 +1167,8 @@ __device__ __noinline__ void compute_warp(const Params &p, Smem &sm, const unsig
         bs = __fadd_rn(bs, ws[k]);
         ba = __fadd_rn(ba, ws[kWarps + k]);
       }
+      wfs = ws[w];
+      wfa = ws[kWarps + w];
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[s]);   // this warp is done with the stage
@@ -1138,7 +1179,7 @@ __device__ __noinline__ void compute_warp(const Params &p, Smem &sm, const unsig
       plan_unit(p, sm, us, t, v, tag);
       if (lane == 0) stat_add(sm, S_CY_PLAN, clock64() - c0);
     } else {
-      run_unit(p, sm, us, t, g, v, pf, bs, ba, tag);
+      run_unit(p, sm, us, t, g, v, pf, bs, ba, wfs, wfa, tag);
     }
     if (w == 0 && lane == 0) TL(p, sm.role, 0, u, 3);
     if (w == 0 && lane == 0) TL(p, sm.role, 0, u, 4 - (plan ? 0 : 0));
@@ -1158,6 +1199,7 @@ __device__ __noinline__ void producer_warp(const Params &p, Smem &sm, unsigned c
   const bool deep = units > 2 * nstream;
   const uint32_t depth = deep ? (uint32_t)kStages : 1u;
   int64_t hand = -1;
+  int hint[2] = {0, 0};   // the sums of the last plan and run tiles (they only grow)
   for (uint32_t u = 0;; u++) {
     const int s = (int)(u % kStages);
     TL(p, sm.role, 1, u, 0);
@@ -1183,8 +1225,23 @@ __device__ __noinline__ void producer_warp(const Params &p, Smem &sm, unsigned c
     int64_t k = hand >= 0 ? hand : (int64_t)atomicAdd(&p.ctr[C_TICKET], 1u);
     const bool valid = k < units && !sm.broken;
     TL(p, sm.role, 1, u, 2);
+    if (valid) {
+      // a run unit's copy waits for the scanner to publish its tile's prefix
+      // (bounded; past the limit the compute warps poll for it themselves)
+      bool plan = false;
+      const int64_t t = unit_of(k, ntiles, p.wave, plan);
+      if (!plan && t >= 0) {
+        const uint32_t want = (sm.tag << 8) | 2u;
+        const uint64_t t0 = gtimer();
+        for (uint32_t spin = 0; ld_relaxed_u32(&p.prec[t * kPrecWords].w) != want; spin++) {
+          if ((spin & 15u) == 15u && gtimer() - t0 > p.wait_ns) break;
+          __nanosleep(100);
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");   // the copy reads what the load saw
+      }
+    }
     sm.us[u % kUnitSlots].done_cnt = 0;
-    stage_fill(p, sm, stages, tmap, s, valid ? k : -1, ntiles);
+    stage_fill(p, sm, stages, tmap, s, valid ? k : -1, ntiles, hint);
     TL(p, sm.role, 1, u, 3);
 #ifdef SEQSUM_PROFILE
     if (sm.role - p.nwalkers - 1 >= 0 && sm.role - p.nwalkers - 1 < 4 && u < 96)
@@ -1220,6 +1277,9 @@ __device__ __noinline__ void stream_cta(const Params &p, Smem &sm, unsigned char
 // One CTA turns the tiles' sums into every tile's exclusive prefix, in order
 // (the first tile of a sum starts from s0), a window of up to 1024 tiles at a
 // time as the plan units publish them (double-float sums).
+// A sum's start value as a double-float (the start of its first tile's prefix).
+__device__ __noinline__ DF start_df(const Params &p, int32_t sum) { return df_of_double(p.offsets ? p.s0s[sum] : p.s0); }
+
 __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const uint32_t tag = sm.tag;
@@ -1232,9 +1292,19 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
   int64_t pos = 0;
   uint64_t t_wait = 0;
   int nwin = 0;
+  // this thread's four consecutive tiles of the window: the window's statuses
+  // are loaded while the window before it is scanned
+  uint4 vn[4];
+#pragma unroll
+  for (int j = 0; j < 4; j++) vn[j] = (4 * tid + j < ntiles) ? ld_vol_v4(&p.status[4 * tid + j]) : make_uint4(0, 0, 0, 0);
+  int hint = 0;   // the sum of this thread's last tile (its tiles only grow)
+#ifdef SEQSUM_PROFILE
+  uint64_t scp_last = clock64();
+  uint64_t scp_acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#endif
   while (pos < ntiles) {
-    // this thread's four consecutive tiles of the window
     const uint64_t t_poll = gtimer();
+    SCP(0);
     const int64_t t0 = pos + 4 * tid;
     uint4 v[4];
     bool rd[4];
@@ -1243,12 +1313,8 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
 #pragma unroll
     for (int j = 0; j < 4; j++) {
       const int64_t t = t0 + j;
-      rd[j] = false;
-      v[j] = make_uint4(0, 0, 0, 0);
-      if (t < ntiles) {
-        v[j] = ld_vol_v4(&p.status[t]);
-        rd[j] = (v[j].w >> 8) == tag && (v[j].w & 3u) == 1u;
-      }
+      v[j] = vn[j];
+      rd[j] = t < ntiles && (v[j].w >> 8) == tag && (v[j].w & 3u) == 1u;
     }
     int my_first = kScanTiles;
 #pragma unroll
@@ -1257,6 +1323,7 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
     if (my_first < kScanTiles) atomicMin(&s_ready, my_first);
     __syncthreads();
     const int nready = (int)min((int64_t)s_ready, ntiles - pos);
+    SCP(1);
     if (nready == 0) {
       // nothing new yet: thread 0 decides for the CTA whether to keep waiting
       if (tid == 0) {
@@ -1271,9 +1338,17 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
       __syncthreads();
       if (s_giveup) break;
       __nanosleep(128);
+#pragma unroll
+      for (int j = 0; j < 4; j++) vn[j] = (t0 + j < ntiles) ? ld_vol_v4(&p.status[t0 + j]) : make_uint4(0, 0, 0, 0);
       continue;
     }
     t_wait = 0;
+    {
+      // the next window's statuses, in flight while this one is scanned
+      const int64_t tn0 = pos + nready + 4 * tid;
+#pragma unroll
+      for (int j = 0; j < 4; j++) vn[j] = (tn0 + j < ntiles) ? ld_vol_v4(&p.status[tn0 + j]) : make_uint4(0, 0, 0, 0);
+    }
     SCW(0, t_poll);
     SCW(1, (uint64_t)pos);
     SCW(2, (uint64_t)nready);
@@ -1294,10 +1369,10 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
       if (4 * tid + j < nready) {
         const DF a = DF{__uint_as_float(v[j].x), __uint_as_float(v[j].y)};
         const float aa = __uint_as_float(v[j].z);
-        const Geo g = tile_geo(p, t);
+        const Geo g = tile_geo(p, t, &hint);
         if (t == g.t_first) {
           head[j] = true;
-          s0d[j] = df_of_double(p.offsets ? p.s0s[g.sum] : p.s0);
+          s0d[j] = start_df(p, g.sum);
           acc = df_add(s0d[j], a);
           acca = __fadd_rn(fabsf(s0d[j].hi), aa);
           seen = true;
@@ -1310,6 +1385,7 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
       loca[j] = acca;
       hup[j] = seen;
     }
+    SCP(2);
     // segmented scan of the threads' totals across the warp ...
     DF x = acc;
     float xa = acca;
@@ -1329,7 +1405,7 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
         hx = hx || hy;
       }
     }
-    if (lane == 31) {
+    if (lane == 31 && w < kWarps) {   // (the ninth warp holds no tiles)
       s_wtot[w] = x;
       s_wabs[w] = xa;
       s_whead[w] = hx;
@@ -1340,6 +1416,7 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
     const float xla = __shfl_up_sync(kFull, xa, 1);
     const bool hl = __shfl_up_sync(kFull, hx, 1);
     __syncthreads();
+    SCP(3);
     // ... and across the warps, after the carry of the earlier windows:
     // `before` is the inclusive prefix just before this thread's first tile
     DF before = carry;
@@ -1362,6 +1439,7 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
         before_a = __fadd_rn(before_a, xla);
       }
     }
+    SCP(4);
     // each tile's exclusive prefix: its s0 at a sum start, else the inclusive
     // prefix of the tile before it
 #pragma unroll
@@ -1386,6 +1464,7 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
                                                              __float_as_uint(ea), (tag << 8) | 2u));
       }
     }
+    SCP(5);
     // the carry into the next window: the inclusive prefix of its last tile
     __syncthreads();
     {
@@ -1401,9 +1480,14 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
     __syncthreads();
     if (tid == 0) stat_add(sm, S_SCAN_WINDOWS, 1);
     SCW(3, gtimer());
+    SCP(6);
     nwin++;
     pos += nready;
   }
+#ifdef SEQSUM_PROFILE
+  if (tid == 0)
+    for (int k = 0; k < 7; k++) p.dbg[2400 + 4 * 40 + k] = scp_acc[k];
+#endif
 }
 
 // ------------------------------------------------------------------ the walk: raw terms
@@ -2279,7 +2363,14 @@ __global__ void __launch_bounds__(kBlockThreads, 2) seqsum_kernel(const Params p
       }
       sm.alone = ws == smid + 1 || ss == smid + 1;
       if (sm.alone) sm.stat[kWarps][S_ALONE] += 1;
+#ifdef SEQSUM_PROFILE
+      if (sm.alone) p.dbg[2392 + (ws == smid + 1 ? 0 : 1)] = smid + 1;
+#endif
     }
+#ifdef SEQSUM_PROFILE
+    if (sm.role == 0) p.dbg[2390] = smid + 1;
+    if (sm.role == p.nwalkers) p.dbg[2391] = smid + 1;
+#endif
     const uint32_t e = ld_relaxed_u32(&p.ctr[C_EPOCH]);
     sm.tag = e == 0 ? 1u : e;
     sm.ntiles = p.offsets ? (int64_t)ld_relaxed_u32(&p.ctr[C_NTILES]) : p.ntiles;
