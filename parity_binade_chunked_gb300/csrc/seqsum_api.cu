@@ -129,9 +129,9 @@ int ensure_device_info() {
   if (g_blocks_per_sm == 0) g_blocks_per_sm = sq::kernel_blocks_per_sm();
   if (g_wave == 0) {
     // far enough ahead that the scanner has published a tile's prefix when
-    // its run unit starts, near enough that the tile is still in L2 (1024
-    // tiles = 32 MB of the 129 MB)
-    g_wave = 1024;
+    // its run unit starts, near enough that the tile is still in L2 (2048
+    // tiles = 64 MB of the 129 MB)
+    g_wave = 2048;
     const char *ev = getenv("SEQSUM_WAVE");
     if (ev && atoll(ev) > 0) g_wave = atoll(ev);
   }
