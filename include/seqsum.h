@@ -142,8 +142,9 @@ typedef struct {
   int32_t check_site;        /* self-checking builds: first failed check (0: none) */
   int32_t check_pad;
   int64_t check_value;       /* self-checking builds: the value that failed it */
-  int32_t timeout_site;      /* first bounded device wait that gave up (0: none): 1 plan look-back, 2 TMA copy,
-                                3 walk header */
+  int32_t timeout_site;      /* first bounded device wait that gave up (0: none): 2 a stage's copy, 3 a walk
+                                range's tile headers, 5 a run unit's prefix, 6 the scanner's tile sums, 7 a
+                                stage's release */
   int32_t timeout_pad;
   int64_t timeout_a;         /* its context: the tile */
   int64_t timeout_b;
