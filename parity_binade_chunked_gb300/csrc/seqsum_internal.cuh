@@ -50,7 +50,6 @@ enum : uint32_t {
 };
 
 constexpr int kPrecWords = 5;     // a tile's plan record: its exclusive prefix, then its warps' float sums (5 x 16 B)
-constexpr int kScanTiles = 4 * kThreads;   // tiles the scanner takes per window
 
 // ---- counters in the workspace (32-bit words)
 enum : int {

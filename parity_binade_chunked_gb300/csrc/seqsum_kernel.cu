@@ -605,11 +605,14 @@ __device__ __forceinline__ void row_sums(const uint64_t (&v)[kLaneTerms], float 
   }
 }
 
+// A sum's start value as a double-float (the start of its first tile's prefix).
+__device__ __noinline__ DF start_df(const Params &p, int32_t sum) { return df_of_double(p.offsets ? p.s0s[sum] : p.s0); }
+
 // A plan unit, one warp's 32 rows (already loaded): the warp's float sums;
 // the last warp publishes the warps' sums beside the tile's prefix, and the
 // tile's sums for the scanner.  (No fence orders the two: they only steer
 // the plan, which cannot make a result wrong.)
-__device__ __forceinline__ void plan_unit(const Params &p, Smem &sm, UnitSm &us, int64_t t,
+__device__ __forceinline__ void plan_unit(const Params &p, Smem &sm, UnitSm &us, int64_t t, const Geo &g,
                                           const uint64_t (&v)[kLaneTerms], uint32_t tag) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   float fs, fa;
@@ -643,8 +646,19 @@ __device__ __forceinline__ void plan_unit(const Params &p, Smem &sm, UnitSm &us,
       agg = df_add(agg, DF{us.wfs[k], 0.0f});
       agg_abs = __fadd_rn(agg_abs, us.wfa[k]);
     }
+    uint32_t head = 0;
+    if (t == g.t_first) {
+      // a sum's first tile: its prefix is the sum's start value (published
+      // here), and the sum it gives the scanner starts from it (flag 4)
+      const DF s0 = start_df(p, g.sum);
+      st_vol_v4(&p.prec[t * kPrecWords], make_uint4(__float_as_uint(s0.hi), __float_as_uint(s0.lo),
+                                                    __float_as_uint(fabsf(s0.hi)), (tag << 8) | 2u));
+      agg = df_add(s0, agg);
+      agg_abs = __fadd_rn(fabsf(s0.hi), agg_abs);
+      head = 4u;
+    }
     st_vol_v4(&p.status[t], make_uint4(__float_as_uint(agg.hi), __float_as_uint(agg.lo), __float_as_uint(agg_abs),
-                                       (tag << 8) | 1u));
+                                       (tag << 8) | 1u | head));
   }
 }
 
@@ -1176,7 +1190,7 @@ __device__ __noinline__ void compute_warp(const Params &p, Smem &sm, const unsig
     UnitSm &us = sm.us[u % kUnitSlots];
     if (plan) {
       const uint64_t c0 = clock64();
-      plan_unit(p, sm, us, t, v, tag);
+      plan_unit(p, sm, us, t, g, v, tag);
       if (lane == 0) stat_add(sm, S_CY_PLAN, clock64() - c0);
     } else {
       run_unit(p, sm, us, t, g, v, pf, bs, ba, wfs, wfa, tag);
@@ -1273,108 +1287,81 @@ __device__ __noinline__ void stream_cta(const Params &p, Smem &sm, unsigned char
   if (tid == 0) sm.t_stream_end = gtimer();   // this CTA's last header is published
 }
 
-// ------------------------------------------------------------------ the scanner
-// One CTA turns the tiles' sums into every tile's exclusive prefix, in order
-// (the first tile of a sum starts from s0), a window of up to 1024 tiles at a
-// time as the plan units publish them (double-float sums).
-// A sum's start value as a double-float (the start of its first tile's prefix).
-__device__ __noinline__ DF start_df(const Params &p, int32_t sum) { return df_of_double(p.offsets ? p.s0s[sum] : p.s0); }
-
+// The scanner: the tiles' sums, in order as their plan units publish them,
+// into each tile's exclusive prefix (double-float; a sum's first tile starts
+// from the sum's start value, which its plan unit has added and published).
+// One warp, no barriers: 256 tiles a round (eight consecutive ones a lane,
+// summed in the lane, then a warp scan), the next round's sums loading while
+// this one is scanned.  The round takes the tiles published so far, up to the
+// first that is not.
 __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
   const uint32_t tag = sm.tag;
-  __shared__ DF s_wtot[kWarps];
-  __shared__ float s_wabs[kWarps];
-  __shared__ int s_whead[kWarps];
-  __shared__ int s_ready, s_giveup;
-  DF carry = DF{0.0f, 0.0f};
+  constexpr int kPer = 8, kRound = 32 * kPer;
+  DF carry = DF{0.0f, 0.0f};   // the inclusive prefix of the tile before pos
   float carry_abs = 0.0f;
   int64_t pos = 0;
   uint64_t t_wait = 0;
-  int nwin = 0;
-  // this thread's four consecutive tiles of the window: the window's statuses
-  // are loaded while the window before it is scanned
-  uint4 vn[4];
+  uint4 vn[kPer];
 #pragma unroll
-  for (int j = 0; j < 4; j++) vn[j] = (4 * tid + j < ntiles) ? ld_vol_v4(&p.status[4 * tid + j]) : make_uint4(0, 0, 0, 0);
-  int hint = 0;   // the sum of this thread's last tile (its tiles only grow)
-#ifdef SEQSUM_PROFILE
-  uint64_t scp_last = clock64();
-  uint64_t scp_acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-#endif
+  for (int j = 0; j < kPer; j++)
+    vn[j] = (kPer * lane + j < ntiles) ? ld_vol_v4(&p.status[kPer * lane + j]) : make_uint4(0, 0, 0, 0);
   while (pos < ntiles) {
-    const uint64_t t_poll = gtimer();
-    SCP(0);
-    const int64_t t0 = pos + 4 * tid;
-    uint4 v[4];
-    bool rd[4];
-    if (tid == 0) s_ready = kScanTiles;
-    __syncthreads();
+    const int64_t t0 = pos + kPer * lane;
+    uint4 v[kPer];
+    int my_first = kRound;
 #pragma unroll
-    for (int j = 0; j < 4; j++) {
-      const int64_t t = t0 + j;
+    for (int j = kPer - 1; j >= 0; j--) {
       v[j] = vn[j];
-      rd[j] = t < ntiles && (v[j].w >> 8) == tag && (v[j].w & 3u) == 1u;
+      const bool rd = (v[j].w >> 8) == tag && (v[j].w & 3u) == 1u;
+      if (t0 + j < ntiles && !rd) my_first = kPer * lane + j;
     }
-    int my_first = kScanTiles;
-#pragma unroll
-    for (int j = 3; j >= 0; j--)
-      if (t0 + j < ntiles && !rd[j]) my_first = 4 * tid + j;
-    if (my_first < kScanTiles) atomicMin(&s_ready, my_first);
-    __syncthreads();
-    const int nready = (int)min((int64_t)s_ready, ntiles - pos);
-    SCP(1);
+    const int nready = (int)min((int64_t)__reduce_min_sync(kFull, (uint32_t)my_first), ntiles - pos);
     if (nready == 0) {
-      // nothing new yet: thread 0 decides for the CTA whether to keep waiting
-      if (tid == 0) {
+      // nothing new yet (bounded: past the limit the run units give up on their prefixes too)
+      int giveup = 0;
+      if (lane == 0) {
         stat_add(sm, S_SCAN_POLLS, 1);
-        s_giveup = 0;
         if (!t_wait) t_wait = gtimer();
         else if (gtimer() - t_wait > p.wait_ns) {
           note_timeout(p, ERR_PLAN_TIMEOUT, 6, (uint32_t)pos, 0);
-          s_giveup = 1;   // the run units will give up waiting too (their plans only)
+          giveup = 1;
         }
       }
-      __syncthreads();
-      if (s_giveup) break;
+      if (__shfl_sync(kFull, giveup, 0)) break;
       __nanosleep(128);
 #pragma unroll
-      for (int j = 0; j < 4; j++) vn[j] = (t0 + j < ntiles) ? ld_vol_v4(&p.status[t0 + j]) : make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < kPer; j++)
+        vn[j] = (t0 + j < ntiles) ? ld_vol_v4(&p.status[t0 + j]) : make_uint4(0, 0, 0, 0);
       continue;
     }
     t_wait = 0;
     {
-      // the next window's statuses, in flight while this one is scanned
-      const int64_t tn0 = pos + nready + 4 * tid;
+      // the next round's sums, in flight while this one is scanned
+      const int64_t tn0 = pos + nready + kPer * lane;
 #pragma unroll
-      for (int j = 0; j < 4; j++) vn[j] = (tn0 + j < ntiles) ? ld_vol_v4(&p.status[tn0 + j]) : make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < kPer; j++)
+        vn[j] = (tn0 + j < ntiles) ? ld_vol_v4(&p.status[tn0 + j]) : make_uint4(0, 0, 0, 0);
     }
-    SCW(0, t_poll);
-    SCW(1, (uint64_t)pos);
-    SCW(2, (uint64_t)nready);
-    // This thread's tiles, in order: loc[j] is the inclusive sum from the
-    // thread's first tile (or from the last sum start among them, which
-    // restarts at its s0); hup[j] says whether a sum started at or before j.
-    DF loc[4], s0d[4];
-    float loca[4];
-    bool head[4], hup[4];
+    // the lane's tiles in order: loc[j] the inclusive sum from the lane's
+    // first tile, or from the last sum start among them (hup[j])
+    DF loc[kPer];
+    float loca[kPer];
+    bool hd[kPer], hup[kPer];
     DF acc = DF{0.0f, 0.0f};
     float acca = 0.0f;
     bool seen = false;
 #pragma unroll
-    for (int j = 0; j < 4; j++) {
-      const int64_t t = t0 + j;
-      head[j] = false;
-      s0d[j] = DF{0.0f, 0.0f};
-      if (4 * tid + j < nready) {
+    for (int j = 0; j < kPer; j++) {
+      hd[j] = false;
+      if (kPer * lane + j < nready) {
         const DF a = DF{__uint_as_float(v[j].x), __uint_as_float(v[j].y)};
         const float aa = __uint_as_float(v[j].z);
-        const Geo g = tile_geo(p, t, &hint);
-        if (t == g.t_first) {
-          head[j] = true;
-          s0d[j] = start_df(p, g.sum);
-          acc = df_add(s0d[j], a);
-          acca = __fadd_rn(fabsf(s0d[j].hi), aa);
+        if (v[j].w & 4u) {
+          hd[j] = true;
+          acc = a;
+          acca = aa;
           seen = true;
         } else {
           acc = df_add(acc, a);
@@ -1385,8 +1372,7 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
       loca[j] = acca;
       hup[j] = seen;
     }
-    SCP(2);
-    // segmented scan of the threads' totals across the warp ...
+    // segmented scan of the lanes' totals
     DF x = acc;
     float xa = acca;
     bool hx = seen;
@@ -1405,89 +1391,55 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
         hx = hx || hy;
       }
     }
-    if (lane == 31 && w < kWarps) {   // (the ninth warp holds no tiles)
-      s_wtot[w] = x;
-      s_wabs[w] = xa;
-      s_whead[w] = hx;
+    // the inclusive prefix just before this lane's first tile
+    DF before;
+    before.hi = __shfl_up_sync(kFull, x.hi, 1);
+    before.lo = __shfl_up_sync(kFull, x.lo, 1);
+    float before_a = __shfl_up_sync(kFull, xa, 1);
+    const bool hb = __shfl_up_sync(kFull, hx, 1);
+    if (lane == 0) {
+      before = carry;
+      before_a = carry_abs;
+    } else if (!hb) {
+      before = df_add(carry, before);
+      before_a = __fadd_rn(carry_abs, before_a);
     }
-    DF xl;
-    xl.hi = __shfl_up_sync(kFull, x.hi, 1);
-    xl.lo = __shfl_up_sync(kFull, x.lo, 1);
-    const float xla = __shfl_up_sync(kFull, xa, 1);
-    const bool hl = __shfl_up_sync(kFull, hx, 1);
-    __syncthreads();
-    SCP(3);
-    // ... and across the warps, after the carry of the earlier windows:
-    // `before` is the inclusive prefix just before this thread's first tile
-    DF before = carry;
-    float before_a = carry_abs;
-    for (int k = 0; k < w; k++) {
-      if (s_whead[k]) {
-        before = s_wtot[k];
-        before_a = s_wabs[k];
-      } else {
-        before = df_add(before, s_wtot[k]);
-        before_a = __fadd_rn(before_a, s_wabs[k]);
-      }
-    }
-    if (lane > 0) {
-      if (hl) {
-        before = xl;
-        before_a = xla;
-      } else {
-        before = df_add(before, xl);
-        before_a = __fadd_rn(before_a, xla);
-      }
-    }
-    SCP(4);
-    // each tile's exclusive prefix: its s0 at a sum start, else the inclusive
-    // prefix of the tile before it
+    // each tile's exclusive prefix (a sum's first tile has its own already)
+    DF lastv = DF{0.0f, 0.0f};
+    float lasta = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 4; j++) {
-      if (4 * tid + j < nready) {
-        DF e;
-        float ea;
-        if (head[j]) {
-          e = s0d[j];
-          ea = fabsf(s0d[j].hi);
-        } else if (j == 0) {
-          e = before;
-          ea = before_a;
-        } else if (hup[j - 1]) {
-          e = loc[j - 1];
-          ea = loca[j - 1];
-        } else {
-          e = df_add(before, loc[j - 1]);
-          ea = __fadd_rn(before_a, loca[j - 1]);
+    for (int j = 0; j < kPer; j++) {
+      if (kPer * lane + j < nready) {
+        if (!hd[j]) {
+          DF e;
+          float ea;
+          if (j == 0) {
+            e = before;
+            ea = before_a;
+          } else if (hup[j - 1]) {
+            e = loc[j - 1];
+            ea = loca[j - 1];
+          } else {
+            e = df_add(before, loc[j - 1]);
+            ea = __fadd_rn(before_a, loca[j - 1]);
+          }
+          st_vol_v4(&p.prec[(t0 + j) * kPrecWords], make_uint4(__float_as_uint(e.hi), __float_as_uint(e.lo),
+                                                               __float_as_uint(ea), (tag << 8) | 2u));
         }
-        st_vol_v4(&p.prec[(t0 + j) * kPrecWords], make_uint4(__float_as_uint(e.hi), __float_as_uint(e.lo),
-                                                             __float_as_uint(ea), (tag << 8) | 2u));
+        if (kPer * lane + j == nready - 1) {
+          lastv = hup[j] ? loc[j] : df_add(before, loc[j]);
+          lasta = hup[j] ? loca[j] : __fadd_rn(before_a, loca[j]);
+        }
       }
     }
-    SCP(5);
-    // the carry into the next window: the inclusive prefix of its last tile
-    __syncthreads();
-    {
-      const int j = nready - 1 - 4 * tid;
-      if (j >= 0 && j < 4) {
-        s_wtot[0] = hup[j] ? loc[j] : df_add(before, loc[j]);
-        s_wabs[0] = hup[j] ? loca[j] : __fadd_rn(before_a, loca[j]);
-      }
-    }
-    __syncthreads();
-    carry = s_wtot[0];
-    carry_abs = s_wabs[0];
-    __syncthreads();
-    if (tid == 0) stat_add(sm, S_SCAN_WINDOWS, 1);
-    SCW(3, gtimer());
-    SCP(6);
-    nwin++;
+    // the carry into the next round: the inclusive prefix of the last tile
+    const int src = (nready - 1) / kPer;
+    carry.hi = __shfl_sync(kFull, lastv.hi, src);
+    carry.lo = __shfl_sync(kFull, lastv.lo, src);
+    carry_abs = __shfl_sync(kFull, lasta, src);
+    if (lane == 0) stat_add(sm, S_SCAN_WINDOWS, 1);
     pos += nready;
   }
-#ifdef SEQSUM_PROFILE
-  if (tid == 0)
-    for (int k = 0; k < 7; k++) p.dbg[2400 + 4 * 40 + k] = scp_acc[k];
-#endif
 }
 
 // ------------------------------------------------------------------ the walk: raw terms
