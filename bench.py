@@ -409,6 +409,39 @@ def main():
             cpu4["bits_match_oracle"] = bool(np.array_equal(
                 cpu_outs.view(np.uint64), oracle.seqsum_batched(w4.x, w4.offsets, w4.s0).view(np.uint64)))
             extra["c4"]["cpu_baseline_all_cores"] = cpu4
+        # the lcs variant: four interleaved sums per 1920x1080 window plane, with their float means
+        nl = 1920 * 1080
+        xl = np.empty(4 * nl)
+        xl[0::4] = W.plane_c2(1920, 1080, seed=41)
+        xl[1::4] = W.plane_pow2(nl, 42, -30, 2, stream=5)
+        xl[2::4] = W.plane_pow2(nl, 43, -20, 0, stream=5)
+        xl[3::4] = -W.plane_pow2(nl, 44, -40, 0, stream=5)
+        s0l = np.array([0.0, 1.0, 0.0, -0.5])
+        xld, s0ld = torch.from_numpy(xl).to(dev), torch.from_numpy(s0l).to(dev)
+        outl = torch.empty(4, dtype=torch.float64, device=dev)
+        meanl = torch.empty(4, dtype=torch.float32, device=dev)
+        sq.seqsum_f64_strided(xld, 4, s0ld, outs=outl, means=meanl, stream=stream)
+        stream.synchronize()
+        wl_sums, wl_means = oracle.seqsum_strided(xl, 4, s0l)
+        okl = (np.array_equal(outl.cpu().numpy().view(np.uint64), wl_sums.view(np.uint64)) and
+               np.array_equal(meanl.cpu().numpy().view(np.uint32), wl_means.view(np.uint32)))
+        ts = []
+        for i in range(30):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                sq.seqsum_f64_strided(xld, 4, s0ld, outs=outl, means=meanl, stream=stream)
+                b.record(stream)
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        tl = [a.elapsed_time(b) for a, b in ts[3:]]
+        ml = sum(tl) / len(tl)
+        extra["lcs_4x1920x1080"] = {"n_terms": len(xl), "nsums": 4, "ms_per_step": ml,
+                                    "Gterms/s": len(xl) / (ml * 1e-3) / 1e9,
+                                    "frac_hbm": 8 * len(xl) / (ml * 1e-3) / 1e9 / peak,
+                                    "parity_0ulp": bool(okl),
+                                    "note": "interleaved plane copied apart, then summed batched; float means"}
         line["other_configs"] = extra
 
     if rank == 0:

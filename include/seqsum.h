@@ -108,6 +108,27 @@ int seqsum_f64_batched(const double *x, const int64_t *offsets, int32_t nsums, c
 int seqsum_f64_batched_sized(const double *x, int64_t x_len, const int64_t *offsets, int32_t nsums,
                              const double *s0s, double *outs, cudaStream_t stream);
 
+/* stride interleaved sequential sums over one plane, and their float means:
+ * for each k < stride,
+ *   outs[k] = s0s[k] + x[k] + x[k + stride] + ... + x[k + stride*(n-1)]
+ * added in index order, and, when means is not null,
+ *   means[k] = (float)(outs[k] / n)
+ * (ADR-1464, "float_ssim_cuda sums in raster order on the host", Decision:
+ * the lcs variant keeps four sums per window -- the value and its l, c and s
+ * factors -- interleaved in one plane and summed with one accumulator each,
+ * and the frame score is the float of the sum over the number of windows).
+ *   x        device, stride * n doubles, interleaved (term i of sum k at i*stride + k), read only
+ *   n        terms per sum (windows), n >= 0
+ *   stride   number of sums, 1..64
+ *   s0s      device, stride start values
+ *   outs     device, stride doubles, written
+ *   means    device, stride floats, written; or null
+ * The sums are first copied apart into the workspace (one pass over x), then
+ * summed as a batched call.  Returns SEQSUM_OK, SEQSUM_EINVAL, SEQSUM_ENOMEM or
+ * SEQSUM_ECUDA. */
+int seqsum_f64_strided(const double *x, int64_t n, int32_t stride, const double *s0s, double *outs, float *means,
+                       cudaStream_t stream);
+
 /* Counters accumulated on the device by the calls since the last
  * seqsum_get_stats() on the same (device, stream) workspace as the most
  * recent call of this process. */

@@ -58,6 +58,9 @@ def lib():
             L.oracle_seqsum_batched.argtypes = [dp, ip, ctypes.c_int32, dp, dp]
             L.oracle_seqsum_trace.restype = None
             L.oracle_seqsum_trace.argtypes = [dp, ctypes.c_int64, ctypes.c_double, dp]
+            L.oracle_seqsum_strided.restype = None
+            L.oracle_seqsum_strided.argtypes = [dp, ctypes.c_int64, ctypes.c_int32, dp, dp,
+                                                ctypes.POINTER(ctypes.c_float)]
             L.oracle_env_check.restype = ctypes.c_int
             L.oracle_env_check.argtypes = []
             bad = L.oracle_env_check()
@@ -87,6 +90,20 @@ def seqsum_batched(x: np.ndarray, offsets: np.ndarray, s0s: np.ndarray) -> np.nd
     lib().oracle_seqsum_batched(_dptr(x), offsets.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
                                 n, _dptr(s0s), _dptr(out))
     return out
+
+
+def seqsum_strided(x: np.ndarray, stride: int, s0s: np.ndarray):
+    """stride interleaved sums (term i of sum k at x[i*stride + k]), one
+    accumulator each, and their float means (float)(sum / n).  Returns
+    (sums, means)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    s0s = np.ascontiguousarray(s0s, dtype=np.float64)
+    n = len(x) // stride
+    outs = np.empty(stride, dtype=np.float64)
+    means = np.empty(stride, dtype=np.float32)
+    lib().oracle_seqsum_strided(_dptr(x), n, int(stride), _dptr(s0s), _dptr(outs),
+                                means.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+    return outs, means
 
 
 def seqsum_trace(x: np.ndarray, s0: float = 0.0) -> np.ndarray:

@@ -52,6 +52,23 @@ void oracle_seqsum_batched(const double *x, const int64_t *offsets, int32_t nsum
         outs[k] = oracle_seqsum(x + offsets[k], offsets[k + 1] - offsets[k], s0s[k]);
 }
 
+/* stride interleaved sums, one accumulator each (ADR-1464, "float_ssim_cuda
+ * sums in raster order on the host", Decision: the lcs variant's four sums
+ * per window): outs[k] = s0s[k] + x[k] + x[k + stride] + ... over n terms,
+ * and the frame score's epilogue means[k] = (float)(outs[k] / n). */
+void oracle_seqsum_strided(const double *x, int64_t n, int32_t stride, const double *s0s, double *outs,
+                           float *means)
+{
+    for (int32_t k = 0; k < stride; k++) {
+        volatile double s = s0s[k];
+        for (int64_t i = 0; i < n; i++)
+            s = s + x[i * stride + k];
+        outs[k] = s;
+        volatile double q = s / (double)n;
+        means[k] = (float)q;
+    }
+}
+
 /* Trace variant: writes the running sum after every add (out[i] = s after
  * term i).  Used by tests that need the exact S at a chunk boundary. */
 void oracle_seqsum_trace(const double *x, int64_t n, double s0, double *out)

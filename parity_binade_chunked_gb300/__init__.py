@@ -19,6 +19,7 @@ from . import build as _build
 
 __all__ = ["seqsum_f64", "seqsum_f64_static", "seqsum_f64_batched", "seqsum_f64_batched_sized", "get_stats",
            "debug_set_plan", "debug_set_fault", "debug_counters", "release_workspace", "version", "lib", "lib_path",
+           "seqsum_f64_strided",
            "SeqsumError"]
 
 _lock = threading.Lock()
@@ -61,6 +62,8 @@ def lib():
             L.seqsum_f64_batched.restype = ctypes.c_int
             L.seqsum_f64_batched_sized.argtypes = [vp, i64, vp, i32, vp, vp, vp]
             L.seqsum_f64_batched_sized.restype = ctypes.c_int
+            L.seqsum_f64_strided.argtypes = [vp, i64, i32, vp, vp, vp, vp]
+            L.seqsum_f64_strided.restype = ctypes.c_int
             L.seqsum_get_stats.argtypes = [ctypes.POINTER(_Stats)]
             L.seqsum_get_stats.restype = ctypes.c_int
             L.seqsum_strerror.argtypes = [ctypes.c_int]
@@ -141,6 +144,37 @@ def seqsum_f64_static(x, s0: float = 0.0, out=None, stream=None):
         _check(lib().seqsum_f64_static(ctypes.c_void_p(x.data_ptr()), x.numel(), float(s0),
                                        ctypes.c_void_p(out.data_ptr()), _stream_handle(stream)))
     return out
+
+
+def seqsum_f64_strided(x, stride: int, s0s=None, outs=None, means=None, stream=None):
+    """stride interleaved sums: outs[k] = s0s[k] + x[k] + x[k + stride] + ...
+    in index order; means (a float32 tensor, or True to allocate one) gets
+    float(outs[k] / n).  Returns outs, or (outs, means) when means is given."""
+    import torch
+    x = _dev_f64(x, "x").reshape(-1)
+    stride = int(stride)
+    if stride < 1 or x.numel() % stride:
+        raise ValueError("x must hold a whole number of interleaved rows of `stride` terms")
+    n = x.numel() // stride
+    if s0s is None:
+        s0s = torch.zeros(stride, dtype=torch.float64, device=x.device)
+    _dev_f64(s0s, "s0s")
+    if outs is None:
+        outs = torch.empty(stride, dtype=torch.float64, device=x.device)
+    _dev_f64(outs, "outs")
+    m = None
+    if means is True:
+        m = torch.empty(stride, dtype=torch.float32, device=x.device)
+    elif means is not None:
+        m = means
+        if not (m.is_cuda and m.dtype == torch.float32 and m.is_contiguous() and m.numel() >= stride):
+            raise TypeError("means must be a contiguous CUDA float32 tensor of stride entries")
+    with torch.cuda.device(x.device):
+        _check(lib().seqsum_f64_strided(ctypes.c_void_p(x.data_ptr()), n, stride, ctypes.c_void_p(s0s.data_ptr()),
+                                        ctypes.c_void_p(outs.data_ptr()),
+                                        ctypes.c_void_p(m.data_ptr() if m is not None else 0),
+                                        _stream_handle(stream)))
+    return (outs, m) if m is not None else outs
 
 
 def seqsum_f64_batched(x, offsets, s0s, outs=None, stream=None):

@@ -33,6 +33,9 @@ struct Workspace {
   unsigned long long *stats = nullptr;
   unsigned long long *dbg = nullptr;
   int64_t *h_pin = nullptr;          // pinned bounce for the batched size read-back
+  double *planes = nullptr;          // strided calls: the interleaved sums laid out one after another
+  int64_t *soffs = nullptr;          // ... and their offsets
+  int64_t cap_planes = 0;
   // tensor map cache
   const void *tm_ptr = nullptr;
   int64_t tm_rows = -1;
@@ -283,6 +286,49 @@ int seqsum_f64_batched_sized(const double *x, int64_t x_len, const int64_t *offs
   return batched_impl(x, x_len, offsets, nsums, s0s, outs, true, stream);
 }
 
+int seqsum_f64_strided(const double *x, int64_t n, int32_t stride, const double *s0s, double *outs, float *means,
+                       cudaStream_t stream) {
+  if (n < 0 || stride < 1 || stride > sq::kMaxStride || !s0s || !outs || (n > 0 && !x)) return SEQSUM_EINVAL;
+  double *planes = nullptr;
+  int64_t *soffs = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int rc = ensure_device_info();
+    if (rc) return rc;
+    Workspace *w = nullptr;
+    rc = get_ws(stream, 1, stride, &w);
+    if (rc) return rc;
+    const int64_t need = n * stride;
+    if (!w->soffs) {
+      cudaError_t e = cudaMalloc(&w->soffs, (sq::kMaxStride + 1) * sizeof(int64_t));
+      if (e != cudaSuccess) return SEQSUM_ENOMEM;
+    }
+    if (need > w->cap_planes) {
+      cudaError_t e = cudaStreamSynchronize(stream);   // earlier calls may still read the old copy
+      if (e != cudaSuccess) return cuda_fail(e);
+      cudaFree(w->planes);
+      w->planes = nullptr;
+      w->cap_planes = 0;
+      if (cudaMalloc(&w->planes, (need > 0 ? need : 1) * sizeof(double)) != cudaSuccess) {
+        g_last_cuda = (int)cudaGetLastError();
+        return SEQSUM_ENOMEM;
+      }
+      w->cap_planes = need;
+    }
+    planes = w->planes;
+    soffs = w->soffs;
+    cudaError_t e = sq::launch_deinterleave(x, n, stride, planes, soffs, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  int rc = batched_impl(planes, n * stride, soffs, stride, s0s, outs, true, stream);
+  if (rc) return rc;
+  if (means) {
+    cudaError_t e = sq::launch_mean(outs, stride, n, means, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return SEQSUM_OK;
+}
+
 int seqsum_get_stats(seqsum_stats *st) {
   if (!st) return SEQSUM_EINVAL;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -371,6 +417,8 @@ void seqsum_release_workspace(void) {
     cudaFree(w->ctr);
     cudaFree(w->stats);
     cudaFree(w->dbg);
+    cudaFree(w->planes);
+    cudaFree(w->soffs);
     cudaFreeHost(w->h_pin);
     delete w;
   }

@@ -145,6 +145,10 @@ constexpr int kDbgWords = 4096;
 
 cudaError_t launch_seqsum(const Params &p, const CUtensorMap *tmap, int grid, cudaStream_t st);
 cudaError_t launch_setup(const Params &p, cudaStream_t st);
+cudaError_t launch_deinterleave(const double *x, int64_t n, int stride, double *planes, int64_t *offsets,
+                                cudaStream_t st);
+cudaError_t launch_mean(const double *outs, int stride, int64_t n, float *means, cudaStream_t st);
+constexpr int kMaxStride = 64;                   // interleaved sums a strided call takes
 int kernel_blocks_per_sm();
 
 }  // namespace sq

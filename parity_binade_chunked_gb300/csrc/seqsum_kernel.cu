@@ -2480,4 +2480,36 @@ cudaError_t launch_setup(const Params &p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ interleaved sums (strided)
+// The stride sums of an interleaved plane (sum k: x[k], x[k + stride], ...)
+// laid out one after another, so the batched kernel takes them as stride
+// sums of n terms each; offsets[k] = k n.  A copy only: no term changes.
+__global__ void __launch_bounds__(kThreads) deinterleave_kernel(const double *x, int64_t n, int stride,
+                                                                double *planes, int64_t *offsets) {
+  for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kThreads)
+    for (int k = 0; k < stride; k++) planes[(int64_t)k * n + i] = x[i * stride + k];
+  if (blockIdx.x == 0 && threadIdx.x <= stride) offsets[threadIdx.x] = (int64_t)threadIdx.x * n;
+}
+
+// The frame score's epilogue: each sum's mean as a float, (float)(sum / n),
+// with the correctly rounded division and conversion the host loop uses.
+__global__ void mean_kernel(const double *outs, int stride, int64_t n, float *means) {
+  const int k = threadIdx.x;
+  if (k < stride) means[k] = __double2float_rn(__ddiv_rn(outs[k], (double)n));
+}
+
+cudaError_t launch_deinterleave(const double *x, int64_t n, int stride, double *planes, int64_t *offsets,
+                                cudaStream_t st) {
+  int64_t blocks = (n + kThreads - 1) / kThreads;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  deinterleave_kernel<<<(int)blocks, kThreads, 0, st>>>(x, n, stride, planes, offsets);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mean(const double *outs, int stride, int64_t n, float *means, cudaStream_t st) {
+  mean_kernel<<<1, 64, 0, st>>>(outs, stride, n, means);
+  return cudaGetLastError();
+}
+
 }  // namespace sq

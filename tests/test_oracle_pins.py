@@ -170,6 +170,44 @@ def test_batched_vs_simulation(oracle_mod):
     del rng
 
 
+def test_strided_vs_simulation(oracle_mod):
+    """Interleaved sums (ADR-1464, Decision: the lcs variant's four sums per
+    window, one accumulator each): every sum is pinned to the exact
+    simulation of its own subsequence, and every mean to the division
+    rounded to the nearest double by exact rational arithmetic, then to the
+    nearest float (the host's (float)(sum / windows))."""
+    from fractions import Fraction
+    rng = random.Random(21)
+    for stride in [1, 2, 4, 7]:
+        for n in [1, 2, 5, 33, 200]:
+            xs = []
+            for _ in range(n * stride):
+                e = rng.randint(-60, 8)
+                xs.append(rng.choice([1.0, -1.0, 1.0]) * rng.randint(1, 2 ** 20) * 2.0 ** e)
+            s0s = [rng.choice([0.0, 1.0, -0.5, 3.0]) for _ in range(stride)]
+            sums, means = oracle_mod.seqsum_strided(np.array(xs), stride, np.array(s0s))
+            for k in range(stride):
+                want = sim.seqsum(xs[k::stride], s0s[k])
+                assert same(sums[k], want), (stride, n, k)
+                q = float(Fraction(want) / n)          # correctly rounded double quotient
+                assert np.float32(q).view(np.uint32) == means[k].view(np.uint32), (stride, n, k)
+
+
+def test_strided_closed_forms(oracle_mod):
+    """Integer terms: each interleaved sum is the exact integer total; with
+    n a power of two the mean is that total scaled exactly; 1/3 as a float
+    is 0x3EAAAAAB."""
+    n, stride = 1024, 4
+    x = np.arange(n * stride, dtype=np.float64)
+    sums, means = oracle_mod.seqsum_strided(x, stride, np.zeros(stride))
+    for k in range(stride):
+        exact = sum(i * stride + k for i in range(n))
+        assert sums[k] == float(exact)
+        assert means[k] == np.float32(exact / 1024.0)
+    sums, means = oracle_mod.seqsum_strided(np.array([1.0, 0.0, 0.0]), 1, np.zeros(1))
+    assert sums[0] == 1.0 and means[0].view(np.uint32) == 0x3EAAAAAB
+
+
 # ------------------------------------------------------- planted mistakes
 
 def _pin_suite_passes(fn):
