@@ -442,6 +442,41 @@ def main():
                                     "frac_hbm": 8 * len(xl) / (ml * 1e-3) / 1e9 / peak,
                                     "parity_0ulp": bool(okl),
                                     "note": "interleaved plane copied apart, then summed batched; float means"}
+        # plan reuse: a sequence of frames close to one another (the workload's
+        # plane, each term scaled by its own factor in [1 - 2^-7, 1 + 2^-7]),
+        # one plan kept from frame to frame
+        u = [W.uniform53(W.draws_u64(100 + k, 7, n)) for k in range(4)]
+        frames = [x * (1.0 + 2.0 ** -7 * (2.0 * uk - 1.0)) for uk in u]
+        fd = [torch.from_numpy(f).to(dev) for f in frames]
+        outs_p = torch.empty(4, dtype=torch.float64, device=dev)
+        plan = sq.SeqsumPlan()
+        with torch.cuda.stream(stream):
+            for k in range(4):
+                plan(fd[k], s0, out=outs_p[k:k + 1], stream=stream)
+        stream.synchronize()
+        sq.get_stats()
+        ts = []
+        for i in range(40):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                plan(fd[i % 4], s0, out=outs_p[i % 4:i % 4 + 1], stream=stream)
+                b.record(stream)
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        stp = sq.get_stats()
+        okp = all(np.float64(outs_p[k].item()).view(np.uint64) == np.float64(oracle.seqsum(frames[k], s0)).view(np.uint64)
+                  for k in range(4))
+        plan.close()
+        tp = [a.elapsed_time(b) for a, b in ts[4:]]
+        mp = sum(tp) / len(tp)
+        extra["planned_frames"] = {"workload": args.config, "n_terms": n, "ms_per_step": mp,
+                                   "Gterms/s": n / (mp * 1e-3) / 1e9,
+                                   "frac_hbm": 8 * n / (mp * 1e-3) / 1e9 / peak, "parity_0ulp": bool(okp),
+                                   "tiles_redone_per_call": stp["tiles_redone"] / 40.0,
+                                   "note": "seqsum_f64_planned over 4 frames in turn, the plan of each call "
+                                           "from the call before"}
         line["other_configs"] = extra
 
     if rank == 0:

@@ -129,6 +129,40 @@ int seqsum_f64_batched_sized(const double *x, int64_t x_len, const int64_t *offs
 int seqsum_f64_strided(const double *x, int64_t n, int32_t stride, const double *s0s, double *outs, float *means,
                        cudaStream_t stream);
 
+/* A plan kept from one call to the next (opaque; one per sequence of frames).
+ * Research-1433, "Forming the CPU's sequential double sums on a GPU, bit for
+ * bit", Open questions (throughput): keep the previous frame's plan, form the
+ * runs under it in the same pass that forms the new plan's sums, and form
+ * again only the chunks whose plan changed. */
+typedef struct seqsum_plan seqsum_plan;
+
+/* Creates an empty plan.  Returns SEQSUM_OK, SEQSUM_EINVAL (out is null) or
+ * SEQSUM_ENOMEM.  The plan holds no device memory until its first call. */
+int seqsum_plan_create(seqsum_plan **out);
+
+/* Waits for the device (its calls may still read the plan) and frees the
+ * plan.  A null plan is ignored. */
+void seqsum_plan_destroy(seqsum_plan *plan);
+
+/* As seqsum_f64, for one frame of a sequence: *out = s0 + x[0] + ... +
+ * x[n-1] in index order, bit for bit, whatever the frames hold.
+ *   plan   from seqsum_plan_create; the call reads the plan of the frame
+ *          before and leaves this frame's (2 x 80 bytes a 4096-term tile of
+ *          device memory, allocated when n changes)
+ *   x, n, s0, out, stream  as for seqsum_f64
+ * The first call, and a call whose n differs from the call before, forms its
+ * plan first (the two passes of seqsum_f64).  Every other call reads x once:
+ * each tile's runs are formed on the stored prefix while its sums for the new
+ * plan are taken; a tile whose new prefix no longer keeps the binades its runs
+ * were formed in is formed again on the new prefix before the walk reaches it.
+ * A frame close to the one before costs one pass; a frame unlike it costs at
+ * most about what seqsum_f64 does.  Calls on one plan must be ordered (one
+ * stream, or synchronised); a plan is tied to the device of its first call
+ * until n changes.
+ * Returns SEQSUM_OK, SEQSUM_EINVAL, SEQSUM_ENOMEM or SEQSUM_ECUDA. */
+int seqsum_f64_planned(seqsum_plan *plan, const double *x, int64_t n, double s0, double *out,
+                       cudaStream_t stream);
+
 /* Counters accumulated on the device by the calls since the last
  * seqsum_get_stats() on the same (device, stream) workspace as the most
  * recent call of this process. */
@@ -155,9 +189,12 @@ typedef struct {
   int64_t scan_polls;        /* scanner polls that found no new tile sums */
   int64_t pfx_late;          /* run units whose prefix was not yet published when their copy landed */
   int64_t ctas_alone;        /* streaming CTAs that left their SM to the walker or the scanner */
+  int64_t tiles_redone;      /* planned calls: tiles formed again because the new prefix moved their binades */
   int64_t t_stream_ns;       /* latest call: kernel start to the last tile header */
   int64_t t_walk_tail_ns;    /* latest call: last tile header to the end of the walk */
   int64_t t_total_ns;        /* latest call: kernel start to the end of the walk */
+  int64_t t_scan_ns;         /* latest call: kernel start to the end of the scanner */
+  int64_t t_units_ns;        /* latest call: kernel start to the last tile header formed */
   int32_t device_status;     /* 0, or a negative SEQSUM_E* code */
   int32_t device_error_bits; /* raw device error bits */
   int32_t check_site;        /* self-checking builds: first failed check (0: none) */
@@ -165,7 +202,8 @@ typedef struct {
   int64_t check_value;       /* self-checking builds: the value that failed it */
   int32_t timeout_site;      /* first bounded device wait that gave up (0: none): 2 a stage's copy, 3 a walk
                                 range's tile headers, 5 a run unit's prefix, 6 the scanner's tile sums, 7 a
-                                stage's release */
+                                stage's release, 8 a planned call's redo list, 9 a planned call's check
+                                of a round */
   int32_t timeout_pad;
   int64_t timeout_a;         /* its context: the tile */
   int64_t timeout_b;

@@ -19,7 +19,7 @@ from . import build as _build
 
 __all__ = ["seqsum_f64", "seqsum_f64_static", "seqsum_f64_batched", "seqsum_f64_batched_sized", "get_stats",
            "debug_set_plan", "debug_set_fault", "debug_counters", "release_workspace", "version", "lib", "lib_path",
-           "seqsum_f64_strided",
+           "seqsum_f64_strided", "SeqsumPlan",
            "SeqsumError"]
 
 _lock = threading.Lock()
@@ -34,8 +34,8 @@ class _Stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
         "tiles", "tiles_complex", "ranges_from_x", "lanes_raw", "lanes_raw2", "lanes_tie", "walk_batches",
         "walk_segments", "runs_rejected", "terms_dadd", "raw_rounds", "cy_walk_wait", "cy_walk_serial",
-        "cy_walk_raw", "cy_tma_wait", "cy_plan", "cy_pfx_wait", "cy_run", "scan_windows", "scan_polls", "pfx_late", "ctas_alone",
-        "t_stream_ns", "t_walk_tail_ns", "t_total_ns")] + [
+        "cy_walk_raw", "cy_tma_wait", "cy_plan", "cy_pfx_wait", "cy_run", "scan_windows", "scan_polls", "pfx_late", "ctas_alone", "tiles_redone",
+        "t_stream_ns", "t_walk_tail_ns", "t_total_ns", "t_scan_ns", "t_units_ns")] + [
         ("device_status", ctypes.c_int32), ("device_error_bits", ctypes.c_int32),
         ("check_site", ctypes.c_int32), ("check_pad", ctypes.c_int32), ("check_value", ctypes.c_int64),
         ("timeout_site", ctypes.c_int32), ("timeout_pad", ctypes.c_int32), ("timeout_a", ctypes.c_int64),
@@ -64,6 +64,12 @@ def lib():
             L.seqsum_f64_batched_sized.restype = ctypes.c_int
             L.seqsum_f64_strided.argtypes = [vp, i64, i32, vp, vp, vp, vp]
             L.seqsum_f64_strided.restype = ctypes.c_int
+            L.seqsum_plan_create.argtypes = [ctypes.POINTER(vp)]
+            L.seqsum_plan_create.restype = ctypes.c_int
+            L.seqsum_plan_destroy.argtypes = [vp]
+            L.seqsum_plan_destroy.restype = None
+            L.seqsum_f64_planned.argtypes = [vp, vp, i64, d, vp, vp]
+            L.seqsum_f64_planned.restype = ctypes.c_int
             L.seqsum_get_stats.argtypes = [ctypes.POINTER(_Stats)]
             L.seqsum_get_stats.restype = ctypes.c_int
             L.seqsum_strerror.argtypes = [ctypes.c_int]
@@ -126,6 +132,48 @@ def seqsum_f64(x, s0: float = 0.0, out=None, stream=None):
         _check(lib().seqsum_f64(ctypes.c_void_p(x.data_ptr()), x.numel(), float(s0),
                                 ctypes.c_void_p(out.data_ptr()), _stream_handle(stream)))
     return out
+
+
+class SeqsumPlan:
+    """A plan kept from one frame to the next (seqsum_plan_create /
+    seqsum_f64_planned / seqsum_plan_destroy).  ``plan(x, s0)`` returns the
+    same bits as seqsum_f64(x, s0); after the first frame it reads x once and
+    forms again only the tiles whose binades the new prefix moved."""
+
+    def __init__(self):
+        h = ctypes.c_void_p()
+        _check(lib().seqsum_plan_create(ctypes.byref(h)))
+        self._h = h
+
+    def __call__(self, x, s0: float = 0.0, out=None, stream=None):
+        import torch
+        if self._h is None:
+            raise SeqsumError("seqsum: the plan was closed")
+        x = _dev_f64(x, "x").reshape(-1)
+        if out is None:
+            out = torch.empty(1, dtype=torch.float64, device=x.device)
+        _dev_f64(out, "out")
+        with torch.cuda.device(x.device):
+            _check(lib().seqsum_f64_planned(self._h, ctypes.c_void_p(x.data_ptr()), x.numel(), float(s0),
+                                            ctypes.c_void_p(out.data_ptr()), _stream_handle(stream)))
+        return out
+
+    def close(self):
+        if self._h is not None and _lib is not None:
+            _lib.seqsum_plan_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
 
 
 STATIC_MAX_TERMS = 1 << 21

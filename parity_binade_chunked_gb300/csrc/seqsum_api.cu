@@ -10,6 +10,7 @@
 
 #include <map>
 #include <mutex>
+#include <new>
 #include <utility>
 
 #include "../../include/seqsum.h"
@@ -36,6 +37,8 @@ struct Workspace {
   double *planes = nullptr;          // strided calls: the interleaved sums laid out one after another
   int64_t *soffs = nullptr;          // ... and their offsets
   int64_t cap_planes = 0;
+  uint32_t *conf = nullptr;          // planned calls: per tile, the tag once its header may be walked
+  uint32_t *redo = nullptr;          // planned calls: the redo list
   // tensor map cache
   const void *tm_ptr = nullptr;
   int64_t tm_rows = -1;
@@ -67,6 +70,10 @@ void ws_free(Workspace *w) {
   cudaFree(w->hdr);
   cudaFree(w->items);
   cudaFree(w->tile_begin);
+  cudaFree(w->conf);
+  cudaFree(w->redo);
+  w->conf = nullptr;
+  w->redo = nullptr;
   w->status = nullptr;
   w->hdr = w->items = nullptr;
   w->tile_begin = nullptr;
@@ -103,7 +110,9 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
         cudaMalloc(&w->prec, ct * sq::kPrecWords * sizeof(uint4)) != cudaSuccess ||
         cudaMalloc(&w->hdr, ct * sizeof(Rec)) != cudaSuccess ||
         cudaMalloc(&w->items, ct * sq::kItemSlots * sizeof(Rec)) != cudaSuccess ||
-        cudaMalloc(&w->tile_begin, (cs + 1) * sizeof(int64_t)) != cudaSuccess) {
+        cudaMalloc(&w->tile_begin, (cs + 1) * sizeof(int64_t)) != cudaSuccess ||
+        cudaMalloc(&w->conf, ct * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMalloc(&w->redo, ct * sizeof(uint32_t)) != cudaSuccess) {
       ws_free(w);
       g_last_cuda = (int)cudaGetLastError();
       return SEQSUM_ENOMEM;
@@ -112,6 +121,8 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
     cudaMemset(w->status, 0, ct * sizeof(uint4));
     cudaMemset(w->prec, 0, ct * sq::kPrecWords * sizeof(uint4));
     cudaMemset(w->hdr, 0, ct * sizeof(Rec));
+    cudaMemset(w->conf, 0, ct * sizeof(uint32_t));
+    cudaMemset(w->redo, 0, ct * sizeof(uint32_t));
     cudaMemset(w->ctr, 0, sq::C_COUNT * sizeof(uint32_t));
     w->cap_tiles = ct;
     w->cap_sums = cs;
@@ -174,6 +185,9 @@ int64_t tensor_map(Workspace *w, const double *x, int64_t n_total) {
 void fill_ws(Params &p, Workspace *w) {
   p.status = w->status;
   p.prec = w->prec;
+  p.prec_ws = w->prec;
+  p.conf = w->conf;
+  p.redo = w->redo;
   p.wave = g_wave;
   p.hdr = w->hdr;
   p.items = w->items;
@@ -272,6 +286,111 @@ int seqsum_f64(const double *x, int64_t n, double s0, double *out, cudaStream_t 
   static CUtensorMap dummy;
   cudaError_t e = sq::launch_seqsum(p, p.tma_rows ? &w->tmap : &dummy, (int)grid, stream);
   if (e != cudaSuccess) return cuda_fail(e);
+  g_last = w;
+  return SEQSUM_OK;
+}
+
+}  // extern "C"
+
+// A plan kept across calls: each tile's plan record (prefix and warps' sums)
+// of the latest call, and a second array the next call writes its own into.
+struct seqsum_plan {
+  int device = -1;
+  int64_t tiles = 0;       // tiles the records are for (0: none yet)
+  uint4 *rec[2] = {nullptr, nullptr};
+  int cur = 0;             // rec[cur] holds the latest call's plan
+};
+
+extern "C" {
+
+int seqsum_plan_create(seqsum_plan **out) {
+  if (!out) return SEQSUM_EINVAL;
+  *out = new (std::nothrow) seqsum_plan();
+  return *out ? SEQSUM_OK : SEQSUM_ENOMEM;
+}
+
+void seqsum_plan_destroy(seqsum_plan *plan) {
+  if (!plan) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (plan->device >= 0) {
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(plan->device);
+    cudaDeviceSynchronize();   // calls still in flight may read the records
+    cudaFree(plan->rec[0]);
+    cudaFree(plan->rec[1]);
+    cudaSetDevice(prev);
+  }
+  delete plan;
+}
+
+int seqsum_f64_planned(seqsum_plan *plan, const double *x, int64_t n, double s0, double *out,
+                       cudaStream_t stream) {
+  if (!plan || n < 0 || !out || (n > 0 && !x)) return SEQSUM_EINVAL;
+  std::lock_guard<std::mutex> lk(g_mu);
+  int rc = ensure_device_info();
+  if (rc) return rc;
+  const int64_t tiles = (n + sq::kTileTerms - 1) / sq::kTileTerms;
+  Workspace *w = nullptr;
+  rc = get_ws(stream, tiles > 0 ? tiles : 1, 1, &w);
+  if (rc) return rc;
+  bool fresh = false;
+  if (plan->device != w->device || plan->tiles != tiles || !plan->rec[0]) {
+    // a first call, or a plane of another size: new records, a full (two-pass) call fills them
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (plan->device >= 0) {
+      int prev = 0;
+      cudaGetDevice(&prev);
+      cudaSetDevice(plan->device);
+      cudaDeviceSynchronize();
+      cudaFree(plan->rec[0]);
+      cudaFree(plan->rec[1]);
+      cudaSetDevice(prev);
+    }
+    plan->rec[0] = plan->rec[1] = nullptr;
+    plan->tiles = 0;
+    const size_t bytes = (size_t)(tiles > 0 ? tiles : 1) * sq::kPrecWords * sizeof(uint4);
+    if (cudaMalloc(&plan->rec[0], bytes) != cudaSuccess || cudaMalloc(&plan->rec[1], bytes) != cudaSuccess) {
+      cudaFree(plan->rec[0]);
+      plan->rec[0] = plan->rec[1] = nullptr;
+      g_last_cuda = (int)cudaGetLastError();
+      return SEQSUM_ENOMEM;
+    }
+    cudaMemsetAsync(plan->rec[0], 0, bytes, stream);
+    cudaMemsetAsync(plan->rec[1], 0, bytes, stream);
+    plan->device = w->device;
+    plan->tiles = tiles;
+    plan->cur = 0;
+    fresh = true;
+  }
+  Params p;
+  memset(&p, 0, sizeof p);
+  p.x = x;
+  p.x_len = n;
+  p.outs = out;
+  p.s0 = s0;
+  p.n = n;
+  p.ntiles = tiles;
+  p.nsums = 1;
+  fill_ws(p, w);
+  if (fresh) {
+    p.prec = plan->rec[plan->cur];   // the two-pass call leaves its plan here
+  } else {
+    p.planned = 1;
+    p.prec = plan->rec[plan->cur];
+    p.prec_next = plan->rec[plan->cur ^ 1];
+  }
+  p.tma_rows = n > 0 ? tensor_map(w, x, n) : 0;
+  p.nwalkers = 1;
+  int64_t grid = (int64_t)g_num_sms[w->device] * g_blocks_per_sm;
+  const int64_t units = fresh ? 2 * tiles : tiles;
+  if (units + 2 < grid) grid = units + 2;
+  if (grid < 3) grid = 3;
+  static CUtensorMap dummy;
+  cudaError_t e = sq::launch_seqsum(p, p.tma_rows ? &w->tmap : &dummy, (int)grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (!fresh) plan->cur ^= 1;      // stream order: the next call reads what this one writes
   g_last = w;
   return SEQSUM_OK;
 }
@@ -377,10 +496,14 @@ int seqsum_get_stats(seqsum_stats *st) {
   st->scan_polls = (int64_t)s[sq::S_SCAN_POLLS];
   st->pfx_late = (int64_t)s[sq::S_PFX_LATE];
   st->ctas_alone = (int64_t)s[sq::S_ALONE];
+  st->tiles_redone = (int64_t)s[sq::S_REDO];
   const int64_t t0 = (int64_t)s[sq::S_T_START], t1 = (int64_t)s[sq::S_T_STREAM_END], t2 = (int64_t)s[sq::S_T_WALK_END];
   st->t_stream_ns = (t0 && t1) ? t1 - t0 : 0;
   st->t_walk_tail_ns = (t1 && t2) ? t2 - t1 : 0;
   st->t_total_ns = (t0 && t2) ? t2 - t0 : 0;
+  const int64_t t3 = (int64_t)s[sq::S_T_SCAN_END], t4 = (int64_t)s[sq::S_T_UNITS_END];
+  st->t_scan_ns = (t0 && t3) ? t3 - t0 : 0;
+  st->t_units_ns = (t0 && t4) ? t4 - t0 : 0;
   st->device_error_bits = (int32_t)err;
   if (err & sq::ERR_CAPACITY) st->device_status = SEQSUM_ECAPACITY;
   else if (err & sq::ERR_BAD_OFFSETS) st->device_status = SEQSUM_EOFFSETS;

@@ -24,6 +24,14 @@ constexpr int kWarpSlots = 32;                   // 32-byte item slots of one wa
 constexpr int kItemSlots = kWarps * kWarpSlots;  // a tile's item area (8 KB): one region per compute warp
 constexpr int kMaxWalkers = 8;
 
+// ---- units of a streaming CTA
+enum : int {
+  U_RUN = 0,    // a tile's runs on the prefix its plan unit and the scanner gave
+  U_PLAN = 1,   // a tile's sums (for the scanner) and its warps' sums
+  U_SPEC = 2,   // planned calls: a tile's runs on the stored prefix, and its sums for the new plan
+  U_REDO = 3    // planned calls: a tile's runs again, on the new prefix
+};
+
 // ---- records
 // A tile header or an item: four 64-bit words.  A header carries the call's
 // 8-bit tag in the top byte of every word (a 16-byte access need not be
@@ -69,7 +77,9 @@ enum : int {
   C_TO_B = 13,
   C_WALK_SM = 14,    // 1 + the SM of the (first) walker: a streaming CTA there takes no units
   C_SCAN_SM = 15,    // 1 + the SM of the scanner: likewise
-  C_COUNT = 16
+  C_REDO_RES = 16,   // planned calls: places of the redo list taken so far
+  C_SCAN_FIN = 17,   // planned calls: the scanner and its checkers are done (C_REDO_RES is final)
+  C_COUNT = 18
 };
 enum : uint32_t {
   ERR_TMA_TIMEOUT = 1u,     // a TMA copy did not land within the wait limit (the tile was read from x)
@@ -103,10 +113,13 @@ enum : int {
   S_SCAN_POLLS,       // scanner polls of tiles' sums
   S_PFX_LATE,         // run units whose prefix came after their copy
   S_ALONE,            // streaming CTAs that left their SM to the walker or the scanner
+  S_REDO,             // planned calls: tiles whose stored plan no longer held (formed again)
   S_ACCUM_END,
   S_T_START = 24,     // timestamps of the latest call (globaltimer): first CTA start
   S_T_STREAM_END,     // last tile header published (max over CTAs)
   S_T_WALK_END,       // last walk ended
+  S_T_SCAN_END,       // the scanner ended
+  S_T_UNITS_END,      // last unit's tile header published (max over CTAs)
   S_COUNT = 32
 };
 static_assert(S_ACCUM_END <= S_T_START, "summed counters overlap the timestamps");
@@ -129,6 +142,13 @@ struct Params {
   int64_t fault_arg;
   uint64_t wait_ns;            // limit of every bounded device wait
   int64_t wave;                // plan units run this many tiles ahead of run units
+  int32_t planned;             // a planned call: every tile formed on the stored plan in prec, then again
+                               // where the new prefix shows that plan no longer holds; the new plan (the
+                               // tiles' sums and prefixes) goes to prec_next
+  uint4 *prec_next;
+  uint4 *prec_ws;              // the workspace's plan records (cap_tiles of them), cleared when the tag wraps
+  uint32_t *conf;              // planned calls, per tile: the tag once its header may be walked (null: none)
+  uint32_t *redo;              // planned calls: the tiles to form again, each (tag << 24) | tile
   // workspace
   uint4 *status;               // per tile: the tile's own sums, published by its plan unit (16 bytes)
   uint4 *prec;                 // per tile: kPrecWords words -- the exclusive prefix (the scanner), the warp sums (the plan)

@@ -110,6 +110,17 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t *p) {
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u32(uint32_t *p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ void fence_acq_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ uint64_t dbits(double v) { return (uint64_t)__double_as_longlong(v); }
 __device__ __forceinline__ double bitsd(uint64_t b) { return __longlong_as_double((long long)b); }
@@ -293,7 +304,7 @@ struct __align__(16) StageSm {
   int64_t tile;                 // -1: none (the compute warps stop)
   int64_t geo[5];               // row0, g_lo, g_hi, t_first, sum
   uint32_t tma;                 // the tile comes by TMA
-  int plan;                     // a plan unit (else a run unit)
+  int kind;                     // U_RUN, U_PLAN, U_SPEC or U_REDO
 };
 
 // The combining state of a unit while its warps finish it (a ring of 4: a
@@ -327,6 +338,13 @@ struct Smem {
   uint32_t prof_i;                   // profiling builds: how a raw row with tables ended
   uint32_t prof_n;                   // profiling builds: walk steps logged
   uint64_t t_stream_end;
+  uint64_t t_units_end;              // a streaming CTA: when its latest unit's header was published
+  // the scanner's CTA in a planned call: the rounds handed to the checker warps
+  int64_t ring_pos[16];              // a ring slot's first tile
+  int ring_n[16];                    // ... and its tiles
+  int ring_pub;                      // rounds in the ring so far
+  int ring_end;                      // -1, then the number of rounds once the scan is over
+  int chk_done[kWarps];              // rounds each checker warp has finished
   // the walk's slots: handed over by mbarriers, their uses counted on each side
   uint64_t wfull[kWarps];
   uint64_t wempty[kWarps];
@@ -424,7 +442,8 @@ __device__ __forceinline__ void saturate(Run &r) {
 // Ticket k names a unit: the plan of a tile (its float sums published), or
 // the runs of a tile, W tiles behind the plans, once the scanner has turned
 // the sums into the tile's prefix.  Every unit depends only on units with
-// smaller tickets, so the smallest unfinished unit can always proceed.
+// smaller tickets, so the smallest unfinished unit can always proceed.  (A
+// planned call takes its tickets otherwise: see producer_warp.)
 __device__ __forceinline__ int64_t unit_of(int64_t k, int64_t P, int64_t W, bool &plan) {
   plan = false;
   if (k < 0) return -1;
@@ -475,10 +494,9 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 // tile's plan record (prefix and warp sums) beside it.  The stage's per-unit
 // state is cleared first; the mbarrier completion publishes it to the warps.
 __device__ __forceinline__ void stage_fill(const Params &p, Smem &sm, unsigned char *stages, const CUtensorMap *tmap,
-                                           int s, int64_t k, int64_t ntiles, int (&hint)[2]) {
+                                           int s, int64_t t, int kind, int (&hint)[2]) {
   StageSm &st = sm.st[s];
-  bool plan = false;
-  const int64_t t = unit_of(k, ntiles, p.wave, plan);
+  const bool plan = kind == U_PLAN;
   if (t < 0) {
     st.tile = -1;
     st.tma = 0;
@@ -487,7 +505,7 @@ __device__ __forceinline__ void stage_fill(const Params &p, Smem &sm, unsigned c
   }
   const Geo g = tile_geo(p, t, &hint[plan ? 0 : 1]);
   st.tile = t;
-  st.plan = plan ? 1 : 0;
+  st.kind = kind;
   st.geo[0] = g.row0;
   st.geo[1] = g.g_lo;
   st.geo[2] = g.g_hi;
@@ -499,7 +517,7 @@ __device__ __forceinline__ void stage_fill(const Params &p, Smem &sm, unsigned c
   if (tma || side) {
     mbar_expect_tx(&sm.full[s], (tma ? (uint32_t)kStageBytes : 0u) + side);
     if (tma) tma_load_2d(stages + s * kStageBytes, tmap, &sm.full[s], 0, (int32_t)g.row0);
-    if (side) bulk_load(st.prec, p.prec + t * kPrecWords, side, &sm.full[s]);
+    if (side) bulk_load(st.prec, (kind == U_REDO ? p.prec_next : p.prec) + t * kPrecWords, side, &sm.full[s]);
   } else {
     mbar_arrive(&sm.full[s]);
   }
@@ -608,6 +626,42 @@ __device__ __forceinline__ void row_sums(const uint64_t (&v)[kLaneTerms], float 
 // A sum's start value as a double-float (the start of its first tile's prefix).
 __device__ __noinline__ DF start_df(const Params &p, int32_t sum) { return df_of_double(p.offsets ? p.s0s[sum] : p.s0); }
 
+// The last warp of a tile's plan: the warps' sums beside the tile's prefix
+// (in `rec`), and the tile's sums for the scanner; a sum's first tile also
+// publishes its prefix, the sum's start value.  key: the binade of a tile of
+// one run formed on a stored plan (0: none).
+__device__ __noinline__ void publish_plan(const Params &p, UnitSm &us, int64_t t, const Geo &g, uint32_t tag,
+                                          uint4 *rec, uint32_t key) {
+  const int lane = threadIdx.x & 31;
+  if (lane < 2 * kWarps / 4) {
+    // the warps' sums (4 floats a lane) beside the tile's prefix
+    const float *src = lane < kWarps / 4 ? &us.wfs[4 * lane] : &us.wfa[4 * (lane - kWarps / 4)];
+    st_vol_v4(&rec[t * kPrecWords + 1 + lane], make_uint4(__float_as_uint(src[0]), __float_as_uint(src[1]),
+                                                         __float_as_uint(src[2]), __float_as_uint(src[3])));
+  }
+  if (lane == 0) {
+    DF agg = DF{0.0f, 0.0f};
+    float agg_abs = 0.0f;
+    for (int k = 0; k < kWarps; k++) {
+      agg = df_add(agg, DF{us.wfs[k], 0.0f});
+      agg_abs = __fadd_rn(agg_abs, us.wfa[k]);
+    }
+    uint32_t head = 0;
+    if (t == g.t_first) {
+      // a sum's first tile: its prefix is the sum's start value (published
+      // here), and the sum it gives the scanner starts from it (flag 4)
+      const DF s0 = start_df(p, g.sum);
+      st_vol_v4(&rec[t * kPrecWords], make_uint4(__float_as_uint(s0.hi), __float_as_uint(s0.lo),
+                                                 __float_as_uint(fabsf(s0.hi)), (tag << 8) | 2u));
+      agg = df_add(s0, agg);
+      agg_abs = __fadd_rn(fabsf(s0.hi), agg_abs);
+      head = 4u;
+    }
+    st_vol_v4(&p.status[t], make_uint4(__float_as_uint(agg.hi), __float_as_uint(agg.lo), __float_as_uint(agg_abs),
+                                       (key << 16) | (tag << 8) | 1u | head));
+  }
+}
+
 // A plan unit, one warp's 32 rows (already loaded): the warp's float sums;
 // the last warp publishes the warps' sums beside the tile's prefix, and the
 // tile's sums for the scanner.  (No fence orders the two: they only steer
@@ -633,34 +687,9 @@ __device__ __forceinline__ void plan_unit(const Params &p, Smem &sm, UnitSm &us,
   last = __shfl_sync(kFull, last, 0);
   if (!last) return;
   __threadfence_block();
-  if (lane < 2 * kWarps / 4) {
-    // the warps' sums (4 floats a lane) beside the tile's prefix
-    const float *src = lane < kWarps / 4 ? &us.wfs[4 * lane] : &us.wfa[4 * (lane - kWarps / 4)];
-    st_vol_v4(&p.prec[t * kPrecWords + 1 + lane], make_uint4(__float_as_uint(src[0]), __float_as_uint(src[1]),
-                                                             __float_as_uint(src[2]), __float_as_uint(src[3])));
-  }
-  if (lane == 0) {
-    DF agg = DF{0.0f, 0.0f};
-    float agg_abs = 0.0f;
-    for (int k = 0; k < kWarps; k++) {
-      agg = df_add(agg, DF{us.wfs[k], 0.0f});
-      agg_abs = __fadd_rn(agg_abs, us.wfa[k]);
-    }
-    uint32_t head = 0;
-    if (t == g.t_first) {
-      // a sum's first tile: its prefix is the sum's start value (published
-      // here), and the sum it gives the scanner starts from it (flag 4)
-      const DF s0 = start_df(p, g.sum);
-      st_vol_v4(&p.prec[t * kPrecWords], make_uint4(__float_as_uint(s0.hi), __float_as_uint(s0.lo),
-                                                    __float_as_uint(fabsf(s0.hi)), (tag << 8) | 2u));
-      agg = df_add(s0, agg);
-      agg_abs = __fadd_rn(fabsf(s0.hi), agg_abs);
-      head = 4u;
-    }
-    st_vol_v4(&p.status[t], make_uint4(__float_as_uint(agg.hi), __float_as_uint(agg.lo), __float_as_uint(agg_abs),
-                                       (tag << 8) | 1u | head));
-  }
+  publish_plan(p, us, t, g, tag, p.prec, 0u);
 }
+
 
 // The last warp of a complex tile's run unit: the tile's items merged and
 // its header published (out of line: rare, and kept out of the units' loop).
@@ -800,16 +829,27 @@ __device__ __noinline__ void complex_merge(const Params &p, Smem &sm, UnitSm &us
 // it, bs/ba the sums of the warps before this one.
 __device__ __forceinline__ void run_unit(const Params &p, Smem &sm, UnitSm &us, int64_t t, const Geo &g,
                                          const uint64_t (&v)[kLaneTerms], uint4 pf, float bs, float ba, float wfs,
-                                         float wfa, uint32_t tag) {
+                                         float wfa, uint32_t tag, int kind) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, tid = threadIdx.x;
-  if (!((pf.w >> 8) == tag && (pf.w & 3u) == 2u)) {
+  if (kind == U_SPEC) {
+    // a planned call: the stored plan of the call before (any tag); a sum's
+    // first tile starts from this call's start value; a tile without a stored
+    // plan is planned from 0 (the scanner then sends it back)
+    if (t == g.t_first) {
+      const DF s0 = start_df(p, g.sum);
+      pf = make_uint4(__float_as_uint(s0.hi), __float_as_uint(s0.lo), __float_as_uint(fabsf(s0.hi)), 2u);
+    } else if ((pf.w & 3u) != 2u) {
+      pf = make_uint4(0, 0, 0, 2u);
+    }
+  } else if (!((pf.w >> 8) == tag && (pf.w & 3u) == 2u)) {
     // the scanner had not published the prefix when the copy ran: poll it
     const uint64_t c0 = clock64();
+    const uint4 *pr = kind == U_REDO ? p.prec_next : p.prec;
     int ok = 0;
     if (lane == 0) {
       uint64_t t0 = 0;
       for (uint32_t spin = 0;; spin++) {
-        pf = ld_vol_v4(&p.prec[t * kPrecWords]);
+        pf = ld_vol_v4(&pr[t * kPrecWords]);
         if ((pf.w >> 8) == tag && (pf.w & 3u) == 2u) {
           ok = 1;
           break;
@@ -1094,6 +1134,20 @@ __device__ __forceinline__ void run_unit(const Params &p, Smem &sm, UnitSm &us, 
       us.wcnt[w] = total;
     }
   }
+  if (kind == U_SPEC) {
+    // the next call's plan: this tile's sums, as a plan unit forms them
+    if (fbw) row_sums(v, fs, fa, mx);
+    float ws_ = fs, wa_ = fa;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ws_ = __fadd_rn(ws_, __shfl_xor_sync(kFull, ws_, o));
+      wa_ = __fadd_rn(wa_, __shfl_xor_sync(kFull, wa_, o));
+    }
+    if (lane == 0) {
+      us.wfs[w] = ws_;
+      us.wfa[w] = wa_;
+    }
+  }
   __syncwarp();
   int last = 0;
   if (lane == 0) {
@@ -1147,9 +1201,26 @@ __device__ __forceinline__ void run_unit(const Params &p, Smem &sm, UnitSm &us, 
   } else {
     complex_merge(p, sm, us, t, tag);
   }
+  if (kind == U_SPEC) {
+    // the tile's sums for the scanner: the binade of a tile of one run goes
+    // with them, so that the scanner can tell whether the new prefix keeps
+    // it.  (No fence after the header: the walk waits for the header's own
+    // tags, and a second unit of the tile waits for them before it writes.)
+    publish_plan(p, us, t, g, tag, p.prec_next, one && k0 > 0 ? (uint32_t)k0 : 0u);
+  } else if (kind == U_REDO) {
+    // the header may now be walked
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence();
+      st_release_u32(&p.conf[t], tag);
+      stat_add(sm, S_REDO, 1);
+    }
+  }
   if (lane == 0) {
     stat_add(sm, S_TILES, 1);
     stat_add(sm, S_CY_RUN, clock64() - c0);
+    const uint64_t now = gtimer();
+    if (now > sm.t_units_end) sm.t_units_end = now;
   }
 }
 
@@ -1167,7 +1238,8 @@ __device__ __noinline__ void compute_warp(const Params &p, Smem &sm, const unsig
     const int64_t t = st.tile;
     if (w == 0 && lane == 0) TL(p, sm.role, 0, u, 1);
     if (t < 0) break;
-    const bool plan = st.plan != 0;
+    const int kind = st.kind;
+    const bool plan = kind == U_PLAN;
     const Geo g = stage_geo(st);
     const int64_t row = g.row0 + threadIdx.x;
     uint64_t v[kLaneTerms];
@@ -1193,10 +1265,36 @@ __device__ __noinline__ void compute_warp(const Params &p, Smem &sm, const unsig
       plan_unit(p, sm, us, t, g, v, tag);
       if (lane == 0) stat_add(sm, S_CY_PLAN, clock64() - c0);
     } else {
-      run_unit(p, sm, us, t, g, v, pf, bs, ba, wfs, wfa, tag);
+      run_unit(p, sm, us, t, g, v, pf, bs, ba, wfs, wfa, tag, kind);
     }
     if (w == 0 && lane == 0) TL(p, sm.role, 0, u, 3);
     if (w == 0 && lane == 0) TL(p, sm.role, 0, u, 4 - (plan ? 0 : 0));
+  }
+}
+
+// A planned call's ticket for place j of the redo list: the tile the scanner
+// put there, or -1 once the list is final and shorter (bounded: -1 past the
+// limit, and the walk then gives up on that tile's header).
+__device__ __noinline__ int64_t redo_wait(const Params &p, int64_t j, uint32_t tag) {
+  // (every idle producer polls here while the scanner finishes: plain loads,
+  // far apart, so that they do not crowd the memory system)
+  const uint64_t t0 = gtimer();
+  for (uint32_t spin = 0;; spin++) {
+    const uint32_t fin = ld_relaxed_u32(&p.ctr[C_SCAN_FIN]);
+    fence_acq_rel();   // the flag read first: then the count is final
+    const uint32_t n = ld_relaxed_u32(&p.ctr[C_REDO_RES]);
+    if ((int64_t)n > j) {
+      // the place is taken: its entry lands with the call's tag
+      const uint32_t v = ld_acquire_u32(&p.redo[j]);
+      if ((v >> 24) == tag) return (int64_t)(v & 0xFFFFFFu);
+    } else if (fin) {
+      return -1;
+    }
+    if ((spin & 3u) == 3u && gtimer() - t0 > p.wait_ns) {
+      note_timeout(p, ERR_PLAN_TIMEOUT, 8, (uint32_t)j, 0);
+      return -1;
+    }
+    __nanosleep(1000);
   }
 }
 
@@ -1209,7 +1307,7 @@ __device__ __noinline__ void compute_warp(const Params &p, Smem &sm, const unsig
 __device__ __noinline__ void producer_warp(const Params &p, Smem &sm, unsigned char *stages, const CUtensorMap *tmap,
                                            int64_t ntiles) {
   if ((threadIdx.x & 31) != 0) return;
-  const int64_t nstream = (int64_t)gridDim.x - p.nwalkers - 1, units = 2 * ntiles;
+  const int64_t nstream = (int64_t)gridDim.x - p.nwalkers - 1, units = p.planned ? ntiles : 2 * ntiles;
   const bool deep = units > 2 * nstream;
   const uint32_t depth = deep ? (uint32_t)kStages : 1u;
   int64_t hand = -1;
@@ -1236,26 +1334,48 @@ __device__ __noinline__ void producer_warp(const Params &p, Smem &sm, unsigned c
       }
     }
     TL(p, sm.role, 1, u, 1);
-    int64_t k = hand >= 0 ? hand : (int64_t)atomicAdd(&p.ctr[C_TICKET], 1u);
-    const bool valid = k < units && !sm.broken;
-    TL(p, sm.role, 1, u, 2);
-    if (valid) {
-      // a run unit's copy waits for the scanner to publish its tile's prefix
-      // (bounded; past the limit the compute warps poll for it themselves)
-      bool plan = false;
-      const int64_t t = unit_of(k, ntiles, p.wave, plan);
-      if (!plan && t >= 0) {
-        const uint32_t want = (sm.tag << 8) | 2u;
-        const uint64_t t0 = gtimer();
-        for (uint32_t spin = 0; ld_relaxed_u32(&p.prec[t * kPrecWords].w) != want; spin++) {
-          if ((spin & 15u) == 15u && gtimer() - t0 > p.wait_ns) break;
-          __nanosleep(100);
-        }
-        asm volatile("fence.proxy.async.global;" ::: "memory");   // the copy reads what the load saw
+    const int64_t k = hand >= 0 ? hand : (int64_t)atomicAdd(&p.ctr[C_TICKET], 1u);
+    int64_t t = -1;
+    int kind = U_RUN;
+    if (!sm.broken) {
+      if (!p.planned) {
+        bool plan = false;
+        t = unit_of(k, ntiles, p.wave, plan);
+        kind = plan ? U_PLAN : U_RUN;
+      } else if (k < ntiles) {
+        t = k;   // a planned call: every tile on the stored plan, in order
+        kind = U_SPEC;
+      } else {
+        t = redo_wait(p, k - ntiles, sm.tag);   // then the tiles the scanner sends back
+        kind = U_REDO;
       }
     }
+    const bool valid = t >= 0;
+    TL(p, sm.role, 1, u, 2);
+    if (valid && kind == U_REDO) {
+      // the tile's first header (and items) must have landed before this
+      // unit writes its own over them (bounded)
+      const uint64_t t0 = gtimer();
+      for (uint32_t spin = 0; !tags_ok(ld_rec_vol(&p.hdr[t]), sm.tag); spin++) {
+        if ((spin & 15u) == 15u && gtimer() - t0 > p.wait_ns) break;
+        __nanosleep(100);
+      }
+      fence_acq_rel();
+    }
+    if (valid && (kind == U_RUN || kind == U_REDO)) {
+      // a run unit's copy waits for the scanner to publish its tile's prefix
+      // (bounded; past the limit the compute warps poll for it themselves)
+      const uint4 *pr = kind == U_REDO ? p.prec_next : p.prec;
+      const uint32_t want = (sm.tag << 8) | 2u;
+      const uint64_t t0 = gtimer();
+      for (uint32_t spin = 0; ld_relaxed_u32(&pr[t * kPrecWords].w) != want; spin++) {
+        if ((spin & 15u) == 15u && gtimer() - t0 > p.wait_ns) break;
+        __nanosleep(100);
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");   // the copy reads what the load saw
+    }
     sm.us[u % kUnitSlots].done_cnt = 0;
-    stage_fill(p, sm, stages, tmap, s, valid ? k : -1, ntiles, hint);
+    stage_fill(p, sm, stages, tmap, s, t, kind, hint);
     TL(p, sm.role, 1, u, 3);
 #ifdef SEQSUM_PROFILE
     if (sm.role - p.nwalkers - 1 >= 0 && sm.role - p.nwalkers - 1 < 4 && u < 96)
@@ -1274,6 +1394,7 @@ __device__ __noinline__ void stream_cta(const Params &p, Smem &sm, unsigned char
   if (tid == 0) {
     sm.broken = 0;
     sm.t_stream_end = 0;
+    sm.t_units_end = 0;
     for (int s = 0; s < kStages; s++) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kWarps);
@@ -1284,7 +1405,142 @@ __device__ __noinline__ void stream_cta(const Params &p, Smem &sm, unsigned char
   if ((tid >> 5) < kWarps) compute_warp(p, sm, stages);
   else producer_warp(p, sm, stages, tmap, ntiles);
   __syncthreads();
-  if (tid == 0) sm.t_stream_end = gtimer();   // this CTA's last header is published
+  if (tid == 0) {
+    sm.t_stream_end = gtimer();   // this CTA's last header is published
+    if (sm.t_units_end) atomicMax(&p.stats[S_T_UNITS_END], (unsigned long long)sm.t_units_end);
+  }
+}
+
+// A planned call: whether the header that tile t's unit formed on the stored
+// plan serves as well as one formed on the new prefix (e, ea).  A tile of one
+// run in binade `key` (carried with its sums in s) keeps it while the tile's
+// whole range of partial sums, with twice the allowance the units take, stays
+// in that binade; a tile of zeros always keeps it (plan_range_holds, inline:
+// the scanner's next loads stay in flight).  Any other tile keeps it when its
+// warps' sums are, word for word, the new ones and its stored prefix is
+// within 2^-36 of the magnitudes of the new one (the prefix of magnitudes,
+// which only sizes the allowance, within 2^-20): far inside the allowance of
+// 2^-21 that its rows' binades were chosen with (plan_words_hold; the
+// scanner's sums round a little differently from call to call, as its rounds
+// fall).  A wrong answer costs time, never bits: the walk checks every run
+// against the exact sum.
+__device__ __forceinline__ bool plan_range_holds(DF e, float ea, uint4 s) {
+  if (s.z == 0u && (s.x << 1) == 0u && (s.y << 1) == 0u) return true;   // zeros add nothing
+  const uint32_t key = (s.w >> 16) & 0x7FFu;
+  if (key == 0) return false;
+  const float fs = __fadd_rn(__uint_as_float(s.x), __uint_as_float(s.y)), fa = __uint_as_float(s.z);
+  const float P = __fadd_rn(e.hi, e.lo);
+  const float m = __fadd_rn(__fmul_rn(__fadd_rn(ea, fa), 9.5367431640625e-7f /* 2^-20 */), 1e-30f);
+  const float pos = __fmul_rn(0.5f, __fadd_rn(fa, fs)), neg = __fmul_rn(0.5f, __fsub_rn(fa, fs));
+  const float lo = __fsub_rn(__fsub_rn(P, neg), m), hi = __fadd_rn(__fadd_rn(P, pos), m);
+  const bool up = lo > 0.0f;
+  if (!up && !(hi < 0.0f)) return false;
+  const int a = float_binade(up ? lo : -hi), b = float_binade(up ? hi : -lo);
+  return a == b && a >= 1 && a <= 254 && (uint32_t)(a - 127 + 1023) == key;
+}
+__device__ __noinline__ bool plan_words_hold(const Params &p, int64_t t, DF e, float ea, uint4 s) {
+  // (every word at once: one round trip)
+  uint4 o, a[kPrecWords - 1], b[kPrecWords - 1];
+  o = ld_vol_v4(&p.prec[t * kPrecWords]);
+#pragma unroll
+  for (int q = 1; q < kPrecWords; q++) {
+    a[q - 1] = ld_vol_v4(&p.prec[t * kPrecWords + q]);
+    b[q - 1] = ld_vol_v4(&p.prec_next[t * kPrecWords + q]);
+  }
+  if ((o.w & 3u) != 2u) return false;
+  const float A = __fadd_rn(ea, __uint_as_float(s.z));
+  const float d = __fadd_rn(__fsub_rn(e.hi, __uint_as_float(o.x)), __fsub_rn(e.lo, __uint_as_float(o.y)));
+  if (!(fabsf(d) <= __fmul_rn(A, 1.4551915228366852e-11f /* 2^-36 */) &&
+        fabsf(__fsub_rn(ea, __uint_as_float(o.z))) <= __fmul_rn(A, 9.5367431640625e-7f /* 2^-20 */)))
+    return false;
+  bool same = true;
+#pragma unroll
+  for (int q = 0; q < kPrecWords - 1; q++)
+    same = same && a[q].x == b[q].x && a[q].y == b[q].y && a[q].z == b[q].z && a[q].w == b[q].w;
+  return same;
+}
+
+// A planned call, a sum's first tile: its prefix is this call's start value
+// (which its unit wrote beside the new plan), its own sums those in s less
+// that value.
+__device__ __noinline__ bool plan_holds_head(const Params &p, int64_t t, uint4 s) {
+  const uint4 h = ld_vol_v4(&p.prec_next[t * kPrecWords]);
+  const DF e = DF{__uint_as_float(h.x), __uint_as_float(h.y)};
+  const float ea = __uint_as_float(h.z);
+  const float fs = __fadd_rn(__fsub_rn(__uint_as_float(s.x), e.hi), __fsub_rn(__uint_as_float(s.y), e.lo));
+  const float fa = fmaxf(__fsub_rn(__uint_as_float(s.z), ea), 0.0f);
+  const uint4 own = make_uint4(__float_as_uint(fs), 0u, __float_as_uint(fa), s.w);
+  return plan_range_holds(e, ea, own) || plan_words_hold(p, t, e, ea, own);
+}
+
+constexpr int kRingSlots = 16;
+
+// A planned call's checker warps (warps 1-8 of the scanner's CTA): each
+// round the scanning warp hands over (its first tile and count in a ring of
+// kRingSlots), a tile a lane -- does the header formed on the stored plan
+// stand, given the tile's sums and the new prefix the scanning warp has just
+// written?  Then the walk may take it; otherwise the tile goes on the redo
+// list (places taken by one atomic a warp; each entry carries the call's
+// tag, so a reader knows it landed).
+__device__ __noinline__ void scan_check(const Params &p, Smem &sm) {
+  const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) - 1;
+  const uint32_t tag = sm.tag;
+  volatile int *pub = &sm.ring_pub, *end = &sm.ring_end;
+  for (int r = 0;; r++) {
+    int state = 0;   // 1: round r is in the ring; 2: no more rounds
+    if (lane == 0) {
+      const uint64_t t0 = gtimer();
+      for (uint32_t spin = 0;; spin++) {
+        if (*pub > r) {
+          state = 1;
+          break;
+        }
+        const int e = *end;
+        if (e >= 0 && e <= r) {
+          state = 2;
+          break;
+        }
+        if ((spin & 255u) == 255u && gtimer() - t0 > p.wait_ns) {
+          note_timeout(p, ERR_PLAN_TIMEOUT, 9, (uint32_t)r, 0);
+          state = 2;
+          break;
+        }
+        __nanosleep(256);   // (the scanning warp shares the SM: poll gently)
+      }
+    }
+    state = __shfl_sync(kFull, state, 0);
+    if (state == 2) break;
+    __threadfence_block();
+    const int slot = r % kRingSlots;   // (the round's first tile and count)
+    const int n = ((volatile int *)sm.ring_n)[slot];
+    const int64_t pos = ((volatile int64_t *)sm.ring_pos)[slot];
+    const int i = 32 * w + lane;
+    bool redo = false;
+    int64_t t = -1;
+    if (i < n) {
+      t = pos + i;
+      const uint4 s = ld_vol_v4(&p.status[t]), h = ld_vol_v4(&p.prec_next[t * kPrecWords]);
+      const DF e = DF{__uint_as_float(h.x), __uint_as_float(h.y)};
+      const float ea = __uint_as_float(h.z);
+      const bool holds = (s.w & 4u) ? plan_holds_head(p, t, s)
+                                     : (plan_range_holds(e, ea, s) || plan_words_hold(p, t, e, ea, s));
+      if (holds) st_relaxed_u32(&p.conf[t], tag);   // the walk still waits for the header's own tags
+      else redo = true;
+    }
+    const uint32_t m = __ballot_sync(kFull, redo);
+    if (m) {
+      uint32_t base = 0;
+      if (lane == 0) base = atomicAdd(&p.ctr[C_REDO_RES], (uint32_t)__popc(m));
+      base = __shfl_sync(kFull, base, 0);
+      if (redo) st_release_u32(&p.redo[base + __popc(m & ((1u << lane) - 1u))], (tag << 24) | (uint32_t)t);
+      __threadfence();   // the places taken before the round is reported done
+    }
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      ((volatile int *)sm.chk_done)[w] = r + 1;
+    }
+  }
 }
 
 // The scanner: the tiles' sums, in order as their plan units publish them,
@@ -1293,9 +1549,16 @@ __device__ __noinline__ void stream_cta(const Params &p, Smem &sm, unsigned char
 // One warp, no barriers: 256 tiles a round (eight consecutive ones a lane,
 // summed in the lane, then a warp scan), the next round's sums loading while
 // this one is scanned.  The round takes the tiles published so far, up to the
-// first that is not.
+// first that is not.  In a planned call (kPlanned) it also tells, tile by
+// tile, whether the header formed on the stored plan stands (plan_range_holds,
+// plan_words_hold) and
+// releases it to the walk, or sends the tile back to the streaming CTAs.
+template <bool kPlanned>
 __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles) {
-  if (threadIdx.x >= 32) return;
+  if (threadIdx.x >= 32) {
+    if (kPlanned && threadIdx.x < 32 * (kWarps + 1)) scan_check(p, sm);
+    return;
+  }
   const int lane = threadIdx.x;
   const uint32_t tag = sm.tag;
   constexpr int kPer = 8, kRound = 32 * kPer;
@@ -1303,6 +1566,7 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
   float carry_abs = 0.0f;
   int64_t pos = 0;
   uint64_t t_wait = 0;
+  int round = 0;               // a planned call: rounds handed to the checkers
   uint4 vn[kPer];
 #pragma unroll
   for (int j = 0; j < kPer; j++)
@@ -1314,7 +1578,7 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
 #pragma unroll
     for (int j = kPer - 1; j >= 0; j--) {
       v[j] = vn[j];
-      const bool rd = (v[j].w >> 8) == tag && (v[j].w & 3u) == 1u;
+      const bool rd = ((v[j].w >> 8) & 0xFFu) == tag && (v[j].w & 3u) == 1u;
       if (t0 + j < ntiles && !rd) my_first = kPer * lane + j;
     }
     const int nready = (int)min((int64_t)__reduce_min_sync(kFull, (uint32_t)my_first), ntiles - pos);
@@ -1423,14 +1687,36 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
             e = df_add(before, loc[j - 1]);
             ea = __fadd_rn(before_a, loca[j - 1]);
           }
-          st_vol_v4(&p.prec[(t0 + j) * kPrecWords], make_uint4(__float_as_uint(e.hi), __float_as_uint(e.lo),
-                                                               __float_as_uint(ea), (tag << 8) | 2u));
+          st_vol_v4(&(kPlanned ? p.prec_next : p.prec)[(t0 + j) * kPrecWords],
+                    make_uint4(__float_as_uint(e.hi), __float_as_uint(e.lo), __float_as_uint(ea), (tag << 8) | 2u));
         }
         if (kPer * lane + j == nready - 1) {
           lastv = hup[j] ? loc[j] : df_add(before, loc[j]);
           lasta = hup[j] ? loca[j] : __fadd_rn(before_a, loca[j]);
         }
       }
+    }
+    if (kPlanned) {
+      // the round to the checkers, once the ring has room (bounded: past the
+      // limit the round is dropped, and the walk gives up on its tiles)
+      __syncwarp();
+      if (lane == 0) {
+        const uint64_t tw = gtimer();
+        bool room = round < kRingSlots;
+        for (uint32_t spin = 0; !room; spin++) {
+          room = true;
+          for (int k = 0; k < kWarps; k++) room = room && ((volatile int *)sm.chk_done)[k] > round - kRingSlots;
+          if (!room && (spin & 255u) == 255u && gtimer() - tw > p.wait_ns) break;
+        }
+        if (room) {
+          ((volatile int64_t *)sm.ring_pos)[round % kRingSlots] = pos;
+          ((volatile int *)sm.ring_n)[round % kRingSlots] = nready;
+          __threadfence_block();
+          *(volatile int *)&sm.ring_pub = round + 1;
+          round++;
+        }
+      }
+      round = __shfl_sync(kFull, round, 0);
     }
     // the carry into the next round: the inclusive prefix of the last tile
     const int src = (nready - 1) / kPer;
@@ -1440,6 +1726,24 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
     if (lane == 0) stat_add(sm, S_SCAN_WINDOWS, 1);
     pos += nready;
   }
+
+  if (kPlanned) {
+    // no more rounds; once every checker is done, the redo list is final
+    // (also when the scanner gave up; bounded)
+    if (lane == 0) {
+      *(volatile int *)&sm.ring_end = round;
+      const uint64_t tw = gtimer();
+      bool done = false;
+      for (uint32_t spin = 0; !done; spin++) {
+        done = true;
+        for (int k = 0; k < kWarps; k++) done = done && ((volatile int *)sm.chk_done)[k] >= round;
+        if (!done && (spin & 255u) == 255u && gtimer() - tw > p.wait_ns) break;
+      }
+      __threadfence();
+      st_release_u32(&p.ctr[C_SCAN_FIN], 1u);
+    }
+  }
+  if (lane == 0) p.stats[S_T_SCAN_END] = gtimer();
 }
 
 // ------------------------------------------------------------------ the walk: raw terms
@@ -1843,8 +2147,12 @@ __device__ __noinline__ void walk_producer(const Params &p, Smem &sm, RangeSlot 
 #pragma unroll
       for (int j = 0; j < 4; j++) {
         if (need & (1u << j)) {
-          h[j] = ld_rec_vol(&p.hdr[ta + 4 * lane + j]);
-          if (tags_ok(h[j], tag)) need &= ~(1u << j);
+          // (a planned call: once the scanner, or the tile's second unit, has released it)
+          const int64_t tj = ta + 4 * lane + j;
+          if (!p.planned || ld_acquire_u32(&p.conf[tj]) == tag) {
+            h[j] = ld_rec_vol(&p.hdr[tj]);
+            if (tags_ok(h[j], tag)) need &= ~(1u << j);
+          }
         }
       }
       if (__all_sync(kFull, need == 0u)) break;
@@ -2294,17 +2602,22 @@ __global__ void __launch_bounds__(kBlockThreads, 2) seqsum_kernel(const Params p
   const int tid = threadIdx.x;
   for (int i = tid; i < kBlockWarps * S_ACCUM_END; i += kBlockThreads) (&sm.stat[0][0])[i] = 0;
   if (tid == 0) {
+    sm.ring_pub = 0;
+    sm.ring_end = -1;
+    for (int k = 0; k < kWarps; k++) sm.chk_done[k] = 0;
     sm.role = (int)atomicAdd(&p.ctr[C_ROLE], 1u);
     uint32_t smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
     // the walker and the scanner are latency-bound: a streaming CTA that finds
     // itself on their SM leaves it to them.  Both roles are taken by CTAs
     // already running, which write their SM right after taking the role; a
-    // streaming CTA waits for both words (bounded: past the limit it streams)
+    // streaming CTA waits for both words (bounded: past the limit it streams).
+    // (A small grid keeps every CTA streaming: there the others may be too few.)
     if (sm.role == 0) atomicExch(&p.ctr[C_WALK_SM], smid + 1);
     if (sm.role == p.nwalkers) atomicExch(&p.ctr[C_SCAN_SM], smid + 1);
+
     sm.alone = 0;
-    if (sm.role > p.nwalkers) {
+    if (sm.role > p.nwalkers && gridDim.x >= 64) {
       uint32_t ws = 0, ss = 0;
       const uint64_t t0 = gtimer();
       for (;;) {
@@ -2342,7 +2655,8 @@ __global__ void __launch_bounds__(kBlockThreads, 2) seqsum_kernel(const Params p
       walk_loop(p, sm, dyn, ntiles);
       if (tid == 0) atomicMax(&p.stats[S_T_WALK_END], (unsigned long long)gtimer());
     } else if (sm.role == p.nwalkers) {
-      scan_cta(p, sm, ntiles);
+      if (p.planned) scan_cta<true>(p, sm, ntiles);
+      else scan_cta<false>(p, sm, ntiles);
     } else if (!sm.alone) {
       stream_cta(p, sm, dyn, &tmap, ntiles);
       if (tid == 0 && sm.t_stream_end) atomicMax(&p.stats[S_T_STREAM_END], (unsigned long long)sm.t_stream_end);
@@ -2369,7 +2683,9 @@ __global__ void __launch_bounds__(kBlockThreads, 2) seqsum_kernel(const Params p
     if (next > 255u) {
       for (int64_t i = tid; i < p.cap_tiles; i += kBlockThreads) {
         p.status[i] = make_uint4(0, 0, 0, 0);
-        p.prec[i * kPrecWords] = make_uint4(0, 0, 0, 0);
+        p.prec_ws[i * kPrecWords] = make_uint4(0, 0, 0, 0);
+        if (p.conf) p.conf[i] = 0;
+        if (p.redo) p.redo[i] = 0;
         Rec z;
         z.w[0] = z.w[1] = z.w[2] = z.w[3] = 0;
         st_rec(&p.hdr[i], z);
@@ -2383,6 +2699,8 @@ __global__ void __launch_bounds__(kBlockThreads, 2) seqsum_kernel(const Params p
       p.ctr[C_SUMTICKET] = 0;
       p.ctr[C_WALK_SM] = 0;
       p.ctr[C_SCAN_SM] = 0;
+      p.ctr[C_REDO_RES] = 0;
+      p.ctr[C_SCAN_FIN] = 0;
       p.ctr[C_EPOCH] = next > 255u ? 1u : next;
       __threadfence();
       p.ctr[C_EXIT] = 0;

@@ -138,6 +138,7 @@ extern "C" int seqsum_f64_static(const double *x, int64_t n, double s0, double *
   p.nsums = 1;
   p.status = d.status;
   p.prec = d.prec;
+  p.prec_ws = d.prec;
   p.wave = 2048;
   p.hdr = d.hdr;
   p.items = d.items;

@@ -57,6 +57,19 @@ def test_argument_errors_need_no_gpu(libpath):
     lib.seqsum_f64_batched.argtypes = [ctypes.c_void_p] * 2 + [ctypes.c_int32] + [ctypes.c_void_p] * 3
     assert lib.seqsum_f64_batched(None, None, -1, None, None, None) == -1
     assert lib.seqsum_f64_batched(None, None, 0, None, None, None) == 0
+    # a plan is host state until its first call; bad arguments are refused first
+    lib.seqsum_plan_create.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+    lib.seqsum_plan_destroy.argtypes = [ctypes.c_void_p]
+    lib.seqsum_f64_planned.argtypes = [ctypes.c_void_p] * 2 + [ctypes.c_int64, ctypes.c_double] + [ctypes.c_void_p] * 2
+    assert lib.seqsum_plan_create(None) == -1
+    h = ctypes.c_void_p()
+    assert lib.seqsum_plan_create(ctypes.byref(h)) == 0 and h.value
+    assert lib.seqsum_f64_planned(None, None, 0, 0.0, ctypes.c_void_p(8), None) == -1
+    assert lib.seqsum_f64_planned(h, None, 5, 0.0, ctypes.c_void_p(8), None) == -1
+    assert lib.seqsum_f64_planned(h, None, -1, 0.0, ctypes.c_void_p(8), None) == -1
+    assert lib.seqsum_f64_planned(h, None, 0, 0.0, None, None) == -1
+    lib.seqsum_plan_destroy(h)
+    lib.seqsum_plan_destroy(None)
 
 
 def test_device_code_is_built_strict_fp():
