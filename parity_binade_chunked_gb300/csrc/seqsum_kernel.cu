@@ -339,12 +339,11 @@ struct Smem {
   uint32_t prof_n;                   // profiling builds: walk steps logged
   uint64_t t_stream_end;
   uint64_t t_units_end;              // a streaming CTA: when its latest unit's header was published
-  // the scanner's CTA in a planned call: the rounds handed to the checker warps
-  int64_t ring_pos[16];              // a ring slot's first tile
-  int ring_n[16];                    // ... and its tiles
-  int ring_pub;                      // rounds in the ring so far
-  int ring_end;                      // -1, then the number of rounds once the scan is over
-  int chk_done[kWarps];              // rounds each checker warp has finished
+  // the scanner's warps: each one's first unpublished tile of the round
+  // (two buffers, by iteration), their totals, and the give-up flag
+  int scan_first[2][kWarps];
+  float4 scan_tot[kWarps];
+  int scan_stop;
   // the walk's slots: handed over by mbarriers, their uses counted on each side
   uint64_t wfull[kWarps];
   uint64_t wempty[kWarps];
@@ -1473,173 +1472,93 @@ __device__ __noinline__ bool plan_holds_head(const Params &p, int64_t t, uint4 s
   return plan_range_holds(e, ea, own) || plan_words_hold(p, t, e, ea, own);
 }
 
-constexpr int kRingSlots = 16;
-
-// A planned call's checker warps (warps 1-8 of the scanner's CTA): each
-// round the scanning warp hands over (its first tile and count in a ring of
-// kRingSlots), a tile a lane -- does the header formed on the stored plan
-// stand, given the tile's sums and the new prefix the scanning warp has just
-// written?  Then the walk may take it; otherwise the tile goes on the redo
-// list (places taken by one atomic a warp; each entry carries the call's
-// tag, so a reader knows it landed).
-__device__ __noinline__ void scan_check(const Params &p, Smem &sm) {
-  const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) - 1;
-  const uint32_t tag = sm.tag;
-  volatile int *pub = &sm.ring_pub, *end = &sm.ring_end;
-  for (int r = 0;; r++) {
-    int state = 0;   // 1: round r is in the ring; 2: no more rounds
-    if (lane == 0) {
-      const uint64_t t0 = gtimer();
-      for (uint32_t spin = 0;; spin++) {
-        if (*pub > r) {
-          state = 1;
-          break;
-        }
-        const int e = *end;
-        if (e >= 0 && e <= r) {
-          state = 2;
-          break;
-        }
-        if ((spin & 255u) == 255u && gtimer() - t0 > p.wait_ns) {
-          note_timeout(p, ERR_PLAN_TIMEOUT, 9, (uint32_t)r, 0);
-          state = 2;
-          break;
-        }
-        __nanosleep(256);   // (the scanning warp shares the SM: poll gently)
-      }
-    }
-    state = __shfl_sync(kFull, state, 0);
-    if (state == 2) break;
-    __threadfence_block();
-    const int slot = r % kRingSlots;   // (the round's first tile and count)
-    const int n = ((volatile int *)sm.ring_n)[slot];
-    const int64_t pos = ((volatile int64_t *)sm.ring_pos)[slot];
-    const int i = 32 * w + lane;
-    bool redo = false;
-    int64_t t = -1;
-    if (i < n) {
-      t = pos + i;
-      const uint4 s = ld_vol_v4(&p.status[t]), h = ld_vol_v4(&p.prec_next[t * kPrecWords]);
-      const DF e = DF{__uint_as_float(h.x), __uint_as_float(h.y)};
-      const float ea = __uint_as_float(h.z);
-      const bool holds = (s.w & 4u) ? plan_holds_head(p, t, s)
-                                     : (plan_range_holds(e, ea, s) || plan_words_hold(p, t, e, ea, s));
-      if (holds) st_relaxed_u32(&p.conf[t], tag);   // the walk still waits for the header's own tags
-      else redo = true;
-    }
-    const uint32_t m = __ballot_sync(kFull, redo);
-    if (m) {
-      uint32_t base = 0;
-      if (lane == 0) base = atomicAdd(&p.ctr[C_REDO_RES], (uint32_t)__popc(m));
-      base = __shfl_sync(kFull, base, 0);
-      if (redo) st_release_u32(&p.redo[base + __popc(m & ((1u << lane) - 1u))], (tag << 24) | (uint32_t)t);
-      __threadfence();   // the places taken before the round is reported done
-    }
-    __syncwarp();
-    if (lane == 0) {
-      __threadfence_block();
-      ((volatile int *)sm.chk_done)[w] = r + 1;
-    }
+// A planned call, in the scanner: tile t's header, formed on the stored plan,
+// stands (the walk may take it: its release word gets the call's tag) or the
+// tile goes on the redo list (one atomic a warp for the places; each entry
+// carries the call's tag, so that a reader knows it landed).
+__device__ __forceinline__ void scan_release(const Params &p, int64_t t, bool in, bool head, DF e, float ea, uint4 v,
+                                             uint32_t tag) {
+  const int lane = threadIdx.x & 31;
+  bool redo = false;
+  if (in) {
+    const bool holds = head ? plan_holds_head(p, t, v)
+                            : (plan_range_holds(e, ea, v) || plan_words_hold(p, t, e, ea, v));
+    if (holds) st_relaxed_u32(&p.conf[t], tag);   // the walk still waits for the header's own tags
+    else redo = true;
+  }
+  const uint32_t m = __ballot_sync(kFull, redo);
+  if (m) {
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(&p.ctr[C_REDO_RES], (uint32_t)__popc(m));
+    base = __shfl_sync(kFull, base, 0);
+    if (redo) st_release_u32(&p.redo[base + __popc(m & ((1u << lane) - 1u))], (tag << 24) | (uint32_t)t);
   }
 }
 
-// The scanner: the tiles' sums, in order as their plan units publish them,
-// into each tile's exclusive prefix (double-float; a sum's first tile starts
-// from the sum's start value, which its plan unit has added and published).
-// One warp, no barriers: 256 tiles a round (eight consecutive ones a lane,
-// summed in the lane, then a warp scan), the next round's sums loading while
-// this one is scanned.  The round takes the tiles published so far, up to the
-// first that is not.  In a planned call (kPlanned) it also tells, tile by
-// tile, whether the header formed on the stored plan stands (plan_range_holds,
-// plan_words_hold) and
-// releases it to the walk, or sends the tile back to the streaming CTAs.
+__device__ __forceinline__ void scan_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+
+// The scanner: the tiles' sums, in order as their units publish them, into
+// each tile's exclusive prefix (double-float; a sum's first tile starts from
+// the sum's start value, which its unit has added and published).  Warps 0-7,
+// one tile a thread: a round takes the 256 tiles from pos, up to the first
+// that is not published; each warp scans its 32 (segmented at a sum's first
+// tile), the warps' totals meet in shared memory (two named barriers a
+// round), and every thread publishes its tile's prefix; the next round's sums
+// are loaded while this one is scanned.  In a planned call (kPlanned) each
+// thread also tells whether its tile's header stands (scan_release).
 template <bool kPlanned>
 __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles) {
-  if (threadIdx.x >= 32) {
-    if (kPlanned && threadIdx.x < 32 * (kWarps + 1)) scan_check(p, sm);
-    return;
-  }
-  const int lane = threadIdx.x;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (w >= kWarps) return;
   const uint32_t tag = sm.tag;
-  constexpr int kPer = 8, kRound = 32 * kPer;
+  constexpr int kRound = kThreads;
+  uint4 *const pout = kPlanned ? p.prec_next : p.prec;
   DF carry = DF{0.0f, 0.0f};   // the inclusive prefix of the tile before pos
   float carry_abs = 0.0f;
   int64_t pos = 0;
   uint64_t t_wait = 0;
-  int round = 0;               // a planned call: rounds handed to the checkers
-  uint4 vn[kPer];
-#pragma unroll
-  for (int j = 0; j < kPer; j++)
-    vn[j] = (kPer * lane + j < ntiles) ? ld_vol_v4(&p.status[kPer * lane + j]) : make_uint4(0, 0, 0, 0);
+  int stop = 0;                // warp 0, lane 0: the scan gives up (bounded wait)
+  uint32_t it = 0;             // iterations: the parity picks the buffer of first-unready indices
+  uint4 v = threadIdx.x < ntiles ? ld_vol_v4(&p.status[threadIdx.x]) : make_uint4(0, 0, 0, 0);
   while (pos < ntiles) {
-    const int64_t t0 = pos + kPer * lane;
-    uint4 v[kPer];
-    int my_first = kRound;
+    const int i = threadIdx.x;   // this thread's tile: pos + i
+    const bool in = pos + i < ntiles;
+    const bool rd = ((v.w >> 8) & 0xFFu) == tag && (v.w & 3u) == 1u;
+    const uint32_t nrm = __ballot_sync(kFull, in && !rd);
+    const int wfirst = nrm ? 32 * w + __ffs(nrm) - 1 : kRound;   // (a warp all published does not bound the round)
+    if (lane == 0) sm.scan_first[it & 1][w] = wfirst;
+    if (w == 0 && lane == 0) sm.scan_stop = stop;
+    scan_bar();
+    if (sm.scan_stop) break;
+    int nready = kRound;
 #pragma unroll
-    for (int j = kPer - 1; j >= 0; j--) {
-      v[j] = vn[j];
-      const bool rd = ((v[j].w >> 8) & 0xFFu) == tag && (v[j].w & 3u) == 1u;
-      if (t0 + j < ntiles && !rd) my_first = kPer * lane + j;
-    }
-    const int nready = (int)min((int64_t)__reduce_min_sync(kFull, (uint32_t)my_first), ntiles - pos);
+    for (int k = 0; k < kWarps; k++) nready = min(nready, sm.scan_first[it & 1][k]);
+    nready = (int)min((int64_t)nready, ntiles - pos);
+    it++;
     if (nready == 0) {
       // nothing new yet (bounded: past the limit the run units give up on their prefixes too)
-      int giveup = 0;
-      if (lane == 0) {
+      if (w == 0 && lane == 0) {
         stat_add(sm, S_SCAN_POLLS, 1);
         if (!t_wait) t_wait = gtimer();
         else if (gtimer() - t_wait > p.wait_ns) {
           note_timeout(p, ERR_PLAN_TIMEOUT, 6, (uint32_t)pos, 0);
-          giveup = 1;
+          stop = 1;
         }
       }
-      if (__shfl_sync(kFull, giveup, 0)) break;
       __nanosleep(128);
-#pragma unroll
-      for (int j = 0; j < kPer; j++)
-        vn[j] = (t0 + j < ntiles) ? ld_vol_v4(&p.status[t0 + j]) : make_uint4(0, 0, 0, 0);
+      v = in ? ld_vol_v4(&p.status[pos + i]) : make_uint4(0, 0, 0, 0);
       continue;
     }
     t_wait = 0;
-    {
-      // the next round's sums, in flight while this one is scanned
-      const int64_t tn0 = pos + nready + kPer * lane;
-#pragma unroll
-      for (int j = 0; j < kPer; j++)
-        vn[j] = (tn0 + j < ntiles) ? ld_vol_v4(&p.status[tn0 + j]) : make_uint4(0, 0, 0, 0);
-    }
-    // the lane's tiles in order: loc[j] the inclusive sum from the lane's
-    // first tile, or from the last sum start among them (hup[j])
-    DF loc[kPer];
-    float loca[kPer];
-    bool hd[kPer], hup[kPer];
-    DF acc = DF{0.0f, 0.0f};
-    float acca = 0.0f;
-    bool seen = false;
-#pragma unroll
-    for (int j = 0; j < kPer; j++) {
-      hd[j] = false;
-      if (kPer * lane + j < nready) {
-        const DF a = DF{__uint_as_float(v[j].x), __uint_as_float(v[j].y)};
-        const float aa = __uint_as_float(v[j].z);
-        if (v[j].w & 4u) {
-          hd[j] = true;
-          acc = a;
-          acca = aa;
-          seen = true;
-        } else {
-          acc = df_add(acc, a);
-          acca = __fadd_rn(acca, aa);
-        }
-      }
-      loc[j] = acc;
-      loca[j] = acca;
-      hup[j] = seen;
-    }
-    // segmented scan of the lanes' totals
-    DF x = acc;
-    float xa = acca;
-    bool hx = seen;
+    const bool mine = i < nready;
+    const uint4 cur = v;
+    // the next round's sums, in flight while this one is scanned
+    v = pos + nready + i < ntiles ? ld_vol_v4(&p.status[pos + nready + i]) : make_uint4(0, 0, 0, 0);
+    // the warp's segmented inclusive scan (a sum's first tile, flag 4, restarts it)
+    const bool hd = mine && (cur.w & 4u) != 0u;
+    DF x = mine ? DF{__uint_as_float(cur.x), __uint_as_float(cur.y)} : DF{0.0f, 0.0f};
+    float xa = mine ? __uint_as_float(cur.z) : 0.0f;
+    bool hx = hd;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       DF y;
@@ -1655,95 +1574,66 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
         hx = hx || hy;
       }
     }
-    // the inclusive prefix just before this lane's first tile
-    DF before;
-    before.hi = __shfl_up_sync(kFull, x.hi, 1);
-    before.lo = __shfl_up_sync(kFull, x.lo, 1);
-    float before_a = __shfl_up_sync(kFull, xa, 1);
-    const bool hb = __shfl_up_sync(kFull, hx, 1);
-    if (lane == 0) {
-      before = carry;
-      before_a = carry_abs;
-    } else if (!hb) {
-      before = df_add(carry, before);
-      before_a = __fadd_rn(carry_abs, before_a);
+    if (lane == 31) {
+      sm.scan_tot[w] = make_float4(x.hi, x.lo, xa, hx ? 1.0f : 0.0f);
     }
-    // each tile's exclusive prefix (a sum's first tile has its own already)
-    DF lastv = DF{0.0f, 0.0f};
-    float lasta = 0.0f;
+    scan_bar();
+    // the prefix before this warp's tiles, and the carry into the next round
+    DF base = carry;
+    float base_a = carry_abs;
 #pragma unroll
-    for (int j = 0; j < kPer; j++) {
-      if (kPer * lane + j < nready) {
-        if (!hd[j]) {
-          DF e;
-          float ea;
-          if (j == 0) {
-            e = before;
-            ea = before_a;
-          } else if (hup[j - 1]) {
-            e = loc[j - 1];
-            ea = loca[j - 1];
+    for (int k = 0; k < kWarps; k++) {
+      const float4 tk = sm.scan_tot[k];
+      DF nb;
+      float na;
+      if (tk.w != 0.0f) {
+        nb = DF{tk.x, tk.y};
+        na = tk.z;
+      } else {
+        nb = df_add(base, DF{tk.x, tk.y});
+        na = __fadd_rn(base_a, tk.z);
+      }
+      if (k == w) {
+        // this warp: each tile's exclusive prefix from the lane before it
+        DF y;
+        y.hi = __shfl_up_sync(kFull, x.hi, 1);
+        y.lo = __shfl_up_sync(kFull, x.lo, 1);
+        const float ya = __shfl_up_sync(kFull, xa, 1);
+        const bool hy = __shfl_up_sync(kFull, hx, 1);
+        DF e = base;
+        float ea = base_a;
+        if (lane > 0) {
+          if (hy) {
+            e = y;
+            ea = ya;
           } else {
-            e = df_add(before, loc[j - 1]);
-            ea = __fadd_rn(before_a, loca[j - 1]);
+            e = df_add(base, y);
+            ea = __fadd_rn(base_a, ya);
           }
-          st_vol_v4(&(kPlanned ? p.prec_next : p.prec)[(t0 + j) * kPrecWords],
+        }
+        if (mine && !hd)
+          st_vol_v4(&pout[(pos + i) * kPrecWords],
                     make_uint4(__float_as_uint(e.hi), __float_as_uint(e.lo), __float_as_uint(ea), (tag << 8) | 2u));
-        }
-        if (kPer * lane + j == nready - 1) {
-          lastv = hup[j] ? loc[j] : df_add(before, loc[j]);
-          lasta = hup[j] ? loca[j] : __fadd_rn(before_a, loca[j]);
-        }
+        if (kPlanned) scan_release(p, pos + i, mine, hd, e, ea, cur, tag);
       }
+      base = nb;
+      base_a = na;
     }
-    if (kPlanned) {
-      // the round to the checkers, once the ring has room (bounded: past the
-      // limit the round is dropped, and the walk gives up on its tiles)
-      __syncwarp();
-      if (lane == 0) {
-        const uint64_t tw = gtimer();
-        bool room = round < kRingSlots;
-        for (uint32_t spin = 0; !room; spin++) {
-          room = true;
-          for (int k = 0; k < kWarps; k++) room = room && ((volatile int *)sm.chk_done)[k] > round - kRingSlots;
-          if (!room && (spin & 255u) == 255u && gtimer() - tw > p.wait_ns) break;
-        }
-        if (room) {
-          ((volatile int64_t *)sm.ring_pos)[round % kRingSlots] = pos;
-          ((volatile int *)sm.ring_n)[round % kRingSlots] = nready;
-          __threadfence_block();
-          *(volatile int *)&sm.ring_pub = round + 1;
-          round++;
-        }
-      }
-      round = __shfl_sync(kFull, round, 0);
-    }
-    // the carry into the next round: the inclusive prefix of the last tile
-    const int src = (nready - 1) / kPer;
-    carry.hi = __shfl_sync(kFull, lastv.hi, src);
-    carry.lo = __shfl_sync(kFull, lastv.lo, src);
-    carry_abs = __shfl_sync(kFull, lasta, src);
-    if (lane == 0) stat_add(sm, S_SCAN_WINDOWS, 1);
+    carry = base;
+    carry_abs = base_a;
+    if (w == 0 && lane == 0) stat_add(sm, S_SCAN_WINDOWS, 1);
     pos += nready;
   }
-
   if (kPlanned) {
-    // no more rounds; once every checker is done, the redo list is final
-    // (also when the scanner gave up; bounded)
-    if (lane == 0) {
-      *(volatile int *)&sm.ring_end = round;
-      const uint64_t tw = gtimer();
-      bool done = false;
-      for (uint32_t spin = 0; !done; spin++) {
-        done = true;
-        for (int k = 0; k < kWarps; k++) done = done && ((volatile int *)sm.chk_done)[k] >= round;
-        if (!done && (spin & 255u) == 255u && gtimer() - tw > p.wait_ns) break;
-      }
+    // every warp's places on the redo list are taken: the list is final
+    // (also when the scan gave up)
+    scan_bar();
+    if (w == 0 && lane == 0) {
       __threadfence();
       st_release_u32(&p.ctr[C_SCAN_FIN], 1u);
     }
   }
-  if (lane == 0) p.stats[S_T_SCAN_END] = gtimer();
+  if (w == 0 && lane == 0) p.stats[S_T_SCAN_END] = gtimer();
 }
 
 // ------------------------------------------------------------------ the walk: raw terms
@@ -2602,9 +2492,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) seqsum_kernel(const Params p
   const int tid = threadIdx.x;
   for (int i = tid; i < kBlockWarps * S_ACCUM_END; i += kBlockThreads) (&sm.stat[0][0])[i] = 0;
   if (tid == 0) {
-    sm.ring_pub = 0;
-    sm.ring_end = -1;
-    for (int k = 0; k < kWarps; k++) sm.chk_done[k] = 0;
+    sm.scan_stop = 0;
     sm.role = (int)atomicAdd(&p.ctr[C_ROLE], 1u);
     uint32_t smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
