@@ -184,9 +184,12 @@ __device__ __forceinline__ void tl_mark(const Params &p, int role, int who, uint
     if (threadIdx.x == 0 && nwin < 64) p.dbg[2400 + 4 * nwin + (k)] = (v);     \
   } while (0)
 // range 0's producer phases (stamps)
+#ifndef SEQSUM_WR0_RANGE
+#define SEQSUM_WR0_RANGE 4
+#endif
 #define WR0(r, k)                                                            \
   do {                                                                       \
-    if ((threadIdx.x & 31) == 0 && (r) == 4 && (k) < 40) p.dbg[2360 + (k)] = gtimer(); \
+    if ((threadIdx.x & 31) == 0 && (r) == SEQSUM_WR0_RANGE && (k) < 40) p.dbg[2360 + (k)] = gtimer(); \
   } while (0)
 #else
 #define WRT(r, k) ((void)0)
@@ -1578,49 +1581,49 @@ __device__ __noinline__ void scan_cta(const Params &p, Smem &sm, int64_t ntiles)
       sm.scan_tot[w] = make_float4(x.hi, x.lo, xa, hx ? 1.0f : 0.0f);
     }
     scan_bar();
-    // the prefix before this warp's tiles, and the carry into the next round
-    DF base = carry;
-    float base_a = carry_abs;
+    // the prefix before this warp's tiles (wbase), and the carry into the next round
+    DF base = carry, wbase = carry;
+    float base_a = carry_abs, wbase_a = carry_abs;
 #pragma unroll
     for (int k = 0; k < kWarps; k++) {
-      const float4 tk = sm.scan_tot[k];
-      DF nb;
-      float na;
-      if (tk.w != 0.0f) {
-        nb = DF{tk.x, tk.y};
-        na = tk.z;
-      } else {
-        nb = df_add(base, DF{tk.x, tk.y});
-        na = __fadd_rn(base_a, tk.z);
-      }
       if (k == w) {
-        // this warp: each tile's exclusive prefix from the lane before it
-        DF y;
-        y.hi = __shfl_up_sync(kFull, x.hi, 1);
-        y.lo = __shfl_up_sync(kFull, x.lo, 1);
-        const float ya = __shfl_up_sync(kFull, xa, 1);
-        const bool hy = __shfl_up_sync(kFull, hx, 1);
-        DF e = base;
-        float ea = base_a;
-        if (lane > 0) {
-          if (hy) {
-            e = y;
-            ea = ya;
-          } else {
-            e = df_add(base, y);
-            ea = __fadd_rn(base_a, ya);
-          }
-        }
-        if (mine && !hd)
-          st_vol_v4(&pout[(pos + i) * kPrecWords],
-                    make_uint4(__float_as_uint(e.hi), __float_as_uint(e.lo), __float_as_uint(ea), (tag << 8) | 2u));
-        if (kPlanned) scan_release(p, pos + i, mine, hd, e, ea, cur, tag);
+        wbase = base;
+        wbase_a = base_a;
       }
-      base = nb;
-      base_a = na;
+      const float4 tk = sm.scan_tot[k];
+      if (tk.w != 0.0f) {
+        base = DF{tk.x, tk.y};
+        base_a = tk.z;
+      } else {
+        base = df_add(base, DF{tk.x, tk.y});
+        base_a = __fadd_rn(base_a, tk.z);
+      }
     }
     carry = base;
     carry_abs = base_a;
+    {
+      // each tile's exclusive prefix from the lane before it
+      DF y;
+      y.hi = __shfl_up_sync(kFull, x.hi, 1);
+      y.lo = __shfl_up_sync(kFull, x.lo, 1);
+      const float ya = __shfl_up_sync(kFull, xa, 1);
+      const bool hy = __shfl_up_sync(kFull, hx, 1);
+      DF e = wbase;
+      float ea = wbase_a;
+      if (lane > 0) {
+        if (hy) {
+          e = y;
+          ea = ya;
+        } else {
+          e = df_add(wbase, y);
+          ea = __fadd_rn(wbase_a, ya);
+        }
+      }
+      if (mine && !hd)
+        st_vol_v4(&pout[(pos + i) * kPrecWords],
+                  make_uint4(__float_as_uint(e.hi), __float_as_uint(e.lo), __float_as_uint(ea), (tag << 8) | 2u));
+      if (kPlanned) scan_release(p, pos + i, mine, hd, e, ea, cur, tag);
+    }
     if (w == 0 && lane == 0) stat_add(sm, S_SCAN_WINDOWS, 1);
     pos += nready;
   }
@@ -2540,8 +2543,14 @@ __global__ void __launch_bounds__(kBlockThreads, 2) seqsum_kernel(const Params p
     // roles in the order the CTAs start: the walkers, the scanner, then the
     // streaming CTAs (every waiting role is held by a CTA already running)
     if (sm.role < p.nwalkers) {
+#ifdef SEQSUM_PROFILE
+      if (tid == 0 && sm.role == 0) p.dbg[2096] = gtimer();
+#endif
       walk_loop(p, sm, dyn, ntiles);
       if (tid == 0) atomicMax(&p.stats[S_T_WALK_END], (unsigned long long)gtimer());
+#ifdef SEQSUM_PROFILE
+      if (tid == 0 && sm.role == 0) p.dbg[2097] = gtimer();
+#endif
     } else if (sm.role == p.nwalkers) {
       if (p.planned) scan_cta<true>(p, sm, ntiles);
       else scan_cta<false>(p, sm, ntiles);
