@@ -391,9 +391,9 @@ def main():
                              oracle.seqsum_batched(w4.x, w4.offsets, w4.s0).view(np.uint64))
         ts = []
         for i in range(30):
-            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             with torch.cuda.stream(stream):
+                flush()   # (on the timed stream: it must not overlap the call)
                 a.record(stream)
                 sq.seqsum_f64_batched_sized(x4, o4, s4, outs=outs, stream=stream)
                 b.record(stream)
@@ -427,9 +427,9 @@ def main():
                np.array_equal(meanl.cpu().numpy().view(np.uint32), wl_means.view(np.uint32)))
         ts = []
         for i in range(30):
-            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             with torch.cuda.stream(stream):
+                flush()   # (on the timed stream: it must not overlap the call)
                 a.record(stream)
                 sq.seqsum_f64_strided(xld, 4, s0ld, outs=outl, means=meanl, stream=stream)
                 b.record(stream)
@@ -457,9 +457,9 @@ def main():
         sq.get_stats()
         ts = []
         for i in range(40):
-            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             with torch.cuda.stream(stream):
+                flush()
                 a.record(stream)
                 plan(fd[i % 4], s0, out=outs_p[i % 4:i % 4 + 1], stream=stream)
                 b.record(stream)

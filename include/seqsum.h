@@ -202,8 +202,7 @@ typedef struct {
   int64_t check_value;       /* self-checking builds: the value that failed it */
   int32_t timeout_site;      /* first bounded device wait that gave up (0: none): 2 a stage's copy, 3 a walk
                                 range's tile headers, 5 a run unit's prefix, 6 the scanner's tile sums, 7 a
-                                stage's release, 8 a planned call's redo list, 9 a planned call's check
-                                of a round */
+                                stage's release, 8 a planned call's redo list */
   int32_t timeout_pad;
   int64_t timeout_a;         /* its context: the tile */
   int64_t timeout_b;
