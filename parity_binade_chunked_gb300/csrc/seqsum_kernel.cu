@@ -269,6 +269,13 @@ __device__ __forceinline__ Rec ld_rec_vol(const Rec *p) {
   ld_vol_v2(&p->w[2], q.w[2], q.w[3]);
   return q;
 }
+// (a record another warp of this CTA wrote and fenced at CTA scope)
+__device__ __forceinline__ Rec ld_rec_cta(const Rec *p) {
+  Rec q;
+  asm volatile("ld.relaxed.cta.global.v2.u64 {%0, %1}, [%2];" : "=l"(q.w[0]), "=l"(q.w[1]) : "l"(&p->w[0]) : "memory");
+  asm volatile("ld.relaxed.cta.global.v2.u64 {%0, %1}, [%2];" : "=l"(q.w[2]), "=l"(q.w[3]) : "l"(&p->w[2]) : "memory");
+  return q;
+}
 __device__ __forceinline__ void st_rec_vol(Rec *p, const Rec &q) {
   st_vol_v2(&p->w[0], q.w[0], q.w[1]);
   st_vol_v2(&p->w[2], q.w[2], q.w[3]);
@@ -750,7 +757,7 @@ __device__ __noinline__ void complex_merge(const Params &p, Smem &sm, UnitSm &us
         it.count = 32 * kLaneTerms;
         it.start = (uint32_t)k * 32 * kLaneTerms;
       } else {
-        it = unpack_item(ld_rec_vol(&area[k * kWarpSlots + (i - (int)kex)]));
+        it = unpack_item(ld_rec_cta(&area[k * kWarpSlots + (i - (int)kex)]));
       }
     }
     const uint32_t key = (in && it.kind == K_RUN) ? it.eb : kNoKey;
@@ -1129,7 +1136,10 @@ __device__ __forceinline__ void run_unit(const Params &p, Smem &sm, UnitSm &us, 
         it.start = (uint32_t)(w * 32 + sstart) * kLaneTerms;
         st_rec(&area[at], pack_item(it, 0));
       }
-      __threadfence();   // the items before the header that publishes them
+      // the items before the count that tells the tile's last warp (of this
+      // CTA) to merge them: a CTA-scope fence; the merged items the walk
+      // reads are fenced at GPU scope before the header
+      __threadfence_block();
     }
     if (lane == 0) {
       us.wkey[w] = -1;
