@@ -24,6 +24,13 @@
  * share a (device, stream) pair are ordered by the stream; two host threads
  * must not call at the same time on the same stream.
  *
+ * Graphs: a call may be captured into a CUDA graph once the same entry has
+ * run on the same stream with the same sizes (its workspace then exists, and
+ * the capture allocates nothing).  Every launch takes its call tag from a
+ * device counter that the kernel advances itself, so each replay is a call
+ * of its own.  A captured seqsum_f64_planned call reads, on every replay,
+ * the plan stored when it was captured (its results stay exact).
+ *
  * Errors: a negative return value; nothing is enqueued then.  Device-side
  * conditions (a bounded wait that gave up, a capacity overflow) are reported
  * by seqsum_get_stats().  No exception crosses this interface.
