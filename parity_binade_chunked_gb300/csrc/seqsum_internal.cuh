@@ -40,10 +40,10 @@ enum : int {
 //   w[0] inc, w[1] lo, w[2] hi: 56-bit two's complement
 //   w[3] meta: kind (3 bits), biased binade (11 bits, 0 = none), d + 1 (2 bits),
 //        flags (8 bits), count (13 bits), start (13 bits)
-// A K_COMPLEX header carries instead, in w[0], the number of the tile's items:
-// records from slot 0 of its item area, in the order of their terms, runs of
-// one binade that touch already composed; a raw row's terms stay in x.  (While
-// a tile is formed, warp k writes its own items from slot 32 k.)
+// A K_COMPLEX header carries instead, in w[0], each warp's count of items
+// (warp k's in bits 6k..6k+5): warp k's items are the records from slot 32 k
+// of the tile's item area, in the order of their terms (a warp that is one run
+// has that run as its one item); a raw row's terms stay in x.
 struct __align__(16) Rec {
   uint64_t w[4];
 };
@@ -51,7 +51,7 @@ struct __align__(16) Rec {
 enum : uint32_t {
   K_RUN = 0,       // a run of adds inside binade eb (or a run of zeros)
   K_RAW = 1,       // item: a row of 16 terms the walk adds itself
-  K_COMPLEX = 2,   // header: the tile's records are its warps' item regions
+  K_COMPLEX = 2,   // header: the tile's records are its warps' item regions (counts in w[0])
   K_OVERFLOW = 3,  // header: the tile's items did not fit; the walk reads its terms from x
   K_RAW2 = 4       // item: a raw row across one power of two, from binade eb to eb + 1, all of its
                    // terms of one sign (w[0]: 1 if negative); the walk builds prefix tables for it

@@ -269,13 +269,6 @@ __device__ __forceinline__ Rec ld_rec_vol(const Rec *p) {
   ld_vol_v2(&p->w[2], q.w[2], q.w[3]);
   return q;
 }
-// (a record another warp of this CTA wrote and fenced at CTA scope)
-__device__ __forceinline__ Rec ld_rec_cta(const Rec *p) {
-  Rec q;
-  asm volatile("ld.relaxed.cta.global.v2.u64 {%0, %1}, [%2];" : "=l"(q.w[0]), "=l"(q.w[1]) : "l"(&p->w[0]) : "memory");
-  asm volatile("ld.relaxed.cta.global.v2.u64 {%0, %1}, [%2];" : "=l"(q.w[2]), "=l"(q.w[3]) : "l"(&p->w[2]) : "memory");
-  return q;
-}
 __device__ __forceinline__ void st_rec_vol(Rec *p, const Rec &q) {
   st_vol_v2(&p->w[0], q.w[0], q.w[1]);
   st_vol_v2(&p->w[2], q.w[2], q.w[3]);
@@ -700,130 +693,43 @@ __device__ __forceinline__ void plan_unit(const Params &p, Smem &sm, UnitSm &us,
 }
 
 
-// The last warp of a complex tile's run unit: the tile's items merged and
-// its header published (out of line: rare, and kept out of the units' loop).
-__device__ __noinline__ void complex_merge(const Params &p, Smem &sm, UnitSm &us, int64_t t, uint32_t tag) {
+// The last warp of a complex tile's run unit (out of line: rare, and kept
+// out of the units' loop): a warp that is one run gets it written as the one
+// item of its region; the header carries every warp's count of items (6 bits
+// each), and the walk reads warp k's items from slot 32 k.  The warps' own
+// items were fenced at CTA scope before the count that named this warp the
+// last; one GPU-scope fence here orders all of them before the header.
+__device__ __noinline__ void complex_publish(const Params &p, Smem &sm, UnitSm &us, int64_t t, uint32_t tag) {
   const int lane = threadIdx.x & 31;
-  // a complex tile: the warps' items in the order of their terms (a warp
-  // that is one run gives its run), consecutive runs of one binade composed,
-  // written compactly from slot 0 of the tile's item area.  The tile's item
-  // i lies at slot 32 k + j >= i (a warp has at most 32), so every write
-  // lands on a slot already read.
-  uint32_t ck = 0;
-  if (lane < kWarps) ck = us.wkey[lane] >= 0 ? 1u : us.wcnt[lane];
-  uint32_t cex = ck;
-#pragma unroll
-  for (int o = 1; o < kWarps; o <<= 1) {
-    const uint32_t q = __shfl_up_sync(kFull, cex, o);
-    if (lane >= o) cex += q;
-  }
-  const int T = (int)__shfl_sync(kFull, cex, kWarps - 1);
-  cex -= ck;
   Rec *area = p.items + t * kItemSlots;
-  const uint32_t lt = (1u << lane) - 1u;
-  int M = 0;
-  Run carry = run_empty();                 // the open run at the end of the chunk before
-  uint32_t ckey = kNoKey, cstart = 0, cend = 0;
-  bool pending = false;
-  for (int c = 0; c < T; c += 32) {
-    const int i = c + lane;
-    const bool in = i < T;
-    // the warp whose items hold item i
-    int k = 0;
-    uint32_t kex = 0;
-#pragma unroll
-    for (int q = 0; q < kWarps; q++) {
-      const uint32_t e = __shfl_sync(kFull, cex, q), n = __shfl_sync(kFull, ck, q);
-      if (in && e <= (uint32_t)i && (uint32_t)i < e + n) {
-        k = q;
-        kex = e;
-      }
+  uint32_t cnt = 0;
+  if (lane < kWarps) {
+    if (us.wkey[lane] >= 0) {
+      Item it;
+      it.r.inc = us.wred[lane][0];
+      it.r.lo = us.wred[lane][1];
+      it.r.hi = us.wred[lane][2];
+      it.r.d = us.wd[lane];
+      it.r.flags = us.wflags[lane];
+      saturate(it.r);
+      it.kind = K_RUN;
+      it.eb = (uint32_t)us.wkey[lane];
+      it.count = 32 * kLaneTerms;
+      it.start = (uint32_t)lane * 32 * kLaneTerms;
+      st_rec(&area[lane * kWarpSlots], pack_item(it, 0));
+      cnt = 1;
+    } else {
+      cnt = min(us.wcnt[lane], (uint32_t)kWarpSlots);
     }
-    Item it;
-    it.r = run_empty();
-    it.kind = K_OVERFLOW;
-    it.eb = 0;
-    it.start = it.count = 0;
-    if (in) {
-      if (us.wkey[k] >= 0) {
-        it.r.inc = us.wred[k][0];
-        it.r.lo = us.wred[k][1];
-        it.r.hi = us.wred[k][2];
-        it.r.d = us.wd[k];
-        it.r.flags = us.wflags[k];
-        saturate(it.r);
-        it.kind = K_RUN;
-        it.eb = (uint32_t)us.wkey[k];
-        it.count = 32 * kLaneTerms;
-        it.start = (uint32_t)k * 32 * kLaneTerms;
-      } else {
-        it = unpack_item(ld_rec_cta(&area[k * kWarpSlots + (i - (int)kex)]));
-      }
-    }
-    const uint32_t key = (in && it.kind == K_RUN) ? it.eb : kNoKey;
-    uint32_t pkey = __shfl_up_sync(kFull, key, 1);
-    if (lane == 0) pkey = ckey;
-    const bool head = in && (i == 0 || key == kNoKey || pkey == kNoKey || key != pkey);
-    // the open run of the chunk before ends if this chunk begins with a head
-    const bool close_prev = __shfl_sync(kFull, head, 0) && pending;
-    Run rr = it.r;
-    bool f = head;
-    uint32_t from = head ? it.start : 0u;
-    if (lane == 0 && in && !head) {
-      rr = run_compose(carry, rr);
-      from = cstart;
-      f = true;
-    }
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const Run q = shfl_run_up(rr, o);
-      const bool qh = __shfl_up_sync(kFull, f, o);
-      const uint32_t qf = __shfl_up_sync(kFull, from, o);
-      if (lane >= o) {
-        if (!f) rr = run_compose(q, rr);
-        f = f || qh;
-        from = max(from, qf);
-      }
-    }
-    const uint32_t nkey = __shfl_down_sync(kFull, key, 1);
-    const bool tail = in && (key == kNoKey || i == T - 1 || (lane < 31 && (nkey == kNoKey || nkey != key)));
-    const uint32_t tb = __ballot_sync(kFull, tail);
-    __syncwarp();   // every read of the chunk before any write
-    if (close_prev) {
-      if (lane == 0 && SQ_OK(p, M < c, 2, M)) {
-        Item m;
-        m.r = carry;
-        saturate(m.r);
-        m.kind = K_RUN;
-        m.eb = ckey;
-        m.start = cstart;
-        m.count = cend - cstart;
-        st_rec(&area[M], pack_item(m, 0));
-      }
-      M++;
-    }
-    if (tail) {
-      Item m = it;
-      if (it.kind == K_RUN) {
-        m.r = rr;
-        saturate(m.r);
-        m.start = from;
-        m.count = it.start + it.count - from;
-      }
-      const int at = M + __popc(tb & lt);
-      if (SQ_OK(p, at <= i && at < kItemSlots, 2, at)) st_rec(&area[at], pack_item(m, 0));
-    }
-    M += __popc(tb);
-    carry = shfl_run_idx(rr, 31);
-    ckey = __shfl_sync(kFull, key, 31);
-    cstart = __shfl_sync(kFull, from, 31);
-    cend = __shfl_sync(kFull, it.start + it.count, 31);
-    pending = __shfl_sync(kFull, in && !tail, 31);
   }
-  __threadfence();   // the items before the header that publishes them
+  uint64_t packed = 0;
+#pragma unroll
+  for (int k = 0; k < kWarps; k++) packed |= (uint64_t)__shfl_sync(kFull, cnt, k) << (6 * k);
+  __syncwarp();
   if (lane == 0) {
+    __threadfence();   // every warp's items before the header that publishes them
     Rec q;
-    q.w[0] = ((uint64_t)M & kPay56) | ((uint64_t)tag << 56);
+    q.w[0] = packed | ((uint64_t)tag << 56);
     q.w[1] = (uint64_t)tag << 56;
     q.w[2] = (uint64_t)tag << 56;
     q.w[3] = pack_meta(K_COMPLEX, 0, 0, 0, 0, 0) | ((uint64_t)tag << 56);
@@ -1211,7 +1117,7 @@ __device__ __forceinline__ void run_unit(const Params &p, Smem &sm, UnitSm &us, 
       if (!(p.fault_mode == 1 && t == p.fault_arg)) st_rec_vol(&p.hdr[t], pack_item(h, tag));
     }
   } else {
-    complex_merge(p, sm, us, t, tag);
+    complex_publish(p, sm, us, t, tag);
   }
   if (kind == U_SPEC) {
     // the tile's sums for the scanner: the binade of a tile of one run goes
@@ -1921,9 +1827,29 @@ struct Elem {
 
 // The number of items of a complex tile's compact list (0: none usable, the
 // tile is read from x).
+// A complex tile's header: warp k's count of items in bits 6k..6k+5.  The
+// tile's items (0 if a count is out of range).
 __device__ __forceinline__ uint32_t complex_items(const Rec &h) {
-  const uint64_t m = h.w[0] & kPay56;
-  return (m >= 1 && m <= (uint64_t)kItemSlots) ? (uint32_t)m : 0u;
+  uint32_t n = 0;
+  bool ok = true;
+#pragma unroll
+  for (int k = 0; k < kWarps; k++) {
+    const uint32_t c = (uint32_t)(h.w[0] >> (6 * k)) & 63u;
+    ok = ok && c <= (uint32_t)kWarpSlots;
+    n += c;
+  }
+  return ok ? n : 0u;
+}
+// The slot of a complex tile's item kk (its items in the order of their terms).
+__device__ __forceinline__ uint32_t complex_slot(const Rec &h, uint32_t kk) {
+  uint32_t base = 0, slot = 0;
+#pragma unroll
+  for (int k = 0; k < kWarps; k++) {
+    const uint32_t c = (uint32_t)(h.w[0] >> (6 * k)) & 63u;
+    if (kk >= base && kk < base + c) slot = (uint32_t)k * kWarpSlots + (kk - base);
+    base += c;
+  }
+  return slot;
 }
 
 // Element E of the range, in two parts so that the record of the next chunk
@@ -1978,7 +1904,7 @@ __device__ __forceinline__ ElemRec range_fetch(const Params &p, const Rec (&hl)[
   if (hk == K_RUN) {
     er.what = 0;
   } else if (hk == K_COMPLEX && complex_items(h) > 0 && SQ_OK(p, kk < complex_items(h), 3, kk)) {
-    er.q = ld_rec_vol(&p.items[(ta + tt) * kItemSlots + kk]);
+    er.q = ld_rec_vol(&p.items[(ta + tt) * kItemSlots + complex_slot(h, kk)]);
     er.what = 1;
   }
   return er;
