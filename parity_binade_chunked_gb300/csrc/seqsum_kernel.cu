@@ -1956,10 +1956,8 @@ __device__ __noinline__ void walk_producer(const Params &p, Smem &sm, RangeSlot 
   bool failed_all = false;
   const bool x16 = (reinterpret_cast<uintptr_t>(p.x) & 15u) == 0;   // rows can be copied 16 bytes at a time
   for (int r = pw; r < nranges; r += kWarps) {
-    // the slot's previous use must have been applied
     const uint32_t use = sm.wuse_p[pw];
     bool ok = !failed_all;
-    if (use > 0) ok = mbar_wait_bounded(&sm.wempty[pw], (use - 1) & 1u, 4 * p.wait_ns);
     const int64_t ta = ws.tb + range_start(r);
     const int tn = (int)min(range_start(r + 1) - range_start(r), ws.te - ta);
     // ---- the range's headers (four a lane), as they arrive
@@ -2013,6 +2011,9 @@ __device__ __noinline__ void walk_producer(const Params &p, Smem &sm, RangeSlot 
       const uint32_t q = __shfl_up_sync(kFull, off, o);
       if (lane >= o) off += q;
     }
+    // the slot's previous use must have been applied (waited for only now:
+    // the headers above were read while the in-order warp still held it)
+    if (use > 0) ok = __all_sync(kFull, mbar_wait_bounded(&sm.wempty[pw], (use - 1) & 1u, 4 * p.wait_ns)) && ok;
     const int N = ok ? (int)__shfl_sync(kFull, off, 31) : 0;
     const bool direct = N == tn;   // every tile one element
     WR0(r, 0);
