@@ -1042,9 +1042,9 @@ __device__ __forceinline__ void run_unit(const Params &p, Smem &sm, UnitSm &us, 
         it.start = (uint32_t)(w * 32 + sstart) * kLaneTerms;
         st_rec(&area[at], pack_item(it, 0));
       }
-      // the items before the count that tells the tile's last warp (of this
-      // CTA) to merge them: a CTA-scope fence; the merged items the walk
-      // reads are fenced at GPU scope before the header
+      // the items before the count that names the tile's last warp (of this
+      // CTA): a CTA-scope fence; that warp's GPU-scope fence orders them
+      // before the header the walk reads
       __threadfence_block();
     }
     if (lane == 0) {
