@@ -192,7 +192,7 @@ typedef struct {
   int64_t cy_plan;           /* ... plan units (the tiles' sums) */
   int64_t cy_pfx_wait;       /* ... run units waiting for a prefix the copy did not bring */
   int64_t cy_run;            /* ... run units (the rows' runs and the tile's header) */
-  int64_t scan_windows;      /* windows of tiles' prefixes the scanner published */
+  int64_t scan_windows;      /* rounds of tiles' prefixes the scanner published */
   int64_t scan_polls;        /* scanner polls that found no new tile sums */
   int64_t pfx_late;          /* run units whose prefix was not yet published when their copy landed */
   int64_t ctas_alone;        /* streaming CTAs that left their SM to the walker or the scanner */

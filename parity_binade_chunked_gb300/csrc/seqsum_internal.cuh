@@ -109,7 +109,7 @@ enum : int {
   S_CY_PLAN,          // ... plan units (from the copy to the tile's sums published)
   S_CY_PFX_WAIT,      // ... run units waiting for a prefix that the copy did not bring
   S_CY_RUN,           // ... run units (from the prefix to the tile's header)
-  S_SCAN_WINDOWS,     // windows the scanner published
+  S_SCAN_WINDOWS,     // rounds the scanner published
   S_SCAN_POLLS,       // scanner polls of tiles' sums
   S_PFX_LATE,         // run units whose prefix came after their copy
   S_ALONE,            // streaming CTAs that left their SM to the walker or the scanner
