@@ -1680,9 +1680,8 @@ __device__ __noinline__ uint64_t raw_from_x(const Params &p, Smem &sm, uint64_t 
 // within the binade (m + P <= 2^53) is added at once, and the term after it
 // with the hardware add.  The rest goes term by term (raw_chunk).
 __device__ __forceinline__ uint64_t raw2_row(Smem &sm, uint64_t S, const uint64_t *data, uint32_t lims, uint32_t ea,
-                                          uint64_t neg) {
+                                          uint64_t neg, uint32_t &n_rounds, uint32_t &n_dadds) {
   const int lane = threadIdx.x & 31;
-  const uint64_t t_in = clock64();
   const int la = (int)(lims & 31u), lb = (int)((lims >> 5) & 31u);
   const uint64_t t = lane < kLaneTerms ? data[lane] : kNegZero;
   const uint64_t pa = lane < kLaneTerms ? data[kLaneTerms + lane] : 0ull;
@@ -1736,11 +1735,8 @@ __device__ __forceinline__ uint64_t raw2_row(Smem &sm, uint64_t S, const uint64_
     dadds++;
     i = k + 1;
   }
-  if (lane == 0) {
-    stat_add(sm, S_RAW_ROUNDS, rounds);
-    stat_add(sm, S_TERMS_DADD, dadds);
-    stat_add(sm, S_CY_WALK_RAW, clock64() - t_in);
-  }
+  n_rounds += rounds;   // (the caller's counters: no shared-memory update on the in-order path)
+  n_dadds += dadds;
 #ifdef SEQSUM_PROFILE
   if (lane == 0) sm.prof_i = (uint32_t)i | (rounds << 8) | (dadds << 16) | (((uint32_t)(S >> 52) & 0x7FFu) << 20);
 #endif
@@ -2274,7 +2270,8 @@ __device__ __noinline__ uint64_t walk_serial(const Params &p, Smem &sm, RangeSlo
                                              int nranges, uint64_t S) {
   const int lane = threadIdx.x & 31;
   bool failed = false;
-  uint32_t nrun = 0;
+  uint32_t nrun = 0, n_rounds = 0, n_dadds = 0;
+  uint64_t cy_serial = 0, cy_raw = 0;
   for (int r = 0; r < nranges; r++) {
     const int pw = r % kWarps;
     RangeSlot &rs = slots[pw];
@@ -2327,8 +2324,13 @@ __device__ __noinline__ uint64_t walk_serial(const Params &p, Smem &sm, RangeSlo
           nrun++;
         } else if ((kind == ST_RAW || kind == ST_RAW2) && st.inc < kRangeRaw) {
           const uint64_t *data = rs.raw[st.inc];
-          if (kind == ST_RAW) S = row_dadd(sm, S, lane < kLaneTerms ? data[lane] : kNegZero, 0, kLaneTerms);
-          else S = raw2_row(sm, S, data, rs.rawlim[st.inc], eb, (st.meta >> 15) & 1u);
+          if (kind == ST_RAW) {
+            S = row_dadd(sm, S, lane < kLaneTerms ? data[lane] : kNegZero, 0, kLaneTerms);
+          } else {
+            const uint64_t t_in = clock64();
+            S = raw2_row(sm, S, data, rs.rawlim[st.inc], eb, (st.meta >> 15) & 1u, n_rounds, n_dadds);
+            cy_raw += clock64() - t_in;
+          }
           done = true;
         }
         if (!done) {
@@ -2351,16 +2353,20 @@ __device__ __noinline__ uint64_t walk_serial(const Params &p, Smem &sm, RangeSlo
       }
     }
     WRT(r, 3);
-    if (lane == 0) {
-      sm.wuse_c[pw] = use + 1;
-      stat_add(sm, S_WALK_BATCHES, 1);
-      stat_add(sm, S_CY_WALK_SERIAL, clock64() - c1);
-    }
+    cy_serial += clock64() - c1;
+    if (lane == 0) sm.wuse_c[pw] = use + 1;
     __syncwarp();
     if (got && lane == 0) mbar_arrive(&sm.wempty[pw]);
     if (!got) break;   // the slot may still be written: stop using them
   }
-  if (lane == 0) stat_add(sm, S_WALK_SEGMENTS, nrun);
+  if (lane == 0) {
+    stat_add(sm, S_WALK_SEGMENTS, nrun);
+    stat_add(sm, S_WALK_BATCHES, (unsigned long long)nranges);
+    stat_add(sm, S_CY_WALK_SERIAL, cy_serial);
+    stat_add(sm, S_CY_WALK_RAW, cy_raw);
+    stat_add(sm, S_RAW_ROUNDS, n_rounds);
+    stat_add(sm, S_TERMS_DADD, n_dadds);
+  }
   return failed ? 0x7FF8000000000000ull : S;
 }
 
