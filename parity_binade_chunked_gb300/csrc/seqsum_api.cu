@@ -31,6 +31,7 @@ struct Workspace {
   Rec *items = nullptr;              // kItemSlots item slots per tile
   uint32_t *ctr = nullptr;
   int64_t *tile_begin = nullptr;
+  int32_t *order = nullptr;          // batched: the sums in the order the kernel takes them
   unsigned long long *stats = nullptr;
   unsigned long long *dbg = nullptr;
   int64_t *h_pin = nullptr;          // pinned bounce for the batched size read-back
@@ -70,6 +71,8 @@ void ws_free(Workspace *w) {
   cudaFree(w->hdr);
   cudaFree(w->items);
   cudaFree(w->tile_begin);
+  cudaFree(w->order);
+  w->order = nullptr;
   cudaFree(w->conf);
   cudaFree(w->redo);
   w->conf = nullptr;
@@ -111,6 +114,7 @@ int get_ws(cudaStream_t stream, int64_t tiles, int64_t sums, Workspace **out) {
         cudaMalloc(&w->hdr, ct * sizeof(Rec)) != cudaSuccess ||
         cudaMalloc(&w->items, ct * sq::kItemSlots * sizeof(Rec)) != cudaSuccess ||
         cudaMalloc(&w->tile_begin, (cs + 1) * sizeof(int64_t)) != cudaSuccess ||
+        cudaMalloc(&w->order, cs * sizeof(int32_t)) != cudaSuccess ||
         cudaMalloc(&w->conf, ct * sizeof(uint32_t)) != cudaSuccess ||
         cudaMalloc(&w->redo, ct * sizeof(uint32_t)) != cudaSuccess) {
       ws_free(w);
@@ -193,6 +197,7 @@ void fill_ws(Params &p, Workspace *w) {
   p.items = w->items;
   p.ctr = w->ctr;
   p.tile_begin = w->tile_begin;
+  p.order = w->order;
   p.cap_tiles = w->cap_tiles;
   p.stats = w->stats;
   p.dbg = w->dbg;

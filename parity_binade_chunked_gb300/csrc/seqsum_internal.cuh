@@ -22,7 +22,7 @@ constexpr int kStageBytes = kTileTerms * 8;
 constexpr int kDynSmem = kStages * kStageBytes + 1024;   // + alignment slack for the 128-byte swizzle
 constexpr int kWarpSlots = 32;                   // 32-byte item slots of one warp's region (one per row)
 constexpr int kItemSlots = kWarps * kWarpSlots;  // a tile's item area (8 KB): one region per compute warp
-constexpr int kMaxWalkers = 8;
+constexpr int kMaxWalkers = 16;
 
 // ---- units of a streaming CTA
 enum : int {
@@ -155,7 +155,8 @@ struct Params {
   Rec *hdr;                    // per tile: its header
   Rec *items;                  // kItemSlots per tile
   uint32_t *ctr;               // C_COUNT counters
-  int64_t *tile_begin;         // batched: nsums + 1 entries
+  int64_t *tile_begin;         // batched: nsums + 1 entries, by position in `order`
+  int32_t *order;              // batched: the sums in the order they stream and are walked (set-up kernel)
   int64_t cap_tiles;           // tiles the workspace holds
   unsigned long long *stats;   // S_COUNT counters
   unsigned long long *dbg;     // self-checking builds: diagnostic words

@@ -382,7 +382,8 @@ __device__ __forceinline__ Geo tile_geo(const Params &p, int64_t t, int *hint = 
     g.sum = 0;
     return g;
   }
-  // the sum k with tile_begin[k] <= t < tile_begin[k+1] (the last such k: empty sums share a start)
+  // the position lo with tile_begin[lo] <= t < tile_begin[lo+1] (the last such: empty sums share
+  // a start); the sum there is order[lo]
   int lo = 0, hi = p.nsums;   // invariant: tile_begin[lo] <= t < tile_begin[hi]
   if (hint && *hint >= 0 && *hint < p.nsums && __ldg(&p.tile_begin[*hint]) <= t) {
     lo = *hint;
@@ -399,12 +400,13 @@ __device__ __forceinline__ Geo tile_geo(const Params &p, int64_t t, int *hint = 
     else hi = mid;
   }
   if (hint) *hint = lo;
-  const int64_t off = __ldg(&p.offsets[lo]);
+  const int k = __ldg(&p.order[lo]);
+  const int64_t off = __ldg(&p.offsets[k]);
   g.t_first = __ldg(&p.tile_begin[lo]);
   g.row0 = (off >> 4) + (t - g.t_first) * kTileRows;
   g.g_lo = off;
-  g.g_hi = __ldg(&p.offsets[lo + 1]);
-  g.sum = lo;
+  g.g_hi = __ldg(&p.offsets[k + 1]);
+  g.sum = k;
   return g;
 }
 
@@ -2402,13 +2404,15 @@ __device__ __noinline__ void walk_loop(const Params &p, Smem &sm, unsigned char 
   while (true) {
     if (tid == 0) sm.wk = p.offsets ? (int)atomicAdd(&p.ctr[C_SUMTICKET], 1u) : (sm.wk == 0 ? 0 : 1);
     __syncthreads();
-    const int k = sm.wk;
-    if (k >= p.nsums) break;
+    const int j = sm.wk;
+    if (j >= p.nsums) break;
     WalkSum ws;
     double s0;
+    int k = 0;
     if (p.offsets) {
-      ws.tb = p.tile_begin[k];
-      ws.te = p.tile_begin[k + 1];
+      k = p.order[j];
+      ws.tb = p.tile_begin[j];
+      ws.te = p.tile_begin[j + 1];
       ws.g_lo = p.offsets[k];
       ws.g_hi = p.offsets[k + 1];
       ws.row_base = ws.g_lo >> 4;
@@ -2548,18 +2552,38 @@ __global__ void __launch_bounds__(kBlockThreads, 2) seqsum_kernel(const Params p
   }
 }
 
-// The batched calls' set-up: checks the offsets, counts each sum's tiles and
-// writes tile_begin (one CTA).  On bad offsets or too many tiles every output
-// is NaN and the main kernel does nothing.
+// A sum's tiles: its rows of 16 terms (the first and the last may be partial)
+// in tiles of kTileRows.
+__device__ __forceinline__ int64_t sum_tiles(const Params &p, int k) {
+  const int64_t a = p.offsets[k], b = p.offsets[k + 1];
+  if (b <= a) return 0;
+  const int64_t rows = ((b + 15) >> 4) - (a >> 4);
+  return (rows + kTileRows - 1) / kTileRows;
+}
+// The size class that orders the sums: the bit length of the tile count.
+constexpr int kSizeClasses = 65;
+__device__ __forceinline__ int size_class(int64_t nt) { return 64 - __clzll((long long)nt); }
+
+// The batched calls' set-up (one CTA): checks the offsets, puts the sums in
+// the order the kernel takes them and writes tile_begin by that order.  The
+// order is by size class, smaller first, and by index within a class: a small
+// sum's walk costs about the same time whatever its length, so small sums go
+// first, where their walks overlap the streaming of the larger ones, and the
+// walk that ends last is a large sum's, which keeps pace with its tiles.  On
+// bad offsets or too many tiles every output is NaN and the main kernel does
+// nothing.
 __global__ void __launch_bounds__(kThreads) setup_kernel(const Params p) {
   __shared__ int bad;
   __shared__ int64_t carry;
   __shared__ int64_t wsum[kWarps];
+  __shared__ int cbase[kSizeClasses];          // the next position of each class
+  __shared__ int ccount[kWarps][kSizeClasses]; // a chunk's sums of each class, per warp
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   if (tid == 0) {
     bad = 0;
     carry = 0;
   }
+  for (int c = tid; c < kSizeClasses; c += kThreads) cbase[c] = 0;
   __syncthreads();
   for (int k = tid; k <= p.nsums; k += kThreads) {
     const int64_t o = p.offsets[k];
@@ -2568,16 +2592,45 @@ __global__ void __launch_bounds__(kThreads) setup_kernel(const Params p) {
   }
   __syncthreads();
   if (!bad) {
+    // the order: a counting sort by size class, stable (ranks within a warp
+    // from match masks, then the warps of the chunk in turn)
+    for (int k = tid; k < p.nsums; k += kThreads) atomicAdd(&cbase[size_class(sum_tiles(p, k))], 1);
+    __syncthreads();
+    if (tid == 0) {
+      int run = 0;
+      for (int c = 0; c < kSizeClasses; c++) {
+        const int n = cbase[c];
+        cbase[c] = run;
+        run += n;
+      }
+    }
+    __syncthreads();
     for (int k0 = 0; k0 < p.nsums; k0 += kThreads) {
       const int k = k0 + tid;
-      int64_t nt = 0;
-      if (k < p.nsums) {
-        const int64_t a = p.offsets[k], b = p.offsets[k + 1];
-        if (b > a) {
-          const int64_t rows = ((b + 15) >> 4) - (a >> 4);
-          nt = (rows + kTileRows - 1) / kTileRows;
-        }
+      for (int i = tid; i < kWarps * kSizeClasses; i += kThreads) (&ccount[0][0])[i] = 0;
+      __syncthreads();
+      const int c = k < p.nsums ? size_class(sum_tiles(p, k)) : -1;
+      const uint32_t peers = __match_any_sync(kFull, c);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      if (c >= 0 && rank == 0) ccount[w][c] = __popc(peers);
+      __syncthreads();
+      if (c >= 0) {
+        int pos = cbase[c] + rank;
+        for (int j = 0; j < w; j++) pos += ccount[j][c];
+        p.order[pos] = k;
       }
+      __syncthreads();
+      for (int cc = tid; cc < kSizeClasses; cc += kThreads) {
+        int n = 0;
+        for (int j = 0; j < kWarps; j++) n += ccount[j][cc];
+        cbase[cc] += n;
+      }
+      __syncthreads();
+    }
+    // tile_begin by position
+    for (int j0 = 0; j0 < p.nsums; j0 += kThreads) {
+      const int j = j0 + tid;
+      const int64_t nt = j < p.nsums ? sum_tiles(p, p.order[j]) : 0;
       int64_t inc = nt;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -2587,12 +2640,12 @@ __global__ void __launch_bounds__(kThreads) setup_kernel(const Params p) {
       if (lane == 31) wsum[w] = inc;
       __syncthreads();
       int64_t base = carry;
-      for (int j = 0; j < w; j++) base += wsum[j];
-      if (k < p.nsums) p.tile_begin[k] = base + inc - nt;
+      for (int i = 0; i < w; i++) base += wsum[i];
+      if (j < p.nsums) p.tile_begin[j] = base + inc - nt;
       __syncthreads();
       if (tid == 0) {
         int64_t tot = 0;
-        for (int j = 0; j < kWarps; j++) tot += wsum[j];
+        for (int i = 0; i < kWarps; i++) tot += wsum[i];
         carry += tot;
       }
       __syncthreads();
