@@ -22,7 +22,7 @@ constexpr int kStageBytes = kTileTerms * 8;
 constexpr int kDynSmem = kStages * kStageBytes + 1024;   // + alignment slack for the 128-byte swizzle
 constexpr int kWarpSlots = 32;                   // 32-byte item slots of one warp's region (one per row)
 constexpr int kItemSlots = kWarps * kWarpSlots;  // a tile's item area (8 KB): one region per compute warp
-constexpr int kMaxWalkers = 16;
+constexpr int kMaxWalkers = 8;      // walkers of a batched call (more take slots from the stream)
 
 // ---- units of a streaming CTA
 enum : int {
