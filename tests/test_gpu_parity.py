@@ -308,6 +308,36 @@ def test_batched_ragged_and_empty(sq):
             assert_same(got[k], want[k], f"ragged sum {k} (len {lens[k]})")
 
 
+def many_sums(seed=11, nsums=700):
+    """nsums sums whose lengths cover tile counts from 0 to 40 and one of
+    about 300 tiles, in shuffled order, over a 2^U * mant plane (every sum
+    crosses binades from its own start)."""
+    rng = np.random.default_rng(seed)
+    kinds = [0, 1, 15, 16, 17, 4095, 4096, 4097, 8195, 20000, 70000, 163839]
+    lens = [int(v) for v in rng.choice(kinds, size=nsums - 1)] + [300 * 4096 + 5]
+    rng.shuffle(lens)
+    offs = np.zeros(nsums + 1, dtype=np.int64)
+    offs[1:] = np.cumsum(lens)
+    x = W.plane_c3(int(offs[-1]), 1, seed=seed, zero_rows=0)
+    s0s = rng.standard_normal(nsums)
+    s0s[::50] = 0.0
+    s0s[7] = -0.0
+    return W.Workload("many", x, offs, s0s), lens
+
+
+def test_batched_many_sums_in_mixed_size_order(sq):
+    """The sums are streamed and walked in size order, smaller first (the
+    set-up kernel sorts them 256 at a time); every result must still land at
+    its own index with the oracle's bits."""
+    wl, lens = many_sums()
+    want = oracle.seqsum_batched(wl.x, wl.offsets, wl.s0)
+    for sized in [False, True]:
+        got = _batched(sq, wl, sized)
+        for k in range(len(lens)):
+            assert_same(got[k], want[k], f"sum {k} of {len(lens)} (len {lens[k]}, sized {sized})")
+    assert sq.get_stats()["device_status"] == 0
+
+
 def test_batched_offset_start(sq):
     x = W.plane_c3(200, 100, zero_rows=3)
     offs = np.array([1000, 1000, 5003, 9000, 20000], dtype=np.int64)
