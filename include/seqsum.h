@@ -239,9 +239,10 @@ int seqsum_debug_set_plan(int mode);
  * of the library record (zeros otherwise) and clears them. */
 int seqsum_debug_read(unsigned long long *out, int n);
 
-/* Diagnostics of a call that does not finish: copies the first n (1..16)
- * device counters of the most recent call's workspace (tickets, roles, exits,
- * error bits, tag) into out.  It takes no lock and reads on a stream of its
+/* Diagnostics of a call that does not finish: copies the first n (1..18)
+ * device counters of the most recent call's workspace into out: tickets,
+ * roles, exits, error bits, tag, the self-checks' and the bounded waits'
+ * records, the walker's and the scanner's SMs, a planned call's redo list.  It takes no lock and reads on a stream of its
  * own, so it can run while another thread waits on that call. */
 int seqsum_debug_counters(unsigned long long *out, int n);
 

@@ -291,14 +291,16 @@ def debug_set_fault(mode: int, arg: int = 0, wait_ns: int = 0) -> None:
 
 
 _COUNTER_NAMES = ["ticket", "role", "exit", "sum_ticket", "err", "epoch", "ntiles", "skip", "check_site",
-                  "check_lo", "check_hi", "timeout_site", "timeout_a", "timeout_b", "pad14", "pad15"]
+                  "check_lo", "check_hi", "timeout_site", "timeout_a", "timeout_b", "walk_sm", "scan_sm",
+                  "redo_reserved", "scan_finished"]
 
 
 def debug_counters() -> dict:
     """The device counters of the most recent call, read without waiting for
     it (diagnostics of a call that does not finish)."""
-    buf = (ctypes.c_ulonglong * 16)()
-    _check(lib().seqsum_debug_counters(buf, 16))
+    n = len(_COUNTER_NAMES)
+    buf = (ctypes.c_ulonglong * n)()
+    _check(lib().seqsum_debug_counters(buf, n))
     return dict(zip(_COUNTER_NAMES, list(buf)))
 
 
